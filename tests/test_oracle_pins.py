@@ -1,0 +1,273 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle (``oracle/``) against something other than its own
+code: hand-worked fixtures under ``tests/golden/``, closed-form identities of
+the ops (fVDB PR #757's test plan names the refine->coarsen round trip, the
+k3s1 = [-1,1]^3 dilation alias and the +-4096 / negative-octant cases), brute
+force on tiny inputs, and invariants such as V_out = 8 V_in for refinement.
+"""
+import itertools
+
+import numpy as np
+import pytest
+
+import oracle
+from sparse_voxel_grid_leaf_gb300 import synth
+from tests import _helpers as H
+
+FIELDS = ["leaf_offsets", "origins", "masks", "voxel_offset", "word_prefix", "leaf_bbox",
+          "leaf_grid", "leaf_parent", "voxel_counts", "grid_bbox", "node_counts",
+          "lower_offsets", "upper_offsets", "lower_origins", "lower_parent", "upper_origins"]
+
+
+def same(a, b):
+    for k in FIELDS:
+        assert a[k].shape == b[k].shape, k
+        assert np.array_equal(a[k], b[k]), k
+
+
+def canon(o):
+    o = [int(v) for v in o]
+    return tuple(v // 4096 for v in o) + tuple((v // 128) % 32 for v in o) + tuple((v // 8) % 16 for v in o)
+
+
+def strictly_canonical(res):
+    B = len(res["leaf_offsets"]) - 1
+    for g in range(B):
+        lo, hi = int(res["leaf_offsets"][g]), int(res["leaf_offsets"][g + 1])
+        keys = [canon(o) for o in res["origins"][lo:hi]]
+        assert all(a < b for a, b in zip(keys, keys[1:]))
+
+
+# ---------------------------------------------------------------- golden files
+
+def test_golden_canonical_order():
+    sec = H.read_sections("canonical_order.txt")
+    vox = np.array([[int(v) for v in row] for row in sec["voxels"]], np.int32)
+    exp = np.array([[int(v) for v in row] for row in sec["expected_origins"]], np.int32)
+    res = oracle.run_voxels(vox, np.array([0, len(vox)], np.int64))
+    assert np.array_equal(res["origins"], exp)
+    assert list(res["node_counts"][0]) == [int(v) for v in sec["expected_node_counts"][0]]
+    H.check_derived(res)
+
+
+def test_golden_leaf_bits():
+    sec = H.read_sections("leaf_bits.txt")
+    B = int(sec["num_grids"][0][0])
+    rows = [[int(v) for v in r] for r in sec["voxels"]]
+    sets = [set() for _ in range(B)]
+    for g, x, y, z in rows:
+        sets[g].add((x, y, z))
+    ijk, off = H.pack_sets(sets)
+    res = oracle.run_voxels(ijk, off)
+    exp = sec["expected_leaves"]
+    assert res["origins"].shape[0] == len(exp)
+    for i, r in enumerate(exp):
+        assert list(res["origins"][i]) == [int(v) for v in r[0:3]]
+        assert [int(w) for w in res["masks"][i]] == [int(v, 16) for v in r[3:11]]
+        assert int(res["voxel_offset"][i]) == int(r[11])
+        assert int(res["word_prefix"][i]) == int(r[12], 16)
+        assert list(res["leaf_bbox"][i]) == [int(v) for v in r[13:19]]
+    for g, r in enumerate(sec["expected_grids"]):
+        r = [int(v) for v in r]
+        assert int(res["voxel_counts"][g]) == r[0]
+        assert list(res["grid_bbox"][g]) == r[1:7]
+        assert list(res["node_counts"][g]) == r[7:10]
+
+
+# ------------------------------------------------------------- from ijk (front end)
+
+def test_from_ijk_dedups_and_matches_set():
+    ijk, off = synth.random_voxels(3, 400, 40, seed=5, origin=(-20, -13, 4090), empty=(1,))
+    res = oracle.run_voxels(ijk, off)
+    sets = H.jagged_sets(ijk, off)
+    for g in range(3):
+        assert H.grid_voxels(res, g) == sets[g]
+        assert res["voxel_counts"][g] == len(sets[g])
+    strictly_canonical(res)
+    H.check_derived(res)
+
+
+# ------------------------------------------------------------------ refine
+
+@pytest.mark.parametrize("f", [2, 4, 8])
+def test_refine_brute_and_count(f):
+    ijk, off = synth.random_voxels(2, 30, 20, seed=11, origin=(-10, -3, -4100))
+    res = oracle.run_voxels(ijk, off, [("refine", f)])
+    sets = H.jagged_sets(ijk, off)
+    for g in range(2):
+        got = H.grid_voxels(res, g)
+        assert got == H.brute_refine(sets[g], f)
+        assert len(got) == f ** 3 * len(sets[g])
+    strictly_canonical(res)
+    H.check_derived(res)
+
+
+def test_refine_single_voxel_negative():
+    # voxel (-1, 0, 5) -> children x in {-2,-1}, y in {0,1}, z in {10,11}
+    res = oracle.run_voxels(np.array([[-1, 0, 5]], np.int32), np.array([0, 1]), [("refine", 2)])
+    exp = {(x, y, z) for x in (-2, -1) for y in (0, 1) for z in (10, 11)}
+    assert H.grid_voxels(res, 0) == exp
+    assert res["origins"].tolist() == [[-8, 0, 8]]
+
+
+def test_refine_coarsen_round_trip_stress_members():
+    ijk, off = synth.make("stress_b64_res512")
+    # a handful of members straddling +-4096 boundaries in different octants
+    pick = [0, 3, 5, 10, 13]
+    sub = [ijk[off[g]:off[g + 1]] for g in pick]
+    ijk2, off2 = synth._pack(sub)
+    base = oracle.run_voxels(ijk2, off2)
+    back = oracle.run_voxels(ijk2, off2, [("refine", 2), ("coarsen", 2)])
+    same(base, back)
+    ref = oracle.run_voxels(ijk2, off2, [("refine", 2)])
+    assert np.array_equal(ref["voxel_counts"], 8 * base["voxel_counts"])
+    strictly_canonical(ref)
+
+
+def test_refine_leaf_origins_equal_8_coarsen4():
+    ijk, off = synth.make("pr1_b2_res32")
+    ijk = ijk - np.array([16, 40, 3], np.int32)   # move into negative octants
+    r2 = oracle.run_voxels(ijk, off, [("refine", 2)])
+    c4 = oracle.run_voxels(ijk, off, [("coarsen", 4)])
+    for g in range(2):
+        lo, hi = r2["leaf_offsets"][g], r2["leaf_offsets"][g + 1]
+        leaf_set = {tuple(o) for o in r2["origins"][lo:hi].tolist()}
+        vox = {tuple(8 * v for v in t) for t in H.grid_voxels(c4, g)}
+        assert leaf_set == vox
+
+
+def test_refine_translation():
+    ijk, off = synth.random_voxels(1, 60, 30, seed=3)
+    t = np.array([8 * 37, -8 * 600, 8 * 5], np.int32)
+    a = oracle.run_voxels(ijk, off, [("refine", 2)])
+    b = oracle.run_voxels(ijk + t, off, [("refine", 2)])
+    assert {tuple(v) for v in (a["origins"] + 2 * t).tolist()} == {tuple(v) for v in b["origins"].tolist()}
+
+
+# ------------------------------------------------------------------ coarsen
+
+def test_coarsen_floor_single_voxels():
+    pts = [(-1, -1, -1), (-2, 3, -3), (3, -4, 0), (-9, 9, -17), (2 ** 31 - 1, -2 ** 31, 0)]
+    for p in pts:
+        res = oracle.run_voxels(np.array([p], np.int32), np.array([0, 1]), [("coarsen", 2)])
+        assert H.grid_voxels(res, 0) == {tuple(v // 2 for v in p)}
+    res = oracle.run_voxels(np.array([[-1, 0, 7]], np.int32), np.array([0, 1]), [("coarsen", 8)])
+    assert H.grid_voxels(res, 0) == {(-1, 0, 0)}
+
+
+@pytest.mark.parametrize("f", [2, 4, 8])
+def test_coarsen_brute(f):
+    ijk, off = synth.random_voxels(2, 300, 70, seed=9, origin=(-35, -4096 - 30, 20))
+    res = oracle.run_voxels(ijk, off, [("coarsen", f)])
+    sets = H.jagged_sets(ijk, off)
+    for g in range(2):
+        got = H.grid_voxels(res, g)
+        assert got == H.brute_coarsen(sets[g], f)
+        assert len(got) <= len(sets[g])
+    H.check_derived(res)
+
+
+def test_coarsen_chained_equals_direct():
+    ijk, off = synth.make("pr1_b2_res32")
+    ijk = ijk - np.array([20, 5, 31], np.int32)
+    same(oracle.run_voxels(ijk, off, [("coarsen", 2), ("coarsen", 2)]),
+         oracle.run_voxels(ijk, off, [("coarsen", 4)]))
+    same(oracle.run_voxels(ijk, off, [("coarsen", 2)] * 3),
+         oracle.run_voxels(ijk, off, [("coarsen", 8)]))
+    same(oracle.run_voxels(ijk, off, [("refine", 2)] * 2),
+         oracle.run_voxels(ijk, off, [("refine", 4)]))
+
+
+# ------------------------------------------------------------------ dilate
+
+BOXES = [((-1, -1, -1), (1, 1, 1)), ((-1, -1, -1), (0, 0, 0)), ((0, 0, 0), (1, 1, 1)),
+         ((-1, 0, 0), (0, 1, 1)), ((0, -1, 0), (1, 0, 1))]
+
+
+@pytest.mark.parametrize("box", BOXES)
+def test_dilate_brute_minkowski(box):
+    ijk, off = synth.random_voxels(2, 40, 24, seed=21, origin=(-12, 4084, -8))
+    res = oracle.run_voxels(ijk, off, [("dilate", box[0], box[1])])
+    sets = H.jagged_sets(ijk, off)
+    for g in range(2):
+        assert H.grid_voxels(res, g) == H.brute_dilate(sets[g], *box)
+    strictly_canonical(res)
+    H.check_derived(res)
+
+
+def test_dilate_single_voxel_counts():
+    one = (np.array([[7, -1, 8]], np.int32), np.array([0, 1]))
+    n = [int(oracle.run_voxels(*one, [("dilate", lo, hi)])["voxel_counts"][0]) for lo, hi in BOXES[:3]]
+    assert n == [27, 8, 8]
+
+
+def test_dilate_pad_composition_and_reflection():
+    ijk, off = synth.make("pr1_b2_res32")
+    full = oracle.run_voxels(ijk, off, [("dilate", (-1,) * 3, (1,) * 3)])
+    comp = oracle.run_voxels(ijk, off, [("dilate", (-1,) * 3, (0,) * 3), ("dilate", (0,) * 3, (1,) * 3)])
+    same(full, comp)
+    neg = -ijk
+    a = oracle.run_voxels(neg, off, [("dilate", (0,) * 3, (1,) * 3)])
+    b = oracle.run_voxels(ijk, off, [("dilate", (-1,) * 3, (0,) * 3)])
+    for g in range(2):
+        assert H.grid_voxels(a, g) == {(-x, -y, -z) for (x, y, z) in H.grid_voxels(b, g)}
+
+
+# ------------------------------------------------------------------ batches
+
+@pytest.mark.parametrize("empty", [(0,), (2,), (4,), (0, 1, 2, 3, 4)])
+def test_empty_members(empty):
+    ijk, off = synth.random_voxels(5, 50, 30, seed=2, empty=empty)
+    for ops in ([], [("refine", 2)], [("coarsen", 2)], [("dilate", (-1,) * 3, (1,) * 3)]):
+        res = oracle.run_voxels(ijk, off, ops)
+        for g in empty:
+            assert res["leaf_offsets"][g] == res["leaf_offsets"][g + 1]
+            assert res["voxel_counts"][g] == 0
+            assert list(res["grid_bbox"][g]) == [2 ** 31 - 1] * 3 + [-2 ** 31] * 3
+            assert list(res["node_counts"][g]) == [0, 0, 0]
+        H.check_derived(res)
+
+
+def test_zero_grids():
+    res = oracle.run_voxels(np.zeros((0, 3), np.int32), np.zeros(1, np.int64), [("refine", 2)])
+    assert res["leaf_offsets"].tolist() == [0]
+    assert res["origins"].shape == (0, 3)
+
+
+def test_batch_members_independent():
+    ijk, off = synth.make("pr1_b2_res32")
+    both = oracle.run_voxels(ijk, off, [("refine", 2)])
+    for g in range(2):
+        alone = oracle.run_voxels(ijk[off[g]:off[g + 1]], np.array([0, off[g + 1] - off[g]]), [("refine", 2)])
+        same(oracle.member(both, g), alone)
+
+
+def test_run_leaves_equals_run_voxels():
+    ijk, off = synth.random_voxels(3, 200, 50, seed=4, origin=(-25, -25, -25), empty=(1,))
+    a = oracle.run_voxels(ijk, off)
+    b = oracle.run_leaves(a["origins"], a["masks"], a["leaf_offsets"])
+    same(a, b)
+    c = oracle.run_leaves(a["origins"], a["masks"], a["leaf_offsets"], [("refine", 2)])
+    same(oracle.run_voxels(ijk, off, [("refine", 2)]), c)
+
+
+def test_overflow_is_reported():
+    ijk = np.array([[2 ** 30, 0, 0]], np.int32)
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.run_voxels(ijk, np.array([0, 1]), [("refine", 2)])
+    assert e.value.status == oracle.STATUS_OVERFLOW
+    with pytest.raises(oracle.OracleError):
+        oracle.run_voxels(np.array([[2 ** 31 - 1, 0, 0]], np.int32), np.array([0, 1]),
+                          [("dilate", (0, 0, 0), (1, 1, 1))])
+    # the largest coordinate that still refines
+    res = oracle.run_voxels(np.array([[2 ** 30 - 1, -2 ** 30, 0]], np.int32), np.array([0, 1]), [("refine", 2)])
+    assert res["voxel_counts"][0] == 8
+
+
+def test_workload_shells_structure():
+    ijk, off = synth.make("shells_b16_res64")
+    res = oracle.run_voxels(ijk, off)
+    assert res["origins"].shape[0] > 0
+    strictly_canonical(res)
+    assert np.array_equal(res["voxel_counts"], np.array([len(s) for s in H.jagged_sets(ijk, off)]))
