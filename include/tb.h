@@ -1,0 +1,208 @@
+/*
+ * tb.h -- batched generated-topology passes for sparse voxel grids (GB300).
+ *
+ * C ABI of libtb.so.  The operations are the ones fVDB issue #755
+ * ("Generated-topology grid construction dominates per-iteration
+ * ConvolutionPlan cost", Suggested direction) asks for and fVDB PR #757
+ * ("Batched leaf-mask topology construction for generated conv grids",
+ * Summary items 1-2) describes: build the refined, coarsened or box-dilated
+ * topology of every member of a grid batch in one batched pass instead of one
+ * member at a time.
+ *
+ * Data model.  A batch holds B grids.  Each grid is a set of 8^3 leaves; a
+ * leaf is an int32 origin (a multiple of 8 on each axis) and a 512-bit
+ * active mask stored as eight little-endian 64-bit words: voxel
+ * (origin + (lx, ly, lz)) is bit 8*ly + lz of word lx.  Leaves of a grid are
+ * stored in canonical node order (PR #757, Summary item 1, sort bullet): by
+ * root tile floor(v/4096) compared as signed integers, then by the x-major
+ * child offset inside the 4096^3 upper node (floor(v/128) mod 32), then by the
+ * x-major child offset inside the 128^3 lower node (floor(v/8) mod 16); x is
+ * the most significant axis at every level.  Grids follow in input order.
+ *
+ * Outputs of every producing call (PR #757, Summary item 1, writer bullet):
+ * per-grid leaf offsets, per-leaf voxel offsets (0-based within the grid),
+ * per-leaf word popcount prefix, per-leaf and per-grid bounding boxes,
+ * per-grid voxel and node counts, and lower/upper node lists with parent
+ * linkage.  All arrays live in device memory owned by the batch.
+ *
+ * Conventions shared by every call:
+ *  - Streams.  All device work is enqueued on `stream` (NULL = legacy default
+ *    stream) of the current CUDA device.  A producing call blocks the host
+ *    once, on the readback of the per-grid counts (PR #757, Summary item 1,
+ *    readback bullet); tb_from_ijk and tb_from_leaves block once more, on a
+ *    coordinate-range readback that sizes the sort key.  Outputs are ready in
+ *    stream order when the call returns.
+ *  - Memory.  `alloc` may be NULL: memory then comes from cudaMallocAsync on
+ *    the device's default memory pool.  Otherwise every device allocation
+ *    (outputs and per-call scratch) goes through alloc->alloc / alloc->free,
+ *    which receive `stream`; the batch keeps a copy of the allocator and frees
+ *    its memory through it.
+ *  - Ownership.  Inputs are borrowed, read only, and may be freed once the
+ *    call returns.  On TB_OK, *out is a new batch the caller releases with
+ *    tb_batch_free.  On any error *out is set to NULL and nothing is leaked.
+ *  - Errors.  Every call returns a tb_status; tb_last_error() gives a message
+ *    for the calling thread's most recent failure.
+ */
+#ifndef TB_H_
+#define TB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__) || defined(__clang__)
+#define TB_API __attribute__((visibility("default")))
+#else
+#define TB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* tb_stream; /* identical to cudaStream_t */
+
+typedef enum {
+  TB_OK = 0,
+  TB_ERR_INVALID_ARG = 1,     /* bad pointer, size, factor, box or offsets          */
+  TB_ERR_OOM = 2,             /* the allocator returned NULL                         */
+  TB_ERR_CUDA = 3,            /* a CUDA runtime call failed                          */
+  TB_ERR_COORD_OVERFLOW = 4,  /* an output coordinate would leave int32              */
+  TB_ERR_NOT_CANONICAL = 5,   /* tb_validate found an order/mask/offset violation    */
+  TB_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait gave up (result invalid) */
+  TB_ERR_TOO_LARGE = 7        /* sizes beyond the library's documented limits        */
+} tb_status;
+
+typedef struct tb_allocator {
+  void* (*alloc)(void* ctx, size_t bytes, tb_stream stream); /* NULL on failure */
+  void (*free)(void* ctx, void* ptr, tb_stream stream);
+  void* ctx;
+} tb_allocator;
+
+typedef enum { TB_OP_REFINE = 0, TB_OP_COARSEN = 1, TB_OP_BOX_DILATE = 2 } tb_op_kind;
+
+/* One pass of a chain.  REFINE / COARSEN use `factor` (2, 4 or 8); BOX_DILATE
+ * uses lo[a] in {-1, 0} and hi[a] in {0, 1} per axis a (x, y, z). */
+typedef struct tb_op {
+  int32_t kind;
+  int32_t factor;
+  int32_t lo[3];
+  int32_t hi[3];
+} tb_op;
+
+typedef struct tb_batch tb_batch; /* opaque; owns its device arrays */
+
+/* Read-only view of a batch.  Device pointers are NULL when their array is
+ * empty.  Shapes use B = num_grids, L = num_leaves, NL = num_lowers,
+ * NU = num_uppers; all arrays are C-contiguous. */
+typedef struct tb_batch_view {
+  int32_t num_grids;
+  int32_t device;
+  int64_t num_leaves;
+  int64_t num_lowers;
+  int64_t num_uppers;
+  const int64_t* leaf_offsets_host;  /* [B+1] host copy, owned by the batch      */
+  int32_t bbox[6];                   /* whole-batch voxel bbox (min xyz, max xyz) */
+  const int64_t* leaf_offsets;       /* [B+1] first leaf of each grid             */
+  const int32_t* origins;            /* [L,3] leaf origins                         */
+  const uint64_t* masks;             /* [L,8] active masks                         */
+  const int64_t* voxel_offset;       /* [L] voxels in earlier leaves of the grid  */
+  const uint64_t* word_prefix;       /* [L] 7 x 9-bit fields: field k-1 = voxels
+                                        in words 0..k-1, k = 1..7                  */
+  const int32_t* leaf_bbox;          /* [L,6] inclusive voxel bbox of each leaf   */
+  const int32_t* leaf_grid;          /* [L] grid index of each leaf               */
+  const int32_t* leaf_parent;        /* [L] index of the leaf's lower node within
+                                        its grid                                   */
+  const int64_t* voxel_counts;       /* [B] active voxels per grid                */
+  const int32_t* grid_bbox;          /* [B,6]; empty grid: INT32_MAX x3, INT32_MIN x3 */
+  const int32_t* node_counts;        /* [B,3] upper nodes (= root tiles), lower
+                                        nodes, leaves                              */
+  const int64_t* lower_offsets;      /* [B+1] first lower node of each grid       */
+  const int64_t* upper_offsets;      /* [B+1] first upper node of each grid       */
+  const int32_t* lower_origins;      /* [NL,3] lower-node origins (multiples of 128) */
+  const int32_t* lower_parent;       /* [NL] index of the upper node within the grid */
+  const int32_t* upper_origins;      /* [NU,3] upper-node origins (multiples of 4096) */
+} tb_batch_view;
+
+/* Batch from a jagged list of voxel coordinates: the ijk front end that fVDB
+ * PR #757 (Follow-ups paragraph) names for BuildGridFromIjk.
+ *   ijk      [num_voxels, 3] int32, host or device memory; duplicates allowed,
+ *            any order.
+ *   offsets  [num_grids + 1] int64, host or device memory; offsets[0] == 0,
+ *            non-decreasing, offsets[num_grids] == num_voxels.  Grid g holds
+ *            ijk[offsets[g] .. offsets[g+1]).  Empty grids are allowed.
+ * Limits: num_grids <= 2^24, num_voxels < 2^30.  Violations of the offsets
+ * contract return TB_ERR_INVALID_ARG (checked on the device). */
+TB_API tb_status tb_from_ijk(const int32_t* ijk, const int64_t* offsets, int32_t num_grids,
+                      int64_t num_voxels, const tb_allocator* alloc, tb_stream stream,
+                      tb_batch** out);
+
+/* Batch from a jagged list of leaves in any order.  Leaves with equal origin
+ * in one grid are merged by OR-ing their masks; all-zero masks are dropped.
+ *   origins  [num_leaves, 3] int32 (multiples of 8), masks [num_leaves, 8]
+ *            uint64, leaf_offsets [num_grids + 1] int64; host or device memory.
+ * Limits: num_grids <= 2^24, num_leaves < 2^27. */
+TB_API tb_status tb_from_leaves(const int32_t* origins, const uint64_t* masks, const int64_t* leaf_offsets,
+                         int32_t num_grids, int64_t num_leaves, const tb_allocator* alloc,
+                         tb_stream stream, tb_batch** out);
+
+/* Refinement (PR #757 Summary item 1; conv_transpose_grid k2s2 for factor 2):
+ * every voxel v becomes the factor^3 voxels factor*v + [0, factor)^3.
+ * factor in {2, 4, 8}; 4 and 8 run as chained x2 passes (Summary item 1,
+ * multi-pass paragraph) with one readback in total. */
+TB_API tb_status tb_refine(const tb_batch* in, int32_t factor, const tb_allocator* alloc, tb_stream stream,
+                    tb_batch** out);
+
+/* Coarsening (PR #757 Summary item 1; conv_grid k2s2 for factor 2): voxel V is
+ * active iff some v with floor(v / factor) == V is active.  factor in
+ * {2, 4, 8}, chained x2 passes as for tb_refine. */
+TB_API tb_status tb_coarsen(const tb_batch* in, int32_t factor, const tb_allocator* alloc, tb_stream stream,
+                     tb_batch** out);
+
+/* Box dilation (PR #757 Summary item 2): the Minkowski sum of each grid with
+ * the box [lo, hi] (per axis lo in {-1,0}, hi in {0,1}).  [-1,1]^3 is
+ * conv_grid k3s1; {-1,0}^3 and {0,1}^3 are the two PadGrid octants. */
+TB_API tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const int32_t hi[3],
+                        const tb_allocator* alloc, tb_stream stream, tb_batch** out);
+
+/* Chain of passes applied in order, intermediate results kept on the device
+ * (PR #757 Summary items 1-2: multi-pass factors and the k3s2 transpose =
+ * refine x2 then the {-1,0}^3 pad).  n_ops == 0 copies the batch. */
+TB_API tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, const tb_allocator* alloc,
+                   tb_stream stream, tb_batch** out);
+
+/* Checks the canonical-batch invariants on the device: origins multiples of
+ * 8, masks non-zero, leaf_grid consistent with leaf_offsets, leaves strictly
+ * increasing in canonical order within each grid.  Blocks once.  Returns
+ * TB_OK or TB_ERR_NOT_CANONICAL. */
+TB_API tb_status tb_validate(const tb_batch* batch, tb_stream stream);
+
+/* Fills *view.  No device work. */
+TB_API tb_status tb_batch_get_view(const tb_batch* batch, tb_batch_view* view);
+
+/* Copies leaf records into caller buffers (host or device memory; any may be
+ * NULL to skip): origins [L,3] int32, masks [L,8] uint64, voxel_offset [L]
+ * int64, leaf_offsets [B+1] int64.  Enqueued on `stream`; the caller
+ * synchronizes before reading host buffers. */
+TB_API tb_status tb_batch_export(const tb_batch* batch, int32_t* origins, uint64_t* masks,
+                          int64_t* voxel_offset, int64_t* leaf_offsets, tb_stream stream);
+
+/* Releases the batch's memory (stream-ordered on `stream`).  NULL is a no-op. */
+TB_API tb_status tb_batch_free(tb_batch* batch, tb_stream stream);
+
+/* Message for the calling thread's most recent failure ("" if none). */
+TB_API const char* tb_last_error(void);
+
+/* Static name of a status code. */
+TB_API const char* tb_status_string(tb_status status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+TB_API int32_t tb_version(void);
+
+/* Number of kernels this thread has launched through the library so far. */
+TB_API int64_t tb_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TB_H_ */

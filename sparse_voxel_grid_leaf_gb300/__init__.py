@@ -1,0 +1,337 @@
+"""Batched generated-topology passes for sparse voxel grids on GB300.
+
+Python binding of ``libtb.so`` (C ABI in ``include/tb.h``).  Every step of a
+pass runs in the library's CUDA kernels; this module only marshals arguments
+(pointers, sizes, the current torch CUDA stream) and exposes the resulting
+device arrays as zero-copy torch tensors.  There is no CPU fallback: calling
+any op without the built library raises ``TBError``.
+
+Operations follow fVDB PR #757 ("Batched leaf-mask topology construction for
+generated conv grids", Summary items 1-2) and the ijk front end named in its
+Follow-ups paragraph:
+
+* ``from_ijk(ijk, offsets)``  jagged voxel coordinates -> batch
+* ``from_leaves(origins, masks, offsets)``  jagged leaves -> batch
+* ``refine(b, f)``, ``coarsen(b, f)``  f in {2, 4, 8}
+* ``box_dilate(b, lo, hi)``  Minkowski sum with [lo, hi]^3 (unit boxes)
+* ``chain(b, ops)``  several passes with intermediate results on the device
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Dict, Iterable, Optional, Sequence, Tuple
+
+import numpy as np
+
+from . import synth  # noqa: F401  (seeded workloads; no method arithmetic)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtb.so")
+
+TB_OK = 0
+STATUS_NAMES = {0: "TB_OK", 1: "TB_ERR_INVALID_ARG", 2: "TB_ERR_OOM", 3: "TB_ERR_CUDA",
+                4: "TB_ERR_COORD_OVERFLOW", 5: "TB_ERR_NOT_CANONICAL", 6: "TB_ERR_DEVICE_TIMEOUT",
+                7: "TB_ERR_TOO_LARGE"}
+OP_REFINE, OP_COARSEN, OP_BOX_DILATE = 0, 1, 2
+
+
+class TBError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+class _Op(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("factor", ctypes.c_int32),
+                ("lo", ctypes.c_int32 * 3), ("hi", ctypes.c_int32 * 3)]
+
+
+class _View(ctypes.Structure):
+    _fields_ = [("num_grids", ctypes.c_int32), ("device", ctypes.c_int32),
+                ("num_leaves", ctypes.c_int64), ("num_lowers", ctypes.c_int64),
+                ("num_uppers", ctypes.c_int64), ("leaf_offsets_host", ctypes.c_void_p),
+                ("bbox", ctypes.c_int32 * 6)] + \
+               [(n, ctypes.c_void_p) for n in (
+                   "leaf_offsets", "origins", "masks", "voxel_offset", "word_prefix", "leaf_bbox",
+                   "leaf_grid", "leaf_parent", "voxel_counts", "grid_bbox", "node_counts",
+                   "lower_offsets", "upper_offsets", "lower_origins", "lower_parent", "upper_origins")]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def lib():
+    """The loaded ``libtb.so`` (raises ``TBError`` if it has not been built)."""
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise TBError(-1, "libtb.so is not built (run __graft_entry__.build() or "
+                                  "python -m sparse_voxel_grid_leaf_gb300._build)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            pp = ctypes.POINTER(ctypes.c_void_p)
+            sig = {
+                "tb_from_ijk": [vp, vp, i32, i64, vp, vp, pp],
+                "tb_from_leaves": [vp, vp, vp, i32, i64, vp, vp, pp],
+                "tb_refine": [vp, i32, vp, vp, pp],
+                "tb_coarsen": [vp, i32, vp, vp, pp],
+                "tb_box_dilate": [vp, vp, vp, vp, vp, pp],
+                "tb_chain": [vp, vp, i32, vp, vp, pp],
+                "tb_validate": [vp, vp],
+                "tb_batch_get_view": [vp, ctypes.POINTER(_View)],
+                "tb_batch_export": [vp, vp, vp, vp, vp, vp],
+                "tb_batch_free": [vp, vp],
+            }
+            for name, args in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            L.tb_last_error.restype = ctypes.c_char_p
+            L.tb_last_error.argtypes = []
+            L.tb_version.restype = ctypes.c_int32
+            L.tb_kernel_launch_count.restype = ctypes.c_int64
+            _lib = L
+        return _lib
+
+
+def _check(st: int):
+    if st != TB_OK:
+        raise TBError(st, lib().tb_last_error().decode())
+
+
+def _stream(stream=None) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(getattr(stream, "cuda_stream", stream) or 0)
+
+
+def kernel_launch_count() -> int:
+    """Kernels launched through the library by the calling thread so far."""
+    return int(lib().tb_kernel_launch_count())
+
+
+class _CAI:
+    """__cuda_array_interface__ holder that keeps its batch alive."""
+
+    def __init__(self, owner, ptr, shape, typestr):
+        self._owner = owner
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 2, "strides": None}
+
+
+_ARRAYS = {
+    # name: (dtype typestr, numpy dtype, shape function of (B, L, NL, NU))
+    "leaf_offsets": ("<i8", np.int64, lambda B, L, NL, NU: (B + 1,)),
+    "origins": ("<i4", np.int32, lambda B, L, NL, NU: (L, 3)),
+    "masks": ("<i8", np.uint64, lambda B, L, NL, NU: (L, 8)),
+    "voxel_offset": ("<i8", np.int64, lambda B, L, NL, NU: (L,)),
+    "word_prefix": ("<i8", np.uint64, lambda B, L, NL, NU: (L,)),
+    "leaf_bbox": ("<i4", np.int32, lambda B, L, NL, NU: (L, 6)),
+    "leaf_grid": ("<i4", np.int32, lambda B, L, NL, NU: (L,)),
+    "leaf_parent": ("<i4", np.int32, lambda B, L, NL, NU: (L,)),
+    "voxel_counts": ("<i8", np.int64, lambda B, L, NL, NU: (B,)),
+    "grid_bbox": ("<i4", np.int32, lambda B, L, NL, NU: (B, 6)),
+    "node_counts": ("<i4", np.int32, lambda B, L, NL, NU: (B, 3)),
+    "lower_offsets": ("<i8", np.int64, lambda B, L, NL, NU: (B + 1,)),
+    "upper_offsets": ("<i8", np.int64, lambda B, L, NL, NU: (B + 1,)),
+    "lower_origins": ("<i4", np.int32, lambda B, L, NL, NU: (NL, 3)),
+    "lower_parent": ("<i4", np.int32, lambda B, L, NL, NU: (NL,)),
+    "upper_origins": ("<i4", np.int32, lambda B, L, NL, NU: (NU, 3)),
+}
+ARRAY_NAMES = tuple(_ARRAYS)
+
+
+class Batch:
+    """A batch of grids produced by the library (owns its device memory)."""
+
+    def __init__(self, handle: int):
+        self._h = ctypes.c_void_p(handle)
+        v = _View()
+        _check(lib().tb_batch_get_view(self._h, ctypes.byref(v)))
+        self._v = v
+        self.num_grids = int(v.num_grids)
+        self.num_leaves = int(v.num_leaves)
+        self.num_lowers = int(v.num_lowers)
+        self.num_uppers = int(v.num_uppers)
+        self.device = int(v.device)
+        self.bbox = tuple(int(x) for x in v.bbox)
+        n = self.num_grids + 1
+        self.leaf_offsets_host = np.ctypeslib.as_array(
+            ctypes.cast(v.leaf_offsets_host, ctypes.POINTER(ctypes.c_int64)), shape=(n,)).copy()
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        if self._h is None:
+            raise TBError(1, "batch already freed")
+        return self._h
+
+    def tensor(self, name: str):
+        """Zero-copy torch CUDA tensor of one device array of the batch (64-bit
+    masks and word prefixes are exposed as int64 bit patterns)."""
+        import torch
+        typestr, npdt, shp = _ARRAYS[name]
+        shape = shp(self.num_grids, self.num_leaves, self.num_lowers, self.num_uppers)
+        ptr = getattr(self._v, name)
+        if not ptr or int(np.prod(shape)) == 0:
+            return torch.empty(shape, dtype=_torch_dtype(npdt), device="cuda:%d" % self.device)
+        return torch.as_tensor(_CAI(self, ptr, shape, typestr), device="cuda:%d" % self.device)
+
+    def __getattr__(self, name):
+        if name in _ARRAYS:
+            return self.tensor(name)
+        raise AttributeError(name)
+
+    def to_numpy(self, names: Sequence[str] = ARRAY_NAMES) -> Dict[str, np.ndarray]:
+        """Copies arrays to host numpy (synchronizes the current stream)."""
+        import torch
+        out = {}
+        for n in names:
+            out[n] = self.tensor(n).cpu().numpy()
+            if _ARRAYS[n][1] == np.uint64:
+                out[n] = out[n].view(np.uint64)
+        torch.cuda.current_stream().synchronize()
+        return out
+
+    def validate(self, stream=None):
+        _check(lib().tb_validate(self.handle, ctypes.c_void_p(_stream(stream))))
+
+    def free(self, stream=None):
+        if self._h is not None:
+            lib().tb_batch_free(self._h, ctypes.c_void_p(_stream(stream)))
+            self._h = None
+
+    def __del__(self):
+        try:
+            if self._h is not None and _lib is not None:
+                _lib.tb_batch_free(self._h, None)
+                self._h = None
+        except Exception:
+            pass
+
+
+def _torch_dtype(npdt):
+    import torch
+    return {np.int32: torch.int32, np.int64: torch.int64, np.uint64: torch.int64}[npdt]
+
+
+def _ptr(x) -> Tuple[int, object]:
+    """(address, keep-alive) of a torch tensor or numpy array, C-contiguous."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            if not x.is_contiguous():
+                x = x.contiguous()
+            return x.data_ptr(), x
+    except ImportError:
+        pass
+    a = np.ascontiguousarray(x)
+    return a.ctypes.data, a
+
+
+def _new(fn, *args) -> Batch:
+    out = ctypes.c_void_p()
+    _check(fn(*args, ctypes.byref(out)))
+    return Batch(out.value)
+
+
+def from_ijk(ijk, offsets, stream=None) -> Batch:
+    """Batch from int32 voxel coordinates ``ijk [N,3]`` and int64 ``offsets [B+1]``
+    (torch tensors on the GPU or the host, or numpy arrays)."""
+    pi, ki = _ptr(ijk)
+    po, ko = _ptr(offsets)
+    B = int(ko.shape[0]) - 1
+    N = int(ki.shape[0]) if ki.ndim else 0
+    _dtype_check(ki, "int32")
+    _dtype_check(ko, "int64")
+    return _new(lib().tb_from_ijk, ctypes.c_void_p(pi), ctypes.c_void_p(po), B, N, None,
+                ctypes.c_void_p(_stream(stream)))
+
+
+def from_leaves(origins, masks, offsets, stream=None) -> Batch:
+    """Batch from leaves: int32 ``origins [L,3]``, uint64 ``masks [L,8]``, int64 ``offsets [B+1]``."""
+    po, ko = _ptr(origins)
+    pm, km = _ptr(masks)
+    pf, kf = _ptr(offsets)
+    _dtype_check(ko, "int32")
+    _dtype_check(km, "uint64", "int64")
+    _dtype_check(kf, "int64")
+    return _new(lib().tb_from_leaves, ctypes.c_void_p(po), ctypes.c_void_p(pm), ctypes.c_void_p(pf),
+                int(kf.shape[0]) - 1, int(ko.shape[0]), None, ctypes.c_void_p(_stream(stream)))
+
+
+def _dtype_check(x, *names):
+    n = str(x.dtype).replace("torch.", "")
+    if n not in names:
+        raise TBError(1, "expected dtype %s, got %s" % ("/".join(names), n))
+
+
+def refine(b: Batch, factor: int = 2, stream=None) -> Batch:
+    return _new(lib().tb_refine, b.handle, int(factor), None, ctypes.c_void_p(_stream(stream)))
+
+
+def coarsen(b: Batch, factor: int = 2, stream=None) -> Batch:
+    return _new(lib().tb_coarsen, b.handle, int(factor), None, ctypes.c_void_p(_stream(stream)))
+
+
+def box_dilate(b: Batch, lo=(-1, -1, -1), hi=(1, 1, 1), stream=None) -> Batch:
+    lo_a = (ctypes.c_int32 * 3)(*lo)
+    hi_a = (ctypes.c_int32 * 3)(*hi)
+    return _new(lib().tb_box_dilate, b.handle, lo_a, hi_a, None, ctypes.c_void_p(_stream(stream)))
+
+
+def make_ops(ops: Iterable[Tuple]):
+    """Op tuples ``("refine", f)``, ``("coarsen", f)``, ``("dilate", lo, hi)`` -> C array."""
+    ops = list(ops)
+    arr = (_Op * max(1, len(ops)))()
+    for i, op in enumerate(ops):
+        if op[0] == "refine":
+            arr[i].kind, arr[i].factor = OP_REFINE, int(op[1])
+        elif op[0] == "coarsen":
+            arr[i].kind, arr[i].factor = OP_COARSEN, int(op[1])
+        elif op[0] == "dilate":
+            arr[i].kind, arr[i].factor = OP_BOX_DILATE, 1
+            for a in range(3):
+                arr[i].lo[a], arr[i].hi[a] = int(op[1][a]), int(op[2][a])
+        else:
+            raise TBError(1, "unknown op %r" % (op[0],))
+    return arr, len(ops)
+
+
+def chain(b: Batch, ops: Iterable[Tuple], stream=None) -> Batch:
+    arr, n = make_ops(ops)
+    return _new(lib().tb_chain, b.handle, arr, n, None, ctypes.c_void_p(_stream(stream)))
+
+
+# Convolution-topology aliases named by fVDB PR #757 (Summary and Measurements).
+def conv_grid_k2s2(b: Batch, stream=None) -> Batch:
+    """conv_grid with kernel 2, stride 2: coarsening by 2."""
+    return coarsen(b, 2, stream)
+
+
+def conv_transpose_grid_k2s2(b: Batch, stream=None) -> Batch:
+    """conv_transpose_grid with kernel 2, stride 2: refinement by 2."""
+    return refine(b, 2, stream)
+
+
+def conv_grid_k3s1(b: Batch, stream=None) -> Batch:
+    """conv_grid with kernel 3, stride 1: dilation by [-1, 1]^3."""
+    return box_dilate(b, (-1, -1, -1), (1, 1, 1), stream)
+
+
+def conv_transpose_grid_k3s2(b: Batch, stream=None) -> Batch:
+    """conv_transpose_grid with kernel 3, stride 2: refine by 2, then the {-1,0}^3 pad."""
+    return chain(b, [("refine", 2), ("dilate", (-1, -1, -1), (0, 0, 0))], stream)
+
+
+def export_host(b: Batch, origins: np.ndarray, masks: np.ndarray, voxel_offset: Optional[np.ndarray] = None,
+                leaf_offsets: Optional[np.ndarray] = None, stream=None):
+    """Enqueues copies of leaf records into host buffers (caller synchronizes)."""
+    def p(x):
+        return None if x is None else ctypes.c_void_p(_ptr(x)[0])
+    _check(lib().tb_batch_export(b.handle, p(origins), p(masks), p(voxel_offset), p(leaf_offsets),
+                                 ctypes.c_void_p(_stream(stream))))

@@ -1,0 +1,892 @@
+// Host driver and C ABI of libtb.so (declared in include/tb.h).
+//
+// One call = one stream-ordered sequence of passes (fVDB PR #757 "Batched
+// leaf-mask topology construction for generated conv grids", Summary item 1):
+// per pass an emission kernel, the digit passes of the radix sort and the
+// dedup scan; intermediate passes of a chain hand their leaves to the next
+// pass on the device, and the last pass does the one count readback,
+// allocates the outputs and runs the batched writer.  All buffers of a call
+// are sized from host-known upper bounds (refine emits at most 8 leaves per
+// source leaf, coarsen 1, a box dilation at most 27), so no readback is
+// needed between passes.
+//
+// The sort key's width follows the batch's voxel bounding box, which the
+// host tracks exactly: refine maps [lo, hi] to [2 lo, 2 hi + 1], coarsen to
+// [floor(lo/2), floor(hi/2)], a box dilation to [lo + d_lo, hi + d_hi], and
+// the front ends read it back from a small prepass.
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "../../include/tb.h"
+#include "tb_common.cuh"
+#include "tb_launch.h"
+
+using namespace tb;
+
+struct tb_batch {
+  int32_t B = 0;
+  int device = 0;
+  int64_t L = 0, NL = 0, NU = 0;
+  bool has_alloc = false;
+  tb_allocator alloc{};
+  void* mem = nullptr;
+  std::vector<int64_t> leaf_offsets_host;
+  int32_t bbox[6] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MIN, INT32_MIN, INT32_MIN};
+  int64_t* leaf_offsets = nullptr;
+  int32_t* origins = nullptr;
+  uint64_t* masks = nullptr;
+  int64_t* voxel_offset = nullptr;
+  uint64_t* word_prefix = nullptr;
+  int32_t* leaf_bbox = nullptr;
+  int32_t* leaf_grid = nullptr;
+  int32_t* leaf_parent = nullptr;
+  int64_t* voxel_counts = nullptr;
+  int32_t* grid_bbox = nullptr;
+  int32_t* node_counts = nullptr;
+  int64_t* lower_offsets = nullptr;
+  int64_t* upper_offsets = nullptr;
+  int32_t* lower_origins = nullptr;
+  int32_t* lower_parent = nullptr;
+  int32_t* upper_origins = nullptr;
+};
+
+namespace {
+
+thread_local std::string t_err;
+thread_local long long t_launches = 0;
+
+tb_status fail(tb_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return st;
+}
+
+#define TB_CUDA(expr)                                                                          \
+  do {                                                                                         \
+    cudaError_t e_ = (expr);                                                                   \
+    if (e_ != cudaSuccess) return fail(TB_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+// ---------------------------------------------------------------- device info
+
+struct DeviceInfo {
+  int sms = 0;
+  int occ_sort = 1, occ_dedup = 1;
+  int occ_write[5][2] = {};
+  bool ready = false;
+};
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+
+tb_status device_info(int dev, DeviceInfo** out) {
+  if (dev < 0 || dev >= 64) return fail(TB_ERR_INVALID_ARG, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    TB_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
+    d.occ_sort = occupancy_sort();
+    d.occ_dedup = occupancy_dedup();
+    for (int op = 0; op < 5; ++op)
+      for (int f = 0; f < 2; ++f) d.occ_write[op][f] = occupancy_write(op, f != 0);
+    // keep freed memory in the default pool between calls
+    cudaMemPool_t pool;
+    if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
+      uint64_t thr = UINT64_MAX;
+      cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &thr);
+    }
+    cudaGetLastError();
+    d.ready = true;
+  }
+  *out = &d;
+  return TB_OK;
+}
+
+// ---------------------------------------------------------------- memory
+
+struct Mem {
+  const tb_allocator* a;
+  cudaStream_t s;
+  void* get(size_t n) const {
+    if (n == 0) return nullptr;
+    if (a) return a->alloc(a->ctx, n, (tb_stream)s);
+    void* p = nullptr;
+    if (cudaMallocAsync(&p, n, s) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return p;
+  }
+  void put(void* p) const {
+    if (!p) return;
+    if (a) a->free(a->ctx, p, (tb_stream)s);
+    else cudaFreeAsync(p, s);
+  }
+};
+
+// Frees a buffer at scope exit unless released.
+struct Guard {
+  const Mem* m;
+  void* p;
+  ~Guard() {
+    if (p) m->put(p);
+  }
+};
+
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes, size_t align = 256) {
+    off = (off + align - 1) & ~(align - 1);
+    const size_t r = off;
+    off += bytes;
+    return r;
+  }
+};
+
+struct Pinned {
+  void* p = nullptr;
+  size_t n = 0;
+  ~Pinned() {
+    if (p) cudaFreeHost(p);
+  }
+  void* get(size_t bytes) {
+    if (bytes > n) {
+      if (p) cudaFreeHost(p);
+      p = nullptr;
+      n = 0;
+      if (cudaHostAlloc(&p, bytes, cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+      }
+      n = bytes;
+    }
+    return p;
+  }
+};
+thread_local Pinned t_pinned;
+
+bool device_accessible(const void* p) {
+  if (!p) return false;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
+}
+
+// ---------------------------------------------------------------- key layout
+
+int bitwidth(uint64_t x) {
+  int n = 0;
+  while (x) {
+    ++n;
+    x >>= 1;
+  }
+  return n;
+}
+int64_t floor_div(int64_t a, int64_t b) {
+  int64_t q = a / b;
+  if ((a % b != 0) && (a < 0)) --q;
+  return q;
+}
+
+// Returns false if the key needs more than 64 bits.
+bool make_layout(int32_t B, const int32_t bb[6], bool empty, KeyLayout& K) {
+  std::memset(&K, 0, sizeof K);
+  K.gw = B > 1 ? bitwidth((uint64_t)(B - 1)) : 0;
+  for (int a = 0; a < 3; ++a) {
+    int lw = 0;
+    if (!empty) {
+      const int64_t Lo = floor_div(bb[a], 8), Hi = floor_div(bb[3 + a], 8);
+      const int64_t tlo = floor_div(Lo, 512), thi = floor_div(Hi, 512);
+      K.tile_base[a] = (int32_t)tlo;
+      K.tw[a] = bitwidth((uint64_t)(thi - tlo));
+      lw = (thi > tlo) ? 9 : std::min(9, bitwidth((uint64_t)(Lo ^ Hi)));
+      K.lc_const[a] = (int32_t)(Lo & 0x1FF & ~((1 << lw) - 1));
+    }
+    K.lwl[a] = std::min(lw, 4);
+    K.uw[a] = std::max(lw - 4, 0);
+  }
+  K.lshift[2] = 0;
+  K.lshift[1] = K.lwl[2];
+  K.lshift[0] = K.lwl[2] + K.lwl[1];
+  K.lower_bits = K.lwl[0] + K.lwl[1] + K.lwl[2];
+  K.ushift[2] = K.lower_bits;
+  K.ushift[1] = K.ushift[2] + K.uw[2];
+  K.ushift[0] = K.ushift[1] + K.uw[1];
+  K.node_bits = K.ushift[0] + K.uw[0];
+  K.tshift[2] = K.node_bits;
+  K.tshift[1] = K.tshift[2] + K.tw[2];
+  K.tshift[0] = K.tshift[1] + K.tw[1];
+  K.gshift = K.tshift[0] + K.tw[0];
+  K.W = K.gshift + K.gw;
+  return K.W <= 64;
+}
+
+// ---------------------------------------------------------------- pass plan
+
+struct PassSpec {
+  int op;
+  int32_t lo[3], hi[3];
+};
+
+struct PassPlan {
+  PassSpec spec;
+  long long in_cap = 0, slot_cap = 0;
+  bool empty = true;         // output has no voxels
+  int32_t bbox[6];           // output voxel bbox (exact)
+  KeyLayout K;
+  int P = 0;
+  long long sort_tiles = 0, dedup_tiles = 0, write_tiles = 0;
+  size_t rb = 0, ctl = 0, sort_status = 0, dedup_status = 0, write_status = 0, first = 0, gbox = 0;
+};
+
+long long slots_per_source(const PassSpec& s) {
+  switch (s.op) {
+    case kRefine: return 8;
+    case kDilate: return (long long)(s.hi[0] - s.lo[0] + 1) * (s.hi[1] - s.lo[1] + 1) * (s.hi[2] - s.lo[2] + 1);
+    default: return 1;
+  }
+}
+
+// Output bbox of one pass from its input bbox; false on int32 overflow.
+bool propagate_bbox(const PassSpec& s, const int32_t in[6], int32_t out[6]) {
+  for (int a = 0; a < 3; ++a) {
+    int64_t lo = in[a], hi = in[3 + a];
+    if (s.op == kRefine) {
+      lo = 2 * lo;
+      hi = 2 * hi + 1;
+    } else if (s.op == kCoarsen) {
+      lo = floor_div(lo, 2);
+      hi = floor_div(hi, 2);
+    } else if (s.op == kDilate) {
+      lo += s.lo[a];
+      hi += s.hi[a];
+    }
+    if (lo < INT32_MIN || hi > INT32_MAX) return false;
+    out[a] = (int32_t)lo;
+    out[3 + a] = (int32_t)hi;
+  }
+  return true;
+}
+
+tb_status plan_layouts(std::vector<PassPlan>& plans, int32_t B, const int32_t bbox_in[6], bool empty_in) {
+  int32_t cur[6];
+  std::memcpy(cur, bbox_in, sizeof cur);
+  bool empty = empty_in;
+  for (size_t p = 0; p < plans.size(); ++p) {
+    PassPlan& pl = plans[p];
+    if (!empty && !propagate_bbox(pl.spec, cur, pl.bbox))
+      return fail(TB_ERR_COORD_OVERFLOW, "pass %zu would move voxel coordinates outside int32", p);
+    if (empty) std::memcpy(pl.bbox, cur, sizeof cur);
+    pl.empty = empty;
+    if (!make_layout(B, pl.bbox, empty, pl.K))
+      return fail(TB_ERR_TOO_LARGE, "pass %zu: the batch's grid count and coordinate range need a %d-bit sort key (max 64)",
+                  p, pl.K.W);
+    pl.P = (pl.K.W + 7) / 8;
+    std::memcpy(cur, pl.bbox, sizeof cur);
+  }
+  return TB_OK;
+}
+
+// ---------------------------------------------------------------- sources
+
+enum SrcKind { kSrcBatch, kSrcIjk, kSrcLeaves };
+
+struct Source {
+  SrcKind kind;
+  const tb_batch* batch = nullptr;
+  const int32_t* ijk = nullptr;
+  const int32_t* origins = nullptr;
+  const uint64_t* masks = nullptr;
+  const int64_t* offsets = nullptr;
+  int32_t B = 0;
+  long long count = 0;
+};
+
+void batch_set_view(tb_batch* b, char* base, const size_t off[16]) {
+  auto at = [&](int k) -> char* { return base ? base + off[k] : nullptr; };
+  b->leaf_offsets = (int64_t*)at(0);
+  b->origins = (int32_t*)at(1);
+  b->masks = (uint64_t*)at(2);
+  b->voxel_offset = (int64_t*)at(3);
+  b->word_prefix = (uint64_t*)at(4);
+  b->leaf_bbox = (int32_t*)at(5);
+  b->leaf_grid = (int32_t*)at(6);
+  b->leaf_parent = (int32_t*)at(7);
+  b->voxel_counts = (int64_t*)at(8);
+  b->grid_bbox = (int32_t*)at(9);
+  b->node_counts = (int32_t*)at(10);
+  b->lower_offsets = (int64_t*)at(11);
+  b->upper_offsets = (int64_t*)at(12);
+  b->lower_origins = (int32_t*)at(13);
+  b->lower_parent = (int32_t*)at(14);
+  b->upper_origins = (int32_t*)at(15);
+}
+
+int blocks_for(long long work, long long per_block, long long cap) {
+  long long n = (work + per_block - 1) / per_block;
+  if (n < 1) n = 1;
+  if (n > cap) n = cap;
+  return (int)n;
+}
+
+// ---------------------------------------------------------------- the driver
+
+tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_allocator* alloc,
+              cudaStream_t stream, tb_batch** out) {
+  if (!out) return fail(TB_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (alloc && (!alloc->alloc || !alloc->free)) return fail(TB_ERR_INVALID_ARG, "allocator without alloc/free");
+  if (specs.empty()) return fail(TB_ERR_INVALID_ARG, "no passes");
+  int dev = 0;
+  TB_CUDA(cudaGetDevice(&dev));
+  DeviceInfo* di = nullptr;
+  tb_status st = device_info(dev, &di);
+  if (st != TB_OK) return st;
+  const Mem mem{alloc, stream};
+  const int32_t B = src.B;
+  const bool front = src.kind != kSrcBatch;
+
+  // ---- bounds of every pass (host-known, no readback)
+  std::vector<PassPlan> plans(specs.size());
+  long long cap = src.count;
+  long long max_slots = 0, max_inter = 0;
+  for (size_t p = 0; p < specs.size(); ++p) {
+    PassPlan& pl = plans[p];
+    pl.spec = specs[p];
+    pl.in_cap = cap;
+    if (pl.spec.op != kIjk && cap >= (1ll << (32 - kSrcShift)))
+      return fail(TB_ERR_TOO_LARGE, "pass %zu: %lld source leaves exceed the limit of 2^27", p, cap);
+    pl.slot_cap = cap * slots_per_source(pl.spec);
+    if (pl.slot_cap >= (1ll << 30))
+      return fail(TB_ERR_TOO_LARGE, "pass %zu: up to %lld candidate leaves exceed the limit of 2^30", p,
+                  pl.slot_cap);
+    cap = pl.slot_cap;
+    max_slots = std::max(max_slots, pl.slot_cap);
+    if (p + 1 < specs.size()) max_inter = std::max(max_inter, pl.slot_cap);
+  }
+
+  // ---- key layouts (front ends: after the range prepass)
+  if (!front) {
+    const tb_batch* b = src.batch;
+    const bool empty = b->L == 0;
+    st = plan_layouts(plans, B, b->bbox, empty);
+    if (st != TB_OK) return st;
+  } else {
+    for (auto& pl : plans) pl.P = kMaxDigitPasses;  // sized for the widest key until the prepass
+  }
+
+  // ---- workspace layout: a zeroed control region, then the slot buffers
+  Carve c;
+  for (auto& pl : plans) {
+    pl.sort_tiles = std::max(1ll, (pl.slot_cap + kSortTile - 1) / kSortTile);
+    pl.dedup_tiles = std::max(1ll, (pl.slot_cap + kDedupTile - 1) / kDedupTile);
+    pl.write_tiles = std::max(1ll, (pl.slot_cap + kWriteTile - 1) / kWriteTile);
+    pl.rb = c.take(sizeof(ReadbackHeader) + 3 * sizeof(int64_t) * (size_t)(B + 1));
+    pl.ctl = c.take(sizeof(PassCtl));
+    pl.sort_status = c.take((size_t)pl.P * pl.sort_tiles * kBins * 4);
+    pl.dedup_status = c.take((size_t)pl.dedup_tiles * 3 * 8);
+    pl.write_status = c.take((size_t)pl.write_tiles * 8);
+    pl.first = c.take((size_t)3 * B * 4);
+    pl.gbox = c.take((size_t)6 * B * 4);
+  }
+  const size_t zero_bytes = c.off;
+  const size_t o_keys0 = c.take((size_t)max_slots * 8), o_keys1 = c.take((size_t)max_slots * 8);
+  const size_t o_vals0 = c.take((size_t)max_slots * 4), o_vals1 = c.take((size_t)max_slots * 4);
+  const size_t o_run = c.take((size_t)(max_slots + 1) * 4);
+  const size_t o_llow = c.take((size_t)max_slots * 4), o_lup = c.take((size_t)max_slots * 4);
+  size_t o_inter[2][3];
+  for (int k = 0; k < 2; ++k) {
+    o_inter[k][0] = c.take((size_t)max_inter * 12);
+    o_inter[k][1] = c.take((size_t)max_inter * 64);
+    o_inter[k][2] = c.take((size_t)max_inter * 4);
+  }
+  // staging of host-resident inputs
+  const int32_t* in_ijk = src.ijk;
+  const int32_t* in_orig = src.origins;
+  const uint64_t* in_mask = src.masks;
+  const int64_t* in_off = src.offsets;
+  size_t o_st_a = 0, o_st_b = 0, o_st_off = 0;
+  bool st_a = false, st_b = false, st_off = false;
+  if (src.kind == kSrcIjk) {
+    st_a = src.count > 0 && !device_accessible(src.ijk);
+    if (st_a) o_st_a = c.take((size_t)src.count * 12);
+  } else if (src.kind == kSrcLeaves) {
+    st_a = src.count > 0 && !device_accessible(src.origins);
+    st_b = src.count > 0 && !device_accessible(src.masks);
+    if (st_a) o_st_a = c.take((size_t)src.count * 12);
+    if (st_b) o_st_b = c.take((size_t)src.count * 64);
+  }
+  if (front) {
+    st_off = !device_accessible(src.offsets);
+    if (st_off) o_st_off = c.take((size_t)(B + 1) * 8);
+  }
+  const size_t ws_bytes = c.off;
+  char* ws = (char*)mem.get(ws_bytes);
+  if (!ws && ws_bytes) return fail(TB_ERR_OOM, "workspace allocation of %zu bytes failed", ws_bytes);
+  Guard ws_guard{&mem, ws};
+  TB_CUDA(cudaMemsetAsync(ws, 0, zero_bytes, stream));
+  if (st_a) {
+    void* d = ws + o_st_a;
+    TB_CUDA(cudaMemcpyAsync(d, src.kind == kSrcIjk ? (const void*)src.ijk : (const void*)src.origins,
+                            (size_t)src.count * 12, cudaMemcpyDefault, stream));
+    if (src.kind == kSrcIjk) in_ijk = (const int32_t*)d;
+    else in_orig = (const int32_t*)d;
+  }
+  if (st_b) {
+    TB_CUDA(cudaMemcpyAsync(ws + o_st_b, src.masks, (size_t)src.count * 64, cudaMemcpyDefault, stream));
+    in_mask = (const uint64_t*)(ws + o_st_b);
+  }
+  if (st_off) {
+    TB_CUDA(cudaMemcpyAsync(ws + o_st_off, src.offsets, (size_t)(B + 1) * 8, cudaMemcpyDefault, stream));
+    in_off = (const int64_t*)(ws + o_st_off);
+  }
+
+  const size_t rb_bytes = sizeof(ReadbackHeader) + 3 * sizeof(int64_t) * (size_t)(B + 1);
+  ReadbackHeader* host_rb = (ReadbackHeader*)t_pinned.get(rb_bytes + 4 * plans.size());
+  if (!host_rb) return fail(TB_ERR_OOM, "pinned host buffer of %zu bytes failed", rb_bytes);
+
+  // ---- front ends: range prepass and its readback
+  if (front) {
+    ReadbackHeader* rb0 = (ReadbackHeader*)(ws + plans[0].rb);
+    const int blocks = blocks_for(src.count, 256, (long long)di->sms * 4);
+    if (src.kind == kSrcIjk) TB_CUDA(launch_prepass_ijk(in_ijk, src.count, in_off, B, rb0, blocks, stream));
+    else TB_CUDA(launch_prepass_leaves(in_orig, in_mask, src.count, in_off, B, rb0, blocks, stream));
+    ++t_launches;
+    TB_CUDA(cudaMemcpyAsync(host_rb, rb0, sizeof(ReadbackHeader), cudaMemcpyDeviceToHost, stream));
+    TB_CUDA(cudaStreamSynchronize(stream));
+    if (host_rb->err & kErrBadOffsets)
+      return fail(TB_ERR_INVALID_ARG, "offsets must start at 0, be non-decreasing and end at %lld", src.count);
+    if (host_rb->err & kErrNotAligned) return fail(TB_ERR_INVALID_ARG, "leaf origins must be multiples of 8");
+    int32_t bb[6];
+    for (int a = 0; a < 3; ++a) {
+      bb[a] = dec_min(host_rb->bbox_enc[a]);
+      bb[3 + a] = dec_max(host_rb->bbox_enc[3 + a]);
+    }
+    const bool empty = bb[0] > bb[3];
+    const int P_alloc = plans[0].P;
+    st = plan_layouts(plans, B, bb, empty);
+    if (st != TB_OK) return st;
+    if (plans[0].P > P_alloc) return fail(TB_ERR_CUDA, "internal: digit passes exceed the allocation");
+    // the status region was sized for P_alloc passes; the stride stays sort_tiles
+  }
+
+  // ---- passes
+  PassArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.B = B;
+  a.keys[0] = (uint64_t*)(ws + o_keys0);
+  a.keys[1] = (uint64_t*)(ws + o_keys1);
+  a.vals[0] = (uint32_t*)(ws + o_vals0);
+  a.vals[1] = (uint32_t*)(ws + o_vals1);
+  a.run_start = (uint32_t*)(ws + o_run);
+  a.leaf_lower = (uint32_t*)(ws + o_llow);
+  a.leaf_upper = (uint32_t*)(ws + o_lup);
+  a.ijk = in_ijk;
+  a.in_offsets = in_off;
+  if (src.kind == kSrcBatch) {
+    a.src_origins = src.batch->origins;
+    a.src_masks = src.batch->masks;
+    a.src_grid = src.batch->leaf_grid;
+    a.src_count = src.batch->L;
+  } else {
+    a.src_origins = in_orig;
+    a.src_masks = in_mask;
+    a.src_grid = nullptr;
+    a.src_count = src.count;
+  }
+  a.src_count_dev = nullptr;
+
+  const int op_last = plans.back().spec.op;
+  for (size_t p = 0; p < plans.size(); ++p) {
+    PassPlan& pl = plans[p];
+    const bool last = p + 1 == plans.size();
+    a.K = pl.K;
+    a.P = pl.P;
+    for (int ax = 0; ax < 3; ++ax) {
+      a.lo[ax] = pl.spec.lo[ax];
+      a.hi[ax] = pl.spec.hi[ax];
+    }
+    a.rb = (ReadbackHeader*)(ws + pl.rb);
+    a.leaf_off = (int64_t*)(ws + pl.rb + sizeof(ReadbackHeader));
+    a.lower_off = a.leaf_off + (B + 1);
+    a.upper_off = a.lower_off + (B + 1);
+    a.ctl = (PassCtl*)(ws + pl.ctl);
+    a.slot_cap = pl.slot_cap;
+    a.sort_status = (uint32_t*)(ws + pl.sort_status);
+    a.sort_tiles_cap = pl.sort_tiles;
+    a.dedup_status = (unsigned long long*)(ws + pl.dedup_status);
+    a.write_status = (unsigned long long*)(ws + pl.write_status);
+    a.first = (uint32_t*)(ws + pl.first);
+    a.gbox = (unsigned int*)(ws + pl.gbox);
+
+    const int eb = blocks_for(pl.in_cap, 256, (long long)di->sms * 8);
+    TB_CUDA(launch_emit(pl.spec.op, a, eb, stream));
+    ++t_launches;
+    for (int d = 0; d < pl.P; ++d) {
+      TB_CUDA(launch_sort_pass(a, d, blocks_for(pl.sort_tiles, 1, (long long)di->sms * di->occ_sort), stream));
+      ++t_launches;
+    }
+    a.sorted = pl.P & 1;
+    TB_CUDA(launch_dedup(a, blocks_for(pl.dedup_tiles, 1, (long long)di->sms * di->occ_dedup), stream));
+    ++t_launches;
+    if (last) break;
+    // hand the leaves to the next pass without a readback
+    WriteOut wo;
+    std::memset(&wo, 0, sizeof wo);
+    const int k = (int)(p & 1);
+    wo.origins = (int32_t*)(ws + o_inter[k][0]);
+    wo.masks = (uint64_t*)(ws + o_inter[k][1]);
+    wo.leaf_grid = (int32_t*)(ws + o_inter[k][2]);
+    TB_CUDA(launch_write(pl.spec.op, false, a, wo,
+                         blocks_for(pl.write_tiles, 1, (long long)di->sms * di->occ_write[pl.spec.op][0]), stream));
+    ++t_launches;
+    a.src_origins = wo.origins;
+    a.src_masks = wo.masks;
+    a.src_grid = wo.leaf_grid;
+    a.src_count_dev = &a.rb->num_leaves;
+    a.src_count = 0;
+  }
+
+  // ---- the one count readback of the pass
+  // (plus the error words of the earlier passes of a chain)
+  unsigned int* host_err = (unsigned int*)((char*)host_rb + rb_bytes);
+  for (size_t p = 0; p + 1 < plans.size(); ++p)
+    TB_CUDA(cudaMemcpyAsync(host_err + p, ws + plans[p].rb + offsetof(ReadbackHeader, err), 4,
+                            cudaMemcpyDeviceToHost, stream));
+  TB_CUDA(cudaMemcpyAsync(host_rb, a.rb, rb_bytes, cudaMemcpyDeviceToHost, stream));
+  TB_CUDA(cudaStreamSynchronize(stream));
+  unsigned int err = host_rb->err;
+  for (size_t p = 0; p + 1 < plans.size(); ++p) err |= host_err[p];
+  if (err & kErrTimeout) return fail(TB_ERR_DEVICE_TIMEOUT, "a device-side look-back wait timed out");
+  if (err & kErrSlotOverflow) return fail(TB_ERR_CUDA, "internal: emitted slots exceeded the bound");
+  const int64_t L = (int64_t)host_rb->num_leaves, NL = (int64_t)host_rb->num_lowers,
+                NU = (int64_t)host_rb->num_uppers;
+  const int64_t* hoff = (const int64_t*)(host_rb + 1);
+
+  // ---- outputs
+  tb_batch* b = new tb_batch();
+  b->B = B;
+  b->device = dev;
+  b->L = L;
+  b->NL = NL;
+  b->NU = NU;
+  b->has_alloc = alloc != nullptr;
+  if (alloc) b->alloc = *alloc;
+  b->leaf_offsets_host.assign(hoff, hoff + B + 1);
+  std::memcpy(b->bbox, plans.back().bbox, sizeof b->bbox);
+  if (plans.back().empty || L == 0) {
+    const int32_t e[6] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MIN, INT32_MIN, INT32_MIN};
+    std::memcpy(b->bbox, e, sizeof e);
+  }
+  Carve oc;
+  size_t off[16];
+  off[0] = oc.take((size_t)(B + 1) * 8);
+  off[1] = oc.take((size_t)L * 12);
+  off[2] = oc.take((size_t)L * 64);
+  off[3] = oc.take((size_t)L * 8);
+  off[4] = oc.take((size_t)L * 8);
+  off[5] = oc.take((size_t)L * 24);
+  off[6] = oc.take((size_t)L * 4);
+  off[7] = oc.take((size_t)L * 4);
+  off[8] = oc.take((size_t)B * 8);
+  off[9] = oc.take((size_t)B * 24);
+  off[10] = oc.take((size_t)B * 12);
+  off[11] = oc.take((size_t)(B + 1) * 8);
+  off[12] = oc.take((size_t)(B + 1) * 8);
+  off[13] = oc.take((size_t)NL * 12);
+  off[14] = oc.take((size_t)NL * 4);
+  off[15] = oc.take((size_t)NU * 12);
+  b->mem = mem.get(oc.off);
+  if (!b->mem) {
+    delete b;
+    return fail(TB_ERR_OOM, "output allocation of %zu bytes failed", oc.off);
+  }
+  batch_set_view(b, (char*)b->mem, off);
+  auto nz = [](void* p, int64_t n) { return n > 0 ? p : nullptr; };
+  b->origins = (int32_t*)nz(b->origins, L);
+  b->masks = (uint64_t*)nz(b->masks, L);
+  b->voxel_offset = (int64_t*)nz(b->voxel_offset, L);
+  b->word_prefix = (uint64_t*)nz(b->word_prefix, L);
+  b->leaf_bbox = (int32_t*)nz(b->leaf_bbox, L);
+  b->leaf_grid = (int32_t*)nz(b->leaf_grid, L);
+  b->leaf_parent = (int32_t*)nz(b->leaf_parent, L);
+  b->voxel_counts = (int64_t*)nz(b->voxel_counts, B);
+  b->grid_bbox = (int32_t*)nz(b->grid_bbox, B);
+  b->node_counts = (int32_t*)nz(b->node_counts, B);
+  b->lower_origins = (int32_t*)nz(b->lower_origins, NL);
+  b->lower_parent = (int32_t*)nz(b->lower_parent, NL);
+  b->upper_origins = (int32_t*)nz(b->upper_origins, NU);
+
+  WriteOut wo;
+  wo.origins = b->origins;
+  wo.masks = b->masks;
+  wo.leaf_grid = b->leaf_grid;
+  wo.voxel_offset = b->voxel_offset;
+  wo.word_prefix = b->word_prefix;
+  wo.leaf_bbox = b->leaf_bbox;
+  wo.leaf_parent = b->leaf_parent;
+  wo.voxel_counts = b->voxel_counts;
+  wo.grid_bbox = b->grid_bbox;
+  wo.node_counts = b->node_counts;
+  wo.leaf_offsets = b->leaf_offsets;
+  wo.lower_offsets = b->lower_offsets;
+  wo.upper_offsets = b->upper_offsets;
+  wo.lower_origins = b->lower_origins;
+  wo.lower_parent = b->lower_parent;
+  wo.upper_origins = b->upper_origins;
+  const int wb = blocks_for(L, kWriteTile, (long long)di->sms * di->occ_write[op_last][1]);
+  cudaError_t e = launch_write(op_last, true, a, wo, wb, stream);
+  ++t_launches;
+  if (e != cudaSuccess) {
+    mem.put(b->mem);
+    delete b;
+    return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
+  }
+  *out = b;
+  return TB_OK;
+}
+
+std::vector<PassSpec> expand_ops(const tb_op* ops, int32_t n, tb_status* st) {
+  std::vector<PassSpec> v;
+  *st = TB_OK;
+  for (int32_t i = 0; i < n; ++i) {
+    const tb_op& o = ops[i];
+    PassSpec s;
+    std::memset(&s, 0, sizeof s);
+    if (o.kind == TB_OP_REFINE || o.kind == TB_OP_COARSEN) {
+      int reps = o.factor == 2 ? 1 : o.factor == 4 ? 2 : o.factor == 8 ? 3 : 0;
+      if (!reps) {
+        *st = fail(TB_ERR_INVALID_ARG, "op %d: factor %d is not 2, 4 or 8", i, o.factor);
+        return {};
+      }
+      s.op = o.kind == TB_OP_REFINE ? kRefine : kCoarsen;
+      for (int r = 0; r < reps; ++r) v.push_back(s);
+    } else if (o.kind == TB_OP_BOX_DILATE) {
+      s.op = kDilate;
+      for (int a = 0; a < 3; ++a) {
+        if (o.lo[a] < -1 || o.lo[a] > 0 || o.hi[a] < 0 || o.hi[a] > 1) {
+          *st = fail(TB_ERR_INVALID_ARG, "op %d: box bounds must be lo in {-1,0}, hi in {0,1}", i);
+          return {};
+        }
+        s.lo[a] = o.lo[a];
+        s.hi[a] = o.hi[a];
+      }
+      v.push_back(s);
+    } else {
+      *st = fail(TB_ERR_INVALID_ARG, "op %d: unknown kind %d", i, o.kind);
+      return {};
+    }
+  }
+  return v;
+}
+
+tb_status check_batch(const tb_batch* b) {
+  if (!b) return fail(TB_ERR_INVALID_ARG, "batch is NULL");
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return fail(TB_ERR_CUDA, "cudaGetDevice failed");
+  if (dev != b->device) return fail(TB_ERR_INVALID_ARG, "batch lives on device %d, current device is %d", b->device, dev);
+  return TB_OK;
+}
+
+tb_status run_ops(const tb_batch* in, const std::vector<PassSpec>& specs, const tb_allocator* alloc,
+                  cudaStream_t s, tb_batch** out) {
+  if (out) *out = nullptr;
+  tb_status st = check_batch(in);
+  if (st != TB_OK) return st;
+  Source src;
+  src.kind = kSrcBatch;
+  src.batch = in;
+  src.B = in->B;
+  src.count = in->L;
+  return run(src, specs, alloc, s, out);
+}
+
+}  // namespace
+
+// ================================================================ C ABI
+
+extern "C" {
+
+tb_status tb_from_ijk(const int32_t* ijk, const int64_t* offsets, int32_t num_grids, int64_t num_voxels,
+                      const tb_allocator* alloc, tb_stream stream, tb_batch** out) {
+  if (out) *out = nullptr;
+  if (!out || !offsets || num_grids < 0 || num_voxels < 0 || (num_voxels > 0 && !ijk))
+    return fail(TB_ERR_INVALID_ARG, "tb_from_ijk: bad pointer or negative size");
+  if (num_grids > (1 << 24)) return fail(TB_ERR_TOO_LARGE, "tb_from_ijk: more than 2^24 grids");
+  if (num_voxels >= (1ll << 30)) return fail(TB_ERR_TOO_LARGE, "tb_from_ijk: 2^30 or more voxels");
+  if (num_grids == 0 && num_voxels != 0) return fail(TB_ERR_INVALID_ARG, "tb_from_ijk: voxels without grids");
+  Source src;
+  src.kind = kSrcIjk;
+  src.ijk = ijk;
+  src.offsets = offsets;
+  src.B = num_grids;
+  src.count = num_voxels;
+  PassSpec s;
+  std::memset(&s, 0, sizeof s);
+  s.op = kIjk;
+  return run(src, {s}, alloc, (cudaStream_t)stream, out);
+}
+
+tb_status tb_from_leaves(const int32_t* origins, const uint64_t* masks, const int64_t* leaf_offsets,
+                         int32_t num_grids, int64_t num_leaves, const tb_allocator* alloc, tb_stream stream,
+                         tb_batch** out) {
+  if (out) *out = nullptr;
+  if (!out || !leaf_offsets || num_grids < 0 || num_leaves < 0 || (num_leaves > 0 && (!origins || !masks)))
+    return fail(TB_ERR_INVALID_ARG, "tb_from_leaves: bad pointer or negative size");
+  if (num_grids > (1 << 24)) return fail(TB_ERR_TOO_LARGE, "tb_from_leaves: more than 2^24 grids");
+  if (num_leaves >= (1ll << 27)) return fail(TB_ERR_TOO_LARGE, "tb_from_leaves: 2^27 or more leaves");
+  if (num_grids == 0 && num_leaves != 0) return fail(TB_ERR_INVALID_ARG, "tb_from_leaves: leaves without grids");
+  if (((uintptr_t)masks & 15) != 0) return fail(TB_ERR_INVALID_ARG, "tb_from_leaves: masks must be 16-byte aligned");
+  Source src;
+  src.kind = kSrcLeaves;
+  src.origins = origins;
+  src.masks = masks;
+  src.offsets = leaf_offsets;
+  src.B = num_grids;
+  src.count = num_leaves;
+  PassSpec s;
+  std::memset(&s, 0, sizeof s);
+  s.op = kLeaves;
+  return run(src, {s}, alloc, (cudaStream_t)stream, out);
+}
+
+tb_status tb_refine(const tb_batch* in, int32_t factor, const tb_allocator* alloc, tb_stream stream, tb_batch** out) {
+  tb_op op{TB_OP_REFINE, factor, {0, 0, 0}, {0, 0, 0}};
+  return tb_chain(in, &op, 1, alloc, stream, out);
+}
+
+tb_status tb_coarsen(const tb_batch* in, int32_t factor, const tb_allocator* alloc, tb_stream stream,
+                     tb_batch** out) {
+  tb_op op{TB_OP_COARSEN, factor, {0, 0, 0}, {0, 0, 0}};
+  return tb_chain(in, &op, 1, alloc, stream, out);
+}
+
+tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const int32_t hi[3], const tb_allocator* alloc,
+                        tb_stream stream, tb_batch** out) {
+  if (out) *out = nullptr;
+  if (!lo || !hi) return fail(TB_ERR_INVALID_ARG, "tb_box_dilate: lo/hi NULL");
+  tb_op op{TB_OP_BOX_DILATE, 1, {lo[0], lo[1], lo[2]}, {hi[0], hi[1], hi[2]}};
+  return tb_chain(in, &op, 1, alloc, stream, out);
+}
+
+tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, const tb_allocator* alloc, tb_stream stream,
+                   tb_batch** out) {
+  if (out) *out = nullptr;
+  if (!out) return fail(TB_ERR_INVALID_ARG, "out is NULL");
+  if (n_ops < 0 || (n_ops > 0 && !ops)) return fail(TB_ERR_INVALID_ARG, "tb_chain: bad op list");
+  tb_status st;
+  std::vector<PassSpec> specs = expand_ops(ops, n_ops, &st);
+  if (st != TB_OK) return st;
+  if (specs.empty()) {  // a copy: one identity pass over the leaves
+    PassSpec s;
+    std::memset(&s, 0, sizeof s);
+    s.op = kLeaves;
+    specs.push_back(s);
+  }
+  return run_ops(in, specs, alloc, (cudaStream_t)stream, out);
+}
+
+tb_status tb_validate(const tb_batch* b, tb_stream stream) {
+  tb_status st = check_batch(b);
+  if (st != TB_OK) return st;
+  const Mem mem{b->has_alloc ? &b->alloc : nullptr, (cudaStream_t)stream};
+  unsigned int* err = (unsigned int*)mem.get(4);
+  if (!err) return fail(TB_ERR_OOM, "tb_validate: allocation failed");
+  Guard g{&mem, err};
+  TB_CUDA(cudaMemsetAsync(err, 0, 4, (cudaStream_t)stream));
+  DeviceInfo* di = nullptr;
+  st = device_info(b->device, &di);
+  if (st != TB_OK) return st;
+  const int blocks = blocks_for(std::max<long long>(b->L, b->B + 1), 256, (long long)di->sms * 4);
+  TB_CUDA(launch_validate(b->origins, b->masks, b->leaf_grid, b->leaf_offsets, b->L, b->B, err, blocks,
+                          (cudaStream_t)stream));
+  ++t_launches;
+  unsigned int* h = (unsigned int*)t_pinned.get(64);
+  if (!h) return fail(TB_ERR_OOM, "pinned buffer");
+  TB_CUDA(cudaMemcpyAsync(h, err, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream));
+  TB_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  if (*h) return fail(TB_ERR_NOT_CANONICAL, "batch violates the canonical-order invariants");
+  return TB_OK;
+}
+
+tb_status tb_batch_get_view(const tb_batch* b, tb_batch_view* v) {
+  if (!b || !v) return fail(TB_ERR_INVALID_ARG, "tb_batch_get_view: NULL argument");
+  v->num_grids = b->B;
+  v->device = b->device;
+  v->num_leaves = b->L;
+  v->num_lowers = b->NL;
+  v->num_uppers = b->NU;
+  v->leaf_offsets_host = b->leaf_offsets_host.data();
+  std::memcpy(v->bbox, b->bbox, sizeof v->bbox);
+  v->leaf_offsets = b->leaf_offsets;
+  v->origins = b->origins;
+  v->masks = b->masks;
+  v->voxel_offset = b->voxel_offset;
+  v->word_prefix = b->word_prefix;
+  v->leaf_bbox = b->leaf_bbox;
+  v->leaf_grid = b->leaf_grid;
+  v->leaf_parent = b->leaf_parent;
+  v->voxel_counts = b->voxel_counts;
+  v->grid_bbox = b->grid_bbox;
+  v->node_counts = b->node_counts;
+  v->lower_offsets = b->lower_offsets;
+  v->upper_offsets = b->upper_offsets;
+  v->lower_origins = b->lower_origins;
+  v->lower_parent = b->lower_parent;
+  v->upper_origins = b->upper_origins;
+  return TB_OK;
+}
+
+tb_status tb_batch_export(const tb_batch* b, int32_t* origins, uint64_t* masks, int64_t* voxel_offset,
+                          int64_t* leaf_offsets, tb_stream stream) {
+  if (!b) return fail(TB_ERR_INVALID_ARG, "tb_batch_export: batch is NULL");
+  cudaStream_t s = (cudaStream_t)stream;
+  if (origins && b->L) TB_CUDA(cudaMemcpyAsync(origins, b->origins, (size_t)b->L * 12, cudaMemcpyDefault, s));
+  if (masks && b->L) TB_CUDA(cudaMemcpyAsync(masks, b->masks, (size_t)b->L * 64, cudaMemcpyDefault, s));
+  if (voxel_offset && b->L)
+    TB_CUDA(cudaMemcpyAsync(voxel_offset, b->voxel_offset, (size_t)b->L * 8, cudaMemcpyDefault, s));
+  if (leaf_offsets)
+    TB_CUDA(cudaMemcpyAsync(leaf_offsets, b->leaf_offsets, (size_t)(b->B + 1) * 8, cudaMemcpyDefault, s));
+  return TB_OK;
+}
+
+tb_status tb_batch_free(tb_batch* b, tb_stream stream) {
+  if (!b) return TB_OK;
+  const Mem mem{b->has_alloc ? &b->alloc : nullptr, (cudaStream_t)stream};
+  mem.put(b->mem);
+  delete b;
+  return TB_OK;
+}
+
+const char* tb_last_error(void) { return t_err.c_str(); }
+
+const char* tb_status_string(tb_status s) {
+  switch (s) {
+    case TB_OK: return "TB_OK";
+    case TB_ERR_INVALID_ARG: return "TB_ERR_INVALID_ARG";
+    case TB_ERR_OOM: return "TB_ERR_OOM";
+    case TB_ERR_CUDA: return "TB_ERR_CUDA";
+    case TB_ERR_COORD_OVERFLOW: return "TB_ERR_COORD_OVERFLOW";
+    case TB_ERR_NOT_CANONICAL: return "TB_ERR_NOT_CANONICAL";
+    case TB_ERR_DEVICE_TIMEOUT: return "TB_ERR_DEVICE_TIMEOUT";
+    case TB_ERR_TOO_LARGE: return "TB_ERR_TOO_LARGE";
+  }
+  return "TB_ERR_UNKNOWN";
+}
+
+int32_t tb_version(void) { return 100; }
+
+int64_t tb_kernel_launch_count(void) { return t_launches; }
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+"""C-ABI checks that need no GPU: the library builds for sm_103a, loads, and
+exports every entry point that ``include/tb.h`` declares; host-side argument
+checks answer before any device work."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tb.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"TB_API\s+[\w\s\*]+?\b(tb_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_voxel_grid_leaf_gb300 import _build
+    path = _build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("tb_from_ijk", "tb_from_leaves", "tb_refine", "tb_coarsen", "tb_box_dilate",
+                 "tb_chain", "tb_batch_free", "tb_batch_get_view", "tb_validate", "tb_last_error"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_build_targets_sm103a_only():
+    from sparse_voxel_grid_leaf_gb300 import _build
+    assert _build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_host_side_argument_errors(lib):
+    lib.tb_last_error.restype = ctypes.c_char_p
+    lib.tb_status_string.restype = ctypes.c_char_p
+    lib.tb_version.restype = ctypes.c_int32
+    assert lib.tb_version() >= 100
+    assert lib.tb_status_string(4) == b"TB_ERR_COORD_OVERFLOW"
+    # out == NULL is rejected before any CUDA call
+    st = lib.tb_from_ijk(None, None, ctypes.c_int32(1), ctypes.c_int64(0), None, None, None)
+    assert st == 1
+    assert b"bad pointer" in lib.tb_last_error()
+    out = ctypes.c_void_p(123)
+    st = lib.tb_chain(None, None, ctypes.c_int32(-1), None, None, ctypes.byref(out))
+    assert st == 1 and out.value is None
+    st = lib.tb_batch_get_view(None, None)
+    assert st == 1
+    assert lib.tb_batch_free(None, None) == 0
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import sparse_voxel_grid_leaf_gb300 as tb
+    monkeypatch.setattr(tb, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(tb, "_lib", None)
+    with pytest.raises(tb.TBError):
+        tb.lib()

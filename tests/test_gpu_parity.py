@@ -1,0 +1,250 @@
+"""GPU parity: every output array of the CUDA path equals the oracle's, bit for
+bit, on the same seeded inputs (fVDB PR #757's test plan compares topologies
+element-wise; the result is a unique set in a total order, so any difference
+is a bug).  Calls go through the C ABI via the Python binding."""
+import numpy as np
+import pytest
+
+import oracle
+from sparse_voxel_grid_leaf_gb300 import synth
+from tests import _helpers as H
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():  # pragma: no cover - CPU containers
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import sparse_voxel_grid_leaf_gb300 as tb  # noqa: E402
+
+DIL = ("dilate", (-1, -1, -1), (1, 1, 1))
+PAD_N = ("dilate", (-1, -1, -1), (0, 0, 0))
+PAD_P = ("dilate", (0, 0, 0), (1, 1, 1))
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+def assert_same(got, exp, where=""):
+    for k in tb.ARRAY_NAMES:
+        g, e = got[k], exp[k]
+        assert g.shape == e.shape, "%s %s shape %s vs %s" % (where, k, g.shape, e.shape)
+        if not np.array_equal(g, e):
+            bad = np.argwhere(g != e)[:5]
+            raise AssertionError("%s %s differs at %s: got %s expected %s"
+                                 % (where, k, bad.tolist(), g[tuple(bad[0])], e[tuple(bad[0])]))
+
+
+def gpu_chain(ijk, off, ops):
+    b = tb.from_ijk(dev(ijk), dev(off))
+    if ops:
+        b = tb.chain(b, ops)
+    return b
+
+
+def check(ijk, off, ops, where=""):
+    b = gpu_chain(ijk, off, ops)
+    got = b.to_numpy()
+    exp = oracle.run_voxels(ijk, off, ops)
+    assert_same(got, exp, where)
+    b.validate()
+    return b, got
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+# ------------------------------------------------------------- small exact cases
+
+def test_pr1_from_ijk_then_refine():
+    ijk, off = synth.make("pr1_b2_res32")
+    check(ijk, off, [], "from_ijk")
+    check(ijk, off, [("refine", 2)], "refine")
+
+
+@pytest.mark.parametrize("ops", [
+    [("refine", 2)], [("refine", 4)], [("refine", 8)],
+    [("coarsen", 2)], [("coarsen", 4)], [("coarsen", 8)],
+    [DIL], [PAD_N], [PAD_P], [("dilate", (-1, 0, -1), (0, 1, 1))], [("dilate", (0, -1, 0), (0, 0, 1))],
+    [("refine", 2), PAD_N],                       # k3s2 transpose
+    [("refine", 2), ("coarsen", 2)],               # round trip
+    [("coarsen", 2), DIL, ("refine", 2), PAD_P],
+], ids=lambda ops: "-".join(o[0] + str(o[1] if o[0] != "dilate" else "") for o in ops))
+def test_ops_negative_and_tile_crossing(ops):
+    # members straddle the +-4096 root-tile boundaries in negative octants
+    ijk, off = synth.random_voxels(5, 300, 90, seed=13, origin=(-4140, -45, 4050), empty=(2,))
+    check(ijk, off, ops)
+
+
+def test_duplicates_and_unsorted_ijk():
+    ijk, off = synth.random_voxels(3, 2000, 12, seed=1, origin=(-6, -6, -6))  # many duplicates
+    rng = np.random.default_rng(0)
+    perm = np.concatenate([off[g] + rng.permutation(off[g + 1] - off[g]) for g in range(3)])
+    check(ijk[perm], off, [])
+
+
+@pytest.mark.parametrize("empty", [(0,), (3,), (6,), tuple(range(7))])
+def test_empty_members(empty):
+    ijk, off = synth.random_voxels(7, 120, 40, seed=3, origin=(-20, 0, -20), empty=empty)
+    for ops in ([], [("refine", 2)], [("coarsen", 2)], [DIL], [("refine", 2), PAD_N]):
+        check(ijk, off, ops, "empty=%s ops=%s" % (empty, ops))
+
+
+def test_zero_grids_and_zero_voxels():
+    b = tb.from_ijk(dev(np.zeros((0, 3), np.int32)), dev(np.zeros(1, np.int64)))
+    assert b.num_grids == 0 and b.num_leaves == 0
+    r = tb.refine(b)
+    assert r.num_leaves == 0 and r.leaf_offsets_host.tolist() == [0]
+    b = tb.from_ijk(dev(np.zeros((0, 3), np.int32)), dev(np.zeros(4, np.int64)))
+    got = tb.box_dilate(b).to_numpy()
+    assert_same(got, oracle.run_voxels(np.zeros((0, 3), np.int32), np.zeros(4, np.int64), [DIL]))
+
+
+def test_single_voxel_extremes():
+    # coordinates at the int32 limits that each op can still represent
+    for p, ops_list in (([2 ** 30 - 1, -2 ** 30, 0], ([], [("refine", 2)], [("coarsen", 8)], [DIL])),
+                        ([-1, -1, -1], ([], [("refine", 8)], [("coarsen", 2)], [DIL])),
+                        ([2 ** 31 - 2, -2 ** 31 + 1, 4095], ([], [("coarsen", 4)], [DIL], [PAD_N]))):
+        for ops in ops_list:
+            check(np.array([p], np.int32), np.array([0, 1]), ops, "%s %s" % (p, ops))
+
+
+def test_key_wider_than_64_bits_is_reported():
+    # one grid spanning most of the int32 range on two axes needs a >64-bit key
+    pts = np.array([[-2 ** 31, -2 ** 31, -2 ** 31], [2 ** 31 - 1, 2 ** 31 - 1, 2 ** 31 - 1]], np.int32)
+    with pytest.raises(tb.TBError) as e:
+        tb.from_ijk(dev(pts), dev(np.array([0, 2])))
+    assert e.value.status == 7
+
+
+def test_from_leaves_merges_and_sorts():
+    ijk, off = synth.random_voxels(4, 400, 30, seed=8, origin=(-15, 7, -4100))
+    exp = oracle.run_voxels(ijk, off)
+    # shuffle the leaves, split each into two half masks, add an all-zero leaf
+    o, m, lo = exp["origins"], exp["masks"], exp["leaf_offsets"]
+    rng = np.random.default_rng(1)
+    origins, masks, offs = [], [], [0]
+    for g in range(4):
+        idx = rng.permutation(np.arange(lo[g], lo[g + 1]))
+        for i in idx:
+            half = m[i] & np.uint64(0x5555555555555555)
+            origins += [o[i], o[i]]
+            masks += [half, m[i] ^ half]
+        origins.append(np.array([8, 8, 8], np.int32))
+        masks.append(np.zeros(8, np.uint64))
+        offs.append(len(origins))
+    origins = np.array(origins, np.int32)
+    masks = np.array(masks, np.uint64)
+    offs = np.array(offs, np.int64)
+    b = tb.from_leaves(dev(origins), dev(masks.view(np.int64)), dev(offs))
+    assert_same(b.to_numpy(), exp, "from_leaves")
+
+
+def test_host_inputs_match_device_inputs():
+    ijk, off = synth.make("pr1_b2_res32")
+    a = tb.from_ijk(ijk, off).to_numpy()          # numpy: staged by the library
+    b = tb.from_ijk(dev(ijk), dev(off)).to_numpy()
+    assert_same(a, b, "host vs device")
+
+
+def test_errors_leave_the_device_usable():
+    with pytest.raises(tb.TBError) as e:
+        tb.refine(tb.from_ijk(dev(np.array([[2 ** 30, 0, 0]], np.int32)), dev(np.array([0, 1]))))
+    assert e.value.status == 4
+    with pytest.raises(tb.TBError) as e:
+        tb.from_ijk(dev(np.zeros((3, 3), np.int32)), dev(np.array([0, 2, 1, 3])))
+    assert e.value.status == 1
+    with pytest.raises(tb.TBError) as e:
+        tb.refine(tb.from_ijk(dev(np.zeros((1, 3), np.int32)), dev(np.array([0, 1]))), 3)
+    assert e.value.status == 1
+    with pytest.raises(tb.TBError) as e:
+        tb.from_leaves(dev(np.array([[4, 0, 0]], np.int32)), dev(np.ones((1, 8), np.int64)), dev(np.array([0, 1])))
+    assert e.value.status == 1
+    check(*synth.make("pr1_b2_res32"), [("refine", 2)], "after errors")
+
+
+def test_deterministic_repeat():
+    ijk, off = synth.make("shells_b16_res64")
+    b = tb.from_ijk(dev(ijk), dev(off))
+    first = tb.box_dilate(b).to_numpy()
+    for _ in range(3):
+        assert_same(tb.box_dilate(b).to_numpy(), first, "repeat")
+
+
+def test_launches_are_counted():
+    n0 = tb.kernel_launch_count()
+    ijk, off = synth.make("pr1_b2_res32")
+    tb.refine(tb.from_ijk(dev(ijk), dev(off)))
+    assert tb.kernel_launch_count() - n0 >= 8
+
+
+# ---------------------------------------------------------- workload-sized cases
+
+@pytest.mark.parametrize("ops", [[("coarsen", 2)], [("refine", 2)], [DIL], [PAD_N], [PAD_P],
+                                 [("refine", 2), PAD_N]])
+def test_shells_b16(ops):
+    ijk, off = synth.make("shells_b16_res64")
+    check(ijk, off, ops, "b16 %s" % (ops,))
+
+
+@pytest.mark.parametrize("ops", [[("refine", 2)], [("coarsen", 2)], [DIL], [PAD_N]])
+def test_shells_b48(ops):
+    ijk, off = synth.make("shells_b48_res64")
+    check(ijk, off, ops, "b48 %s" % (ops,))
+
+
+def test_pyramid_b48_schedule():
+    """4-level pyramid: coarsen x2/x4/x8 from the finest grid, then refine back
+    with a k3s1 dilation at each level (11 passes in 8 calls)."""
+    ijk, off = synth.make("pyramid_b48_res64")
+    L0 = tb.from_ijk(dev(ijk), dev(off))
+    e1, e2, e3 = tb.coarsen(L0, 2), tb.coarsen(L0, 4), tb.coarsen(L0, 8)
+    u2 = tb.refine(e3, 2)
+    d2 = tb.box_dilate(u2)
+    u1 = tb.refine(d2, 2)
+    d1 = tb.box_dilate(u1)
+    u0 = tb.refine(d1, 2)
+    sched = {"e1": (e1, [("coarsen", 2)]), "e2": (e2, [("coarsen", 4)]), "e3": (e3, [("coarsen", 8)]),
+             "u2": (u2, [("coarsen", 8), ("refine", 2)]),
+             "d2": (d2, [("coarsen", 8), ("refine", 2), DIL]),
+             "u1": (u1, [("coarsen", 8), ("refine", 2), DIL, ("refine", 2)]),
+             "d1": (d1, [("coarsen", 8), ("refine", 2), DIL, ("refine", 2), DIL]),
+             "u0": (u0, [("coarsen", 8), ("refine", 2), DIL, ("refine", 2), DIL, ("refine", 2)])}
+    for name, (b, ops) in sched.items():
+        assert_same(b.to_numpy(), oracle.run_voxels(ijk, off, ops), name)
+
+
+STRESS_SAMPLE = [0, 1, 6, 9, 14, 31, 46, 63]   # shells and blobs, all eight octants
+
+
+@pytest.fixture(scope="module")
+def stress():
+    ijk, off = synth.make("stress_b64_res512")
+    return ijk, off, tb.from_ijk(dev(ijk), dev(off))
+
+
+@pytest.mark.parametrize("ops", [[], [("refine", 2)], [("coarsen", 4)], [DIL]])
+def test_stress_full_size_sampled_members(stress, ops):
+    """Full B=64 res-512 batch on the GPU; the oracle runs sampled members alone
+    (members are independent), compared array by array."""
+    ijk, off, b0 = stress
+    b = tb.chain(b0, ops) if ops else b0
+    got = b.to_numpy()
+    b.validate()
+    for g in STRESS_SAMPLE:
+        sub_ijk = ijk[off[g]:off[g + 1]]
+        exp = oracle.run_voxels(sub_ijk, np.array([0, len(sub_ijk)]), ops)
+        assert_same(oracle.member(got, g), exp, "member %d" % g)
+    # whole-batch properties that hold at any size
+    if ops == [("refine", 2)]:
+        assert np.array_equal(got["voxel_counts"], 8 * b0.to_numpy(["voxel_counts"])["voxel_counts"])
+
+
+def test_stress_round_trip_full_size(stress):
+    ijk, off, b0 = stress
+    back = tb.chain(b0, [("refine", 2), ("coarsen", 2)]).to_numpy()
+    assert_same(back, b0.to_numpy(), "refine->coarsen")
