@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Benchmark of the batched generated-topology pass (one JSON line on stdout).
+
+Workload (default): B=16 one-voxel-thick ellipsoid shells at resolution 64
+(semi-axes U[0.30,0.48]*64, seed 0) -- the synthetic shell batches fVDB PR
+#757 times its conv-grid builders on ("Measurements": ~7.8k voxels per
+member, resolution 64, median of 20 CUDA-event iterations).
+
+One step runs every pass of the hot path once over the batch, each through
+the library's C ABI:
+  from_ijk (ijk front end), refine x2 (conv_transpose_grid k2s2),
+  coarsen x2 (conv_grid k2s2), dilate [-1,1]^3 (conv_grid k3s1), the two pad
+  octants {-1,0}^3 and {0,1}^3, the k3s2 transpose chain (refine x2 then the
+  {-1,0}^3 pad), and coarsen x4 (a two-pass chain)  -- 10 passes, 8 calls.
+value = output voxels of all passes of a step / device time of the step.
+
+Legs: device-resident inputs (value); end to end from pinned host memory with
+the results read back (e2e); a repetition with per-kernel CUDA events for the
+roofline of the dominant kernel; the CPU oracle on a bounded sample
+(cpu_baseline).  ``--impl reference`` times the oracle alone (the reference
+arm of this benchmark).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "output voxels/s per batched topology pass (device-timed); % of HBM roofline"
+UNIT = "voxels/s"
+DIL = ("dilate", (-1, -1, -1), (1, 1, 1))
+PAD_N = ("dilate", (-1, -1, -1), (0, 0, 0))
+PAD_P = ("dilate", (0, 0, 0), (1, 1, 1))
+# (label, ops of the call); an empty op list is the from_ijk front end
+STEP = [("from_ijk", []), ("refine2", [("refine", 2)]), ("coarsen2", [("coarsen", 2)]),
+        ("dilate_k3s1", [DIL]), ("pad_neg", [PAD_N]), ("pad_pos", [PAD_P]),
+        ("k3s2", [("refine", 2), PAD_N]), ("coarsen4", [("coarsen", 4)])]
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default="shells_b16_res64")
+    p.add_argument("--no-extra", action="store_true", help="skip the per-op and larger-workload tables")
+    p.add_argument("--cpu-sample-steps", type=int, default=2)
+    return p.parse_args()
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """Samples nvidia-smi every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", "tb_clocks_%d_%d.csv" % (os.getpid(), index))
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return None
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        except Exception:
+            return None
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def kernel_traffic(name):
+    """DRAM bytes per launch of `name` from the committed ncu summary, if the
+    kernel sources are unchanged since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    if d.get("source_hash") != source_hash():
+        return None
+    k = d.get("kernels", {}).get(name)
+    return None if k is None else k.get("dram_bytes_per_launch")
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_voxel_grid_leaf_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_step(ijk, off, threads):
+    """One step of the oracle, members spread over `threads` threads.
+    Returns output voxels of the step's passes."""
+    import concurrent.futures as cf
+    import numpy as np
+    import oracle
+    B = len(off) - 1
+    members = [(ijk[off[g]:off[g + 1]], np.array([0, off[g + 1] - off[g]], np.int64)) for g in range(B)]
+    total = 0
+
+    def one(args):
+        sub, o, ops = args
+        return int(oracle.run_voxels(sub, o, ops)["voxel_counts"].sum())
+
+    jobs = []
+    for _, ops in STEP:
+        for sub, o in members:
+            jobs.append((sub, o, ops))
+            if len(ops) == 2:  # a chain: its first pass's output voxels count too
+                jobs.append((sub, o, ops[:1]))
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        for v in ex.map(one, jobs):
+            total += v
+    return total
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    from sparse_voxel_grid_leaf_gb300 import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    ijk, off = synth.make(args.workload)
+    threads = cpu_threads()
+    for _ in range(args.warmup):
+        oracle_step(ijk, off, threads)
+    t0 = time.perf_counter()
+    vox = 0
+    for _ in range(args.steps):
+        vox += oracle_step(ijk, off, threads)
+    dt = time.perf_counter() - t0
+    value = vox / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+            "data": "synthetic", "config": {"workload": args.workload, "step": [s for s, _ in STEP]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "%d full steps, members over %d threads" % (args.steps, threads)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_step(tb, b_src, inputs):
+    """Runs the step's calls; returns (batches, outputs by label)."""
+    out = {}
+    b0 = tb.from_ijk(*inputs)
+    out["from_ijk"] = b0
+    for label, ops in STEP[1:]:
+        out[label] = tb.chain(b0, ops)
+    return out
+
+
+def step_voxels(outs):
+    """Output voxels of every pass of a step (chains count their first pass too)."""
+    v = {k: int(b.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for k, b in outs.items()}
+    total = sum(v.values()) + v["refine2"] + v["coarsen2"]  # first passes of k3s2 and coarsen4
+    return total, v
+
+
+def free_all(outs):
+    for b in outs.values():
+        b.free()
+
+
+def pass_stats(outs):
+    """Per pass (L_in, S, L_out, P, NL, NU, kind) for the byte model."""
+    b0 = outs["from_ijk"]
+    ps = []
+
+    def add(kind, L_in, b):
+        ps.append({"kind": kind, "L_in": L_in, "S": b.build_slots, "L_out": b.num_leaves,
+                   "P": b.build_digit_passes, "NL": b.num_lowers, "NU": b.num_uppers, "B": b.num_grids})
+    add("ijk", b0.build_source_leaves, b0)
+    add("refine", b0.num_leaves, outs["refine2"])
+    add("coarsen", b0.num_leaves, outs["coarsen2"])
+    add("dilate", b0.num_leaves, outs["dilate_k3s1"])
+    add("dilate", b0.num_leaves, outs["pad_neg"])
+    add("dilate", b0.num_leaves, outs["pad_pos"])
+    # chains: the intermediate pass equals the single-op call on the same input
+    r = dict(ps[1])
+    r["inter"] = True
+    ps.append(r)
+    add("dilate", outs["refine2"].num_leaves, outs["k3s2"])
+    c = dict(ps[2])
+    c["inter"] = True
+    ps.append(c)
+    add("coarsen", outs["coarsen2"].num_leaves, outs["coarsen4"])
+    return ps
+
+
+def kernel_bytes(ps):
+    """Algorithmic DRAM bytes per kernel kind over one step (each record read or
+    written once; per-grid arrays ignored)."""
+    by = {}
+
+    def acc(name, n):
+        by[name] = by.get(name, 0) + n
+    for p in ps:
+        L_in, S, L_out = p["L_in"], p["S"], p["L_out"]
+        src = 12 * L_in if p["kind"] == "ijk" else 80 * L_in      # voxel ijk, or origin+mask+grid
+        acc("emit_" + ("ijk" if p["kind"] == "ijk" else p["kind"]), src + 12 * S)
+        acc("sort_pass", 24 * S * p["P"])
+        acc("dedup", 8 * S + 12 * L_out)
+        rd = 20 * L_out + 4 * S + (12 * S if p["kind"] == "ijk" else 64 * L_in)
+        if p.get("inter"):
+            acc("write_%s_inter" % p["kind"], rd + 80 * L_out)
+        else:
+            acc("write_" + p["kind"], rd + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])
+    return by
+
+
+def pass_model_bytes(ps):
+    """Whole-pass byte model: 76 B per source leaf, 116 B per output leaf,
+    24 B per slot per digit pass."""
+    return sum(76 * p["L_in"] + 116 * p["L_out"] + 24 * p["S"] * p["P"] for p in ps)
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import sparse_voxel_grid_leaf_gb300 as tb
+    from sparse_voxel_grid_leaf_gb300 import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    tb.lib()
+    stream = torch.cuda.current_stream()
+
+    # weak scaling: every rank builds its own batch of the same shape
+    ijk, off = synth.make(args.workload, seed=rank)
+    ijk_d = torch.from_numpy(ijk).cuda()
+    off_d = torch.from_numpy(off).cuda()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+
+    # ---- warm-up and the step's output size
+    for _ in range(max(args.warmup, 3)):
+        outs = run_step(tb, None, (ijk_d, off_d))
+        free_all(outs)
+    outs = run_step(tb, None, (ijk_d, off_d))
+    voxels, per_label = step_voxels(outs)
+    ps = pass_stats(outs)
+    out_leaves = {k: (b.num_grids, b.num_leaves) for k, b in outs.items()}
+    free_all(outs)
+    torch.cuda.synchronize()
+
+    # ---- timed region: device-resident inputs
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = tb.kernel_launch_count()
+    times = []
+    with Clocks(local) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            outs = run_step(tb, None, (ijk_d, off_d))
+            free_all(outs)
+            e.record(stream)
+            e.synchronize()
+            times.append(s.elapsed_time(e))
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    launches = tb.kernel_launch_count() - launches0
+    total_ms = sum(times)
+    if dist:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+        v = torch.tensor([float(voxels)], device="cuda")
+        dist.all_reduce(v)
+        job_voxels = float(v.item())
+    else:
+        job_voxels = float(voxels)
+    value = job_voxels * args.steps / (total_ms / 1e3)
+    ms_per_step = total_ms / args.steps
+
+    # ---- end to end: pinned host inputs in, leaf records back to pinned host memory
+    ijk_h = torch.from_numpy(ijk).pin_memory()
+    off_h = torch.from_numpy(off).pin_memory()
+    host_out = {k: (torch.empty((L, 3), dtype=torch.int32).pin_memory(),
+                    torch.empty((L, 8), dtype=torch.int64).pin_memory(),
+                    torch.empty((L,), dtype=torch.int64).pin_memory(),
+                    torch.empty((B + 1,), dtype=torch.int64).pin_memory()) for k, (B, L) in out_leaves.items()}
+    d2h = sum(12 * L + 64 * L + 8 * L + 8 * (B + 1) for B, L in out_leaves.values())
+    h2d = ijk_h.numel() * 4 + off_h.numel() * 8
+    e2e_times = []
+    for it in range(args.warmup + args.steps):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        outs = run_step(tb, None, (ijk_h, off_h))
+        for k, b in outs.items():
+            o, m, vo, lo = host_out[k]
+            tb.export_host(b, o, m, vo, lo)
+        e.record(stream)
+        e.synchronize()
+        free_all(outs)
+        if it >= args.warmup:
+            e2e_times.append(s.elapsed_time(e))
+    e2e_ms = sum(e2e_times)
+    if dist:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = job_voxels * len(e2e_times) / (e2e_ms / 1e3)
+
+    # ---- roofline of the dominant kernel (instrumented repetition)
+    peak, peak_kind = measured_peaks()
+    reps = max(3, min(args.steps, 10))
+    tb.profile_read()
+    tb.profile_enable(True)
+    for _ in range(reps):
+        flush.zero_()
+        outs = run_step(tb, None, (ijk_d, off_d))
+        free_all(outs)
+    torch.cuda.synchronize()
+    prof = tb.profile_read()
+    tb.profile_enable(False)
+    kb = kernel_bytes(ps)
+    tot_kernel_ms = sum(ms for _, ms in prof.values())
+    dom = max(prof, key=lambda k: prof[k][1])
+    n_launch, dom_ms = prof[dom]
+    bytes_step = kb.get(dom, 0)
+    achieved = bytes_step * reps / (dom_ms / 1e3) / 1e9
+    traffic = kernel_traffic(dom)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": dom,
+                "bytes_per_launch": bytes_step * reps / n_launch, "us_per_launch": 1e3 * dom_ms / n_launch,
+                "share_of_kernel_time": dom_ms / tot_kernel_ms, "peak_source": peak_kind + " hbm_gbs (copy)"}
+    kernels = {k: {"launches_per_step": n / reps, "us_per_launch": 1e3 * ms / n,
+                   "share": ms / tot_kernel_ms,
+                   "GBps": (kb.get(k, 0) * reps / (ms / 1e3) / 1e9) if kb.get(k) else None}
+               for k, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1])}
+    model = pass_model_bytes(ps)
+
+    # ---- CPU oracle on a bounded sample (rank 0, one GPU only)
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_sample_steps > 0:
+        threads = cpu_threads()
+        t0 = time.perf_counter()
+        cv = 0
+        for _ in range(args.cpu_sample_steps):
+            cv += oracle_step(ijk, off, threads)
+        dt = time.perf_counter() - t0
+        cpu = {"value": cv / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": "%d full steps of the same workload (all passes, all members), members over %d threads"
+                         % (args.cpu_sample_steps, threads)}
+
+    # ---- per-op and larger-workload tables (median of 20 after 5 warm-ups)
+    extra = {}
+    if not args.no_extra and rank == 0:
+        extra = per_op_tables(tb, torch, synth, stream, flush, args.workload)
+
+    if rank != 0:
+        return
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": args.workload, "B": len(off) - 1, "input_voxels": int(len(ijk)),
+                       "step": [s for s, _ in STEP], "passes_per_step": len(ps),
+                       "output_voxels_per_step": voxels, "output_voxels_by_call": per_label,
+                       "l2": "flushed before every step (256 MB write, untimed)", "inputs": "device-resident"},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms / len(e2e_times)},
+            "roofline": roofline,
+            "pass_model": {"bytes_per_step": model, "GBps": model / (ms_per_step / 1e3) / 1e9,
+                           "frac": model / (ms_per_step / 1e3) / 1e9 / peak},
+            "kernels": kernels, "gpu_launches": launches, "cpu_baseline": cpu,
+            "clocks": clk.summary(), "per_op": extra}
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def per_op_tables(tb, torch, synth, stream, flush, main_workload):
+    """ms per call (median of 20 CUDA-event iterations after 5 warm-ups, L2
+    flushed before each) for each single pass on three workloads."""
+    res = {}
+    ops = [("refine2", [("refine", 2)]), ("coarsen2", [("coarsen", 2)]), ("dilate_k3s1", [DIL]),
+           ("pad_neg", [PAD_N]), ("k3s2", [("refine", 2), PAD_N])]
+    for wl in (main_workload, "shells_b48_res64", "stress_b64_res512"):
+        ijk, off = synth.make(wl)
+        ijk_d, off_d = torch.from_numpy(ijk).cuda(), torch.from_numpy(off).cuda()
+        b0 = tb.from_ijk(ijk_d, off_d)
+        row = {}
+        calls = [("from_ijk", lambda: tb.from_ijk(ijk_d, off_d))] + \
+                [(lab, (lambda o=o: tb.chain(b0, o))) for lab, o in ops]
+        for lab, fn in calls:
+            ts = []
+            vox = 0
+            for it in range(25):
+                flush.zero_()
+                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                s.record(stream)
+                r = fn()
+                e.record(stream)
+                e.synchronize()
+                if it == 0:
+                    vox = int(r.to_numpy(["voxel_counts"])["voxel_counts"].sum())
+                r.free()
+                if it >= 5:
+                    ts.append(s.elapsed_time(e))
+            med = statistics.median(ts)
+            row[lab] = {"ms": med, "out_voxels": vox, "Gvox_per_s": vox / med / 1e6}
+        res[wl] = row
+        b0.free()
+    return res
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -121,7 +121,19 @@ typedef struct tb_batch_view {
   const int32_t* lower_origins;      /* [NL,3] lower-node origins (multiples of 128) */
   const int32_t* lower_parent;       /* [NL] index of the upper node within the grid */
   const int32_t* upper_origins;      /* [NU,3] upper-node origins (multiples of 4096) */
+  /* statistics of the pass that produced the batch */
+  int64_t build_slots;               /* candidate leaves emitted and sorted       */
+  int64_t build_source_leaves;       /* leaves (or voxels) the pass read          */
+  int32_t build_key_bits;            /* width of the compressed sort key          */
+  int32_t build_digit_passes;        /* 8-bit radix passes run                    */
 } tb_batch_view;
+
+/* Per-kernel timing record (see tb_profile_enable). */
+typedef struct tb_kernel_stat {
+  const char* name;     /* static kernel name                                   */
+  int64_t launches;
+  double total_ms;      /* sum of CUDA-event durations on the launching stream  */
+} tb_kernel_stat;
 
 /* Batch from a jagged list of voxel coordinates: the ijk front end that fVDB
  * PR #757 (Follow-ups paragraph) names for BuildGridFromIjk.
@@ -197,6 +209,15 @@ TB_API const char* tb_status_string(tb_status status);
 
 /* Library version: major * 10000 + minor * 100 + patch. */
 TB_API int32_t tb_version(void);
+
+/* Kernel timing for profiling (library extension, no counterpart on the
+ * pages).  While enabled on the calling thread, every kernel the library
+ * launches is bracketed by two CUDA events on its stream.  tb_profile_read
+ * waits for the recorded events, writes up to `max` per-kernel records
+ * (aggregated by kernel name) and clears them; it returns the number of
+ * distinct kernels recorded (which may exceed `max`). */
+TB_API tb_status tb_profile_enable(int32_t on);
+TB_API int32_t tb_profile_read(tb_kernel_stat* stats, int32_t max);
 
 /* Number of kernels this thread has launched through the library so far. */
 TB_API int64_t tb_kernel_launch_count(void);

@@ -56,7 +56,13 @@ class _View(ctypes.Structure):
                [(n, ctypes.c_void_p) for n in (
                    "leaf_offsets", "origins", "masks", "voxel_offset", "word_prefix", "leaf_bbox",
                    "leaf_grid", "leaf_parent", "voxel_counts", "grid_bbox", "node_counts",
-                   "lower_offsets", "upper_offsets", "lower_origins", "lower_parent", "upper_origins")]
+                   "lower_offsets", "upper_offsets", "lower_origins", "lower_parent", "upper_origins")] + \
+               [("build_slots", ctypes.c_int64), ("build_source_leaves", ctypes.c_int64),
+                ("build_key_bits", ctypes.c_int32), ("build_digit_passes", ctypes.c_int32)]
+
+
+class _KStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", ctypes.c_int64), ("total_ms", ctypes.c_double)]
 
 
 _lib = None
@@ -94,6 +100,10 @@ def lib():
             L.tb_last_error.argtypes = []
             L.tb_version.restype = ctypes.c_int32
             L.tb_kernel_launch_count.restype = ctypes.c_int64
+            L.tb_profile_enable.argtypes = [ctypes.c_int32]
+            L.tb_profile_enable.restype = ctypes.c_int
+            L.tb_profile_read.argtypes = [ctypes.POINTER(_KStat), ctypes.c_int32]
+            L.tb_profile_read.restype = ctypes.c_int32
             _lib = L
         return _lib
 
@@ -113,6 +123,18 @@ def _stream(stream=None) -> int:
 def kernel_launch_count() -> int:
     """Kernels launched through the library by the calling thread so far."""
     return int(lib().tb_kernel_launch_count())
+
+
+def profile_enable(on: bool = True):
+    """Times every library kernel of this thread with CUDA events on its stream."""
+    lib().tb_profile_enable(1 if on else 0)
+
+
+def profile_read() -> Dict[str, Tuple[int, float]]:
+    """{kernel name: (launches, total ms)} since the last read; waits for the events."""
+    arr = (_KStat * 64)()
+    n = lib().tb_profile_read(arr, 64)
+    return {arr[i].name.decode(): (int(arr[i].launches), float(arr[i].total_ms)) for i in range(min(n, 64))}
 
 
 class _CAI:
@@ -160,6 +182,10 @@ class Batch:
         self.num_uppers = int(v.num_uppers)
         self.device = int(v.device)
         self.bbox = tuple(int(x) for x in v.bbox)
+        self.build_slots = int(v.build_slots)
+        self.build_source_leaves = int(v.build_source_leaves)
+        self.build_key_bits = int(v.build_key_bits)
+        self.build_digit_passes = int(v.build_digit_passes)
         n = self.num_grids + 1
         self.leaf_offsets_host = np.ctypeslib.as_array(
             ctypes.cast(v.leaf_offsets_host, ctypes.POINTER(ctypes.c_int64)), shape=(n,)).copy()

@@ -29,6 +29,8 @@
 using namespace tb;
 
 struct tb_batch {
+  int64_t build_slots = 0, build_sources = 0;
+  int32_t build_key_bits = 0, build_digit_passes = 0;
   int32_t B = 0;
   int device = 0;
   int64_t L = 0, NL = 0, NU = 0;
@@ -59,6 +61,53 @@ namespace {
 
 thread_local std::string t_err;
 thread_local long long t_launches = 0;
+
+// ---------------------------------------------------------------- kernel timing
+
+enum KernelKind {
+  kKPrepassIjk, kKPrepassLeaves, kKEmit0, kKSort = kKEmit0 + 5, kKDedup, kKWriteInter0,
+  kKWriteFinal0 = kKWriteInter0 + 5, kKValidate = kKWriteFinal0 + 5, kKNumKinds
+};
+const char* const kKernelNames[kKNumKinds] = {
+    "prepass_ijk", "prepass_leaves", "emit_ijk", "emit_leaves", "emit_refine", "emit_coarsen", "emit_dilate",
+    "sort_pass", "dedup", "write_ijk_inter", "write_leaves_inter", "write_refine_inter", "write_coarsen_inter",
+    "write_dilate_inter", "write_ijk", "write_leaves", "write_refine", "write_coarsen", "write_dilate",
+    "validate"};
+
+struct ProfRec {
+  int kind;
+  cudaEvent_t a, b;
+};
+thread_local bool t_prof = false;
+thread_local std::vector<ProfRec> t_recs;
+thread_local std::vector<cudaEvent_t> t_events;
+
+cudaEvent_t pooled_event() {
+  if (!t_events.empty()) {
+    cudaEvent_t e = t_events.back();
+    t_events.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return e;
+}
+
+// Launches through `f` (returning cudaError_t); counted, and timed when enabled.
+template <class F>
+cudaError_t launch(int kind, cudaStream_t s, F&& f) {
+  ++t_launches;
+  if (!t_prof) return f();
+  cudaEvent_t a = pooled_event(), b = pooled_event();
+  if (a) cudaEventRecord(a, s);
+  const cudaError_t e = f();
+  if (b) cudaEventRecord(b, s);
+  if (a && b) t_recs.push_back({kind, a, b});
+  return e;
+}
 
 tb_status fail(tb_status st, const char* fmt, ...) {
   char buf[512];
@@ -460,9 +509,13 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   if (front) {
     ReadbackHeader* rb0 = (ReadbackHeader*)(ws + plans[0].rb);
     const int blocks = blocks_for(src.count, 256, (long long)di->sms * 4);
-    if (src.kind == kSrcIjk) TB_CUDA(launch_prepass_ijk(in_ijk, src.count, in_off, B, rb0, blocks, stream));
-    else TB_CUDA(launch_prepass_leaves(in_orig, in_mask, src.count, in_off, B, rb0, blocks, stream));
-    ++t_launches;
+    if (src.kind == kSrcIjk)
+      TB_CUDA(launch(kKPrepassIjk, stream,
+                     [&] { return launch_prepass_ijk(in_ijk, src.count, in_off, B, rb0, blocks, stream); }));
+    else
+      TB_CUDA(launch(kKPrepassLeaves, stream, [&] {
+        return launch_prepass_leaves(in_orig, in_mask, src.count, in_off, B, rb0, blocks, stream);
+      }));
     TB_CUDA(cudaMemcpyAsync(host_rb, rb0, sizeof(ReadbackHeader), cudaMemcpyDeviceToHost, stream));
     TB_CUDA(cudaStreamSynchronize(stream));
     if (host_rb->err & kErrBadOffsets)
@@ -531,15 +584,13 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     a.gbox = (unsigned int*)(ws + pl.gbox);
 
     const int eb = blocks_for(pl.in_cap, 256, (long long)di->sms * 8);
-    TB_CUDA(launch_emit(pl.spec.op, a, eb, stream));
-    ++t_launches;
-    for (int d = 0; d < pl.P; ++d) {
-      TB_CUDA(launch_sort_pass(a, d, blocks_for(pl.sort_tiles, 1, (long long)di->sms * di->occ_sort), stream));
-      ++t_launches;
-    }
+    TB_CUDA(launch(kKEmit0 + pl.spec.op, stream, [&] { return launch_emit(pl.spec.op, a, eb, stream); }));
+    const int sb = blocks_for(pl.sort_tiles, 1, (long long)di->sms * di->occ_sort);
+    for (int d = 0; d < pl.P; ++d)
+      TB_CUDA(launch(kKSort, stream, [&] { return launch_sort_pass(a, d, sb, stream); }));
     a.sorted = pl.P & 1;
-    TB_CUDA(launch_dedup(a, blocks_for(pl.dedup_tiles, 1, (long long)di->sms * di->occ_dedup), stream));
-    ++t_launches;
+    const int db = blocks_for(pl.dedup_tiles, 1, (long long)di->sms * di->occ_dedup);
+    TB_CUDA(launch(kKDedup, stream, [&] { return launch_dedup(a, db, stream); }));
     if (last) break;
     // hand the leaves to the next pass without a readback
     WriteOut wo;
@@ -548,9 +599,8 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     wo.origins = (int32_t*)(ws + o_inter[k][0]);
     wo.masks = (uint64_t*)(ws + o_inter[k][1]);
     wo.leaf_grid = (int32_t*)(ws + o_inter[k][2]);
-    TB_CUDA(launch_write(pl.spec.op, false, a, wo,
-                         blocks_for(pl.write_tiles, 1, (long long)di->sms * di->occ_write[pl.spec.op][0]), stream));
-    ++t_launches;
+    const int wb = blocks_for(pl.write_tiles, 1, (long long)di->sms * di->occ_write[pl.spec.op][0]);
+    TB_CUDA(launch(kKWriteInter0 + pl.spec.op, stream, [&] { return launch_write(pl.spec.op, false, a, wo, wb, stream); }));
     a.src_origins = wo.origins;
     a.src_masks = wo.masks;
     a.src_grid = wo.leaf_grid;
@@ -585,6 +635,10 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   if (alloc) b->alloc = *alloc;
   b->leaf_offsets_host.assign(hoff, hoff + B + 1);
   std::memcpy(b->bbox, plans.back().bbox, sizeof b->bbox);
+  b->build_slots = (int64_t)host_rb->num_slots;
+  b->build_sources = plans.size() == 1 ? (int64_t)plans.back().in_cap : -1;
+  b->build_key_bits = plans.back().K.W;
+  b->build_digit_passes = plans.back().P;
   if (plans.back().empty || L == 0) {
     const int32_t e[6] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MIN, INT32_MIN, INT32_MIN};
     std::memcpy(b->bbox, e, sizeof e);
@@ -646,8 +700,7 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   wo.lower_parent = b->lower_parent;
   wo.upper_origins = b->upper_origins;
   const int wb = blocks_for(L, kWriteTile, (long long)di->sms * di->occ_write[op_last][1]);
-  cudaError_t e = launch_write(op_last, true, a, wo, wb, stream);
-  ++t_launches;
+  cudaError_t e = launch(kKWriteFinal0 + op_last, stream, [&] { return launch_write(op_last, true, a, wo, wb, stream); });
   if (e != cudaSuccess) {
     mem.put(b->mem);
     delete b;
@@ -809,9 +862,10 @@ tb_status tb_validate(const tb_batch* b, tb_stream stream) {
   st = device_info(b->device, &di);
   if (st != TB_OK) return st;
   const int blocks = blocks_for(std::max<long long>(b->L, b->B + 1), 256, (long long)di->sms * 4);
-  TB_CUDA(launch_validate(b->origins, b->masks, b->leaf_grid, b->leaf_offsets, b->L, b->B, err, blocks,
-                          (cudaStream_t)stream));
-  ++t_launches;
+  TB_CUDA(launch(kKValidate, (cudaStream_t)stream, [&] {
+    return launch_validate(b->origins, b->masks, b->leaf_grid, b->leaf_offsets, b->L, b->B, err, blocks,
+                           (cudaStream_t)stream);
+  }));
   unsigned int* h = (unsigned int*)t_pinned.get(64);
   if (!h) return fail(TB_ERR_OOM, "pinned buffer");
   TB_CUDA(cudaMemcpyAsync(h, err, 4, cudaMemcpyDeviceToHost, (cudaStream_t)stream));
@@ -845,6 +899,10 @@ tb_status tb_batch_get_view(const tb_batch* b, tb_batch_view* v) {
   v->lower_origins = b->lower_origins;
   v->lower_parent = b->lower_parent;
   v->upper_origins = b->upper_origins;
+  v->build_slots = b->build_slots;
+  v->build_source_leaves = b->build_sources;
+  v->build_key_bits = b->build_key_bits;
+  v->build_digit_passes = b->build_digit_passes;
   return TB_OK;
 }
 
@@ -888,5 +946,33 @@ const char* tb_status_string(tb_status s) {
 int32_t tb_version(void) { return 100; }
 
 int64_t tb_kernel_launch_count(void) { return t_launches; }
+
+tb_status tb_profile_enable(int32_t on) {
+  t_prof = on != 0;
+  return TB_OK;
+}
+
+int32_t tb_profile_read(tb_kernel_stat* stats, int32_t max) {
+  double ms[kKNumKinds] = {};
+  int64_t n[kKNumKinds] = {};
+  for (const ProfRec& r : t_recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.b) == cudaSuccess && cudaEventElapsedTime(&t, r.a, r.b) == cudaSuccess) {
+      ms[r.kind] += t;
+      n[r.kind] += 1;
+    }
+    cudaGetLastError();
+    t_events.push_back(r.a);
+    t_events.push_back(r.b);
+  }
+  t_recs.clear();
+  int32_t k = 0;
+  for (int i = 0; i < kKNumKinds; ++i) {
+    if (!n[i]) continue;
+    if (stats && k < max) stats[k] = tb_kernel_stat{kKernelNames[i], n[i], ms[i]};
+    ++k;
+  }
+  return k;
+}
 
 }  // extern "C"
