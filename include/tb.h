@@ -210,6 +210,56 @@ TB_API const char* tb_status_string(tb_status status);
 /* Library version: major * 10000 + minor * 100 + patch. */
 TB_API int32_t tb_version(void);
 
+/* Output buffers of tb_refine_static, all device memory owned by the caller.
+ * Per-grid arrays hold num_grids (+1) rows; per-leaf arrays leaf_capacity
+ * rows, lower-node arrays lower_capacity rows, upper_origins upper_capacity
+ * rows.  Shapes and meanings match the arrays of tb_batch_view. */
+typedef struct tb_out_buffers {
+  int64_t leaf_capacity;
+  int64_t lower_capacity;
+  int64_t upper_capacity;
+  int64_t* leaf_offsets;   /* [B+1] */
+  int64_t* lower_offsets;  /* [B+1] */
+  int64_t* upper_offsets;  /* [B+1] */
+  int64_t* voxel_counts;   /* [B]   */
+  int32_t* grid_bbox;      /* [B,6] */
+  int32_t* node_counts;    /* [B,3] */
+  int32_t* origins;        /* [leaf_capacity,3] */
+  uint64_t* masks;         /* [leaf_capacity,8] */
+  int64_t* voxel_offset;   /* [leaf_capacity]   */
+  uint64_t* word_prefix;   /* [leaf_capacity]   */
+  int32_t* leaf_bbox;      /* [leaf_capacity,6] */
+  int32_t* leaf_grid;      /* [leaf_capacity]   */
+  int32_t* leaf_parent;    /* [leaf_capacity]   */
+  int32_t* lower_origins;  /* [lower_capacity,3] */
+  int32_t* lower_parent;   /* [lower_capacity]   */
+  int32_t* upper_origins;  /* [upper_capacity,3] */
+} tb_out_buffers;
+
+/* Refinement by 2 that allocates nothing.  The paper has no counterpart: this
+ * is for callers that cannot call cudaMalloc -- applications that reserve all
+ * device memory in their own arena, or code running where the CUDA allocator
+ * must not be entered (a deadline-bound loop, a callback of the caller's own
+ * allocator).  The result equals tb_refine(batch, 2) on the same leaves.
+ *   origins [num_leaves,3], masks [num_leaves,8] (16-byte aligned),
+ *   leaf_offsets [num_grids+1]: the input leaves in device memory, any order
+ *   (duplicates merge); out: caller-owned output buffers (see tb_out_buffers);
+ *   out_counts: optional host int64[3] receiving the output's leaf, lower-node
+ *   and upper-node totals (also written when the capacity check fails).
+ * Scratch is one static device array of 32 MiB that every GPU loading the
+ * library holds until the process exits; about 40 bytes per candidate leaf
+ * (8 per input leaf) plus per-grid control, so inputs of up to roughly 100k
+ * leaves fit.  Larger inputs, or outputs beyond the given capacities, return
+ * TB_ERR_TOO_LARGE before anything is written.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress); make it before
+ * any stream capture.  Calls share the array and its contents persist: each
+ * call clears its control region first, and calls that overlap on the GPU
+ * race.  Blocks twice (range readback, count readback) into host stack
+ * memory. */
+TB_API tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const int64_t* leaf_offsets,
+                                  int32_t num_grids, int64_t num_leaves, const tb_out_buffers* out,
+                                  int64_t* out_counts, tb_stream stream);
+
 /* Kernel timing for profiling (library extension, no counterpart on the
  * pages).  While enabled on the calling thread, every kernel the library
  * launches is bracketed by two CUDA events on its stream.  tb_profile_read

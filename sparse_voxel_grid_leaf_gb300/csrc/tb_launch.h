@@ -31,6 +31,9 @@ cudaError_t launch_validate(const int32_t* origins, const uint64_t* masks, const
                             const int64_t* leaf_offsets, long long L, int32_t B, unsigned int* err,
                             int blocks, cudaStream_t s);
 
+// Sets the calling thread's tb_last_error() message.
+void set_error_message(const char* msg);
+
 // Occupancy-derived resident block counts (per SM) of the persistent kernels.
 int occupancy_sort();
 int occupancy_dedup();
