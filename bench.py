@@ -256,8 +256,10 @@ def pass_stats(outs):
 
 
 def kernel_bytes(ps):
-    """Algorithmic DRAM bytes per kernel kind over one step (each record read or
-    written once; per-grid arrays ignored)."""
+    """Algorithmic DRAM bytes per kernel over one step (each record read or
+    written once; per-grid arrays ignored).  "chain" is the cooperative kernel
+    of a call: emission, digit passes, dedup and the count or hand-off phase of
+    each of its passes; "write_<op>" is the final writer."""
     by = {}
 
     def acc(name, n):
@@ -265,14 +267,12 @@ def kernel_bytes(ps):
     for p in ps:
         L_in, S, L_out = p["L_in"], p["S"], p["L_out"]
         src = 12 * L_in if p["kind"] == "ijk" else 80 * L_in      # voxel ijk, or origin+mask+grid
-        acc("emit_" + ("ijk" if p["kind"] == "ijk" else p["kind"]), src + 12 * S)
-        acc("sort_pass", 24 * S * p["P"])
-        acc("dedup", 8 * S + 12 * L_out)
-        rd = 20 * L_out + 4 * S + (12 * S if p["kind"] == "ijk" else 64 * L_in)
-        if p.get("inter"):
-            acc("write_%s_inter" % p["kind"], rd + 80 * L_out)
-        else:
-            acc("write_" + p["kind"], rd + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])
+        merge = 20 * L_out + 4 * S + (12 * S if p["kind"] == "ijk" else 64 * L_in)
+        chain = src + 12 * S + 24 * S * p["P"] + 8 * S + 12 * L_out + merge
+        chain += 80 * L_out if p.get("inter") else 8 * L_out
+        acc("chain", chain)
+        if not p.get("inter"):
+            acc("write_" + p["kind"], merge + 16 * L_out + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])
     return by
 
 

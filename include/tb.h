@@ -247,8 +247,8 @@ typedef struct tb_out_buffers {
  *   out_counts: optional host int64[3] receiving the output's leaf, lower-node
  *   and upper-node totals (also written when the capacity check fails).
  * Scratch is one static device array of 32 MiB that every GPU loading the
- * library holds until the process exits; about 40 bytes per candidate leaf
- * (8 per input leaf) plus per-grid control, so inputs of up to roughly 100k
+ * library holds until the process exits; about 44 bytes per candidate leaf
+ * (8 per input leaf) plus per-grid control, so inputs of up to roughly 90k
  * leaves fit.  Larger inputs, or outputs beyond the given capacities, return
  * TB_ERR_TOO_LARGE before anything is written.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress); make it before
@@ -261,11 +261,12 @@ TB_API tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks,
                                   int64_t* out_counts, tb_stream stream);
 
 /* Kernel timing for profiling (library extension, no counterpart on the
- * pages).  While enabled on the calling thread, every kernel the library
- * launches is bracketed by two CUDA events on its stream.  tb_profile_read
- * waits for the recorded events, writes up to `max` per-kernel records
- * (aggregated by kernel name) and clears them; it returns the number of
- * distinct kernels recorded (which may exceed `max`). */
+ * pages).  With `on` >= 1 on the calling thread, every kernel the library
+ * launches is bracketed by two CUDA events on its stream; with `on` >= 2 the
+ * pass kernel also stamps the GPU global timer at each of its phase
+ * boundaries (records named "phase_*").  tb_profile_read waits for the
+ * recorded events, writes up to `max` records (aggregated by name) and clears
+ * them; it returns the number of distinct records (which may exceed `max`). */
 TB_API tb_status tb_profile_enable(int32_t on);
 TB_API int32_t tb_profile_read(tb_kernel_stat* stats, int32_t max);
 

@@ -114,10 +114,14 @@ def _check(st: int):
 
 
 def _stream(stream=None) -> int:
+    """Raw cudaStream_t of `stream` (default: torch's current stream)."""
+    if stream is not None:
+        return int(getattr(stream, "cuda_stream", stream) or 0)
     import torch
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return int(getattr(stream, "cuda_stream", stream) or 0)
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return int(raw(torch._C._cuda_getDevice()))
+    return int(torch.cuda.current_stream().cuda_stream)
 
 
 def kernel_launch_count() -> int:
@@ -125,9 +129,10 @@ def kernel_launch_count() -> int:
     return int(lib().tb_kernel_launch_count())
 
 
-def profile_enable(on: bool = True):
-    """Times every library kernel of this thread with CUDA events on its stream."""
-    lib().tb_profile_enable(1 if on else 0)
+def profile_enable(on=True):
+    """Times every library kernel of this thread with CUDA events on its stream
+    (``on`` = 2 also stamps the pass kernel's phase boundaries)."""
+    lib().tb_profile_enable(int(on))
 
 
 def profile_read() -> Dict[str, Tuple[int, float]]:
@@ -169,26 +174,21 @@ ARRAY_NAMES = tuple(_ARRAYS)
 
 
 class Batch:
-    """A batch of grids produced by the library (owns its device memory)."""
+    """A batch of grids produced by the library (owns its device memory).
+
+    Sizes and device arrays are read lazily from the library's view of the
+    batch, so passing batches from one call to the next costs nothing here."""
 
     def __init__(self, handle: int):
         self._h = ctypes.c_void_p(handle)
-        v = _View()
-        _check(lib().tb_batch_get_view(self._h, ctypes.byref(v)))
-        self._v = v
-        self.num_grids = int(v.num_grids)
-        self.num_leaves = int(v.num_leaves)
-        self.num_lowers = int(v.num_lowers)
-        self.num_uppers = int(v.num_uppers)
-        self.device = int(v.device)
-        self.bbox = tuple(int(x) for x in v.bbox)
-        self.build_slots = int(v.build_slots)
-        self.build_source_leaves = int(v.build_source_leaves)
-        self.build_key_bits = int(v.build_key_bits)
-        self.build_digit_passes = int(v.build_digit_passes)
-        n = self.num_grids + 1
-        self.leaf_offsets_host = np.ctypeslib.as_array(
-            ctypes.cast(v.leaf_offsets_host, ctypes.POINTER(ctypes.c_int64)), shape=(n,)).copy()
+        self._v = None
+
+    def _view(self) -> _View:
+        if self._v is None:
+            v = _View()
+            _check(lib().tb_batch_get_view(self.handle, ctypes.byref(v)))
+            self._v = v
+        return self._v
 
     @property
     def handle(self) -> ctypes.c_void_p:
@@ -196,16 +196,35 @@ class Batch:
             raise TBError(1, "batch already freed")
         return self._h
 
+    num_grids = property(lambda self: int(self._view().num_grids))
+    num_leaves = property(lambda self: int(self._view().num_leaves))
+    num_lowers = property(lambda self: int(self._view().num_lowers))
+    num_uppers = property(lambda self: int(self._view().num_uppers))
+    device = property(lambda self: int(self._view().device))
+    bbox = property(lambda self: tuple(int(x) for x in self._view().bbox))
+    build_slots = property(lambda self: int(self._view().build_slots))
+    build_source_leaves = property(lambda self: int(self._view().build_source_leaves))
+    build_key_bits = property(lambda self: int(self._view().build_key_bits))
+    build_digit_passes = property(lambda self: int(self._view().build_digit_passes))
+
+    @property
+    def leaf_offsets_host(self) -> np.ndarray:
+        v = self._view()
+        return np.ctypeslib.as_array(ctypes.cast(v.leaf_offsets_host, ctypes.POINTER(ctypes.c_int64)),
+                                     shape=(v.num_grids + 1,)).copy()
+
     def tensor(self, name: str):
         """Zero-copy torch CUDA tensor of one device array of the batch (64-bit
-    masks and word prefixes are exposed as int64 bit patterns)."""
+        masks and word prefixes are exposed as int64 bit patterns)."""
         import torch
         typestr, npdt, shp = _ARRAYS[name]
-        shape = shp(self.num_grids, self.num_leaves, self.num_lowers, self.num_uppers)
-        ptr = getattr(self._v, name)
+        v = self._view()
+        shape = shp(v.num_grids, v.num_leaves, v.num_lowers, v.num_uppers)
+        ptr = getattr(v, name)
+        dev = "cuda:%d" % v.device
         if not ptr or int(np.prod(shape)) == 0:
-            return torch.empty(shape, dtype=_torch_dtype(npdt), device="cuda:%d" % self.device)
-        return torch.as_tensor(_CAI(self, ptr, shape, typestr), device="cuda:%d" % self.device)
+            return torch.empty(shape, dtype=_torch_dtype(npdt), device=dev)
+        return torch.as_tensor(_CAI(self, ptr, shape, typestr), device=dev)
 
     def __getattr__(self, name):
         if name in _ARRAYS:
@@ -230,6 +249,7 @@ class Batch:
         if self._h is not None:
             lib().tb_batch_free(self._h, ctypes.c_void_p(_stream(stream)))
             self._h = None
+            self._v = None
 
     def __del__(self):
         try:
@@ -310,9 +330,15 @@ def box_dilate(b: Batch, lo=(-1, -1, -1), hi=(1, 1, 1), stream=None) -> Batch:
     return _new(lib().tb_box_dilate, b.handle, lo_a, hi_a, None, ctypes.c_void_p(_stream(stream)))
 
 
+_OPS_CACHE: Dict[Tuple, Tuple] = {}
+
+
 def make_ops(ops: Iterable[Tuple]):
     """Op tuples ``("refine", f)``, ``("coarsen", f)``, ``("dilate", lo, hi)`` -> C array."""
-    ops = list(ops)
+    ops = tuple((o[0],) + tuple(tuple(x) if isinstance(x, (list, tuple)) else x for x in o[1:]) for o in ops)
+    hit = _OPS_CACHE.get(ops)
+    if hit is not None:
+        return hit
     arr = (_Op * max(1, len(ops)))()
     for i, op in enumerate(ops):
         if op[0] == "refine":
@@ -325,6 +351,8 @@ def make_ops(ops: Iterable[Tuple]):
                 arr[i].lo[a], arr[i].hi[a] = int(op[1][a]), int(op[2][a])
         else:
             raise TBError(1, "unknown op %r" % (op[0],))
+    if len(_OPS_CACHE) < 1024:
+        _OPS_CACHE[ops] = (arr, len(ops))
     return arr, len(ops)
 
 

@@ -15,6 +15,7 @@
 // [floor(lo/2), floor(hi/2)], a box dilation to [lo + d_lo, hi + d_hi], and
 // the front ends read it back from a small prepass.
 #include <algorithm>
+#include <chrono>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -65,21 +66,26 @@ thread_local long long t_launches = 0;
 
 // ---------------------------------------------------------------- kernel timing
 
-enum KernelKind {
-  kKPrepassIjk, kKPrepassLeaves, kKEmit0, kKSort = kKEmit0 + 5, kKDedup, kKWriteInter0,
-  kKWriteFinal0 = kKWriteInter0 + 5, kKValidate = kKWriteFinal0 + 5, kKNumKinds
-};
-const char* const kKernelNames[kKNumKinds] = {
-    "prepass_ijk", "prepass_leaves", "emit_ijk", "emit_leaves", "emit_refine", "emit_coarsen", "emit_dilate",
-    "sort_pass", "dedup", "write_ijk_inter", "write_leaves_inter", "write_refine_inter", "write_coarsen_inter",
-    "write_dilate_inter", "write_ijk", "write_leaves", "write_refine", "write_coarsen", "write_dilate",
-    "validate"};
+enum KernelKind { kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + 5, kKNumKinds };
+const char* const kKernelNames[kKNumKinds] = {"prepass_ijk", "prepass_leaves", "chain",      "write_ijk",
+                                              "write_leaves", "write_refine",   "write_coarsen", "write_dilate",
+                                              "validate"};
 
 struct ProfRec {
   int kind;
   cudaEvent_t a, b;
 };
-thread_local bool t_prof = false;
+thread_local int t_prof = 0;  // 1: kernel events, 2: also pass-phase stamps
+constexpr int kNumGpuPhases = 4;
+constexpr int kNumPhases = 7;
+const char* const kPhaseNames[kNumPhases] = {"phase_emit",       "phase_sort",     "phase_dedup_merge",
+                                             "phase_offsets",    "host_before_sync", "host_sync_wait",
+                                             "host_after_sync"};
+double host_ms_since(const std::chrono::steady_clock::time_point& t0) {
+  return std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+}
+thread_local double t_phase_ms[kNumPhases] = {};
+thread_local long long t_phase_n[kNumPhases] = {};
 thread_local std::vector<ProfRec> t_recs;
 thread_local std::vector<cudaEvent_t> t_events;
 
@@ -130,8 +136,9 @@ tb_status fail(tb_status st, const char* fmt, ...) {
 
 struct DeviceInfo {
   int sms = 0;
-  int occ_sort = 1, occ_dedup = 1;
-  int occ_write[5][2] = {};
+  int occ_chain = 1;
+  int occ_write[5] = {};
+  bool coop = false;
   bool ready = false;
 };
 std::mutex g_dev_mu;
@@ -143,10 +150,12 @@ tb_status device_info(int dev, DeviceInfo** out) {
   DeviceInfo& d = g_dev[dev];
   if (!d.ready) {
     TB_CUDA(cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev));
-    d.occ_sort = occupancy_sort();
-    d.occ_dedup = occupancy_dedup();
-    for (int op = 0; op < 5; ++op)
-      for (int f = 0; f < 2; ++f) d.occ_write[op][f] = occupancy_write(op, f != 0);
+    int coop = 0;
+    TB_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
+    if (!coop) return fail(TB_ERR_CUDA, "device %d does not support cooperative launches", dev);
+    d.coop = true;
+    d.occ_chain = chain_occupancy();
+    for (int op = 0; op < 5; ++op) d.occ_write[op] = write_final_occupancy(op);
     // keep freed memory in the default pool between calls
     cudaMemPool_t pool;
     if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
@@ -247,8 +256,8 @@ struct PassPlan {
   int32_t bbox[6];           // output voxel bbox (exact)
   KeyLayout K;
   int P = 0;
-  long long sort_tiles = 0, dedup_tiles = 0, write_tiles = 0;
-  size_t rb = 0, ctl = 0, sort_status = 0, dedup_status = 0, write_status = 0, first = 0, gbox = 0;
+  long long sort_tiles = 0, dedup_tiles = 0;
+  size_t rb = 0, ctl = 0, sort_status = 0, dedup_status = 0, first = 0;
 };
 
 long long slots_per_source(const PassSpec& s) {
@@ -349,6 +358,7 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   *out = nullptr;
   if (alloc && (!alloc->alloc || !alloc->free)) return fail(TB_ERR_INVALID_ARG, "allocator without alloc/free");
   if (specs.empty()) return fail(TB_ERR_INVALID_ARG, "no passes");
+  const auto t_entry = std::chrono::steady_clock::now();
   int dev = 0;
   TB_CUDA(cudaGetDevice(&dev));
   DeviceInfo* di = nullptr;
@@ -357,6 +367,7 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   const Mem mem{alloc, stream};
   const int32_t B = src.B;
   const bool front = src.kind != kSrcBatch;
+  const size_t rb_bytes = readback_bytes(B);
 
   // ---- bounds of every pass (host-known, no readback)
   std::vector<PassPlan> plans(specs.size());
@@ -376,36 +387,36 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     max_slots = std::max(max_slots, pl.slot_cap);
     if (p + 1 < specs.size()) max_inter = std::max(max_inter, pl.slot_cap);
   }
+  const long long last_slots = plans.back().slot_cap;
 
   // ---- key layouts (front ends: after the range prepass)
   if (!front) {
-    const tb_batch* b = src.batch;
-    const bool empty = b->L == 0;
-    st = plan_layouts(plans, B, b->bbox, empty);
+    st = plan_layouts(plans, B, src.batch->bbox, src.batch->L == 0);
     if (st != TB_OK) return st;
   } else {
     for (auto& pl : plans) pl.P = kMaxDigitPasses;  // sized for the widest key until the prepass
   }
 
-  // ---- workspace layout: a zeroed control region, then the slot buffers
+  // ---- workspace: a zeroed control region, then the slot buffers
+  const int n_launch = (int)((plans.size() + kMaxChainPasses - 1) / kMaxChainPasses);
   Carve c;
+  const size_t o_bar = c.take(sizeof(GridBarrier) * n_launch);
   for (auto& pl : plans) {
     pl.sort_tiles = std::max(1ll, (pl.slot_cap + kSortTile - 1) / kSortTile);
     pl.dedup_tiles = std::max(1ll, (pl.slot_cap + kDedupTile - 1) / kDedupTile);
-    pl.write_tiles = std::max(1ll, (pl.slot_cap + kWriteTile - 1) / kWriteTile);
-    pl.rb = c.take(sizeof(ReadbackHeader) + 3 * sizeof(int64_t) * (size_t)(B + 1));
+    pl.rb = c.take(rb_bytes);
     pl.ctl = c.take(sizeof(PassCtl));
     pl.sort_status = c.take((size_t)pl.P * pl.sort_tiles * kBins * 4);
-    pl.dedup_status = c.take((size_t)pl.dedup_tiles * 3 * 8);
-    pl.write_status = c.take((size_t)pl.write_tiles * 8);
+    pl.dedup_status = c.take((size_t)pl.dedup_tiles * 4 * 8);
     pl.first = c.take((size_t)3 * B * 4);
-    pl.gbox = c.take((size_t)6 * B * 4);
   }
+  const size_t o_ts = c.take(t_prof >= 2 ? plans.size() * 8 * sizeof(unsigned long long) : 0);
   const size_t zero_bytes = c.off;
   const size_t o_keys0 = c.take((size_t)max_slots * 8), o_keys1 = c.take((size_t)max_slots * 8);
   const size_t o_vals0 = c.take((size_t)max_slots * 4), o_vals1 = c.take((size_t)max_slots * 4);
   const size_t o_run = c.take((size_t)(max_slots + 1) * 4);
   const size_t o_llow = c.take((size_t)max_slots * 4), o_lup = c.take((size_t)max_slots * 4);
+  const size_t o_voff = c.take((size_t)last_slots * 8);
   size_t o_inter[2][3];
   for (int k = 0; k < 2; ++k) {
     o_inter[k][0] = c.take((size_t)max_inter * 12);
@@ -452,9 +463,8 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     TB_CUDA(cudaMemcpyAsync(ws + o_st_off, src.offsets, (size_t)(B + 1) * 8, cudaMemcpyDefault, stream));
     in_off = (const int64_t*)(ws + o_st_off);
   }
-
-  const size_t rb_bytes = sizeof(ReadbackHeader) + 3 * sizeof(int64_t) * (size_t)(B + 1);
-  ReadbackHeader* host_rb = (ReadbackHeader*)t_pinned.get(rb_bytes + 4 * plans.size());
+  ReadbackHeader* host_rb =
+      (ReadbackHeader*)t_pinned.get(rb_bytes + 4 * plans.size() + 64 * plans.size() + 64);
   if (!host_rb) return fail(TB_ERR_OOM, "pinned host buffer of %zu bytes failed", rb_bytes);
 
   // ---- front ends: range prepass and its readback
@@ -478,99 +488,124 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
       bb[a] = dec_min(host_rb->bbox_enc[a]);
       bb[3 + a] = dec_max(host_rb->bbox_enc[3 + a]);
     }
-    const bool empty = bb[0] > bb[3];
     const int P_alloc = plans[0].P;
-    st = plan_layouts(plans, B, bb, empty);
+    st = plan_layouts(plans, B, bb, bb[0] > bb[3]);
     if (st != TB_OK) return st;
     if (plans[0].P > P_alloc) return fail(TB_ERR_CUDA, "internal: digit passes exceed the allocation");
-    // the status region was sized for P_alloc passes; the stride stays sort_tiles
+    // the prepass wrote the bbox into the pass header; the pass accumulates on top of zeroed counters only
   }
 
-  // ---- passes
-  PassArgs a;
-  std::memset(&a, 0, sizeof a);
-  a.B = B;
-  a.keys[0] = (uint64_t*)(ws + o_keys0);
-  a.keys[1] = (uint64_t*)(ws + o_keys1);
-  a.vals[0] = (uint32_t*)(ws + o_vals0);
-  a.vals[1] = (uint32_t*)(ws + o_vals1);
-  a.run_start = (uint32_t*)(ws + o_run);
-  a.leaf_lower = (uint32_t*)(ws + o_llow);
-  a.leaf_upper = (uint32_t*)(ws + o_lup);
-  a.ijk = in_ijk;
-  a.in_offsets = in_off;
-  if (src.kind == kSrcBatch) {
-    a.src_origins = src.batch->origins;
-    a.src_masks = src.batch->masks;
-    a.src_grid = src.batch->leaf_grid;
-    a.src_count = src.batch->L;
-  } else {
-    a.src_origins = in_orig;
-    a.src_masks = in_mask;
-    a.src_grid = nullptr;
-    a.src_count = src.count;
-  }
-  a.src_count_dev = nullptr;
-
-  const int op_last = plans.back().spec.op;
+  // ---- pass arguments
+  std::vector<PassArgs> args(plans.size());
+  long long work_blocks = 1;
   for (size_t p = 0; p < plans.size(); ++p) {
     PassPlan& pl = plans[p];
-    const bool last = p + 1 == plans.size();
+    PassArgs& a = args[p];
+    std::memset(&a, 0, sizeof a);
     a.K = pl.K;
+    a.op = pl.spec.op;
+    a.B = B;
     a.P = pl.P;
+    a.last = p + 1 == plans.size();
     for (int ax = 0; ax < 3; ++ax) {
       a.lo[ax] = pl.spec.lo[ax];
       a.hi[ax] = pl.spec.hi[ax];
+    }
+    if (p == 0) {
+      a.ijk = in_ijk;
+      a.in_offsets = in_off;
+      if (src.kind == kSrcBatch) {
+        a.src_origins = src.batch->origins;
+        a.src_masks = src.batch->masks;
+        a.src_grid = src.batch->leaf_grid;
+        a.src_count = src.batch->L;
+      } else {
+        a.src_origins = in_orig;
+        a.src_masks = in_mask;
+        a.src_count = src.count;
+      }
+    } else {
+      const PassArgs& prev = args[p - 1];
+      a.src_origins = prev.out_origins;
+      a.src_masks = prev.out_masks;
+      a.src_grid = prev.out_grid;
+      a.src_count_dev = &prev.rb->num_leaves;
     }
     a.rb = (ReadbackHeader*)(ws + pl.rb);
     a.leaf_off = (int64_t*)(ws + pl.rb + sizeof(ReadbackHeader));
     a.lower_off = a.leaf_off + (B + 1);
     a.upper_off = a.lower_off + (B + 1);
+    a.grid_vox = a.upper_off + (B + 1);
+    a.gbox = (unsigned int*)(a.grid_vox + B);
     a.ctl = (PassCtl*)(ws + pl.ctl);
-    a.slot_cap = pl.slot_cap;
     a.sort_status = (uint32_t*)(ws + pl.sort_status);
     a.sort_tiles_cap = pl.sort_tiles;
     a.dedup_status = (unsigned long long*)(ws + pl.dedup_status);
-    a.write_status = (unsigned long long*)(ws + pl.write_status);
     a.first = (uint32_t*)(ws + pl.first);
-    a.gbox = (unsigned int*)(ws + pl.gbox);
-
-    const int eb = blocks_for(pl.in_cap, 256, (long long)di->sms * 8);
-    TB_CUDA(launch(kKEmit0 + pl.spec.op, stream, [&] { return launch_emit(pl.spec.op, a, eb, stream); }));
-    const int sb = blocks_for(pl.sort_tiles, 1, (long long)di->sms * di->occ_sort);
-    for (int d = 0; d < pl.P; ++d)
-      TB_CUDA(launch(kKSort, stream, [&] { return launch_sort_pass(a, d, sb, stream); }));
+    a.slot_cap = pl.slot_cap;
+    a.keys[0] = (uint64_t*)(ws + o_keys0);
+    a.keys[1] = (uint64_t*)(ws + o_keys1);
+    a.vals[0] = (uint32_t*)(ws + o_vals0);
+    a.vals[1] = (uint32_t*)(ws + o_vals1);
     a.sorted = pl.P & 1;
-    const int db = blocks_for(pl.dedup_tiles, 1, (long long)di->sms * di->occ_dedup);
-    TB_CUDA(launch(kKDedup, stream, [&] { return launch_dedup(a, db, stream); }));
-    if (last) break;
-    // hand the leaves to the next pass without a readback
-    WriteOut wo;
-    std::memset(&wo, 0, sizeof wo);
-    const int k = (int)(p & 1);
-    wo.origins = (int32_t*)(ws + o_inter[k][0]);
-    wo.masks = (uint64_t*)(ws + o_inter[k][1]);
-    wo.leaf_grid = (int32_t*)(ws + o_inter[k][2]);
-    const int wb = blocks_for(pl.write_tiles, 1, (long long)di->sms * di->occ_write[pl.spec.op][0]);
-    TB_CUDA(launch(kKWriteInter0 + pl.spec.op, stream, [&] { return launch_write(pl.spec.op, false, a, wo, wb, stream); }));
-    a.src_origins = wo.origins;
-    a.src_masks = wo.masks;
-    a.src_grid = wo.leaf_grid;
-    a.src_count_dev = &a.rb->num_leaves;
-    a.src_count = 0;
+    a.run_start = (uint32_t*)(ws + o_run);
+    a.leaf_lower = (uint32_t*)(ws + o_llow);
+    a.leaf_upper = (uint32_t*)(ws + o_lup);
+    a.leaf_voff = (int64_t*)(ws + o_voff);
+    a.phase_ts = t_prof >= 2 ? (unsigned long long*)(ws + o_ts) + 8 * p : nullptr;
+    if (!a.last) {
+      const int k = (int)(p & 1);
+      a.out_origins = (int32_t*)(ws + o_inter[k][0]);
+      a.out_masks = (uint64_t*)(ws + o_inter[k][1]);
+      a.out_grid = (int32_t*)(ws + o_inter[k][2]);
+    }
+    work_blocks = std::max({work_blocks, (pl.in_cap + 255) / 256, pl.sort_tiles, pl.dedup_tiles});
   }
 
-  // ---- the one count readback of the pass
-  // (plus the error words of the earlier passes of a chain)
+  // ---- the cooperative pass kernel(s)
+  const int G = blocks_for(work_blocks, 1, (long long)di->sms * di->occ_chain);
+  for (int l = 0; l < n_launch; ++l) {
+    ChainArgs ca;
+    std::memset(&ca, 0, sizeof ca);
+    ca.bar = (GridBarrier*)(ws + o_bar) + l;
+    const size_t p0 = (size_t)l * kMaxChainPasses;
+    ca.n_pass = (int32_t)std::min<size_t>(kMaxChainPasses, plans.size() - p0);
+    for (int k = 0; k < ca.n_pass; ++k) ca.pass[k] = args[p0 + k];
+    TB_CUDA(launch(kKChain, stream, [&] { return launch_chain(ca, G, stream); }));
+  }
+
+  // ---- the one count readback of the call (plus the error words of the earlier passes)
+  const PassArgs& a = args.back();
   unsigned int* host_err = (unsigned int*)((char*)host_rb + rb_bytes);
   for (size_t p = 0; p + 1 < plans.size(); ++p)
     TB_CUDA(cudaMemcpyAsync(host_err + p, ws + plans[p].rb + offsetof(ReadbackHeader, err), 4,
                             cudaMemcpyDeviceToHost, stream));
+  unsigned long long* host_ts =
+      (unsigned long long*)(((uintptr_t)host_err + 4 * plans.size() + 63) & ~(uintptr_t)63);
+  if (t_prof >= 2)
+    TB_CUDA(cudaMemcpyAsync(host_ts, ws + o_ts, plans.size() * 64, cudaMemcpyDeviceToHost, stream));
   TB_CUDA(cudaMemcpyAsync(host_rb, a.rb, rb_bytes, cudaMemcpyDeviceToHost, stream));
+  const auto t_sync = std::chrono::steady_clock::now();
   TB_CUDA(cudaStreamSynchronize(stream));
+  const auto t_synced = std::chrono::steady_clock::now();
+  if (t_prof >= 2) {
+    t_phase_ms[4] += std::chrono::duration<double, std::milli>(t_sync - t_entry).count();
+    t_phase_ms[5] += std::chrono::duration<double, std::milli>(t_synced - t_sync).count();
+    t_phase_n[4] += 1;
+    t_phase_n[5] += 1;
+  }
+  if (t_prof >= 2)
+    for (size_t p = 0; p < plans.size(); ++p)
+      for (int k = 0; k < kNumGpuPhases; ++k) {
+        const unsigned long long t0 = k == 0 ? ~host_ts[8 * p] : host_ts[8 * p + k], t1 = host_ts[8 * p + k + 1];
+        if (t1 >= t0 && t0) {
+          t_phase_ms[k] += (double)(t1 - t0) * 1e-6;
+          t_phase_n[k] += 1;
+        }
+      }
   unsigned int err = host_rb->err;
   for (size_t p = 0; p + 1 < plans.size(); ++p) err |= host_err[p];
-  if (err & kErrTimeout) return fail(TB_ERR_DEVICE_TIMEOUT, "a device-side look-back wait timed out");
+  if (err & kErrTimeout) return fail(TB_ERR_DEVICE_TIMEOUT, "a device-side wait timed out");
   if (err & kErrSlotOverflow) return fail(TB_ERR_CUDA, "internal: emitted slots exceeded the bound");
   const int64_t L = (int64_t)host_rb->num_leaves, NL = (int64_t)host_rb->num_lowers,
                 NU = (int64_t)host_rb->num_uppers;
@@ -587,14 +622,14 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   if (alloc) b->alloc = *alloc;
   b->leaf_offsets_host.assign(hoff, hoff + B + 1);
   std::memcpy(b->bbox, plans.back().bbox, sizeof b->bbox);
-  b->build_slots = (int64_t)host_rb->num_slots;
-  b->build_sources = plans.size() == 1 ? (int64_t)plans.back().in_cap : -1;
-  b->build_key_bits = plans.back().K.W;
-  b->build_digit_passes = plans.back().P;
   if (plans.back().empty || L == 0) {
     const int32_t e[6] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MIN, INT32_MIN, INT32_MIN};
     std::memcpy(b->bbox, e, sizeof e);
   }
+  b->build_slots = (int64_t)host_rb->num_slots;
+  b->build_sources = plans.size() == 1 ? (int64_t)plans.back().in_cap : -1;
+  b->build_key_bits = plans.back().K.W;
+  b->build_digit_passes = plans.back().P;
   Carve oc;
   size_t off[16];
   off[0] = oc.take((size_t)(B + 1) * 8);
@@ -651,14 +686,20 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   wo.lower_origins = b->lower_origins;
   wo.lower_parent = b->lower_parent;
   wo.upper_origins = b->upper_origins;
-  const int wb = blocks_for(L, kWriteTile, (long long)di->sms * di->occ_write[op_last][1]);
-  cudaError_t e = launch(kKWriteFinal0 + op_last, stream, [&] { return launch_write(op_last, true, a, wo, wb, stream); });
+  const int op_last = plans.back().spec.op;
+  const int wb = blocks_for(std::max<long long>(L, B + 1), kWriteLeavesPerBlock,
+                            (long long)di->sms * di->occ_write[op_last]);
+  cudaError_t e = launch(kKWrite0 + op_last, stream, [&] { return launch_write_final(op_last, a, wo, wb, stream); });
   if (e != cudaSuccess) {
     mem.put(b->mem);
     delete b;
     return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
   }
   *out = b;
+  if (t_prof >= 2) {
+    t_phase_ms[6] += host_ms_since(t_synced);
+    t_phase_n[6] += 1;
+  }
   return TB_OK;
 }
 
@@ -902,7 +943,7 @@ int32_t tb_version(void) { return 100; }
 int64_t tb_kernel_launch_count(void) { return t_launches; }
 
 tb_status tb_profile_enable(int32_t on) {
-  t_prof = on != 0;
+  t_prof = on < 0 ? 0 : on;
   return TB_OK;
 }
 
@@ -925,6 +966,13 @@ int32_t tb_profile_read(tb_kernel_stat* stats, int32_t max) {
     if (!n[i]) continue;
     if (stats && k < max) stats[k] = tb_kernel_stat{kKernelNames[i], n[i], ms[i]};
     ++k;
+  }
+  for (int i = 0; i < kNumPhases; ++i) {
+    if (!t_phase_n[i]) continue;
+    if (stats && k < max) stats[k] = tb_kernel_stat{kPhaseNames[i], t_phase_n[i], t_phase_ms[i]};
+    ++k;
+    t_phase_n[i] = 0;
+    t_phase_ms[i] = 0.0;
   }
   return k;
 }

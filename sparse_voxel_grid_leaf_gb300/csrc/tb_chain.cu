@@ -1,0 +1,923 @@
+// The batched pass as one cooperative, persistent kernel per call, and the
+// final writer (fVDB PR #757 "Batched leaf-mask topology construction for
+// generated conv grids", Summary item 1; item 2 for the box dilation).
+//
+// k_chain runs every pass of a call (a chain of up to kMaxChainPasses) with
+// all blocks co-resident; phases are separated by a bounded software grid
+// barrier:
+//   emission  -> digit pass 0 .. P-1 -> dedup -> per-grid offsets
+//             -> count (last pass: voxel offsets, grid voxel counts and bboxes)
+//             or hand-off (intermediate pass: leaves for the next pass).
+// Everything the host needs to size the outputs then comes back in one
+// readback, and k_write_final writes the leaf records without any scan.
+//
+// Emission: one thread per source leaf (or input voxel) writes one slot per
+// non-empty target leaf -- 8 octant children for refine x2, the coarse leaf
+// for coarsen x2, up to 27 neighbours for a box dilation -- with
+// warp-aggregated slot claims, and builds the radix histograms of every digit
+// pass in shared memory.
+// Sort: the grid index is the key's most significant field, so one global LSD
+// sort over the varying key bits replaces the PR's segmented sorts.  A digit
+// pass is a onesweep tile loop: warp multisplit ranking (match.any), per-digit
+// decoupled look-back, shared-memory staging, coalesced scatter.
+// Dedup: head flags on the sorted keys (new leaf / lower node / upper node /
+// grid), a tile scan with warp-window look-back.
+#include "tb_common.cuh"
+#include "tb_launch.h"
+
+namespace tb {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+struct SmemSort {
+  uint32_t whist[kThreads / 32][kBins];
+  uint32_t binstart[kBins];
+  uint32_t glob[kBins];
+  uint32_t binbase[kBins];
+  uint64_t keys[kSortTile];
+  uint32_t vals[kSortTile];
+  uint32_t scan[8];
+  uint32_t tile;
+};
+struct SmemEmit {
+  unsigned int hist[kMaxDigitPasses][kBins];
+};
+struct SmemDedup {
+  unsigned long long scan[8];
+  unsigned long long base[4];
+  uint32_t seg_f[8];
+  unsigned long long seg_v[8];
+  uint32_t head_pos[kDedupTile];   // slot of each leaf head of the tile, in order
+  uint32_t head_fl[kDedupTile];    // its head flags (bit 3: first leaf of a grid)
+  uint32_t head_pop[kDedupTile];   // voxels of its merged mask
+  uint32_t head_g[kDedupTile];     // its grid
+  uint32_t grp_g[kThreads / 8];            // per 8-lane group: grid of its pending bbox
+  unsigned int grp_box[kThreads / 8][6];   // per group: pending encoded bbox
+  uint32_t tail_end;               // end of the tile's last run
+  uint32_t tail_newgrid;           // 1 if that run is the last of its grid
+  uint32_t tile;
+  uint32_t last;
+};
+struct SmemFinish {
+  uint32_t s[kThreads];
+};
+union Smem {
+  SmemSort sort;
+  SmemEmit emit;
+  SmemDedup dedup;
+  SmemFinish fin;
+};
+
+// Profiling stamps of the GPU global timer over all blocks: slot 0 holds the
+// earliest block start (as the max of its complement), slot k > 0 the latest
+// block end of phase k.
+__device__ __forceinline__ void stamp(const PassArgs& a, int k) {
+  if (a.phase_ts && threadIdx.x == 0) {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    atomicMax(&a.phase_ts[k], k == 0 ? ~t : t);
+  }
+}
+
+// ---------------------------------------------------------------- emission
+
+__device__ __forceinline__ int grid_of(const int64_t* offsets, int32_t B, long long i) {
+  int lo = 0, hi = B;  // last g with offsets[g] <= i
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (__ldg(offsets + mid) <= i) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// Bit set of the non-empty targets of one source leaf.
+template <int OP>
+__device__ __forceinline__ uint32_t targets_of(const PassArgs& a, const uint64_t m[8]) {
+  uint64_t all = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) all |= m[w];
+  if (OP == kLeaves || OP == kCoarsen) return all ? 1u : 0u;
+  if (OP == kRefine) {
+    // child c = 4*cx + 2*cy + cz is non-empty iff the parent's octant c holds a voxel
+    uint32_t bits = 0;
+#pragma unroll
+    for (int cx = 0; cx < 2; ++cx) {
+      const uint64_t t = m[4 * cx] | m[4 * cx + 1] | m[4 * cx + 2] | m[4 * cx + 3];
+#pragma unroll
+      for (int cy = 0; cy < 2; ++cy)
+#pragma unroll
+        for (int cz = 0; cz < 2; ++cz)
+          if (t & (0x0F0F0F0Full << (32 * cy + 4 * cz))) bits |= 1u << (4 * cx + 2 * cy + cz);
+    }
+    return bits;
+  }
+  // box dilation: target offset t (code 9(tx+1) + 3(ty+1) + (tz+1)) is reached iff a
+  // voxel lies in its zone -- anywhere for t = 0, the last plane for t = +1 (hi = 1),
+  // the first plane for t = -1 (lo = -1)
+  const uint64_t xs[3] = {m[0], all, m[7]};
+  const uint64_t ym[3] = {0x00000000000000FFull, ~0ull, 0xFF00000000000000ull};
+  const uint64_t zm[3] = {0x0101010101010101ull, ~0ull, 0x8080808080808080ull};
+  uint32_t bits = 0;
+#pragma unroll
+  for (int tx = -1; tx <= 1; ++tx)
+#pragma unroll
+    for (int ty = -1; ty <= 1; ++ty)
+#pragma unroll
+      for (int tz = -1; tz <= 1; ++tz) {
+        if (tx < a.lo[0] || tx > a.hi[0] || ty < a.lo[1] || ty > a.hi[1] || tz < a.lo[2] || tz > a.hi[2]) continue;
+        if (xs[tx + 1] & ym[ty + 1] & zm[tz + 1]) bits |= 1u << (9 * (tx + 1) + 3 * (ty + 1) + (tz + 1));
+      }
+  return bits;
+}
+
+template <int OP>
+__device__ __forceinline__ void target_lc(const int32_t lc[3], uint32_t code, int32_t out[3]) {
+  if (OP == kRefine) {
+    out[0] = 2 * lc[0] + (int32_t)((code >> 2) & 1);
+    out[1] = 2 * lc[1] + (int32_t)((code >> 1) & 1);
+    out[2] = 2 * lc[2] + (int32_t)(code & 1);
+  } else if (OP == kCoarsen) {
+    out[0] = lc[0] >> 1;
+    out[1] = lc[1] >> 1;
+    out[2] = lc[2] >> 1;
+  } else if (OP == kDilate) {
+    out[0] = lc[0] + (int32_t)(code / 9) - 1;
+    out[1] = lc[1] + (int32_t)((code / 3) % 3) - 1;
+    out[2] = lc[2] + (int32_t)(code % 3) - 1;
+  } else {
+    out[0] = lc[0];
+    out[1] = lc[1];
+    out[2] = lc[2];
+  }
+}
+
+// Claims `n` consecutive slots for this lane within one warp-wide range;
+// returns the lane's first slot and the warp's range [wbase, wbase + wtotal).
+__device__ __forceinline__ unsigned long long claim_slots(const PassArgs& a, uint32_t n, unsigned long long& wbase,
+                                                          uint32_t& wtotal) {
+  const int lane = threadIdx.x & 31;
+  uint32_t incl = n;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  wtotal = __shfl_sync(0xffffffffu, incl, 31);
+  unsigned long long base = 0;
+  if (lane == 31 && wtotal) base = atomicAdd(&a.rb->num_slots, (unsigned long long)wtotal);
+  wbase = __shfl_sync(0xffffffffu, base, 31);
+  return wbase + incl - n;
+}
+
+__device__ __forceinline__ void put_slot(const PassArgs& a, unsigned long long pos, uint64_t key, uint32_t val) {
+  if (pos < (unsigned long long)a.slot_cap) {
+    a.keys[0][pos] = key;
+    a.vals[0][pos] = val;
+  } else {
+    atomicOr(&a.rb->err, kErrSlotOverflow);
+  }
+}
+
+// Adds one key per lane (valid lanes only) to the block's digit histograms,
+// one shared-memory atomic per distinct digit value in the warp.
+__device__ __forceinline__ void hist_warp(const PassArgs& a, unsigned int (*hist)[kBins], uint64_t key, bool valid) {
+  const int lane = threadIdx.x & 31;
+  for (int p = 0; p < a.P; ++p) {
+    const uint32_t d = valid ? ((uint32_t)(key >> (8 * p)) & 255u) : kBins;
+    const uint32_t peers = __match_any_sync(0xffffffffu, d);
+    if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(&hist[p][d], (unsigned int)__popc(peers));
+  }
+}
+
+template <int OP>
+__device__ void phase_emit(const PassArgs& a, Smem& sm) {
+  for (int i = threadIdx.x; i < a.P * kBins; i += kThreads) (&sm.emit.hist[0][0])[i] = 0;
+  __syncthreads();
+  const long long n = a.src_count_dev ? (long long)__ldcg(a.src_count_dev) : a.src_count;
+  const long long stride = (long long)gridDim.x * kThreads;
+  const int lane = threadIdx.x & 31;
+  for (long long base = (long long)blockIdx.x * kThreads; base < n; base += stride) {
+    const long long i = base + threadIdx.x;
+    unsigned long long wbase;
+    uint32_t wtotal;
+    if (OP == kIjk) {
+      const bool valid = i < n;
+      const unsigned long long pos = claim_slots(a, valid ? 1u : 0u, wbase, wtotal);
+      uint64_t key = 0;
+      if (valid) {
+        const int32_t x = __ldg(a.ijk + 3 * i), y = __ldg(a.ijk + 3 * i + 1), z = __ldg(a.ijk + 3 * i + 2);
+        const uint32_t g = (uint32_t)grid_of(a.in_offsets, a.B, i);
+        key = encode_key(a.K, g, x >> 3, y >> 3, z >> 3);
+        put_slot(a, pos, key, (uint32_t)i);
+      }
+      hist_warp(a, sm.emit.hist, key, valid);
+    } else {
+      uint32_t bits = 0;
+      int32_t lc[3] = {0, 0, 0};
+      uint32_t g = 0;
+      if (i < n) {
+        uint64_t m[8];
+        load_mask(a.src_masks, i, m);
+        bits = targets_of<OP>(a, m);
+        lc[0] = __ldcg(a.src_origins + 3 * i) >> 3;
+        lc[1] = __ldcg(a.src_origins + 3 * i + 1) >> 3;
+        lc[2] = __ldcg(a.src_origins + 3 * i + 2) >> 3;
+        g = a.src_grid ? (uint32_t)__ldcg(a.src_grid + i) : (uint32_t)grid_of(a.in_offsets, a.B, i);
+      }
+      unsigned long long pos = claim_slots(a, __popc(bits), wbase, wtotal);
+      while (bits) {
+        const uint32_t code = __ffs(bits) - 1;
+        bits &= bits - 1;
+        int32_t t[3];
+        target_lc<OP>(lc, code, t);
+        // coarsen: the code is the source leaf's octant inside its coarse leaf
+        const uint32_t ref = OP == kCoarsen ? (uint32_t)(((lc[0] & 1) << 2) | ((lc[1] & 1) << 1) | (lc[2] & 1)) : code;
+        put_slot(a, pos++, encode_key(a.K, g, t[0], t[1], t[2]), ((uint32_t)i << kSrcShift) | ref);
+      }
+      // histogram the warp's freshly written range, 32 keys at a time
+      __syncwarp();
+      for (uint32_t off = 0; off < wtotal; off += 32) {
+        const unsigned long long j = wbase + off + lane;
+        const bool valid = off + lane < wtotal && j < (unsigned long long)a.slot_cap;
+        const uint64_t key = valid ? __ldcg(a.keys[0] + j) : 0ull;
+        hist_warp(a, sm.emit.hist, key, valid);
+      }
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < a.P * kBins; i += kThreads) {
+    const unsigned int c = (&sm.emit.hist[0][0])[i];
+    if (c) atomicAdd(&(&a.ctl->hist[0][0])[i], c);
+  }
+}
+
+// ---------------------------------------------------------------- radix digit pass
+
+__device__ void phase_sort(const PassArgs& a, int pass, Smem& sm) {
+  constexpr int NW = kThreads / 32;
+  constexpr int WITEMS = 32 * kSortItems;
+  SmemSort& s = sm.sort;
+  const int shift = 8 * pass;
+  const uint64_t* kin = a.keys[pass & 1];
+  const uint32_t* vin = a.vals[pass & 1];
+  uint64_t* kout = a.keys[(pass + 1) & 1];
+  uint32_t* vout = a.vals[(pass + 1) & 1];
+  long long S = (long long)__ldcg(&a.rb->num_slots);
+  if (S > a.slot_cap) S = a.slot_cap;
+  const long long ntiles = (S + kSortTile - 1) / kSortTile;
+  uint32_t* status = a.sort_status + (long long)pass * a.sort_tiles_cap * kBins;
+  unsigned int* ctr = &a.ctl->sort_tile_ctr[pass];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  {
+    uint32_t total;
+    s.binbase[tid] = block_excl_scan_256(__ldcg(&a.ctl->hist[pass][tid]), s.scan, &total);
+  }
+  for (;;) {
+    if (tid == 0) s.tile = atomicAdd(ctr, 1u);
+    for (int k = tid; k < NW * kBins; k += kThreads) (&s.whist[0][0])[k] = 0;
+    __syncthreads();
+    const long long tile = s.tile;
+    if (tile >= ntiles) break;
+    const long long base = tile * kSortTile + (long long)warp * WITEMS;
+    uint64_t k[kSortItems];
+    uint32_t v[kSortItems], d[kSortItems], r[kSortItems];
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) {
+      const long long idx = base + j * 32 + lane;
+      if (idx < S) {
+        k[j] = __ldcg(kin + idx);
+        v[j] = __ldcg(vin + idx);
+        d[j] = (uint32_t)(k[j] >> shift) & 255u;
+      } else {
+        k[j] = 0;
+        v[j] = 0;
+        d[j] = kBins;  // padding: ranked nowhere
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) {
+      const uint32_t peers = __match_any_sync(0xffffffffu, d[j]);
+      const uint32_t lt = peers & ((1u << lane) - 1u);
+      uint32_t cnt = 0;
+      if (d[j] < kBins) cnt = s.whist[warp][d[j]];
+      __syncwarp();
+      if (d[j] < kBins && lt == 0) s.whist[warp][d[j]] = cnt + __popc(peers);
+      __syncwarp();
+      r[j] = cnt + __popc(lt);
+    }
+    __syncthreads();
+    uint32_t tot = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const uint32_t c = s.whist[w][tid];
+      s.whist[w][tid] = tot;
+      tot += c;
+    }
+    uint32_t all;
+    const uint32_t ex = block_excl_scan_256(tot, s.scan, &all);
+    s.binstart[tid] = ex;
+    const uint32_t prefix = lookback32(status + tid, kBins, tile, tot, &a.rb->err);
+    s.glob[tid] = s.binbase[tid] + prefix - ex;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) {
+      if (d[j] < kBins) {
+        const uint32_t lp = s.binstart[d[j]] + s.whist[warp][d[j]] + r[j];
+        s.keys[lp] = k[j];
+        s.vals[lp] = v[j];
+      }
+    }
+    __syncthreads();
+    const long long rem = S - tile * kSortTile;
+    const int nvalid = rem < kSortTile ? (int)rem : kSortTile;
+    for (int i = tid; i < nvalid; i += kThreads) {
+      const uint64_t key = s.keys[i];
+      const uint32_t gp = s.glob[(uint32_t)(key >> shift) & 255u] + (uint32_t)i;
+      if (gp < (uint64_t)S) {  // always true when the histograms match the slots
+        kout[gp] = key;
+        vout[gp] = s.vals[i];
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------- merged masks
+
+// Word w (this lane's, within an aligned group of 8 lanes) of the OR of the
+// run of slots [s0, s1).  Refinement runs have one slot per leaf, so each lane
+// recomputes its own word; the other ops spread the run's slots over the 8
+// lanes, build full 8-word contributions and reduce-scatter them.
+template <int OP>
+__device__ __forceinline__ uint64_t merge_run(const PassArgs& a, const uint32_t* vals, uint32_t s0, uint32_t s1,
+                                              int w) {
+  if constexpr (OP == kRefine) {
+    uint64_t word = 0;
+    for (uint32_t s = s0; s < s1; ++s) {
+      const uint32_t val = __ldcg(vals + s);
+      const long long src = (long long)(val >> kSrcShift);
+      const int cx = (val >> 2) & 1, cy = (val >> 1) & 1, cz = val & 1;
+      word |= refine_word(__ldcg(a.src_masks + 8 * src + 4 * cx + (w >> 1)), cy, cz);
+    }
+    return word;
+  } else {
+  uint64_t c[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) c[k] = 0;
+  for (uint32_t s = s0 + w; s < s1; s += 8) {
+    const uint32_t val = __ldcg(vals + s);
+    if constexpr (OP == kIjk) {
+      const long long n = val;
+      const int32_t x = __ldg(a.ijk + 3 * n), y = __ldg(a.ijk + 3 * n + 1), z = __ldg(a.ijk + 3 * n + 2);
+      const uint64_t bit = 1ull << (8 * (y & 7) + (z & 7));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) c[k] |= ((x & 7) == k) ? bit : 0ull;
+    } else {
+    uint64_t m[8];
+    load_mask(a.src_masks, (long long)(val >> kSrcShift), m);
+    const uint32_t code = val & 31u;
+    if (OP == kLeaves) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) c[k] |= m[k];
+    } else if (OP == kCoarsen) {
+      const int qx = (code >> 2) & 1, qy = (code >> 1) & 1, qz = code & 1;
+      uint64_t cw[4];
+#pragma unroll
+      for (int X = 0; X < 4; ++X) cw[X] = coarsen_word(m[2 * X] | m[2 * X + 1], qy, qz);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) c[k] |= ((k >> 2) == qx) ? cw[k & 3] : 0ull;
+    } else {  // kDilate
+      const int tx = (int)(code / 9) - 1, ty = (int)((code / 3) % 3) - 1, tz = (int)(code % 3) - 1;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        uint64_t r;
+        if (tx == 0) {
+          r = m[k];
+          if (a.hi[0] > 0 && k >= 1) r |= m[k - 1];
+          if (a.lo[0] < 0 && k <= 6) r |= m[k + 1];
+        } else if (tx > 0) {
+          r = (k == 0) ? m[7] : 0ull;
+        } else {
+          r = (k == 7) ? m[0] : 0ull;
+        }
+        c[k] |= dilate_y(dilate_z(r, tz, a.lo[2], a.hi[2]), ty, a.lo[1], a.hi[1]);
+      }
+    }
+    }
+  }
+  return reduce_scatter8(c, w);
+  }
+}
+
+__device__ __forceinline__ uint32_t bits_of_bytes(uint64_t m) {
+  uint32_t b = 0;
+#pragma unroll
+  for (int r = 0; r < 8; ++r)
+    if ((m >> (8 * r)) & 0xFFull) b |= 1u << r;
+  return b;
+}
+
+// Inclusive min/max of the set voxels of a leaf from its 8-lane group's word
+// (lane w holds word w); valid in every lane of the group.
+__device__ __forceinline__ void leaf_bounds(uint64_t word, int w, int lane, int32_t mn[3], int32_t mx[3]) {
+  uint64_t orm = word;
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) orm |= __shfl_xor_sync(0xffffffffu, orm, off);
+  const uint32_t xb = (__ballot_sync(0xffffffffu, word != 0) >> (lane & ~7)) & 0xFFu;
+  const uint32_t yb = bits_of_bytes(orm);
+  uint64_t z = orm | (orm >> 32);
+  z |= z >> 16;
+  z |= z >> 8;
+  const uint32_t zb = (uint32_t)(z & 0xFFull);
+  (void)w;
+  mn[0] = __ffs(xb) - 1;
+  mx[0] = 31 - __clz(xb);
+  mn[1] = __ffs(yb) - 1;
+  mx[1] = 31 - __clz(yb);
+  mn[2] = __ffs(zb) - 1;
+  mx[2] = 31 - __clz(zb);
+}
+
+// ---------------------------------------------------------------- dedup, merge, count
+
+// out[g] = first index of the first non-empty grid >= g, or `total`; out[B] = total.
+__device__ void suffix_fill(const uint32_t* first, int32_t B, unsigned long long total, int64_t* out, Smem& sm) {
+  uint32_t* s = sm.fin.s;
+  const int tid = threadIdx.x;
+  uint32_t carry = 0xFFFFFFFFu;
+  if (B > 0) {
+    for (long long base = ((long long)(B - 1) / kThreads) * kThreads; base >= 0; base -= kThreads) {
+      const long long g = base + tid;
+      uint32_t v = 0xFFFFFFFFu;
+      if (g < B) {
+        const uint32_t f = __ldcg(first + g);
+        if (f) v = f - 1;
+      }
+      s[tid] = v;
+      __syncthreads();
+      for (int off = 1; off < kThreads; off <<= 1) {
+        const uint32_t t = (tid + off < kThreads) ? s[tid + off] : 0xFFFFFFFFu;
+        __syncthreads();
+        s[tid] = min(s[tid], t);
+        __syncthreads();
+      }
+      const uint32_t res = min(s[tid], carry);
+      if (g < B) out[g] = (res == 0xFFFFFFFFu) ? (int64_t)total : (int64_t)res;
+      carry = min(carry, s[0]);
+      __syncthreads();
+    }
+  }
+  if (tid == 0) out[B] = (int64_t)total;
+}
+
+// One phase after the sort.  Per 1024-slot tile:
+//   head flags on the sorted keys (new leaf / lower node / upper node / grid),
+//   a block scan and a look-back of the three head counts (unique-leaf, lower-
+//   and upper-node indices), the run of every leaf head (a run may continue
+//   into later tiles), the OR-merge of each run by an 8-lane group, then
+//   - last pass: popcounts and bboxes (grid bboxes by atomics), a segmented
+//     voxel scan over the tile's leaves with a look-back (segments = grids),
+//     voxel offsets per leaf and voxels per grid;
+//   - intermediate pass: the merged leaves themselves, for the next pass.
+// The last block to finish writes the totals and the per-grid offsets.
+template <int OP>
+__device__ void phase_dedup(const PassArgs& a, Smem& sm) {
+  SmemDedup& s = sm.dedup;
+  const uint64_t* keys = a.keys[a.sorted];
+  const uint32_t* vals = a.vals[a.sorted];
+  long long S = (long long)__ldcg(&a.rb->num_slots);
+  if (S > a.slot_cap) S = a.slot_cap;
+  const long long ntiles = (S + kDedupTile - 1) / kDedupTile;
+  const int lb = a.K.lower_bits, nb = a.K.node_bits, gsh = a.K.gw ? a.K.gshift : 64;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, w = tid & 7;
+  const int32_t B = a.B;
+  constexpr unsigned long long M21 = (1ull << 21) - 1;
+  for (;;) {
+    if (tid == 0) s.tile = atomicAdd(&a.ctl->dedup_tile_ctr, 1u);
+    __syncthreads();
+    const long long tile = s.tile;
+    if (tile >= ntiles) break;
+    const long long t0 = tile * kDedupTile;
+    const long long t1 = (t0 + kDedupTile < S) ? t0 + kDedupTile : S;
+    const long long i0 = t0 + (long long)tid * kDedupItems;
+    uint64_t prev = (i0 > 0 && i0 - 1 < S) ? __ldcg(keys + i0 - 1) : 0ull;
+    uint64_t kk[kDedupItems];
+    uint32_t fl[kDedupItems];
+    unsigned long long c = 0;
+#pragma unroll
+    for (int j = 0; j < kDedupItems; ++j) {
+      const long long i = i0 + j;
+      fl[j] = 0;
+      kk[j] = 0;
+      if (i < S) {
+        const uint64_t key = __ldcg(keys + i);
+        kk[j] = key;
+        const bool first = (i == 0);
+        const bool hl = first || key != prev;
+        const bool hlo = first || shr64(key, lb) != shr64(prev, lb);
+        const bool hup = first || shr64(key, nb) != shr64(prev, nb);
+        const bool hg = first || shr64(key, gsh) != shr64(prev, gsh);
+        fl[j] = (hl ? 1u : 0u) | (hlo ? 2u : 0u) | (hup ? 4u : 0u) | (hg ? 8u : 0u);
+        c += (hl ? 1ull : 0ull) | (hlo ? (1ull << 21) : 0ull) | (hup ? (1ull << 42) : 0ull);
+        prev = key;
+      }
+    }
+    unsigned long long tot;
+    const unsigned long long ex = block_excl_scan_256(c, s.scan, &tot);
+    const int nheads = (int)(tot & M21);
+    if (warp < 3) {
+      const unsigned long long field = (tot >> (21 * warp)) & M21;
+      lb64_publish(a.dedup_status + warp, 4, tile, field, false);
+    }
+    // compact the heads of the tile
+    {
+      int k = (int)(ex & M21);
+#pragma unroll
+      for (int j = 0; j < kDedupItems; ++j)
+        if (fl[j] & 1u) {
+          s.head_pos[k] = (uint32_t)(i0 + j);
+          s.head_fl[k] = fl[j];
+          ++k;
+        }
+    }
+    // end of the tile's last run: the first slot at or after t1 with another key
+    if (warp == 0) {
+      uint32_t end = (uint32_t)S, newgrid = 1;
+      if (t1 < S) {
+        const uint64_t last_key = __ldcg(keys + t1 - 1);
+        for (long long b = t1;; b += 32) {
+          const long long j = b + lane;
+          const uint64_t kj = j < S ? __ldcg(keys + j) : ~0ull;
+          const uint32_t diff = __ballot_sync(0xffffffffu, j >= S || kj != last_key);
+          if (diff) {
+            const int l = __ffs(diff) - 1;
+            const long long je = b + l;
+            const uint64_t kd = __shfl_sync(0xffffffffu, kj, l);
+            end = (uint32_t)(je < S ? je : S);
+            newgrid = (je >= S || shr64(kd, gsh) != shr64(last_key, gsh)) ? 1u : 0u;
+            break;
+          }
+        }
+      }
+      if (lane == 0) {
+        s.tail_end = end;
+        s.tail_newgrid = newgrid;
+      }
+    }
+    __syncthreads();
+    // leaf / lower / upper bases of the tile
+    if (warp < 3) {
+      const unsigned long long field = (tot >> (21 * warp)) & M21;
+      const unsigned long long b = lb64_resolve(a.dedup_status + warp, 4, tile, field, false, &a.rb->err);
+      if (lane == 0) {
+        s.base[warp] = b;
+        if (field) atomicAdd(&a.ctl->head_totals[warp], field);
+      }
+    }
+    __syncthreads();
+    const unsigned long long ubase = s.base[0];
+    {
+      unsigned long long cl = ubase + (ex & M21);
+      unsigned long long clo = s.base[1] + ((ex >> 21) & M21);
+      unsigned long long cup = s.base[2] + ((ex >> 42) & M21);
+#pragma unroll
+      for (int j = 0; j < kDedupItems; ++j) {
+        if (!(fl[j] & 1u)) continue;
+        if (fl[j] & 2u) ++clo;
+        if (fl[j] & 4u) ++cup;
+        const unsigned long long u = cl++;
+        if (a.last) {
+          a.run_start[u] = (uint32_t)(i0 + j);
+          a.leaf_lower[u] = (uint32_t)(clo - 1);
+          a.leaf_upper[u] = (uint32_t)(cup - 1);
+        }
+        if (fl[j] & 8u) {
+          const uint32_t g = (uint32_t)shr64(kk[j], gsh);
+          if (g < (uint32_t)B) {
+            a.first[g] = (uint32_t)(u + 1);
+            a.first[B + g] = (uint32_t)clo;
+            a.first[2 * B + g] = (uint32_t)cup;
+          }
+        }
+      }
+    }
+    // merge every run of the tile: one 8-lane group per leaf head (warp-uniform
+    // loop); refinement runs are single slots, so a group takes four at once.
+    // Leaf bboxes accumulate per group in registers (heads arrive in grid
+    // order) and reach memory once per grid change.
+    constexpr int kU = OP == kRefine ? 4 : 1;
+    uint32_t acc_g = 0xFFFFFFFFu;
+    unsigned int acc_e = 0;
+    for (int kb = warp * 4; kb < nheads; kb += kU * (kThreads / 8)) {
+      uint64_t word[kU];
+      uint32_t gg[kU];
+      int32_t lcs[kU][3];
+      bool valid[kU];
+#pragma unroll
+      for (int r = 0; r < kU; ++r) {
+        const int k = kb + r * (kThreads / 8) + (lane >> 3);
+        valid[r] = k < nheads;
+        uint32_t s0 = 0, s1 = 0;
+        gg[r] = 0;
+        lcs[r][0] = lcs[r][1] = lcs[r][2] = 0;
+        if (valid[r]) {
+          s0 = s.head_pos[k];
+          s1 = (k + 1 < nheads) ? s.head_pos[k + 1] : s.tail_end;
+          decode_key(a.K, __ldcg(keys + s0), gg[r], lcs[r]);
+        }
+        word[r] = merge_run<OP>(a, vals, s0, s1, w);
+      }
+#pragma unroll
+      for (int r = 0; r < kU; ++r) {
+        const int k = kb + r * (kThreads / 8) + (lane >> 3);
+        const uint32_t g = gg[r];
+        if (a.last) {
+          uint32_t pop = __popcll(word[r]);
+#pragma unroll
+          for (int off = 1; off < 8; off <<= 1) pop += __shfl_xor_sync(0xffffffffu, pop, off);
+          int32_t mn[3], mx[3];
+          leaf_bounds(word[r], w, lane, mn, mx);
+          if (valid[r]) {
+            if (w < 6) {
+              const int ax = w < 3 ? w : w - 3;
+              const int32_t o = (int32_t)((uint32_t)lcs[r][ax] << 3);
+              const unsigned int e = w < 3 ? enc_min(o + mn[ax]) : enc_max(o + mx[ax]);
+              if (g != acc_g) {
+                if (acc_g != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * acc_g + w], acc_e);
+                acc_g = g;
+                acc_e = e;
+              } else {
+                acc_e = max(acc_e, e);
+              }
+            }
+            if (w == 0) {
+              s.head_pop[k] = pop;
+              s.head_g[k] = g;
+            }
+          }
+        } else if (valid[r]) {
+          const unsigned long long u = ubase + k;
+          a.out_masks[8 * u + w] = word[r];
+          if (w < 3) a.out_origins[3 * u + w] = (int32_t)((uint32_t)lcs[r][w] << 3);
+          if (w == 3) a.out_grid[u] = (int32_t)g;
+        }
+      }
+    }
+    if (a.last) {
+      // combine the groups' pending bboxes: one atomic per grid and axis bound
+      if (w < 6) s.grp_box[tid >> 3][w] = acc_e;
+      if (w == 0) s.grp_g[tid >> 3] = acc_g;
+    }
+    if (a.last) {
+      __syncthreads();
+      if (tid < 6) {
+        uint32_t cg = 0xFFFFFFFFu;
+        unsigned int ce = 0;
+        for (int j = 0; j < kThreads / 8; ++j) {
+          const uint32_t gj = s.grp_g[j];
+          if (gj == 0xFFFFFFFFu) continue;
+          const unsigned int ej = s.grp_box[j][tid];
+          if (gj == cg) {
+            ce = max(ce, ej);
+          } else {
+            if (cg != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * cg + tid], ce);
+            cg = gj;
+            ce = ej;
+          }
+        }
+        if (cg != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * cg + tid], ce);
+      }
+      // segmented voxel scan over the tile's leaves (segments start at each grid's first leaf)
+      uint32_t f = 0;
+      unsigned long long v = 0;
+#pragma unroll
+      for (int q = 0; q < kDedupItems; ++q) {
+        const int k = tid * kDedupItems + q;
+        if (k < nheads) {
+          if (s.head_fl[k] & 8u) {
+            f = 1;
+            v = s.head_pop[k];
+          } else {
+            v += s.head_pop[k];
+          }
+        }
+      }
+      uint32_t ef, tf;
+      unsigned long long ev, tv;
+      block_seg_scan_256(f, v, s.seg_f, s.seg_v, ef, ev, tf, tv);
+      if (warp == 3) {
+        lb64_publish(a.dedup_status + 3, 4, tile, tv, tf != 0);
+        const unsigned long long b = lb64_resolve(a.dedup_status + 3, 4, tile, tv, tf != 0, &a.rb->err);
+        if (lane == 0) s.base[3] = b;
+      }
+      __syncthreads();
+      const unsigned long long vbase = s.base[3];
+      uint32_t rf = ef;
+      unsigned long long rv = ev;
+#pragma unroll
+      for (int q = 0; q < kDedupItems; ++q) {
+        const int k = tid * kDedupItems + q;
+        if (k >= nheads) break;
+        const bool head = (s.head_fl[k] & 8u) != 0;
+        const unsigned long long off = head ? 0ull : rv + (rf ? 0ull : vbase);
+        const uint32_t pop = s.head_pop[k];
+        a.leaf_voff[ubase + k] = (long long)off;
+        const bool grid_last = (k + 1 < nheads) ? (s.head_fl[k + 1] & 8u) != 0 : s.tail_newgrid != 0;
+        if (grid_last) a.grid_vox[s.head_g[k]] = (long long)(off + pop);
+        if (head) {
+          rf = 1;
+          rv = pop;
+        } else {
+          rv += pop;
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // the last block: totals and per-grid offsets
+  stamp(a, 3);
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s.last = (atomicAdd(&a.ctl->dedup_ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+  __syncthreads();
+  if (!s.last) return;
+  __threadfence();
+  const unsigned long long U = __ldcg(&a.ctl->head_totals[0]);
+  const unsigned long long NL = __ldcg(&a.ctl->head_totals[1]);
+  const unsigned long long NU = __ldcg(&a.ctl->head_totals[2]);
+  __syncthreads();
+  if (tid == 0) {
+    a.rb->num_leaves = U;
+    a.rb->num_lowers = NL;
+    a.rb->num_uppers = NU;
+    if (a.last) a.run_start[U] = (uint32_t)S;
+  }
+  if (a.last) {
+    suffix_fill(a.first, B, U, a.leaf_off, sm);
+    suffix_fill(a.first + B, B, NL, a.lower_off, sm);
+    suffix_fill(a.first + 2 * B, B, NU, a.upper_off, sm);
+  }
+  stamp(a, 4);
+}
+
+// Phases: 1 emission, 2 digit passes, 3 dedup / merge / count, 4 per-grid offsets.
+template <int OP>
+__device__ void run_pass(const PassArgs& a, GridBarrier* bar, Smem& sm) {
+  unsigned int* err = &a.rb->err;
+  stamp(a, 0);
+  phase_emit<OP>(a, sm);
+  stamp(a, 1);
+  grid_sync(bar, err);
+  for (int d = 0; d < a.P; ++d) {
+    phase_sort(a, d, sm);
+    grid_sync(bar, err);
+  }
+  stamp(a, 2);
+  phase_dedup<OP>(a, sm);
+  if (!a.last) grid_sync(bar, err);
+}
+
+__global__ void __launch_bounds__(kThreads) k_chain(const __grid_constant__ ChainArgs c) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  for (int p = 0; p < c.n_pass; ++p) {
+    const PassArgs& a = c.pass[p];
+    switch (a.op) {
+      case kIjk: run_pass<kIjk>(a, c.bar, sm); break;
+      case kLeaves: run_pass<kLeaves>(a, c.bar, sm); break;
+      case kRefine: run_pass<kRefine>(a, c.bar, sm); break;
+      case kCoarsen: run_pass<kCoarsen>(a, c.bar, sm); break;
+      default: run_pass<kDilate>(a, c.bar, sm); break;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- final writer
+
+// After the readback: one 8-lane group per output leaf writes its record
+// (origin, merged mask, voxel offset, word prefix, bbox, grid, parent) and
+// node records at node heads; per-grid arrays by the first threads.
+template <int OP>
+__global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, const WriteOut o) {
+  const uint64_t* keys = a.keys[a.sorted];
+  const uint32_t* vals = a.vals[a.sorted];
+  const long long U = (long long)a.rb->num_leaves;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid & 7;
+  const long long gtid = (long long)blockIdx.x * kThreads + tid;
+  for (long long g = gtid; g <= a.B; g += (long long)gridDim.x * kThreads) {
+    o.leaf_offsets[g] = a.leaf_off[g];
+    o.lower_offsets[g] = a.lower_off[g];
+    o.upper_offsets[g] = a.upper_off[g];
+    if (g == a.B) break;
+    o.node_counts[3 * g + 0] = (int32_t)(a.upper_off[g + 1] - a.upper_off[g]);
+    o.node_counts[3 * g + 1] = (int32_t)(a.lower_off[g + 1] - a.lower_off[g]);
+    o.node_counts[3 * g + 2] = (int32_t)(a.leaf_off[g + 1] - a.leaf_off[g]);
+    o.voxel_counts[g] = a.grid_vox[g];
+#pragma unroll
+    for (int c = 0; c < 6; ++c) {
+      const unsigned int e = a.gbox[6 * g + c];
+      o.grid_bbox[6 * g + c] = c < 3 ? dec_min(e) : dec_max(e);
+    }
+  }
+  const long long groups = (long long)gridDim.x * (kThreads / 8);
+  for (long long ub = (long long)blockIdx.x * (kThreads / 8) + (tid >> 5) * 4; ub < U; ub += groups) {
+    const long long u = ub + (lane >> 3);
+    const bool valid = u < U;
+    uint32_t s0 = 0, s1 = 0, g = 0;
+    int32_t lc[3] = {0, 0, 0};
+    if (valid) {
+      s0 = a.run_start[u];
+      s1 = a.run_start[u + 1];
+      decode_key(a.K, keys[s0], g, lc);
+    }
+    const uint64_t word = merge_run<OP>(a, vals, s0, s1, w);
+    const uint32_t pop = __popcll(word);
+    uint32_t incl = pop;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off, 8);
+      if (w >= off) incl += y;
+    }
+    uint64_t wp = w ? ((uint64_t)(incl - pop) << (9 * (w - 1))) : 0ull;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) wp |= __shfl_xor_sync(0xffffffffu, wp, off);
+    int32_t mn[3], mx[3];
+    leaf_bounds(word, w, lane, mn, mx);
+    if (!valid) continue;
+    const int32_t org[3] = {(int32_t)((uint32_t)lc[0] << 3), (int32_t)((uint32_t)lc[1] << 3),
+                            (int32_t)((uint32_t)lc[2] << 3)};
+    o.masks[8 * u + w] = word;
+    if (w < 3) o.origins[3 * u + w] = org[w];
+    if (w < 6) o.leaf_bbox[6 * u + w] = w < 3 ? org[w] + mn[w] : org[w - 3] + mx[w - 3];
+    if (w == 6) o.word_prefix[u] = wp;
+    if (w == 7) o.leaf_grid[u] = (int32_t)g;
+    if (w == 0) o.voxel_offset[u] = a.leaf_voff[u];
+    if (w == 3) o.leaf_parent[u] = (int32_t)((long long)a.leaf_lower[u] - a.lower_off[g]);
+    if (w == 4) {
+      const uint32_t lw = a.leaf_lower[u];
+      if (u == 0 || a.leaf_lower[u - 1] != lw) {
+#pragma unroll
+        for (int c = 0; c < 3; ++c) o.lower_origins[3 * (long long)lw + c] = (int32_t)((uint32_t)org[c] & ~127u);
+        o.lower_parent[lw] = (int32_t)((long long)a.leaf_upper[u] - a.upper_off[g]);
+      }
+    }
+    if (w == 5) {
+      const uint32_t up = a.leaf_upper[u];
+      if (u == 0 || a.leaf_upper[u - 1] != up) {
+#pragma unroll
+        for (int c = 0; c < 3; ++c) o.upper_origins[3 * (long long)up + c] = (int32_t)((uint32_t)org[c] & ~4095u);
+      }
+    }
+  }
+}
+
+template <int OP>
+int write_occupancy() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_write_final<OP>, kThreads, 0) != cudaSuccess) n = 1;
+  return n > 0 ? n : 1;
+}
+
+}  // namespace
+
+size_t chain_smem_bytes() { return sizeof(Smem); }
+
+int chain_occupancy() {
+  int n = 0;
+  if (cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)) != cudaSuccess)
+    return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_chain, kThreads, sizeof(Smem)) != cudaSuccess) n = 1;
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch_chain(const ChainArgs& c, int blocks, cudaStream_t s) {
+  void* args[] = {(void*)&c};
+  return cudaLaunchCooperativeKernel((const void*)k_chain, dim3(blocks), dim3(kThreads), args, sizeof(Smem), s);
+}
+
+int write_final_occupancy(int op) {
+  switch (op) {
+    case kIjk: return write_occupancy<kIjk>();
+    case kLeaves: return write_occupancy<kLeaves>();
+    case kRefine: return write_occupancy<kRefine>();
+    case kCoarsen: return write_occupancy<kCoarsen>();
+    default: return write_occupancy<kDilate>();
+  }
+}
+
+cudaError_t launch_write_final(int op, const PassArgs& a, const WriteOut& o, int blocks, cudaStream_t s) {
+  switch (op) {
+    case kIjk: k_write_final<kIjk><<<blocks, kThreads, 0, s>>>(a, o); break;
+    case kLeaves: k_write_final<kLeaves><<<blocks, kThreads, 0, s>>>(a, o); break;
+    case kRefine: k_write_final<kRefine><<<blocks, kThreads, 0, s>>>(a, o); break;
+    case kCoarsen: k_write_final<kCoarsen><<<blocks, kThreads, 0, s>>>(a, o); break;
+    case kDilate: k_write_final<kDilate><<<blocks, kThreads, 0, s>>>(a, o); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace tb

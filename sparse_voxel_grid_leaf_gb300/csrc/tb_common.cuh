@@ -1,14 +1,14 @@
 // Shared definitions of the batched topology pass (host + device).
 //
 // The pass follows fVDB PR #757 ("Batched leaf-mask topology construction for
-// generated conv grids", Summary item 1): an emission kernel over all source
-// leaves of all grids writes candidate output-leaf slots, a segmented radix
-// sort puts them in canonical node order, a head-flag scan dedups them and
-// derives per-grid counts and parent linkage, one readback sizes the outputs,
-// and batched writers emit the leaf records.
+// generated conv grids", Summary item 1): an emission step over all source
+// leaves of all grids writes candidate output-leaf slots, a radix sort puts
+// them in canonical node order, a head-flag scan dedups them and derives
+// per-grid counts and parent linkage, one readback sizes the outputs, and a
+// batched writer emits the leaf records.
 //
 // Slots carry a 64-bit canonical key and a 32-bit source reference only; the
-// 512-bit output masks are recomputed from the source masks by the writer,
+// 512-bit output masks are recomputed from the source masks where needed,
 // which keeps the sort payload at 12 bytes per slot.
 #pragma once
 
@@ -19,15 +19,16 @@
 namespace tb {
 
 // Pass kinds.  kIjk and kLeaves are the front ends (one slot per input voxel
-// or input leaf); the other three are the topology ops of the chain.
+// or input leaf); the other three are the topology ops of a chain.
 enum PassOp : int32_t { kIjk = 0, kLeaves = 1, kRefine = 2, kCoarsen = 3, kDilate = 4 };
 
 constexpr int kBins = 256;            // 8-bit radix digits
 constexpr int kMaxDigitPasses = 8;    // 64-bit key
 constexpr int kSrcShift = 5;          // slot value = source index << 5 | target code
+constexpr int kMaxChainPasses = 6;    // passes per cooperative launch
 
 // Error bits reported through the readback header.
-constexpr uint32_t kErrTimeout = 1u;       // a bounded look-back wait gave up
+constexpr uint32_t kErrTimeout = 1u;       // a bounded wait (look-back or grid barrier) gave up
 constexpr uint32_t kErrBadOffsets = 2u;    // jagged offsets not monotone / not covering
 constexpr uint32_t kErrNotAligned = 4u;    // a leaf origin is not a multiple of 8
 constexpr uint32_t kErrNotCanonical = 8u;  // tb_validate: order or mask violation
@@ -37,30 +38,33 @@ constexpr uint32_t kErrSlotOverflow = 16u; // emission exceeded the host's bound
 constexpr uint32_t kFlagA32 = 1u << 30, kFlagP32 = 2u << 30, kVal32 = (1u << 30) - 1;
 constexpr uint64_t kFlagA64 = 1ull << 62, kFlagP64 = 2ull << 62, kSeg64 = 1ull << 61,
                    kVal64 = (1ull << 61) - 1;
-constexpr uint32_t kSpinLimit = 1u << 22;  // about 0.1-1 s of polling
+constexpr uint32_t kSpinLimit = 1u << 24;  // polls (with a short sleep) before a wait gives up
 
-// Compressed canonical sort key.  Field order from the most significant bit:
-// grid | tile x | tile y | tile z | upper x | upper y | upper z | lower x |
-// lower y | lower z, where for leaf coordinate lc = origin >> 3 the tile is
-// lc >> 9 (offset by the batch minimum), the upper child offset is
-// (lc >> 4) & 31 and the lower child offset is lc & 15.  Bits that are
-// constant over the batch's coordinate range are dropped; the order of the
-// remaining fields is the canonical order.
+// Compressed canonical sort key.  Canonical order is lexicographic over
+// (grid, T.x, T.y, T.z, U.x, U.y, U.z, V.x, V.y, V.z) where, for leaf
+// coordinate lc = origin >> 3 on an axis, T = lc >> 9 (root tile),
+// U = (lc >> 4) & 31 (child of the upper node), V = lc & 15 (child of the
+// lower node).  Given the batch's range [Lo, Hi] of lc per axis, each field is
+// stored relative to the smallest value it takes in its enclosing node:
+//   T' = T - T(Lo);   U' = U - (T == T(Lo) ? U(Lo) : 0);
+//   V' = V - (lc >> 4 == Lo >> 4 ? V(Lo) : 0).
+// U is only ever compared between keys with equal T (and V between keys with
+// equal T and U), so these per-node shifts keep the order while letting the
+// fields shrink to the bits the range needs.
 struct KeyLayout {
   int32_t W;             // total key width in bits (<= 64)
   int32_t gw, gshift;    // grid field
-  int32_t tile_base[3];  // minimum tile coordinate per axis
-  int32_t tw[3];         // tile field widths
-  int32_t uw[3];         // upper-offset field widths (0..5)
-  int32_t lwl[3];        // lower-offset field widths (0..4)
-  int32_t tshift[3], ushift[3], lshift[3];
-  int32_t lc_const[3];   // leaf-coordinate bits 0..8 that are constant and dropped
-  int32_t lower_bits;    // key >> lower_bits                 == (grid, tile, upper offset)
-  int32_t node_bits;     // key >> (lower_bits + upper bits)  == (grid, tile)
+  int32_t t_lo[3];       // T(Lo) per axis
+  int32_t u_lo[3];       // U(Lo)
+  int32_t v_lo[3];       // V(Lo)
+  int32_t tw[3], uw[3], vw[3];  // field widths
+  int32_t tshift[3], ushift[3], vshift[3];
+  int32_t lower_bits;    // key >> lower_bits == (grid, tile, upper child)
+  int32_t node_bits;     // key >> node_bits  == (grid, tile)
 };
 
-// Host-visible part of a pass's control block (read back in one copy,
-// followed by leaf/lower/upper offsets [B+1] each).
+// Host-visible block of a pass (read back in one copy):
+// header | leaf_off[B+1] | lower_off[B+1] | upper_off[B+1] | voxels[B] | gbox[B*6]
 struct ReadbackHeader {
   unsigned long long num_slots;
   unsigned long long num_leaves;
@@ -74,16 +78,17 @@ static_assert(sizeof(ReadbackHeader) == 64, "readback header layout");
 
 // Device-only counters and histograms of one pass (zeroed at call start).
 struct PassCtl {
-  unsigned int emit_ticket;
   unsigned int dedup_tile_ctr;
   unsigned int dedup_ticket;
-  unsigned int write_tile_ctr;
-  unsigned int write_ticket;
-  unsigned int pad[3];
+  unsigned int pad[6];
   unsigned int sort_tile_ctr[kMaxDigitPasses];
   unsigned long long head_totals[4];
   unsigned int hist[kMaxDigitPasses][kBins];
-  unsigned int bin_base[kMaxDigitPasses][kBins];
+};
+
+struct GridBarrier {
+  unsigned int count;
+  unsigned int gen;
 };
 
 // Order-preserving encodings for atomicMax-based min/max on zero-initialised
@@ -98,45 +103,58 @@ __host__ __device__ inline int32_t dec_min(unsigned int e) { return (int32_t)(~e
 
 struct PassArgs {
   KeyLayout K;
+  int32_t op;
   int32_t B;
   int32_t P;              // digit passes
+  int32_t last;           // 1: final pass (count phase), 0: intermediate (hands leaves on)
   int32_t lo[3], hi[3];   // box of a dilation pass
   // source
   const int32_t* ijk;            // kIjk: [N,3]
-  const int64_t* in_offsets;     // kIjk / kLeaves without leaf_grid: [B+1]
+  const int64_t* in_offsets;     // kIjk / kLeaves without src_grid: [B+1]
   const int32_t* src_origins;    // [L,3]
   const uint64_t* src_masks;     // [L,8]
   const int32_t* src_grid;       // [L] or null
   const unsigned long long* src_count_dev;  // device count (chained pass) or null
   long long src_count;                      // host count when src_count_dev is null
-  // control
+  // control (zeroed region)
   ReadbackHeader* rb;
   int64_t* leaf_off;   // [B+1]
   int64_t* lower_off;  // [B+1]
   int64_t* upper_off;  // [B+1]
+  int64_t* grid_vox;   // [B] voxels per grid
+  unsigned int* gbox;  // [B][6] encoded grid bbox accumulators
   PassCtl* ctl;
+  uint32_t* sort_status;             // [P][sort_tiles_cap][256]
+  long long sort_tiles_cap;
+  unsigned long long* dedup_status;  // [dedup_tiles_cap][4]: leaves, lower nodes, upper nodes, voxels
+  uint32_t* first;                   // [3][B]: 1 + first leaf / lower / upper index of each grid
   long long slot_cap;
-  // sort buffers
+  // slot buffers (not zeroed)
   uint64_t* keys[2];
   uint32_t* vals[2];
-  uint32_t* sort_status;   // [P][sort_tiles_cap][256]
-  long long sort_tiles_cap;
-  unsigned long long* dedup_status;  // [dedup_tiles_cap][3]
-  unsigned long long* write_status;  // [write_tiles_cap]
-  uint32_t* first;       // [3][B]: 1 + first leaf / lower / upper index of each grid
+  int32_t sorted;        // which keys/vals buffer holds the sorted slots
   uint32_t* run_start;   // [slot_cap + 1]
   uint32_t* leaf_lower;  // [slot_cap]
   uint32_t* leaf_upper;  // [slot_cap]
-  unsigned int* gbox;    // [B][6] encoded grid bbox accumulators
-  int32_t sorted;        // which keys/vals buffer holds the sorted slots
+  int64_t* leaf_voff;    // [slot_cap] voxel offset of each unique leaf (final pass)
+  unsigned long long* phase_ts;  // optional [8] globaltimer stamps (profiling), else null
+  // intermediate output (next pass's source)
+  int32_t* out_origins;
+  uint64_t* out_masks;
+  int32_t* out_grid;
 };
 
-// Outputs of a writer: the final batch arrays, or the next pass's source.
+struct ChainArgs {
+  int32_t n_pass;
+  GridBarrier* bar;
+  PassArgs pass[kMaxChainPasses];
+};
+
+// Outputs of the final writer.
 struct WriteOut {
   int32_t* origins;
   uint64_t* masks;
   int32_t* leaf_grid;
-  // final only
   int64_t* voxel_offset;
   uint64_t* word_prefix;
   int32_t* leaf_bbox;
@@ -151,6 +169,46 @@ struct WriteOut {
   int32_t* lower_parent;
   int32_t* upper_origins;
 };
+
+// ---------------------------------------------------------------- keys
+
+__host__ __device__ inline uint64_t shr64(uint64_t x, int s) { return s >= 64 ? 0ull : (x >> s); }
+
+__host__ __device__ inline uint64_t encode_key(const KeyLayout& K, uint32_t g, int32_t lcx, int32_t lcy,
+                                               int32_t lcz) {
+  const int32_t lc[3] = {lcx, lcy, lcz};
+  uint64_t key = K.gw ? ((uint64_t)g << K.gshift) : 0ull;
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    const int32_t T = lc[a] >> 9;
+    const uint32_t U = ((uint32_t)lc[a] >> 4) & 31u, V = (uint32_t)lc[a] & 15u;
+    const bool t0 = (T == K.t_lo[a]);
+    const bool b0 = t0 && (U == (uint32_t)K.u_lo[a]);
+    const uint32_t t = (uint32_t)(T - K.t_lo[a]);
+    const uint32_t u = U - (t0 ? (uint32_t)K.u_lo[a] : 0u);
+    const uint32_t v = V - (b0 ? (uint32_t)K.v_lo[a] : 0u);
+    if (K.tw[a]) key |= (uint64_t)t << K.tshift[a];
+    if (K.uw[a]) key |= (uint64_t)u << K.ushift[a];
+    if (K.vw[a]) key |= (uint64_t)v << K.vshift[a];
+  }
+  return key;
+}
+
+__host__ __device__ inline void decode_key(const KeyLayout& K, uint64_t key, uint32_t& g, int32_t lc[3]) {
+  g = K.gw ? (uint32_t)(key >> K.gshift) : 0u;
+#pragma unroll
+  for (int a = 0; a < 3; ++a) {
+    const uint32_t t = K.tw[a] ? (uint32_t)((key >> K.tshift[a]) & ((1ull << K.tw[a]) - 1ull)) : 0u;
+    const uint32_t u = K.uw[a] ? (uint32_t)(key >> K.ushift[a]) & ((1u << K.uw[a]) - 1u) : 0u;
+    const uint32_t v = K.vw[a] ? (uint32_t)(key >> K.vshift[a]) & ((1u << K.vw[a]) - 1u) : 0u;
+    const int32_t T = K.t_lo[a] + (int32_t)t;
+    const bool t0 = (t == 0);
+    const uint32_t U = u + (t0 ? (uint32_t)K.u_lo[a] : 0u);
+    const bool b0 = t0 && (U == (uint32_t)K.u_lo[a]);
+    const uint32_t V = v + (b0 ? (uint32_t)K.v_lo[a] : 0u);
+    lc[a] = (int32_t)(((uint32_t)T << 9) | (U << 4) | V);
+  }
+}
 
 #ifdef __CUDACC__
 
@@ -172,44 +230,22 @@ __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
 __device__ __forceinline__ void st_relaxed(uint32_t* p, uint32_t v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ void load_mask(const uint64_t* masks, long long i, uint64_t m[8]) {
   const uint4* p = reinterpret_cast<const uint4*>(masks + 8 * i);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    uint4 v = __ldg(p + q);
+    uint4 v = __ldcg(p + q);
     m[2 * q] = (uint64_t)v.x | ((uint64_t)v.y << 32);
     m[2 * q + 1] = (uint64_t)v.z | ((uint64_t)v.w << 32);
-  }
-}
-
-// ---------------------------------------------------------------- keys
-
-__device__ __forceinline__ uint64_t shr64(uint64_t x, int s) { return s >= 64 ? 0ull : (x >> s); }
-
-__device__ __forceinline__ uint64_t encode_key(const KeyLayout& K, uint32_t g, int32_t lcx, int32_t lcy,
-                                               int32_t lcz) {
-  const int32_t lc[3] = {lcx, lcy, lcz};
-  uint64_t key = K.gw ? ((uint64_t)g << K.gshift) : 0ull;
-#pragma unroll
-  for (int a = 0; a < 3; ++a) {
-    const uint32_t t = (uint32_t)((lc[a] >> 9) - K.tile_base[a]);
-    if (K.tw[a]) key |= (uint64_t)t << K.tshift[a];
-    key |= (uint64_t)(((uint32_t)lc[a] >> 4) & ((1u << K.uw[a]) - 1u)) << K.ushift[a];
-    key |= (uint64_t)((uint32_t)lc[a] & ((1u << K.lwl[a]) - 1u)) << K.lshift[a];
-  }
-  return key;
-}
-
-__device__ __forceinline__ void decode_key(const KeyLayout& K, uint64_t key, uint32_t& g, int32_t lc[3]) {
-  g = K.gw ? (uint32_t)(key >> K.gshift) : 0u;
-#pragma unroll
-  for (int a = 0; a < 3; ++a) {
-    const uint32_t t = K.tw[a] ? (uint32_t)((key >> K.tshift[a]) & ((1ull << K.tw[a]) - 1ull)) : 0u;
-    const uint32_t u = (uint32_t)(key >> K.ushift[a]) & ((1u << K.uw[a]) - 1u);
-    const uint32_t l = (uint32_t)(key >> K.lshift[a]) & ((1u << K.lwl[a]) - 1u);
-    const uint32_t tile = (uint32_t)K.tile_base[a] + t;
-    lc[a] = (int32_t)((tile << 9) | (uint32_t)K.lc_const[a] | (u << 4) | l);
   }
 }
 
@@ -272,7 +308,28 @@ __device__ __forceinline__ uint64_t dilate_y(uint64_t s, int ty, int lo, int hi)
   return s << 56;              // row 0 moves to row 7 of the previous leaf
 }
 
-// ---------------------------------------------------------------- scans and look-back
+// OR-reduce-scatter over an aligned group of 8 lanes: lane w of the group
+// returns the OR over the group's lanes of c[w].
+__device__ __forceinline__ uint64_t reduce_scatter8(const uint64_t c[8], int w) {
+  uint64_t k4[4], k2[2];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint64_t send = (w & 4) ? c[k] : c[k + 4];
+    const uint64_t recv = __shfl_xor_sync(0xffffffffu, send, 4);
+    k4[k] = ((w & 4) ? c[k + 4] : c[k]) | recv;
+  }
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const uint64_t send = (w & 2) ? k4[k] : k4[k + 2];
+    const uint64_t recv = __shfl_xor_sync(0xffffffffu, send, 2);
+    k2[k] = ((w & 2) ? k4[k + 2] : k4[k]) | recv;
+  }
+  const uint64_t send = (w & 1) ? k2[0] : k2[1];
+  const uint64_t recv = __shfl_xor_sync(0xffffffffu, send, 1);
+  return ((w & 1) ? k2[1] : k2[0]) | recv;
+}
+
+// ---------------------------------------------------------------- scans, look-back, barrier
 
 // Exclusive scan over a 256-thread block; returns the thread's exclusive
 // prefix and writes the block total to *total.  `scratch` holds 8 words.
@@ -299,11 +356,10 @@ __device__ __forceinline__ T block_excl_scan_256(T v, T* scratch, T* total) {
   return warp_base + incl - v;
 }
 
-// Decoupled look-back over 32-bit status words (one per tile).  Publishes
-// the tile's aggregate, accumulates predecessors until an inclusive prefix is
-// found, then publishes the tile's inclusive prefix.  Returns the exclusive
-// prefix.  A wait on a tile that never publishes ends after kSpinLimit polls
-// with kErrTimeout set.
+// Decoupled look-back over 32-bit status words (one thread per digit): publish
+// the tile's aggregate, add predecessors until an inclusive prefix is found,
+// publish the inclusive prefix.  Returns the exclusive prefix.  A wait on a
+// tile that never publishes ends after kSpinLimit polls with kErrTimeout set.
 __device__ __forceinline__ uint32_t lookback32(uint32_t* status, long long stride, long long tile,
                                                uint32_t agg, unsigned int* err) {
   if (tile == 0) {
@@ -333,48 +389,127 @@ __device__ __forceinline__ uint32_t lookback32(uint32_t* status, long long strid
   return excl;
 }
 
-// Same on 64-bit words; with `seg` the scan is segmented: an aggregate that
-// contains a segment head stops the walk (its value is the sum since that head).
-__device__ __forceinline__ uint64_t lookback64(unsigned long long* status, long long stride, long long tile,
-                                               uint64_t agg, bool has_head, unsigned int* err) {
-  const uint64_t seg = has_head ? kSeg64 : 0ull;
-  if (tile == 0) {
-    st_relaxed(status, kFlagP64 | agg);
-    return 0;
-  }
-  st_relaxed(status + tile * stride, kFlagA64 | seg | agg);
+// Warp-wide decoupled look-back over 64-bit status words, in two steps so a
+// tile can publish its aggregate early and resolve its prefix later.
+// lb64_publish: lane 0 stores the tile's aggregate (with the segment flag when
+// the tile holds a segment head).  lb64_resolve (a whole warp; lanes inspect
+// 32 predecessors at once) adds predecessor values until an inclusive prefix
+// -- or, for a segmented scan, an aggregate holding a segment head -- ends the
+// walk, publishes the tile's inclusive prefix and returns the exclusive prefix
+// in every lane.  A wait on a tile that never publishes ends after kSpinLimit
+// polls with kErrTimeout set.
+__device__ __forceinline__ void lb64_publish(unsigned long long* status, long long stride, long long tile,
+                                             uint64_t agg, bool has_head) {
+  if ((threadIdx.x & 31) == 0)
+    st_relaxed(status + tile * stride, (tile == 0 ? kFlagP64 : (kFlagA64 | (has_head ? kSeg64 : 0ull))) | agg);
+}
+
+__device__ __forceinline__ uint64_t lb64_resolve(unsigned long long* status, long long stride, long long tile,
+                                                 uint64_t agg, bool has_head, unsigned int* err) {
+  const int lane = threadIdx.x & 31;
+  if (tile == 0) return 0;
   uint64_t excl = 0;
-  long long t = tile - 1;
+  long long base = tile - 1;  // window covers tiles base, base-1, ..., base-31
   uint32_t spins = 0;
-  while (t >= 0) {
-    const uint64_t w = ld_relaxed(status + t * stride);
-    const uint64_t f = w & (3ull << 62);
-    if (f == 0) {
+  while (base >= 0) {
+    const long long t = base - lane;
+    const uint64_t w = t >= 0 ? ld_relaxed(status + t * stride) : kFlagP64;  // before tile 0: an empty prefix
+    const bool ready = (w >> 62) != 0;
+    const bool stop = ((w >> 62) == 2) || (w & kSeg64);
+    const uint32_t stop_mask = __ballot_sync(0xffffffffu, ready && stop);
+    const uint32_t ready_mask = __ballot_sync(0xffffffffu, ready);
+    const int first_stop = stop_mask ? __ffs(stop_mask) - 1 : 32;
+    const uint32_t need = first_stop == 32 ? 0xffffffffu : ((2u << first_stop) - 1u);
+    if ((ready_mask & need) != need) {
       if (++spins > kSpinLimit) {
-        atomicOr(err, kErrTimeout);
+        if (lane == 0) atomicOr(err, kErrTimeout);
         break;
       }
       __nanosleep(32);
       continue;
     }
-    excl += w & kVal64;
-    if (f == kFlagP64 || (w & kSeg64)) break;
-    --t;
+    uint64_t v = (lane <= first_stop && t >= 0) ? (w & kVal64) : 0ull;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    excl += v;
+    if (first_stop < 32) break;
+    base -= 32;
   }
-  st_relaxed(status + tile * stride, kFlagP64 | (has_head ? agg : excl + agg));
+  if (lane == 0) st_relaxed(status + tile * stride, kFlagP64 | (has_head ? agg : excl + agg));
   return excl;
 }
 
-// "Last block done": returns true in exactly one block, after every other
-// block of the grid has passed this point (its prior writes made visible).
-__device__ __forceinline__ bool last_block_done(unsigned int* ticket) {
-  __shared__ unsigned int s_last;
-  __threadfence();
+// Segmented exclusive scan over a 256-thread block of (head flag f, value v)
+// pairs in thread order; a set flag starts a new segment.  Returns the
+// thread's exclusive (flag, sum since the last head) and the block aggregate.
+// `scratch_f` / `scratch_v` hold 8 entries.
+__device__ __forceinline__ void block_seg_scan_256(uint32_t f, unsigned long long v, uint32_t* scratch_f,
+                                                   unsigned long long* scratch_v, uint32_t& ef,
+                                                   unsigned long long& ev, uint32_t& tf, unsigned long long& tv) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t F = f;
+  unsigned long long V = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t F2 = __shfl_up_sync(0xffffffffu, F, off);
+    const unsigned long long V2 = __shfl_up_sync(0xffffffffu, V, off);
+    if (lane >= off) {
+      if (!F) V += V2;
+      F |= F2;
+    }
+  }
+  uint32_t lf = __shfl_up_sync(0xffffffffu, F, 1);
+  unsigned long long lv = __shfl_up_sync(0xffffffffu, V, 1);
+  if (lane == 0) {
+    lf = 0;
+    lv = 0;
+  }
+  if (lane == 31) {
+    scratch_f[warp] = F;
+    scratch_v[warp] = V;
+  }
   __syncthreads();
-  if (threadIdx.x == 0) s_last = (atomicAdd(ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
+  uint32_t pf = 0;
+  unsigned long long pv = 0;
+  tf = 0;
+  tv = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const uint32_t wf = scratch_f[w];
+    const unsigned long long wv = scratch_v[w];
+    if (w < warp) {
+      pv = wf ? wv : pv + wv;
+      pf |= wf;
+    }
+    tv = wf ? wv : tv + wv;
+    tf |= wf;
+  }
   __syncthreads();
-  if (s_last) __threadfence();
-  return s_last != 0;
+  ef = pf | lf;
+  ev = lf ? lv : pv + lv;
+}
+
+// Software grid barrier for a cooperative launch (all blocks co-resident):
+// a monotone arrival counter; barrier n completes when the counter reaches
+// n * gridDim.x.  The wait gives up after kSpinLimit polls with kErrTimeout
+// set, so a broken barrier ends the kernel instead of hanging it.
+__device__ __forceinline__ void grid_sync(GridBarrier* bar, unsigned int* err) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned int old = atomicAdd(&bar->count, 1u);
+    const unsigned int target = (old / gridDim.x + 1) * gridDim.x;
+    uint32_t spins = 0;
+    while ((int)(ld_relaxed(&bar->count) - target) < 0) {
+      if (++spins > kSpinLimit) {
+        atomicOr(err, kErrTimeout);
+        break;
+      }
+      if (spins > 256) __nanosleep(32);
+    }
+    __threadfence();
+  }
+  __syncthreads();
 }
 
 #endif  // __CUDACC__

@@ -7,36 +7,36 @@
 
 namespace tb {
 
-constexpr int kSortThreads = 256;
 constexpr int kSortItems = 8;
-constexpr int kSortTile = kSortThreads * kSortItems;   // slots per digit-pass tile
-constexpr int kDedupThreads = 256;
+constexpr int kSortTile = 256 * kSortItems;   // slots per digit-pass tile
 constexpr int kDedupItems = 4;
-constexpr int kDedupTile = kDedupThreads * kDedupItems;
-constexpr int kWriteThreads = 256;                      // 8 lanes per leaf
-constexpr int kWriteRows = 4;
-constexpr int kWriteTile = (kWriteThreads / 8) * kWriteRows;  // leaves per writer tile
+constexpr int kDedupTile = 256 * kDedupItems;  // slots per dedup tile
+constexpr int kWriteLeavesPerBlock = 32;       // 8 lanes per leaf, 256 threads
 
-cudaError_t launch_emit(int op, const PassArgs& a, int blocks, cudaStream_t s);
+// Bytes of a pass's readback block for B grids:
+// header | leaf_off[B+1] | lower_off[B+1] | upper_off[B+1] | voxels[B] | gbox[6B]
+inline size_t readback_bytes(int32_t B) {
+  return sizeof(ReadbackHeader) + 3 * sizeof(int64_t) * (size_t)(B + 1) + sizeof(int64_t) * (size_t)B +
+         6 * sizeof(unsigned int) * (size_t)B;
+}
+
 cudaError_t launch_prepass_ijk(const int32_t* ijk, long long N, const int64_t* off, int32_t B,
                                ReadbackHeader* rb, int blocks, cudaStream_t s);
 cudaError_t launch_prepass_leaves(const int32_t* origins, const uint64_t* masks, long long L,
                                   const int64_t* off, int32_t B, ReadbackHeader* rb, int blocks,
                                   cudaStream_t s);
-cudaError_t launch_sort_pass(const PassArgs& a, int pass, int blocks, cudaStream_t s);
-cudaError_t launch_dedup(const PassArgs& a, int blocks, cudaStream_t s);
-cudaError_t launch_write(int op, bool final_pass, const PassArgs& a, const WriteOut& o, int blocks,
-                         cudaStream_t s);
 cudaError_t launch_validate(const int32_t* origins, const uint64_t* masks, const int32_t* leaf_grid,
                             const int64_t* leaf_offsets, long long L, int32_t B, unsigned int* err,
                             int blocks, cudaStream_t s);
 
+// The cooperative pass kernel (all blocks co-resident) and the final writer.
+size_t chain_smem_bytes();
+int chain_occupancy();
+cudaError_t launch_chain(const ChainArgs& c, int blocks, cudaStream_t s);
+int write_final_occupancy(int op);
+cudaError_t launch_write_final(int op, const PassArgs& a, const WriteOut& o, int blocks, cudaStream_t s);
+
 // Sets the calling thread's tb_last_error() message.
 void set_error_message(const char* msg);
-
-// Occupancy-derived resident block counts (per SM) of the persistent kernels.
-int occupancy_sort();
-int occupancy_dedup();
-int occupancy_write(int op, bool final_pass);
 
 }  // namespace tb

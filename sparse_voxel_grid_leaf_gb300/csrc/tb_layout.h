@@ -24,28 +24,33 @@ inline int64_t floor_div(int64_t a, int64_t b) {
   return q;
 }
 
-// Key layout for B grids whose voxels lie in the bbox bb (min xyz, max xyz).
-// Returns false if the key needs more than 64 bits.
+inline int64_t floor_mod(int64_t a, int64_t b) { return a - b * floor_div(a, b); }
+
+// Key layout for B grids whose voxels lie in the bbox bb (min xyz, max xyz);
+// see KeyLayout for the per-node shifted fields.  Returns false if the key
+// needs more than 64 bits.
 inline bool make_layout(int32_t B, const int32_t bb[6], bool empty, KeyLayout& K) {
   std::memset(&K, 0, sizeof K);
   K.gw = B > 1 ? bitwidth((uint64_t)(B - 1)) : 0;
-  for (int a = 0; a < 3; ++a) {
-    int lw = 0;
-    if (!empty) {
-      const int64_t Lo = floor_div(bb[a], 8), Hi = floor_div(bb[3 + a], 8);
-      const int64_t tlo = floor_div(Lo, 512), thi = floor_div(Hi, 512);
-      K.tile_base[a] = (int32_t)tlo;
-      K.tw[a] = bitwidth((uint64_t)(thi - tlo));
-      lw = (thi > tlo) ? 9 : std::min(9, bitwidth((uint64_t)(Lo ^ Hi)));
-      K.lc_const[a] = (int32_t)(Lo & 0x1FF & ~((1 << lw) - 1));
-    }
-    K.lwl[a] = std::min(lw, 4);
-    K.uw[a] = std::max(lw - 4, 0);
+  for (int a = 0; a < 3 && !empty; ++a) {
+    const int64_t Lo = floor_div(bb[a], 8), Hi = floor_div(bb[3 + a], 8);  // leaf coordinates
+    const int64_t Tlo = floor_div(Lo, 512), Thi = floor_div(Hi, 512);
+    const int64_t Ulo = floor_mod(floor_div(Lo, 16), 32), Uhi = floor_mod(floor_div(Hi, 16), 32);
+    const int64_t Blo = floor_div(Lo, 16), Bhi = floor_div(Hi, 16);     // lower-node blocks
+    const int64_t Vlo = floor_mod(Lo, 16), Vhi = floor_mod(Hi, 16);
+    K.t_lo[a] = (int32_t)Tlo;
+    K.u_lo[a] = (int32_t)Ulo;
+    K.v_lo[a] = (int32_t)Vlo;
+    K.tw[a] = bitwidth((uint64_t)(Thi - Tlo));
+    const int64_t umax = (Thi == Tlo) ? Uhi - Ulo : std::max<int64_t>(31 - Ulo, Thi - Tlo >= 2 ? 31 : Uhi);
+    const int64_t vmax = (Bhi == Blo) ? Vhi - Vlo : std::max<int64_t>(15 - Vlo, Bhi - Blo >= 2 ? 15 : Vhi);
+    K.uw[a] = bitwidth((uint64_t)umax);
+    K.vw[a] = bitwidth((uint64_t)vmax);
   }
-  K.lshift[2] = 0;
-  K.lshift[1] = K.lwl[2];
-  K.lshift[0] = K.lwl[2] + K.lwl[1];
-  K.lower_bits = K.lwl[0] + K.lwl[1] + K.lwl[2];
+  K.vshift[2] = 0;
+  K.vshift[1] = K.vw[2];
+  K.vshift[0] = K.vw[2] + K.vw[1];
+  K.lower_bits = K.vw[0] + K.vw[1] + K.vw[2];
   K.ushift[2] = K.lower_bits;
   K.ushift[1] = K.ushift[2] + K.uw[2];
   K.ushift[0] = K.ushift[1] + K.uw[1];

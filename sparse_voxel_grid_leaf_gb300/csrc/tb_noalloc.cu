@@ -18,6 +18,7 @@
 // Every call reuses the array, whose contents persist between calls: the
 // control region is cleared at the start of each call, and calls that
 // overlap on the GPU (other streams, other threads) race on it.
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -94,9 +95,8 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   TB_STATIC_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
 
   // ---- coordinate range of the input (the key layout depends on it)
-  const size_t rb_bytes = sizeof(ReadbackHeader) + 3 * sizeof(int64_t) * (size_t)(B + 1);
   ReadbackHeader* rb0 = (ReadbackHeader*)scratch;
-  if (align256(rb_bytes) > kStaticScratchBytes)
+  if (readback_bytes(B) + 4096 + sizeof(PassCtl) > kStaticScratchBytes)
     return static_fail(TB_ERR_TOO_LARGE, "tb_refine_static: too many grids for the static scratch");
   TB_STATIC_CUDA(cudaMemsetAsync(rb0, 0, sizeof(ReadbackHeader), stream));
   TB_STATIC_CUDA(launch_prepass_leaves(origins, masks, L, leaf_offsets, B, rb0,
@@ -129,27 +129,28 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   const long long S = 8 * L;
   const long long sort_tiles = std::max(1ll, (S + kSortTile - 1) / kSortTile);
   const long long dedup_tiles = std::max(1ll, (S + kDedupTile - 1) / kDedupTile);
-  const long long write_tiles = std::max(1ll, (S + kWriteTile - 1) / kWriteTile);
-  size_t off = align256(rb_bytes);  // the prepass header stays at offset 0
+  const size_t rbb = readback_bytes(B);
+  size_t off = 256;  // the prepass header stays at offset 0
   auto take = [&](size_t n) {
     const size_t r = off;
     off = align256(off + n);
     return r;
   };
-  const size_t o_rb = take(rb_bytes), o_ctl = take(sizeof(PassCtl)),
-               o_sort = take((size_t)a.P * sort_tiles * kBins * 4), o_dedup = take((size_t)dedup_tiles * 24),
-               o_write = take((size_t)write_tiles * 8), o_first = take((size_t)3 * B * 4),
-               o_gbox = take((size_t)6 * B * 4);
-  const size_t zero_begin = o_rb, zero_end = off;
+  const size_t o_bar = take(sizeof(GridBarrier)), o_rb = take(rbb), o_ctl = take(sizeof(PassCtl)),
+               o_sort = take((size_t)a.P * sort_tiles * kBins * 4), o_dedup = take((size_t)dedup_tiles * 32),
+               o_first = take((size_t)3 * B * 4);
+  const size_t zero_begin = o_bar, zero_end = off;
   const size_t o_k0 = take((size_t)S * 8), o_k1 = take((size_t)S * 8), o_v0 = take((size_t)S * 4),
                o_v1 = take((size_t)S * 4), o_run = take((size_t)(S + 1) * 4), o_ll = take((size_t)S * 4),
-               o_lu = take((size_t)S * 4);
+               o_lu = take((size_t)S * 4), o_voff = take((size_t)S * 8);
   if (off > kStaticScratchBytes)
     return static_fail(TB_ERR_TOO_LARGE,
-                       "tb_refine_static: input needs more than the 32 MiB static scratch (about 100k leaves)");
+                       "tb_refine_static: input needs more than the 32 MiB static scratch (about 90k leaves)");
   TB_STATIC_CUDA(cudaMemsetAsync(scratch + zero_begin, 0, zero_end - zero_begin, stream));
 
+  a.op = kRefine;
   a.B = B;
+  a.last = 1;
   a.src_origins = origins;
   a.src_masks = masks;
   a.src_grid = nullptr;
@@ -159,28 +160,32 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   a.leaf_off = (int64_t*)(scratch + o_rb + sizeof(ReadbackHeader));
   a.lower_off = a.leaf_off + (B + 1);
   a.upper_off = a.lower_off + (B + 1);
+  a.grid_vox = a.upper_off + (B + 1);
+  a.gbox = (unsigned int*)(a.grid_vox + B);
   a.ctl = (PassCtl*)(scratch + o_ctl);
+  a.sort_status = (uint32_t*)(scratch + o_sort);
+  a.sort_tiles_cap = sort_tiles;
+  a.dedup_status = (unsigned long long*)(scratch + o_dedup);
+  a.first = (uint32_t*)(scratch + o_first);
   a.slot_cap = S;
   a.keys[0] = (uint64_t*)(scratch + o_k0);
   a.keys[1] = (uint64_t*)(scratch + o_k1);
   a.vals[0] = (uint32_t*)(scratch + o_v0);
   a.vals[1] = (uint32_t*)(scratch + o_v1);
-  a.sort_status = (uint32_t*)(scratch + o_sort);
-  a.sort_tiles_cap = sort_tiles;
-  a.dedup_status = (unsigned long long*)(scratch + o_dedup);
-  a.write_status = (unsigned long long*)(scratch + o_write);
-  a.first = (uint32_t*)(scratch + o_first);
-  a.gbox = (unsigned int*)(scratch + o_gbox);
+  a.sorted = a.P & 1;
   a.run_start = (uint32_t*)(scratch + o_run);
   a.leaf_lower = (uint32_t*)(scratch + o_ll);
   a.leaf_upper = (uint32_t*)(scratch + o_lu);
+  a.leaf_voff = (int64_t*)(scratch + o_voff);
 
-  // ---- emission, sort, dedup (same kernels as tb_refine)
-  TB_STATIC_CUDA(launch_emit(kRefine, a, blocks_of(L, 256, (long long)sms * 8), stream));
-  const int sb = blocks_of(sort_tiles, 1, (long long)sms * occupancy_sort());
-  for (int d = 0; d < a.P; ++d) TB_STATIC_CUDA(launch_sort_pass(a, d, sb, stream));
-  a.sorted = a.P & 1;
-  TB_STATIC_CUDA(launch_dedup(a, blocks_of(dedup_tiles, 1, (long long)sms * occupancy_dedup()), stream));
+  // ---- the same cooperative pass kernel as tb_refine
+  ChainArgs ca;
+  std::memset(&ca, 0, sizeof ca);
+  ca.n_pass = 1;
+  ca.bar = (GridBarrier*)(scratch + o_bar);
+  ca.pass[0] = a;
+  const long long work = std::max({(L + 255) / 256, sort_tiles, dedup_tiles, 1ll});
+  TB_STATIC_CUDA(launch_chain(ca, blocks_of(work, 1, (long long)sms * chain_occupancy()), stream));
   ReadbackHeader r;
   TB_STATIC_CUDA(cudaMemcpyAsync(&r, a.rb, sizeof r, cudaMemcpyDeviceToHost, stream));
   TB_STATIC_CUDA(cudaStreamSynchronize(stream));
@@ -220,8 +225,9 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   o.lower_origins = out->lower_origins;
   o.lower_parent = out->lower_parent;
   o.upper_origins = out->upper_origins;
-  const int wb = blocks_of((long long)r.num_leaves, kWriteTile, (long long)sms * occupancy_write(kRefine, true));
-  TB_STATIC_CUDA(launch_write(kRefine, true, a, o, wb, stream));
+  const int wb = blocks_of(std::max<long long>((long long)r.num_leaves, B + 1), kWriteLeavesPerBlock,
+                           (long long)sms * write_final_occupancy(kRefine));
+  TB_STATIC_CUDA(launch_write_final(kRefine, a, o, wb, stream));
   return TB_OK;
 }
 

@@ -1,0 +1,163 @@
+// Front-end range prepasses and the canonical-batch validator.
+//
+// The ijk and leaf front ends (fVDB PR #757 "Batched leaf-mask topology
+// construction for generated conv grids", Follow-ups paragraph) first read
+// the input's voxel bounding box, which sizes the sort key, and check the
+// jagged offsets; tb_validate checks the invariants every produced batch
+// satisfies (canonical order per grid, non-zero masks, aligned origins).
+#include "tb_common.cuh"
+#include "tb_launch.h"
+
+namespace tb {
+
+namespace {
+
+// ---------------------------------------------------------------- front-end prepasses
+
+__device__ void reduce_bbox(const int32_t mn[3], const int32_t mx[3], unsigned int* enc) {
+  // block-level reduction of the encoded bounds, then one atomic per block
+  __shared__ unsigned int s_enc[6];
+  if (threadIdx.x < 6) s_enc[threadIdx.x] = 0;
+  __syncthreads();
+  unsigned int e[6] = {enc_min(mn[0]), enc_min(mn[1]), enc_min(mn[2]), enc_max(mx[0]), enc_max(mx[1]),
+                       enc_max(mx[2])};
+#pragma unroll
+  for (int k = 0; k < 6; ++k) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) e[k] = max(e[k], __shfl_xor_sync(0xffffffffu, e[k], off));
+  }
+  if ((threadIdx.x & 31) == 0)
+#pragma unroll
+    for (int k = 0; k < 6; ++k) atomicMax(&s_enc[k], e[k]);
+  __syncthreads();
+  if (threadIdx.x < 6 && s_enc[threadIdx.x]) atomicMax(&enc[threadIdx.x], s_enc[threadIdx.x]);
+}
+
+__device__ void check_offsets(const int64_t* off, int32_t B, long long n, unsigned int* err) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g <= B; g += stride) {
+    const int64_t v = off[g];
+    bool bad = (g == 0 && v != 0) || (g == B && v != n) || v < 0 || v > n;
+    if (g > 0 && off[g - 1] > v) bad = true;
+    if (bad) atomicOr(err, kErrBadOffsets);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_prepass_ijk(const int32_t* ijk, long long N, const int64_t* off,
+                                                     int32_t B, ReadbackHeader* rb) {
+  int32_t mn[3] = {INT32_MAX, INT32_MAX, INT32_MAX}, mx[3] = {INT32_MIN, INT32_MIN, INT32_MIN};
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += stride)
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      const int32_t v = __ldg(ijk + 3 * i + a);
+      mn[a] = min(mn[a], v);
+      mx[a] = max(mx[a], v);
+    }
+  reduce_bbox(mn, mx, rb->bbox_enc);
+  check_offsets(off, B, N, &rb->err);
+}
+
+// Exact voxel bbox of a leaf list (from the set bits), plus origin alignment.
+__global__ void __launch_bounds__(256) k_prepass_leaves(const int32_t* origins, const uint64_t* masks,
+                                                        long long L, const int64_t* off, int32_t B,
+                                                        ReadbackHeader* rb) {
+  int32_t mn[3] = {INT32_MAX, INT32_MAX, INT32_MAX}, mx[3] = {INT32_MIN, INT32_MIN, INT32_MIN};
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < L; i += stride) {
+    uint64_t m[8];
+    load_mask(masks, i, m);
+    uint64_t all = 0;
+    uint32_t xbits = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      all |= m[w];
+      if (m[w]) xbits |= 1u << w;
+    }
+    const int32_t o[3] = {__ldg(origins + 3 * i), __ldg(origins + 3 * i + 1), __ldg(origins + 3 * i + 2)};
+    if ((o[0] | o[1] | o[2]) & 7) atomicOr(&rb->err, kErrNotAligned);
+    if (!all) continue;
+    uint32_t ybits = 0;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if ((all >> (8 * r)) & 0xFFull) ybits |= 1u << r;
+    uint64_t z = all | (all >> 32);
+    z |= z >> 16;
+    z |= z >> 8;
+    const uint32_t zbits = (uint32_t)(z & 0xFFull);
+    const uint32_t b[3] = {xbits, ybits, zbits};
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      mn[a] = min(mn[a], o[a] + (__ffs(b[a]) - 1));
+      mx[a] = max(mx[a], o[a] + (31 - __clz(b[a])));
+    }
+  }
+  reduce_bbox(mn, mx, rb->bbox_enc);
+  check_offsets(off, B, L, &rb->err);
+}
+
+// Canonical-order comparison of two leaf origins: signed tile, then x-major
+// upper child offset, then x-major lower child offset.
+__device__ __forceinline__ bool canon_less(const int32_t a[3], const int32_t b[3]) {
+#pragma unroll
+  for (int ax = 0; ax < 3; ++ax)
+    if ((a[ax] >> 12) != (b[ax] >> 12)) return (a[ax] >> 12) < (b[ax] >> 12);
+#pragma unroll
+  for (int ax = 0; ax < 3; ++ax)
+    if (((a[ax] >> 7) & 31) != ((b[ax] >> 7) & 31)) return ((a[ax] >> 7) & 31) < ((b[ax] >> 7) & 31);
+#pragma unroll
+  for (int ax = 0; ax < 3; ++ax)
+    if (((a[ax] >> 3) & 15) != ((b[ax] >> 3) & 15)) return ((a[ax] >> 3) & 15) < ((b[ax] >> 3) & 15);
+  return false;
+}
+
+__global__ void __launch_bounds__(256) k_validate(const int32_t* origins, const uint64_t* masks,
+                                                  const int32_t* leaf_grid, const int64_t* off, long long L,
+                                                  int32_t B, unsigned int* err) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g <= B; g += stride) {
+    const int64_t v = off[g];
+    if ((g == 0 && v != 0) || (g == B && v != L) || (g > 0 && off[g - 1] > v)) atomicOr(err, kErrNotCanonical);
+  }
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < L; i += stride) {
+    const int32_t o[3] = {origins[3 * i], origins[3 * i + 1], origins[3 * i + 2]};
+    bool bad = ((o[0] | o[1] | o[2]) & 7) != 0;
+    uint64_t m[8];
+    load_mask(masks, i, m);
+    uint64_t any = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) any |= m[w];
+    bad |= (any == 0);
+    const int32_t g = leaf_grid[i];
+    if (g < 0 || g >= B || i < off[g] || i >= off[g + 1]) {
+      bad = true;
+    } else if (i > off[g]) {
+      const int32_t p[3] = {origins[3 * i - 3], origins[3 * i - 2], origins[3 * i - 1]};
+      if (!canon_less(p, o)) bad = true;
+    }
+    if (bad) atomicOr(err, kErrNotCanonical);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prepass_ijk(const int32_t* ijk, long long N, const int64_t* off, int32_t B,
+                               ReadbackHeader* rb, int blocks, cudaStream_t s) {
+  k_prepass_ijk<<<blocks, 256, 0, s>>>(ijk, N, off, B, rb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prepass_leaves(const int32_t* origins, const uint64_t* masks, long long L, const int64_t* off,
+                                  int32_t B, ReadbackHeader* rb, int blocks, cudaStream_t s) {
+  k_prepass_leaves<<<blocks, 256, 0, s>>>(origins, masks, L, off, B, rb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_validate(const int32_t* origins, const uint64_t* masks, const int32_t* leaf_grid,
+                            const int64_t* leaf_offsets, long long L, int32_t B, unsigned int* err, int blocks,
+                            cudaStream_t s) {
+  k_validate<<<blocks, 256, 0, s>>>(origins, masks, leaf_grid, leaf_offsets, L, B, err);
+  return cudaGetLastError();
+}
+
+}  // namespace tb
