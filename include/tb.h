@@ -247,8 +247,8 @@ typedef struct tb_out_buffers {
  *   out_counts: optional host int64[3] receiving the output's leaf, lower-node
  *   and upper-node totals (also written when the capacity check fails).
  * Scratch is one static device array of 32 MiB that every GPU loading the
- * library holds until the process exits; about 44 bytes per candidate leaf
- * (8 per input leaf) plus per-grid control, so inputs of up to roughly 90k
+ * library holds until the process exits; about 52 bytes per candidate leaf
+ * (8 per input leaf) plus per-grid control, so inputs of up to roughly 75k
  * leaves fit.  Larger inputs, or outputs beyond the given capacities, return
  * TB_ERR_TOO_LARGE before anything is written.  The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress); make it before

@@ -407,7 +407,7 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     pl.rb = c.take(rb_bytes);
     pl.ctl = c.take(sizeof(PassCtl));
     pl.sort_status = c.take((size_t)pl.P * pl.sort_tiles * kBins * 4);
-    pl.dedup_status = c.take((size_t)pl.dedup_tiles * 4 * 8);
+    pl.dedup_status = c.take((size_t)pl.dedup_tiles * 3 * 8);
     pl.first = c.take((size_t)3 * B * 4);
   }
   const size_t o_ts = c.take(t_prof >= 2 ? plans.size() * 8 * sizeof(unsigned long long) : 0);
@@ -417,6 +417,9 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   const size_t o_run = c.take((size_t)(max_slots + 1) * 4);
   const size_t o_llow = c.take((size_t)max_slots * 4), o_lup = c.take((size_t)max_slots * 4);
   const size_t o_voff = c.take((size_t)last_slots * 8);
+  const size_t o_pop = c.take((size_t)last_slots * 4), o_lg = c.take((size_t)last_slots * 4);
+  const int G = di->sms * di->occ_chain;  // every co-resident block
+  const size_t o_blk = c.take((size_t)G * 8);
   size_t o_inter[2][3];
   for (int k = 0; k < 2; ++k) {
     o_inter[k][0] = c.take((size_t)max_inter * 12);
@@ -497,7 +500,6 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
 
   // ---- pass arguments
   std::vector<PassArgs> args(plans.size());
-  long long work_blocks = 1;
   for (size_t p = 0; p < plans.size(); ++p) {
     PassPlan& pl = plans[p];
     PassArgs& a = args[p];
@@ -507,6 +509,11 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     a.B = B;
     a.P = pl.P;
     a.last = p + 1 == plans.size();
+    {  // targets per emission thread: about one round of the grid's threads
+      const long long T = slots_per_source(pl.spec);
+      const long long want = (pl.in_cap * T + (long long)G * 256 - 1) / ((long long)G * 256);
+      a.tchunk = (int32_t)std::max(1ll, std::min(T, want));
+    }
     for (int ax = 0; ax < 3; ++ax) {
       a.lo[ax] = pl.spec.lo[ax];
       a.hi[ax] = pl.spec.hi[ax];
@@ -552,6 +559,9 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     a.leaf_lower = (uint32_t*)(ws + o_llow);
     a.leaf_upper = (uint32_t*)(ws + o_lup);
     a.leaf_voff = (int64_t*)(ws + o_voff);
+    a.leaf_pop = (uint32_t*)(ws + o_pop);
+    a.leaf_g = (uint32_t*)(ws + o_lg);
+    a.blk_agg = (unsigned long long*)(ws + o_blk);
     a.phase_ts = t_prof >= 2 ? (unsigned long long*)(ws + o_ts) + 8 * p : nullptr;
     if (!a.last) {
       const int k = (int)(p & 1);
@@ -559,11 +569,9 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
       a.out_masks = (uint64_t*)(ws + o_inter[k][1]);
       a.out_grid = (int32_t*)(ws + o_inter[k][2]);
     }
-    work_blocks = std::max({work_blocks, (pl.in_cap + 255) / 256, pl.sort_tiles, pl.dedup_tiles});
   }
 
   // ---- the cooperative pass kernel(s)
-  const int G = blocks_for(work_blocks, 1, (long long)di->sms * di->occ_chain);
   for (int l = 0; l < n_launch; ++l) {
     ChainArgs ca;
     std::memset(&ca, 0, sizeof ca);

@@ -46,19 +46,15 @@ struct SmemEmit {
 };
 struct SmemDedup {
   unsigned long long scan[8];
-  unsigned long long base[4];
-  uint32_t seg_f[8];
-  unsigned long long seg_v[8];
-  uint32_t head_pos[kDedupTile];   // slot of each leaf head of the tile, in order
-  uint32_t head_fl[kDedupTile];    // its head flags (bit 3: first leaf of a grid)
-  uint32_t head_pop[kDedupTile];   // voxels of its merged mask
-  uint32_t head_g[kDedupTile];     // its grid
-  uint32_t grp_g[kThreads / 8];            // per 8-lane group: grid of its pending bbox
-  unsigned int grp_box[kThreads / 8][6];   // per group: pending encoded bbox
-  uint32_t tail_end;               // end of the tile's last run
-  uint32_t tail_newgrid;           // 1 if that run is the last of its grid
+  unsigned long long base[3];
   uint32_t tile;
-  uint32_t last;
+};
+struct SmemLeaves {
+  uint32_t grp_f[kThreads / 8];            // per 8-lane group: segmented aggregate of its leaves
+  unsigned long long grp_v[kThreads / 8];
+  uint32_t grp_g[kThreads / 8];            // grid of its pending bbox
+  unsigned int grp_box[kThreads / 8][6];   // its pending encoded bbox
+  unsigned long long blk_prefix;           // voxels before the block's first leaf in the same grid
 };
 struct SmemFinish {
   uint32_t s[kThreads];
@@ -68,6 +64,12 @@ union Smem {
   SmemEmit emit;
   SmemDedup dedup;
   SmemFinish fin;
+};
+// the leaves phase keeps its group aggregates across one grid barrier, so it
+// has shared memory of its own
+struct SmemAll {
+  Smem u;
+  SmemLeaves lv;
 };
 
 // Profiling stamps of the GPU global timer over all blocks: slot 0 holds the
@@ -90,67 +92,6 @@ __device__ __forceinline__ int grid_of(const int64_t* offsets, int32_t B, long l
     if (__ldg(offsets + mid) <= i) lo = mid; else hi = mid;
   }
   return lo;
-}
-
-// Bit set of the non-empty targets of one source leaf.
-template <int OP>
-__device__ __forceinline__ uint32_t targets_of(const PassArgs& a, const uint64_t m[8]) {
-  uint64_t all = 0;
-#pragma unroll
-  for (int w = 0; w < 8; ++w) all |= m[w];
-  if (OP == kLeaves || OP == kCoarsen) return all ? 1u : 0u;
-  if (OP == kRefine) {
-    // child c = 4*cx + 2*cy + cz is non-empty iff the parent's octant c holds a voxel
-    uint32_t bits = 0;
-#pragma unroll
-    for (int cx = 0; cx < 2; ++cx) {
-      const uint64_t t = m[4 * cx] | m[4 * cx + 1] | m[4 * cx + 2] | m[4 * cx + 3];
-#pragma unroll
-      for (int cy = 0; cy < 2; ++cy)
-#pragma unroll
-        for (int cz = 0; cz < 2; ++cz)
-          if (t & (0x0F0F0F0Full << (32 * cy + 4 * cz))) bits |= 1u << (4 * cx + 2 * cy + cz);
-    }
-    return bits;
-  }
-  // box dilation: target offset t (code 9(tx+1) + 3(ty+1) + (tz+1)) is reached iff a
-  // voxel lies in its zone -- anywhere for t = 0, the last plane for t = +1 (hi = 1),
-  // the first plane for t = -1 (lo = -1)
-  const uint64_t xs[3] = {m[0], all, m[7]};
-  const uint64_t ym[3] = {0x00000000000000FFull, ~0ull, 0xFF00000000000000ull};
-  const uint64_t zm[3] = {0x0101010101010101ull, ~0ull, 0x8080808080808080ull};
-  uint32_t bits = 0;
-#pragma unroll
-  for (int tx = -1; tx <= 1; ++tx)
-#pragma unroll
-    for (int ty = -1; ty <= 1; ++ty)
-#pragma unroll
-      for (int tz = -1; tz <= 1; ++tz) {
-        if (tx < a.lo[0] || tx > a.hi[0] || ty < a.lo[1] || ty > a.hi[1] || tz < a.lo[2] || tz > a.hi[2]) continue;
-        if (xs[tx + 1] & ym[ty + 1] & zm[tz + 1]) bits |= 1u << (9 * (tx + 1) + 3 * (ty + 1) + (tz + 1));
-      }
-  return bits;
-}
-
-template <int OP>
-__device__ __forceinline__ void target_lc(const int32_t lc[3], uint32_t code, int32_t out[3]) {
-  if (OP == kRefine) {
-    out[0] = 2 * lc[0] + (int32_t)((code >> 2) & 1);
-    out[1] = 2 * lc[1] + (int32_t)((code >> 1) & 1);
-    out[2] = 2 * lc[2] + (int32_t)(code & 1);
-  } else if (OP == kCoarsen) {
-    out[0] = lc[0] >> 1;
-    out[1] = lc[1] >> 1;
-    out[2] = lc[2] >> 1;
-  } else if (OP == kDilate) {
-    out[0] = lc[0] + (int32_t)(code / 9) - 1;
-    out[1] = lc[1] + (int32_t)((code / 3) % 3) - 1;
-    out[2] = lc[2] + (int32_t)(code % 3) - 1;
-  } else {
-    out[0] = lc[0];
-    out[1] = lc[1];
-    out[2] = lc[2];
-  }
 }
 
 // Claims `n` consecutive slots for this lane within one warp-wide range;
@@ -191,59 +132,125 @@ __device__ __forceinline__ void hist_warp(const PassArgs& a, unsigned int (*hist
   }
 }
 
+// Is target `t` (an index into the op's target set) of a source leaf with
+// mask m non-empty?  Sets the target's slot code and leaf coordinate.
+template <int OP>
+__device__ __forceinline__ bool target_nonempty(const PassArgs& a, const uint64_t m[8], const int32_t lc[3],
+                                                uint32_t t, uint32_t& code, int32_t out[3]) {
+  if (OP == kRefine) {  // child t = 4*cx + 2*cy + cz: the parent's octant t holds a voxel
+    const int cx = (t >> 2) & 1, cy = (t >> 1) & 1, cz = t & 1;
+    const uint64_t h = m[4 * cx] | m[4 * cx + 1] | m[4 * cx + 2] | m[4 * cx + 3];
+    code = t;
+    out[0] = 2 * lc[0] + cx;
+    out[1] = 2 * lc[1] + cy;
+    out[2] = 2 * lc[2] + cz;
+    return (h & (0x0F0F0F0Full << (32 * cy + 4 * cz))) != 0;
+  }
+  uint64_t all = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) all |= m[k];
+  if (OP == kLeaves || OP == kCoarsen) {
+    // coarsen: the code is the source leaf's octant inside its coarse leaf
+    code = OP == kCoarsen ? (uint32_t)(((lc[0] & 1) << 2) | ((lc[1] & 1) << 1) | (lc[2] & 1)) : 0u;
+    const int sh = OP == kCoarsen ? 1 : 0;
+    out[0] = lc[0] >> sh;
+    out[1] = lc[1] >> sh;
+    out[2] = lc[2] >> sh;
+    return all != 0;
+  }
+  // box dilation: targets enumerate the box [lo, hi]^3 (per axis offsets in
+  // {-1, 0, 1}); target offset d is reached iff a voxel lies in its zone --
+  // anywhere for d = 0, the last plane for d = +1, the first plane for d = -1
+  const int nx = a.hi[0] - a.lo[0] + 1, ny = a.hi[1] - a.lo[1] + 1, nz = a.hi[2] - a.lo[2] + 1;
+  (void)nx;
+  const int tz = a.lo[2] + (int)(t % nz), ty = a.lo[1] + (int)((t / nz) % ny), tx = a.lo[0] + (int)(t / (nz * ny));
+  const uint64_t xs = tx < 0 ? m[0] : (tx > 0 ? m[7] : all);
+  const uint64_t ym = ty < 0 ? 0x00000000000000FFull : (ty > 0 ? 0xFF00000000000000ull : ~0ull);
+  const uint64_t zm = tz < 0 ? 0x0101010101010101ull : (tz > 0 ? 0x8080808080808080ull : ~0ull);
+  code = (uint32_t)(9 * (tx + 1) + 3 * (ty + 1) + (tz + 1));
+  out[0] = lc[0] + tx;
+  out[1] = lc[1] + ty;
+  out[2] = lc[2] + tz;
+  return (xs & ym & zm) != 0;
+}
+
+// Targets per source leaf of an op.
+template <int OP>
+__device__ __forceinline__ uint32_t targets_per_source(const PassArgs& a) {
+  if (OP == kRefine) return 8u;
+  if (OP == kDilate) return (uint32_t)((a.hi[0] - a.lo[0] + 1) * (a.hi[1] - a.lo[1] + 1) * (a.hi[2] - a.lo[2] + 1));
+  return 1u;
+}
+
+// One thread per (source, chunk of a.tchunk targets): it tests its targets,
+// claims one warp-aggregated range of slots for the non-empty ones, and
+// writes them in warp-synchronous rounds that also feed the block's digit
+// histograms.  The host sizes the chunk so that all candidates of a pass are
+// covered by about one round of the grid's threads.
 template <int OP>
 __device__ void phase_emit(const PassArgs& a, Smem& sm) {
   for (int i = threadIdx.x; i < a.P * kBins; i += kThreads) (&sm.emit.hist[0][0])[i] = 0;
   __syncthreads();
   const long long n = a.src_count_dev ? (long long)__ldcg(a.src_count_dev) : a.src_count;
+  const uint32_t T = targets_per_source<OP>(a);
+  const uint32_t k = (a.tchunk > 0 && (uint32_t)a.tchunk < T) ? (uint32_t)a.tchunk : T;
+  const uint32_t nchunks = (T + k - 1) / k;
+  const long long items = n * (long long)nchunks;
   const long long stride = (long long)gridDim.x * kThreads;
-  const int lane = threadIdx.x & 31;
-  for (long long base = (long long)blockIdx.x * kThreads; base < n; base += stride) {
-    const long long i = base + threadIdx.x;
-    unsigned long long wbase;
-    uint32_t wtotal;
-    if (OP == kIjk) {
-      const bool valid = i < n;
-      const unsigned long long pos = claim_slots(a, valid ? 1u : 0u, wbase, wtotal);
-      uint64_t key = 0;
-      if (valid) {
-        const int32_t x = __ldg(a.ijk + 3 * i), y = __ldg(a.ijk + 3 * i + 1), z = __ldg(a.ijk + 3 * i + 2);
-        const uint32_t g = (uint32_t)grid_of(a.in_offsets, a.B, i);
-        key = encode_key(a.K, g, x >> 3, y >> 3, z >> 3);
-        put_slot(a, pos, key, (uint32_t)i);
-      }
-      hist_warp(a, sm.emit.hist, key, valid);
-    } else {
-      uint32_t bits = 0;
-      int32_t lc[3] = {0, 0, 0};
-      uint32_t g = 0;
-      if (i < n) {
-        uint64_t m[8];
+  for (long long base = (long long)blockIdx.x * kThreads; base < items; base += stride) {
+    const long long idx = base + threadIdx.x;
+    uint32_t bits = 0, t0 = 0, g = 0;
+    long long i = 0;
+    uint64_t m[8];
+    int32_t lc[3] = {0, 0, 0};
+    if (idx < items) {
+      i = idx / nchunks;
+      t0 = (uint32_t)(idx - i * nchunks) * k;
+      const uint32_t t1 = t0 + k < T ? t0 + k : T;
+      if (OP == kIjk) {
+        lc[0] = __ldg(a.ijk + 3 * i);
+        lc[1] = __ldg(a.ijk + 3 * i + 1);
+        lc[2] = __ldg(a.ijk + 3 * i + 2);
+        g = (uint32_t)grid_of(a.in_offsets, a.B, i);
+        bits = 1u;
+      } else {
         load_mask(a.src_masks, i, m);
-        bits = targets_of<OP>(a, m);
         lc[0] = __ldcg(a.src_origins + 3 * i) >> 3;
         lc[1] = __ldcg(a.src_origins + 3 * i + 1) >> 3;
         lc[2] = __ldcg(a.src_origins + 3 * i + 2) >> 3;
-        g = a.src_grid ? (uint32_t)__ldcg(a.src_grid + i) : (uint32_t)grid_of(a.in_offsets, a.B, i);
+        for (uint32_t t = t0; t < t1; ++t) {
+          uint32_t code;
+          int32_t tl[3];
+          if (target_nonempty<OP>(a, m, lc, t, code, tl)) bits |= 1u << (t - t0);
+        }
+        if (bits) g = a.src_grid ? (uint32_t)__ldcg(a.src_grid + i) : (uint32_t)grid_of(a.in_offsets, a.B, i);
       }
-      unsigned long long pos = claim_slots(a, __popc(bits), wbase, wtotal);
-      while (bits) {
-        const uint32_t code = __ffs(bits) - 1;
+    }
+    const uint32_t nt = __popc(bits);
+    unsigned long long wbase;
+    uint32_t wtotal;
+    unsigned long long pos = claim_slots(a, nt, wbase, wtotal);
+    const uint32_t rounds = __reduce_max_sync(0xffffffffu, nt);
+    for (uint32_t r = 0; r < rounds; ++r) {
+      const bool valid = bits != 0;
+      uint64_t key = 0;
+      if (valid) {
+        const uint32_t t = t0 + (uint32_t)(__ffs(bits) - 1);
         bits &= bits - 1;
-        int32_t t[3];
-        target_lc<OP>(lc, code, t);
-        // coarsen: the code is the source leaf's octant inside its coarse leaf
-        const uint32_t ref = OP == kCoarsen ? (uint32_t)(((lc[0] & 1) << 2) | ((lc[1] & 1) << 1) | (lc[2] & 1)) : code;
-        put_slot(a, pos++, encode_key(a.K, g, t[0], t[1], t[2]), ((uint32_t)i << kSrcShift) | ref);
+        uint32_t val;
+        if (OP == kIjk) {
+          key = encode_key(a.K, g, lc[0] >> 3, lc[1] >> 3, lc[2] >> 3);
+          val = (uint32_t)i;
+        } else {
+          uint32_t code;
+          int32_t tl[3];
+          target_nonempty<OP>(a, m, lc, t, code, tl);
+          key = encode_key(a.K, g, tl[0], tl[1], tl[2]);
+          val = ((uint32_t)i << kSrcShift) | code;
+        }
+        put_slot(a, pos++, key, val);
       }
-      // histogram the warp's freshly written range, 32 keys at a time
-      __syncwarp();
-      for (uint32_t off = 0; off < wtotal; off += 32) {
-        const unsigned long long j = wbase + off + lane;
-        const bool valid = off + lane < wtotal && j < (unsigned long long)a.slot_cap;
-        const uint64_t key = valid ? __ldcg(a.keys[0] + j) : 0ull;
-        hist_warp(a, sm.emit.hist, key, valid);
-      }
+      hist_warp(a, sm.emit.hist, key, valid);
     }
   }
   __syncthreads();
@@ -440,7 +447,92 @@ __device__ __forceinline__ void leaf_bounds(uint64_t word, int w, int lane, int3
   mx[2] = 31 - __clz(zb);
 }
 
-// ---------------------------------------------------------------- dedup, merge, count
+// ---------------------------------------------------------------- dedup and index
+
+constexpr uint32_t kGridFirst = 0x80000000u;  // leaf_upper flag: first leaf of its grid
+
+// Head flags on the sorted keys -- a new leaf where the key changes, a new
+// lower node where (grid, tile, upper child) changes, a new upper node where
+// (grid, tile) changes, a new grid where the grid field changes -- and a
+// 1024-slot tile scan of the three head counts with a warp-window look-back.
+// Every unique leaf u gets its run start and (last pass) its lower / upper
+// node indices, the upper index flagged when u is its grid's first leaf;
+// each grid gets its first leaf / lower / upper indices.
+__device__ void phase_index(const PassArgs& a, Smem& sm) {
+  SmemDedup& s = sm.dedup;
+  const uint64_t* keys = a.keys[a.sorted];
+  long long S = (long long)__ldcg(&a.rb->num_slots);
+  if (S > a.slot_cap) S = a.slot_cap;
+  const long long ntiles = (S + kDedupTile - 1) / kDedupTile;
+  const int lb = a.K.lower_bits, nb = a.K.node_bits, gsh = a.K.gw ? a.K.gshift : 64;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int32_t B = a.B;
+  constexpr unsigned long long M21 = (1ull << 21) - 1;
+  for (;;) {
+    if (tid == 0) s.tile = atomicAdd(&a.ctl->dedup_tile_ctr, 1u);
+    __syncthreads();
+    const long long tile = s.tile;
+    if (tile >= ntiles) break;
+    const long long i0 = tile * kDedupTile + (long long)tid * kDedupItems;
+    uint64_t prev = (i0 > 0 && i0 - 1 < S) ? __ldcg(keys + i0 - 1) : 0ull;
+    uint64_t kk[kDedupItems];
+    uint32_t fl[kDedupItems];
+    unsigned long long c = 0;
+#pragma unroll
+    for (int j = 0; j < kDedupItems; ++j) {
+      const long long i = i0 + j;
+      fl[j] = 0;
+      kk[j] = 0;
+      if (i < S) {
+        const uint64_t key = __ldcg(keys + i);
+        kk[j] = key;
+        const bool first = (i == 0);
+        const bool hl = first || key != prev;
+        const bool hlo = first || shr64(key, lb) != shr64(prev, lb);
+        const bool hup = first || shr64(key, nb) != shr64(prev, nb);
+        const bool hg = first || shr64(key, gsh) != shr64(prev, gsh);
+        fl[j] = (hl ? 1u : 0u) | (hlo ? 2u : 0u) | (hup ? 4u : 0u) | (hg ? 8u : 0u);
+        c += (hl ? 1ull : 0ull) | (hlo ? (1ull << 21) : 0ull) | (hup ? (1ull << 42) : 0ull);
+        prev = key;
+      }
+    }
+    unsigned long long tot;
+    const unsigned long long ex = block_excl_scan_256(c, s.scan, &tot);
+    if (warp < 3) {
+      const unsigned long long field = (tot >> (21 * warp)) & M21;
+      lb64_publish(a.dedup_status + warp, 3, tile, field, false);
+      const unsigned long long b = lb64_resolve(a.dedup_status + warp, 3, tile, field, false, &a.rb->err);
+      if (lane == 0) {
+        s.base[warp] = b;
+        if (field) atomicAdd(&a.ctl->head_totals[warp], field);
+      }
+    }
+    __syncthreads();
+    unsigned long long cl = s.base[0] + (ex & M21);
+    unsigned long long clo = s.base[1] + ((ex >> 21) & M21);
+    unsigned long long cup = s.base[2] + ((ex >> 42) & M21);
+#pragma unroll
+    for (int j = 0; j < kDedupItems; ++j) {
+      if (!(fl[j] & 1u)) continue;
+      if (fl[j] & 2u) ++clo;
+      if (fl[j] & 4u) ++cup;
+      const unsigned long long u = cl++;
+      a.run_start[u] = (uint32_t)(i0 + j);
+      if (!a.last) continue;
+      a.leaf_lower[u] = (uint32_t)(clo - 1);
+      a.leaf_upper[u] = (uint32_t)(cup - 1) | ((fl[j] & 8u) ? kGridFirst : 0u);
+      if (fl[j] & 8u) {
+        const uint32_t g = (uint32_t)shr64(kk[j], gsh);
+        if (g < (uint32_t)B) {
+          a.first[g] = (uint32_t)(u + 1);
+          a.first[B + g] = (uint32_t)clo;
+          a.first[2 * B + g] = (uint32_t)cup;
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
 
 // out[g] = first index of the first non-empty grid >= g, or `total`; out[B] = total.
 __device__ void suffix_fill(const uint32_t* first, int32_t B, unsigned long long total, int64_t* out, Smem& sm) {
@@ -472,325 +564,246 @@ __device__ void suffix_fill(const uint32_t* first, int32_t B, unsigned long long
   if (tid == 0) out[B] = (int64_t)total;
 }
 
-// One phase after the sort.  Per 1024-slot tile:
-//   head flags on the sorted keys (new leaf / lower node / upper node / grid),
-//   a block scan and a look-back of the three head counts (unique-leaf, lower-
-//   and upper-node indices), the run of every leaf head (a run may continue
-//   into later tiles), the OR-merge of each run by an 8-lane group, then
-//   - last pass: popcounts and bboxes (grid bboxes by atomics), a segmented
-//     voxel scan over the tile's leaves with a look-back (segments = grids),
-//     voxel offsets per leaf and voxels per grid;
-//   - intermediate pass: the merged leaves themselves, for the next pass.
-// The last block to finish writes the totals and the per-grid offsets.
+// Block 0 after the index phase: totals, run sentinel, per-grid offsets.
+__device__ void phase_finish(const PassArgs& a, Smem& sm) {
+  long long S = (long long)__ldcg(&a.rb->num_slots);
+  if (S > a.slot_cap) S = a.slot_cap;
+  const unsigned long long U = __ldcg(&a.ctl->head_totals[0]);
+  const unsigned long long NL = __ldcg(&a.ctl->head_totals[1]);
+  const unsigned long long NU = __ldcg(&a.ctl->head_totals[2]);
+  if (threadIdx.x == 0) {
+    a.rb->num_leaves = U;
+    a.rb->num_lowers = NL;
+    a.rb->num_uppers = NU;
+    a.run_start[U] = (uint32_t)S;
+  }
+  if (a.last) {
+    suffix_fill(a.first, a.B, U, a.leaf_off, sm);
+    suffix_fill(a.first + a.B, a.B, NL, a.lower_off, sm);
+    suffix_fill(a.first + 2 * a.B, a.B, NU, a.upper_off, sm);
+  }
+}
+
+// Leaves of the pass, spread over the whole grid: block b takes a contiguous
+// range of leaves and each of its 8-lane groups a contiguous sub-range, so a
+// group sees its leaves in grid order.  Per leaf the run of slots is merged;
+//  - last pass: popcount and bbox (grid bboxes accumulate per group and reach
+//    memory once per grid change), per-leaf voxels, and the segmented voxel
+//    aggregate of each group and block (segments start at grid-first leaves);
+//  - intermediate pass: the merged leaves for the next pass.
 template <int OP>
-__device__ void phase_dedup(const PassArgs& a, Smem& sm) {
-  SmemDedup& s = sm.dedup;
+__device__ void phase_leaves(const PassArgs& a, SmemAll& sa) {
+  SmemLeaves& s = sa.lv;
   const uint64_t* keys = a.keys[a.sorted];
   const uint32_t* vals = a.vals[a.sorted];
   long long S = (long long)__ldcg(&a.rb->num_slots);
   if (S > a.slot_cap) S = a.slot_cap;
-  const long long ntiles = (S + kDedupTile - 1) / kDedupTile;
-  const int lb = a.K.lower_bits, nb = a.K.node_bits, gsh = a.K.gw ? a.K.gshift : 64;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, w = tid & 7;
-  const int32_t B = a.B;
-  constexpr unsigned long long M21 = (1ull << 21) - 1;
-  for (;;) {
-    if (tid == 0) s.tile = atomicAdd(&a.ctl->dedup_tile_ctr, 1u);
-    __syncthreads();
-    const long long tile = s.tile;
-    if (tile >= ntiles) break;
-    const long long t0 = tile * kDedupTile;
-    const long long t1 = (t0 + kDedupTile < S) ? t0 + kDedupTile : S;
-    const long long i0 = t0 + (long long)tid * kDedupItems;
-    uint64_t prev = (i0 > 0 && i0 - 1 < S) ? __ldcg(keys + i0 - 1) : 0ull;
-    uint64_t kk[kDedupItems];
-    uint32_t fl[kDedupItems];
-    unsigned long long c = 0;
+  const long long U = (long long)__ldcg(&a.ctl->head_totals[0]);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid & 7, grp = tid >> 3;
+  const long long C = (U + gridDim.x - 1) / gridDim.x;
+  const long long c = (C + kThreads / 8 - 1) / (kThreads / 8);
+  const long long bbeg = (long long)blockIdx.x * C, bend = bbeg + C < U ? bbeg + C : U;
+  const long long gbeg = bbeg + grp * c, gend = gbeg + c < bend ? gbeg + c : bend;
+  constexpr int kU = OP == kRefine ? 4 : 1;
+  uint32_t acc_g = 0xFFFFFFFFu, F = 0;
+  unsigned int acc_e = 0;
+  unsigned long long V = 0;
+  for (long long q = 0; q < c; q += kU) {
+    uint64_t word[kU];
+    uint32_t gg[kU];
+    int32_t lcs[kU][3];
+    bool valid[kU];
 #pragma unroll
-    for (int j = 0; j < kDedupItems; ++j) {
-      const long long i = i0 + j;
-      fl[j] = 0;
-      kk[j] = 0;
-      if (i < S) {
-        const uint64_t key = __ldcg(keys + i);
-        kk[j] = key;
-        const bool first = (i == 0);
-        const bool hl = first || key != prev;
-        const bool hlo = first || shr64(key, lb) != shr64(prev, lb);
-        const bool hup = first || shr64(key, nb) != shr64(prev, nb);
-        const bool hg = first || shr64(key, gsh) != shr64(prev, gsh);
-        fl[j] = (hl ? 1u : 0u) | (hlo ? 2u : 0u) | (hup ? 4u : 0u) | (hg ? 8u : 0u);
-        c += (hl ? 1ull : 0ull) | (hlo ? (1ull << 21) : 0ull) | (hup ? (1ull << 42) : 0ull);
-        prev = key;
+    for (int r = 0; r < kU; ++r) {
+      const long long u = gbeg + q + r;
+      valid[r] = u < gend;
+      uint32_t s0 = 0, s1 = 0;
+      gg[r] = 0;
+      lcs[r][0] = lcs[r][1] = lcs[r][2] = 0;
+      if (valid[r]) {
+        s0 = __ldcg(a.run_start + u);
+        s1 = u + 1 < U ? __ldcg(a.run_start + u + 1) : (uint32_t)S;
+        decode_key(a.K, __ldcg(keys + s0), gg[r], lcs[r]);
       }
+      word[r] = merge_run<OP>(a, vals, s0, s1, w);
     }
-    unsigned long long tot;
-    const unsigned long long ex = block_excl_scan_256(c, s.scan, &tot);
-    const int nheads = (int)(tot & M21);
-    if (warp < 3) {
-      const unsigned long long field = (tot >> (21 * warp)) & M21;
-      lb64_publish(a.dedup_status + warp, 4, tile, field, false);
-    }
-    // compact the heads of the tile
-    {
-      int k = (int)(ex & M21);
 #pragma unroll
-      for (int j = 0; j < kDedupItems; ++j)
-        if (fl[j] & 1u) {
-          s.head_pos[k] = (uint32_t)(i0 + j);
-          s.head_fl[k] = fl[j];
-          ++k;
-        }
-    }
-    // end of the tile's last run: the first slot at or after t1 with another key
-    if (warp == 0) {
-      uint32_t end = (uint32_t)S, newgrid = 1;
-      if (t1 < S) {
-        const uint64_t last_key = __ldcg(keys + t1 - 1);
-        for (long long b = t1;; b += 32) {
-          const long long j = b + lane;
-          const uint64_t kj = j < S ? __ldcg(keys + j) : ~0ull;
-          const uint32_t diff = __ballot_sync(0xffffffffu, j >= S || kj != last_key);
-          if (diff) {
-            const int l = __ffs(diff) - 1;
-            const long long je = b + l;
-            const uint64_t kd = __shfl_sync(0xffffffffu, kj, l);
-            end = (uint32_t)(je < S ? je : S);
-            newgrid = (je >= S || shr64(kd, gsh) != shr64(last_key, gsh)) ? 1u : 0u;
-            break;
-          }
-        }
-      }
-      if (lane == 0) {
-        s.tail_end = end;
-        s.tail_newgrid = newgrid;
-      }
-    }
-    __syncthreads();
-    // leaf / lower / upper bases of the tile
-    if (warp < 3) {
-      const unsigned long long field = (tot >> (21 * warp)) & M21;
-      const unsigned long long b = lb64_resolve(a.dedup_status + warp, 4, tile, field, false, &a.rb->err);
-      if (lane == 0) {
-        s.base[warp] = b;
-        if (field) atomicAdd(&a.ctl->head_totals[warp], field);
-      }
-    }
-    __syncthreads();
-    const unsigned long long ubase = s.base[0];
-    {
-      unsigned long long cl = ubase + (ex & M21);
-      unsigned long long clo = s.base[1] + ((ex >> 21) & M21);
-      unsigned long long cup = s.base[2] + ((ex >> 42) & M21);
+    for (int r = 0; r < kU; ++r) {
+      const long long u = gbeg + q + r;
+      const uint32_t g = gg[r];
+      if (a.last) {
+        uint32_t pop = __popcll(word[r]);
 #pragma unroll
-      for (int j = 0; j < kDedupItems; ++j) {
-        if (!(fl[j] & 1u)) continue;
-        if (fl[j] & 2u) ++clo;
-        if (fl[j] & 4u) ++cup;
-        const unsigned long long u = cl++;
-        if (a.last) {
-          a.run_start[u] = (uint32_t)(i0 + j);
-          a.leaf_lower[u] = (uint32_t)(clo - 1);
-          a.leaf_upper[u] = (uint32_t)(cup - 1);
-        }
-        if (fl[j] & 8u) {
-          const uint32_t g = (uint32_t)shr64(kk[j], gsh);
-          if (g < (uint32_t)B) {
-            a.first[g] = (uint32_t)(u + 1);
-            a.first[B + g] = (uint32_t)clo;
-            a.first[2 * B + g] = (uint32_t)cup;
-          }
-        }
-      }
-    }
-    // merge every run of the tile: one 8-lane group per leaf head (warp-uniform
-    // loop); refinement runs are single slots, so a group takes four at once.
-    // Leaf bboxes accumulate per group in registers (heads arrive in grid
-    // order) and reach memory once per grid change.
-    constexpr int kU = OP == kRefine ? 4 : 1;
-    uint32_t acc_g = 0xFFFFFFFFu;
-    unsigned int acc_e = 0;
-    for (int kb = warp * 4; kb < nheads; kb += kU * (kThreads / 8)) {
-      uint64_t word[kU];
-      uint32_t gg[kU];
-      int32_t lcs[kU][3];
-      bool valid[kU];
-#pragma unroll
-      for (int r = 0; r < kU; ++r) {
-        const int k = kb + r * (kThreads / 8) + (lane >> 3);
-        valid[r] = k < nheads;
-        uint32_t s0 = 0, s1 = 0;
-        gg[r] = 0;
-        lcs[r][0] = lcs[r][1] = lcs[r][2] = 0;
+        for (int off = 1; off < 8; off <<= 1) pop += __shfl_xor_sync(0xffffffffu, pop, off);
+        int32_t mn[3], mx[3];
+        leaf_bounds(word[r], w, lane, mn, mx);
         if (valid[r]) {
-          s0 = s.head_pos[k];
-          s1 = (k + 1 < nheads) ? s.head_pos[k + 1] : s.tail_end;
-          decode_key(a.K, __ldcg(keys + s0), gg[r], lcs[r]);
-        }
-        word[r] = merge_run<OP>(a, vals, s0, s1, w);
-      }
-#pragma unroll
-      for (int r = 0; r < kU; ++r) {
-        const int k = kb + r * (kThreads / 8) + (lane >> 3);
-        const uint32_t g = gg[r];
-        if (a.last) {
-          uint32_t pop = __popcll(word[r]);
-#pragma unroll
-          for (int off = 1; off < 8; off <<= 1) pop += __shfl_xor_sync(0xffffffffu, pop, off);
-          int32_t mn[3], mx[3];
-          leaf_bounds(word[r], w, lane, mn, mx);
-          if (valid[r]) {
-            if (w < 6) {
-              const int ax = w < 3 ? w : w - 3;
-              const int32_t o = (int32_t)((uint32_t)lcs[r][ax] << 3);
-              const unsigned int e = w < 3 ? enc_min(o + mn[ax]) : enc_max(o + mx[ax]);
-              if (g != acc_g) {
-                if (acc_g != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * acc_g + w], acc_e);
-                acc_g = g;
-                acc_e = e;
-              } else {
-                acc_e = max(acc_e, e);
-              }
-            }
-            if (w == 0) {
-              s.head_pop[k] = pop;
-              s.head_g[k] = g;
+          if (w < 6) {
+            const int ax = w < 3 ? w : w - 3;
+            const int32_t o = (int32_t)((uint32_t)lcs[r][ax] << 3);
+            const unsigned int e = w < 3 ? enc_min(o + mn[ax]) : enc_max(o + mx[ax]);
+            if (g != acc_g) {
+              if (acc_g != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * acc_g + w], acc_e);
+              acc_g = g;
+              acc_e = e;
+            } else {
+              acc_e = max(acc_e, e);
             }
           }
-        } else if (valid[r]) {
-          const unsigned long long u = ubase + k;
-          a.out_masks[8 * u + w] = word[r];
-          if (w < 3) a.out_origins[3 * u + w] = (int32_t)((uint32_t)lcs[r][w] << 3);
-          if (w == 3) a.out_grid[u] = (int32_t)g;
-        }
-      }
-    }
-    if (a.last) {
-      // combine the groups' pending bboxes: one atomic per grid and axis bound
-      if (w < 6) s.grp_box[tid >> 3][w] = acc_e;
-      if (w == 0) s.grp_g[tid >> 3] = acc_g;
-    }
-    if (a.last) {
-      __syncthreads();
-      if (tid < 6) {
-        uint32_t cg = 0xFFFFFFFFu;
-        unsigned int ce = 0;
-        for (int j = 0; j < kThreads / 8; ++j) {
-          const uint32_t gj = s.grp_g[j];
-          if (gj == 0xFFFFFFFFu) continue;
-          const unsigned int ej = s.grp_box[j][tid];
-          if (gj == cg) {
-            ce = max(ce, ej);
+          if (w == 0) {
+            a.leaf_pop[u] = pop;
+            a.leaf_g[u] = g;
+          }
+          if (__ldcg(a.leaf_upper + u) & kGridFirst) {
+            F = 1;
+            V = pop;
           } else {
-            if (cg != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * cg + tid], ce);
-            cg = gj;
-            ce = ej;
+            V += pop;
           }
         }
+      } else if (valid[r]) {
+        a.out_masks[8 * u + w] = word[r];
+        if (w < 3) a.out_origins[3 * u + w] = (int32_t)((uint32_t)lcs[r][w] << 3);
+        if (w == 3) a.out_grid[u] = (int32_t)g;
+      }
+    }
+  }
+  if (!a.last) return;
+  if (w == 0) {
+    s.grp_f[grp] = F;
+    s.grp_v[grp] = V;
+    s.grp_g[grp] = acc_g;
+  }
+  if (w < 6) s.grp_box[grp][w] = acc_e;
+  __syncthreads();
+  if (tid < 6) {  // grid bboxes: one atomic per grid run of the groups
+    uint32_t cg = 0xFFFFFFFFu;
+    unsigned int ce = 0;
+    for (int j = 0; j < kThreads / 8; ++j) {
+      const uint32_t gj = s.grp_g[j];
+      if (gj == 0xFFFFFFFFu) continue;
+      const unsigned int ej = s.grp_box[j][tid];
+      if (gj == cg) {
+        ce = max(ce, ej);
+      } else {
         if (cg != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * cg + tid], ce);
-      }
-      // segmented voxel scan over the tile's leaves (segments start at each grid's first leaf)
-      uint32_t f = 0;
-      unsigned long long v = 0;
-#pragma unroll
-      for (int q = 0; q < kDedupItems; ++q) {
-        const int k = tid * kDedupItems + q;
-        if (k < nheads) {
-          if (s.head_fl[k] & 8u) {
-            f = 1;
-            v = s.head_pop[k];
-          } else {
-            v += s.head_pop[k];
-          }
-        }
-      }
-      uint32_t ef, tf;
-      unsigned long long ev, tv;
-      block_seg_scan_256(f, v, s.seg_f, s.seg_v, ef, ev, tf, tv);
-      if (warp == 3) {
-        lb64_publish(a.dedup_status + 3, 4, tile, tv, tf != 0);
-        const unsigned long long b = lb64_resolve(a.dedup_status + 3, 4, tile, tv, tf != 0, &a.rb->err);
-        if (lane == 0) s.base[3] = b;
-      }
-      __syncthreads();
-      const unsigned long long vbase = s.base[3];
-      uint32_t rf = ef;
-      unsigned long long rv = ev;
-#pragma unroll
-      for (int q = 0; q < kDedupItems; ++q) {
-        const int k = tid * kDedupItems + q;
-        if (k >= nheads) break;
-        const bool head = (s.head_fl[k] & 8u) != 0;
-        const unsigned long long off = head ? 0ull : rv + (rf ? 0ull : vbase);
-        const uint32_t pop = s.head_pop[k];
-        a.leaf_voff[ubase + k] = (long long)off;
-        const bool grid_last = (k + 1 < nheads) ? (s.head_fl[k + 1] & 8u) != 0 : s.tail_newgrid != 0;
-        if (grid_last) a.grid_vox[s.head_g[k]] = (long long)(off + pop);
-        if (head) {
-          rf = 1;
-          rv = pop;
-        } else {
-          rv += pop;
-        }
+        cg = gj;
+        ce = ej;
       }
     }
-    __syncthreads();
+    if (cg != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * cg + tid], ce);
   }
-
-  // the last block: totals and per-grid offsets
-  stamp(a, 3);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s.last = (atomicAdd(&a.ctl->dedup_ticket, 1u) == gridDim.x - 1) ? 1u : 0u;
-  __syncthreads();
-  if (!s.last) return;
-  __threadfence();
-  const unsigned long long U = __ldcg(&a.ctl->head_totals[0]);
-  const unsigned long long NL = __ldcg(&a.ctl->head_totals[1]);
-  const unsigned long long NU = __ldcg(&a.ctl->head_totals[2]);
-  __syncthreads();
-  if (tid == 0) {
-    a.rb->num_leaves = U;
-    a.rb->num_lowers = NL;
-    a.rb->num_uppers = NU;
-    if (a.last) a.run_start[U] = (uint32_t)S;
+  if (tid == 32) {  // the block's segmented voxel aggregate
+    uint32_t bf = 0;
+    unsigned long long bv = 0;
+    for (int j = 0; j < kThreads / 8; ++j) {
+      bv = s.grp_f[j] ? s.grp_v[j] : bv + s.grp_v[j];
+      bf |= s.grp_f[j];
+    }
+    a.blk_agg[blockIdx.x] = ((unsigned long long)bf << 63) | bv;
   }
-  if (a.last) {
-    suffix_fill(a.first, B, U, a.leaf_off, sm);
-    suffix_fill(a.first + B, B, NL, a.lower_off, sm);
-    suffix_fill(a.first + 2 * B, B, NU, a.upper_off, sm);
-  }
-  stamp(a, 4);
 }
 
-// Phases: 1 emission, 2 digit passes, 3 dedup / merge / count, 4 per-grid offsets.
+// After a grid barrier: each block reads the aggregates of the blocks before
+// it (complete, so no waiting) for its carried-in voxel count; each group then
+// scans its leaves eight at a time and writes their per-grid voxel offsets,
+// and every grid's last leaf writes the grid's voxel total.
+__device__ void phase_voxel_offsets(const PassArgs& a, SmemAll& sa) {
+  SmemLeaves& s = sa.lv;
+  const long long U = (long long)__ldcg(&a.ctl->head_totals[0]);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid & 7, grp = tid >> 3;
+  if (tid < 32) {
+    unsigned long long carry = 0;
+    for (long long base = (long long)blockIdx.x - 1; base >= 0; base -= 32) {
+      const long long b = base - lane;
+      const unsigned long long e = b >= 0 ? __ldcg(a.blk_agg + b) : (1ull << 63);
+      const uint32_t stop = __ballot_sync(0xffffffffu, (e >> 63) != 0);
+      const int first = stop ? __ffs(stop) - 1 : 32;
+      unsigned long long v = (lane <= first && b >= 0) ? (e & ~(1ull << 63)) : 0ull;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+      carry += v;
+      if (first < 32) break;
+    }
+    if (lane == 0) s.blk_prefix = carry;
+  }
+  __syncthreads();
+  const long long C = (U + gridDim.x - 1) / gridDim.x;
+  const long long c = (C + kThreads / 8 - 1) / (kThreads / 8);
+  const long long bbeg = (long long)blockIdx.x * C, bend = bbeg + C < U ? bbeg + C : U;
+  const long long gbeg = bbeg + grp * c, gend = gbeg + c < bend ? gbeg + c : bend;
+  // carried-in value of this group: the block's prefix, then the groups before it
+  unsigned long long cv = s.blk_prefix;
+  for (int j = 0; j < grp; ++j) cv = s.grp_f[j] ? s.grp_v[j] : cv + s.grp_v[j];
+  const uint32_t gmask = 0xFFu << (lane & ~7);
+  for (long long base = gbeg; base < gend; base += 8) {  // uniform within the group
+    const long long u = base + w;
+    const bool valid = u < gend;
+    const uint32_t pop = valid ? __ldcg(a.leaf_pop + u) : 0u;
+    const uint32_t f = valid ? ((__ldcg(a.leaf_upper + u) & kGridFirst) ? 1u : 0u) : 0u;
+    uint32_t Fi = f;
+    unsigned long long Vi = pop;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      const uint32_t F2 = __shfl_up_sync(gmask, Fi, off, 8);
+      const unsigned long long V2 = __shfl_up_sync(gmask, Vi, off, 8);
+      if (w >= off) {
+        if (!Fi) Vi += V2;
+        Fi |= F2;
+      }
+    }
+    uint32_t Fe = __shfl_up_sync(gmask, Fi, 1, 8);
+    unsigned long long Ve = __shfl_up_sync(gmask, Vi, 1, 8);
+    if (w == 0) {
+      Fe = 0;
+      Ve = 0;
+    }
+    const unsigned long long off = f ? 0ull : (Fe ? Ve : cv + Ve);
+    if (valid) {
+      a.leaf_voff[u] = (long long)off;
+      const bool last = (u + 1 == U) || (__ldcg(a.leaf_upper + u + 1) & kGridFirst);
+      if (last) a.grid_vox[__ldcg(a.leaf_g + u)] = (long long)(off + pop);
+    }
+    const uint32_t Ft = __shfl_sync(gmask, Fi, 7, 8);
+    const unsigned long long Vt = __shfl_sync(gmask, Vi, 7, 8);
+    cv = Ft ? Vt : cv + Vt;
+  }
+}
+
+// Phases: 1 emission, 2 digit passes, 3 index, 4 leaves (and offsets).
 template <int OP>
-__device__ void run_pass(const PassArgs& a, GridBarrier* bar, Smem& sm) {
+__device__ void run_pass(const PassArgs& a, GridBarrier* bar, SmemAll& sa) {
   unsigned int* err = &a.rb->err;
   stamp(a, 0);
-  phase_emit<OP>(a, sm);
+  phase_emit<OP>(a, sa.u);
   stamp(a, 1);
   grid_sync(bar, err);
   for (int d = 0; d < a.P; ++d) {
-    phase_sort(a, d, sm);
+    phase_sort(a, d, sa.u);
     grid_sync(bar, err);
   }
   stamp(a, 2);
-  phase_dedup<OP>(a, sm);
-  if (!a.last) grid_sync(bar, err);
+  phase_index(a, sa.u);
+  stamp(a, 3);
+  grid_sync(bar, err);
+  if (blockIdx.x == gridDim.x - 1) phase_finish(a, sa.u);  // the block with the fewest leaves
+  phase_leaves<OP>(a, sa);
+  grid_sync(bar, err);
+  if (a.last) phase_voxel_offsets(a, sa);
+  stamp(a, 4);
 }
 
 __global__ void __launch_bounds__(kThreads) k_chain(const __grid_constant__ ChainArgs c) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  SmemAll& sa = *reinterpret_cast<SmemAll*>(smem_raw);
   for (int p = 0; p < c.n_pass; ++p) {
     const PassArgs& a = c.pass[p];
     switch (a.op) {
-      case kIjk: run_pass<kIjk>(a, c.bar, sm); break;
-      case kLeaves: run_pass<kLeaves>(a, c.bar, sm); break;
-      case kRefine: run_pass<kRefine>(a, c.bar, sm); break;
-      case kCoarsen: run_pass<kCoarsen>(a, c.bar, sm); break;
-      default: run_pass<kDilate>(a, c.bar, sm); break;
+      case kIjk: run_pass<kIjk>(a, c.bar, sa); break;
+      case kLeaves: run_pass<kLeaves>(a, c.bar, sa); break;
+      case kRefine: run_pass<kRefine>(a, c.bar, sa); break;
+      case kCoarsen: run_pass<kCoarsen>(a, c.bar, sa); break;
+      default: run_pass<kDilate>(a, c.bar, sa); break;
     }
   }
 }
@@ -861,12 +874,12 @@ __global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, cons
       if (u == 0 || a.leaf_lower[u - 1] != lw) {
 #pragma unroll
         for (int c = 0; c < 3; ++c) o.lower_origins[3 * (long long)lw + c] = (int32_t)((uint32_t)org[c] & ~127u);
-        o.lower_parent[lw] = (int32_t)((long long)a.leaf_upper[u] - a.upper_off[g]);
+        o.lower_parent[lw] = (int32_t)((long long)(a.leaf_upper[u] & ~kGridFirst) - a.upper_off[g]);
       }
     }
     if (w == 5) {
-      const uint32_t up = a.leaf_upper[u];
-      if (u == 0 || a.leaf_upper[u - 1] != up) {
+      const uint32_t up = a.leaf_upper[u] & ~kGridFirst;
+      if (u == 0 || (a.leaf_upper[u - 1] & ~kGridFirst) != up) {
 #pragma unroll
         for (int c = 0; c < 3; ++c) o.upper_origins[3 * (long long)up + c] = (int32_t)((uint32_t)org[c] & ~4095u);
       }
@@ -883,19 +896,20 @@ int write_occupancy() {
 
 }  // namespace
 
-size_t chain_smem_bytes() { return sizeof(Smem); }
+size_t chain_smem_bytes() { return sizeof(SmemAll); }
 
 int chain_occupancy() {
   int n = 0;
-  if (cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)) != cudaSuccess)
+  if (cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SmemAll)) !=
+      cudaSuccess)
     return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_chain, kThreads, sizeof(Smem)) != cudaSuccess) n = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_chain, kThreads, sizeof(SmemAll)) != cudaSuccess) n = 1;
   return n > 0 ? n : 1;
 }
 
 cudaError_t launch_chain(const ChainArgs& c, int blocks, cudaStream_t s) {
   void* args[] = {(void*)&c};
-  return cudaLaunchCooperativeKernel((const void*)k_chain, dim3(blocks), dim3(kThreads), args, sizeof(Smem), s);
+  return cudaLaunchCooperativeKernel((const void*)k_chain, dim3(blocks), dim3(kThreads), args, sizeof(SmemAll), s);
 }
 
 int write_final_occupancy(int op) {

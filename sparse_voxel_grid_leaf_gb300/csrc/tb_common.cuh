@@ -107,6 +107,7 @@ struct PassArgs {
   int32_t B;
   int32_t P;              // digit passes
   int32_t last;           // 1: final pass (count phase), 0: intermediate (hands leaves on)
+  int32_t tchunk;         // targets per emission thread (1 .. targets per source)
   int32_t lo[3], hi[3];   // box of a dilation pass
   // source
   const int32_t* ijk;            // kIjk: [N,3]
@@ -126,7 +127,7 @@ struct PassArgs {
   PassCtl* ctl;
   uint32_t* sort_status;             // [P][sort_tiles_cap][256]
   long long sort_tiles_cap;
-  unsigned long long* dedup_status;  // [dedup_tiles_cap][4]: leaves, lower nodes, upper nodes, voxels
+  unsigned long long* dedup_status;  // [dedup_tiles_cap][3]: leaves, lower nodes, upper nodes
   uint32_t* first;                   // [3][B]: 1 + first leaf / lower / upper index of each grid
   long long slot_cap;
   // slot buffers (not zeroed)
@@ -136,7 +137,10 @@ struct PassArgs {
   uint32_t* run_start;   // [slot_cap + 1]
   uint32_t* leaf_lower;  // [slot_cap]
   uint32_t* leaf_upper;  // [slot_cap]
-  int64_t* leaf_voff;    // [slot_cap] voxel offset of each unique leaf (final pass)
+  int64_t* leaf_voff;    // [slot_cap] voxel offset of each unique leaf (last pass)
+  uint32_t* leaf_pop;    // [slot_cap] voxels of each unique leaf (last pass)
+  uint32_t* leaf_g;      // [slot_cap] grid of each unique leaf (last pass)
+  unsigned long long* blk_agg;  // [gridDim.x] segmented voxel aggregate per block (last pass)
   unsigned long long* phase_ts;  // optional [8] globaltimer stamps (profiling), else null
   // intermediate output (next pass's source)
   int32_t* out_origins;

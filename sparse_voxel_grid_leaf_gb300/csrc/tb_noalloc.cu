@@ -137,20 +137,24 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
     return r;
   };
   const size_t o_bar = take(sizeof(GridBarrier)), o_rb = take(rbb), o_ctl = take(sizeof(PassCtl)),
-               o_sort = take((size_t)a.P * sort_tiles * kBins * 4), o_dedup = take((size_t)dedup_tiles * 32),
+               o_sort = take((size_t)a.P * sort_tiles * kBins * 4), o_dedup = take((size_t)dedup_tiles * 24),
                o_first = take((size_t)3 * B * 4);
   const size_t zero_begin = o_bar, zero_end = off;
   const size_t o_k0 = take((size_t)S * 8), o_k1 = take((size_t)S * 8), o_v0 = take((size_t)S * 4),
                o_v1 = take((size_t)S * 4), o_run = take((size_t)(S + 1) * 4), o_ll = take((size_t)S * 4),
-               o_lu = take((size_t)S * 4), o_voff = take((size_t)S * 8);
+               o_lu = take((size_t)S * 4), o_voff = take((size_t)S * 8), o_pop = take((size_t)S * 4),
+               o_lg = take((size_t)S * 4);
+  const int G = sms * chain_occupancy();
+  const size_t o_blk = take((size_t)G * 8);
   if (off > kStaticScratchBytes)
     return static_fail(TB_ERR_TOO_LARGE,
-                       "tb_refine_static: input needs more than the 32 MiB static scratch (about 90k leaves)");
+                       "tb_refine_static: input needs more than the 32 MiB static scratch (about 75k leaves)");
   TB_STATIC_CUDA(cudaMemsetAsync(scratch + zero_begin, 0, zero_end - zero_begin, stream));
 
   a.op = kRefine;
   a.B = B;
   a.last = 1;
+  a.tchunk = (int32_t)std::max(1ll, std::min(8ll, (8 * L + (long long)G * 256 - 1) / ((long long)G * 256)));
   a.src_origins = origins;
   a.src_masks = masks;
   a.src_grid = nullptr;
@@ -177,6 +181,9 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   a.leaf_lower = (uint32_t*)(scratch + o_ll);
   a.leaf_upper = (uint32_t*)(scratch + o_lu);
   a.leaf_voff = (int64_t*)(scratch + o_voff);
+  a.leaf_pop = (uint32_t*)(scratch + o_pop);
+  a.leaf_g = (uint32_t*)(scratch + o_lg);
+  a.blk_agg = (unsigned long long*)(scratch + o_blk);
 
   // ---- the same cooperative pass kernel as tb_refine
   ChainArgs ca;
@@ -184,8 +191,7 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   ca.n_pass = 1;
   ca.bar = (GridBarrier*)(scratch + o_bar);
   ca.pass[0] = a;
-  const long long work = std::max({(L + 255) / 256, sort_tiles, dedup_tiles, 1ll});
-  TB_STATIC_CUDA(launch_chain(ca, blocks_of(work, 1, (long long)sms * chain_occupancy()), stream));
+  TB_STATIC_CUDA(launch_chain(ca, G, stream));
   ReadbackHeader r;
   TB_STATIC_CUDA(cudaMemcpyAsync(&r, a.rb, sizeof r, cudaMemcpyDeviceToHost, stream));
   TB_STATIC_CUDA(cudaStreamSynchronize(stream));
