@@ -54,6 +54,7 @@ def parse():
     p.add_argument("--workload", default="shells_b16_res64")
     p.add_argument("--no-extra", action="store_true", help="skip the per-op and larger-workload tables")
     p.add_argument("--cpu-sample-steps", type=int, default=2)
+    p.add_argument("--separate", action="store_true", help="one C-ABI call per chain instead of one tb_multi call")
     return p.parse_args()
 
 
@@ -207,13 +208,21 @@ def run_reference(args):
 
 # ------------------------------------------------------------------ our arm
 
+SEPARATE = False  # --separate: one C-ABI call per chain instead of one tb_multi call
+
+
 def run_step(tb, b_src, inputs):
-    """Runs the step's calls; returns (batches, outputs by label)."""
+    """Runs the step: the ijk front end, then every chain on its output (one
+    tb_multi call, or one call per chain); returns the batches by label."""
     out = {}
     b0 = tb.from_ijk(*inputs)
     out["from_ijk"] = b0
-    for label, ops in STEP[1:]:
-        out[label] = tb.chain(b0, ops)
+    if SEPARATE:
+        for label, ops in STEP[1:]:
+            out[label] = tb.chain(b0, ops)
+    else:
+        for (label, _), b in zip(STEP[1:], tb.multi(b0, [ops for _, ops in STEP[1:]])):
+            out[label] = b
     return out
 
 
@@ -434,7 +443,8 @@ def run_ours(args):
             "config": {"workload": args.workload, "B": len(off) - 1, "input_voxels": int(len(ijk)),
                        "step": [s for s, _ in STEP], "passes_per_step": len(ps),
                        "output_voxels_per_step": voxels, "output_voxels_by_call": per_label,
-                       "l2": "flushed before every step (256 MB write, untimed)", "inputs": "device-resident"},
+                       "l2": "flushed before every step (256 MB write, untimed)", "inputs": "device-resident",
+                       "calls": "from_ijk + one call per chain" if SEPARATE else "from_ijk + one tb_multi call"},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms / len(e2e_times)},
             "roofline": roofline,
@@ -459,7 +469,8 @@ def per_op_tables(tb, torch, synth, stream, flush, main_workload):
         b0 = tb.from_ijk(ijk_d, off_d)
         row = {}
         calls = [("from_ijk", lambda: tb.from_ijk(ijk_d, off_d))] + \
-                [(lab, (lambda o=o: tb.chain(b0, o))) for lab, o in ops]
+                [(lab, (lambda o=o: tb.chain(b0, o))) for lab, o in ops] + \
+                [("multi_all", lambda: tb.multi(b0, [o for _, o in ops]))]
         for lab, fn in calls:
             ts = []
             vox = 0
@@ -470,9 +481,11 @@ def per_op_tables(tb, torch, synth, stream, flush, main_workload):
                 r = fn()
                 e.record(stream)
                 e.synchronize()
+                rs = r if isinstance(r, list) else [r]
                 if it == 0:
-                    vox = int(r.to_numpy(["voxel_counts"])["voxel_counts"].sum())
-                r.free()
+                    vox = sum(int(x.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for x in rs)
+                for x in rs:
+                    x.free()
                 if it >= 5:
                     ts.append(s.elapsed_time(e))
             med = statistics.median(ts)
@@ -483,7 +496,9 @@ def per_op_tables(tb, torch, synth, stream, flush, main_workload):
 
 
 def main():
+    global SEPARATE
     args = parse()
+    SEPARATE = args.separate
     if args.impl == "reference":
         run_reference(args)
     else:

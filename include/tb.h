@@ -182,6 +182,18 @@ TB_API tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const in
 TB_API tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, const tb_allocator* alloc,
                    tb_stream stream, tb_batch** out);
 
+/* Several chains over the same input in one call: chain c applies
+ * chain_lengths[c] ops taken in order from `ops` (the chains' ops are
+ * concatenated); outs[c] receives its result (a copy of the input when its
+ * length is 0).  All chains run in one cooperative launch, phase by phase, so
+ * they share the grid barriers, the readback and the call's host overhead --
+ * the batching of PR #757 (Summary) extended from batch members to the
+ * several topologies a convolution plan derives from one grid.  Results equal
+ * those of separate tb_chain calls.  On error every outs[c] is NULL.
+ * Limit: n_chains <= 1024. */
+TB_API tb_status tb_multi(const tb_batch* in, const tb_op* ops, const int32_t* chain_lengths, int32_t n_chains,
+                          const tb_allocator* alloc, tb_stream stream, tb_batch** outs);
+
 /* Checks the canonical-batch invariants on the device: origins multiples of
  * 8, masks non-zero, leaf_grid consistent with leaf_offsets, leaves strictly
  * increasing in canonical order within each grid.  Blocks once.  Returns

@@ -87,6 +87,7 @@ def lib():
                 "tb_coarsen": [vp, i32, vp, vp, pp],
                 "tb_box_dilate": [vp, vp, vp, vp, vp, pp],
                 "tb_chain": [vp, vp, i32, vp, vp, pp],
+                "tb_multi": [vp, vp, vp, i32, vp, vp, pp],
                 "tb_validate": [vp, vp],
                 "tb_batch_get_view": [vp, ctypes.POINTER(_View)],
                 "tb_batch_export": [vp, vp, vp, vp, vp, vp],
@@ -359,6 +360,19 @@ def make_ops(ops: Iterable[Tuple]):
 def chain(b: Batch, ops: Iterable[Tuple], stream=None) -> Batch:
     arr, n = make_ops(ops)
     return _new(lib().tb_chain, b.handle, arr, n, None, ctypes.c_void_p(_stream(stream)))
+
+
+def multi(b: Batch, chains: Sequence[Iterable[Tuple]], stream=None) -> list:
+    """Several chains of ops over the same batch in one call (one launch, one
+    readback); returns one batch per chain."""
+    chains = [list(c) for c in chains]
+    flat = [op for c in chains for op in c]
+    arr, _ = make_ops(flat)
+    lens = (ctypes.c_int32 * len(chains))(*[len(c) for c in chains])
+    outs = (ctypes.c_void_p * len(chains))()
+    _check(lib().tb_multi(b.handle, arr, lens, len(chains), None, ctypes.c_void_p(_stream(stream)),
+                          ctypes.cast(outs, ctypes.POINTER(ctypes.c_void_p))))
+    return [Batch(outs[i]) for i in range(len(chains))]
 
 
 # Convolution-topology aliases named by fVDB PR #757 (Summary and Measurements).

@@ -352,12 +352,79 @@ int blocks_for(long long work, long long per_block, long long cap) {
 
 // ---------------------------------------------------------------- the driver
 
-tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_allocator* alloc,
-              cudaStream_t stream, tb_batch** out) {
-  if (!out) return fail(TB_ERR_INVALID_ARG, "out is NULL");
-  *out = nullptr;
+// Allocates the exact output arrays of a batch whose sizes (B, L, NL, NU)
+// are set, in one allocation carved into 256-byte-aligned arrays.
+tb_status alloc_outputs(tb_batch* b, const Mem& mem) {
+  const int64_t B = b->B, L = b->L, NL = b->NL, NU = b->NU;
+  Carve oc;
+  size_t off[16];
+  off[0] = oc.take((size_t)(B + 1) * 8);
+  off[1] = oc.take((size_t)L * 12);
+  off[2] = oc.take((size_t)L * 64);
+  off[3] = oc.take((size_t)L * 8);
+  off[4] = oc.take((size_t)L * 8);
+  off[5] = oc.take((size_t)L * 24);
+  off[6] = oc.take((size_t)L * 4);
+  off[7] = oc.take((size_t)L * 4);
+  off[8] = oc.take((size_t)B * 8);
+  off[9] = oc.take((size_t)B * 24);
+  off[10] = oc.take((size_t)B * 12);
+  off[11] = oc.take((size_t)(B + 1) * 8);
+  off[12] = oc.take((size_t)(B + 1) * 8);
+  off[13] = oc.take((size_t)NL * 12);
+  off[14] = oc.take((size_t)NL * 4);
+  off[15] = oc.take((size_t)NU * 12);
+  b->mem = mem.get(oc.off);
+  if (!b->mem) return fail(TB_ERR_OOM, "output allocation of %zu bytes failed", oc.off);
+  batch_set_view(b, (char*)b->mem, off);
+  auto nz = [](void* p, int64_t n) { return n > 0 ? p : nullptr; };
+  b->origins = (int32_t*)nz(b->origins, L);
+  b->masks = (uint64_t*)nz(b->masks, L);
+  b->voxel_offset = (int64_t*)nz(b->voxel_offset, L);
+  b->word_prefix = (uint64_t*)nz(b->word_prefix, L);
+  b->leaf_bbox = (int32_t*)nz(b->leaf_bbox, L);
+  b->leaf_grid = (int32_t*)nz(b->leaf_grid, L);
+  b->leaf_parent = (int32_t*)nz(b->leaf_parent, L);
+  b->voxel_counts = (int64_t*)nz(b->voxel_counts, B);
+  b->grid_bbox = (int32_t*)nz(b->grid_bbox, B);
+  b->node_counts = (int32_t*)nz(b->node_counts, B);
+  b->lower_origins = (int32_t*)nz(b->lower_origins, NL);
+  b->lower_parent = (int32_t*)nz(b->lower_parent, NL);
+  b->upper_origins = (int32_t*)nz(b->upper_origins, NU);
+  return TB_OK;
+}
+
+void fill_write_out(const tb_batch* b, WriteOut& wo) {
+  wo.origins = b->origins;
+  wo.masks = b->masks;
+  wo.leaf_grid = b->leaf_grid;
+  wo.voxel_offset = b->voxel_offset;
+  wo.word_prefix = b->word_prefix;
+  wo.leaf_bbox = b->leaf_bbox;
+  wo.leaf_parent = b->leaf_parent;
+  wo.voxel_counts = b->voxel_counts;
+  wo.grid_bbox = b->grid_bbox;
+  wo.node_counts = b->node_counts;
+  wo.leaf_offsets = b->leaf_offsets;
+  wo.lower_offsets = b->lower_offsets;
+  wo.upper_offsets = b->upper_offsets;
+  wo.lower_origins = b->lower_origins;
+  wo.lower_parent = b->lower_parent;
+  wo.upper_origins = b->upper_origins;
+}
+
+// Runs n chains of passes over one source in one cooperative launch and
+// writes one output batch per chain (outs[c]).  A front-end source (ijk or
+// leaves) takes exactly one chain.
+tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chains, const tb_allocator* alloc,
+              cudaStream_t stream, tb_batch** outs) {
+  const int n_chain = (int)chains.size();
+  if (!outs) return fail(TB_ERR_INVALID_ARG, "out is NULL");
+  for (int ch = 0; ch < n_chain; ++ch) outs[ch] = nullptr;
   if (alloc && (!alloc->alloc || !alloc->free)) return fail(TB_ERR_INVALID_ARG, "allocator without alloc/free");
-  if (specs.empty()) return fail(TB_ERR_INVALID_ARG, "no passes");
+  if (n_chain == 0) return fail(TB_ERR_INVALID_ARG, "no chains");
+  for (const auto& c : chains)
+    if (c.empty()) return fail(TB_ERR_INVALID_ARG, "a chain without passes");
   const auto t_entry = std::chrono::steady_clock::now();
   int dev = 0;
   TB_CUDA(cudaGetDevice(&dev));
@@ -367,65 +434,97 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
   const Mem mem{alloc, stream};
   const int32_t B = src.B;
   const bool front = src.kind != kSrcBatch;
+  if (front && n_chain != 1) return fail(TB_ERR_INVALID_ARG, "a front end runs one chain");
   const size_t rb_bytes = readback_bytes(B);
+  const size_t rb_stride = (rb_bytes + 255) & ~(size_t)255;
+  const int G = di->sms * di->occ_chain;  // every co-resident block
 
   // ---- bounds of every pass (host-known, no readback)
-  std::vector<PassPlan> plans(specs.size());
-  long long cap = src.count;
-  long long max_slots = 0, max_inter = 0;
-  for (size_t p = 0; p < specs.size(); ++p) {
-    PassPlan& pl = plans[p];
-    pl.spec = specs[p];
-    pl.in_cap = cap;
-    if (pl.spec.op != kIjk && cap >= (1ll << (32 - kSrcShift)))
-      return fail(TB_ERR_TOO_LARGE, "pass %zu: %lld source leaves exceed the limit of 2^27", p, cap);
-    pl.slot_cap = cap * slots_per_source(pl.spec);
-    if (pl.slot_cap >= (1ll << 30))
-      return fail(TB_ERR_TOO_LARGE, "pass %zu: up to %lld candidate leaves exceed the limit of 2^30", p,
-                  pl.slot_cap);
-    cap = pl.slot_cap;
-    max_slots = std::max(max_slots, pl.slot_cap);
-    if (p + 1 < specs.size()) max_inter = std::max(max_inter, pl.slot_cap);
+  std::vector<std::vector<PassPlan>> plans(n_chain);
+  int n_stage = 0;
+  for (int ch = 0; ch < n_chain; ++ch) {
+    plans[ch].resize(chains[ch].size());
+    n_stage = std::max(n_stage, (int)chains[ch].size());
+    long long cap = src.count;
+    for (size_t p = 0; p < chains[ch].size(); ++p) {
+      PassPlan& pl = plans[ch][p];
+      pl.spec = chains[ch][p];
+      pl.in_cap = cap;
+      if (pl.spec.op != kIjk && cap >= (1ll << (32 - kSrcShift)))
+        return fail(TB_ERR_TOO_LARGE, "pass %zu: %lld source leaves exceed the limit of 2^27", p, cap);
+      pl.slot_cap = cap * slots_per_source(pl.spec);
+      if (pl.slot_cap >= (1ll << 30))
+        return fail(TB_ERR_TOO_LARGE, "pass %zu: up to %lld candidate leaves exceed the limit of 2^30", p,
+                    pl.slot_cap);
+      cap = pl.slot_cap;
+    }
   }
-  const long long last_slots = plans.back().slot_cap;
 
   // ---- key layouts (front ends: after the range prepass)
-  if (!front) {
-    st = plan_layouts(plans, B, src.batch->bbox, src.batch->L == 0);
-    if (st != TB_OK) return st;
-  } else {
-    for (auto& pl : plans) pl.P = kMaxDigitPasses;  // sized for the widest key until the prepass
+  for (auto& pc : plans) {
+    if (!front) {
+      st = plan_layouts(pc, B, src.batch->bbox, src.batch->L == 0);
+      if (st != TB_OK) return st;
+    } else {
+      for (auto& pl : pc) pl.P = kMaxDigitPasses;  // sized for the widest key until the prepass
+    }
   }
 
-  // ---- workspace: a zeroed control region, then the slot buffers
-  const int n_launch = (int)((plans.size() + kMaxChainPasses - 1) / kMaxChainPasses);
+  // ---- workspace: a zeroed control region (the call's error word and the
+  // last passes' readback blocks first, so one copy reads them all), then the
+  // slot buffers of every chain
   Carve c;
-  const size_t o_bar = c.take(sizeof(GridBarrier) * n_launch);
-  for (auto& pl : plans) {
-    pl.sort_tiles = std::max(1ll, (pl.slot_cap + kSortTile - 1) / kSortTile);
-    pl.dedup_tiles = std::max(1ll, (pl.slot_cap + kDedupTile - 1) / kDedupTile);
-    pl.rb = c.take(rb_bytes);
-    pl.ctl = c.take(sizeof(PassCtl));
-    pl.sort_status = c.take((size_t)pl.P * pl.sort_tiles * kBins * 4);
-    pl.dedup_status = c.take((size_t)pl.dedup_tiles * 3 * 8);
-    pl.first = c.take((size_t)3 * B * 4);
-  }
-  const size_t o_ts = c.take(t_prof >= 2 ? plans.size() * 8 * sizeof(unsigned long long) : 0);
+  const size_t o_err = c.take(256);
+  std::vector<size_t> o_rb_last(n_chain);
+  for (int ch = 0; ch < n_chain; ++ch) o_rb_last[ch] = c.take(rb_stride);
+  const size_t readback_span = c.off;
+  const size_t o_bar = c.take(sizeof(GridBarrier));
+  for (int ch = 0; ch < n_chain; ++ch)
+    for (size_t p = 0; p < plans[ch].size(); ++p) {
+      PassPlan& pl = plans[ch][p];
+      pl.sort_tiles = std::max(1ll, (pl.slot_cap + kSortTile - 1) / kSortTile);
+      pl.dedup_tiles = std::max(1ll, (pl.slot_cap + kDedupTile - 1) / kDedupTile);
+      pl.rb = p + 1 == plans[ch].size() ? o_rb_last[ch] : c.take(rb_bytes);
+      pl.ctl = c.take(sizeof(PassCtl));
+      pl.sort_status = c.take((size_t)pl.P * pl.sort_tiles * kBins * 4);
+      pl.dedup_status = c.take((size_t)pl.dedup_tiles * 3 * 8);
+      pl.first = c.take((size_t)3 * B * 4);
+    }
+  size_t n_pass_total = 0;
+  for (auto& pc : plans) n_pass_total += pc.size();
+  const size_t o_ts = c.take(t_prof >= 2 ? n_pass_total * 8 * sizeof(unsigned long long) : 0);
   const size_t zero_bytes = c.off;
-  const size_t o_keys0 = c.take((size_t)max_slots * 8), o_keys1 = c.take((size_t)max_slots * 8);
-  const size_t o_vals0 = c.take((size_t)max_slots * 4), o_vals1 = c.take((size_t)max_slots * 4);
-  const size_t o_run = c.take((size_t)(max_slots + 1) * 4);
-  const size_t o_llow = c.take((size_t)max_slots * 4), o_lup = c.take((size_t)max_slots * 4);
-  const size_t o_voff = c.take((size_t)last_slots * 8);
-  const size_t o_pop = c.take((size_t)last_slots * 4), o_lg = c.take((size_t)last_slots * 4);
-  const int G = di->sms * di->occ_chain;  // every co-resident block
-  const size_t o_blk = c.take((size_t)G * 8);
-  size_t o_inter[2][3];
-  for (int k = 0; k < 2; ++k) {
-    o_inter[k][0] = c.take((size_t)max_inter * 12);
-    o_inter[k][1] = c.take((size_t)max_inter * 64);
-    o_inter[k][2] = c.take((size_t)max_inter * 4);
+  struct ChainBufs {
+    size_t keys0, keys1, vals0, vals1, run, llow, lup, voff, pop, lg, blk, grp, inter[2][3];
+  };
+  std::vector<ChainBufs> cb(n_chain);
+  for (int ch = 0; ch < n_chain; ++ch) {
+    long long max_slots = 0, max_inter = 0;
+    for (size_t p = 0; p < plans[ch].size(); ++p) {
+      max_slots = std::max(max_slots, plans[ch][p].slot_cap);
+      if (p + 1 < plans[ch].size()) max_inter = std::max(max_inter, plans[ch][p].slot_cap);
+    }
+    const long long last_slots = plans[ch].back().slot_cap;
+    ChainBufs& b = cb[ch];
+    b.keys0 = c.take((size_t)max_slots * 8);
+    b.keys1 = c.take((size_t)max_slots * 8);
+    b.vals0 = c.take((size_t)max_slots * 4);
+    b.vals1 = c.take((size_t)max_slots * 4);
+    b.run = c.take((size_t)(max_slots + 1) * 4);
+    b.llow = c.take((size_t)last_slots * 4);
+    b.lup = c.take((size_t)last_slots * 4);
+    b.voff = c.take((size_t)last_slots * 8);
+    b.pop = c.take((size_t)last_slots * 4);
+    b.lg = c.take((size_t)last_slots * 4);
+    b.blk = c.take((size_t)G * 8);
+    b.grp = c.take((size_t)G * 32 * 8);
+    for (int k = 0; k < 2; ++k) {
+      b.inter[k][0] = c.take((size_t)max_inter * 12);
+      b.inter[k][1] = c.take((size_t)max_inter * 64);
+      b.inter[k][2] = c.take((size_t)max_inter * 4);
+    }
   }
+  const size_t o_args = c.take(sizeof(PassArgs) * (size_t)n_chain * n_stage);
   // staging of host-resident inputs
   const int32_t* in_ijk = src.ijk;
   const int32_t* in_orig = src.origins;
@@ -466,13 +565,18 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     TB_CUDA(cudaMemcpyAsync(ws + o_st_off, src.offsets, (size_t)(B + 1) * 8, cudaMemcpyDefault, stream));
     in_off = (const int64_t*)(ws + o_st_off);
   }
-  ReadbackHeader* host_rb =
-      (ReadbackHeader*)t_pinned.get(rb_bytes + 4 * plans.size() + 64 * plans.size() + 64);
-  if (!host_rb) return fail(TB_ERR_OOM, "pinned host buffer of %zu bytes failed", rb_bytes);
+  // pinned host memory: readback span | phase stamps | pass arguments
+  const size_t args_bytes = sizeof(PassArgs) * (size_t)n_chain * n_stage;
+  const size_t ts_bytes = t_prof >= 2 ? n_pass_total * 64 : 0;
+  char* pinned = (char*)t_pinned.get(readback_span + ts_bytes + args_bytes + 64);
+  if (!pinned) return fail(TB_ERR_OOM, "pinned host buffer failed");
+  unsigned long long* host_ts = (unsigned long long*)(pinned + readback_span);
+  PassArgs* host_args = (PassArgs*)(pinned + readback_span + ts_bytes);
+  const ReadbackHeader* host_rb0 = (const ReadbackHeader*)(pinned + o_rb_last[0]);
 
   // ---- front ends: range prepass and its readback
   if (front) {
-    ReadbackHeader* rb0 = (ReadbackHeader*)(ws + plans[0].rb);
+    ReadbackHeader* rb0 = (ReadbackHeader*)(ws + plans[0][0].rb);
     const int blocks = blocks_for(src.count, 256, (long long)di->sms * 4);
     if (src.kind == kSrcIjk)
       TB_CUDA(launch(kKPrepassIjk, stream,
@@ -481,118 +585,117 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
       TB_CUDA(launch(kKPrepassLeaves, stream, [&] {
         return launch_prepass_leaves(in_orig, in_mask, src.count, in_off, B, rb0, blocks, stream);
       }));
-    TB_CUDA(cudaMemcpyAsync(host_rb, rb0, sizeof(ReadbackHeader), cudaMemcpyDeviceToHost, stream));
+    TB_CUDA(cudaMemcpyAsync((void*)host_rb0, rb0, sizeof(ReadbackHeader), cudaMemcpyDeviceToHost, stream));
     TB_CUDA(cudaStreamSynchronize(stream));
-    if (host_rb->err & kErrBadOffsets)
+    if (host_rb0->err & kErrBadOffsets)
       return fail(TB_ERR_INVALID_ARG, "offsets must start at 0, be non-decreasing and end at %lld", src.count);
-    if (host_rb->err & kErrNotAligned) return fail(TB_ERR_INVALID_ARG, "leaf origins must be multiples of 8");
+    if (host_rb0->err & kErrNotAligned) return fail(TB_ERR_INVALID_ARG, "leaf origins must be multiples of 8");
     int32_t bb[6];
     for (int a = 0; a < 3; ++a) {
-      bb[a] = dec_min(host_rb->bbox_enc[a]);
-      bb[3 + a] = dec_max(host_rb->bbox_enc[3 + a]);
+      bb[a] = dec_min(host_rb0->bbox_enc[a]);
+      bb[3 + a] = dec_max(host_rb0->bbox_enc[3 + a]);
     }
-    const int P_alloc = plans[0].P;
-    st = plan_layouts(plans, B, bb, bb[0] > bb[3]);
+    const int P_alloc = plans[0][0].P;
+    st = plan_layouts(plans[0], B, bb, bb[0] > bb[3]);
     if (st != TB_OK) return st;
-    if (plans[0].P > P_alloc) return fail(TB_ERR_CUDA, "internal: digit passes exceed the allocation");
-    // the prepass wrote the bbox into the pass header; the pass accumulates on top of zeroed counters only
+    if (plans[0][0].P > P_alloc) return fail(TB_ERR_CUDA, "internal: digit passes exceed the allocation");
   }
 
-  // ---- pass arguments
-  std::vector<PassArgs> args(plans.size());
-  for (size_t p = 0; p < plans.size(); ++p) {
-    PassPlan& pl = plans[p];
-    PassArgs& a = args[p];
-    std::memset(&a, 0, sizeof a);
-    a.K = pl.K;
-    a.op = pl.spec.op;
-    a.B = B;
-    a.P = pl.P;
-    a.last = p + 1 == plans.size();
-    {  // targets per emission thread: about one round of the grid's threads
-      const long long T = slots_per_source(pl.spec);
-      const long long want = (pl.in_cap * T + (long long)G * 256 - 1) / ((long long)G * 256);
-      a.tchunk = (int32_t)std::max(1ll, std::min(T, want));
-    }
-    for (int ax = 0; ax < 3; ++ax) {
-      a.lo[ax] = pl.spec.lo[ax];
-      a.hi[ax] = pl.spec.hi[ax];
-    }
-    if (p == 0) {
-      a.ijk = in_ijk;
-      a.in_offsets = in_off;
-      if (src.kind == kSrcBatch) {
-        a.src_origins = src.batch->origins;
-        a.src_masks = src.batch->masks;
-        a.src_grid = src.batch->leaf_grid;
-        a.src_count = src.batch->L;
-      } else {
-        a.src_origins = in_orig;
-        a.src_masks = in_mask;
-        a.src_count = src.count;
+  // ---- pass arguments, [chain][stage], copied to the device
+  size_t pass_index = 0;
+  for (int ch = 0; ch < n_chain; ++ch) {
+    const ChainBufs& bf = cb[ch];
+    for (int k = 0; k < n_stage; ++k) {
+      PassArgs& a = host_args[(size_t)ch * n_stage + k];
+      std::memset(&a, 0, sizeof a);
+      a.op = -1;
+      if (k >= (int)plans[ch].size()) continue;
+      const PassPlan& pl = plans[ch][k];
+      a.K = pl.K;
+      a.op = pl.spec.op;
+      a.B = B;
+      a.P = pl.P;
+      a.last = k + 1 == (int)plans[ch].size();
+      {  // targets per emission thread: about one round of the grid's threads
+        const long long T = slots_per_source(pl.spec);
+        const long long want = (pl.in_cap * T + (long long)G * 256 - 1) / ((long long)G * 256);
+        a.tchunk = (int32_t)std::max(1ll, std::min(T, want));
       }
-    } else {
-      const PassArgs& prev = args[p - 1];
-      a.src_origins = prev.out_origins;
-      a.src_masks = prev.out_masks;
-      a.src_grid = prev.out_grid;
-      a.src_count_dev = &prev.rb->num_leaves;
-    }
-    a.rb = (ReadbackHeader*)(ws + pl.rb);
-    a.leaf_off = (int64_t*)(ws + pl.rb + sizeof(ReadbackHeader));
-    a.lower_off = a.leaf_off + (B + 1);
-    a.upper_off = a.lower_off + (B + 1);
-    a.grid_vox = a.upper_off + (B + 1);
-    a.gbox = (unsigned int*)(a.grid_vox + B);
-    a.ctl = (PassCtl*)(ws + pl.ctl);
-    a.sort_status = (uint32_t*)(ws + pl.sort_status);
-    a.sort_tiles_cap = pl.sort_tiles;
-    a.dedup_status = (unsigned long long*)(ws + pl.dedup_status);
-    a.first = (uint32_t*)(ws + pl.first);
-    a.slot_cap = pl.slot_cap;
-    a.keys[0] = (uint64_t*)(ws + o_keys0);
-    a.keys[1] = (uint64_t*)(ws + o_keys1);
-    a.vals[0] = (uint32_t*)(ws + o_vals0);
-    a.vals[1] = (uint32_t*)(ws + o_vals1);
-    a.sorted = pl.P & 1;
-    a.run_start = (uint32_t*)(ws + o_run);
-    a.leaf_lower = (uint32_t*)(ws + o_llow);
-    a.leaf_upper = (uint32_t*)(ws + o_lup);
-    a.leaf_voff = (int64_t*)(ws + o_voff);
-    a.leaf_pop = (uint32_t*)(ws + o_pop);
-    a.leaf_g = (uint32_t*)(ws + o_lg);
-    a.blk_agg = (unsigned long long*)(ws + o_blk);
-    a.phase_ts = t_prof >= 2 ? (unsigned long long*)(ws + o_ts) + 8 * p : nullptr;
-    if (!a.last) {
-      const int k = (int)(p & 1);
-      a.out_origins = (int32_t*)(ws + o_inter[k][0]);
-      a.out_masks = (uint64_t*)(ws + o_inter[k][1]);
-      a.out_grid = (int32_t*)(ws + o_inter[k][2]);
+      for (int ax = 0; ax < 3; ++ax) {
+        a.lo[ax] = pl.spec.lo[ax];
+        a.hi[ax] = pl.spec.hi[ax];
+      }
+      if (k == 0) {
+        a.ijk = in_ijk;
+        a.in_offsets = in_off;
+        if (src.kind == kSrcBatch) {
+          a.src_origins = src.batch->origins;
+          a.src_masks = src.batch->masks;
+          a.src_grid = src.batch->leaf_grid;
+          a.src_count = src.batch->L;
+        } else {
+          a.src_origins = in_orig;
+          a.src_masks = in_mask;
+          a.src_count = src.count;
+        }
+      } else {
+        const PassArgs& prev = host_args[(size_t)ch * n_stage + k - 1];
+        a.src_origins = prev.out_origins;
+        a.src_masks = prev.out_masks;
+        a.src_grid = prev.out_grid;
+        a.src_count_dev = &prev.rb->num_leaves;
+      }
+      a.err = (unsigned int*)(ws + o_err);
+      a.rb = (ReadbackHeader*)(ws + pl.rb);
+      a.leaf_off = (int64_t*)(ws + pl.rb + sizeof(ReadbackHeader));
+      a.lower_off = a.leaf_off + (B + 1);
+      a.upper_off = a.lower_off + (B + 1);
+      a.grid_vox = a.upper_off + (B + 1);
+      a.gbox = (unsigned int*)(a.grid_vox + B);
+      a.ctl = (PassCtl*)(ws + pl.ctl);
+      a.sort_status = (uint32_t*)(ws + pl.sort_status);
+      a.sort_tiles_cap = pl.sort_tiles;
+      a.dedup_status = (unsigned long long*)(ws + pl.dedup_status);
+      a.first = (uint32_t*)(ws + pl.first);
+      a.slot_cap = pl.slot_cap;
+      a.keys[0] = (uint64_t*)(ws + bf.keys0);
+      a.keys[1] = (uint64_t*)(ws + bf.keys1);
+      a.vals[0] = (uint32_t*)(ws + bf.vals0);
+      a.vals[1] = (uint32_t*)(ws + bf.vals1);
+      a.sorted = pl.P & 1;
+      a.run_start = (uint32_t*)(ws + bf.run);
+      a.leaf_lower = (uint32_t*)(ws + bf.llow);
+      a.leaf_upper = (uint32_t*)(ws + bf.lup);
+      a.leaf_voff = (int64_t*)(ws + bf.voff);
+      a.leaf_pop = (uint32_t*)(ws + bf.pop);
+      a.leaf_g = (uint32_t*)(ws + bf.lg);
+      a.blk_agg = (unsigned long long*)(ws + bf.blk);
+      a.grp_agg = (unsigned long long*)(ws + bf.grp);
+      a.phase_ts = t_prof >= 2 ? (unsigned long long*)(ws + o_ts) + 8 * pass_index : nullptr;
+      ++pass_index;
+      if (!a.last) {
+        a.out_origins = (int32_t*)(ws + bf.inter[k & 1][0]);
+        a.out_masks = (uint64_t*)(ws + bf.inter[k & 1][1]);
+        a.out_grid = (int32_t*)(ws + bf.inter[k & 1][2]);
+      }
     }
   }
+  TB_CUDA(cudaMemcpyAsync(ws + o_args, host_args, args_bytes, cudaMemcpyHostToDevice, stream));
 
-  // ---- the cooperative pass kernel(s)
-  for (int l = 0; l < n_launch; ++l) {
+  // ---- the cooperative pass kernel
+  {
     ChainArgs ca;
-    std::memset(&ca, 0, sizeof ca);
-    ca.bar = (GridBarrier*)(ws + o_bar) + l;
-    const size_t p0 = (size_t)l * kMaxChainPasses;
-    ca.n_pass = (int32_t)std::min<size_t>(kMaxChainPasses, plans.size() - p0);
-    for (int k = 0; k < ca.n_pass; ++k) ca.pass[k] = args[p0 + k];
+    ca.pass = (const PassArgs*)(ws + o_args);
+    ca.n_chain = n_chain;
+    ca.n_stage = n_stage;
+    ca.bar = (GridBarrier*)(ws + o_bar);
+    ca.err = (unsigned int*)(ws + o_err);
     TB_CUDA(launch(kKChain, stream, [&] { return launch_chain(ca, G, stream); }));
   }
 
-  // ---- the one count readback of the call (plus the error words of the earlier passes)
-  const PassArgs& a = args.back();
-  unsigned int* host_err = (unsigned int*)((char*)host_rb + rb_bytes);
-  for (size_t p = 0; p + 1 < plans.size(); ++p)
-    TB_CUDA(cudaMemcpyAsync(host_err + p, ws + plans[p].rb + offsetof(ReadbackHeader, err), 4,
-                            cudaMemcpyDeviceToHost, stream));
-  unsigned long long* host_ts =
-      (unsigned long long*)(((uintptr_t)host_err + 4 * plans.size() + 63) & ~(uintptr_t)63);
-  if (t_prof >= 2)
-    TB_CUDA(cudaMemcpyAsync(host_ts, ws + o_ts, plans.size() * 64, cudaMemcpyDeviceToHost, stream));
-  TB_CUDA(cudaMemcpyAsync(host_rb, a.rb, rb_bytes, cudaMemcpyDeviceToHost, stream));
+  // ---- the one count readback of the call
+  if (t_prof >= 2) TB_CUDA(cudaMemcpyAsync(host_ts, ws + o_ts, ts_bytes, cudaMemcpyDeviceToHost, stream));
+  TB_CUDA(cudaMemcpyAsync(pinned, ws, readback_span, cudaMemcpyDeviceToHost, stream));
   const auto t_sync = std::chrono::steady_clock::now();
   TB_CUDA(cudaStreamSynchronize(stream));
   const auto t_synced = std::chrono::steady_clock::now();
@@ -601,9 +704,7 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
     t_phase_ms[5] += std::chrono::duration<double, std::milli>(t_synced - t_sync).count();
     t_phase_n[4] += 1;
     t_phase_n[5] += 1;
-  }
-  if (t_prof >= 2)
-    for (size_t p = 0; p < plans.size(); ++p)
+    for (size_t p = 0; p < n_pass_total; ++p)
       for (int k = 0; k < kNumGpuPhases; ++k) {
         const unsigned long long t0 = k == 0 ? ~host_ts[8 * p] : host_ts[8 * p + k], t1 = host_ts[8 * p + k + 1];
         if (t1 >= t0 && t0) {
@@ -611,99 +712,63 @@ tb_status run(const Source& src, const std::vector<PassSpec>& specs, const tb_al
           t_phase_n[k] += 1;
         }
       }
-  unsigned int err = host_rb->err;
-  for (size_t p = 0; p + 1 < plans.size(); ++p) err |= host_err[p];
+  }
+  const unsigned int err = *(const unsigned int*)(pinned + o_err);
   if (err & kErrTimeout) return fail(TB_ERR_DEVICE_TIMEOUT, "a device-side wait timed out");
   if (err & kErrSlotOverflow) return fail(TB_ERR_CUDA, "internal: emitted slots exceeded the bound");
-  const int64_t L = (int64_t)host_rb->num_leaves, NL = (int64_t)host_rb->num_lowers,
-                NU = (int64_t)host_rb->num_uppers;
-  const int64_t* hoff = (const int64_t*)(host_rb + 1);
 
-  // ---- outputs
-  tb_batch* b = new tb_batch();
-  b->B = B;
-  b->device = dev;
-  b->L = L;
-  b->NL = NL;
-  b->NU = NU;
-  b->has_alloc = alloc != nullptr;
-  if (alloc) b->alloc = *alloc;
-  b->leaf_offsets_host.assign(hoff, hoff + B + 1);
-  std::memcpy(b->bbox, plans.back().bbox, sizeof b->bbox);
-  if (plans.back().empty || L == 0) {
-    const int32_t e[6] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MIN, INT32_MIN, INT32_MIN};
-    std::memcpy(b->bbox, e, sizeof e);
+  // ---- outputs, one writer launch per chain
+  std::vector<tb_batch*> made(n_chain, nullptr);
+  auto undo = [&] {
+    for (tb_batch* b : made)
+      if (b) {
+        mem.put(b->mem);
+        delete b;
+      }
+  };
+  for (int ch = 0; ch < n_chain; ++ch) {
+    const PassPlan& last = plans[ch].back();
+    const ReadbackHeader* hr = (const ReadbackHeader*)(pinned + o_rb_last[ch]);
+    const int64_t L = (int64_t)hr->num_leaves, NL = (int64_t)hr->num_lowers, NU = (int64_t)hr->num_uppers;
+    const int64_t* hoff = (const int64_t*)(hr + 1);
+    tb_batch* b = new tb_batch();
+    made[ch] = b;
+    b->B = B;
+    b->device = dev;
+    b->L = L;
+    b->NL = NL;
+    b->NU = NU;
+    b->has_alloc = alloc != nullptr;
+    if (alloc) b->alloc = *alloc;
+    b->leaf_offsets_host.assign(hoff, hoff + B + 1);
+    std::memcpy(b->bbox, last.bbox, sizeof b->bbox);
+    if (last.empty || L == 0) {
+      const int32_t e[6] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MIN, INT32_MIN, INT32_MIN};
+      std::memcpy(b->bbox, e, sizeof e);
+    }
+    b->build_slots = (int64_t)hr->num_slots;
+    b->build_sources = plans[ch].size() == 1 ? (int64_t)last.in_cap : -1;
+    b->build_key_bits = last.K.W;
+    b->build_digit_passes = last.P;
+    st = alloc_outputs(b, mem);
+    if (st != TB_OK) {
+      undo();
+      return st;
+    }
+    WriteOut wo;
+    fill_write_out(b, wo);
+    const int op_last = last.spec.op;
+    const int wb = blocks_for(std::max<long long>(L, B + 1), kWriteLeavesPerBlock,
+                              (long long)di->sms * di->occ_write[op_last]);
+    const PassArgs& a = host_args[(size_t)ch * n_stage + plans[ch].size() - 1];
+    const cudaError_t e =
+        launch(kKWrite0 + op_last, stream, [&] { return launch_write_final(op_last, a, wo, wb, stream); });
+    if (e != cudaSuccess) {
+      undo();
+      return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
+    }
   }
-  b->build_slots = (int64_t)host_rb->num_slots;
-  b->build_sources = plans.size() == 1 ? (int64_t)plans.back().in_cap : -1;
-  b->build_key_bits = plans.back().K.W;
-  b->build_digit_passes = plans.back().P;
-  Carve oc;
-  size_t off[16];
-  off[0] = oc.take((size_t)(B + 1) * 8);
-  off[1] = oc.take((size_t)L * 12);
-  off[2] = oc.take((size_t)L * 64);
-  off[3] = oc.take((size_t)L * 8);
-  off[4] = oc.take((size_t)L * 8);
-  off[5] = oc.take((size_t)L * 24);
-  off[6] = oc.take((size_t)L * 4);
-  off[7] = oc.take((size_t)L * 4);
-  off[8] = oc.take((size_t)B * 8);
-  off[9] = oc.take((size_t)B * 24);
-  off[10] = oc.take((size_t)B * 12);
-  off[11] = oc.take((size_t)(B + 1) * 8);
-  off[12] = oc.take((size_t)(B + 1) * 8);
-  off[13] = oc.take((size_t)NL * 12);
-  off[14] = oc.take((size_t)NL * 4);
-  off[15] = oc.take((size_t)NU * 12);
-  b->mem = mem.get(oc.off);
-  if (!b->mem) {
-    delete b;
-    return fail(TB_ERR_OOM, "output allocation of %zu bytes failed", oc.off);
-  }
-  batch_set_view(b, (char*)b->mem, off);
-  auto nz = [](void* p, int64_t n) { return n > 0 ? p : nullptr; };
-  b->origins = (int32_t*)nz(b->origins, L);
-  b->masks = (uint64_t*)nz(b->masks, L);
-  b->voxel_offset = (int64_t*)nz(b->voxel_offset, L);
-  b->word_prefix = (uint64_t*)nz(b->word_prefix, L);
-  b->leaf_bbox = (int32_t*)nz(b->leaf_bbox, L);
-  b->leaf_grid = (int32_t*)nz(b->leaf_grid, L);
-  b->leaf_parent = (int32_t*)nz(b->leaf_parent, L);
-  b->voxel_counts = (int64_t*)nz(b->voxel_counts, B);
-  b->grid_bbox = (int32_t*)nz(b->grid_bbox, B);
-  b->node_counts = (int32_t*)nz(b->node_counts, B);
-  b->lower_origins = (int32_t*)nz(b->lower_origins, NL);
-  b->lower_parent = (int32_t*)nz(b->lower_parent, NL);
-  b->upper_origins = (int32_t*)nz(b->upper_origins, NU);
-
-  WriteOut wo;
-  wo.origins = b->origins;
-  wo.masks = b->masks;
-  wo.leaf_grid = b->leaf_grid;
-  wo.voxel_offset = b->voxel_offset;
-  wo.word_prefix = b->word_prefix;
-  wo.leaf_bbox = b->leaf_bbox;
-  wo.leaf_parent = b->leaf_parent;
-  wo.voxel_counts = b->voxel_counts;
-  wo.grid_bbox = b->grid_bbox;
-  wo.node_counts = b->node_counts;
-  wo.leaf_offsets = b->leaf_offsets;
-  wo.lower_offsets = b->lower_offsets;
-  wo.upper_offsets = b->upper_offsets;
-  wo.lower_origins = b->lower_origins;
-  wo.lower_parent = b->lower_parent;
-  wo.upper_origins = b->upper_origins;
-  const int op_last = plans.back().spec.op;
-  const int wb = blocks_for(std::max<long long>(L, B + 1), kWriteLeavesPerBlock,
-                            (long long)di->sms * di->occ_write[op_last]);
-  cudaError_t e = launch(kKWrite0 + op_last, stream, [&] { return launch_write_final(op_last, a, wo, wb, stream); });
-  if (e != cudaSuccess) {
-    mem.put(b->mem);
-    delete b;
-    return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
-  }
-  *out = b;
+  for (int ch = 0; ch < n_chain; ++ch) outs[ch] = made[ch];
   if (t_prof >= 2) {
     t_phase_ms[6] += host_ms_since(t_synced);
     t_phase_n[6] += 1;
@@ -753,9 +818,8 @@ tb_status check_batch(const tb_batch* b) {
   return TB_OK;
 }
 
-tb_status run_ops(const tb_batch* in, const std::vector<PassSpec>& specs, const tb_allocator* alloc,
-                  cudaStream_t s, tb_batch** out) {
-  if (out) *out = nullptr;
+tb_status run_ops(const tb_batch* in, const std::vector<std::vector<PassSpec>>& chains, const tb_allocator* alloc,
+                  cudaStream_t s, tb_batch** outs) {
   tb_status st = check_batch(in);
   if (st != TB_OK) return st;
   Source src;
@@ -763,7 +827,22 @@ tb_status run_ops(const tb_batch* in, const std::vector<PassSpec>& specs, const 
   src.batch = in;
   src.B = in->B;
   src.count = in->L;
-  return run(src, specs, alloc, s, out);
+  return run(src, chains, alloc, s, outs);
+}
+
+// The passes of one chain of ops; an empty chain copies its input (one
+// identity pass over the leaves).
+tb_status chain_specs(const tb_op* ops, int32_t n_ops, std::vector<PassSpec>* specs) {
+  tb_status st;
+  *specs = expand_ops(ops, n_ops, &st);
+  if (st != TB_OK) return st;
+  if (specs->empty()) {
+    PassSpec s;
+    std::memset(&s, 0, sizeof s);
+    s.op = kLeaves;
+    specs->push_back(s);
+  }
+  return TB_OK;
 }
 
 }  // namespace
@@ -788,10 +867,10 @@ tb_status tb_from_ijk(const int32_t* ijk, const int64_t* offsets, int32_t num_gr
   src.offsets = offsets;
   src.B = num_grids;
   src.count = num_voxels;
-  PassSpec s;
-  std::memset(&s, 0, sizeof s);
-  s.op = kIjk;
-  return run(src, {s}, alloc, (cudaStream_t)stream, out);
+  std::vector<std::vector<PassSpec>> chains(1, std::vector<PassSpec>(1));
+  std::memset(&chains[0][0], 0, sizeof(PassSpec));
+  chains[0][0].op = kIjk;
+  return run(src, chains, alloc, (cudaStream_t)stream, out);
 }
 
 tb_status tb_from_leaves(const int32_t* origins, const uint64_t* masks, const int64_t* leaf_offsets,
@@ -811,10 +890,10 @@ tb_status tb_from_leaves(const int32_t* origins, const uint64_t* masks, const in
   src.offsets = leaf_offsets;
   src.B = num_grids;
   src.count = num_leaves;
-  PassSpec s;
-  std::memset(&s, 0, sizeof s);
-  s.op = kLeaves;
-  return run(src, {s}, alloc, (cudaStream_t)stream, out);
+  std::vector<std::vector<PassSpec>> chains(1, std::vector<PassSpec>(1));
+  std::memset(&chains[0][0], 0, sizeof(PassSpec));
+  chains[0][0].op = kLeaves;
+  return run(src, chains, alloc, (cudaStream_t)stream, out);
 }
 
 tb_status tb_refine(const tb_batch* in, int32_t factor, const tb_allocator* alloc, tb_stream stream, tb_batch** out) {
@@ -841,16 +920,27 @@ tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, const tb
   if (out) *out = nullptr;
   if (!out) return fail(TB_ERR_INVALID_ARG, "out is NULL");
   if (n_ops < 0 || (n_ops > 0 && !ops)) return fail(TB_ERR_INVALID_ARG, "tb_chain: bad op list");
-  tb_status st;
-  std::vector<PassSpec> specs = expand_ops(ops, n_ops, &st);
+  std::vector<std::vector<PassSpec>> chains(1);
+  tb_status st = chain_specs(ops, n_ops, &chains[0]);
   if (st != TB_OK) return st;
-  if (specs.empty()) {  // a copy: one identity pass over the leaves
-    PassSpec s;
-    std::memset(&s, 0, sizeof s);
-    s.op = kLeaves;
-    specs.push_back(s);
+  return run_ops(in, chains, alloc, (cudaStream_t)stream, out);
+}
+
+tb_status tb_multi(const tb_batch* in, const tb_op* ops, const int32_t* chain_lengths, int32_t n_chains,
+                   const tb_allocator* alloc, tb_stream stream, tb_batch** outs) {
+  if (!outs || n_chains <= 0 || !chain_lengths) return fail(TB_ERR_INVALID_ARG, "tb_multi: bad chain list");
+  for (int32_t c = 0; c < n_chains; ++c) outs[c] = nullptr;
+  if (n_chains > 1024) return fail(TB_ERR_TOO_LARGE, "tb_multi: more than 1024 chains");
+  std::vector<std::vector<PassSpec>> chains(n_chains);
+  long long first = 0;
+  for (int32_t c = 0; c < n_chains; ++c) {
+    if (chain_lengths[c] < 0 || (chain_lengths[c] > 0 && !ops))
+      return fail(TB_ERR_INVALID_ARG, "tb_multi: bad length of chain %d", c);
+    tb_status st = chain_specs(ops + first, chain_lengths[c], &chains[c]);
+    if (st != TB_OK) return st;
+    first += chain_lengths[c];
   }
-  return run_ops(in, specs, alloc, (cudaStream_t)stream, out);
+  return run_ops(in, chains, alloc, (cudaStream_t)stream, outs);
 }
 
 tb_status tb_validate(const tb_batch* b, tb_stream stream) {

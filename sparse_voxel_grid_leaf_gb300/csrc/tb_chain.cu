@@ -2,12 +2,11 @@
 // final writer (fVDB PR #757 "Batched leaf-mask topology construction for
 // generated conv grids", Summary item 1; item 2 for the box dilation).
 //
-// k_chain runs every pass of a call (a chain of up to kMaxChainPasses) with
-// all blocks co-resident; phases are separated by a bounded software grid
-// barrier:
-//   emission  -> digit pass 0 .. P-1 -> dedup -> per-grid offsets
-//             -> count (last pass: voxel offsets, grid voxel counts and bboxes)
-//             or hand-off (intermediate pass: leaves for the next pass).
+// k_chain runs every pass of a call -- one or several chains of passes over
+// the same input -- with all blocks co-resident; phases are separated by a
+// bounded software grid barrier:
+//   emission -> digit pass 0 .. P-1 -> index -> leaves (merge, popcounts,
+//   bboxes; or the hand-off of an intermediate pass) -> voxel offsets.
 // Everything the host needs to size the outputs then comes back in one
 // readback, and k_write_final writes the leaf records without any scan.
 //
@@ -36,6 +35,7 @@ struct SmemSort {
   uint32_t binstart[kBins];
   uint32_t glob[kBins];
   uint32_t binbase[kBins];
+  unsigned int next_hist[kBins];  // histogram of the next digit over this block's tiles
   uint64_t keys[kSortTile];
   uint32_t vals[kSortTile];
   uint32_t scan[8];
@@ -55,6 +55,7 @@ struct SmemLeaves {
   uint32_t grp_g[kThreads / 8];            // grid of its pending bbox
   unsigned int grp_box[kThreads / 8][6];   // its pending encoded bbox
   unsigned long long blk_prefix;           // voxels before the block's first leaf in the same grid
+  unsigned long long grp_prefix[kThreads / 8];
 };
 struct SmemFinish {
   uint32_t s[kThreads];
@@ -64,11 +65,6 @@ union Smem {
   SmemEmit emit;
   SmemDedup dedup;
   SmemFinish fin;
-};
-// the leaves phase keeps its group aggregates across one grid barrier, so it
-// has shared memory of its own
-struct SmemAll {
-  Smem u;
   SmemLeaves lv;
 };
 
@@ -117,19 +113,17 @@ __device__ __forceinline__ void put_slot(const PassArgs& a, unsigned long long p
     a.keys[0][pos] = key;
     a.vals[0][pos] = val;
   } else {
-    atomicOr(&a.rb->err, kErrSlotOverflow);
+    atomicOr(a.err, kErrSlotOverflow);
   }
 }
 
-// Adds one key per lane (valid lanes only) to the block's digit histograms,
-// one shared-memory atomic per distinct digit value in the warp.
-__device__ __forceinline__ void hist_warp(const PassArgs& a, unsigned int (*hist)[kBins], uint64_t key, bool valid) {
+// Adds digit `pass` of one key per lane (valid lanes only) to a shared
+// histogram, one shared-memory atomic per distinct digit value in the warp.
+__device__ __forceinline__ void hist_digit(unsigned int* hist, uint64_t key, int pass, bool valid) {
   const int lane = threadIdx.x & 31;
-  for (int p = 0; p < a.P; ++p) {
-    const uint32_t d = valid ? ((uint32_t)(key >> (8 * p)) & 255u) : kBins;
-    const uint32_t peers = __match_any_sync(0xffffffffu, d);
-    if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(&hist[p][d], (unsigned int)__popc(peers));
-  }
+  const uint32_t d = valid ? ((uint32_t)(key >> (8 * pass)) & 255u) : kBins;
+  const uint32_t peers = __match_any_sync(0xffffffffu, d);
+  if (valid && (peers & ((1u << lane) - 1u)) == 0) atomicAdd(&hist[d], (unsigned int)__popc(peers));
 }
 
 // Is target `t` (an index into the op's target set) of a source leaf with
@@ -189,7 +183,7 @@ __device__ __forceinline__ uint32_t targets_per_source(const PassArgs& a) {
 // covered by about one round of the grid's threads.
 template <int OP>
 __device__ void phase_emit(const PassArgs& a, Smem& sm) {
-  for (int i = threadIdx.x; i < a.P * kBins; i += kThreads) (&sm.emit.hist[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < kBins; i += kThreads) sm.emit.hist[0][i] = 0;
   __syncthreads();
   const long long n = a.src_count_dev ? (long long)__ldcg(a.src_count_dev) : a.src_count;
   const uint32_t T = targets_per_source<OP>(a);
@@ -250,13 +244,13 @@ __device__ void phase_emit(const PassArgs& a, Smem& sm) {
         }
         put_slot(a, pos++, key, val);
       }
-      hist_warp(a, sm.emit.hist, key, valid);
+      if (a.P > 0) hist_digit(sm.emit.hist[0], key, 0, valid);
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < a.P * kBins; i += kThreads) {
-    const unsigned int c = (&sm.emit.hist[0][0])[i];
-    if (c) atomicAdd(&(&a.ctl->hist[0][0])[i], c);
+  for (int i = threadIdx.x; i < kBins; i += kThreads) {
+    const unsigned int c = sm.emit.hist[0][i];
+    if (c && a.P > 0) atomicAdd(&a.ctl->hist[0][i], c);
   }
 }
 
@@ -280,7 +274,9 @@ __device__ void phase_sort(const PassArgs& a, int pass, Smem& sm) {
   {
     uint32_t total;
     s.binbase[tid] = block_excl_scan_256(__ldcg(&a.ctl->hist[pass][tid]), s.scan, &total);
+    s.next_hist[tid] = 0;
   }
+  const bool count_next = pass + 1 < a.P;
   for (;;) {
     if (tid == 0) s.tile = atomicAdd(ctr, 1u);
     for (int k = tid; k < NW * kBins; k += kThreads) (&s.whist[0][0])[k] = 0;
@@ -325,7 +321,7 @@ __device__ void phase_sort(const PassArgs& a, int pass, Smem& sm) {
     uint32_t all;
     const uint32_t ex = block_excl_scan_256(tot, s.scan, &all);
     s.binstart[tid] = ex;
-    const uint32_t prefix = lookback32(status + tid, kBins, tile, tot, &a.rb->err);
+    const uint32_t prefix = lookback32(status + tid, kBins, tile, tot, a.err);
     s.glob[tid] = s.binbase[tid] + prefix - ex;
     __syncthreads();
 #pragma unroll
@@ -339,16 +335,23 @@ __device__ void phase_sort(const PassArgs& a, int pass, Smem& sm) {
     __syncthreads();
     const long long rem = S - tile * kSortTile;
     const int nvalid = rem < kSortTile ? (int)rem : kSortTile;
-    for (int i = tid; i < nvalid; i += kThreads) {
-      const uint64_t key = s.keys[i];
-      const uint32_t gp = s.glob[(uint32_t)(key >> shift) & 255u] + (uint32_t)i;
-      if (gp < (uint64_t)S) {  // always true when the histograms match the slots
-        kout[gp] = key;
-        vout[gp] = s.vals[i];
+    for (int i0 = 0; i0 < nvalid; i0 += kThreads) {  // uniform bound: the warps also histogram
+      const int i = i0 + tid;
+      const bool valid = i < nvalid;
+      uint64_t key = 0;
+      if (valid) {
+        key = s.keys[i];
+        const uint32_t gp = s.glob[(uint32_t)(key >> shift) & 255u] + (uint32_t)i;
+        if (gp < (uint64_t)S) {  // always true when the histograms match the slots
+          kout[gp] = key;
+          vout[gp] = s.vals[i];
+        }
       }
+      if (count_next) hist_digit(s.next_hist, key, pass + 1, valid);
     }
     __syncthreads();
   }
+  if (count_next && s.next_hist[tid]) atomicAdd(&a.ctl->hist[pass + 1][tid], s.next_hist[tid]);
 }
 
 // ---------------------------------------------------------------- merged masks
@@ -501,7 +504,7 @@ __device__ void phase_index(const PassArgs& a, Smem& sm) {
     if (warp < 3) {
       const unsigned long long field = (tot >> (21 * warp)) & M21;
       lb64_publish(a.dedup_status + warp, 3, tile, field, false);
-      const unsigned long long b = lb64_resolve(a.dedup_status + warp, 3, tile, field, false, &a.rb->err);
+      const unsigned long long b = lb64_resolve(a.dedup_status + warp, 3, tile, field, false, a.err);
       if (lane == 0) {
         s.base[warp] = b;
         if (field) atomicAdd(&a.ctl->head_totals[warp], field);
@@ -592,8 +595,8 @@ __device__ void phase_finish(const PassArgs& a, Smem& sm) {
 //    aggregate of each group and block (segments start at grid-first leaves);
 //  - intermediate pass: the merged leaves for the next pass.
 template <int OP>
-__device__ void phase_leaves(const PassArgs& a, SmemAll& sa) {
-  SmemLeaves& s = sa.lv;
+__device__ void phase_leaves(const PassArgs& a, Smem& sm) {
+  SmemLeaves& s = sm.lv;
   const uint64_t* keys = a.keys[a.sorted];
   const uint32_t* vals = a.vals[a.sorted];
   long long S = (long long)__ldcg(&a.rb->num_slots);
@@ -673,6 +676,7 @@ __device__ void phase_leaves(const PassArgs& a, SmemAll& sa) {
     s.grp_f[grp] = F;
     s.grp_v[grp] = V;
     s.grp_g[grp] = acc_g;
+    a.grp_agg[(long long)blockIdx.x * (kThreads / 8) + grp] = ((unsigned long long)F << 63) | V;
   }
   if (w < 6) s.grp_box[grp][w] = acc_e;
   __syncthreads();
@@ -708,8 +712,8 @@ __device__ void phase_leaves(const PassArgs& a, SmemAll& sa) {
 // it (complete, so no waiting) for its carried-in voxel count; each group then
 // scans its leaves eight at a time and writes their per-grid voxel offsets,
 // and every grid's last leaf writes the grid's voxel total.
-__device__ void phase_voxel_offsets(const PassArgs& a, SmemAll& sa) {
-  SmemLeaves& s = sa.lv;
+__device__ void phase_voxel_offsets(const PassArgs& a, Smem& sm) {
+  SmemLeaves& s = sm.lv;
   const long long U = (long long)__ldcg(&a.ctl->head_totals[0]);
   const int tid = threadIdx.x, lane = tid & 31, w = tid & 7, grp = tid >> 3;
   if (tid < 32) {
@@ -725,16 +729,34 @@ __device__ void phase_voxel_offsets(const PassArgs& a, SmemAll& sa) {
       carry += v;
       if (first < 32) break;
     }
-    if (lane == 0) s.blk_prefix = carry;
+    // carried-in value of each group: the block's prefix, then the groups before it
+    const unsigned long long ga = __ldcg(a.grp_agg + (long long)blockIdx.x * (kThreads / 8) + lane);
+    const uint32_t gf = (uint32_t)(ga >> 63);
+    unsigned long long gv = ga & ~(1ull << 63);
+    uint32_t F = gf;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t F2 = __shfl_up_sync(0xffffffffu, F, off);
+      const unsigned long long V2 = __shfl_up_sync(0xffffffffu, gv, off);
+      if (lane >= off) {
+        if (!F) gv += V2;
+        F |= F2;
+      }
+    }
+    uint32_t Fe = __shfl_up_sync(0xffffffffu, F, 1);
+    unsigned long long Ve = __shfl_up_sync(0xffffffffu, gv, 1);
+    if (lane == 0) {
+      Fe = 0;
+      Ve = 0;
+    }
+    s.grp_prefix[lane] = Fe ? Ve : carry + Ve;
   }
   __syncthreads();
   const long long C = (U + gridDim.x - 1) / gridDim.x;
   const long long c = (C + kThreads / 8 - 1) / (kThreads / 8);
   const long long bbeg = (long long)blockIdx.x * C, bend = bbeg + C < U ? bbeg + C : U;
   const long long gbeg = bbeg + grp * c, gend = gbeg + c < bend ? gbeg + c : bend;
-  // carried-in value of this group: the block's prefix, then the groups before it
-  unsigned long long cv = s.blk_prefix;
-  for (int j = 0; j < grp; ++j) cv = s.grp_f[j] ? s.grp_v[j] : cv + s.grp_v[j];
+  unsigned long long cv = s.grp_prefix[grp];
   const uint32_t gmask = 0xFFu << (lane & ~7);
   for (long long base = gbeg; base < gend; base += 8) {  // uniform within the group
     const long long u = base + w;
@@ -770,41 +792,86 @@ __device__ void phase_voxel_offsets(const PassArgs& a, SmemAll& sa) {
   }
 }
 
-// Phases: 1 emission, 2 digit passes, 3 index, 4 leaves (and offsets).
-template <int OP>
-__device__ void run_pass(const PassArgs& a, GridBarrier* bar, SmemAll& sa) {
-  unsigned int* err = &a.rb->err;
-  stamp(a, 0);
-  phase_emit<OP>(a, sa.u);
-  stamp(a, 1);
-  grid_sync(bar, err);
-  for (int d = 0; d < a.P; ++d) {
-    phase_sort(a, d, sa.u);
-    grid_sync(bar, err);
+// One stage of the launch runs stage k of every chain, phase by phase, so the
+// chains share the grid barriers.  Stamps: 1 emission, 2 digit passes,
+// 3 index, 4 leaves and voxel offsets.
+__device__ void dispatch_emit(const PassArgs& a, Smem& sm) {
+  switch (a.op) {
+    case kIjk: phase_emit<kIjk>(a, sm); break;
+    case kLeaves: phase_emit<kLeaves>(a, sm); break;
+    case kRefine: phase_emit<kRefine>(a, sm); break;
+    case kCoarsen: phase_emit<kCoarsen>(a, sm); break;
+    default: phase_emit<kDilate>(a, sm); break;
   }
-  stamp(a, 2);
-  phase_index(a, sa.u);
-  stamp(a, 3);
-  grid_sync(bar, err);
-  if (blockIdx.x == gridDim.x - 1) phase_finish(a, sa.u);  // the block with the fewest leaves
-  phase_leaves<OP>(a, sa);
-  grid_sync(bar, err);
-  if (a.last) phase_voxel_offsets(a, sa);
-  stamp(a, 4);
 }
 
-__global__ void __launch_bounds__(kThreads) k_chain(const __grid_constant__ ChainArgs c) {
+__device__ void dispatch_leaves(const PassArgs& a, Smem& sm) {
+  switch (a.op) {
+    case kIjk: phase_leaves<kIjk>(a, sm); break;
+    case kLeaves: phase_leaves<kLeaves>(a, sm); break;
+    case kRefine: phase_leaves<kRefine>(a, sm); break;
+    case kCoarsen: phase_leaves<kCoarsen>(a, sm); break;
+    default: phase_leaves<kDilate>(a, sm); break;
+  }
+}
+
+// Copies pass (ch, k) into the block's shared copy; returns its op (< 0: none).
+__device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, PassArgs& dst) {
+  static_assert(sizeof(PassArgs) % 8 == 0 && sizeof(PassArgs) / 8 <= kThreads, "pass argument copy");
+  __syncthreads();
+  const unsigned long long* from = reinterpret_cast<const unsigned long long*>(c.pass + ch * c.n_stage + k);
+  if (threadIdx.x < sizeof(PassArgs) / 8) reinterpret_cast<unsigned long long*>(&dst)[threadIdx.x] = __ldg(from + threadIdx.x);
+  __syncthreads();
+  return dst.op;
+}
+
+__global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  SmemAll& sa = *reinterpret_cast<SmemAll*>(smem_raw);
-  for (int p = 0; p < c.n_pass; ++p) {
-    const PassArgs& a = c.pass[p];
-    switch (a.op) {
-      case kIjk: run_pass<kIjk>(a, c.bar, sa); break;
-      case kLeaves: run_pass<kLeaves>(a, c.bar, sa); break;
-      case kRefine: run_pass<kRefine>(a, c.bar, sa); break;
-      case kCoarsen: run_pass<kCoarsen>(a, c.bar, sa); break;
-      default: run_pass<kDilate>(a, c.bar, sa); break;
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  __shared__ __align__(16) PassArgs a;
+  for (int k = 0; k < c.n_stage; ++k) {
+    int maxP = 0;
+    bool more = false;
+    for (int ch = 0; ch < c.n_chain; ++ch) {
+      if (load_pass(c, ch, k, a) < 0) continue;
+      maxP = a.P > maxP ? a.P : maxP;
+      more |= !a.last;
+      stamp(a, 0);
+      dispatch_emit(a, sm);
+      stamp(a, 1);
     }
+    grid_sync(c.bar, c.err);
+    for (int d = 0; d < maxP; ++d) {
+      for (int ch = 0; ch < c.n_chain; ++ch) {
+        if (load_pass(c, ch, k, a) < 0 || d >= a.P) continue;
+        phase_sort(a, d, sm);
+      }
+      grid_sync(c.bar, c.err);
+    }
+    for (int ch = 0; ch < c.n_chain; ++ch) {
+      if (load_pass(c, ch, k, a) < 0) continue;
+      stamp(a, 2);
+      phase_index(a, sm);
+      stamp(a, 3);
+    }
+    grid_sync(c.bar, c.err);
+    for (int ch = 0; ch < c.n_chain; ++ch) {
+      if (load_pass(c, ch, k, a) < 0) continue;
+      // the totals and per-grid offsets of chain ch: a block near the end of the
+      // grid, which holds few leaves
+      if (blockIdx.x == gridDim.x - 1 - (ch % gridDim.x)) {
+        phase_finish(a, sm);
+        __syncthreads();
+      }
+      dispatch_leaves(a, sm);
+    }
+    grid_sync(c.bar, c.err);
+    for (int ch = 0; ch < c.n_chain; ++ch) {
+      if (load_pass(c, ch, k, a) < 0 || !a.last) continue;
+      phase_voxel_offsets(a, sm);
+      stamp(a, 4);
+    }
+    if (more) grid_sync(c.bar, c.err);
   }
 }
 
@@ -896,20 +963,19 @@ int write_occupancy() {
 
 }  // namespace
 
-size_t chain_smem_bytes() { return sizeof(SmemAll); }
+size_t chain_smem_bytes() { return sizeof(Smem); }
 
 int chain_occupancy() {
   int n = 0;
-  if (cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(SmemAll)) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(k_chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)) != cudaSuccess)
     return 1;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_chain, kThreads, sizeof(SmemAll)) != cudaSuccess) n = 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_chain, kThreads, sizeof(Smem)) != cudaSuccess) n = 1;
   return n > 0 ? n : 1;
 }
 
 cudaError_t launch_chain(const ChainArgs& c, int blocks, cudaStream_t s) {
   void* args[] = {(void*)&c};
-  return cudaLaunchCooperativeKernel((const void*)k_chain, dim3(blocks), dim3(kThreads), args, sizeof(SmemAll), s);
+  return cudaLaunchCooperativeKernel((const void*)k_chain, dim3(blocks), dim3(kThreads), args, sizeof(Smem), s);
 }
 
 int write_final_occupancy(int op) {

@@ -25,7 +25,6 @@ enum PassOp : int32_t { kIjk = 0, kLeaves = 1, kRefine = 2, kCoarsen = 3, kDilat
 constexpr int kBins = 256;            // 8-bit radix digits
 constexpr int kMaxDigitPasses = 8;    // 64-bit key
 constexpr int kSrcShift = 5;          // slot value = source index << 5 | target code
-constexpr int kMaxChainPasses = 6;    // passes per cooperative launch
 
 // Error bits reported through the readback header.
 constexpr uint32_t kErrTimeout = 1u;       // a bounded wait (look-back or grid barrier) gave up
@@ -103,7 +102,7 @@ __host__ __device__ inline int32_t dec_min(unsigned int e) { return (int32_t)(~e
 
 struct PassArgs {
   KeyLayout K;
-  int32_t op;
+  int32_t op;             // PassOp, or -1: no pass at this stage of the chain
   int32_t B;
   int32_t P;              // digit passes
   int32_t last;           // 1: final pass (count phase), 0: intermediate (hands leaves on)
@@ -118,6 +117,7 @@ struct PassArgs {
   const unsigned long long* src_count_dev;  // device count (chained pass) or null
   long long src_count;                      // host count when src_count_dev is null
   // control (zeroed region)
+  unsigned int* err;   // the call's device error word
   ReadbackHeader* rb;
   int64_t* leaf_off;   // [B+1]
   int64_t* lower_off;  // [B+1]
@@ -141,6 +141,7 @@ struct PassArgs {
   uint32_t* leaf_pop;    // [slot_cap] voxels of each unique leaf (last pass)
   uint32_t* leaf_g;      // [slot_cap] grid of each unique leaf (last pass)
   unsigned long long* blk_agg;  // [gridDim.x] segmented voxel aggregate per block (last pass)
+  unsigned long long* grp_agg;  // [gridDim.x * 32] segmented voxel aggregate per 8-lane group (last pass)
   unsigned long long* phase_ts;  // optional [8] globaltimer stamps (profiling), else null
   // intermediate output (next pass's source)
   int32_t* out_origins;
@@ -148,10 +149,15 @@ struct PassArgs {
   int32_t* out_grid;
 };
 
+// Arguments of one cooperative launch: n_chain chains of up to n_stage
+// passes over the same input; pass[c * n_stage + k] is stage k of chain c
+// (op < 0 where chain c is shorter).  The array lives in device memory.
 struct ChainArgs {
-  int32_t n_pass;
+  const PassArgs* pass;
+  int32_t n_chain;
+  int32_t n_stage;
   GridBarrier* bar;
-  PassArgs pass[kMaxChainPasses];
+  unsigned int* err;
 };
 
 // Outputs of the final writer.

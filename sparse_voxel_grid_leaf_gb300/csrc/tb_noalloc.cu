@@ -136,16 +136,16 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
     off = align256(off + n);
     return r;
   };
-  const size_t o_bar = take(sizeof(GridBarrier)), o_rb = take(rbb), o_ctl = take(sizeof(PassCtl)),
+  const size_t o_err = take(4), o_bar = take(sizeof(GridBarrier)), o_rb = take(rbb), o_ctl = take(sizeof(PassCtl)),
                o_sort = take((size_t)a.P * sort_tiles * kBins * 4), o_dedup = take((size_t)dedup_tiles * 24),
                o_first = take((size_t)3 * B * 4);
-  const size_t zero_begin = o_bar, zero_end = off;
+  const size_t zero_begin = o_err, zero_end = off;
   const size_t o_k0 = take((size_t)S * 8), o_k1 = take((size_t)S * 8), o_v0 = take((size_t)S * 4),
                o_v1 = take((size_t)S * 4), o_run = take((size_t)(S + 1) * 4), o_ll = take((size_t)S * 4),
                o_lu = take((size_t)S * 4), o_voff = take((size_t)S * 8), o_pop = take((size_t)S * 4),
                o_lg = take((size_t)S * 4);
   const int G = sms * chain_occupancy();
-  const size_t o_blk = take((size_t)G * 8);
+  const size_t o_blk = take((size_t)G * 8), o_grp = take((size_t)G * 32 * 8), o_args = take(sizeof(PassArgs));
   if (off > kStaticScratchBytes)
     return static_fail(TB_ERR_TOO_LARGE,
                        "tb_refine_static: input needs more than the 32 MiB static scratch (about 75k leaves)");
@@ -184,17 +184,25 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   a.leaf_pop = (uint32_t*)(scratch + o_pop);
   a.leaf_g = (uint32_t*)(scratch + o_lg);
   a.blk_agg = (unsigned long long*)(scratch + o_blk);
+  a.grp_agg = (unsigned long long*)(scratch + o_grp);
+  a.err = (unsigned int*)(scratch + o_err);
 
   // ---- the same cooperative pass kernel as tb_refine
+  // the pass arguments go to the scratch array from host stack memory
+  TB_STATIC_CUDA(cudaMemcpyAsync(scratch + o_args, &a, sizeof a, cudaMemcpyHostToDevice, stream));
   ChainArgs ca;
-  std::memset(&ca, 0, sizeof ca);
-  ca.n_pass = 1;
+  ca.pass = (const PassArgs*)(scratch + o_args);
+  ca.n_chain = 1;
+  ca.n_stage = 1;
   ca.bar = (GridBarrier*)(scratch + o_bar);
-  ca.pass[0] = a;
+  ca.err = (unsigned int*)(scratch + o_err);
   TB_STATIC_CUDA(launch_chain(ca, G, stream));
   ReadbackHeader r;
+  unsigned int derr = 0;
   TB_STATIC_CUDA(cudaMemcpyAsync(&r, a.rb, sizeof r, cudaMemcpyDeviceToHost, stream));
+  TB_STATIC_CUDA(cudaMemcpyAsync(&derr, a.err, sizeof derr, cudaMemcpyDeviceToHost, stream));
   TB_STATIC_CUDA(cudaStreamSynchronize(stream));
+  r.err |= derr;
   if (r.err & kErrTimeout) return static_fail(TB_ERR_DEVICE_TIMEOUT, "tb_refine_static: a device wait timed out");
   if (r.err & kErrSlotOverflow) return static_fail(TB_ERR_CUDA, "tb_refine_static: internal slot bound exceeded");
   if (out_counts) {

@@ -167,6 +167,31 @@ def test_errors_leave_the_device_usable():
     check(*synth.make("pr1_b2_res32"), [("refine", 2)], "after errors")
 
 
+@pytest.mark.parametrize("workload", ["shells_b16_res64", "mixed"])
+def test_multi_equals_separate_chains(workload):
+    if workload == "mixed":
+        ijk, off = synth.random_voxels(5, 300, 90, seed=13, origin=(-4140, -45, 4050), empty=(2,))
+    else:
+        ijk, off = synth.make(workload)
+    chains = [[("refine", 2)], [("coarsen", 2)], [DIL], [PAD_N], [PAD_P], [("refine", 2), PAD_N],
+              [("coarsen", 4)], [], [("coarsen", 2), DIL, ("refine", 2)]]
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    outs = tb.multi(b0, chains)
+    assert len(outs) == len(chains)
+    for ops, b in zip(chains, outs):
+        assert_same(b.to_numpy(), oracle.run_voxels(ijk, off, ops), "multi %s" % (ops,))
+        b.validate()
+
+
+def test_multi_single_launch():
+    ijk, off = synth.make("pr1_b2_res32")
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    n0 = tb.kernel_launch_count()
+    tb.multi(b0, [[("refine", 2)], [("coarsen", 2)], [DIL]])
+    # one pass kernel for all chains, one writer per chain
+    assert tb.kernel_launch_count() - n0 == 4
+
+
 def test_deterministic_repeat():
     ijk, off = synth.make("shells_b16_res64")
     b = tb.from_ijk(dev(ijk), dev(off))
