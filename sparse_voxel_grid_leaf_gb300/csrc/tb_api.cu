@@ -66,10 +66,12 @@ thread_local long long t_launches = 0;
 
 // ---------------------------------------------------------------- kernel timing
 
-enum KernelKind { kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + 5, kKNumKinds };
-const char* const kKernelNames[kKNumKinds] = {"prepass_ijk", "prepass_leaves", "chain",      "write_ijk",
-                                              "write_leaves", "write_refine",   "write_coarsen", "write_dilate",
-                                              "validate"};
+enum KernelKind {
+  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + 5, kKWriteMulti, kKNumKinds
+};
+const char* const kKernelNames[kKNumKinds] = {"prepass_ijk",   "prepass_leaves", "chain",        "write_ijk",
+                                              "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
+                                              "validate",      "write_multi"};
 
 struct ProfRec {
   int kind;
@@ -138,6 +140,7 @@ struct DeviceInfo {
   int sms = 0;
   int occ_chain = 1;
   int occ_write[5] = {};
+  int occ_write_multi = 1;
   bool coop = false;
   bool ready = false;
 };
@@ -156,6 +159,7 @@ tb_status device_info(int dev, DeviceInfo** out) {
     d.coop = true;
     d.occ_chain = chain_occupancy();
     for (int op = 0; op < 5; ++op) d.occ_write[op] = write_final_occupancy(op);
+    d.occ_write_multi = write_multi_occupancy();
     // keep freed memory in the default pool between calls
     cudaMemPool_t pool;
     if (cudaDeviceGetDefaultMemPool(&pool, dev) == cudaSuccess) {
@@ -525,6 +529,7 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     }
   }
   const size_t o_args = c.take(sizeof(PassArgs) * (size_t)n_chain * n_stage);
+  const size_t o_tasks = c.take(n_chain > 1 ? sizeof(WriteTask) * (size_t)n_chain : 0);
   // staging of host-resident inputs
   const int32_t* in_ijk = src.ijk;
   const int32_t* in_orig = src.origins;
@@ -755,17 +760,47 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       undo();
       return st;
     }
+  }
+  if (n_chain == 1) {
     WriteOut wo;
-    fill_write_out(b, wo);
-    const int op_last = last.spec.op;
-    const int wb = blocks_for(std::max<long long>(L, B + 1), kWriteLeavesPerBlock,
+    fill_write_out(made[0], wo);
+    const int op_last = plans[0].back().spec.op;
+    const int wb = blocks_for(std::max<long long>(made[0]->L, B + 1), kWriteLeavesPerBlock,
                               (long long)di->sms * di->occ_write[op_last]);
-    const PassArgs& a = host_args[(size_t)ch * n_stage + plans[ch].size() - 1];
+    const PassArgs& a = host_args[plans[0].size() - 1];
     const cudaError_t e =
         launch(kKWrite0 + op_last, stream, [&] { return launch_write_final(op_last, a, wo, wb, stream); });
     if (e != cudaSuccess) {
       undo();
       return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
+    }
+  } else {
+    // one writer launch per kMaxWriteTasks chains; the tasks go through
+    // pageable memory, which the driver copies before the call returns
+    std::vector<WriteTask> tasks(n_chain);
+    for (int c0 = 0; c0 < n_chain; c0 += kMaxWriteTasks) {
+      const int nt = std::min(kMaxWriteTasks, n_chain - c0);
+      long long quads = 0, leaves_max = B + 1;
+      for (int j = 0; j < nt; ++j) {
+        const int ch = c0 + j;
+        WriteTask& t = tasks[ch];
+        std::memset(&t, 0, sizeof t);
+        t.a = host_args[(size_t)ch * n_stage + plans[ch].size() - 1];
+        fill_write_out(made[ch], t.o);
+        t.leaves = made[ch]->L;
+        t.quad_base = quads;
+        t.quads = (t.leaves + 3) / 4;
+        quads += t.quads;
+        leaves_max = std::max<long long>(leaves_max, quads * 4);
+      }
+      WriteTask* dtasks = (WriteTask*)(ws + o_tasks) + c0;
+      TB_CUDA(cudaMemcpyAsync(dtasks, &tasks[c0], sizeof(WriteTask) * nt, cudaMemcpyHostToDevice, stream));
+      const int wb = blocks_for(leaves_max, kWriteLeavesPerBlock, (long long)di->sms * di->occ_write_multi);
+      const cudaError_t e = launch(kKWriteMulti, stream, [&] { return launch_write_multi(dtasks, nt, wb, stream); });
+      if (e != cudaSuccess) {
+        undo();
+        return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
+      }
     }
   }
   for (int ch = 0; ch < n_chain; ++ch) outs[ch] = made[ch];

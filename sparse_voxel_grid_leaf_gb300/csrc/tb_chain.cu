@@ -877,79 +877,118 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
 
 // ---------------------------------------------------------------- final writer
 
-// After the readback: one 8-lane group per output leaf writes its record
-// (origin, merged mask, voxel offset, word prefix, bbox, grid, parent) and
-// node records at node heads; per-grid arrays by the first threads.
+// After the readback: per-grid arrays, and one 8-lane group per output leaf
+// writing its record (origin, merged mask, voxel offset, word prefix, bbox,
+// grid, parent) and the node records at node heads.
+__device__ __forceinline__ void write_grid_arrays(const PassArgs& a, const WriteOut& o, long long g) {
+  o.leaf_offsets[g] = a.leaf_off[g];
+  o.lower_offsets[g] = a.lower_off[g];
+  o.upper_offsets[g] = a.upper_off[g];
+  if (g == a.B) return;
+  o.node_counts[3 * g + 0] = (int32_t)(a.upper_off[g + 1] - a.upper_off[g]);
+  o.node_counts[3 * g + 1] = (int32_t)(a.lower_off[g + 1] - a.lower_off[g]);
+  o.node_counts[3 * g + 2] = (int32_t)(a.leaf_off[g + 1] - a.leaf_off[g]);
+  o.voxel_counts[g] = a.grid_vox[g];
+#pragma unroll
+  for (int c = 0; c < 6; ++c) {
+    const unsigned int e = a.gbox[6 * g + c];
+    o.grid_bbox[6 * g + c] = c < 3 ? dec_min(e) : dec_max(e);
+  }
+}
+
+// Leaf u of the group of the calling lane (all 32 lanes of the warp call it).
 template <int OP>
-__global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, const WriteOut o) {
+__device__ __forceinline__ void write_leaf(const PassArgs& a, const WriteOut& o, long long u, long long U) {
+  const int lane = threadIdx.x & 31, w = lane & 7;
   const uint64_t* keys = a.keys[a.sorted];
   const uint32_t* vals = a.vals[a.sorted];
-  const long long U = (long long)a.rb->num_leaves;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid & 7;
-  const long long gtid = (long long)blockIdx.x * kThreads + tid;
-  for (long long g = gtid; g <= a.B; g += (long long)gridDim.x * kThreads) {
-    o.leaf_offsets[g] = a.leaf_off[g];
-    o.lower_offsets[g] = a.lower_off[g];
-    o.upper_offsets[g] = a.upper_off[g];
-    if (g == a.B) break;
-    o.node_counts[3 * g + 0] = (int32_t)(a.upper_off[g + 1] - a.upper_off[g]);
-    o.node_counts[3 * g + 1] = (int32_t)(a.lower_off[g + 1] - a.lower_off[g]);
-    o.node_counts[3 * g + 2] = (int32_t)(a.leaf_off[g + 1] - a.leaf_off[g]);
-    o.voxel_counts[g] = a.grid_vox[g];
+  const bool valid = u < U;
+  uint32_t s0 = 0, s1 = 0, g = 0;
+  int32_t lc[3] = {0, 0, 0};
+  if (valid) {
+    s0 = a.run_start[u];
+    s1 = a.run_start[u + 1];
+    decode_key(a.K, keys[s0], g, lc);
+  }
+  const uint64_t word = merge_run<OP>(a, vals, s0, s1, w);
+  const uint32_t pop = __popcll(word);
+  uint32_t incl = pop;
 #pragma unroll
-    for (int c = 0; c < 6; ++c) {
-      const unsigned int e = a.gbox[6 * g + c];
-      o.grid_bbox[6 * g + c] = c < 3 ? dec_min(e) : dec_max(e);
+  for (int off = 1; off < 8; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off, 8);
+    if (w >= off) incl += y;
+  }
+  uint64_t wp = w ? ((uint64_t)(incl - pop) << (9 * (w - 1))) : 0ull;
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) wp |= __shfl_xor_sync(0xffffffffu, wp, off);
+  int32_t mn[3], mx[3];
+  leaf_bounds(word, w, lane, mn, mx);
+  if (!valid) return;
+  const int32_t org[3] = {(int32_t)((uint32_t)lc[0] << 3), (int32_t)((uint32_t)lc[1] << 3),
+                          (int32_t)((uint32_t)lc[2] << 3)};
+  o.masks[8 * u + w] = word;
+  if (w < 3) o.origins[3 * u + w] = org[w];
+  if (w < 6) o.leaf_bbox[6 * u + w] = w < 3 ? org[w] + mn[w] : org[w - 3] + mx[w - 3];
+  if (w == 6) o.word_prefix[u] = wp;
+  if (w == 7) o.leaf_grid[u] = (int32_t)g;
+  if (w == 0) o.voxel_offset[u] = a.leaf_voff[u];
+  if (w == 3) o.leaf_parent[u] = (int32_t)((long long)a.leaf_lower[u] - a.lower_off[g]);
+  if (w == 4) {
+    const uint32_t lw = a.leaf_lower[u];
+    if (u == 0 || a.leaf_lower[u - 1] != lw) {
+#pragma unroll
+      for (int c = 0; c < 3; ++c) o.lower_origins[3 * (long long)lw + c] = (int32_t)((uint32_t)org[c] & ~127u);
+      o.lower_parent[lw] = (int32_t)((long long)(a.leaf_upper[u] & ~kGridFirst) - a.upper_off[g]);
     }
   }
+  if (w == 5) {
+    const uint32_t up = a.leaf_upper[u] & ~kGridFirst;
+    if (u == 0 || (a.leaf_upper[u - 1] & ~kGridFirst) != up) {
+#pragma unroll
+      for (int c = 0; c < 3; ++c) o.upper_origins[3 * (long long)up + c] = (int32_t)((uint32_t)org[c] & ~4095u);
+    }
+  }
+}
+
+template <int OP>
+__global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, const WriteOut o) {
+  const long long U = (long long)a.rb->num_leaves;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const long long gtid = (long long)blockIdx.x * kThreads + tid;
+  for (long long g = gtid; g <= a.B; g += (long long)gridDim.x * kThreads) write_grid_arrays(a, o, g);
   const long long groups = (long long)gridDim.x * (kThreads / 8);
-  for (long long ub = (long long)blockIdx.x * (kThreads / 8) + (tid >> 5) * 4; ub < U; ub += groups) {
-    const long long u = ub + (lane >> 3);
-    const bool valid = u < U;
-    uint32_t s0 = 0, s1 = 0, g = 0;
-    int32_t lc[3] = {0, 0, 0};
-    if (valid) {
-      s0 = a.run_start[u];
-      s1 = a.run_start[u + 1];
-      decode_key(a.K, keys[s0], g, lc);
-    }
-    const uint64_t word = merge_run<OP>(a, vals, s0, s1, w);
-    const uint32_t pop = __popcll(word);
-    uint32_t incl = pop;
-#pragma unroll
-    for (int off = 1; off < 8; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off, 8);
-      if (w >= off) incl += y;
-    }
-    uint64_t wp = w ? ((uint64_t)(incl - pop) << (9 * (w - 1))) : 0ull;
-#pragma unroll
-    for (int off = 1; off < 8; off <<= 1) wp |= __shfl_xor_sync(0xffffffffu, wp, off);
-    int32_t mn[3], mx[3];
-    leaf_bounds(word, w, lane, mn, mx);
-    if (!valid) continue;
-    const int32_t org[3] = {(int32_t)((uint32_t)lc[0] << 3), (int32_t)((uint32_t)lc[1] << 3),
-                            (int32_t)((uint32_t)lc[2] << 3)};
-    o.masks[8 * u + w] = word;
-    if (w < 3) o.origins[3 * u + w] = org[w];
-    if (w < 6) o.leaf_bbox[6 * u + w] = w < 3 ? org[w] + mn[w] : org[w - 3] + mx[w - 3];
-    if (w == 6) o.word_prefix[u] = wp;
-    if (w == 7) o.leaf_grid[u] = (int32_t)g;
-    if (w == 0) o.voxel_offset[u] = a.leaf_voff[u];
-    if (w == 3) o.leaf_parent[u] = (int32_t)((long long)a.leaf_lower[u] - a.lower_off[g]);
-    if (w == 4) {
-      const uint32_t lw = a.leaf_lower[u];
-      if (u == 0 || a.leaf_lower[u - 1] != lw) {
-#pragma unroll
-        for (int c = 0; c < 3; ++c) o.lower_origins[3 * (long long)lw + c] = (int32_t)((uint32_t)org[c] & ~127u);
-        o.lower_parent[lw] = (int32_t)((long long)(a.leaf_upper[u] & ~kGridFirst) - a.upper_off[g]);
-      }
-    }
-    if (w == 5) {
-      const uint32_t up = a.leaf_upper[u] & ~kGridFirst;
-      if (u == 0 || (a.leaf_upper[u - 1] & ~kGridFirst) != up) {
-#pragma unroll
-        for (int c = 0; c < 3; ++c) o.upper_origins[3 * (long long)up + c] = (int32_t)((uint32_t)org[c] & ~4095u);
-      }
+  for (long long ub = (long long)blockIdx.x * (kThreads / 8) + (tid >> 5) * 4; ub < U; ub += groups)
+    write_leaf<OP>(a, o, ub + (lane >> 3), U);
+}
+
+// The writers of several chains in one launch.  Tasks (one per chain, up to
+// kMaxWriteTasks) are staged in shared memory; the leaves of all chains form
+// one index space in units of 4 leaves, so a warp's 4 groups always belong to
+// one chain and take the same code path.
+__global__ void __launch_bounds__(kThreads) k_write_multi(const WriteTask* tasks, int n_task) {
+  __shared__ __align__(16) WriteTask t[kMaxWriteTasks];
+  static_assert(sizeof(WriteTask) % 8 == 0, "task copy");
+  for (int i = threadIdx.x; i < n_task * (int)(sizeof(WriteTask) / 8); i += kThreads)
+    reinterpret_cast<unsigned long long*>(t)[i] = __ldg(reinterpret_cast<const unsigned long long*>(tasks) + i);
+  __syncthreads();
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int B = t[0].a.B;
+  const long long gtid = (long long)blockIdx.x * kThreads + tid, nthreads = (long long)gridDim.x * kThreads;
+  for (long long i = gtid; i < (long long)n_task * (B + 1); i += nthreads)
+    write_grid_arrays(t[i / (B + 1)].a, t[i / (B + 1)].o, i % (B + 1));
+  const long long total = t[n_task - 1].quad_base + t[n_task - 1].quads;
+  const long long nwarps = nthreads / 32;
+  for (long long q = gtid / 32; q < total; q += nwarps) {
+    int ch = 0;
+    while (ch + 1 < n_task && t[ch + 1].quad_base <= q) ++ch;
+    const WriteTask& tk = t[ch];
+    const long long u = (q - tk.quad_base) * 4 + (lane >> 3);
+    switch (tk.a.op) {
+      case kIjk: write_leaf<kIjk>(tk.a, tk.o, u, tk.leaves); break;
+      case kLeaves: write_leaf<kLeaves>(tk.a, tk.o, u, tk.leaves); break;
+      case kRefine: write_leaf<kRefine>(tk.a, tk.o, u, tk.leaves); break;
+      case kCoarsen: write_leaf<kCoarsen>(tk.a, tk.o, u, tk.leaves); break;
+      default: write_leaf<kDilate>(tk.a, tk.o, u, tk.leaves); break;
     }
   }
 }
@@ -986,6 +1025,17 @@ int write_final_occupancy(int op) {
     case kCoarsen: return write_occupancy<kCoarsen>();
     default: return write_occupancy<kDilate>();
   }
+}
+
+int write_multi_occupancy() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_write_multi, kThreads, 0) != cudaSuccess) n = 1;
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch_write_multi(const WriteTask* tasks, int n_task, int blocks, cudaStream_t s) {
+  k_write_multi<<<blocks, kThreads, 0, s>>>(tasks, n_task);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_write_final(int op, const PassArgs& a, const WriteOut& o, int blocks, cudaStream_t s) {

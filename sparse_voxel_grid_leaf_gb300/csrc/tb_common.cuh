@@ -220,6 +220,16 @@ __host__ __device__ inline void decode_key(const KeyLayout& K, uint64_t key, uin
   }
 }
 
+// One chain's share of a multi-chain writer launch.
+constexpr int kMaxWriteTasks = 16;
+struct WriteTask {
+  PassArgs a;
+  WriteOut o;
+  long long leaves;     // output leaves of the chain
+  long long quad_base;  // first 4-leaf unit of the chain in the launch's index space
+  long long quads;      // its 4-leaf units
+};
+
 #ifdef __CUDACC__
 
 // ---------------------------------------------------------------- memory helpers

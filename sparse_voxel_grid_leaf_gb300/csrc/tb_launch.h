@@ -35,6 +35,8 @@ int chain_occupancy();
 cudaError_t launch_chain(const ChainArgs& c, int blocks, cudaStream_t s);
 int write_final_occupancy(int op);
 cudaError_t launch_write_final(int op, const PassArgs& a, const WriteOut& o, int blocks, cudaStream_t s);
+int write_multi_occupancy();
+cudaError_t launch_write_multi(const WriteTask* tasks, int n_task, int blocks, cudaStream_t s);
 
 // Sets the calling thread's tb_last_error() message.
 void set_error_message(const char* msg);

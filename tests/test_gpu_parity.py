@@ -188,8 +188,8 @@ def test_multi_single_launch():
     b0 = tb.from_ijk(dev(ijk), dev(off))
     n0 = tb.kernel_launch_count()
     tb.multi(b0, [[("refine", 2)], [("coarsen", 2)], [DIL]])
-    # one pass kernel for all chains, one writer per chain
-    assert tb.kernel_launch_count() - n0 == 4
+    # one pass kernel and one writer for all chains
+    assert tb.kernel_launch_count() - n0 == 2
 
 
 def test_deterministic_repeat():
