@@ -182,7 +182,7 @@ __device__ __forceinline__ uint32_t targets_per_source(const PassArgs& a) {
 // histograms.  The host sizes the chunk so that all candidates of a pass are
 // covered by about one round of the grid's threads.
 template <int OP>
-__device__ void phase_emit(const PassArgs& a, Smem& sm) {
+__device__ void phase_emit(const PassArgs& a, Smem& sm, int vb, int vg) {
   for (int i = threadIdx.x; i < kBins; i += kThreads) sm.emit.hist[0][i] = 0;
   __syncthreads();
   const long long n = a.src_count_dev ? (long long)__ldcg(a.src_count_dev) : a.src_count;
@@ -190,8 +190,8 @@ __device__ void phase_emit(const PassArgs& a, Smem& sm) {
   const uint32_t k = (a.tchunk > 0 && (uint32_t)a.tchunk < T) ? (uint32_t)a.tchunk : T;
   const uint32_t nchunks = (T + k - 1) / k;
   const long long items = n * (long long)nchunks;
-  const long long stride = (long long)gridDim.x * kThreads;
-  for (long long base = (long long)blockIdx.x * kThreads; base < items; base += stride) {
+  const long long stride = (long long)vg * kThreads;
+  for (long long base = (long long)vb * kThreads; base < items; base += stride) {
     const long long idx = base + threadIdx.x;
     uint32_t bits = 0, t0 = 0, g = 0;
     long long i = 0;
@@ -595,7 +595,7 @@ __device__ void phase_finish(const PassArgs& a, Smem& sm) {
 //    aggregate of each group and block (segments start at grid-first leaves);
 //  - intermediate pass: the merged leaves for the next pass.
 template <int OP>
-__device__ void phase_leaves(const PassArgs& a, Smem& sm) {
+__device__ void phase_leaves(const PassArgs& a, Smem& sm, int vb, int vg) {
   SmemLeaves& s = sm.lv;
   const uint64_t* keys = a.keys[a.sorted];
   const uint32_t* vals = a.vals[a.sorted];
@@ -603,9 +603,9 @@ __device__ void phase_leaves(const PassArgs& a, Smem& sm) {
   if (S > a.slot_cap) S = a.slot_cap;
   const long long U = (long long)__ldcg(&a.ctl->head_totals[0]);
   const int tid = threadIdx.x, lane = tid & 31, w = tid & 7, grp = tid >> 3;
-  const long long C = (U + gridDim.x - 1) / gridDim.x;
+  const long long C = (U + vg - 1) / vg;
   const long long c = (C + kThreads / 8 - 1) / (kThreads / 8);
-  const long long bbeg = (long long)blockIdx.x * C, bend = bbeg + C < U ? bbeg + C : U;
+  const long long bbeg = (long long)vb * C, bend = bbeg + C < U ? bbeg + C : U;
   const long long gbeg = bbeg + grp * c, gend = gbeg + c < bend ? gbeg + c : bend;
   constexpr int kU = OP == kRefine ? 4 : 1;
   uint32_t acc_g = 0xFFFFFFFFu, F = 0;
@@ -676,7 +676,7 @@ __device__ void phase_leaves(const PassArgs& a, Smem& sm) {
     s.grp_f[grp] = F;
     s.grp_v[grp] = V;
     s.grp_g[grp] = acc_g;
-    a.grp_agg[(long long)blockIdx.x * (kThreads / 8) + grp] = ((unsigned long long)F << 63) | V;
+    a.grp_agg[(long long)vb * (kThreads / 8) + grp] = ((unsigned long long)F << 63) | V;
   }
   if (w < 6) s.grp_box[grp][w] = acc_e;
   __syncthreads();
@@ -704,7 +704,7 @@ __device__ void phase_leaves(const PassArgs& a, Smem& sm) {
       bv = s.grp_f[j] ? s.grp_v[j] : bv + s.grp_v[j];
       bf |= s.grp_f[j];
     }
-    a.blk_agg[blockIdx.x] = ((unsigned long long)bf << 63) | bv;
+    a.blk_agg[vb] = ((unsigned long long)bf << 63) | bv;
   }
 }
 
@@ -712,13 +712,13 @@ __device__ void phase_leaves(const PassArgs& a, Smem& sm) {
 // it (complete, so no waiting) for its carried-in voxel count; each group then
 // scans its leaves eight at a time and writes their per-grid voxel offsets,
 // and every grid's last leaf writes the grid's voxel total.
-__device__ void phase_voxel_offsets(const PassArgs& a, Smem& sm) {
+__device__ void phase_voxel_offsets(const PassArgs& a, Smem& sm, int vb, int vg) {
   SmemLeaves& s = sm.lv;
   const long long U = (long long)__ldcg(&a.ctl->head_totals[0]);
   const int tid = threadIdx.x, lane = tid & 31, w = tid & 7, grp = tid >> 3;
   if (tid < 32) {
     unsigned long long carry = 0;
-    for (long long base = (long long)blockIdx.x - 1; base >= 0; base -= 32) {
+    for (long long base = (long long)vb - 1; base >= 0; base -= 32) {
       const long long b = base - lane;
       const unsigned long long e = b >= 0 ? __ldcg(a.blk_agg + b) : (1ull << 63);
       const uint32_t stop = __ballot_sync(0xffffffffu, (e >> 63) != 0);
@@ -730,7 +730,7 @@ __device__ void phase_voxel_offsets(const PassArgs& a, Smem& sm) {
       if (first < 32) break;
     }
     // carried-in value of each group: the block's prefix, then the groups before it
-    const unsigned long long ga = __ldcg(a.grp_agg + (long long)blockIdx.x * (kThreads / 8) + lane);
+    const unsigned long long ga = __ldcg(a.grp_agg + (long long)vb * (kThreads / 8) + lane);
     const uint32_t gf = (uint32_t)(ga >> 63);
     unsigned long long gv = ga & ~(1ull << 63);
     uint32_t F = gf;
@@ -752,9 +752,9 @@ __device__ void phase_voxel_offsets(const PassArgs& a, Smem& sm) {
     s.grp_prefix[lane] = Fe ? Ve : carry + Ve;
   }
   __syncthreads();
-  const long long C = (U + gridDim.x - 1) / gridDim.x;
+  const long long C = (U + vg - 1) / vg;
   const long long c = (C + kThreads / 8 - 1) / (kThreads / 8);
-  const long long bbeg = (long long)blockIdx.x * C, bend = bbeg + C < U ? bbeg + C : U;
+  const long long bbeg = (long long)vb * C, bend = bbeg + C < U ? bbeg + C : U;
   const long long gbeg = bbeg + grp * c, gend = gbeg + c < bend ? gbeg + c : bend;
   unsigned long long cv = s.grp_prefix[grp];
   const uint32_t gmask = 0xFFu << (lane & ~7);
@@ -792,26 +792,23 @@ __device__ void phase_voxel_offsets(const PassArgs& a, Smem& sm) {
   }
 }
 
-// One stage of the launch runs stage k of every chain, phase by phase, so the
-// chains share the grid barriers.  Stamps: 1 emission, 2 digit passes,
-// 3 index, 4 leaves and voxel offsets.
-__device__ void dispatch_emit(const PassArgs& a, Smem& sm) {
+__device__ void dispatch_emit(const PassArgs& a, Smem& sm, int vb, int vg) {
   switch (a.op) {
-    case kIjk: phase_emit<kIjk>(a, sm); break;
-    case kLeaves: phase_emit<kLeaves>(a, sm); break;
-    case kRefine: phase_emit<kRefine>(a, sm); break;
-    case kCoarsen: phase_emit<kCoarsen>(a, sm); break;
-    default: phase_emit<kDilate>(a, sm); break;
+    case kIjk: phase_emit<kIjk>(a, sm, vb, vg); break;
+    case kLeaves: phase_emit<kLeaves>(a, sm, vb, vg); break;
+    case kRefine: phase_emit<kRefine>(a, sm, vb, vg); break;
+    case kCoarsen: phase_emit<kCoarsen>(a, sm, vb, vg); break;
+    default: phase_emit<kDilate>(a, sm, vb, vg); break;
   }
 }
 
-__device__ void dispatch_leaves(const PassArgs& a, Smem& sm) {
+__device__ void dispatch_leaves(const PassArgs& a, Smem& sm, int vb, int vg) {
   switch (a.op) {
-    case kIjk: phase_leaves<kIjk>(a, sm); break;
-    case kLeaves: phase_leaves<kLeaves>(a, sm); break;
-    case kRefine: phase_leaves<kRefine>(a, sm); break;
-    case kCoarsen: phase_leaves<kCoarsen>(a, sm); break;
-    default: phase_leaves<kDilate>(a, sm); break;
+    case kIjk: phase_leaves<kIjk>(a, sm, vb, vg); break;
+    case kLeaves: phase_leaves<kLeaves>(a, sm, vb, vg); break;
+    case kRefine: phase_leaves<kRefine>(a, sm, vb, vg); break;
+    case kCoarsen: phase_leaves<kCoarsen>(a, sm, vb, vg); break;
+    default: phase_leaves<kDilate>(a, sm, vb, vg); break;
   }
 }
 
@@ -825,52 +822,170 @@ __device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, Pass
   return dst.op;
 }
 
+// ---------------------------------------------------------------- chains side by side
+
+// The phases of the chains of one stage are independent, so each phase splits
+// the grid's blocks over the chains that take part in it, in proportion to
+// their work (candidates, slots or unique leaves), at least one block each.
+// Every block computes the same split from the same counters, so no
+// coordination is needed; a chain's blocks then run its phase as a virtual
+// grid of `vg` blocks.  With more chains than blocks, every block runs every
+// chain in turn instead.
+enum SplitKind { kSplitEmit, kSplitSort, kSplitIndex, kSplitLeaves };
+
+struct Split {
+  int ch, vb, vg;  // this block's chain (< 0: none), its virtual block index and grid size
+  int serial;      // 1: more chains take part than there are blocks
+  int maxP, more;  // emission split: most digit passes of the stage; some pass is intermediate
+};
+
+constexpr unsigned long long kSplitOne = 1ull << 52;  // chain count unit in a packed (count, weight)
+constexpr unsigned long long kSplitWCap = 1ull << 40;  // weights above this are clamped
+
+// Work of chain ch in a phase of stage k, or -1 when it takes no part.
+__device__ __forceinline__ long long split_weight(const ChainArgs& c, int ch, int k, int kind, int d, Split& sp) {
+  const PassArgs* p = c.pass + ch * c.n_stage + k;
+  const int op = __ldg(&p->op);
+  if (op < 0) return -1;
+  unsigned long long w;
+  if (kind == kSplitEmit) {
+    const unsigned long long* cd = p->src_count_dev;
+    const unsigned long long n = cd ? __ldcg(cd) : (unsigned long long)__ldg(&p->src_count);
+    unsigned long long T = 1;
+    if (op == kRefine) {
+      T = 8;
+    } else if (op == kDilate) {
+      T = 1;
+      for (int ax = 0; ax < 3; ++ax) T *= (unsigned long long)(__ldg(&p->hi[ax]) - __ldg(&p->lo[ax]) + 1);
+    }
+    w = n < kSplitWCap ? n * T : kSplitWCap;
+    atomicMax(&sp.maxP, __ldg(&p->P));
+    if (!__ldg(&p->last)) sp.more = 1;
+  } else if (kind == kSplitLeaves) {
+    const PassCtl* ctl = p->ctl;
+    w = __ldcg(&ctl->head_totals[0]);
+  } else {
+    if (kind == kSplitSort && d >= __ldg(&p->P)) return -1;
+    const ReadbackHeader* rb = p->rb;
+    w = __ldcg(&rb->num_slots);
+  }
+  return (long long)(w < kSplitWCap ? w : kSplitWCap);
+}
+
+__device__ void split_grid(const ChainArgs& c, int k, int kind, int d, Split& sp, Smem& sm) {
+  const int tid = threadIdx.x;
+  const unsigned long long G = gridDim.x, b = blockIdx.x;
+  __syncthreads();  // the previous phase is done with sp
+  if (tid == 0) {
+    sp.ch = -1;
+    sp.vb = 0;
+    sp.vg = 0;
+    sp.maxP = 0;
+    sp.more = 0;
+  }
+  __syncthreads();
+  const int n = c.n_chain;
+  unsigned long long total = 0, carry = 0, t;
+  if (n > kThreads) {  // totals first when the chains do not fit one scan
+    for (int base = 0; base < n; base += kThreads) {
+      const int ch = base + tid;
+      const long long w = ch < n ? split_weight(c, ch, k, kind, d, sp) : -1;
+      block_excl_scan_256(w >= 0 ? kSplitOne + (unsigned long long)w : 0ull, sm.dedup.scan, &t);
+      total += t;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      sp.maxP = 0;
+      sp.more = 0;
+    }
+    __syncthreads();
+  }
+  for (int base = 0; base < n; base += kThreads) {
+    const int ch = base + tid;
+    const long long w = ch < n ? split_weight(c, ch, k, kind, d, sp) : -1;
+    const unsigned long long v = w >= 0 ? kSplitOne + (unsigned long long)w : 0ull;
+    const unsigned long long ex = carry + block_excl_scan_256(v, sm.dedup.scan, &t);
+    if (n <= kThreads) total = t;
+    carry += t;
+    const unsigned long long nact = total / kSplitOne, wt = total % kSplitOne;
+    if (w >= 0 && nact <= G) {
+      const unsigned long long ai = ex / kSplitOne, wex = ex % kSplitOne, extra = G - nact;
+      const unsigned long long s0 = ai + (wt ? extra * wex / wt : extra * ai / nact);
+      const unsigned long long s1 = ai + 1 + (wt ? extra * (wex + (unsigned long long)w) / wt : extra * (ai + 1) / nact);
+      if (b >= s0 && b < s1) {
+        sp.ch = ch;
+        sp.vb = (int)(b - s0);
+        sp.vg = (int)(s1 - s0);
+      }
+    }
+  }
+  if (tid == 0) sp.serial = total / kSplitOne > G ? 1 : 0;
+  __syncthreads();
+}
+
+// Runs `body(a, vb, vg)` for this block's share of a phase: its own chain, or
+// in serial mode every chain that takes part, as block blockIdx.x of the grid.
+template <class Body>
+__device__ __forceinline__ void for_share(const ChainArgs& c, int k, int kind, int d, const Split& sp, PassArgs& a,
+                                          Body body) {
+  const int serial = sp.serial;
+  const int nit = serial ? c.n_chain : (sp.ch >= 0 ? 1 : 0);
+  for (int it = 0; it < nit; ++it) {
+    const int ch = serial ? it : sp.ch;
+    if (load_pass(c, ch, k, a) < 0) continue;
+    if (serial && kind == kSplitSort && d >= a.P) continue;
+    body(a, ch, serial ? (int)blockIdx.x : sp.vb, serial ? (int)gridDim.x : sp.vg);
+  }
+}
+
+// One stage of the launch runs stage k of every chain, phase by phase, the
+// chains of a phase side by side on their shares of the grid.  Stamps:
+// 1 emission, 2 digit passes, 3 index, 4 leaves and voxel offsets.
 __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   __shared__ __align__(16) PassArgs a;
+  __shared__ Split sp;
   for (int k = 0; k < c.n_stage; ++k) {
-    int maxP = 0;
-    bool more = false;
-    for (int ch = 0; ch < c.n_chain; ++ch) {
-      if (load_pass(c, ch, k, a) < 0) continue;
-      maxP = a.P > maxP ? a.P : maxP;
-      more |= !a.last;
-      stamp(a, 0);
-      dispatch_emit(a, sm);
-      stamp(a, 1);
-    }
+    split_grid(c, k, kSplitEmit, 0, sp, sm);
+    const int maxP = sp.maxP;
+    const bool more = sp.more != 0;
+    for_share(c, k, kSplitEmit, 0, sp, a, [&](const PassArgs& pa, int, int vb, int vg) {
+      stamp(pa, 0);
+      dispatch_emit(pa, sm, vb, vg);
+      stamp(pa, 1);
+    });
     grid_sync(c.bar, c.err);
     for (int d = 0; d < maxP; ++d) {
-      for (int ch = 0; ch < c.n_chain; ++ch) {
-        if (load_pass(c, ch, k, a) < 0 || d >= a.P) continue;
-        phase_sort(a, d, sm);
-      }
+      split_grid(c, k, kSplitSort, d, sp, sm);
+      for_share(c, k, kSplitSort, d, sp, a, [&](const PassArgs& pa, int, int, int) { phase_sort(pa, d, sm); });
       grid_sync(c.bar, c.err);
     }
-    for (int ch = 0; ch < c.n_chain; ++ch) {
-      if (load_pass(c, ch, k, a) < 0) continue;
-      stamp(a, 2);
-      phase_index(a, sm);
-      stamp(a, 3);
-    }
+    split_grid(c, k, kSplitIndex, 0, sp, sm);
+    for_share(c, k, kSplitIndex, 0, sp, a, [&](const PassArgs& pa, int, int, int) {
+      stamp(pa, 2);
+      phase_index(pa, sm);
+      stamp(pa, 3);
+    });
     grid_sync(c.bar, c.err);
-    for (int ch = 0; ch < c.n_chain; ++ch) {
-      if (load_pass(c, ch, k, a) < 0) continue;
-      // the totals and per-grid offsets of chain ch: a block near the end of the
-      // grid, which holds few leaves
-      if (blockIdx.x == gridDim.x - 1 - (ch % gridDim.x)) {
-        phase_finish(a, sm);
+    // the leaves and voxel offsets share one split: the block aggregates of
+    // the leaves phase are indexed by virtual block
+    split_grid(c, k, kSplitLeaves, 0, sp, sm);
+    for_share(c, k, kSplitLeaves, 0, sp, a, [&](const PassArgs& pa, int ch, int vb, int vg) {
+      // the totals and per-grid offsets: a block near the end of the chain's
+      // share, which holds few leaves
+      if (sp.serial ? (int)blockIdx.x == (int)gridDim.x - 1 - (ch % (int)gridDim.x) : vb == vg - 1) {
+        phase_finish(pa, sm);
         __syncthreads();
       }
-      dispatch_leaves(a, sm);
-    }
+      dispatch_leaves(pa, sm, vb, vg);
+    });
     grid_sync(c.bar, c.err);
-    for (int ch = 0; ch < c.n_chain; ++ch) {
-      if (load_pass(c, ch, k, a) < 0 || !a.last) continue;
-      phase_voxel_offsets(a, sm);
-      stamp(a, 4);
-    }
+    for_share(c, k, -1, 0, sp, a, [&](const PassArgs& pa, int, int vb, int vg) {
+      if (!pa.last) return;
+      phase_voxel_offsets(pa, sm, vb, vg);
+      stamp(pa, 4);
+    });
     if (more) grid_sync(c.bar, c.err);
   }
 }

@@ -183,6 +183,24 @@ def test_multi_equals_separate_chains(workload):
         b.validate()
 
 
+@pytest.mark.parametrize("n", [270, 700])
+def test_multi_many_chains(n):
+    # more chains than one split scan holds (256), and more chains than the
+    # pass kernel has blocks (every block then runs every chain in turn)
+    ijk, off = synth.make("pr1_b2_res32")
+    kinds = [[("refine", 2)], [("coarsen", 2)], [DIL], [PAD_P], [("coarsen", 2), DIL], []]
+    chains = [kinds[i % len(kinds)] for i in range(n)]
+    want = [oracle.run_voxels(ijk, off, ops) for ops in kinds]
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    outs = tb.multi(b0, chains)
+    assert len(outs) == n
+    for i, b in enumerate(outs):
+        if i % 37 == 0 or i >= n - len(kinds):
+            assert_same(b.to_numpy(), want[i % len(kinds)], "chain %d" % i)
+        else:
+            assert b.num_leaves == len(want[i % len(kinds)]["origins"])
+
+
 def test_multi_single_launch():
     ijk, off = synth.make("pr1_b2_res32")
     b0 = tb.from_ijk(dev(ijk), dev(off))
