@@ -268,7 +268,8 @@ def kernel_bytes(ps):
     """Algorithmic DRAM bytes per kernel over one step (each record read or
     written once; per-grid arrays ignored).  "chain" is the cooperative kernel
     of a call: emission, digit passes, dedup and the count or hand-off phase of
-    each of its passes; "write_<op>" is the final writer."""
+    each of its passes; "write_<op>" is the final writer of a one-chain call,
+    "write_multi" the one writer of all chains of a tb_multi call."""
     by = {}
 
     def acc(name, n):
@@ -281,7 +282,8 @@ def kernel_bytes(ps):
         chain += 80 * L_out if p.get("inter") else 8 * L_out
         acc("chain", chain)
         if not p.get("inter"):
-            acc("write_" + p["kind"], merge + 16 * L_out + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])
+            w = "write_" + p["kind"] if SEPARATE or p["kind"] == "ijk" else "write_multi"
+            acc(w, merge + 16 * L_out + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])
     return by
 
 
@@ -289,6 +291,26 @@ def pass_model_bytes(ps):
     """Whole-pass byte model: 76 B per source leaf, 116 B per output leaf,
     24 B per slot per digit pass."""
     return sum(76 * p["L_in"] + 116 * p["L_out"] + 24 * p["S"] * p["P"] for p in ps)
+
+
+def rank_batch(synth, workload, rank):
+    """Weak scaling: every rank builds its own batch of the workload's shape
+    (same generator parameters, seed = rank)."""
+    return synth.make(workload, seed=rank)
+
+
+def job_totals(dist, total_ms, voxels, device):
+    """(slowest rank's timed milliseconds, output voxels of all ranks): the
+    ranks process independent batches, so the job's throughput is the sum of
+    their work over the longest of their times."""
+    if dist is None:
+        return float(total_ms), float(voxels)
+    import torch
+    t = torch.tensor([float(total_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    v = torch.tensor([float(voxels)], dtype=torch.float64, device=device)
+    dist.all_reduce(v)
+    return float(t.item()), float(v.item())
 
 
 def run_ours(args):
@@ -308,8 +330,7 @@ def run_ours(args):
     tb.lib()
     stream = torch.cuda.current_stream()
 
-    # weak scaling: every rank builds its own batch of the same shape
-    ijk, off = synth.make(args.workload, seed=rank)
+    ijk, off = rank_batch(synth, args.workload, rank)
     ijk_d = torch.from_numpy(ijk).cuda()
     off_d = torch.from_numpy(off).cuda()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
@@ -345,16 +366,7 @@ def run_ours(args):
     if dist:
         dist.barrier()
     launches = tb.kernel_launch_count() - launches0
-    total_ms = sum(times)
-    if dist:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-        v = torch.tensor([float(voxels)], device="cuda")
-        dist.all_reduce(v)
-        job_voxels = float(v.item())
-    else:
-        job_voxels = float(voxels)
+    total_ms, job_voxels = job_totals(dist, sum(times), voxels, "cuda")
     value = job_voxels * args.steps / (total_ms / 1e3)
     ms_per_step = total_ms / args.steps
 
@@ -381,11 +393,7 @@ def run_ours(args):
         free_all(outs)
         if it >= args.warmup:
             e2e_times.append(s.elapsed_time(e))
-    e2e_ms = sum(e2e_times)
-    if dist:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, _ = job_totals(dist, sum(e2e_times), voxels, "cuda")
     e2e_value = job_voxels * len(e2e_times) / (e2e_ms / 1e3)
 
     # ---- roofline of the dominant kernel (instrumented repetition)

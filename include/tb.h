@@ -276,7 +276,9 @@ TB_API tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks,
  * pages).  With `on` >= 1 on the calling thread, every kernel the library
  * launches is bracketed by two CUDA events on its stream; with `on` >= 2 the
  * pass kernel also stamps the GPU global timer at each of its phase
- * boundaries (records named "phase_*").  tb_profile_read waits for the
+ * boundaries (records named "phase_*", one per stage of a call: the span from
+ * the end of the previous phase to the latest end of this one over the stage's
+ * chains, which run the phase side by side).  tb_profile_read waits for the
  * recorded events, writes up to `max` records (aggregated by name) and clears
  * them; it returns the number of distinct records (which may exceed `max`). */
 TB_API tb_status tb_profile_enable(int32_t on);

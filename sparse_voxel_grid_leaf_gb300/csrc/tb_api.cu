@@ -503,10 +503,12 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   };
   std::vector<ChainBufs> cb(n_chain);
   for (int ch = 0; ch < n_chain; ++ch) {
-    long long max_slots = 0, max_inter = 0;
+    // merged leaves of pass p go to inter[p & 1]: the next pass's source, or
+    // the last pass's staged records
+    long long max_slots = 0, max_inter[2] = {0, 0};
     for (size_t p = 0; p < plans[ch].size(); ++p) {
       max_slots = std::max(max_slots, plans[ch][p].slot_cap);
-      if (p + 1 < plans[ch].size()) max_inter = std::max(max_inter, plans[ch][p].slot_cap);
+      max_inter[p & 1] = std::max(max_inter[p & 1], plans[ch][p].slot_cap);
     }
     const long long last_slots = plans[ch].back().slot_cap;
     ChainBufs& b = cb[ch];
@@ -523,9 +525,9 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     b.blk = c.take((size_t)G * 8);
     b.grp = c.take((size_t)G * 32 * 8);
     for (int k = 0; k < 2; ++k) {
-      b.inter[k][0] = c.take((size_t)max_inter * 12);
-      b.inter[k][1] = c.take((size_t)max_inter * 64);
-      b.inter[k][2] = c.take((size_t)max_inter * 4);
+      b.inter[k][0] = c.take((size_t)max_inter[k] * 12);
+      b.inter[k][1] = c.take((size_t)max_inter[k] * 64);
+      b.inter[k][2] = c.take((size_t)max_inter[k] * 4);
     }
   }
   const size_t o_args = c.take(sizeof(PassArgs) * (size_t)n_chain * n_stage);
@@ -608,6 +610,7 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
 
   // ---- pass arguments, [chain][stage], copied to the device
   size_t pass_index = 0;
+  std::vector<int> pass_stage;
   for (int ch = 0; ch < n_chain; ++ch) {
     const ChainBufs& bf = cb[ch];
     for (int k = 0; k < n_stage; ++k) {
@@ -678,11 +681,10 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       a.grp_agg = (unsigned long long*)(ws + bf.grp);
       a.phase_ts = t_prof >= 2 ? (unsigned long long*)(ws + o_ts) + 8 * pass_index : nullptr;
       ++pass_index;
-      if (!a.last) {
-        a.out_origins = (int32_t*)(ws + bf.inter[k & 1][0]);
-        a.out_masks = (uint64_t*)(ws + bf.inter[k & 1][1]);
-        a.out_grid = (int32_t*)(ws + bf.inter[k & 1][2]);
-      }
+      pass_stage.push_back(k);
+      a.out_origins = (int32_t*)(ws + bf.inter[k & 1][0]);
+      a.out_masks = (uint64_t*)(ws + bf.inter[k & 1][1]);
+      a.out_grid = (int32_t*)(ws + bf.inter[k & 1][2]);
     }
   }
   TB_CUDA(cudaMemcpyAsync(ws + o_args, host_args, args_bytes, cudaMemcpyHostToDevice, stream));
@@ -709,12 +711,20 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     t_phase_ms[5] += std::chrono::duration<double, std::milli>(t_synced - t_sync).count();
     t_phase_n[4] += 1;
     t_phase_n[5] += 1;
-    for (size_t p = 0; p < n_pass_total; ++p)
-      for (int k = 0; k < kNumGpuPhases; ++k) {
-        const unsigned long long t0 = k == 0 ? ~host_ts[8 * p] : host_ts[8 * p + k], t1 = host_ts[8 * p + k + 1];
-        if (t1 >= t0 && t0) {
-          t_phase_ms[k] += (double)(t1 - t0) * 1e-6;
-          t_phase_n[k] += 1;
+    // phase j of stage k spans, over the chains' passes of the stage, from the
+    // latest end of phase j-1 (the earliest start for j = 0) to the latest end
+    for (int k = 0; k < n_stage; ++k)
+      for (int j = 0; j < kNumGpuPhases; ++j) {
+        unsigned long long t0 = j == 0 ? ~0ull : 0ull, t1 = 0;
+        for (size_t p = 0; p < n_pass_total; ++p) {
+          if (pass_stage[p] != k) continue;
+          const unsigned long long s = j == 0 ? ~host_ts[8 * p] : host_ts[8 * p + j];
+          t0 = j == 0 ? std::min(t0, s) : std::max(t0, s);
+          t1 = std::max(t1, host_ts[8 * p + j + 1]);
+        }
+        if (t1 >= t0 && t0 && t0 != ~0ull) {
+          t_phase_ms[j] += (double)(t1 - t0) * 1e-6;
+          t_phase_n[j] += 1;
         }
       }
   }

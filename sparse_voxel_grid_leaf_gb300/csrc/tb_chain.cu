@@ -657,6 +657,10 @@ __device__ void phase_leaves(const PassArgs& a, Smem& sm, int vb, int vg) {
             a.leaf_pop[u] = pop;
             a.leaf_g[u] = g;
           }
+          if (a.out_masks) {
+            a.out_masks[8 * u + w] = word[r];
+            if (w < 3) a.out_origins[3 * u + w] = (int32_t)((uint32_t)lcs[r][w] << 3);
+          }
           if (__ldcg(a.leaf_upper + u) & kGridFirst) {
             F = 1;
             V = pop;
@@ -826,7 +830,8 @@ __device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, Pass
 
 // The phases of the chains of one stage are independent, so each phase splits
 // the grid's blocks over the chains that take part in it, in proportion to
-// their work (candidates, slots or unique leaves), at least one block each.
+// their work (candidates, slots, or unique leaves plus slots), at least one
+// block each.
 // Every block computes the same split from the same counters, so no
 // coordination is needed; a chain's blocks then run its phase as a virtual
 // grid of `vg` blocks.  With more chains than blocks, every block runs every
@@ -861,9 +866,10 @@ __device__ __forceinline__ long long split_weight(const ChainArgs& c, int ch, in
     w = n < kSplitWCap ? n * T : kSplitWCap;
     atomicMax(&sp.maxP, __ldg(&p->P));
     if (!__ldg(&p->last)) sp.more = 1;
-  } else if (kind == kSplitLeaves) {
+  } else if (kind == kSplitLeaves) {  // a leaf costs its record plus one merge step per slot
     const PassCtl* ctl = p->ctl;
-    w = __ldcg(&ctl->head_totals[0]);
+    const ReadbackHeader* rb = p->rb;
+    w = __ldcg(&ctl->head_totals[0]) + __ldcg(&rb->num_slots);
   } else {
     if (kind == kSplitSort && d >= __ldg(&p->P)) return -1;
     const ReadbackHeader* rb = p->rb;
@@ -982,8 +988,7 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
     });
     grid_sync(c.bar, c.err);
     for_share(c, k, -1, 0, sp, a, [&](const PassArgs& pa, int, int vb, int vg) {
-      if (!pa.last) return;
-      phase_voxel_offsets(pa, sm, vb, vg);
+      if (pa.last) phase_voxel_offsets(pa, sm, vb, vg);
       stamp(pa, 4);
     });
     if (more) grid_sync(c.bar, c.err);
@@ -1011,21 +1016,11 @@ __device__ __forceinline__ void write_grid_arrays(const PassArgs& a, const Write
   }
 }
 
-// Leaf u of the group of the calling lane (all 32 lanes of the warp call it).
-template <int OP>
-__device__ __forceinline__ void write_leaf(const PassArgs& a, const WriteOut& o, long long u, long long U) {
+// The record of leaf u of the calling lane's 8-lane group from its merged
+// mask (lane w holds word w), grid and origin; all 32 lanes of the warp call it.
+__device__ __forceinline__ void write_record(const PassArgs& a, const WriteOut& o, long long u, bool valid,
+                                             uint64_t word, uint32_t g, const int32_t org[3]) {
   const int lane = threadIdx.x & 31, w = lane & 7;
-  const uint64_t* keys = a.keys[a.sorted];
-  const uint32_t* vals = a.vals[a.sorted];
-  const bool valid = u < U;
-  uint32_t s0 = 0, s1 = 0, g = 0;
-  int32_t lc[3] = {0, 0, 0};
-  if (valid) {
-    s0 = a.run_start[u];
-    s1 = a.run_start[u + 1];
-    decode_key(a.K, keys[s0], g, lc);
-  }
-  const uint64_t word = merge_run<OP>(a, vals, s0, s1, w);
   const uint32_t pop = __popcll(word);
   uint32_t incl = pop;
 #pragma unroll
@@ -1039,11 +1034,15 @@ __device__ __forceinline__ void write_leaf(const PassArgs& a, const WriteOut& o,
   int32_t mn[3], mx[3];
   leaf_bounds(word, w, lane, mn, mx);
   if (!valid) return;
-  const int32_t org[3] = {(int32_t)((uint32_t)lc[0] << 3), (int32_t)((uint32_t)lc[1] << 3),
-                          (int32_t)((uint32_t)lc[2] << 3)};
+  // this lane's axis (lanes 0-5: min x y z, max x y z), by selects rather than
+  // a dynamic index into local arrays
+  const int ax = w < 3 ? w : w - 3;
+  const int32_t oa = ax == 0 ? org[0] : (ax == 1 ? org[1] : org[2]);
+  const int32_t ma = w < 3 ? (ax == 0 ? mn[0] : (ax == 1 ? mn[1] : mn[2]))
+                           : (ax == 0 ? mx[0] : (ax == 1 ? mx[1] : mx[2]));
   o.masks[8 * u + w] = word;
-  if (w < 3) o.origins[3 * u + w] = org[w];
-  if (w < 6) o.leaf_bbox[6 * u + w] = w < 3 ? org[w] + mn[w] : org[w - 3] + mx[w - 3];
+  if (w < 3) o.origins[3 * u + w] = oa;
+  if (w < 6) o.leaf_bbox[6 * u + w] = oa + ma;
   if (w == 6) o.word_prefix[u] = wp;
   if (w == 7) o.leaf_grid[u] = (int32_t)g;
   if (w == 0) o.voxel_offset[u] = a.leaf_voff[u];
@@ -1065,6 +1064,47 @@ __device__ __forceinline__ void write_leaf(const PassArgs& a, const WriteOut& o,
   }
 }
 
+// Leaf u (< U or not) from the records staged by the leaves phase.
+__device__ __forceinline__ void write_leaf_staged(const PassArgs& a, const WriteOut& o, long long u, long long U) {
+  const int w = threadIdx.x & 7;
+  const bool valid = u < U;
+  uint32_t g = 0;
+  int32_t org[3] = {0, 0, 0};
+  uint64_t word = 0;
+  if (valid) {
+    word = __ldcg(a.out_masks + 8 * u + w);
+    g = __ldcg(a.leaf_g + u);
+#pragma unroll
+    for (int c = 0; c < 3; ++c) org[c] = __ldcg(a.out_origins + 3 * u + c);
+  }
+  write_record(a, o, u, valid, word, g, org);
+}
+
+// Leaf u of a pass: from the staged records when there are any, else by
+// merging its run of slots here.
+template <int OP>
+__device__ __forceinline__ void write_leaf(const PassArgs& a, const WriteOut& o, long long u, long long U) {
+  if (a.out_masks) {
+    write_leaf_staged(a, o, u, U);
+    return;
+  }
+  const int w = threadIdx.x & 7;
+  const bool valid = u < U;
+  const uint64_t* keys = a.keys[a.sorted];
+  const uint32_t* vals = a.vals[a.sorted];
+  uint32_t s0 = 0, s1 = 0, g = 0;
+  int32_t lc[3] = {0, 0, 0}, org[3] = {0, 0, 0};
+  if (valid) {
+    s0 = a.run_start[u];
+    s1 = a.run_start[u + 1];
+    decode_key(a.K, keys[s0], g, lc);
+#pragma unroll
+    for (int c = 0; c < 3; ++c) org[c] = (int32_t)((uint32_t)lc[c] << 3);
+  }
+  const uint64_t word = merge_run<OP>(a, vals, s0, s1, w);
+  write_record(a, o, u, valid, word, g, org);
+}
+
 template <int OP>
 __global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, const WriteOut o) {
   const long long U = (long long)a.rb->num_leaves;
@@ -1076,10 +1116,10 @@ __global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, cons
     write_leaf<OP>(a, o, ub + (lane >> 3), U);
 }
 
-// The writers of several chains in one launch.  Tasks (one per chain, up to
-// kMaxWriteTasks) are staged in shared memory; the leaves of all chains form
-// one index space in units of 4 leaves, so a warp's 4 groups always belong to
-// one chain and take the same code path.
+// The writers of several chains in one launch, from the records their leaves
+// phases staged.  Tasks (one per chain, up to kMaxWriteTasks) are held in
+// shared memory; the leaves of all chains form one index space in units of 4
+// leaves, so a warp's 4 groups always belong to one chain.
 __global__ void __launch_bounds__(kThreads) k_write_multi(const WriteTask* tasks, int n_task) {
   __shared__ __align__(16) WriteTask t[kMaxWriteTasks];
   static_assert(sizeof(WriteTask) % 8 == 0, "task copy");
@@ -1097,14 +1137,7 @@ __global__ void __launch_bounds__(kThreads) k_write_multi(const WriteTask* tasks
     int ch = 0;
     while (ch + 1 < n_task && t[ch + 1].quad_base <= q) ++ch;
     const WriteTask& tk = t[ch];
-    const long long u = (q - tk.quad_base) * 4 + (lane >> 3);
-    switch (tk.a.op) {
-      case kIjk: write_leaf<kIjk>(tk.a, tk.o, u, tk.leaves); break;
-      case kLeaves: write_leaf<kLeaves>(tk.a, tk.o, u, tk.leaves); break;
-      case kRefine: write_leaf<kRefine>(tk.a, tk.o, u, tk.leaves); break;
-      case kCoarsen: write_leaf<kCoarsen>(tk.a, tk.o, u, tk.leaves); break;
-      default: write_leaf<kDilate>(tk.a, tk.o, u, tk.leaves); break;
-    }
+    write_leaf_staged(tk.a, tk.o, (q - tk.quad_base) * 4 + (lane >> 3), tk.leaves);
   }
 }
 

@@ -143,7 +143,9 @@ struct PassArgs {
   unsigned long long* blk_agg;  // [gridDim.x] segmented voxel aggregate per block (last pass)
   unsigned long long* grp_agg;  // [gridDim.x * 32] segmented voxel aggregate per 8-lane group (last pass)
   unsigned long long* phase_ts;  // optional [8] globaltimer stamps (profiling), else null
-  // intermediate output (next pass's source)
+  // merged leaves: the next pass's source (intermediate pass), or the staged
+  // masks and origins the final writer copies (last pass; null: the writer
+  // merges the runs itself, and out_grid is unused)
   int32_t* out_origins;
   uint64_t* out_masks;
   int32_t* out_grid;
