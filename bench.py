@@ -267,23 +267,36 @@ def pass_stats(outs):
 def kernel_bytes(ps):
     """Algorithmic DRAM bytes per kernel over one step (each record read or
     written once; per-grid arrays ignored).  "chain" is the cooperative kernel
-    of a call: emission, digit passes, dedup and the count or hand-off phase of
-    each of its passes; "write_<op>" is the final writer of a one-chain call,
-    "write_multi" the one writer of all chains of a tb_multi call."""
+    of a call: emission, digit passes, index, leaves and voxel offsets of each
+    of its passes; "write_<op>" is the final writer of a one-chain call,
+    "write_multi" the one writer of all chains of a tb_multi call.
+
+    Per pass, with L_in source leaves (voxels for the ijk front end), S slots,
+    L_out unique leaves and P digit passes:
+      emission   source records (80 B: origin, mask, grid; 12 B per voxel) + 12 S
+      sort       24 S P (key and reference read and written per digit pass)
+      index      8 S (keys) + 12 L_out (run start, lower and upper index)
+      leaves     20 L_out + 4 S + the sources again (64 B masks, or 12 B per
+                 voxel slot), then 80 L_out hand-off (intermediate) or
+                 84 L_out staged record, popcount and grid (last)
+      writer     96 L_out read (staged record, grid, voxel offset, node
+                 indices) + 124 L_out written + 16 per lower + 12 per upper
+    """
     by = {}
 
     def acc(name, n):
         by[name] = by.get(name, 0) + n
     for p in ps:
         L_in, S, L_out = p["L_in"], p["S"], p["L_out"]
-        src = 12 * L_in if p["kind"] == "ijk" else 80 * L_in      # voxel ijk, or origin+mask+grid
-        merge = 20 * L_out + 4 * S + (12 * S if p["kind"] == "ijk" else 64 * L_in)
+        ijk = p["kind"] == "ijk"
+        src = 12 * L_in if ijk else 80 * L_in
+        merge = 20 * L_out + 4 * S + (12 * S if ijk else 64 * L_in)
         chain = src + 12 * S + 24 * S * p["P"] + 8 * S + 12 * L_out + merge
-        chain += 80 * L_out if p.get("inter") else 8 * L_out
+        chain += 80 * L_out if p.get("inter") else 84 * L_out
         acc("chain", chain)
         if not p.get("inter"):
-            w = "write_" + p["kind"] if SEPARATE or p["kind"] == "ijk" else "write_multi"
-            acc(w, merge + 16 * L_out + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])
+            w = "write_" + p["kind"] if SEPARATE or ijk else "write_multi"
+            acc(w, 96 * L_out + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])
     return by
 
 

@@ -486,7 +486,9 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   for (int ch = 0; ch < n_chain; ++ch)
     for (size_t p = 0; p < plans[ch].size(); ++p) {
       PassPlan& pl = plans[ch][p];
-      pl.sort_tiles = std::max(1ll, (pl.slot_cap + kSortTile - 1) / kSortTile);
+      // status words for full tiles, or one short tile per block of a small pass
+      pl.sort_tiles = std::max({1ll, (pl.slot_cap + kSortTile - 1) / kSortTile,
+                                std::min<long long>(G, (pl.slot_cap + 255) / 256)});
       pl.dedup_tiles = std::max(1ll, (pl.slot_cap + kDedupTile - 1) / kDedupTile);
       pl.rb = p + 1 == plans[ch].size() ? o_rb_last[ch] : c.take(rb_bytes);
       pl.ctl = c.take(sizeof(PassCtl));

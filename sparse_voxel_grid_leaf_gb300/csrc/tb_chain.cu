@@ -256,51 +256,77 @@ __device__ void phase_emit(const PassArgs& a, Smem& sm, int vb, int vg) {
 
 // ---------------------------------------------------------------- radix digit pass
 
-__device__ void phase_sort(const PassArgs& a, int pass, Smem& sm) {
+// Tiles vb, vb + ... : a block's first tile is its virtual block index; only
+// when a pass has more tiles than the chain has blocks do the rest come from
+// an atomic counter, in increasing order (so every tile's predecessors are
+// held by running blocks, as the look-back needs).
+__device__ __forceinline__ long long next_tile(unsigned int* ctr, long long ntiles, int vg, uint32_t& shared_tile) {
+  if (ntiles <= vg) return ntiles;
+  __syncthreads();
+  if (threadIdx.x == 0) shared_tile = (uint32_t)vg + atomicAdd(ctr, 1u);
+  __syncthreads();
+  return (long long)shared_tile;
+}
+
+// A digit pass.  Tiles hold `ipt` slots per thread (1..kSortItems), chosen so
+// that the chain's blocks get one tile each where the status words allow: a
+// small pass then runs as many short tiles side by side instead of a few long
+// ones.
+__device__ void phase_sort(const PassArgs& a, int pass, Smem& sm, int vb, int vg) {
   constexpr int NW = kThreads / 32;
-  constexpr int WITEMS = 32 * kSortItems;
   SmemSort& s = sm.sort;
   const int shift = 8 * pass;
   const uint64_t* kin = a.keys[pass & 1];
   const uint32_t* vin = a.vals[pass & 1];
   uint64_t* kout = a.keys[(pass + 1) & 1];
   uint32_t* vout = a.vals[(pass + 1) & 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // the slot count, this pass's digit counts and (speculatively, within the
+  // buffers' capacity) the first tile's keys are loaded together
   long long S = (long long)__ldcg(&a.rb->num_slots);
-  if (S > a.slot_cap) S = a.slot_cap;
-  const long long ntiles = (S + kSortTile - 1) / kSortTile;
+  const uint32_t hist = __ldcg(&a.ctl->hist[pass][tid]);
+  const long long cap = a.slot_cap;
+  if (S > cap) S = cap;
+  const long long per_blk = (S + (long long)vg * kThreads - 1) / ((long long)vg * kThreads);
+  const long long per_cap = (S + a.sort_tiles_cap * kThreads - 1) / (a.sort_tiles_cap * kThreads);
+  long long ipt_l = per_blk > per_cap ? per_blk : per_cap;
+  const int ipt = ipt_l < 1 ? 1 : (ipt_l > kSortItems ? kSortItems : (int)ipt_l);
+  const long long TS = (long long)kThreads * ipt;
+  const long long ntiles = (S + TS - 1) / TS;
   uint32_t* status = a.sort_status + (long long)pass * a.sort_tiles_cap * kBins;
   unsigned int* ctr = &a.ctl->sort_tile_ctr[pass];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  {
-    uint32_t total;
-    s.binbase[tid] = block_excl_scan_256(__ldcg(&a.ctl->hist[pass][tid]), s.scan, &total);
-    s.next_hist[tid] = 0;
-  }
   const bool count_next = pass + 1 < a.P;
-  for (;;) {
-    if (tid == 0) s.tile = atomicAdd(ctr, 1u);
-    for (int k = tid; k < NW * kBins; k += kThreads) (&s.whist[0][0])[k] = 0;
-    __syncthreads();
-    const long long tile = s.tile;
-    if (tile >= ntiles) break;
-    const long long base = tile * kSortTile + (long long)warp * WITEMS;
+  s.next_hist[tid] = 0;
+  bool based = false;
+  for (long long tile = vb; tile < ntiles; tile = next_tile(ctr, ntiles, vg, s.tile)) {
+    const long long base = tile * TS + (long long)warp * 32 * ipt;
     uint64_t k[kSortItems];
     uint32_t v[kSortItems], d[kSortItems], r[kSortItems];
 #pragma unroll
     for (int j = 0; j < kSortItems; ++j) {
       const long long idx = base + j * 32 + lane;
-      if (idx < S) {
+      k[j] = 0;
+      v[j] = 0;
+      if (j < ipt && idx < cap) {
         k[j] = __ldcg(kin + idx);
         v[j] = __ldcg(vin + idx);
-        d[j] = (uint32_t)(k[j] >> shift) & 255u;
-      } else {
-        k[j] = 0;
-        v[j] = 0;
-        d[j] = kBins;  // padding: ranked nowhere
       }
     }
 #pragma unroll
     for (int j = 0; j < kSortItems; ++j) {
+      const long long idx = base + j * 32 + lane;
+      d[j] = (j < ipt && idx < S) ? ((uint32_t)(k[j] >> shift) & 255u) : kBins;  // kBins: ranked nowhere
+    }
+    if (!based) {
+      uint32_t total;
+      s.binbase[tid] = block_excl_scan_256(hist, s.scan, &total);
+      based = true;
+    }
+    for (int i = tid; i < NW * kBins; i += kThreads) (&s.whist[0][0])[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < kSortItems; ++j) {
+      if (j >= ipt) break;  // block-uniform
       const uint32_t peers = __match_any_sync(0xffffffffu, d[j]);
       const uint32_t lt = peers & ((1u << lane) - 1u);
       uint32_t cnt = 0;
@@ -326,31 +352,26 @@ __device__ void phase_sort(const PassArgs& a, int pass, Smem& sm) {
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < kSortItems; ++j) {
-      if (d[j] < kBins) {
+      if (j < ipt && d[j] < kBins) {
         const uint32_t lp = s.binstart[d[j]] + s.whist[warp][d[j]] + r[j];
         s.keys[lp] = k[j];
         s.vals[lp] = v[j];
       }
     }
     __syncthreads();
-    const long long rem = S - tile * kSortTile;
-    const int nvalid = rem < kSortTile ? (int)rem : kSortTile;
-    for (int i0 = 0; i0 < nvalid; i0 += kThreads) {  // uniform bound: the warps also histogram
-      const int i = i0 + tid;
-      const bool valid = i < nvalid;
-      uint64_t key = 0;
-      if (valid) {
-        key = s.keys[i];
-        const uint32_t gp = s.glob[(uint32_t)(key >> shift) & 255u] + (uint32_t)i;
-        if (gp < (uint64_t)S) {  // always true when the histograms match the slots
-          kout[gp] = key;
-          vout[gp] = s.vals[i];
-        }
+    const long long rem = S - tile * TS;
+    const int nvalid = rem < TS ? (int)rem : (int)TS;
+    for (int i = tid; i < nvalid; i += kThreads) {
+      const uint64_t key = s.keys[i];
+      const uint32_t gp = s.glob[(uint32_t)(key >> shift) & 255u] + (uint32_t)i;
+      if (gp < (uint64_t)S) {  // always true when the histograms match the slots
+        kout[gp] = key;
+        vout[gp] = s.vals[i];
       }
-      if (count_next) hist_digit(s.next_hist, key, pass + 1, valid);
+      if (count_next) atomicAdd(&s.next_hist[(uint32_t)(key >> (shift + 8)) & 255u], 1u);
     }
-    __syncthreads();
   }
+  __syncthreads();
   if (count_next && s.next_hist[tid]) atomicAdd(&a.ctl->hist[pass + 1][tid], s.next_hist[tid]);
 }
 
@@ -461,7 +482,7 @@ constexpr uint32_t kGridFirst = 0x80000000u;  // leaf_upper flag: first leaf of 
 // Every unique leaf u gets its run start and (last pass) its lower / upper
 // node indices, the upper index flagged when u is its grid's first leaf;
 // each grid gets its first leaf / lower / upper indices.
-__device__ void phase_index(const PassArgs& a, Smem& sm) {
+__device__ void phase_index(const PassArgs& a, Smem& sm, int vb, int vg) {
   SmemDedup& s = sm.dedup;
   const uint64_t* keys = a.keys[a.sorted];
   long long S = (long long)__ldcg(&a.rb->num_slots);
@@ -471,11 +492,7 @@ __device__ void phase_index(const PassArgs& a, Smem& sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t B = a.B;
   constexpr unsigned long long M21 = (1ull << 21) - 1;
-  for (;;) {
-    if (tid == 0) s.tile = atomicAdd(&a.ctl->dedup_tile_ctr, 1u);
-    __syncthreads();
-    const long long tile = s.tile;
-    if (tile >= ntiles) break;
+  for (long long tile = vb; tile < ntiles; tile = next_tile(&a.ctl->dedup_tile_ctr, ntiles, vg, s.tile)) {
     const long long i0 = tile * kDedupTile + (long long)tid * kDedupItems;
     uint64_t prev = (i0 > 0 && i0 - 1 < S) ? __ldcg(keys + i0 - 1) : 0ull;
     uint64_t kk[kDedupItems];
@@ -816,13 +833,26 @@ __device__ void dispatch_leaves(const PassArgs& a, Smem& sm, int vb, int vg) {
   }
 }
 
-// Copies pass (ch, k) into the block's shared copy; returns its op (< 0: none).
-__device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, PassArgs& dst) {
+// The pass held in a block's shared copy.
+struct Loaded {
+  int ch, k;
+};
+
+// Copies pass (ch, k) into the block's shared copy unless it is already
+// there; returns its op (< 0: none).
+__device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, PassArgs& dst, Loaded& held) {
   static_assert(sizeof(PassArgs) % 8 == 0 && sizeof(PassArgs) / 8 <= kThreads, "pass argument copy");
-  __syncthreads();
-  const unsigned long long* from = reinterpret_cast<const unsigned long long*>(c.pass + ch * c.n_stage + k);
-  if (threadIdx.x < sizeof(PassArgs) / 8) reinterpret_cast<unsigned long long*>(&dst)[threadIdx.x] = __ldg(from + threadIdx.x);
-  __syncthreads();
+  __syncthreads();  // the previous phase is done with dst (and held is settled)
+  if (ch != held.ch || k != held.k) {
+    const unsigned long long* from = reinterpret_cast<const unsigned long long*>(c.pass + ch * c.n_stage + k);
+    if (threadIdx.x < sizeof(PassArgs) / 8)
+      reinterpret_cast<unsigned long long*>(&dst)[threadIdx.x] = __ldg(from + threadIdx.x);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      held.ch = ch;
+      held.k = k;
+    }
+  }
   return dst.op;
 }
 
@@ -876,6 +906,104 @@ __device__ __forceinline__ long long split_weight(const ChainArgs& c, int ch, in
     w = __ldcg(&rb->num_slots);
   }
   return (long long)(w < kSplitWCap ? w : kSplitWCap);
+}
+
+// What the split needs of each chain's pass at the current stage, for calls
+// of up to 32 chains: loaded once per stage, so a split costs one load of
+// the chains' counters, a warp scan and one block barrier.
+constexpr int kWarpChains = 32;
+struct StageInfo {
+  const ReadbackHeader* rb;
+  const PassCtl* ctl;
+  const unsigned long long* src_count_dev;
+  long long src_count;
+  int op, P, last, T;
+};
+
+__device__ void load_stage(const ChainArgs& c, int k, StageInfo* si) {
+  __syncthreads();  // the previous stage's splits are done with si
+  const int ch = threadIdx.x;
+  if (ch < c.n_chain && ch < kWarpChains) {
+    const PassArgs* p = c.pass + ch * c.n_stage + k;
+    StageInfo& e = si[ch];
+    e.op = __ldg(&p->op);
+    e.P = __ldg(&p->P);
+    e.last = __ldg(&p->last);
+    e.rb = p->rb;
+    e.ctl = p->ctl;
+    e.src_count_dev = p->src_count_dev;
+    e.src_count = __ldg(&p->src_count);
+    int T = 1;
+    if (e.op == kRefine) {
+      T = 8;
+    } else if (e.op == kDilate) {
+      for (int ax = 0; ax < 3; ++ax) T *= __ldg(&p->hi[ax]) - __ldg(&p->lo[ax]) + 1;
+    }
+    e.T = T;
+  }
+  __syncthreads();
+}
+
+// The split of split_grid for up to 32 chains, by warp 0.
+__device__ void split_warp(const ChainArgs& c, const StageInfo* si, int kind, int d, Split& sp) {
+  const unsigned long long G = gridDim.x, b = blockIdx.x;
+  const int n = c.n_chain;
+  __syncthreads();  // the previous phase is done with sp
+  if (threadIdx.x < 32) {
+    const int ch = threadIdx.x;
+    long long w = -1;
+    int P = 0, more = 0;
+    if (ch < n && si[ch].op >= 0) {
+      const StageInfo& e = si[ch];
+      unsigned long long v = 0;
+      bool on = true;
+      if (n == 1) {
+        v = 1;  // one chain takes the whole grid whatever its work
+      } else if (kind == kSplitEmit) {
+        const unsigned long long ns = e.src_count_dev ? __ldcg(e.src_count_dev) : (unsigned long long)e.src_count;
+        v = ns < kSplitWCap ? ns * (unsigned long long)e.T : kSplitWCap;
+      } else if (kind == kSplitLeaves) {
+        v = __ldcg(&e.ctl->head_totals[0]) + __ldcg(&e.rb->num_slots);
+      } else {
+        on = !(kind == kSplitSort && d >= e.P);
+        if (on) v = __ldcg(&e.rb->num_slots);
+      }
+      if (on) w = (long long)(v < kSplitWCap ? v : kSplitWCap);
+      P = e.P;
+      more = !e.last;
+    }
+    const unsigned long long own = w >= 0 ? kSplitOne + (unsigned long long)w : 0ull;
+    unsigned long long incl = own;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const unsigned long long y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (ch >= off) incl += y;
+    }
+    const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31), ex = incl - own;
+    const int maxP = __reduce_max_sync(0xffffffffu, (unsigned)P);
+    const bool any_more = __any_sync(0xffffffffu, more);
+    const unsigned long long nact = total / kSplitOne, wt = total % kSplitOne;
+    if (ch == 0) {
+      sp.ch = -1;
+      sp.vb = 0;
+      sp.vg = 0;
+      sp.serial = nact > G ? 1 : 0;
+      sp.maxP = maxP;
+      sp.more = any_more ? 1 : 0;
+    }
+    __syncwarp();
+    if (w >= 0 && nact <= G) {
+      const unsigned long long ai = ex / kSplitOne, wex = ex % kSplitOne, extra = G - nact;
+      const unsigned long long s0 = ai + (wt ? extra * wex / wt : extra * ai / nact);
+      const unsigned long long s1 = ai + 1 + (wt ? extra * (wex + (unsigned long long)w) / wt : extra * (ai + 1) / nact);
+      if (b >= s0 && b < s1) {
+        sp.ch = ch;
+        sp.vb = (int)(b - s0);
+        sp.vg = (int)(s1 - s0);
+      }
+    }
+  }
+  __syncthreads();
 }
 
 __device__ void split_grid(const ChainArgs& c, int k, int kind, int d, Split& sp, Smem& sm) {
@@ -933,12 +1061,12 @@ __device__ void split_grid(const ChainArgs& c, int k, int kind, int d, Split& sp
 // in serial mode every chain that takes part, as block blockIdx.x of the grid.
 template <class Body>
 __device__ __forceinline__ void for_share(const ChainArgs& c, int k, int kind, int d, const Split& sp, PassArgs& a,
-                                          Body body) {
+                                          Loaded& held, Body body) {
   const int serial = sp.serial;
   const int nit = serial ? c.n_chain : (sp.ch >= 0 ? 1 : 0);
   for (int it = 0; it < nit; ++it) {
     const int ch = serial ? it : sp.ch;
-    if (load_pass(c, ch, k, a) < 0) continue;
+    if (load_pass(c, ch, k, a, held) < 0) continue;
     if (serial && kind == kSplitSort && d >= a.P) continue;
     body(a, ch, serial ? (int)blockIdx.x : sp.vb, serial ? (int)gridDim.x : sp.vg);
   }
@@ -952,32 +1080,48 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   __shared__ __align__(16) PassArgs a;
   __shared__ Split sp;
+  __shared__ Loaded held;
+  __shared__ StageInfo si[kWarpChains];
+  if (threadIdx.x == 0) {
+    held.ch = -1;
+    held.k = -1;
+  }
+  const bool small = c.n_chain <= kWarpChains;
+  auto split = [&](int k, int kind, int d) {
+    if (small) {
+      split_warp(c, si, kind, d, sp);
+    } else {
+      split_grid(c, k, kind, d, sp, sm);
+    }
+  };
   for (int k = 0; k < c.n_stage; ++k) {
-    split_grid(c, k, kSplitEmit, 0, sp, sm);
+    if (small) load_stage(c, k, si);
+    split(k, kSplitEmit, 0);
     const int maxP = sp.maxP;
     const bool more = sp.more != 0;
-    for_share(c, k, kSplitEmit, 0, sp, a, [&](const PassArgs& pa, int, int vb, int vg) {
+    for_share(c, k, kSplitEmit, 0, sp, a, held, [&](const PassArgs& pa, int, int vb, int vg) {
       stamp(pa, 0);
       dispatch_emit(pa, sm, vb, vg);
       stamp(pa, 1);
     });
     grid_sync(c.bar, c.err);
     for (int d = 0; d < maxP; ++d) {
-      split_grid(c, k, kSplitSort, d, sp, sm);
-      for_share(c, k, kSplitSort, d, sp, a, [&](const PassArgs& pa, int, int, int) { phase_sort(pa, d, sm); });
+      split(k, kSplitSort, d);
+      for_share(c, k, kSplitSort, d, sp, a, held,
+                [&](const PassArgs& pa, int, int vb, int vg) { phase_sort(pa, d, sm, vb, vg); });
       grid_sync(c.bar, c.err);
     }
-    split_grid(c, k, kSplitIndex, 0, sp, sm);
-    for_share(c, k, kSplitIndex, 0, sp, a, [&](const PassArgs& pa, int, int, int) {
+    split(k, kSplitIndex, 0);
+    for_share(c, k, kSplitIndex, 0, sp, a, held, [&](const PassArgs& pa, int, int vb, int vg) {
       stamp(pa, 2);
-      phase_index(pa, sm);
+      phase_index(pa, sm, vb, vg);
       stamp(pa, 3);
     });
     grid_sync(c.bar, c.err);
     // the leaves and voxel offsets share one split: the block aggregates of
     // the leaves phase are indexed by virtual block
-    split_grid(c, k, kSplitLeaves, 0, sp, sm);
-    for_share(c, k, kSplitLeaves, 0, sp, a, [&](const PassArgs& pa, int ch, int vb, int vg) {
+    split(k, kSplitLeaves, 0);
+    for_share(c, k, kSplitLeaves, 0, sp, a, held, [&](const PassArgs& pa, int ch, int vb, int vg) {
       // the totals and per-grid offsets: a block near the end of the chain's
       // share, which holds few leaves
       if (sp.serial ? (int)blockIdx.x == (int)gridDim.x - 1 - (ch % (int)gridDim.x) : vb == vg - 1) {
@@ -987,7 +1131,7 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
       dispatch_leaves(pa, sm, vb, vg);
     });
     grid_sync(c.bar, c.err);
-    for_share(c, k, -1, 0, sp, a, [&](const PassArgs& pa, int, int vb, int vg) {
+    for_share(c, k, -1, 0, sp, a, held, [&](const PassArgs& pa, int, int vb, int vg) {
       if (pa.last) phase_voxel_offsets(pa, sm, vb, vg);
       stamp(pa, 4);
     });

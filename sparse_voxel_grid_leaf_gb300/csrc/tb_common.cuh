@@ -380,10 +380,14 @@ __device__ __forceinline__ T block_excl_scan_256(T v, T* scratch, T* total) {
 
 // Decoupled look-back over 32-bit status words (one thread per digit): publish
 // the tile's aggregate, add predecessors until an inclusive prefix is found,
-// publish the inclusive prefix.  Returns the exclusive prefix.  A wait on a
-// tile that never publishes ends after kSpinLimit polls with kErrTimeout set.
+// publish the inclusive prefix.  Returns the exclusive prefix.  Predecessors
+// are read eight at a time (independent loads), nearest first, so tiles that
+// run at the same time resolve in about one load latency per window.  A wait
+// on a tile that never publishes ends after kSpinLimit polls with kErrTimeout
+// set.
 __device__ __forceinline__ uint32_t lookback32(uint32_t* status, long long stride, long long tile,
                                                uint32_t agg, unsigned int* err) {
+  constexpr int kWin = 8;
   if (tile == 0) {
     st_relaxed(status, kFlagP32 | agg);
     return 0;
@@ -393,19 +397,29 @@ __device__ __forceinline__ uint32_t lookback32(uint32_t* status, long long strid
   long long t = tile - 1;
   uint32_t spins = 0;
   while (t >= 0) {
-    const uint32_t w = ld_relaxed(status + t * stride);
-    const uint32_t f = w & ~kVal32;
-    if (f == 0) {
+    uint32_t w[kWin];
+#pragma unroll
+    for (int j = 0; j < kWin; ++j) w[j] = t - j >= 0 ? ld_relaxed(status + (t - j) * stride) : kFlagP32;
+    int used = 0;
+    bool done = false;
+#pragma unroll
+    for (int j = 0; j < kWin; ++j) {
+      if (done || used < j) continue;  // stop at the first unpublished predecessor
+      const uint32_t f = w[j] & ~kVal32;
+      if (f == 0) continue;
+      excl += w[j] & kVal32;
+      used = j + 1;
+      done = f == kFlagP32;
+    }
+    if (done) break;
+    t -= used;
+    if (used == 0) {
       if (++spins > kSpinLimit) {
         atomicOr(err, kErrTimeout);
         break;
       }
       __nanosleep(32);
-      continue;
     }
-    excl += w & kVal32;
-    if (f == kFlagP32) break;
-    --t;
   }
   st_relaxed(status + tile * stride, kFlagP32 | (excl + agg));
   return excl;
@@ -516,10 +530,10 @@ __device__ __forceinline__ void block_seg_scan_256(uint32_t f, unsigned long lon
 // n * gridDim.x.  The wait gives up after kSpinLimit polls with kErrTimeout
 // set, so a broken barrier ends the kernel instead of hanging it.
 __device__ __forceinline__ void grid_sync(GridBarrier* bar, unsigned int* err) {
-  __syncthreads();
+  __syncthreads();  // the block's writes before thread 0's release below
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned int old = atomicAdd(&bar->count, 1u);
+    unsigned int old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(&bar->count) : "memory");
     const unsigned int target = (old / gridDim.x + 1) * gridDim.x;
     uint32_t spins = 0;
     while ((int)(ld_relaxed(&bar->count) - target) < 0) {
@@ -529,7 +543,7 @@ __device__ __forceinline__ void grid_sync(GridBarrier* bar, unsigned int* err) {
       }
       if (spins > 256) __nanosleep(32);
     }
-    __threadfence();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");  // with the relaxed poll: an acquire
   }
   __syncthreads();
 }
