@@ -273,6 +273,7 @@ def kernel_bytes(ps):
 
     Per pass, with L_in source leaves (voxels for the ijk front end), S slots,
     L_out unique leaves and P digit passes:
+      front end  the input's bbox: 12 B per voxel (ijk front end)
       emission   source records (80 B: origin, mask, grid; 12 B per voxel) + 12 S
       sort       24 S P (key and reference read and written per digit pass)
       index      8 S (keys) + 12 L_out (run start, lower and upper index)
@@ -289,7 +290,7 @@ def kernel_bytes(ps):
     for p in ps:
         L_in, S, L_out = p["L_in"], p["S"], p["L_out"]
         ijk = p["kind"] == "ijk"
-        src = 12 * L_in if ijk else 80 * L_in
+        src = 24 * L_in if ijk else 80 * L_in     # ijk: the bbox read, then the emission's
         merge = 20 * L_out + 4 * S + (12 * S if ijk else 64 * L_in)
         chain = src + 12 * S + 24 * S * p["P"] + 8 * S + 12 * L_out + merge
         chain += 80 * L_out if p.get("inter") else 84 * L_out

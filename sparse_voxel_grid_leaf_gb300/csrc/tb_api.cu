@@ -1,19 +1,19 @@
 // Host driver and C ABI of libtb.so (declared in include/tb.h).
 //
-// One call = one stream-ordered sequence of passes (fVDB PR #757 "Batched
-// leaf-mask topology construction for generated conv grids", Summary item 1):
-// per pass an emission kernel, the digit passes of the radix sort and the
-// dedup scan; intermediate passes of a chain hand their leaves to the next
-// pass on the device, and the last pass does the one count readback,
-// allocates the outputs and runs the batched writer.  All buffers of a call
-// are sized from host-known upper bounds (refine emits at most 8 leaves per
-// source leaf, coarsen 1, a box dilation at most 27), so no readback is
-// needed between passes.
+// One call = one stream-ordered sequence (fVDB PR #757 "Batched leaf-mask
+// topology construction for generated conv grids", Summary item 1): one
+// cooperative launch of the pass kernel runs every pass of every chain of the
+// call (intermediate passes hand their leaves to the next stage on the
+// device), then the one count readback, the exact output allocation and one
+// writer launch.  All buffers of a call are sized from host-known upper
+// bounds (refine emits at most 8 leaves per source leaf, coarsen 1, a box
+// dilation at most its box volume), so no readback is needed between passes.
 //
 // The sort key's width follows the batch's voxel bounding box, which the
 // host tracks exactly: refine maps [lo, hi] to [2 lo, 2 hi + 1], coarsen to
-// [floor(lo/2), floor(hi/2)], a box dilation to [lo + d_lo, hi + d_hi], and
-// the front ends read it back from a small prepass.
+// [floor(lo/2), floor(hi/2)], a box dilation to [lo + d_lo, hi + d_hi].  For
+// the front ends the pass kernel reads the input's bbox and plans the key
+// itself; the host repeats that plan after the readback.
 #include <algorithm>
 #include <chrono>
 #include <cstdarg>
@@ -274,23 +274,8 @@ long long slots_per_source(const PassSpec& s) {
 
 // Output bbox of one pass from its input bbox; false on int32 overflow.
 bool propagate_bbox(const PassSpec& s, const int32_t in[6], int32_t out[6]) {
-  for (int a = 0; a < 3; ++a) {
-    int64_t lo = in[a], hi = in[3 + a];
-    if (s.op == kRefine) {
-      lo = 2 * lo;
-      hi = 2 * hi + 1;
-    } else if (s.op == kCoarsen) {
-      lo = floor_div(lo, 2);
-      hi = floor_div(hi, 2);
-    } else if (s.op == kDilate) {
-      lo += s.lo[a];
-      hi += s.hi[a];
-    }
-    if (lo < INT32_MIN || hi > INT32_MAX) return false;
-    out[a] = (int32_t)lo;
-    out[3 + a] = (int32_t)hi;
-  }
-  return true;
+  const int32_t lo[3] = {s.lo[0], s.lo[1], s.lo[2]}, hi[3] = {s.hi[0], s.hi[1], s.hi[2]};
+  return tb::propagate_bbox(s.op, lo, hi, in, out);
 }
 
 tb_status plan_layouts(std::vector<PassPlan>& plans, int32_t B, const int32_t bbox_in[6], bool empty_in) {
@@ -583,33 +568,6 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   PassArgs* host_args = (PassArgs*)(pinned + readback_span + ts_bytes);
   const ReadbackHeader* host_rb0 = (const ReadbackHeader*)(pinned + o_rb_last[0]);
 
-  // ---- front ends: range prepass and its readback
-  if (front) {
-    ReadbackHeader* rb0 = (ReadbackHeader*)(ws + plans[0][0].rb);
-    const int blocks = blocks_for(src.count, 256, (long long)di->sms * 4);
-    if (src.kind == kSrcIjk)
-      TB_CUDA(launch(kKPrepassIjk, stream,
-                     [&] { return launch_prepass_ijk(in_ijk, src.count, in_off, B, rb0, blocks, stream); }));
-    else
-      TB_CUDA(launch(kKPrepassLeaves, stream, [&] {
-        return launch_prepass_leaves(in_orig, in_mask, src.count, in_off, B, rb0, blocks, stream);
-      }));
-    TB_CUDA(cudaMemcpyAsync((void*)host_rb0, rb0, sizeof(ReadbackHeader), cudaMemcpyDeviceToHost, stream));
-    TB_CUDA(cudaStreamSynchronize(stream));
-    if (host_rb0->err & kErrBadOffsets)
-      return fail(TB_ERR_INVALID_ARG, "offsets must start at 0, be non-decreasing and end at %lld", src.count);
-    if (host_rb0->err & kErrNotAligned) return fail(TB_ERR_INVALID_ARG, "leaf origins must be multiples of 8");
-    int32_t bb[6];
-    for (int a = 0; a < 3; ++a) {
-      bb[a] = dec_min(host_rb0->bbox_enc[a]);
-      bb[3 + a] = dec_max(host_rb0->bbox_enc[3 + a]);
-    }
-    const int P_alloc = plans[0][0].P;
-    st = plan_layouts(plans[0], B, bb, bb[0] > bb[3]);
-    if (st != TB_OK) return st;
-    if (plans[0][0].P > P_alloc) return fail(TB_ERR_CUDA, "internal: digit passes exceed the allocation");
-  }
-
   // ---- pass arguments, [chain][stage], copied to the device
   size_t pass_index = 0;
   std::vector<int> pass_stage;
@@ -694,11 +652,12 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   // ---- the cooperative pass kernel
   {
     ChainArgs ca;
-    ca.pass = (const PassArgs*)(ws + o_args);
+    ca.pass = (PassArgs*)(ws + o_args);
     ca.n_chain = n_chain;
     ca.n_stage = n_stage;
     ca.bar = (GridBarrier*)(ws + o_bar);
     ca.err = (unsigned int*)(ws + o_err);
+    ca.front = front ? 1 : 0;  // the kernel reads the input's bbox and plans the key itself
     TB_CUDA(launch(kKChain, stream, [&] { return launch_chain(ca, G, stream); }));
   }
 
@@ -733,6 +692,23 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   const unsigned int err = *(const unsigned int*)(pinned + o_err);
   if (err & kErrTimeout) return fail(TB_ERR_DEVICE_TIMEOUT, "a device-side wait timed out");
   if (err & kErrSlotOverflow) return fail(TB_ERR_CUDA, "internal: emitted slots exceeded the bound");
+  if (front) {  // the layout the kernel planned, again on the host, for the batch and the writer
+    if (err & kErrBadOffsets)
+      return fail(TB_ERR_INVALID_ARG, "offsets must start at 0, be non-decreasing and end at %lld", src.count);
+    if (err & kErrNotAligned) return fail(TB_ERR_INVALID_ARG, "leaf origins must be multiples of 8");
+    int32_t bb[6];
+    for (int a = 0; a < 3; ++a) {
+      bb[a] = dec_min(host_rb0->bbox_enc[a]);
+      bb[3 + a] = dec_max(host_rb0->bbox_enc[3 + a]);
+    }
+    st = plan_layouts(plans[0], B, bb, bb[0] > bb[3]);
+    if (st != TB_OK) return st;
+    if (err & kErrLayout) return fail(TB_ERR_CUDA, "internal: device and host key layouts disagree");
+    PassArgs& a0 = host_args[0];
+    a0.K = plans[0][0].K;
+    a0.P = plans[0][0].P;
+    a0.sorted = a0.P & 1;
+  }
 
   // ---- outputs, one writer launch per chain
   std::vector<tb_batch*> made(n_chain, nullptr);

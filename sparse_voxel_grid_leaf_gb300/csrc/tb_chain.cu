@@ -23,6 +23,7 @@
 // grid), a tile scan with warp-window look-back.
 #include "tb_common.cuh"
 #include "tb_launch.h"
+#include "tb_layout.h"
 
 namespace tb {
 
@@ -846,7 +847,7 @@ __device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, Pass
   if (ch != held.ch || k != held.k) {
     const unsigned long long* from = reinterpret_cast<const unsigned long long*>(c.pass + ch * c.n_stage + k);
     if (threadIdx.x < sizeof(PassArgs) / 8)
-      reinterpret_cast<unsigned long long*>(&dst)[threadIdx.x] = __ldg(from + threadIdx.x);
+      reinterpret_cast<unsigned long long*>(&dst)[threadIdx.x] = __ldcg(from + threadIdx.x);  // L2: a front end's arguments are patched in the launch
     __syncthreads();
     if (threadIdx.x == 0) {
       held.ch = ch;
@@ -894,14 +895,14 @@ __device__ __forceinline__ long long split_weight(const ChainArgs& c, int ch, in
       for (int ax = 0; ax < 3; ++ax) T *= (unsigned long long)(__ldg(&p->hi[ax]) - __ldg(&p->lo[ax]) + 1);
     }
     w = n < kSplitWCap ? n * T : kSplitWCap;
-    atomicMax(&sp.maxP, __ldg(&p->P));
+    atomicMax(&sp.maxP, __ldcg(&p->P));
     if (!__ldg(&p->last)) sp.more = 1;
   } else if (kind == kSplitLeaves) {  // a leaf costs its record plus one merge step per slot
     const PassCtl* ctl = p->ctl;
     const ReadbackHeader* rb = p->rb;
     w = __ldcg(&ctl->head_totals[0]) + __ldcg(&rb->num_slots);
   } else {
-    if (kind == kSplitSort && d >= __ldg(&p->P)) return -1;
+    if (kind == kSplitSort && d >= __ldcg(&p->P)) return -1;
     const ReadbackHeader* rb = p->rb;
     w = __ldcg(&rb->num_slots);
   }
@@ -927,7 +928,7 @@ __device__ void load_stage(const ChainArgs& c, int k, StageInfo* si) {
     const PassArgs* p = c.pass + ch * c.n_stage + k;
     StageInfo& e = si[ch];
     e.op = __ldg(&p->op);
-    e.P = __ldg(&p->P);
+    e.P = __ldcg(&p->P);
     e.last = __ldg(&p->last);
     e.rb = p->rb;
     e.ctl = p->ctl;
@@ -1072,6 +1073,54 @@ __device__ __forceinline__ void for_share(const ChainArgs& c, int k, int kind, i
   }
 }
 
+// ---------------------------------------------------------------- front ends
+
+// The input's voxel bbox (into the pass's readback block) and the checks of
+// the jagged offsets and leaf origins (into the call's error word), over the
+// whole grid.
+__device__ void phase_front(const PassArgs& a) {
+  int32_t mn[3], mx[3];
+  if (a.op == kIjk) {
+    ijk_bounds(a.ijk, a.src_count, mn, mx);
+  } else {
+    leaves_bounds(a.src_origins, a.src_masks, a.src_count, mn, mx, a.err);
+  }
+  reduce_bbox(mn, mx, a.rb->bbox_enc);
+  check_offsets(a.in_offsets, a.B, a.src_count, a.err);
+}
+
+// After a grid barrier: every block reads the bbox and the checks, and plans
+// the pass's key layout; block 0 writes it into the pass's arguments in
+// device memory.  Returns false (in every block alike) when the call must
+// stop: bad offsets or origins, or a key wider than 64 bits.
+__device__ bool front_plan(const ChainArgs& c, const PassArgs& a) {
+  __shared__ int ok;
+  if (threadIdx.x == 0) {
+    const unsigned int err = __ldcg(c.err);
+    bool good = (err & (kErrBadOffsets | kErrNotAligned | kErrTimeout)) == 0;
+    if (good) {
+      int32_t bb[6];
+      for (int ax = 0; ax < 3; ++ax) {
+        bb[ax] = dec_min(__ldcg(&a.rb->bbox_enc[ax]));
+        bb[3 + ax] = dec_max(__ldcg(&a.rb->bbox_enc[3 + ax]));
+      }
+      KeyLayout K;
+      good = make_layout(a.B, bb, bb[0] > bb[3], K);
+      if (!good) {
+        if (blockIdx.x == 0) atomicOr(c.err, kErrLayout);
+      } else if (blockIdx.x == 0) {
+        PassArgs& g = c.pass[0];
+        g.K = K;
+        g.P = (K.W + 7) / 8;
+        g.sorted = g.P & 1;
+      }
+    }
+    ok = good ? 1 : 0;
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
 // One stage of the launch runs stage k of every chain, phase by phase, the
 // chains of a phase side by side on their shares of the grid.  Stamps:
 // 1 emission, 2 digit passes, 3 index, 4 leaves and voxel offsets.
@@ -1085,6 +1134,14 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
   if (threadIdx.x == 0) {
     held.ch = -1;
     held.k = -1;
+  }
+  if (c.front) {  // one one-pass chain: plan its key from the input's bbox
+    load_pass(c, 0, 0, a, held);
+    phase_front(a);
+    grid_sync(c.bar, c.err);
+    if (!front_plan(c, a)) return;
+    grid_sync(c.bar, c.err);
+    if (threadIdx.x == 0) held.ch = -1;  // reload the planned arguments
   }
   const bool small = c.n_chain <= kWarpChains;
   auto split = [&](int k, int kind, int d) {

@@ -32,6 +32,7 @@ constexpr uint32_t kErrBadOffsets = 2u;    // jagged offsets not monotone / not 
 constexpr uint32_t kErrNotAligned = 4u;    // a leaf origin is not a multiple of 8
 constexpr uint32_t kErrNotCanonical = 8u;  // tb_validate: order or mask violation
 constexpr uint32_t kErrSlotOverflow = 16u; // emission exceeded the host's bound (bug guard)
+constexpr uint32_t kErrLayout = 32u;       // a front end's input needs a key wider than 64 bits
 
 // Look-back status words: two flag bits on top of the value.
 constexpr uint32_t kFlagA32 = 1u << 30, kFlagP32 = 2u << 30, kVal32 = (1u << 30) - 1;
@@ -154,12 +155,16 @@ struct PassArgs {
 // Arguments of one cooperative launch: n_chain chains of up to n_stage
 // passes over the same input; pass[c * n_stage + k] is stage k of chain c
 // (op < 0 where chain c is shorter).  The array lives in device memory.
+// With `front` set, pass 0 of chain 0 (the only pass) is a front end whose
+// key layout the kernel plans itself from the input's bbox, writing K, P and
+// `sorted` into that pass's arguments before the emission.
 struct ChainArgs {
-  const PassArgs* pass;
+  PassArgs* pass;
   int32_t n_chain;
   int32_t n_stage;
   GridBarrier* bar;
   unsigned int* err;
+  int32_t front;
 };
 
 // Outputs of the final writer.
@@ -523,6 +528,93 @@ __device__ __forceinline__ void block_seg_scan_256(uint32_t f, unsigned long lon
   __syncthreads();
   ef = pf | lf;
   ev = lf ? lv : pv + lv;
+}
+
+// ---------------------------------------------------------------- front-end bounds
+
+// Block reduction of encoded bounds, then one atomic per bound per block.
+__device__ __forceinline__ void reduce_bbox(const int32_t mn[3], const int32_t mx[3], unsigned int* enc) {
+  __shared__ unsigned int s_enc[6];
+  if (threadIdx.x < 6) s_enc[threadIdx.x] = 0;
+  __syncthreads();
+  unsigned int e[6] = {enc_min(mn[0]), enc_min(mn[1]), enc_min(mn[2]), enc_max(mx[0]), enc_max(mx[1]),
+                       enc_max(mx[2])};
+#pragma unroll
+  for (int k = 0; k < 6; ++k) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) e[k] = max(e[k], __shfl_xor_sync(0xffffffffu, e[k], off));
+  }
+  if ((threadIdx.x & 31) == 0)
+#pragma unroll
+    for (int k = 0; k < 6; ++k) atomicMax(&s_enc[k], e[k]);
+  __syncthreads();
+  if (threadIdx.x < 6 && s_enc[threadIdx.x]) atomicMax(&enc[threadIdx.x], s_enc[threadIdx.x]);
+}
+
+// Jagged offsets: offsets[0] == 0, non-decreasing, offsets[B] == n.
+__device__ __forceinline__ void check_offsets(const int64_t* off, int32_t B, long long n, unsigned int* err) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g <= B; g += stride) {
+    const int64_t v = off[g];
+    bool bad = (g == 0 && v != 0) || (g == B && v != n) || v < 0 || v > n;
+    if (g > 0 && off[g - 1] > v) bad = true;
+    if (bad) atomicOr(err, kErrBadOffsets);
+  }
+}
+
+// This thread's share (grid-stride) of the bounds of N voxel coordinates.
+__device__ __forceinline__ void ijk_bounds(const int32_t* ijk, long long N, int32_t mn[3], int32_t mx[3]) {
+  for (int a = 0; a < 3; ++a) {
+    mn[a] = INT32_MAX;
+    mx[a] = INT32_MIN;
+  }
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += stride)
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      const int32_t v = __ldg(ijk + 3 * i + a);
+      mn[a] = min(mn[a], v);
+      mx[a] = max(mx[a], v);
+    }
+}
+
+// This thread's share of the exact voxel bounds of L leaves (from their set
+// bits); flags origins that are not multiples of 8.
+__device__ __forceinline__ void leaves_bounds(const int32_t* origins, const uint64_t* masks, long long L,
+                                              int32_t mn[3], int32_t mx[3], unsigned int* err) {
+  for (int a = 0; a < 3; ++a) {
+    mn[a] = INT32_MAX;
+    mx[a] = INT32_MIN;
+  }
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < L; i += stride) {
+    uint64_t m[8];
+    load_mask(masks, i, m);
+    uint64_t all = 0;
+    uint32_t xbits = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      all |= m[w];
+      if (m[w]) xbits |= 1u << w;
+    }
+    const int32_t o[3] = {__ldg(origins + 3 * i), __ldg(origins + 3 * i + 1), __ldg(origins + 3 * i + 2)};
+    if ((o[0] | o[1] | o[2]) & 7) atomicOr(err, kErrNotAligned);
+    if (!all) continue;
+    uint32_t ybits = 0;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if ((all >> (8 * r)) & 0xFFull) ybits |= 1u << r;
+    uint64_t z = all | (all >> 32);
+    z |= z >> 16;
+    z |= z >> 8;
+    const uint32_t zbits = (uint32_t)(z & 0xFFull);
+    const uint32_t b[3] = {xbits, ybits, zbits};
+#pragma unroll
+    for (int a = 0; a < 3; ++a) {
+      mn[a] = min(mn[a], o[a] + (__ffs(b[a]) - 1));
+      mx[a] = max(mx[a], o[a] + (31 - __clz(b[a])));
+    }
+  }
 }
 
 // Software grid barrier for a cooperative launch (all blocks co-resident):

@@ -1,15 +1,20 @@
-// Host-side sort-key layout helpers shared by the pass drivers.
+// Sort-key layout helpers, on the host (pass planning) and on the device (the
+// pass kernel plans a front end's key once it has read the input's bbox).
 #pragma once
 
-#include <algorithm>
 #include <cstdint>
-#include <cstring>
 
 #include "tb_common.cuh"
 
+#ifdef __CUDACC__
+#define TB_HD __host__ __device__
+#else
+#define TB_HD
+#endif
+
 namespace tb {
 
-inline int bitwidth(uint64_t x) {
+TB_HD inline int bitwidth(uint64_t x) {
   int n = 0;
   while (x) {
     ++n;
@@ -18,19 +23,45 @@ inline int bitwidth(uint64_t x) {
   return n;
 }
 
-inline int64_t floor_div(int64_t a, int64_t b) {
+TB_HD inline int64_t floor_div(int64_t a, int64_t b) {
   int64_t q = a / b;
   if ((a % b != 0) && (a < 0)) --q;
   return q;
 }
 
-inline int64_t floor_mod(int64_t a, int64_t b) { return a - b * floor_div(a, b); }
+TB_HD inline int64_t floor_mod(int64_t a, int64_t b) { return a - b * floor_div(a, b); }
+
+TB_HD inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
+
+// Exact voxel bbox after a pass of kind `op` (refine x2: [2lo, 2hi+1];
+// coarsen x2: floor halves; box dilation by [dlo, dhi]: [lo+dlo, hi+dhi]; the
+// front ends keep it).  Returns false if it leaves int32.
+TB_HD inline bool propagate_bbox(int op, const int32_t dlo[3], const int32_t dhi[3], const int32_t in[6],
+                                 int32_t out[6]) {
+  for (int a = 0; a < 3; ++a) {
+    int64_t lo = in[a], hi = in[3 + a];
+    if (op == kRefine) {
+      lo = 2 * lo;
+      hi = 2 * hi + 1;
+    } else if (op == kCoarsen) {
+      lo = floor_div(lo, 2);
+      hi = floor_div(hi, 2);
+    } else if (op == kDilate) {
+      lo += dlo[a];
+      hi += dhi[a];
+    }
+    if (lo < INT32_MIN || hi > INT32_MAX) return false;
+    out[a] = (int32_t)lo;
+    out[3 + a] = (int32_t)hi;
+  }
+  return true;
+}
 
 // Key layout for B grids whose voxels lie in the bbox bb (min xyz, max xyz);
 // see KeyLayout for the per-node shifted fields.  Returns false if the key
 // needs more than 64 bits.
-inline bool make_layout(int32_t B, const int32_t bb[6], bool empty, KeyLayout& K) {
-  std::memset(&K, 0, sizeof K);
+TB_HD inline bool make_layout(int32_t B, const int32_t bb[6], bool empty, KeyLayout& K) {
+  K = KeyLayout{};
   K.gw = B > 1 ? bitwidth((uint64_t)(B - 1)) : 0;
   for (int a = 0; a < 3 && !empty; ++a) {
     const int64_t Lo = floor_div(bb[a], 8), Hi = floor_div(bb[3 + a], 8);  // leaf coordinates
@@ -42,8 +73,8 @@ inline bool make_layout(int32_t B, const int32_t bb[6], bool empty, KeyLayout& K
     K.u_lo[a] = (int32_t)Ulo;
     K.v_lo[a] = (int32_t)Vlo;
     K.tw[a] = bitwidth((uint64_t)(Thi - Tlo));
-    const int64_t umax = (Thi == Tlo) ? Uhi - Ulo : std::max<int64_t>(31 - Ulo, Thi - Tlo >= 2 ? 31 : Uhi);
-    const int64_t vmax = (Bhi == Blo) ? Vhi - Vlo : std::max<int64_t>(15 - Vlo, Bhi - Blo >= 2 ? 15 : Vhi);
+    const int64_t umax = (Thi == Tlo) ? Uhi - Ulo : max64(31 - Ulo, Thi - Tlo >= 2 ? 31 : Uhi);
+    const int64_t vmax = (Bhi == Blo) ? Vhi - Vlo : max64(15 - Vlo, Bhi - Blo >= 2 ? 15 : Vhi);
     K.uw[a] = bitwidth((uint64_t)umax);
     K.vw[a] = bitwidth((uint64_t)vmax);
   }

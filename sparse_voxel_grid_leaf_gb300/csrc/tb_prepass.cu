@@ -14,46 +14,10 @@ namespace {
 
 // ---------------------------------------------------------------- front-end prepasses
 
-__device__ void reduce_bbox(const int32_t mn[3], const int32_t mx[3], unsigned int* enc) {
-  // block-level reduction of the encoded bounds, then one atomic per block
-  __shared__ unsigned int s_enc[6];
-  if (threadIdx.x < 6) s_enc[threadIdx.x] = 0;
-  __syncthreads();
-  unsigned int e[6] = {enc_min(mn[0]), enc_min(mn[1]), enc_min(mn[2]), enc_max(mx[0]), enc_max(mx[1]),
-                       enc_max(mx[2])};
-#pragma unroll
-  for (int k = 0; k < 6; ++k) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) e[k] = max(e[k], __shfl_xor_sync(0xffffffffu, e[k], off));
-  }
-  if ((threadIdx.x & 31) == 0)
-#pragma unroll
-    for (int k = 0; k < 6; ++k) atomicMax(&s_enc[k], e[k]);
-  __syncthreads();
-  if (threadIdx.x < 6 && s_enc[threadIdx.x]) atomicMax(&enc[threadIdx.x], s_enc[threadIdx.x]);
-}
-
-__device__ void check_offsets(const int64_t* off, int32_t B, long long n, unsigned int* err) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g <= B; g += stride) {
-    const int64_t v = off[g];
-    bool bad = (g == 0 && v != 0) || (g == B && v != n) || v < 0 || v > n;
-    if (g > 0 && off[g - 1] > v) bad = true;
-    if (bad) atomicOr(err, kErrBadOffsets);
-  }
-}
-
 __global__ void __launch_bounds__(256) k_prepass_ijk(const int32_t* ijk, long long N, const int64_t* off,
                                                      int32_t B, ReadbackHeader* rb) {
-  int32_t mn[3] = {INT32_MAX, INT32_MAX, INT32_MAX}, mx[3] = {INT32_MIN, INT32_MIN, INT32_MIN};
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += stride)
-#pragma unroll
-    for (int a = 0; a < 3; ++a) {
-      const int32_t v = __ldg(ijk + 3 * i + a);
-      mn[a] = min(mn[a], v);
-      mx[a] = max(mx[a], v);
-    }
+  int32_t mn[3], mx[3];
+  ijk_bounds(ijk, N, mn, mx);
   reduce_bbox(mn, mx, rb->bbox_enc);
   check_offsets(off, B, N, &rb->err);
 }
@@ -62,36 +26,8 @@ __global__ void __launch_bounds__(256) k_prepass_ijk(const int32_t* ijk, long lo
 __global__ void __launch_bounds__(256) k_prepass_leaves(const int32_t* origins, const uint64_t* masks,
                                                         long long L, const int64_t* off, int32_t B,
                                                         ReadbackHeader* rb) {
-  int32_t mn[3] = {INT32_MAX, INT32_MAX, INT32_MAX}, mx[3] = {INT32_MIN, INT32_MIN, INT32_MIN};
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < L; i += stride) {
-    uint64_t m[8];
-    load_mask(masks, i, m);
-    uint64_t all = 0;
-    uint32_t xbits = 0;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      all |= m[w];
-      if (m[w]) xbits |= 1u << w;
-    }
-    const int32_t o[3] = {__ldg(origins + 3 * i), __ldg(origins + 3 * i + 1), __ldg(origins + 3 * i + 2)};
-    if ((o[0] | o[1] | o[2]) & 7) atomicOr(&rb->err, kErrNotAligned);
-    if (!all) continue;
-    uint32_t ybits = 0;
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if ((all >> (8 * r)) & 0xFFull) ybits |= 1u << r;
-    uint64_t z = all | (all >> 32);
-    z |= z >> 16;
-    z |= z >> 8;
-    const uint32_t zbits = (uint32_t)(z & 0xFFull);
-    const uint32_t b[3] = {xbits, ybits, zbits};
-#pragma unroll
-    for (int a = 0; a < 3; ++a) {
-      mn[a] = min(mn[a], o[a] + (__ffs(b[a]) - 1));
-      mx[a] = max(mx[a], o[a] + (31 - __clz(b[a])));
-    }
-  }
+  int32_t mn[3], mx[3];
+  leaves_bounds(origins, masks, L, mn, mx, &rb->err);
   reduce_bbox(mn, mx, rb->bbox_enc);
   check_offsets(off, B, L, &rb->err);
 }

@@ -222,8 +222,9 @@ def test_launches_are_counted():
     n0 = tb.kernel_launch_count()
     ijk, off = synth.make("pr1_b2_res32")
     tb.refine(tb.from_ijk(dev(ijk), dev(off)))
-    # front end: range prepass, pass kernel, writer; refine: pass kernel, writer
-    assert tb.kernel_launch_count() - n0 == 5
+    # front end: pass kernel (which reads the input's range itself), writer;
+    # refine: pass kernel, writer
+    assert tb.kernel_launch_count() - n0 == 4
 
 
 # ---------------------------------------------------------- workload-sized cases
