@@ -81,7 +81,7 @@ typedef struct tb_allocator {
 typedef enum { TB_OP_REFINE = 0, TB_OP_COARSEN = 1, TB_OP_BOX_DILATE = 2 } tb_op_kind;
 
 /* One pass of a chain.  REFINE / COARSEN use `factor` (2, 4 or 8); BOX_DILATE
- * uses lo[a] in {-1, 0} and hi[a] in {0, 1} per axis a (x, y, z). */
+ * uses lo[a] in [-7, 0] and hi[a] in [0, 7] per axis a (x, y, z). */
 typedef struct tb_op {
   int32_t kind;
   int32_t factor;
@@ -171,10 +171,32 @@ TB_API tb_status tb_coarsen(const tb_batch* in, int32_t factor, const tb_allocat
                      tb_batch** out);
 
 /* Box dilation (PR #757 Summary item 2): the Minkowski sum of each grid with
- * the box [lo, hi] (per axis lo in {-1,0}, hi in {0,1}).  [-1,1]^3 is
- * conv_grid k3s1; {-1,0}^3 and {0,1}^3 are the two PadGrid octants. */
+ * the box [lo, hi], per axis lo in [-7, 0] and hi in [0, 7]; one pass, at most
+ * 27 target leaves per source leaf.  [-1,1]^3 is conv_grid k3s1; {-1,0}^3
+ * and {0,1}^3 are the two PadGrid octants.  The stride-1 topology of a
+ * uniform kernel of size K (2 <= K <= 15; the PR's tests use K in 2..5) is
+ * the box [-floor((K-1)/2), ceil((K-1)/2)]^3 -- for even K the extra offset
+ * is on the positive side, a reading the pages leave open -- and the
+ * integer-radius dilation by r (r <= 7) is [-r, r]^3.  Other bounds return
+ * TB_ERR_INVALID_ARG. */
 TB_API tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const int32_t hi[3],
                         const tb_allocator* alloc, tb_stream stream, tb_batch** out);
+
+/* Masked refinement (fVDB PR #757 test plan: masked refine; Summary item 1:
+ * masked subdivision prunes upstream, then refines): the refinement by
+ * `factor` (2, 4 or 8) of the voxels of `in` whose flag is non-zero.
+ *   voxel_mask  one byte per active voxel of `in`, host or device memory, in
+ *               the batch's voxel order: grid by grid, leaf by leaf, and within
+ *               a leaf by ascending bit index n = 64 x + 8 y + z; so voxel
+ *               (leaf i, rank r among its set bits) of grid g is flag
+ *               sum(voxel_counts[0..g)) + voxel_offset[i] + r.  Borrowed;
+ *               must stay valid until the call returns.  May be NULL when the
+ *               batch has no voxels.
+ * The prune is one kernel before the refinement's pass kernel; the result
+ * equals tb_refine of the batch of the flagged voxels.  Errors as tb_refine;
+ * TB_ERR_INVALID_ARG for a NULL voxel_mask over a non-empty batch. */
+TB_API tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask, int32_t factor,
+                                  const tb_allocator* alloc, tb_stream stream, tb_batch** out);
 
 /* Chain of passes applied in order, intermediate results kept on the device
  * (PR #757 Summary items 1-2: multi-pass factors and the k3s2 transpose =

@@ -172,6 +172,36 @@ def run_leaves(origins: np.ndarray, masks: np.ndarray, offsets: np.ndarray,
     return _collect(lib, h, B)
 
 
+def batch_voxels(result: Dict[str, np.ndarray]) -> Tuple[np.ndarray, np.ndarray]:
+    """The active voxels of a result in the batch's voxel order -- grid by
+    grid, leaf by leaf in canonical order, within a leaf by ascending bit
+    index n = 64 x + 8 y + z (fVDB PR #757: every build path enumerates voxels
+    identically) -- as ``(ijk [V,3], offsets [B+1])``."""
+    origins, masks, lo = result["origins"], result["masks"], result["leaf_offsets"]
+    out, offs = [], [0]
+    for g in range(len(lo) - 1):
+        for i in range(int(lo[g]), int(lo[g + 1])):
+            o = origins[i]
+            for n in range(512):
+                if (int(masks[i][n >> 6]) >> (n & 63)) & 1:
+                    out.append((int(o[0]) + (n >> 6), int(o[1]) + ((n >> 3) & 7), int(o[2]) + (n & 7)))
+        offs.append(len(out))
+    return np.array(out, np.int32).reshape(-1, 3), np.array(offs, np.int64)
+
+
+def run_masked_refine(result: Dict[str, np.ndarray], voxel_mask: np.ndarray, factor: int,
+                      lib=None) -> Dict[str, np.ndarray]:
+    """Masked refinement (PR #757 test plan; masked subdivision prunes, then
+    refines): the refinement by ``factor`` of the voxels of ``result`` whose
+    flag in ``voxel_mask`` (batch voxel order, see batch_voxels) is set."""
+    ijk, offs = batch_voxels(result)
+    keep = np.asarray(voxel_mask).astype(bool).reshape(-1)
+    assert keep.shape[0] == ijk.shape[0]
+    counts = [int(keep[offs[g]:offs[g + 1]].sum()) for g in range(len(offs) - 1)]
+    new_offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    return run_voxels(ijk[keep], new_offs, [("refine", factor)], lib)
+
+
 def member(result: Dict[str, np.ndarray], g: int) -> Dict[str, np.ndarray]:
     """The arrays of grid ``g`` alone, as if it had been run as a batch of one."""
     lo, hi = int(result["leaf_offsets"][g]), int(result["leaf_offsets"][g + 1])

@@ -88,6 +88,7 @@ def lib():
                 "tb_box_dilate": [vp, vp, vp, vp, vp, pp],
                 "tb_chain": [vp, vp, i32, vp, vp, pp],
                 "tb_multi": [vp, vp, vp, i32, vp, vp, pp],
+                "tb_refine_masked": [vp, vp, i32, vp, vp, pp],
                 "tb_validate": [vp, vp],
                 "tb_batch_get_view": [vp, ctypes.POINTER(_View)],
                 "tb_batch_export": [vp, vp, vp, vp, vp, vp],
@@ -329,6 +330,21 @@ def refine(b: Batch, factor: int = 2, stream=None) -> Batch:
     return _new(lib().tb_refine, b.handle, int(factor), None, ctypes.c_void_p(_stream(stream)))
 
 
+def refine_masked(b: Batch, voxel_mask, factor: int = 2, stream=None) -> Batch:
+    """Refinement of the voxels whose flag is set: ``voxel_mask`` holds one
+    bool/uint8 per active voxel of ``b`` in the batch's voxel order (grid by
+    grid, leaf by leaf, ascending bit index), on the GPU or the host."""
+    import torch
+    if isinstance(voxel_mask, torch.Tensor) and voxel_mask.dtype == torch.bool:
+        voxel_mask = voxel_mask.view(torch.uint8)
+    elif isinstance(voxel_mask, np.ndarray) and voxel_mask.dtype == np.bool_:
+        voxel_mask = voxel_mask.view(np.uint8)
+    pm, km = _ptr(voxel_mask)
+    _dtype_check(km, "uint8")
+    return _new(lib().tb_refine_masked, b.handle, ctypes.c_void_p(pm), int(factor), None,
+                ctypes.c_void_p(_stream(stream)))
+
+
 def coarsen(b: Batch, factor: int = 2, stream=None) -> Batch:
     return _new(lib().tb_coarsen, b.handle, int(factor), None, ctypes.c_void_p(_stream(stream)))
 
@@ -416,6 +432,40 @@ def conv_grid_k3s1(b: Batch, stream=None) -> Batch:
 def conv_transpose_grid_k3s2(b: Batch, stream=None) -> Batch:
     """conv_transpose_grid with kernel 3, stride 2: refine by 2, then the {-1,0}^3 pad."""
     return chain(b, [("refine", 2), ("dilate", (-1, -1, -1), (0, 0, 0))], stream)
+
+
+def stride1_box(kernel_size: int, transpose: bool = False) -> Tuple[Tuple[int, int, int], Tuple[int, int, int]]:
+    """Box of the stride-1 topology of a uniform kernel of size K (2..15):
+    [-floor((K-1)/2), ceil((K-1)/2)] per axis for conv_grid (for even K the
+    extra offset is on the positive side, a reading the pages leave open), and
+    its mirror image for conv_transpose_grid."""
+    K = int(kernel_size)
+    if K < 1 or K > 15:
+        raise TBError(1, "kernel size %d is outside 1..15" % K)
+    lo, hi = -((K - 1) // 2), K // 2
+    if transpose:
+        lo, hi = -hi, -lo
+    return (lo, lo, lo), (hi, hi, hi)
+
+
+def conv_grid_stride1(b: Batch, kernel_size: int, stream=None) -> Batch:
+    """conv_grid with a uniform kernel of size K and stride 1 (PR #757 Summary
+    item 2): one box dilation."""
+    lo, hi = stride1_box(kernel_size)
+    return box_dilate(b, lo, hi, stream)
+
+
+def conv_transpose_grid_stride1(b: Batch, kernel_size: int, stream=None) -> Batch:
+    """conv_transpose_grid with a uniform kernel of size K and stride 1: the
+    mirrored box."""
+    lo, hi = stride1_box(kernel_size, transpose=True)
+    return box_dilate(b, lo, hi, stream)
+
+
+def dilated_grid(b: Batch, radius: int, stream=None) -> Batch:
+    """Dilation by an integer radius r (0..7): the box [-r, r]^3."""
+    r = int(radius)
+    return box_dilate(b, (-r, -r, -r), (r, r, r), stream)
 
 
 def export_host(b: Batch, origins: np.ndarray, masks: np.ndarray, voxel_offset: Optional[np.ndarray] = None,

@@ -40,6 +40,7 @@ struct tb_batch {
   tb_allocator alloc{};
   void* mem = nullptr;
   std::vector<int64_t> leaf_offsets_host;
+  std::vector<int64_t> voxel_base_host;  // [B+1] exclusive prefix of the grids' voxel counts
   int32_t bbox[6] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MIN, INT32_MIN, INT32_MIN};
   int64_t* leaf_offsets = nullptr;
   int32_t* origins = nullptr;
@@ -67,11 +68,11 @@ thread_local long long t_launches = 0;
 // ---------------------------------------------------------------- kernel timing
 
 enum KernelKind {
-  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + 5, kKWriteMulti, kKNumKinds
+  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + 5, kKWriteMulti, kKPrune, kKNumKinds
 };
 const char* const kKernelNames[kKNumKinds] = {"prepass_ijk",   "prepass_leaves", "chain",        "write_ijk",
                                               "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
-                                              "validate",      "write_multi"};
+                                              "validate",      "write_multi",   "prune"};
 
 struct ProfRec {
   int kind;
@@ -267,7 +268,7 @@ struct PassPlan {
 long long slots_per_source(const PassSpec& s) {
   switch (s.op) {
     case kRefine: return 8;
-    case kDilate: return (long long)(s.hi[0] - s.lo[0] + 1) * (s.hi[1] - s.lo[1] + 1) * (s.hi[2] - s.lo[2] + 1);
+    case kDilate: return dilate_targets(s.lo, s.hi);
     default: return 1;
   }
 }
@@ -734,6 +735,8 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     b->has_alloc = alloc != nullptr;
     if (alloc) b->alloc = *alloc;
     b->leaf_offsets_host.assign(hoff, hoff + B + 1);
+    b->voxel_base_host.assign(B + 1, 0);
+    for (int32_t g = 0; g < B; ++g) b->voxel_base_host[g + 1] = b->voxel_base_host[g] + hoff[3 * (B + 1) + g];
     std::memcpy(b->bbox, last.bbox, sizeof b->bbox);
     if (last.empty || L == 0) {
       const int32_t e[6] = {INT32_MAX, INT32_MAX, INT32_MAX, INT32_MIN, INT32_MIN, INT32_MIN};
@@ -817,8 +820,8 @@ std::vector<PassSpec> expand_ops(const tb_op* ops, int32_t n, tb_status* st) {
     } else if (o.kind == TB_OP_BOX_DILATE) {
       s.op = kDilate;
       for (int a = 0; a < 3; ++a) {
-        if (o.lo[a] < -1 || o.lo[a] > 0 || o.hi[a] < 0 || o.hi[a] > 1) {
-          *st = fail(TB_ERR_INVALID_ARG, "op %d: box bounds must be lo in {-1,0}, hi in {0,1}", i);
+        if (o.lo[a] < -7 || o.lo[a] > 0 || o.hi[a] < 0 || o.hi[a] > 7) {
+          *st = fail(TB_ERR_INVALID_ARG, "op %d: box bounds must be lo in [-7,0], hi in [0,7]", i);
           return {};
         }
         s.lo[a] = o.lo[a];
@@ -936,6 +939,60 @@ tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const int32_t h
   if (!lo || !hi) return fail(TB_ERR_INVALID_ARG, "tb_box_dilate: lo/hi NULL");
   tb_op op{TB_OP_BOX_DILATE, 1, {lo[0], lo[1], lo[2]}, {hi[0], hi[1], hi[2]}};
   return tb_chain(in, &op, 1, alloc, stream, out);
+}
+
+tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask, int32_t factor, const tb_allocator* alloc,
+                           tb_stream stream, tb_batch** out) {
+  if (out) *out = nullptr;
+  if (!out) return fail(TB_ERR_INVALID_ARG, "out is NULL");
+  tb_status st = check_batch(in);
+  if (st != TB_OK) return st;
+  if (in->voxel_base_host.size() != (size_t)in->B + 1)
+    return fail(TB_ERR_INVALID_ARG, "tb_refine_masked: batch without per-grid voxel counts");
+  const int64_t V = in->voxel_base_host[in->B];
+  if (V > 0 && !voxel_mask) return fail(TB_ERR_INVALID_ARG, "tb_refine_masked: voxel_mask is NULL");
+  tb_op op{TB_OP_REFINE, factor, {0, 0, 0}, {0, 0, 0}};
+  std::vector<std::vector<PassSpec>> chains(1);
+  st = chain_specs(&op, 1, &chains[0]);
+  if (st != TB_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  int dev = 0;
+  TB_CUDA(cudaGetDevice(&dev));
+  DeviceInfo* di = nullptr;
+  st = device_info(dev, &di);
+  if (st != TB_OK) return st;
+  // workspace: pruned masks | per-grid voxel bases | the flags, when they are host memory
+  const Mem mem{alloc, s};
+  const bool stage = V > 0 && !device_accessible(voxel_mask);
+  Carve c;
+  const size_t o_masks = c.take((size_t)in->L * 64), o_base = c.take((size_t)(in->B + 1) * 8),
+               o_flags = c.take(stage ? (size_t)V : 0);
+  char* ws = (char*)mem.get(c.off);
+  if (!ws && c.off) return fail(TB_ERR_OOM, "tb_refine_masked: workspace of %zu bytes", c.off);
+  Guard g{&mem, ws};
+  const uint8_t* flags = voxel_mask;
+  if (stage) {
+    TB_CUDA(cudaMemcpyAsync(ws + o_flags, voxel_mask, (size_t)V, cudaMemcpyHostToDevice, s));
+    flags = (const uint8_t*)(ws + o_flags);
+  }
+  // pageable source: the copy is staged before the call returns
+  TB_CUDA(cudaMemcpyAsync(ws + o_base, in->voxel_base_host.data(), (size_t)(in->B + 1) * 8, cudaMemcpyHostToDevice,
+                          s));
+  tb_batch pruned = *in;
+  pruned.masks = in->L ? (uint64_t*)(ws + o_masks) : nullptr;
+  if (in->L) {
+    const int blocks = blocks_for(in->L, 32, (long long)di->sms * 8);
+    TB_CUDA(launch(kKPrune, s, [&] {
+      return launch_prune(in->masks, in->leaf_grid, in->voxel_offset, (const int64_t*)(ws + o_base), flags, in->L,
+                          pruned.masks, blocks, s);
+    }));
+  }
+  Source src;
+  src.kind = kSrcBatch;
+  src.batch = &pruned;
+  src.B = in->B;
+  src.count = in->L;
+  return run(src, chains, alloc, s, out);
 }
 
 tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, const tb_allocator* alloc, tb_stream stream,

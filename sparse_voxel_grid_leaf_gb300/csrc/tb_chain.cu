@@ -153,15 +153,21 @@ __device__ __forceinline__ bool target_nonempty(const PassArgs& a, const uint64_
     out[2] = lc[2] >> sh;
     return all != 0;
   }
-  // box dilation: targets enumerate the box [lo, hi]^3 (per axis offsets in
-  // {-1, 0, 1}); target offset d is reached iff a voxel lies in its zone --
-  // anywhere for d = 0, the last plane for d = +1, the first plane for d = -1
-  const int nx = a.hi[0] - a.lo[0] + 1, ny = a.hi[1] - a.lo[1] + 1, nz = a.hi[2] - a.lo[2] + 1;
-  (void)nx;
-  const int tz = a.lo[2] + (int)(t % nz), ty = a.lo[1] + (int)((t / nz) % ny), tx = a.lo[0] + (int)(t / (nz * ny));
-  const uint64_t xs = tx < 0 ? m[0] : (tx > 0 ? m[7] : all);
-  const uint64_t ym = ty < 0 ? 0x00000000000000FFull : (ty > 0 ? 0xFF00000000000000ull : ~0ull);
-  const uint64_t zm = tz < 0 ? 0x0101010101010101ull : (tz > 0 ? 0x8080808080808080ull : ~0ull);
+  // box dilation: targets enumerate the offsets t in {-1 if lo < 0, 0, +1 if
+  // hi > 0} per axis; target t is reached iff a voxel lies in its zone
+  // (dilate_zone) on all three axes
+  const int tlx = a.lo[0] < 0 ? -1 : 0, tly = a.lo[1] < 0 ? -1 : 0, tlz = a.lo[2] < 0 ? -1 : 0;
+  const int ny = (a.hi[1] > 0 ? 1 : 0) - tly + 1, nz = (a.hi[2] > 0 ? 1 : 0) - tlz + 1;
+  const int tz = tlz + (int)(t % nz), ty = tly + (int)((t / nz) % ny), tx = tlx + (int)(t / (nz * ny));
+  const uint32_t zx = dilate_zone(tx, a.lo[0], a.hi[0]), zy = dilate_zone(ty, a.lo[1], a.hi[1]),
+                 zz = dilate_zone(tz, a.lo[2], a.hi[2]);
+  uint64_t xs = 0, ym = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if ((zx >> k) & 1u) xs |= m[k];
+    if ((zy >> k) & 1u) ym |= 0xFFull << (8 * k);
+  }
+  const uint64_t zm = 0x0101010101010101ull * zz;
   code = (uint32_t)(9 * (tx + 1) + 3 * (ty + 1) + (tz + 1));
   out[0] = lc[0] + tx;
   out[1] = lc[1] + ty;
@@ -173,7 +179,7 @@ __device__ __forceinline__ bool target_nonempty(const PassArgs& a, const uint64_
 template <int OP>
 __device__ __forceinline__ uint32_t targets_per_source(const PassArgs& a) {
   if (OP == kRefine) return 8u;
-  if (OP == kDilate) return (uint32_t)((a.hi[0] - a.lo[0] + 1) * (a.hi[1] - a.lo[1] + 1) * (a.hi[2] - a.lo[2] + 1));
+  if (OP == kDilate) return (uint32_t)dilate_targets(a.lo, a.hi);
   return 1u;
 }
 
@@ -398,6 +404,10 @@ __device__ __forceinline__ uint64_t merge_run(const PassArgs& a, const uint32_t*
   uint64_t c[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) c[k] = 0;
+  // a box within [-1, 1] per axis takes the constant-mask path
+  const bool unit = OP == kDilate && a.lo[0] >= -1 && a.lo[1] >= -1 && a.lo[2] >= -1 && a.hi[0] <= 1 &&
+                    a.hi[1] <= 1 && a.hi[2] <= 1;
+  (void)unit;
   for (uint32_t s = s0 + w; s < s1; s += 8) {
     const uint32_t val = __ldcg(vals + s);
     if constexpr (OP == kIjk) {
@@ -422,19 +432,16 @@ __device__ __forceinline__ uint64_t merge_run(const PassArgs& a, const uint32_t*
       for (int k = 0; k < 8; ++k) c[k] |= ((k >> 2) == qx) ? cw[k & 3] : 0ull;
     } else {  // kDilate
       const int tx = (int)(code / 9) - 1, ty = (int)((code / 3) % 3) - 1, tz = (int)(code % 3) - 1;
+      if (unit) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint64_t r;
-        if (tx == 0) {
-          r = m[k];
-          if (a.hi[0] > 0 && k >= 1) r |= m[k - 1];
-          if (a.lo[0] < 0 && k <= 6) r |= m[k + 1];
-        } else if (tx > 0) {
-          r = (k == 0) ? m[7] : 0ull;
-        } else {
-          r = (k == 7) ? m[0] : 0ull;
-        }
-        c[k] |= dilate_y(dilate_z(r, tz, a.lo[2], a.hi[2]), ty, a.lo[1], a.hi[1]);
+        for (int k = 0; k < 8; ++k)
+          c[k] |= dilate_y1(dilate_z1(dilate_x1(m, k, tx, a.lo[0], a.hi[0]), tz, a.lo[2], a.hi[2]), ty, a.lo[1],
+                            a.hi[1]);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          c[k] |= dilate_y(dilate_z(dilate_x(m, k, tx, a.lo[0], a.hi[0]), tz, a.lo[2], a.hi[2]), ty, a.lo[1],
+                           a.hi[1]);
       }
     }
     }
@@ -891,8 +898,9 @@ __device__ __forceinline__ long long split_weight(const ChainArgs& c, int ch, in
     if (op == kRefine) {
       T = 8;
     } else if (op == kDilate) {
-      T = 1;
-      for (int ax = 0; ax < 3; ++ax) T *= (unsigned long long)(__ldg(&p->hi[ax]) - __ldg(&p->lo[ax]) + 1);
+      const int32_t lo[3] = {__ldg(&p->lo[0]), __ldg(&p->lo[1]), __ldg(&p->lo[2])};
+      const int32_t hi[3] = {__ldg(&p->hi[0]), __ldg(&p->hi[1]), __ldg(&p->hi[2])};
+      T = (unsigned long long)dilate_targets(lo, hi);
     }
     w = n < kSplitWCap ? n * T : kSplitWCap;
     atomicMax(&sp.maxP, __ldcg(&p->P));
@@ -938,7 +946,9 @@ __device__ void load_stage(const ChainArgs& c, int k, StageInfo* si) {
     if (e.op == kRefine) {
       T = 8;
     } else if (e.op == kDilate) {
-      for (int ax = 0; ax < 3; ++ax) T *= __ldg(&p->hi[ax]) - __ldg(&p->lo[ax]) + 1;
+      const int32_t lo[3] = {__ldg(&p->lo[0]), __ldg(&p->lo[1]), __ldg(&p->lo[2])};
+      const int32_t hi[3] = {__ldg(&p->hi[0]), __ldg(&p->hi[1]), __ldg(&p->hi[2])};
+      T = dilate_targets(lo, hi);
     }
     e.T = T;
   }

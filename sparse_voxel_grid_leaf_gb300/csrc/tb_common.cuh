@@ -312,9 +312,36 @@ __device__ __forceinline__ uint64_t coarsen_word(uint64_t t, int qy, int qz) {
   return out;
 }
 
-// Box dilation restricted to one target leaf offset: the z part (bits within
-// a row) and the y part (rows within a word) for target offset t in {-1,0,1}.
+// Box dilation by [lo, hi] (lo in -7..0, hi in 0..7 per axis) restricted to
+// one target leaf at offset t in {-1, 0, 1} along an axis: a voxel at local
+// coordinate c reaches local coordinate c + d - 8 t of the target for every d
+// in [lo, hi] that keeps it inside 0..7.  Per axis that is an OR of shifts by
+// k = d - 8 t, |k| <= 7.
+//   z: bits within each row (byte) of a word;
+//   y: rows within a word;
+//   x: words of the mask (see dilate_x).
 __device__ __forceinline__ uint64_t dilate_z(uint64_t s, int tz, int lo, int hi) {
+  uint64_t r = 0;
+  for (int d = lo; d <= hi; ++d) {
+    const int k = d - 8 * tz;
+    if (k >= 8 || k <= -8) continue;
+    r |= k >= 0 ? (s << k) & (0x0101010101010101ull * ((0xFFu << k) & 0xFFu))
+                : (s >> -k) & (0x0101010101010101ull * (0xFFu >> -k));
+  }
+  return r;
+}
+__device__ __forceinline__ uint64_t dilate_y(uint64_t s, int ty, int lo, int hi) {
+  uint64_t r = 0;
+  for (int d = lo; d <= hi; ++d) {
+    const int k = d - 8 * ty;
+    if (k >= 8 || k <= -8) continue;
+    r |= k >= 0 ? s << (8 * k) : s >> (-8 * k);
+  }
+  return r;
+}
+// The same three parts for a box within [-1, 1] per axis, with constant
+// masks: the common conv-grid case (k3s1, the pads, the k3s2 transpose).
+__device__ __forceinline__ uint64_t dilate_z1(uint64_t s, int tz, int lo, int hi) {
   if (tz == 0) {
     uint64_t r = s;
     if (hi > 0) r |= (s << 1) & 0xFEFEFEFEFEFEFEFEull;
@@ -324,7 +351,7 @@ __device__ __forceinline__ uint64_t dilate_z(uint64_t s, int tz, int lo, int hi)
   if (tz > 0) return (s >> 7) & 0x0101010101010101ull;  // z = 7 moves to z = 0 of the next leaf
   return (s << 7) & 0x8080808080808080ull;              // z = 0 moves to z = 7 of the previous leaf
 }
-__device__ __forceinline__ uint64_t dilate_y(uint64_t s, int ty, int lo, int hi) {
+__device__ __forceinline__ uint64_t dilate_y1(uint64_t s, int ty, int lo, int hi) {
   if (ty == 0) {
     uint64_t r = s;
     if (hi > 0) r |= s << 8;
@@ -333,6 +360,35 @@ __device__ __forceinline__ uint64_t dilate_y(uint64_t s, int ty, int lo, int hi)
   }
   if (ty > 0) return s >> 56;  // row 7 moves to row 0 of the next leaf
   return s << 56;              // row 0 moves to row 7 of the previous leaf
+}
+__device__ __forceinline__ uint64_t dilate_x1(const uint64_t m[8], int k, int tx, int lo, int hi) {
+  if (tx == 0) {
+    uint64_t r = m[k];
+    if (hi > 0 && k >= 1) r |= m[k - 1];
+    if (lo < 0 && k <= 6) r |= m[k + 1];
+    return r;
+  }
+  if (tx > 0) return k == 0 ? m[7] : 0ull;
+  return k == 7 ? m[0] : 0ull;
+}
+
+// Word k of the x part for target offset tx: the OR of source words k - k'
+// for the shifts k' = d - 8 tx that land inside the target.
+__device__ __forceinline__ uint64_t dilate_x(const uint64_t m[8], int k, int tx, int lo, int hi) {
+  uint64_t r = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int sh = k - j + 8 * tx;  // the d that carries word j to word k
+    if (sh >= lo && sh <= hi) r |= m[j];
+  }
+  return r;
+}
+// The voxels of a source leaf that reach target offset t along an axis lie in
+// local coordinates [8t - hi, 8t + 7 - lo] within 0..7; the bits of that zone
+// as a mask over the 8 positions (bit c = coordinate c).
+__device__ __forceinline__ uint32_t dilate_zone(int t, int lo, int hi) {
+  const int a = 8 * t - hi < 0 ? 0 : 8 * t - hi, b = 8 * t + 7 - lo > 7 ? 7 : 8 * t + 7 - lo;
+  return a > b ? 0u : ((0xFFu >> (7 - b)) & (0xFFu << a)) & 0xFFu;
 }
 
 // OR-reduce-scatter over an aligned group of 8 lanes: lane w of the group

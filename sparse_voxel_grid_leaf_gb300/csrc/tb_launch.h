@@ -25,6 +25,11 @@ cudaError_t launch_prepass_ijk(const int32_t* ijk, long long N, const int64_t* o
 cudaError_t launch_prepass_leaves(const int32_t* origins, const uint64_t* masks, long long L,
                                   const int64_t* off, int32_t B, ReadbackHeader* rb, int blocks,
                                   cudaStream_t s);
+// Masked refinement: keeps the voxels of each leaf whose flag (one byte per
+// voxel, in the batch's voxel order) is non-zero.
+cudaError_t launch_prune(const uint64_t* masks, const int32_t* leaf_grid, const int64_t* voxel_offset,
+                         const int64_t* vbase, const uint8_t* flags, long long L, uint64_t* out, int blocks,
+                         cudaStream_t s);
 cudaError_t launch_validate(const int32_t* origins, const uint64_t* masks, const int32_t* leaf_grid,
                             const int64_t* leaf_offsets, long long L, int32_t B, unsigned int* err,
                             int blocks, cudaStream_t s);

@@ -33,6 +33,14 @@ TB_HD inline int64_t floor_mod(int64_t a, int64_t b) { return a - b * floor_div(
 
 TB_HD inline int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
+// Target leaves per source leaf of a box dilation by [lo, hi] (|lo|, hi <= 7):
+// offsets -1 (if lo < 0), 0, +1 (if hi > 0) per axis.
+TB_HD inline int dilate_targets(const int32_t lo[3], const int32_t hi[3]) {
+  int n = 1;
+  for (int a = 0; a < 3; ++a) n *= 1 + (lo[a] < 0 ? 1 : 0) + (hi[a] > 0 ? 1 : 0);
+  return n;
+}
+
 // Exact voxel bbox after a pass of kind `op` (refine x2: [2lo, 2hi+1];
 // coarsen x2: floor halves; box dilation by [dlo, dhi]: [lo+dlo, hi+dhi]; the
 // front ends keep it).  Returns false if it leaves int32.

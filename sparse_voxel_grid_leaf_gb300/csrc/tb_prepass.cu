@@ -32,6 +32,40 @@ __global__ void __launch_bounds__(256) k_prepass_leaves(const int32_t* origins, 
   check_offsets(off, B, L, &rb->err);
 }
 
+// Masked refinement's pruning step (fVDB PR #757, Summary item 1: masked
+// subdivision prunes upstream, then refines): each leaf keeps the voxels whose
+// flag is set.  Voxel v of grid g sits at flag index vbase[g] + voxel_offset
+// of its leaf + its rank among the leaf's set bits (ascending bit index).
+// One 8-lane group per leaf, lane w on mask word w.
+__global__ void __launch_bounds__(256) k_prune(const uint64_t* masks, const int32_t* leaf_grid,
+                                               const int64_t* voxel_offset, const int64_t* vbase,
+                                               const uint8_t* flags, long long L, uint64_t* out) {
+  const int lane = threadIdx.x & 31, w = lane & 7;
+  const long long groups = (long long)gridDim.x * (blockDim.x / 8);
+  // ub is uniform within the warp, so the group shuffles see all 32 lanes
+  for (long long ub = (long long)blockIdx.x * (blockDim.x / 8) + (threadIdx.x >> 5) * 4; ub < L; ub += groups) {
+    const long long u = ub + (lane >> 3);
+    const bool valid = u < L;
+    const uint64_t word = valid ? __ldg(masks + 8 * u + w) : 0ull;
+    const uint32_t pop = __popcll(word);
+    uint32_t incl = pop;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off, 8);
+      if (w >= off) incl += y;
+    }
+    if (!valid) continue;
+    const long long first = vbase[leaf_grid[u]] + voxel_offset[u] + (incl - pop);
+    uint64_t kept = 0, rest = word;
+    for (uint32_t j = 0; rest; ++j) {
+      const uint64_t bit = rest & (~rest + 1);
+      if (__ldg(flags + first + j)) kept |= bit;
+      rest ^= bit;
+    }
+    out[8 * u + w] = kept;
+  }
+}
+
 // Canonical-order comparison of two leaf origins: signed tile, then x-major
 // upper child offset, then x-major lower child offset.
 __device__ __forceinline__ bool canon_less(const int32_t a[3], const int32_t b[3]) {
@@ -86,6 +120,13 @@ cudaError_t launch_prepass_ijk(const int32_t* ijk, long long N, const int64_t* o
 cudaError_t launch_prepass_leaves(const int32_t* origins, const uint64_t* masks, long long L, const int64_t* off,
                                   int32_t B, ReadbackHeader* rb, int blocks, cudaStream_t s) {
   k_prepass_leaves<<<blocks, 256, 0, s>>>(origins, masks, L, off, B, rb);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prune(const uint64_t* masks, const int32_t* leaf_grid, const int64_t* voxel_offset,
+                         const int64_t* vbase, const uint8_t* flags, long long L, uint64_t* out, int blocks,
+                         cudaStream_t s) {
+  k_prune<<<blocks, 256, 0, s>>>(masks, leaf_grid, voxel_offset, vbase, flags, L, out);
   return cudaGetLastError();
 }
 

@@ -26,7 +26,8 @@ def lib():
 def test_header_declares_the_boundary():
     syms = declared_symbols()
     for name in ("tb_from_ijk", "tb_from_leaves", "tb_refine", "tb_coarsen", "tb_box_dilate",
-                 "tb_chain", "tb_batch_free", "tb_batch_get_view", "tb_validate", "tb_last_error"):
+                 "tb_chain", "tb_multi", "tb_refine_masked", "tb_batch_free", "tb_batch_get_view", "tb_validate",
+                 "tb_last_error"):
         assert name in syms
 
 
@@ -53,6 +54,10 @@ def test_host_side_argument_errors(lib):
     out = ctypes.c_void_p(123)
     st = lib.tb_chain(None, None, ctypes.c_int32(-1), None, None, ctypes.byref(out))
     assert st == 1 and out.value is None
+    out = ctypes.c_void_p(123)
+    st = lib.tb_refine_masked(None, None, ctypes.c_int32(2), None, None, ctypes.byref(out))
+    assert st == 1 and out.value is None
+    assert b"batch is NULL" in lib.tb_last_error()
     st = lib.tb_batch_get_view(None, None)
     assert st == 1
     assert lib.tb_batch_free(None, None) == 0

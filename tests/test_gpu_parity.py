@@ -201,6 +201,53 @@ def test_multi_many_chains(n):
             assert b.num_leaves == len(want[i % len(kinds)]["origins"])
 
 
+GENERAL_BOXES = [((-2,) * 3, (2,) * 3), ((-1,) * 3, (2,) * 3), ((0,) * 3, (1,) * 3), ((-7,) * 3, (7,) * 3),
+                 ((-7, 0, -3), (0, 5, 7)), ((0, -4, -1), (6, 0, 1)), ((-3, -3, 0), (0, 0, 3))]
+
+
+@pytest.mark.parametrize("box", GENERAL_BOXES)
+def test_general_box_dilation(box):
+    # random voxels across the +-4096 tile boundaries and negative octants,
+    # with an empty member; then the shell workload
+    ijk, off = synth.random_voxels(5, 250, 60, seed=31, origin=(-4120, -30, 4070), empty=(3,))
+    check(ijk, off, [("dilate", box[0], box[1])], "random %s" % (box,))
+    volume = np.prod([h - l + 1 for l, h in zip(*box)])
+    if volume <= 125:  # the oracle's cost grows with the box volume
+        ijk, off = synth.make("shells_b16_res64")
+        check(ijk, off, [("dilate", box[0], box[1])], "shells %s" % (box,))
+
+
+@pytest.mark.parametrize("K", [2, 3, 4, 5])
+def test_stride1_uniform_k(K):
+    ijk, off = synth.make("pr1_b2_res32")
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    for transpose in (False, True):
+        lo, hi = tb.stride1_box(K, transpose)
+        got = (tb.conv_transpose_grid_stride1 if transpose else tb.conv_grid_stride1)(b0, K)
+        assert_same(got.to_numpy(), oracle.run_voxels(ijk, off, [("dilate", lo, hi)]), "K=%d %s" % (K, transpose))
+    for r in (0, 1, 2, 3):
+        assert_same(tb.dilated_grid(b0, r).to_numpy(),
+                    oracle.run_voxels(ijk, off, [("dilate", (-r,) * 3, (r,) * 3)]), "radius %d" % r)
+
+
+def test_general_box_in_chains_and_multi():
+    ijk, off = synth.random_voxels(4, 200, 50, seed=33, origin=(-60, 4000, -4100))
+    chains = [[("refine", 2), ("dilate", (-2,) * 3, (1,) * 3)], [("dilate", (-7, 0, 0), (0, 0, 7)), ("coarsen", 2)],
+              [("dilate", (-1,) * 3, (2,) * 3)]]
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    for ops, b in zip(chains, tb.multi(b0, chains)):
+        assert_same(b.to_numpy(), oracle.run_voxels(ijk, off, ops), "multi %s" % (ops,))
+
+
+def test_box_bounds_out_of_range_are_rejected():
+    ijk, off = synth.make("pr1_b2_res32")
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    for lo, hi in (((-8, 0, 0), (0, 0, 0)), ((0, 0, 0), (0, 8, 0)), ((1, 0, 0), (1, 0, 0)), ((0, 0, 0), (0, 0, -1))):
+        with pytest.raises(tb.TBError) as e:
+            tb.box_dilate(b0, lo, hi)
+        assert e.value.status == 1
+
+
 def test_multi_single_launch():
     ijk, off = synth.make("pr1_b2_res32")
     b0 = tb.from_ijk(dev(ijk), dev(off))
@@ -293,3 +340,35 @@ def test_stress_round_trip_full_size(stress):
     ijk, off, b0 = stress
     back = tb.chain(b0, [("refine", 2), ("coarsen", 2)]).to_numpy()
     assert_same(back, b0.to_numpy(), "refine->coarsen")
+
+
+# ---------------------------------------------------------- masked refinement
+
+@pytest.mark.parametrize("factor", [2, 4])
+def test_masked_refine(factor):
+    import torch
+    for ijk, off in (synth.random_voxels(6, 300, 50, seed=51, origin=(-4110, 20, 4080), empty=(0, 4)),
+                     synth.make("shells_b16_res64")):
+        b0 = tb.from_ijk(dev(ijk), dev(off))
+        base = b0.to_numpy()
+        V = int(base["voxel_counts"].sum())
+        rng = np.random.default_rng(factor)
+        flags = (rng.random(V) < 0.35).astype(np.uint8)
+        exp = oracle.run_masked_refine(base, flags, factor)
+        got = tb.refine_masked(b0, torch.from_numpy(flags).cuda(), factor)
+        assert_same(got.to_numpy(), exp, "masked x%d" % factor)
+        got.validate()
+        # flags from host memory and as bools
+        assert_same(tb.refine_masked(b0, flags.astype(bool), factor).to_numpy(), exp, "host flags")
+
+
+def test_masked_refine_all_and_none():
+    import torch
+    ijk, off = synth.make("pr1_b2_res32")
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    V = int(b0.to_numpy(["voxel_counts"])["voxel_counts"].sum())
+    assert_same(tb.refine_masked(b0, torch.ones(V, dtype=torch.bool, device="cuda")).to_numpy(),
+                oracle.run_voxels(ijk, off, [("refine", 2)]), "all flags")
+    none = tb.refine_masked(b0, torch.zeros(V, dtype=torch.bool, device="cuda"))
+    assert none.num_leaves == 0 and none.num_grids == 2
+    none.validate()

@@ -214,6 +214,48 @@ def test_dilate_pad_composition_and_reflection():
         assert H.grid_voxels(a, g) == {(-x, -y, -z) for (x, y, z) in H.grid_voxels(b, g)}
 
 
+# general boxes (stride-1 uniform-K topologies, integer-radius dilation):
+# per axis lo in [-7, 0], hi in [0, 7]
+
+GENERAL_BOXES = [((-2, -2, -2), (2, 2, 2)), ((-1, -1, -1), (2, 2, 2)), ((-7, 0, -3), (0, 5, 7)),
+                 ((0, -4, -1), (6, 0, 1))]
+
+
+@pytest.mark.parametrize("box", GENERAL_BOXES)
+def test_general_box_single_voxel_closed_form(box):
+    # one voxel v -> exactly the box v + [lo, hi]: (hi-lo+1) per axis, bbox v+lo .. v+hi
+    lo, hi = box
+    v = (-9, 4095, 16)
+    res = oracle.run_voxels(np.array([v], np.int32), np.array([0, 1]), [("dilate", lo, hi)])
+    n = 1
+    for a in range(3):
+        n *= hi[a] - lo[a] + 1
+    assert int(res["voxel_counts"][0]) == n
+    assert res["grid_bbox"][0].tolist() == [v[a] + lo[a] for a in range(3)] + [v[a] + hi[a] for a in range(3)]
+    strictly_canonical(res)
+    H.check_derived(res)
+
+
+def test_general_box_is_a_sum_of_unit_boxes():
+    # Minkowski sums of boxes add their bounds: [-2,2] = [-1,1] + [-1,1];
+    # [-1,2] = [-1,1] + [0,1]; [-3,0]x[0,2]x[-1,1] = three unit steps
+    ijk, off = synth.random_voxels(3, 60, 20, seed=5, origin=(-10, 4090, -3))
+    unit = ("dilate", (-1,) * 3, (1,) * 3)
+    same(oracle.run_voxels(ijk, off, [("dilate", (-2,) * 3, (2,) * 3)]), oracle.run_voxels(ijk, off, [unit, unit]))
+    same(oracle.run_voxels(ijk, off, [("dilate", (-1,) * 3, (2,) * 3)]),
+         oracle.run_voxels(ijk, off, [unit, ("dilate", (0,) * 3, (1,) * 3)]))
+    steps = [("dilate", (-1, 0, -1), (0, 1, 0)), ("dilate", (-1, 0, 0), (0, 1, 1)), ("dilate", (-1, 0, 0), (0, 0, 0))]
+    same(oracle.run_voxels(ijk, off, [("dilate", (-3, 0, -1), (0, 2, 1))]), oracle.run_voxels(ijk, off, steps))
+
+
+def test_general_box_reflection():
+    ijk, off = synth.random_voxels(2, 50, 30, seed=6, origin=(-4100, -20, 7))
+    a = oracle.run_voxels(-ijk, off, [("dilate", (-5, 0, -2), (1, 7, 0))])
+    b = oracle.run_voxels(ijk, off, [("dilate", (-1, -7, 0), (5, 0, 2))])
+    for g in range(2):
+        assert H.grid_voxels(a, g) == {(-x, -y, -z) for (x, y, z) in H.grid_voxels(b, g)}
+
+
 # ------------------------------------------------------------------ batches
 
 @pytest.mark.parametrize("empty", [(0,), (2,), (4,), (0, 1, 2, 3, 4)])
@@ -271,3 +313,52 @@ def test_workload_shells_structure():
     assert res["origins"].shape[0] > 0
     strictly_canonical(res)
     assert np.array_equal(res["voxel_counts"], np.array([len(s) for s in H.jagged_sets(ijk, off)]))
+
+
+# ------------------------------------------------------------------ masked refine
+
+def test_batch_voxel_order_matches_voxel_offsets():
+    # the voxel order the masked refinement's flags follow: grid by grid, leaf by
+    # leaf, ascending bit index; consistent with voxel_offset and voxel_counts
+    ijk, off = synth.random_voxels(3, 120, 20, seed=41, origin=(-9, 4090, -4100), empty=(1,))
+    res = oracle.run_voxels(ijk, off)
+    vox, voffs = oracle.batch_voxels(res)
+    assert voffs.tolist() == [0] + np.cumsum(res["voxel_counts"]).tolist()
+    for g in range(3):
+        part = [tuple(v) for v in vox[voffs[g]:voffs[g + 1]]]
+        assert set(part) == H.grid_voxels(res, g)
+        lo = int(res["leaf_offsets"][g])
+        for i in range(lo, int(res["leaf_offsets"][g + 1])):
+            first = int(voffs[g] + res["voxel_offset"][i])
+            o = res["origins"][i]
+            n = min(n for n in range(512) if (int(res["masks"][i][n >> 6]) >> (n & 63)) & 1)
+            assert part[first - voffs[g]] == (o[0] + (n >> 6), o[1] + ((n >> 3) & 7), o[2] + (n & 7))
+
+
+def test_masked_refine_all_none_and_brute():
+    ijk, off = synth.random_voxels(3, 80, 16, seed=42, origin=(-20, 30, -4097))
+    res = oracle.run_voxels(ijk, off)
+    V = int(res["voxel_counts"].sum())
+    same(oracle.run_masked_refine(res, np.ones(V, np.uint8), 2), oracle.run_voxels(ijk, off, [("refine", 2)]))
+    empty = oracle.run_masked_refine(res, np.zeros(V, np.uint8), 2)
+    assert int(empty["leaf_offsets"][-1]) == 0 and len(empty["leaf_offsets"]) == 4
+    rng = np.random.default_rng(3)
+    flags = (rng.random(V) < 0.3).astype(np.uint8)
+    got = oracle.run_masked_refine(res, flags, 4)
+    vox, voffs = oracle.batch_voxels(res)
+    for g in range(3):
+        sel = {tuple(int(c) for c in vox[j]) for j in range(voffs[g], voffs[g + 1]) if flags[j]}
+        assert H.grid_voxels(got, g) == {(4 * x + a, 4 * y + b, 4 * z + c) for (x, y, z) in sel
+                                         for a in range(4) for b in range(4) for c in range(4)}
+
+
+def test_masked_refine_single_flag():
+    # flag only the first voxel of the order: its 8 children at 2v + {0,1}^3
+    one = (np.array([[5, -3, 9], [-8, 0, 1]], np.int32), np.array([0, 2]))
+    res = oracle.run_voxels(*one)
+    flags = np.zeros(2, np.uint8)
+    flags[0] = 1
+    got = oracle.run_masked_refine(res, flags, 2)
+    first = min([(-8, 0, 1), (5, -3, 9)], key=lambda v: canon(v))  # canonical leaf order decides
+    assert H.grid_voxels(got, 0) == {(2 * first[0] + a, 2 * first[1] + b, 2 * first[2] + c)
+                                     for a in (0, 1) for b in (0, 1) for c in (0, 1)}
