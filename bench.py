@@ -11,8 +11,9 @@ the library's C ABI:
   from_ijk (ijk front end), refine x2 (conv_transpose_grid k2s2),
   coarsen x2 (conv_grid k2s2), dilate [-1,1]^3 (conv_grid k3s1), the two pad
   octants {-1,0}^3 and {0,1}^3, the k3s2 transpose chain (refine x2 then the
-  {-1,0}^3 pad), and coarsen x4 (a two-pass chain)  -- 10 passes, 8 calls.
-value = output voxels of all passes of a step / device time of the step.
+  {-1,0}^3 pad) and coarsen x4 -- 8 calls; the library fuses each chain into
+  one pass, so 8 passes.
+value = output voxels of the step's calls / device time of the step.
 
 Legs: device-resident inputs (value); end to end from pinned host memory with
 the results read back (e2e); a repetition with per-kernel CUDA events for the
@@ -148,7 +149,7 @@ def source_hash():
 
 def oracle_step(ijk, off, threads):
     """One step of the oracle, members spread over `threads` threads.
-    Returns output voxels of the step's passes."""
+    Returns output voxels of the step's calls (the metric's count)."""
     import concurrent.futures as cf
     import numpy as np
     import oracle
@@ -164,8 +165,6 @@ def oracle_step(ijk, off, threads):
     for _, ops in STEP:
         for sub, o in members:
             jobs.append((sub, o, ops))
-            if len(ops) == 2:  # a chain: its first pass's output voxels count too
-                jobs.append((sub, o, ops[:1]))
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
         for v in ex.map(one, jobs):
             total += v
@@ -233,10 +232,10 @@ _PLAN = None  # the step's chains, marshalled once
 
 
 def step_voxels(outs):
-    """Output voxels of every pass of a step (chains count their first pass too)."""
+    """Output voxels of the step: the outputs of its eight calls (a chain counts
+    its result only; its passes are fused, so no intermediate is produced)."""
     v = {k: int(b.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for k, b in outs.items()}
-    total = sum(v.values()) + v["refine2"] + v["coarsen2"]  # first passes of k3s2 and coarsen4
-    return total, v
+    return sum(v.values()), v
 
 
 def free_all(outs):
@@ -245,7 +244,9 @@ def free_all(outs):
 
 
 def pass_stats(outs):
-    """Per pass (L_in, S, L_out, P, NL, NU, kind) for the byte model."""
+    """Per pass (L_in, S, L_out, P, NL, NU, kind) for the byte model.  Every
+    call of the step is one pass: k3s2 (refine x2 then the {-1,0}^3 pad) and
+    coarsen x4 are each fused into one pass by the library."""
     b0 = outs["from_ijk"]
     ps = []
 
@@ -258,15 +259,8 @@ def pass_stats(outs):
     add("dilate", b0.num_leaves, outs["dilate_k3s1"])
     add("dilate", b0.num_leaves, outs["pad_neg"])
     add("dilate", b0.num_leaves, outs["pad_pos"])
-    # chains: the intermediate pass equals the single-op call on the same input
-    r = dict(ps[1])
-    r["inter"] = True
-    ps.append(r)
-    add("dilate", outs["refine2"].num_leaves, outs["k3s2"])
-    c = dict(ps[2])
-    c["inter"] = True
-    ps.append(c)
-    add("coarsen", outs["coarsen2"].num_leaves, outs["coarsen4"])
+    add("refine_dilate", b0.num_leaves, outs["k3s2"])
+    add("coarsen", b0.num_leaves, outs["coarsen4"])
     return ps
 
 

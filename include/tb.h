@@ -159,14 +159,15 @@ TB_API tb_status tb_from_leaves(const int32_t* origins, const uint64_t* masks, c
 
 /* Refinement (PR #757 Summary item 1; conv_transpose_grid k2s2 for factor 2):
  * every voxel v becomes the factor^3 voxels factor*v + [0, factor)^3.
- * factor in {2, 4, 8}; 4 and 8 run as chained x2 passes (Summary item 1,
- * multi-pass paragraph) with one readback in total. */
+ * factor in {2, 4, 8}.  The pages chain x2 passes for 4 and 8 (Summary item
+ * 1, multi-pass paragraph); here one pass emits the factor^3 children
+ * directly, with the same result. */
 TB_API tb_status tb_refine(const tb_batch* in, int32_t factor, const tb_allocator* alloc, tb_stream stream,
                     tb_batch** out);
 
 /* Coarsening (PR #757 Summary item 1; conv_grid k2s2 for factor 2): voxel V is
  * active iff some v with floor(v / factor) == V is active.  factor in
- * {2, 4, 8}, chained x2 passes as for tb_refine. */
+ * {2, 4, 8}, one pass for any factor as for tb_refine. */
 TB_API tb_status tb_coarsen(const tb_batch* in, int32_t factor, const tb_allocator* alloc, tb_stream stream,
                      tb_batch** out);
 
@@ -198,9 +199,14 @@ TB_API tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const in
 TB_API tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask, int32_t factor,
                                   const tb_allocator* alloc, tb_stream stream, tb_batch** out);
 
-/* Chain of passes applied in order, intermediate results kept on the device
+/* Chain of ops applied in order, intermediate results kept on the device
  * (PR #757 Summary items 1-2: multi-pass factors and the k3s2 transpose =
- * refine x2 then the {-1,0}^3 pad).  n_ops == 0 copies the batch. */
+ * refine x2 then the {-1,0}^3 pad).  Consecutive ops are fused into one pass
+ * where that pass computes their composition exactly: refinements (or
+ * coarsenings) whose factors multiply to at most 8, box dilations whose
+ * summed bounds stay within [-7, 7], and refinement by 2 followed by a box
+ * within [-1, 1]^3 (so k3s2 is one pass).  The result is the same either way:
+ * each op maps voxels to unions of voxels.  n_ops == 0 copies the batch. */
 TB_API tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, const tb_allocator* alloc,
                    tb_stream stream, tb_batch** out);
 

@@ -68,11 +68,11 @@ thread_local long long t_launches = 0;
 // ---------------------------------------------------------------- kernel timing
 
 enum KernelKind {
-  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + 5, kKWriteMulti, kKPrune, kKNumKinds
+  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKNumKinds
 };
-const char* const kKernelNames[kKNumKinds] = {"prepass_ijk",   "prepass_leaves", "chain",        "write_ijk",
+const char* const kKernelNames[kKNumKinds] = {"prepass_ijk",   "prepass_leaves", "chain",         "write_ijk",
                                               "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
-                                              "validate",      "write_multi",   "prune"};
+                                              "write_refine_dilate", "validate", "write_multi",   "prune"};
 
 struct ProfRec {
   int kind;
@@ -140,7 +140,7 @@ tb_status fail(tb_status st, const char* fmt, ...) {
 struct DeviceInfo {
   int sms = 0;
   int occ_chain = 1;
-  int occ_write[5] = {};
+  int occ_write[kNumOps] = {};
   int occ_write_multi = 1;
   bool coop = false;
   bool ready = false;
@@ -159,7 +159,7 @@ tb_status device_info(int dev, DeviceInfo** out) {
     if (!coop) return fail(TB_ERR_CUDA, "device %d does not support cooperative launches", dev);
     d.coop = true;
     d.occ_chain = chain_occupancy();
-    for (int op = 0; op < 5; ++op) d.occ_write[op] = write_final_occupancy(op);
+    for (int op = 0; op < kNumOps; ++op) d.occ_write[op] = write_final_occupancy(op);
     d.occ_write_multi = write_multi_occupancy();
     // keep freed memory in the default pool between calls
     cudaMemPool_t pool;
@@ -251,6 +251,7 @@ bool device_accessible(const void* p) {
 
 struct PassSpec {
   int op;
+  int32_t factor;  // refine / coarsen
   int32_t lo[3], hi[3];
 };
 
@@ -265,18 +266,12 @@ struct PassPlan {
   size_t rb = 0, ctl = 0, sort_status = 0, dedup_status = 0, first = 0;
 };
 
-long long slots_per_source(const PassSpec& s) {
-  switch (s.op) {
-    case kRefine: return 8;
-    case kDilate: return dilate_targets(s.lo, s.hi);
-    default: return 1;
-  }
-}
+long long slots_per_source(const PassSpec& s) { return pass_targets(s.op, s.factor, s.lo, s.hi); }
 
 // Output bbox of one pass from its input bbox; false on int32 overflow.
 bool propagate_bbox(const PassSpec& s, const int32_t in[6], int32_t out[6]) {
   const int32_t lo[3] = {s.lo[0], s.lo[1], s.lo[2]}, hi[3] = {s.hi[0], s.hi[1], s.hi[2]};
-  return tb::propagate_bbox(s.op, lo, hi, in, out);
+  return tb::propagate_bbox(s.op, s.factor, lo, hi, in, out);
 }
 
 tb_status plan_layouts(std::vector<PassPlan>& plans, int32_t B, const int32_t bbox_in[6], bool empty_in) {
@@ -440,8 +435,9 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       PassPlan& pl = plans[ch][p];
       pl.spec = chains[ch][p];
       pl.in_cap = cap;
-      if (pl.spec.op != kIjk && cap >= (1ll << (32 - kSrcShift)))
-        return fail(TB_ERR_TOO_LARGE, "pass %zu: %lld source leaves exceed the limit of 2^27", p, cap);
+      const int cbits = pass_code_bits(pl.spec.op, pl.spec.factor);
+      if (pl.spec.op != kIjk && cap >= (1ll << (32 - cbits)))
+        return fail(TB_ERR_TOO_LARGE, "pass %zu: %lld source leaves exceed the limit of 2^%d", p, cap, 32 - cbits);
       pl.slot_cap = cap * slots_per_source(pl.spec);
       if (pl.slot_cap >= (1ll << 30))
         return fail(TB_ERR_TOO_LARGE, "pass %zu: up to %lld candidate leaves exceed the limit of 2^30", p,
@@ -588,12 +584,14 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       {  // targets per emission thread: about one round of the grid's threads
         const long long T = slots_per_source(pl.spec);
         const long long want = (pl.in_cap * T + (long long)G * 256 - 1) / ((long long)G * 256);
-        a.tchunk = (int32_t)std::max(1ll, std::min(T, want));
+        a.tchunk = (int32_t)std::max(1ll, std::min({T, want, 32ll}));
       }
       for (int ax = 0; ax < 3; ++ax) {
         a.lo[ax] = pl.spec.lo[ax];
         a.hi[ax] = pl.spec.hi[ax];
       }
+      a.factor = pl.spec.factor;
+      a.code_bits = pass_code_bits(pl.spec.op, pl.spec.factor);
       if (k == 0) {
         a.ijk = in_ijk;
         a.in_offsets = in_off;
@@ -802,7 +800,17 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   return TB_OK;
 }
 
-std::vector<PassSpec> expand_ops(const tb_op* ops, int32_t n, tb_status* st) {
+// The passes of a list of ops.  Consecutive ops are fused where one pass
+// computes their composition exactly (the OR of the per-voxel images commutes
+// with the union that dedups a pass): refinements (or coarsenings) whose
+// factors multiply to at most 8, box dilations whose summed bounds stay
+// within [-7, 7], and refinement by 2 followed by a box within [-1, 1]^3 --
+// the last only for inputs of at most kFuseRefineDilateMax leaves: the fused
+// merge does about four times the mask arithmetic per slot, which pays where
+// a pass is latency-bound (saving a whole pass) and not on large inputs.
+constexpr long long kFuseRefineDilateMax = 32768;
+
+std::vector<PassSpec> expand_ops(const tb_op* ops, int32_t n, tb_status* st, long long in_leaves) {
   std::vector<PassSpec> v;
   *st = TB_OK;
   for (int32_t i = 0; i < n; ++i) {
@@ -810,13 +818,12 @@ std::vector<PassSpec> expand_ops(const tb_op* ops, int32_t n, tb_status* st) {
     PassSpec s;
     std::memset(&s, 0, sizeof s);
     if (o.kind == TB_OP_REFINE || o.kind == TB_OP_COARSEN) {
-      int reps = o.factor == 2 ? 1 : o.factor == 4 ? 2 : o.factor == 8 ? 3 : 0;
-      if (!reps) {
+      if (o.factor != 2 && o.factor != 4 && o.factor != 8) {
         *st = fail(TB_ERR_INVALID_ARG, "op %d: factor %d is not 2, 4 or 8", i, o.factor);
         return {};
       }
       s.op = o.kind == TB_OP_REFINE ? kRefine : kCoarsen;
-      for (int r = 0; r < reps; ++r) v.push_back(s);
+      s.factor = o.factor;
     } else if (o.kind == TB_OP_BOX_DILATE) {
       s.op = kDilate;
       for (int a = 0; a < 3; ++a) {
@@ -827,11 +834,41 @@ std::vector<PassSpec> expand_ops(const tb_op* ops, int32_t n, tb_status* st) {
         s.lo[a] = o.lo[a];
         s.hi[a] = o.hi[a];
       }
-      v.push_back(s);
     } else {
       *st = fail(TB_ERR_INVALID_ARG, "op %d: unknown kind %d", i, o.kind);
       return {};
     }
+    if (!v.empty()) {
+      PassSpec& p = v.back();
+      if ((p.op == kRefine || p.op == kCoarsen) && s.op == p.op && p.factor * s.factor <= 8) {
+        p.factor *= s.factor;
+        continue;
+      }
+      if (p.op == kDilate && s.op == kDilate) {
+        bool fits = true;
+        for (int a = 0; a < 3; ++a) fits &= p.lo[a] + s.lo[a] >= -7 && p.hi[a] + s.hi[a] <= 7;
+        if (fits) {
+          for (int a = 0; a < 3; ++a) {
+            p.lo[a] += s.lo[a];
+            p.hi[a] += s.hi[a];
+          }
+          continue;
+        }
+      }
+      if (p.op == kRefine && p.factor == 2 && s.op == kDilate && in_leaves <= kFuseRefineDilateMax) {
+        bool unit = true;
+        for (int a = 0; a < 3; ++a) unit &= s.lo[a] >= -1 && s.hi[a] <= 1;
+        if (unit) {
+          p.op = kRefineDilate;
+          for (int a = 0; a < 3; ++a) {
+            p.lo[a] = s.lo[a];
+            p.hi[a] = s.hi[a];
+          }
+          continue;
+        }
+      }
+    }
+    v.push_back(s);
   }
   return v;
 }
@@ -858,9 +895,9 @@ tb_status run_ops(const tb_batch* in, const std::vector<std::vector<PassSpec>>& 
 
 // The passes of one chain of ops; an empty chain copies its input (one
 // identity pass over the leaves).
-tb_status chain_specs(const tb_op* ops, int32_t n_ops, std::vector<PassSpec>* specs) {
+tb_status chain_specs(const tb_op* ops, int32_t n_ops, std::vector<PassSpec>* specs, long long in_leaves) {
   tb_status st;
-  *specs = expand_ops(ops, n_ops, &st);
+  *specs = expand_ops(ops, n_ops, &st, in_leaves);
   if (st != TB_OK) return st;
   if (specs->empty()) {
     PassSpec s;
@@ -953,7 +990,7 @@ tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask, int32_
   if (V > 0 && !voxel_mask) return fail(TB_ERR_INVALID_ARG, "tb_refine_masked: voxel_mask is NULL");
   tb_op op{TB_OP_REFINE, factor, {0, 0, 0}, {0, 0, 0}};
   std::vector<std::vector<PassSpec>> chains(1);
-  st = chain_specs(&op, 1, &chains[0]);
+  st = chain_specs(&op, 1, &chains[0], in->L);
   if (st != TB_OK) return st;
   cudaStream_t s = (cudaStream_t)stream;
   int dev = 0;
@@ -1001,7 +1038,7 @@ tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, const tb
   if (!out) return fail(TB_ERR_INVALID_ARG, "out is NULL");
   if (n_ops < 0 || (n_ops > 0 && !ops)) return fail(TB_ERR_INVALID_ARG, "tb_chain: bad op list");
   std::vector<std::vector<PassSpec>> chains(1);
-  tb_status st = chain_specs(ops, n_ops, &chains[0]);
+  tb_status st = chain_specs(ops, n_ops, &chains[0], in ? in->L : 0);
   if (st != TB_OK) return st;
   return run_ops(in, chains, alloc, (cudaStream_t)stream, out);
 }
@@ -1016,7 +1053,7 @@ tb_status tb_multi(const tb_batch* in, const tb_op* ops, const int32_t* chain_le
   for (int32_t c = 0; c < n_chains; ++c) {
     if (chain_lengths[c] < 0 || (chain_lengths[c] > 0 && !ops))
       return fail(TB_ERR_INVALID_ARG, "tb_multi: bad length of chain %d", c);
-    tb_status st = chain_specs(ops + first, chain_lengths[c], &chains[c]);
+    tb_status st = chain_specs(ops + first, chain_lengths[c], &chains[c], in ? in->L : 0);
     if (st != TB_OK) return st;
     first += chain_lengths[c];
   }

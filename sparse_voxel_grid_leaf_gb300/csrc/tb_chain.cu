@@ -132,26 +132,75 @@ __device__ __forceinline__ void hist_digit(unsigned int* hist, uint64_t key, int
 template <int OP>
 __device__ __forceinline__ bool target_nonempty(const PassArgs& a, const uint64_t m[8], const int32_t lc[3],
                                                 uint32_t t, uint32_t& code, int32_t out[3]) {
-  if (OP == kRefine) {  // child t = 4*cx + 2*cy + cz: the parent's octant t holds a voxel
-    const int cx = (t >> 2) & 1, cy = (t >> 1) & 1, cz = t & 1;
-    const uint64_t h = m[4 * cx] | m[4 * cx + 1] | m[4 * cx + 2] | m[4 * cx + 3];
+  if (OP == kRefine) {
+    const int f = a.factor;
+    if (f == 2) {  // child t = 4*cx + 2*cy + cz: the parent's octant t holds a voxel
+      const int cx = (t >> 2) & 1, cy = (t >> 1) & 1, cz = t & 1;
+      const uint64_t h = m[4 * cx] | m[4 * cx + 1] | m[4 * cx + 2] | m[4 * cx + 3];
+      code = t;
+      out[0] = 2 * lc[0] + cx;
+      out[1] = 2 * lc[1] + cy;
+      out[2] = 2 * lc[2] + cz;
+      return (h & (0x0F0F0F0Full << (32 * cy + 4 * cz))) != 0;
+    }
+    // child t = (cx f + cy) f + cz of a refinement by f = 4 or 8: the parent's
+    // block [c 8/f, (c + 1) 8/f) per axis holds a voxel
+    const int bs = 8 / f, cx = (int)t / (f * f), cy = ((int)t / f) % f, cz = (int)t % f;
+    uint64_t h = 0, ym = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (k / bs == cx) h |= m[k];
+      if (k / bs == cy) ym |= 0xFFull << (8 * k);
+    }
+    const uint64_t zm = 0x0101010101010101ull * ((((1u << bs) - 1u) << (cz * bs)) & 0xFFu);
     code = t;
-    out[0] = 2 * lc[0] + cx;
-    out[1] = 2 * lc[1] + cy;
-    out[2] = 2 * lc[2] + cz;
-    return (h & (0x0F0F0F0Full << (32 * cy + 4 * cz))) != 0;
+    out[0] = f * lc[0] + cx;
+    out[1] = f * lc[1] + cy;
+    out[2] = f * lc[2] + cz;
+    return (h & ym & zm) != 0;
   }
   uint64_t all = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k) all |= m[k];
   if (OP == kLeaves || OP == kCoarsen) {
-    // coarsen: the code is the source leaf's octant inside its coarse leaf
-    code = OP == kCoarsen ? (uint32_t)(((lc[0] & 1) << 2) | ((lc[1] & 1) << 1) | (lc[2] & 1)) : 0u;
-    const int sh = OP == kCoarsen ? 1 : 0;
+    // coarsen by f: the code is the source leaf's position q = lc mod f inside
+    // its coarse leaf, (qx f + qy) f + qz
+    const int sh = OP == kCoarsen ? log2_factor(a.factor) : 0, fm = (1 << sh) - 1;
+    code = OP == kCoarsen ? (uint32_t)((((lc[0] & fm) << sh) | (lc[1] & fm)) << sh | (lc[2] & fm)) : 0u;
     out[0] = lc[0] >> sh;
     out[1] = lc[1] >> sh;
     out[2] = lc[2] >> sh;
     return all != 0;
+  }
+  if (OP == kRefineDilate) {
+    // refinement by 2, then a box within [-1, 1]^3: targets are fine leaves at
+    // offsets t (relative to the first child) per axis; the source voxels s
+    // that reach target t along an axis are [(8t - hi) / 2, (8t + 7 - lo) / 2]
+    // (floors), clamped to 0..7
+    const int tlx = refine_dilate_lo(a.lo[0]), tly = refine_dilate_lo(a.lo[1]), tlz = refine_dilate_lo(a.lo[2]);
+    const int ny = refine_dilate_hi(a.hi[1]) - tly + 1, nz = refine_dilate_hi(a.hi[2]) - tlz + 1;
+    const int tz = tlz + (int)(t % nz), ty = tly + (int)((t / nz) % ny), tx = tlx + (int)(t / (nz * ny));
+    const int tt[3] = {tx, ty, tz};
+    uint32_t zone[3];
+#pragma unroll
+    for (int ax = 0; ax < 3; ++ax) {
+      int s0 = (8 * tt[ax] - a.hi[ax]) >> 1, s1 = (8 * tt[ax] + 7 - a.lo[ax]) >> 1;
+      s0 = s0 < 0 ? 0 : s0;
+      s1 = s1 > 7 ? 7 : s1;
+      zone[ax] = s0 > s1 ? 0u : (((0xFFu >> (7 - s1)) & (0xFFu << s0)) & 0xFFu);
+    }
+    uint64_t xs = 0, ym = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if ((zone[0] >> k) & 1u) xs |= m[k];
+      if ((zone[1] >> k) & 1u) ym |= 0xFFull << (8 * k);
+    }
+    const uint64_t zm = 0x0101010101010101ull * zone[2];
+    code = (uint32_t)(((tx + 1) * 4 + (ty + 1)) * 4 + (tz + 1));
+    out[0] = 2 * lc[0] + tx;
+    out[1] = 2 * lc[1] + ty;
+    out[2] = 2 * lc[2] + tz;
+    return (xs & ym & zm) != 0;
   }
   // box dilation: targets enumerate the offsets t in {-1 if lo < 0, 0, +1 if
   // hi > 0} per axis; target t is reached iff a voxel lies in its zone
@@ -178,9 +227,7 @@ __device__ __forceinline__ bool target_nonempty(const PassArgs& a, const uint64_
 // Targets per source leaf of an op.
 template <int OP>
 __device__ __forceinline__ uint32_t targets_per_source(const PassArgs& a) {
-  if (OP == kRefine) return 8u;
-  if (OP == kDilate) return (uint32_t)dilate_targets(a.lo, a.hi);
-  return 1u;
+  return (uint32_t)pass_targets(OP, a.factor, a.lo, a.hi);
 }
 
 // One thread per (source, chunk of a.tchunk targets): it tests its targets,
@@ -194,7 +241,8 @@ __device__ void phase_emit(const PassArgs& a, Smem& sm, int vb, int vg) {
   __syncthreads();
   const long long n = a.src_count_dev ? (long long)__ldcg(a.src_count_dev) : a.src_count;
   const uint32_t T = targets_per_source<OP>(a);
-  const uint32_t k = (a.tchunk > 0 && (uint32_t)a.tchunk < T) ? (uint32_t)a.tchunk : T;
+  uint32_t k = (a.tchunk > 0 && (uint32_t)a.tchunk < T) ? (uint32_t)a.tchunk : T;
+  if (k > 32) k = 32;  // a thread's targets are one 32-bit set
   const uint32_t nchunks = (T + k - 1) / k;
   const long long items = n * (long long)nchunks;
   const long long stride = (long long)vg * kThreads;
@@ -247,7 +295,7 @@ __device__ void phase_emit(const PassArgs& a, Smem& sm, int vb, int vg) {
           int32_t tl[3];
           target_nonempty<OP>(a, m, lc, t, code, tl);
           key = encode_key(a.K, g, tl[0], tl[1], tl[2]);
-          val = ((uint32_t)i << kSrcShift) | code;
+          val = ((uint32_t)i << a.code_bits) | code;
         }
         put_slot(a, pos++, key, val);
       }
@@ -392,12 +440,50 @@ template <int OP>
 __device__ __forceinline__ uint64_t merge_run(const PassArgs& a, const uint32_t* vals, uint32_t s0, uint32_t s1,
                                               int w) {
   if constexpr (OP == kRefine) {
+    const int f = a.factor, cb = a.code_bits;
     uint64_t word = 0;
     for (uint32_t s = s0; s < s1; ++s) {
       const uint32_t val = __ldcg(vals + s);
-      const long long src = (long long)(val >> kSrcShift);
-      const int cx = (val >> 2) & 1, cy = (val >> 1) & 1, cz = val & 1;
-      word |= refine_word(__ldcg(a.src_masks + 8 * src + 4 * cx + (w >> 1)), cy, cz);
+      const long long src = (long long)(val >> cb);
+      const int code = (int)(val & ((1u << cb) - 1u));
+      if (f == 2) {
+        const int cx = (code >> 2) & 1, cy = (code >> 1) & 1, cz = code & 1;
+        word |= refine_word(__ldcg(a.src_masks + 8 * src + 4 * cx + (w >> 1)), cy, cz);
+      } else {
+        const int cx = code / (f * f), cy = (code / f) % f, cz = code % f;
+        word |= refine_word_f(__ldcg(a.src_masks + 8 * src + (8 * cx + w) / f), cy, cz, f);
+      }
+    }
+    return word;
+  } else if constexpr (OP == kRefineDilate) {
+    // lane w builds target word w: along x, the fine positions 8 tx + w - d
+    // (d in [lo, hi]) inside the refined 16^3 block, i.e. source words
+    // (8 tx + w - d) / 2; along y and z, the child quadrants (cy, cz) whose
+    // dilation reaches the target, each refined and dilated as a plane
+    const int cb = a.code_bits;
+    uint64_t word = 0;
+    for (uint32_t s = s0; s < s1; ++s) {
+      const uint32_t val = __ldcg(vals + s);
+      const long long src = (long long)(val >> cb);
+      const int code = (int)(val & 63u);
+      const int tx = (code >> 4) - 1, ty = ((code >> 2) & 3) - 1, tz = (code & 3) - 1;
+      uint64_t mx = 0;
+      for (int d = a.lo[0]; d <= a.hi[0]; ++d) {
+        const int fx = 8 * tx + w - d;
+        if (fx >= 0 && fx < 16) mx |= __ldcg(a.src_masks + 8 * src + (fx >> 1));
+      }
+      if (!mx) continue;
+#pragma unroll
+      for (int cy = 0; cy < 2; ++cy) {
+        const int dy = ty - cy;
+        if (dy < -1 || dy > 1 || (dy < 0 && a.lo[1] >= 0) || (dy > 0 && a.hi[1] <= 0)) continue;
+#pragma unroll
+        for (int cz = 0; cz < 2; ++cz) {
+          const int dz = tz - cz;
+          if (dz < -1 || dz > 1 || (dz < 0 && a.lo[2] >= 0) || (dz > 0 && a.hi[2] <= 0)) continue;
+          word |= dilate_y1(dilate_z1(refine_word(mx, cy, cz), dz, a.lo[2], a.hi[2]), dy, a.lo[1], a.hi[1]);
+        }
+      }
     }
     return word;
   } else {
@@ -418,18 +504,36 @@ __device__ __forceinline__ uint64_t merge_run(const PassArgs& a, const uint32_t*
       for (int k = 0; k < 8; ++k) c[k] |= ((x & 7) == k) ? bit : 0ull;
     } else {
     uint64_t m[8];
-    load_mask(a.src_masks, (long long)(val >> kSrcShift), m);
-    const uint32_t code = val & 31u;
+    load_mask(a.src_masks, (long long)(val >> a.code_bits), m);
+    const uint32_t code = val & ((1u << a.code_bits) - 1u);
     if (OP == kLeaves) {
 #pragma unroll
       for (int k = 0; k < 8; ++k) c[k] |= m[k];
     } else if (OP == kCoarsen) {
-      const int qx = (code >> 2) & 1, qy = (code >> 1) & 1, qz = code & 1;
-      uint64_t cw[4];
+      const int f = a.factor;
+      if (f == 2) {
+        const int qx = (code >> 2) & 1, qy = (code >> 1) & 1, qz = code & 1;
+        uint64_t cw[4];
 #pragma unroll
-      for (int X = 0; X < 4; ++X) cw[X] = coarsen_word(m[2 * X] | m[2 * X + 1], qy, qz);
+        for (int X = 0; X < 4; ++X) cw[X] = coarsen_word(m[2 * X] | m[2 * X + 1], qy, qz);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) c[k] |= ((k >> 2) == qx) ? cw[k & 3] : 0ull;
+        for (int k = 0; k < 8; ++k) c[k] |= ((k >> 2) == qx) ? cw[k & 3] : 0ull;
+      } else {
+        // coarse word k takes source words f (k - qx 8/f) .. + f - 1 when k
+        // lies in the source's share qx 8/f .. (qx + 1) 8/f - 1
+        const int sh = log2_factor(f), fm = f - 1, cs = 8 / f;
+        const int qx = (int)(code >> (2 * sh)), qy = (int)(code >> sh) & fm, qz = (int)code & fm;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const int X = k - qx * cs;
+          if (X < 0 || X >= cs) continue;
+          uint64_t t = 0;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            if (j / f == X) t |= m[j];
+          c[k] |= coarsen_word_f(t, qy, qz, f);
+        }
+      }
     } else {  // kDilate
       const int tx = (int)(code / 9) - 1, ty = (int)((code / 3) % 3) - 1, tz = (int)(code % 3) - 1;
       if (unit) {
@@ -827,8 +931,15 @@ __device__ void dispatch_emit(const PassArgs& a, Smem& sm, int vb, int vg) {
     case kLeaves: phase_emit<kLeaves>(a, sm, vb, vg); break;
     case kRefine: phase_emit<kRefine>(a, sm, vb, vg); break;
     case kCoarsen: phase_emit<kCoarsen>(a, sm, vb, vg); break;
+    case kRefineDilate: phase_emit<kRefineDilate>(a, sm, vb, vg); break;
     default: phase_emit<kDilate>(a, sm, vb, vg); break;
   }
+}
+
+// The fused refine-then-dilate leaves phase as a call of its own: inlined,
+// its register peak would push the whole kernel past 128 registers a thread.
+__device__ __noinline__ void leaves_refine_dilate(const PassArgs& a, Smem& sm, int vb, int vg) {
+  phase_leaves<kRefineDilate>(a, sm, vb, vg);
 }
 
 __device__ void dispatch_leaves(const PassArgs& a, Smem& sm, int vb, int vg) {
@@ -837,6 +948,7 @@ __device__ void dispatch_leaves(const PassArgs& a, Smem& sm, int vb, int vg) {
     case kLeaves: phase_leaves<kLeaves>(a, sm, vb, vg); break;
     case kRefine: phase_leaves<kRefine>(a, sm, vb, vg); break;
     case kCoarsen: phase_leaves<kCoarsen>(a, sm, vb, vg); break;
+    case kRefineDilate: leaves_refine_dilate(a, sm, vb, vg); break;
     default: phase_leaves<kDilate>(a, sm, vb, vg); break;
   }
 }
@@ -868,8 +980,8 @@ __device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, Pass
 
 // The phases of the chains of one stage are independent, so each phase splits
 // the grid's blocks over the chains that take part in it, in proportion to
-// their work (candidates, slots, or unique leaves plus slots), at least one
-// block each.
+// their work (candidates, slots, or unique leaves plus weighted slots), at
+// least one block each.
 // Every block computes the same split from the same counters, so no
 // coordination is needed; a chain's blocks then run its phase as a virtual
 // grid of `vg` blocks.  With more chains than blocks, every block runs every
@@ -881,6 +993,12 @@ struct Split {
   int serial;      // 1: more chains take part than there are blocks
   int maxP, more;  // emission split: most digit passes of the stage; some pass is intermediate
 };
+
+// Relative cost of merging one slot in the leaves phase: a leaf costs its
+// record (1) plus this per slot; the fused refine-then-dilate merge runs a
+// leaf's slots one after another in every lane, the others spread them over
+// the 8 lanes of a group or have one slot per leaf.
+__device__ __forceinline__ unsigned long long leaves_slot_cost(int op) { return op == kRefineDilate ? 3ull : 1ull; }
 
 constexpr unsigned long long kSplitOne = 1ull << 52;  // chain count unit in a packed (count, weight)
 constexpr unsigned long long kSplitWCap = 1ull << 40;  // weights above this are clamped
@@ -894,21 +1012,16 @@ __device__ __forceinline__ long long split_weight(const ChainArgs& c, int ch, in
   if (kind == kSplitEmit) {
     const unsigned long long* cd = p->src_count_dev;
     const unsigned long long n = cd ? __ldcg(cd) : (unsigned long long)__ldg(&p->src_count);
-    unsigned long long T = 1;
-    if (op == kRefine) {
-      T = 8;
-    } else if (op == kDilate) {
-      const int32_t lo[3] = {__ldg(&p->lo[0]), __ldg(&p->lo[1]), __ldg(&p->lo[2])};
-      const int32_t hi[3] = {__ldg(&p->hi[0]), __ldg(&p->hi[1]), __ldg(&p->hi[2])};
-      T = (unsigned long long)dilate_targets(lo, hi);
-    }
+    const int32_t lo[3] = {__ldg(&p->lo[0]), __ldg(&p->lo[1]), __ldg(&p->lo[2])};
+    const int32_t hi[3] = {__ldg(&p->hi[0]), __ldg(&p->hi[1]), __ldg(&p->hi[2])};
+    const unsigned long long T = (unsigned long long)pass_targets(op, __ldg(&p->factor), lo, hi);
     w = n < kSplitWCap ? n * T : kSplitWCap;
     atomicMax(&sp.maxP, __ldcg(&p->P));
     if (!__ldg(&p->last)) sp.more = 1;
-  } else if (kind == kSplitLeaves) {  // a leaf costs its record plus one merge step per slot
+  } else if (kind == kSplitLeaves) {
     const PassCtl* ctl = p->ctl;
     const ReadbackHeader* rb = p->rb;
-    w = __ldcg(&ctl->head_totals[0]) + __ldcg(&rb->num_slots);
+    w = __ldcg(&ctl->head_totals[0]) + leaves_slot_cost(op) * __ldcg(&rb->num_slots);
   } else {
     if (kind == kSplitSort && d >= __ldcg(&p->P)) return -1;
     const ReadbackHeader* rb = p->rb;
@@ -942,15 +1055,9 @@ __device__ void load_stage(const ChainArgs& c, int k, StageInfo* si) {
     e.ctl = p->ctl;
     e.src_count_dev = p->src_count_dev;
     e.src_count = __ldg(&p->src_count);
-    int T = 1;
-    if (e.op == kRefine) {
-      T = 8;
-    } else if (e.op == kDilate) {
-      const int32_t lo[3] = {__ldg(&p->lo[0]), __ldg(&p->lo[1]), __ldg(&p->lo[2])};
-      const int32_t hi[3] = {__ldg(&p->hi[0]), __ldg(&p->hi[1]), __ldg(&p->hi[2])};
-      T = dilate_targets(lo, hi);
-    }
-    e.T = T;
+    const int32_t lo[3] = {__ldg(&p->lo[0]), __ldg(&p->lo[1]), __ldg(&p->lo[2])};
+    const int32_t hi[3] = {__ldg(&p->hi[0]), __ldg(&p->hi[1]), __ldg(&p->hi[2])};
+    e.T = pass_targets(e.op, __ldg(&p->factor), lo, hi);
   }
   __syncthreads();
 }
@@ -974,7 +1081,7 @@ __device__ void split_warp(const ChainArgs& c, const StageInfo* si, int kind, in
         const unsigned long long ns = e.src_count_dev ? __ldcg(e.src_count_dev) : (unsigned long long)e.src_count;
         v = ns < kSplitWCap ? ns * (unsigned long long)e.T : kSplitWCap;
       } else if (kind == kSplitLeaves) {
-        v = __ldcg(&e.ctl->head_totals[0]) + __ldcg(&e.rb->num_slots);
+        v = __ldcg(&e.ctl->head_totals[0]) + leaves_slot_cost(e.op) * __ldcg(&e.rb->num_slots);
       } else {
         on = !(kind == kSplitSort && d >= e.P);
         if (on) v = __ldcg(&e.rb->num_slots);
@@ -1382,6 +1489,7 @@ int write_final_occupancy(int op) {
     case kLeaves: return write_occupancy<kLeaves>();
     case kRefine: return write_occupancy<kRefine>();
     case kCoarsen: return write_occupancy<kCoarsen>();
+    case kRefineDilate: return write_occupancy<kRefineDilate>();
     default: return write_occupancy<kDilate>();
   }
 }
@@ -1404,6 +1512,7 @@ cudaError_t launch_write_final(int op, const PassArgs& a, const WriteOut& o, int
     case kRefine: k_write_final<kRefine><<<blocks, kThreads, 0, s>>>(a, o); break;
     case kCoarsen: k_write_final<kCoarsen><<<blocks, kThreads, 0, s>>>(a, o); break;
     case kDilate: k_write_final<kDilate><<<blocks, kThreads, 0, s>>>(a, o); break;
+    case kRefineDilate: k_write_final<kRefineDilate><<<blocks, kThreads, 0, s>>>(a, o); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

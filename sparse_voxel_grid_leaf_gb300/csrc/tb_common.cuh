@@ -19,12 +19,17 @@
 namespace tb {
 
 // Pass kinds.  kIjk and kLeaves are the front ends (one slot per input voxel
-// or input leaf); the other three are the topology ops of a chain.
-enum PassOp : int32_t { kIjk = 0, kLeaves = 1, kRefine = 2, kCoarsen = 3, kDilate = 4 };
+// or input leaf); the others are the topology ops of a chain: refine and
+// coarsen by a factor 2, 4 or 8 in one pass, a box dilation, and refinement
+// by 2 followed by a box within [-1, 1]^3 (the k3s2 transpose) in one pass.
+enum PassOp : int32_t { kIjk = 0, kLeaves = 1, kRefine = 2, kCoarsen = 3, kDilate = 4, kRefineDilate = 5 };
+constexpr int kNumOps = 6;
 
 constexpr int kBins = 256;            // 8-bit radix digits
 constexpr int kMaxDigitPasses = 8;    // 64-bit key
-constexpr int kSrcShift = 5;          // slot value = source index << 5 | target code
+// slot value = source index << code_bits | target code; code_bits per pass
+// kind (pass_code_bits): 0 for the front ends, 3 log2(f) for refine and
+// coarsen by f, 5 for a box dilation, 6 for refine-then-dilate
 
 // Error bits reported through the readback header.
 constexpr uint32_t kErrTimeout = 1u;       // a bounded wait (look-back or grid barrier) gave up
@@ -109,6 +114,8 @@ struct PassArgs {
   int32_t last;           // 1: final pass (count phase), 0: intermediate (hands leaves on)
   int32_t tchunk;         // targets per emission thread (1 .. targets per source)
   int32_t lo[3], hi[3];   // box of a dilation pass
+  int32_t factor;         // refine / coarsen factor (2, 4, 8)
+  int32_t code_bits;      // width of the target code in a slot value
   // source
   const int32_t* ijk;            // kIjk: [N,3]
   const int64_t* in_offsets;     // kIjk / kLeaves without src_grid: [B+1]
@@ -283,15 +290,52 @@ __device__ __forceinline__ void load_mask(const uint64_t* masks, long long i, ui
 // parent word 4*cx + (w >> 1): parent rows 4*cy .. 4*cy+3, bits 4*cz .. 4*cz+3,
 // each parent bit doubled in z and each row doubled in y.
 __device__ __forceinline__ uint64_t refine_word(uint64_t parent_word, int cy, int cz) {
+  // every row's nibble 4 cz .. 4 cz + 3 at once, each bit doubled in its byte
+  uint64_t x = (parent_word >> (4 * cz)) & 0x0F0F0F0F0F0F0F0Full;
+  x = (x | (x << 2)) & 0x3333333333333333ull;
+  x = (x | (x << 1)) & 0x5555555555555555ull;
+  x |= x << 1;
+  // rows 4 cy .. 4 cy + 3, each doubled
+  uint64_t v = (x >> (32 * cy)) & 0xFFFFFFFFull;
+  v = (v | (v << 16)) & 0x0000FFFF0000FFFFull;
+  v = (v | (v << 8)) & 0x00FF00FF00FF00FFull;
+  return v | (v << 8);
+}
+
+// Refinement by f = 4 or 8: word w of child c = (cx, cy, cz) of a leaf comes
+// from parent word (8 cx + w) / f; child row y from parent row (8 cy + y) / f
+// and child bit z from parent bit (8 cz + z) / f.  parent_word is that word.
+__device__ __forceinline__ uint64_t refine_word_f(uint64_t parent_word, int cy, int cz, int f) {
+  const int bs = 8 / f;  // parent rows (and bits) per child along an axis
   uint64_t out = 0;
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    uint32_t x = (uint32_t)(parent_word >> (8 * (4 * cy + r) + 4 * cz)) & 0xFu;
-    x = (x | (x << 2)) & 0x33u;
-    x = (x | (x << 1)) & 0x55u;
-    x = x | (x << 1);
-    const uint64_t row = (uint64_t)x;
-    out |= (row | (row << 8)) << (16 * r);
+  for (int y = 0; y < 8; ++y) {
+    const uint32_t sb = (uint32_t)(parent_word >> (8 * (cy * bs + y / f))) & 0xFFu;
+    uint32_t tb = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (j < bs && ((sb >> (cz * bs + j)) & 1u)) tb |= ((1u << f) - 1u) << (j * f);
+    out |= (uint64_t)(tb & 0xFFu) << (8 * y);
+  }
+  return out;
+}
+
+// Coarsening by f = 4 or 8 of the rows and bits of t (the OR of the f source
+// words that fall into one coarse word): source row y goes to coarse row
+// qy * 8/f + y / f, bit z to coarse bit qz * 8/f + z / f, where (qy, qz) is
+// the source leaf's position inside the coarse leaf.
+__device__ __forceinline__ uint64_t coarsen_word_f(uint64_t t, int qy, int qz, int f) {
+  if (f == 8) return t ? 1ull << (8 * qy + qz) : 0ull;  // the whole source leaf is one coarse voxel
+  // f == 4: rows 0-3 and 4-7 fold into coarse rows 2 qy and 2 qy + 1; within
+  // a row, bits 0-3 and 4-7 into coarse bits 2 qz and 2 qz + 1
+  uint64_t r = t | (t >> 8);
+  r |= r >> 16;  // byte 0: OR of rows 0-3, byte 4: OR of rows 4-7
+  uint64_t out = 0;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const uint32_t b = (uint32_t)(r >> (32 * h)) & 0xFFu;
+    const uint32_t c = ((b & 0x0Fu) ? 1u : 0u) | ((b & 0xF0u) ? 2u : 0u);
+    out |= (uint64_t)c << (8 * (2 * qy + h) + 2 * qz);
   }
   return out;
 }

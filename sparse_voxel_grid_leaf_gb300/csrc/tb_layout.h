@@ -41,22 +41,53 @@ TB_HD inline int dilate_targets(const int32_t lo[3], const int32_t hi[3]) {
   return n;
 }
 
-// Exact voxel bbox after a pass of kind `op` (refine x2: [2lo, 2hi+1];
-// coarsen x2: floor halves; box dilation by [dlo, dhi]: [lo+dlo, hi+dhi]; the
-// front ends keep it).  Returns false if it leaves int32.
-TB_HD inline bool propagate_bbox(int op, const int32_t dlo[3], const int32_t dhi[3], const int32_t in[6],
+// Refine-then-dilate targets along one axis: fine leaf offsets (relative to
+// the first child) from -1 (if lo < 0) to 2 (if hi > 0), else 0 .. 1.
+TB_HD inline int refine_dilate_lo(int32_t lo) { return lo < 0 ? -1 : 0; }
+TB_HD inline int refine_dilate_hi(int32_t hi) { return hi > 0 ? 2 : 1; }
+
+TB_HD inline int log2_factor(int f) { return f == 8 ? 3 : (f == 4 ? 2 : 1); }
+
+// Candidate target leaves per source leaf (or voxel) of a pass.
+TB_HD inline int pass_targets(int op, int f, const int32_t lo[3], const int32_t hi[3]) {
+  if (op == kRefine) return f * f * f;
+  if (op == kDilate) return dilate_targets(lo, hi);
+  if (op == kRefineDilate) {
+    int n = 1;
+    for (int a = 0; a < 3; ++a) n *= refine_dilate_hi(hi[a]) - refine_dilate_lo(lo[a]) + 1;
+    return n;
+  }
+  return 1;
+}
+
+// Width of the target code in a slot value (see PassArgs::code_bits).
+TB_HD inline int pass_code_bits(int op, int f) {
+  if (op == kRefine || op == kCoarsen) return 3 * log2_factor(f);
+  if (op == kDilate) return 5;
+  if (op == kRefineDilate) return 6;
+  return 0;
+}
+
+// Exact voxel bbox after a pass (refine by f: [f lo, f hi + f - 1]; coarsen by
+// f: floor(lo / f), floor(hi / f); box dilation by [dlo, dhi]: [lo + dlo,
+// hi + dhi]; refine-then-dilate: both; the front ends keep it).  Returns
+// false if it leaves int32.
+TB_HD inline bool propagate_bbox(int op, int f, const int32_t dlo[3], const int32_t dhi[3], const int32_t in[6],
                                  int32_t out[6]) {
   for (int a = 0; a < 3; ++a) {
     int64_t lo = in[a], hi = in[3 + a];
     if (op == kRefine) {
-      lo = 2 * lo;
-      hi = 2 * hi + 1;
+      lo = (int64_t)f * lo;
+      hi = (int64_t)f * hi + f - 1;
     } else if (op == kCoarsen) {
-      lo = floor_div(lo, 2);
-      hi = floor_div(hi, 2);
+      lo = floor_div(lo, f);
+      hi = floor_div(hi, f);
     } else if (op == kDilate) {
       lo += dlo[a];
       hi += dhi[a];
+    } else if (op == kRefineDilate) {
+      lo = 2 * lo + dlo[a];
+      hi = 2 * hi + 1 + dhi[a];
     }
     if (lo < INT32_MIN || hi > INT32_MAX) return false;
     out[a] = (int32_t)lo;

@@ -85,7 +85,7 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
     return static_fail(TB_ERR_INVALID_ARG, "tb_refine_static: bad pointer or negative size");
   if (B == 0 && L != 0) return static_fail(TB_ERR_INVALID_ARG, "tb_refine_static: leaves without grids");
   if (((uintptr_t)masks & 15) != 0) return static_fail(TB_ERR_INVALID_ARG, "tb_refine_static: masks must be 16-byte aligned");
-  if (L >= (1ll << (32 - kSrcShift))) return static_fail(TB_ERR_TOO_LARGE, "tb_refine_static: too many input leaves");
+  if (L >= (1ll << (32 - pass_code_bits(kRefine, 2)))) return static_fail(TB_ERR_TOO_LARGE, "tb_refine_static: too many input leaves");
   int dev = 0;
   TB_STATIC_CUDA(cudaGetDevice(&dev));
   char* scratch = nullptr;
@@ -152,6 +152,8 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   TB_STATIC_CUDA(cudaMemsetAsync(scratch + zero_begin, 0, zero_end - zero_begin, stream));
 
   a.op = kRefine;
+  a.factor = 2;
+  a.code_bits = pass_code_bits(kRefine, 2);
   a.B = B;
   a.last = 1;
   a.tchunk = (int32_t)std::max(1ll, std::min(8ll, (8 * L + (long long)G * 256 - 1) / ((long long)G * 256)));

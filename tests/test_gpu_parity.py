@@ -372,3 +372,34 @@ def test_masked_refine_all_and_none():
     none = tb.refine_masked(b0, torch.zeros(V, dtype=torch.bool, device="cuda"))
     assert none.num_leaves == 0 and none.num_grids == 2
     none.validate()
+
+
+# ---------------------------------------------------------- fused chains
+
+FUSED = [
+    [("refine", 2), ("dilate", (-1, -1, -1), (1, 1, 1))],      # refine then k3s1: one fused pass
+    [("refine", 2), ("dilate", (-1, 0, 0), (0, 1, 1))],
+    [("refine", 2), ("dilate", (0, -1, 0), (1, 0, 0))],
+    [("refine", 2), ("refine", 2)],                            # refine x4 in one pass
+    [("refine", 2), ("refine", 4)],                            # refine x8
+    [("coarsen", 2), ("coarsen", 2), ("coarsen", 2)],          # coarsen x8
+    [("dilate", (-1,) * 3, (1,) * 3), ("dilate", (-1,) * 3, (0,) * 3)],  # boxes add up
+    [("refine", 2), PAD_N, ("coarsen", 4)],
+]
+
+
+@pytest.mark.parametrize("ops", FUSED)
+def test_fused_chains(ops):
+    ijk, off = synth.random_voxels(5, 220, 45, seed=61, origin=(-4105, 4090, -20), empty=(2,))
+    check(ijk, off, ops, "fused random %s" % (ops,))
+    ijk, off = synth.make("shells_b16_res64")
+    check(ijk, off, ops, "fused shells %s" % (ops,))
+
+
+def test_fused_chains_are_one_pass():
+    ijk, off = synth.make("pr1_b2_res32")
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    for ops in ([("refine", 2), PAD_N], [("coarsen", 4)], [("refine", 8)], [DIL, DIL]):
+        b = tb.chain(b0, ops)
+        # one pass: its source leaves are the input's
+        assert b.build_source_leaves == b0.num_leaves, ops
