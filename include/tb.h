@@ -199,6 +199,27 @@ TB_API tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const in
 TB_API tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask, int32_t factor,
                                   const tb_allocator* alloc, tb_stream stream, tb_batch** out);
 
+/* Kernel map of a sparse convolution from batch `in` to batch `out` (the
+ * ConvolutionPlan step after topology generation: issue #755 times the k3s1
+ * same-topology map and the k2s2 transpose map).  For every active voxel p of
+ * `out` (row j = p's index in the batch's voxel order, see tb_refine_masked)
+ * and every offset d of the box [lo, hi] (-7 <= lo <= hi <= 7 per axis;
+ * column k enumerates the offsets x-major: k = ((dx-lo0) ny + (dy-lo1)) nz +
+ * (dz-lo2)), map[j * K + k] is the index, in the voxel order of `in`, of the
+ * input voxel that p reads through d, or -1:
+ *   stride 1:                  p + d
+ *   stride 2, transposed == 0: 2 p + d      (e.g. conv_grid k2s2, box [0,1])
+ *   stride 2, transposed != 0: (p - d) / 2 where p - d is even on every axis
+ *                              (conv_transpose_grid k2s2: box [0,1]; k3s2:
+ *                              box [-1,1])
+ * looked up in the same grid of `in` (both batches have B grids).  K is the
+ * box volume; map is device memory of at least map_len >= V_out * K int32
+ * entries (V_out = the voxels of `out`), written in stream order, no host
+ * synchronization.  Errors: TB_ERR_INVALID_ARG for mismatched batches, bounds,
+ * stride, or a short map; TB_ERR_TOO_LARGE for 2^31 or more input voxels. */
+TB_API tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t lo[3], const int32_t hi[3],
+                               int32_t stride, int32_t transposed, int32_t* map, int64_t map_len, tb_stream stream);
+
 /* Chain of ops applied in order, intermediate results kept on the device
  * (PR #757 Summary items 1-2: multi-pass factors and the k3s2 transpose =
  * refine x2 then the {-1,0}^3 pad).  Consecutive ops are fused into one pass

@@ -202,6 +202,36 @@ def run_masked_refine(result: Dict[str, np.ndarray], voxel_mask: np.ndarray, fac
     return run_voxels(ijk[keep], new_offs, [("refine", factor)], lib)
 
 
+def run_kernel_map(in_result: Dict[str, np.ndarray], out_result: Dict[str, np.ndarray], lo, hi,
+                   stride: int = 1, transposed: bool = False) -> np.ndarray:
+    """Kernel map from its definition: for every voxel p of ``out_result`` (rows
+    in batch voxel order) and every offset d of the box [lo, hi] (columns
+    x-major), the batch voxel index in ``in_result`` of p + d (stride 1),
+    stride * p + d (forward) or (p - d) / stride when divisible (transposed),
+    within the same grid; -1 where there is no such voxel."""
+    vin, oin = batch_voxels(in_result)
+    vout, oout = batch_voxels(out_result)
+    offs = [(dx, dy, dz) for dx in range(lo[0], hi[0] + 1) for dy in range(lo[1], hi[1] + 1)
+            for dz in range(lo[2], hi[2] + 1)]
+    res = np.full((len(vout), len(offs)), -1, np.int32)
+    for g in range(len(oin) - 1):
+        where = {tuple(int(c) for c in vin[i]): i for i in range(oin[g], oin[g + 1])}
+        for j in range(oout[g], oout[g + 1]):
+            p = [int(c) for c in vout[j]]
+            for k, d in enumerate(offs):
+                if transposed:
+                    t = [p[a] - d[a] for a in range(3)]
+                    if any(x % stride for x in t):
+                        continue
+                    q = tuple(x // stride for x in t)
+                else:
+                    q = tuple(stride * p[a] + d[a] for a in range(3))
+                i = where.get(q)
+                if i is not None:
+                    res[j, k] = i
+    return res
+
+
 def member(result: Dict[str, np.ndarray], g: int) -> Dict[str, np.ndarray]:
     """The arrays of grid ``g`` alone, as if it had been run as a batch of one."""
     lo, hi = int(result["leaf_offsets"][g]), int(result["leaf_offsets"][g + 1])

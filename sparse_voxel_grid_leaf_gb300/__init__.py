@@ -89,6 +89,7 @@ def lib():
                 "tb_chain": [vp, vp, i32, vp, vp, pp],
                 "tb_multi": [vp, vp, vp, i32, vp, vp, pp],
                 "tb_refine_masked": [vp, vp, i32, vp, vp, pp],
+                "tb_kernel_map": [vp, vp, vp, vp, i32, i32, vp, i64, vp],
                 "tb_validate": [vp, vp],
                 "tb_batch_get_view": [vp, ctypes.POINTER(_View)],
                 "tb_batch_export": [vp, vp, vp, vp, vp, vp],
@@ -432,6 +433,28 @@ def conv_grid_k3s1(b: Batch, stream=None) -> Batch:
 def conv_transpose_grid_k3s2(b: Batch, stream=None) -> Batch:
     """conv_transpose_grid with kernel 3, stride 2: refine by 2, then the {-1,0}^3 pad."""
     return chain(b, [("refine", 2), ("dilate", (-1, -1, -1), (0, 0, 0))], stream)
+
+
+def kernel_map(b_in: Batch, b_out: Batch, lo=(-1, -1, -1), hi=(1, 1, 1), stride: int = 1,
+               transposed: bool = False, stream=None):
+    """Kernel map of a sparse convolution from ``b_in`` to ``b_out``: an int32
+    CUDA tensor ``[V_out, K]`` (K = box volume, offsets x-major) of input voxel
+    indices, -1 where the input voxel is absent.  Input voxel for output voxel
+    p and offset d: p + d (stride 1), 2 p + d (stride 2), or (p - d) / 2 when
+    even (stride 2, transposed)."""
+    import torch
+    K = 1
+    for a in range(3):
+        K *= int(hi[a]) - int(lo[a]) + 1
+    v = b_out._view()
+    V = int(np.asarray(b_out.to_numpy(["voxel_counts"])["voxel_counts"]).sum()) if v.num_grids else 0
+    out = torch.empty((V, K), dtype=torch.int32, device="cuda:%d" % v.device)
+    lo_a = (ctypes.c_int32 * 3)(*lo)
+    hi_a = (ctypes.c_int32 * 3)(*hi)
+    _check(lib().tb_kernel_map(b_in.handle, b_out.handle, lo_a, hi_a, int(stride), 1 if transposed else 0,
+                               ctypes.c_void_p(out.data_ptr() if out.numel() else 0), int(out.numel()),
+                               ctypes.c_void_p(_stream(stream))))
+    return out
 
 
 def stride1_box(kernel_size: int, transpose: bool = False) -> Tuple[Tuple[int, int, int], Tuple[int, int, int]]:

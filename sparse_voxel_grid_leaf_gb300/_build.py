@@ -13,7 +13,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libtb.so")
-SOURCES = ["tb_api.cu", "tb_prepass.cu", "tb_chain.cu", "tb_noalloc.cu"]
+SOURCES = ["tb_api.cu", "tb_prepass.cu", "tb_chain.cu", "tb_noalloc.cu", "tb_kmap.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr"]

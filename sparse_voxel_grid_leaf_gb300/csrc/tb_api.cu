@@ -68,11 +68,12 @@ thread_local long long t_launches = 0;
 // ---------------------------------------------------------------- kernel timing
 
 enum KernelKind {
-  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKNumKinds
+  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKNumKinds
 };
 const char* const kKernelNames[kKNumKinds] = {"prepass_ijk",   "prepass_leaves", "chain",         "write_ijk",
                                               "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
-                                              "write_refine_dilate", "validate", "write_multi",   "prune"};
+                                              "write_refine_dilate", "validate", "write_multi",   "prune",
+                                              "kernel_map"};
 
 struct ProfRec {
   int kind;
@@ -1030,6 +1031,67 @@ tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask, int32_
   src.B = in->B;
   src.count = in->L;
   return run(src, chains, alloc, s, out);
+}
+
+tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t lo[3], const int32_t hi[3],
+                        int32_t stride, int32_t transposed, int32_t* map, int64_t map_len, tb_stream stream) {
+  tb_status st = check_batch(in);
+  if (st != TB_OK) return st;
+  st = check_batch(out);
+  if (st != TB_OK) return st;
+  if (!lo || !hi) return fail(TB_ERR_INVALID_ARG, "tb_kernel_map: lo/hi NULL");
+  if (in->B != out->B) return fail(TB_ERR_INVALID_ARG, "tb_kernel_map: %d input grids, %d output grids", in->B, out->B);
+  if (stride != 1 && stride != 2) return fail(TB_ERR_INVALID_ARG, "tb_kernel_map: stride %d is not 1 or 2", stride);
+  long long K = 1;
+  for (int a = 0; a < 3; ++a) {
+    if (lo[a] < -7 || hi[a] > 7 || lo[a] > hi[a])
+      return fail(TB_ERR_INVALID_ARG, "tb_kernel_map: box bounds must satisfy -7 <= lo <= hi <= 7");
+    K *= hi[a] - lo[a] + 1;
+  }
+  if (in->voxel_base_host.size() != (size_t)in->B + 1 || out->voxel_base_host.size() != (size_t)out->B + 1)
+    return fail(TB_ERR_INVALID_ARG, "tb_kernel_map: batch without per-grid voxel counts");
+  const int64_t Vin = in->voxel_base_host[in->B], Vout = out->voxel_base_host[out->B];
+  if (Vin >= (1ll << 31)) return fail(TB_ERR_TOO_LARGE, "tb_kernel_map: 2^31 or more input voxels");
+  if (map_len < Vout * K)
+    return fail(TB_ERR_INVALID_ARG, "tb_kernel_map: map holds %lld entries, %lld needed", (long long)map_len,
+                (long long)(Vout * K));
+  if (Vout > 0 && !map) return fail(TB_ERR_INVALID_ARG, "tb_kernel_map: map is NULL");
+  if (out->L == 0) return TB_OK;
+  cudaStream_t s = (cudaStream_t)stream;
+  DeviceInfo* di = nullptr;
+  st = device_info(out->device, &di);
+  if (st != TB_OK) return st;
+  const Mem mem{out->has_alloc ? &out->alloc : nullptr, s};
+  const size_t nb = (size_t)(in->B + 1) * 8;
+  char* ws = (char*)mem.get(2 * nb);
+  if (!ws) return fail(TB_ERR_OOM, "tb_kernel_map: workspace");
+  Guard g{&mem, ws};
+  // pageable sources: staged before the calls return
+  TB_CUDA(cudaMemcpyAsync(ws, in->voxel_base_host.data(), nb, cudaMemcpyHostToDevice, s));
+  TB_CUDA(cudaMemcpyAsync(ws + nb, out->voxel_base_host.data(), nb, cudaMemcpyHostToDevice, s));
+  KmapArgs k;
+  k.in_origins = in->origins;
+  k.in_masks = in->masks;
+  k.in_wp = in->word_prefix;
+  k.in_voff = in->voxel_offset;
+  k.in_leaf_off = in->leaf_offsets;
+  k.in_vbase = (const int64_t*)ws;
+  k.out_origins = out->origins;
+  k.out_masks = out->masks;
+  k.out_voff = out->voxel_offset;
+  k.out_grid = out->leaf_grid;
+  k.out_vbase = (const int64_t*)(ws + nb);
+  k.L_out = out->L;
+  for (int a = 0; a < 3; ++a) {
+    k.lo[a] = lo[a];
+    k.hi[a] = hi[a];
+  }
+  k.stride = stride;
+  k.transposed = transposed ? 1 : 0;
+  k.map = map;
+  const int blocks = blocks_for(out->L, 8, (long long)di->sms * 8);
+  TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap(k, blocks, s); }));
+  return TB_OK;
 }
 
 tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, const tb_allocator* alloc, tb_stream stream,

@@ -25,6 +25,28 @@ cudaError_t launch_prepass_ijk(const int32_t* ijk, long long N, const int64_t* o
 cudaError_t launch_prepass_leaves(const int32_t* origins, const uint64_t* masks, long long L,
                                   const int64_t* off, int32_t B, ReadbackHeader* rb, int blocks,
                                   cudaStream_t s);
+// Kernel map between two batches (tb_kmap.cu).  Box offsets d enumerate
+// [lo, hi] x-major; stride 1 or 2, forward or transposed.
+constexpr int kKmapMaxCand = 128;  // candidate input leaves of one output leaf
+struct KmapArgs {
+  const int32_t* in_origins;
+  const uint64_t* in_masks;
+  const uint64_t* in_wp;
+  const int64_t* in_voff;
+  const int64_t* in_leaf_off;
+  const int64_t* in_vbase;   // [B+1] first voxel index of each input grid
+  const int32_t* out_origins;
+  const uint64_t* out_masks;
+  const int64_t* out_voff;
+  const int32_t* out_grid;
+  const int64_t* out_vbase;  // [B+1] first voxel index of each output grid
+  long long L_out;
+  int32_t lo[3], hi[3];
+  int32_t stride, transposed;
+  int32_t* map;              // [V_out, K]
+};
+cudaError_t launch_kmap(const KmapArgs& k, int blocks, cudaStream_t s);
+
 // Masked refinement: keeps the voxels of each leaf whose flag (one byte per
 // voxel, in the batch's voxel order) is non-zero.
 cudaError_t launch_prune(const uint64_t* masks, const int32_t* leaf_grid, const int64_t* voxel_offset,

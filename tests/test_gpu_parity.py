@@ -403,3 +403,53 @@ def test_fused_chains_are_one_pass():
         b = tb.chain(b0, ops)
         # one pass: its source leaves are the input's
         assert b.build_source_leaves == b0.num_leaves, ops
+
+
+# ---------------------------------------------------------- kernel maps
+
+KMAP_CASES = [
+    # (ops producing the output from the input, box lo, box hi, stride, transposed)
+    ([], (-1,) * 3, (1,) * 3, 1, False),                       # k3s1 same topology
+    ([("dilate", (-1,) * 3, (1,) * 3)], (-1,) * 3, (1,) * 3, 1, False),  # conv_grid k3s1
+    ([("refine", 2)], (0,) * 3, (1,) * 3, 2, True),            # conv_transpose_grid k2s2
+    ([("coarsen", 2)], (0,) * 3, (1,) * 3, 2, False),          # conv_grid k2s2
+    ([("refine", 2), PAD_N], (-1,) * 3, (1,) * 3, 2, True),     # k3s2 transpose
+    ([("coarsen", 2)], (-2, -1, 0), (3, 1, 2), 2, False),       # uneven box, forward stride 2
+    ([], (-7, 0, -2), (0, 7, 2), 1, False),                    # large box
+]
+
+
+@pytest.mark.parametrize("case", range(len(KMAP_CASES)))
+def test_kernel_map(case):
+    ops, lo, hi, stride, transposed = KMAP_CASES[case]
+    ijk, off = synth.random_voxels(4, 150, 26, seed=81, origin=(-4100, 4085, -13), empty=(2,))
+    b_in = tb.from_ijk(dev(ijk), dev(off))
+    b_out = tb.chain(b_in, ops) if ops else b_in
+    got = tb.kernel_map(b_in, b_out, lo, hi, stride, transposed).cpu().numpy()
+    exp = oracle.run_kernel_map(b_in.to_numpy(), b_out.to_numpy(), lo, hi, stride, transposed)
+    assert got.shape == exp.shape
+    assert np.array_equal(got, exp), "kernel map case %d: %d of %d entries differ" % (
+        case, int((got != exp).sum()), got.size)
+
+
+def test_kernel_map_shells_sampled_rows():
+    # full size: the B=16 shells, k3s1 same topology; rows sampled against the oracle's definition
+    ijk, off = synth.make("shells_b16_res64")
+    b = tb.from_ijk(dev(ijk), dev(off))
+    got = tb.kernel_map(b, b).cpu().numpy()
+    res = b.to_numpy()
+    vox, voffs = oracle.batch_voxels(res)
+    assert got.shape == (len(vox), 27)
+    assert (got[:, 13] == np.arange(len(vox))).all()
+    rng = np.random.default_rng(5)
+    for j in rng.choice(len(vox), 400, replace=False):
+        g = int(np.searchsorted(voffs, j, side="right") - 1)
+        where = {tuple(int(c) for c in vox[i]): i for i in range(voffs[g], voffs[g + 1])}
+        p = vox[j]
+        k = 0
+        for dx in (-1, 0, 1):
+            for dy in (-1, 0, 1):
+                for dz in (-1, 0, 1):
+                    q = (int(p[0]) + dx, int(p[1]) + dy, int(p[2]) + dz)
+                    assert got[j, k] == where.get(q, -1)
+                    k += 1

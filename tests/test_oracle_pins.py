@@ -362,3 +362,53 @@ def test_masked_refine_single_flag():
     first = min([(-8, 0, 1), (5, -3, 9)], key=lambda v: canon(v))  # canonical leaf order decides
     assert H.grid_voxels(got, 0) == {(2 * first[0] + a, 2 * first[1] + b, 2 * first[2] + c)
                                      for a in (0, 1) for b in (0, 1) for c in (0, 1)}
+
+
+# ------------------------------------------------------------------ kernel maps
+
+def _small():
+    ijk, off = synth.random_voxels(3, 90, 14, seed=71, origin=(-7, 4088, -4100), empty=(1,))
+    return oracle.run_voxels(ijk, off), ijk, off
+
+
+def test_kernel_map_same_topology_identity_and_symmetry():
+    res, _, _ = _small()
+    m = oracle.run_kernel_map(res, res, (-1,) * 3, (1,) * 3)
+    V = m.shape[0]
+    assert m.shape == (V, 27)
+    assert (m[:, 13] == np.arange(V)).all()          # d = 0 reads the voxel itself
+    for j in range(V):                                # p reads q through d  <=>  q reads p through -d
+        for k in range(27):
+            if m[j, k] >= 0:
+                assert m[m[j, k], 26 - k] == j
+
+
+def test_kernel_map_k2s2_transpose_one_parent():
+    res, ijk, off = _small()
+    fine = oracle.run_voxels(ijk, off, [("refine", 2)])
+    m = oracle.run_kernel_map(res, fine, (0,) * 3, (1,) * 3, stride=2, transposed=True)
+    vin, _ = oracle.batch_voxels(res)
+    vout, _ = oracle.batch_voxels(fine)
+    for j, p in enumerate(vout):
+        hits = np.nonzero(m[j] >= 0)[0]
+        assert len(hits) == 1                          # exactly one parent, through d = p mod 2
+        k = 4 * (p[0] & 1) + 2 * (p[1] & 1) + (p[2] & 1)
+        assert hits[0] == k
+        assert tuple(vin[m[j, k]]) == (p[0] >> 1, p[1] >> 1, p[2] >> 1)
+
+
+def test_kernel_map_k2s2_forward_partitions_the_input():
+    res, ijk, off = _small()
+    coarse = oracle.run_voxels(ijk, off, [("coarsen", 2)])
+    m = oracle.run_kernel_map(res, coarse, (0,) * 3, (1,) * 3, stride=2)
+    hit = m[m >= 0]
+    V = int(res["voxel_counts"].sum())
+    assert sorted(hit.tolist()) == list(range(V))     # every input voxel feeds exactly one coarse voxel
+
+
+def test_kernel_map_dilated_output_reads_each_input_27_times():
+    res, ijk, off = _small()
+    dil = oracle.run_voxels(ijk, off, [("dilate", (-1,) * 3, (1,) * 3)])
+    m = oracle.run_kernel_map(res, dil, (-1,) * 3, (1,) * 3)
+    counts = np.bincount(m[m >= 0], minlength=int(res["voxel_counts"].sum()))
+    assert (counts == 27).all()
