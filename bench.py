@@ -481,21 +481,34 @@ def run_ours(args):
 
 def per_op_tables(tb, torch, synth, stream, flush, main_workload):
     """ms per call (median of 20 CUDA-event iterations after 5 warm-ups, L2
-    flushed before each) for each single pass on three workloads."""
+    flushed before each) for each single call on three workloads: the pages'
+    conv-grid ops, the fused chains, masked refinement (half the voxels
+    flagged), a K=5 stride-1 topology, and two kernel maps (with the GB/s of
+    the map they write)."""
+    import numpy as np
     res = {}
     ops = [("refine2", [("refine", 2)]), ("coarsen2", [("coarsen", 2)]), ("dilate_k3s1", [DIL]),
-           ("pad_neg", [PAD_N]), ("k3s2", [("refine", 2), PAD_N])]
+           ("pad_neg", [PAD_N]), ("k3s2", [("refine", 2), PAD_N]), ("coarsen4", [("coarsen", 4)]),
+           ("conv_k5s1", [("dilate", (-2, -2, -2), (2, 2, 2))])]
     for wl in (main_workload, "shells_b48_res64", "stress_b64_res512"):
         ijk, off = synth.make(wl)
         ijk_d, off_d = torch.from_numpy(ijk).cuda(), torch.from_numpy(off).cuda()
         b0 = tb.from_ijk(ijk_d, off_d)
+        fine = tb.refine(b0)
+        V = int(b0.to_numpy(["voxel_counts"])["voxel_counts"].sum())
+        flags = torch.from_numpy((np.random.default_rng(0).random(V) < 0.5).astype(np.uint8)).cuda()
+        plan = tb.MultiPlan([o for _, o in ops[:5]])
         row = {}
         calls = [("from_ijk", lambda: tb.from_ijk(ijk_d, off_d))] + \
                 [(lab, (lambda o=o: tb.chain(b0, o))) for lab, o in ops] + \
-                [("multi_all", lambda: tb.multi(b0, [o for _, o in ops]))]
+                [("multi5", lambda: plan(b0)),
+                 ("refine_masked_half", lambda: tb.refine_masked(b0, flags)),
+                 ("kmap_k3s1", lambda: tb.kernel_map(b0, b0)),
+                 ("kmap_k2s2_transpose", lambda: tb.kernel_map(b0, fine, (0, 0, 0), (1, 1, 1), 2, True))]
         for lab, fn in calls:
             ts = []
             vox = 0
+            nbytes = 0
             for it in range(25):
                 flush.zero_()
                 s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -503,16 +516,24 @@ def per_op_tables(tb, torch, synth, stream, flush, main_workload):
                 r = fn()
                 e.record(stream)
                 e.synchronize()
-                rs = r if isinstance(r, list) else [r]
-                if it == 0:
-                    vox = sum(int(x.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for x in rs)
-                for x in rs:
-                    x.free()
+                if isinstance(r, torch.Tensor):
+                    nbytes = r.numel() * 4
+                    del r
+                else:
+                    rs = r if isinstance(r, list) else [r]
+                    if it == 0:
+                        vox = sum(int(x.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for x in rs)
+                    for x in rs:
+                        x.free()
                 if it >= 5:
                     ts.append(s.elapsed_time(e))
             med = statistics.median(ts)
-            row[lab] = {"ms": med, "out_voxels": vox, "Gvox_per_s": vox / med / 1e6}
+            if nbytes:
+                row[lab] = {"ms": med, "map_bytes": nbytes, "map_GBps": nbytes / med / 1e6}
+            else:
+                row[lab] = {"ms": med, "out_voxels": vox, "Gvox_per_s": vox / med / 1e6}
         res[wl] = row
+        fine.free()
         b0.free()
     return res
 

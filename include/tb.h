@@ -126,6 +126,7 @@ typedef struct tb_batch_view {
   int64_t build_source_leaves;       /* leaves (or voxels) the pass read          */
   int32_t build_key_bits;            /* width of the compressed sort key          */
   int32_t build_digit_passes;        /* 8-bit radix passes run                    */
+  int64_t num_voxels;                /* active voxels of the whole batch (host)   */
 } tb_batch_view;
 
 /* Per-kernel timing record (see tb_profile_enable). */

@@ -58,7 +58,8 @@ class _View(ctypes.Structure):
                    "leaf_grid", "leaf_parent", "voxel_counts", "grid_bbox", "node_counts",
                    "lower_offsets", "upper_offsets", "lower_origins", "lower_parent", "upper_origins")] + \
                [("build_slots", ctypes.c_int64), ("build_source_leaves", ctypes.c_int64),
-                ("build_key_bits", ctypes.c_int32), ("build_digit_passes", ctypes.c_int32)]
+                ("build_key_bits", ctypes.c_int32), ("build_digit_passes", ctypes.c_int32),
+                ("num_voxels", ctypes.c_int64)]
 
 
 class _KStat(ctypes.Structure):
@@ -217,6 +218,7 @@ class Batch:
     build_source_leaves = property(lambda self: int(self._view().build_source_leaves))
     build_key_bits = property(lambda self: int(self._view().build_key_bits))
     build_digit_passes = property(lambda self: int(self._view().build_digit_passes))
+    num_voxels = property(lambda self: int(self._view().num_voxels))
 
     @property
     def leaf_offsets_host(self) -> np.ndarray:
@@ -447,8 +449,7 @@ def kernel_map(b_in: Batch, b_out: Batch, lo=(-1, -1, -1), hi=(1, 1, 1), stride:
     for a in range(3):
         K *= int(hi[a]) - int(lo[a]) + 1
     v = b_out._view()
-    V = int(np.asarray(b_out.to_numpy(["voxel_counts"])["voxel_counts"]).sum()) if v.num_grids else 0
-    out = torch.empty((V, K), dtype=torch.int32, device="cuda:%d" % v.device)
+    out = torch.empty((int(v.num_voxels), K), dtype=torch.int32, device="cuda:%d" % v.device)
     lo_a = (ctypes.c_int32 * 3)(*lo)
     hi_a = (ctypes.c_int32 * 3)(*hi)
     _check(lib().tb_kernel_map(b_in.handle, b_out.handle, lo_a, hi_a, int(stride), 1 if transposed else 0,

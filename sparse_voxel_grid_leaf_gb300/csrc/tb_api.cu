@@ -1175,6 +1175,7 @@ tb_status tb_batch_get_view(const tb_batch* b, tb_batch_view* v) {
   v->build_source_leaves = b->build_sources;
   v->build_key_bits = b->build_key_bits;
   v->build_digit_passes = b->build_digit_passes;
+  v->num_voxels = b->voxel_base_host.empty() ? 0 : b->voxel_base_host.back();
   return TB_OK;
 }
 

@@ -60,38 +60,45 @@ __device__ long long find_leaf(const int32_t* origins, long long b, long long e,
   return -1;
 }
 
-__device__ __forceinline__ long long floor_div_d(long long a, long long b) {
-  const long long q = a / b;
-  return (a % b != 0 && ((a < 0) != (b < 0))) ? q - 1 : q;
-}
+// Box offsets d of column k, x-major, packed as three bytes (d + 8); kept in
+// shared memory for boxes of up to kKmapTab offsets.
+constexpr int kKmapTab = 1024;
 
 __global__ void __launch_bounds__(kKmapThreads) k_kmap(const KmapArgs k) {
   __shared__ int32_t cand[kKmapWarps][kKmapMaxCand];
   __shared__ uint16_t vox[kKmapWarps][512];
+  __shared__ uint32_t dtab[kKmapTab];
   const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const long long nwarps = (long long)gridDim.x * kKmapWarps;
-  const int nb0 = k.hi[0] - k.lo[0] + 1, nb1 = k.hi[1] - k.lo[1] + 1, nb2 = k.hi[2] - k.lo[2] + 1;
-  const int K = nb0 * nb1 * nb2, s = k.stride;
+  const int nb1 = k.hi[1] - k.lo[1] + 1, nb2 = k.hi[2] - k.lo[2] + 1;
+  const int K = (k.hi[0] - k.lo[0] + 1) * nb1 * nb2;
+  const int sh = k.stride == 2 ? 1 : 0;  // strides 1 and 2
+  const bool tab = K <= kKmapTab;
+  for (int i = threadIdx.x; i < K && tab; i += kKmapThreads)
+    dtab[i] = (uint32_t)(k.lo[0] + i / (nb1 * nb2) + 8) | ((uint32_t)(k.lo[1] + (i / nb2) % nb1 + 8) << 8) |
+              ((uint32_t)(k.lo[2] + i % nb2 + 8) << 16);
+  __syncthreads();
   for (long long u = (long long)blockIdx.x * kKmapWarps + wib; u < k.L_out; u += nwarps) {
     const int32_t g = __ldg(k.out_grid + u);
     const long long o[3] = {__ldg(k.out_origins + 3 * u), __ldg(k.out_origins + 3 * u + 1),
                             __ldg(k.out_origins + 3 * u + 2)};
-    // input leaf coordinate range per axis
-    long long a[3], n[3];
+    // input leaf coordinate range per axis (coordinates >> 3 is a floor)
+    long long a[3];
+    int n[3];
 #pragma unroll
     for (int ax = 0; ax < 3; ++ax) {
       long long qlo, qhi;
       if (k.transposed) {
-        qlo = -floor_div_d(-(o[ax] - k.hi[ax]), s);  // ceil((p_min - hi) / s)
-        qhi = floor_div_d(o[ax] + 7 - k.lo[ax], s);
+        qlo = (o[ax] - k.hi[ax] + (1 << sh) - 1) >> sh;  // ceil((p_min - hi) / s)
+        qhi = (o[ax] + 7 - k.lo[ax]) >> sh;
       } else {
-        qlo = (long long)s * o[ax] + k.lo[ax];
-        qhi = (long long)s * (o[ax] + 7) + k.hi[ax];
+        qlo = (o[ax] << sh) + k.lo[ax];
+        qhi = ((o[ax] + 7) << sh) + k.hi[ax];
       }
-      a[ax] = floor_div_d(qlo, 8);
-      n[ax] = floor_div_d(qhi, 8) - a[ax] + 1;
+      a[ax] = qlo >> 3;
+      n[ax] = (int)((qhi >> 3) - a[ax] + 1);
     }
-    const int C = (int)(n[0] * n[1] * n[2]);  // <= kKmapMaxCand, checked by the host's bounds
+    const int C = n[0] * n[1] * n[2];  // <= kKmapMaxCand, checked by the host's bounds
     const long long ib = __ldg(k.in_leaf_off + g), ie = __ldg(k.in_leaf_off + g + 1);
     for (int c = lane; c < C; c += 32) {
       const long long lx = a[0] + c / (n[1] * n[2]), ly = a[1] + (c / n[2]) % n[1], lz = a[2] + c % n[2];
@@ -115,35 +122,47 @@ __global__ void __launch_bounds__(kKmapThreads) k_kmap(const KmapArgs k) {
       vox[wib][pos++] = (uint16_t)(16 * lane + b);
     }
     __syncwarp();
-    // the leaf's entries: map rows j0 .. j0 + nvox - 1, K entries each
+    // the leaf's entries: map rows j0 .. j0 + nvox - 1, K entries each; lane
+    // entry e = lane + 32 i walks (row r, column kk) without dividing
     const long long j0 = __ldg(k.out_vbase + g) + __ldg(k.out_voff + u);
     const long long E = (long long)nvox * K;
     const long long vin = __ldg(k.in_vbase + g);
     int32_t* row = k.map + j0 * K;
+    int r = lane / K, kk = lane % K;
+    const int step_r = 32 / K, step_k = 32 % K;
     for (long long e = lane; e < E; e += 32) {
-      const int r = (int)(e / K), kk = (int)(e % K);
       const int nbit = vox[wib][r];
-      const long long p[3] = {o[0] + (nbit >> 6), o[1] + ((nbit >> 3) & 7), o[2] + (nbit & 7)};
-      const int d[3] = {k.lo[0] + kk / (nb1 * nb2), k.lo[1] + (kk / nb2) % nb1, k.lo[2] + kk % nb2};
-      long long q[3];
+      int d0, d1, d2;
+      if (tab) {
+        const uint32_t dp = dtab[kk];
+        d0 = (int)(dp & 0xFFu) - 8;
+        d1 = (int)((dp >> 8) & 0xFFu) - 8;
+        d2 = (int)((dp >> 16) & 0xFFu) - 8;
+      } else {
+        d0 = k.lo[0] + kk / (nb1 * nb2);
+        d1 = k.lo[1] + (kk / nb2) % nb1;
+        d2 = k.lo[2] + kk % nb2;
+      }
+      const long long p0 = o[0] + (nbit >> 6), p1 = o[1] + ((nbit >> 3) & 7), p2 = o[2] + (nbit & 7);
+      long long q0, q1, q2;
       bool ok = true;
-#pragma unroll
-      for (int ax = 0; ax < 3; ++ax) {
-        if (k.transposed) {
-          const long long t = p[ax] - d[ax];
-          ok = ok && (t % s == 0);
-          q[ax] = floor_div_d(t, s);
-        } else {
-          q[ax] = (long long)s * p[ax] + d[ax];
-        }
+      if (k.transposed) {
+        const long long t0 = p0 - d0, t1 = p1 - d1, t2 = p2 - d2;
+        ok = ((t0 | t1 | t2) & ((1 << sh) - 1)) == 0;
+        q0 = t0 >> sh;
+        q1 = t1 >> sh;
+        q2 = t2 >> sh;
+      } else {
+        q0 = (p0 << sh) + d0;
+        q1 = (p1 << sh) + d1;
+        q2 = (p2 << sh) + d2;
       }
       int32_t idx = -1;
       if (ok) {
-        const long long c = ((floor_div_d(q[0], 8) - a[0]) * n[1] + (floor_div_d(q[1], 8) - a[1])) * n[2] +
-                            (floor_div_d(q[2], 8) - a[2]);
+        const int c = ((int)((q0 >> 3) - a[0]) * n[1] + (int)((q1 >> 3) - a[1])) * n[2] + (int)((q2 >> 3) - a[2]);
         const int32_t ci = cand[wib][c];
         if (ci >= 0) {
-          const int wx = (int)(q[0] & 7), by = (int)(8 * (q[1] & 7) + (q[2] & 7));
+          const int wx = (int)(q0 & 7), by = (int)(8 * (q1 & 7) + (q2 & 7));
           const uint64_t w = __ldg(k.in_masks + 8 * (long long)ci + wx);
           if ((w >> by) & 1ull) {
             const uint64_t wp = __ldg(k.in_wp + ci);
@@ -153,6 +172,12 @@ __global__ void __launch_bounds__(kKmapThreads) k_kmap(const KmapArgs k) {
         }
       }
       row[e] = idx;
+      r += step_r;
+      kk += step_k;
+      if (kk >= K) {
+        kk -= K;
+        ++r;
+      }
     }
     __syncwarp();
   }

@@ -440,6 +440,7 @@ def test_kernel_map_shells_sampled_rows():
     res = b.to_numpy()
     vox, voffs = oracle.batch_voxels(res)
     assert got.shape == (len(vox), 27)
+    assert b.num_voxels == len(vox) == int(res["voxel_counts"].sum())
     assert (got[:, 13] == np.arange(len(vox))).all()
     rng = np.random.default_rng(5)
     for j in rng.choice(len(vox), 400, replace=False):
