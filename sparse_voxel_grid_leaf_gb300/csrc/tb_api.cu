@@ -68,12 +68,12 @@ thread_local long long t_launches = 0;
 // ---------------------------------------------------------------- kernel timing
 
 enum KernelKind {
-  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKNumKinds
+  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKLeafTable, kKNumKinds
 };
 const char* const kKernelNames[kKNumKinds] = {"prepass_ijk",   "prepass_leaves", "chain",         "write_ijk",
                                               "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
                                               "write_refine_dilate", "validate", "write_multi",   "prune",
-                                              "kernel_map"};
+                                              "kernel_map",    "leaf_table"};
 
 struct ProfRec {
   int kind;
@@ -1062,19 +1062,33 @@ tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t l
   st = device_info(out->device, &di);
   if (st != TB_OK) return st;
   const Mem mem{out->has_alloc ? &out->alloc : nullptr, s};
+  // workspace: the two voxel-base arrays, then a hash table of the input
+  // leaves with at least twice as many slots as leaves
   const size_t nb = (size_t)(in->B + 1) * 8;
-  char* ws = (char*)mem.get(2 * nb);
+  unsigned long long cap = 64;
+  while (cap < 2ull * (unsigned long long)in->L) cap <<= 1;
+  char* ws = (char*)mem.get(2 * nb + cap * 4);
   if (!ws) return fail(TB_ERR_OOM, "tb_kernel_map: workspace");
   Guard g{&mem, ws};
+  int32_t* table = (int32_t*)(ws + 2 * nb);
   // pageable sources: staged before the calls return
   TB_CUDA(cudaMemcpyAsync(ws, in->voxel_base_host.data(), nb, cudaMemcpyHostToDevice, s));
   TB_CUDA(cudaMemcpyAsync(ws + nb, out->voxel_base_host.data(), nb, cudaMemcpyHostToDevice, s));
+  TB_CUDA(cudaMemsetAsync(table, 0xFF, cap * 4, s));
+  if (in->L) {
+    const int tb_blocks = blocks_for(in->L, 256, (long long)di->sms * 8);
+    TB_CUDA(launch(kKLeafTable, s, [&] {
+      return launch_leaf_table(in->origins, in->leaf_grid, in->L, table, cap - 1, tb_blocks, s);
+    }));
+  }
   KmapArgs k;
   k.in_origins = in->origins;
   k.in_masks = in->masks;
   k.in_wp = in->word_prefix;
   k.in_voff = in->voxel_offset;
-  k.in_leaf_off = in->leaf_offsets;
+  k.in_grid = in->leaf_grid;
+  k.table = table;
+  k.table_mask = cap - 1;
   k.in_vbase = (const int64_t*)ws;
   k.out_origins = out->origins;
   k.out_masks = out->masks;

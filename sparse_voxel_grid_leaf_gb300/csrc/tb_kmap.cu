@@ -10,10 +10,10 @@
 //   stride s, transposed: input voxel (p - d) / s where p - d divides by s
 //
 // Voxel indices follow the batch's voxel order (grid by grid, leaf by leaf,
-// ascending bit index), the order of every other per-voxel array.  One warp
-// per output leaf: its candidate input leaves (the few leaves any of its
-// voxels can reach) are found by binary search in the input grid's canonical
-// leaf list and kept in shared memory; the leaf's active voxels are listed in
+// ascending bit index), the order of every other per-voxel array.  A hash
+// table of the input leaves is built first; then one warp per output leaf:
+// its candidate input leaves (the few leaves any of its voxels can reach) are
+// looked up and kept in shared memory; the leaf's active voxels are listed in
 // shared memory; then the warp writes the leaf's voxels x K entries, which
 // are contiguous in the map.
 #include "tb_common.cuh"
@@ -26,36 +26,41 @@ namespace {
 constexpr int kKmapThreads = 256;
 constexpr int kKmapWarps = kKmapThreads / 32;
 
-// Canonical order of leaf coordinates (origin >> 3): signed root tile
-// (coordinate >> 9) x, y, z, then the upper child (>> 4 & 31) and the lower
-// child (& 15), x-major; as a 128-bit (hi, lo) pair.
-__device__ __forceinline__ void leaf_order_key(long long lx, long long ly, long long lz, unsigned long long& hi,
-                                               unsigned long long& lo) {
-  const unsigned long long bias = 1ull << 20;
-  hi = ((unsigned long long)((lx >> 9) + bias) << 42) | ((unsigned long long)((ly >> 9) + bias) << 21) |
-       (unsigned long long)((lz >> 9) + bias);
-  lo = ((unsigned long long)((lx >> 4) & 31) << 22) | ((unsigned long long)((ly >> 4) & 31) << 17) |
-       ((unsigned long long)((lz >> 4) & 31) << 12) | ((unsigned long long)(lx & 15) << 8) |
-       ((unsigned long long)(ly & 15) << 4) | (unsigned long long)(lz & 15);
+// Hash table of the input leaves: open addressing with linear probing over a
+// power-of-two array of leaf indices (-1: empty), keyed by (grid, leaf
+// coordinates); a probe checks the stored leaf's grid and origin.
+__device__ __forceinline__ unsigned long long leaf_hash(int32_t g, long long lx, long long ly, long long lz) {
+  unsigned long long h = (unsigned long long)(uint32_t)g * 0x9E3779B97F4A7C15ull;
+  h ^= (unsigned long long)(uint32_t)lx * 0xC2B2AE3D27D4EB4Full;
+  h ^= (unsigned long long)(uint32_t)ly * 0x165667B19E3779F9ull;
+  h ^= (unsigned long long)(uint32_t)lz * 0xD6E8FEB86659FD93ull;
+  h ^= h >> 29;
+  h *= 0xBF58476D1CE4E5B9ull;
+  return h ^ (h >> 32);
 }
 
-// Index of the leaf with coordinates (lx, ly, lz) among leaves [b, e) of a
-// canonically ordered list, or -1.
-__device__ long long find_leaf(const int32_t* origins, long long b, long long e, long long lx, long long ly,
-                               long long lz) {
-  unsigned long long kh, kl;
-  leaf_order_key(lx, ly, lz, kh, kl);
-  while (b < e) {
-    const long long m = b + (e - b) / 2;
-    unsigned long long mh, ml;
-    leaf_order_key(__ldg(origins + 3 * m) >> 3, __ldg(origins + 3 * m + 1) >> 3, __ldg(origins + 3 * m + 2) >> 3, mh,
-                   ml);
-    if (mh == kh && ml == kl) return m;
-    if (mh < kh || (mh == kh && ml < kl)) {
-      b = m + 1;
-    } else {
-      e = m;
-    }
+// The host sizes the table to at least twice the leaves, so every insert
+// finds an empty slot within the bounded probe loop.
+__global__ void __launch_bounds__(256) k_leaf_table(const int32_t* origins, const int32_t* leaf_grid, long long L,
+                                                    int32_t* table, unsigned long long mask) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < L; i += stride) {
+    unsigned long long h = leaf_hash(leaf_grid[i], origins[3 * i] >> 3, origins[3 * i + 1] >> 3, origins[3 * i + 2] >> 3);
+    for (unsigned long long probe = 0; probe <= mask; ++probe, ++h)  // at most the table's size
+      if (atomicCAS(table + (h & mask), -1, (int32_t)i) == -1) break;
+  }
+}
+
+// Index of the input leaf of grid g at leaf coordinates (lx, ly, lz), or -1.
+__device__ __forceinline__ int32_t find_leaf(const KmapArgs& k, int32_t g, long long lx, long long ly, long long lz) {
+  unsigned long long h = leaf_hash(g, lx, ly, lz);
+  for (unsigned long long probe = 0; probe <= k.table_mask; ++probe, ++h) {
+    const int32_t e = __ldg(k.table + (h & k.table_mask));
+    if (e < 0) return -1;
+    if (__ldg(k.in_grid + e) == g && __ldg(k.in_origins + 3 * (long long)e) == (int32_t)(lx * 8) &&
+        __ldg(k.in_origins + 3 * (long long)e + 1) == (int32_t)(ly * 8) &&
+        __ldg(k.in_origins + 3 * (long long)e + 2) == (int32_t)(lz * 8))
+      return e;
   }
   return -1;
 }
@@ -64,7 +69,7 @@ __device__ long long find_leaf(const int32_t* origins, long long b, long long e,
 // shared memory for boxes of up to kKmapTab offsets.
 constexpr int kKmapTab = 1024;
 
-__global__ void __launch_bounds__(kKmapThreads) k_kmap(const KmapArgs k) {
+__global__ void __launch_bounds__(kKmapThreads, 4) k_kmap(const KmapArgs k) {
   __shared__ int32_t cand[kKmapWarps][kKmapMaxCand];
   __shared__ uint16_t vox[kKmapWarps][512];
   __shared__ uint32_t dtab[kKmapTab];
@@ -99,10 +104,9 @@ __global__ void __launch_bounds__(kKmapThreads) k_kmap(const KmapArgs k) {
       n[ax] = (int)((qhi >> 3) - a[ax] + 1);
     }
     const int C = n[0] * n[1] * n[2];  // <= kKmapMaxCand, checked by the host's bounds
-    const long long ib = __ldg(k.in_leaf_off + g), ie = __ldg(k.in_leaf_off + g + 1);
     for (int c = lane; c < C; c += 32) {
       const long long lx = a[0] + c / (n[1] * n[2]), ly = a[1] + (c / n[2]) % n[1], lz = a[2] + c % n[2];
-      cand[wib][c] = (int32_t)find_leaf(k.in_origins, ib, ie, lx, ly, lz);
+      cand[wib][c] = find_leaf(k, g, lx, ly, lz);
     }
     // the output leaf's active voxels in order: lane l lists bits 16 l .. 16 l + 15
     // (mask word l / 4, quarter l % 4)
@@ -122,8 +126,9 @@ __global__ void __launch_bounds__(kKmapThreads) k_kmap(const KmapArgs k) {
       vox[wib][pos++] = (uint16_t)(16 * lane + b);
     }
     __syncwarp();
-    // the leaf's entries: map rows j0 .. j0 + nvox - 1, K entries each; lane
-    // entry e = lane + 32 i walks (row r, column kk) without dividing
+    // the leaf's entries: map rows j0 .. j0 + nvox - 1, K entries each,
+    // contiguous in the map; lane entry e = lane + 32 i walks (row r, column
+    // kk) without dividing, and the column's offset comes from a shared table
     const long long j0 = __ldg(k.out_vbase + g) + __ldg(k.out_voff + u);
     const long long E = (long long)nvox * K;
     const long long vin = __ldg(k.in_vbase + g);
@@ -184,6 +189,12 @@ __global__ void __launch_bounds__(kKmapThreads) k_kmap(const KmapArgs k) {
 }
 
 }  // namespace
+
+cudaError_t launch_leaf_table(const int32_t* origins, const int32_t* leaf_grid, long long L, int32_t* table,
+                              unsigned long long mask, int blocks, cudaStream_t s) {
+  k_leaf_table<<<blocks, 256, 0, s>>>(origins, leaf_grid, L, table, mask);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_kmap(const KmapArgs& k, int blocks, cudaStream_t s) {
   k_kmap<<<blocks, kKmapThreads, 0, s>>>(k);

@@ -33,7 +33,9 @@ struct KmapArgs {
   const uint64_t* in_masks;
   const uint64_t* in_wp;
   const int64_t* in_voff;
-  const int64_t* in_leaf_off;
+  const int32_t* in_grid;    // [L_in] grid of each input leaf
+  const int32_t* table;      // hash table of the input leaves (leaf index or -1)
+  unsigned long long table_mask;  // table size - 1 (a power of two minus one)
   const int64_t* in_vbase;   // [B+1] first voxel index of each input grid
   const int32_t* out_origins;
   const uint64_t* out_masks;
@@ -45,6 +47,8 @@ struct KmapArgs {
   int32_t stride, transposed;
   int32_t* map;              // [V_out, K]
 };
+cudaError_t launch_leaf_table(const int32_t* origins, const int32_t* leaf_grid, long long L, int32_t* table,
+                              unsigned long long mask, int blocks, cudaStream_t s);
 cudaError_t launch_kmap(const KmapArgs& k, int blocks, cudaStream_t s);
 
 // Masked refinement: keeps the voxels of each leaf whose flag (one byte per
