@@ -399,9 +399,9 @@ def run_ours(args):
         s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s.record(stream)
         outs = run_step(tb, None, (ijk_h, off_h))
-        for k, b in outs.items():
-            o, m, vo, lo = host_out[k]
-            tb.export_host(b, o, m, vo, lo)
+        keys = list(outs)
+        tb.export_many([outs[k] for k in keys], [host_out[k][0] for k in keys], [host_out[k][1] for k in keys],
+                       [host_out[k][2] for k in keys], [host_out[k][3] for k in keys])
         e.record(stream)
         e.synchronize()
         free_all(outs)

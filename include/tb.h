@@ -260,6 +260,18 @@ TB_API tb_status tb_batch_get_view(const tb_batch* batch, tb_batch_view* view);
 TB_API tb_status tb_batch_export(const tb_batch* batch, int32_t* origins, uint64_t* masks,
                           int64_t* voxel_offset, int64_t* leaf_offsets, tb_stream stream);
 
+/* The same for n batches at once: origins[i], masks[i], voxel_offset[i],
+ * leaf_offsets[i] receive batch i's arrays (each of the four lists, and each
+ * entry, may be NULL to skip).  Destinations the device can write -- device
+ * memory, or pinned host memory through its mapped address -- are filled by
+ * one copy kernel for all arrays (up to 64 per launch); others by plain
+ * copies.  Enqueued on `stream`; the caller synchronizes before reading host
+ * buffers. */
+TB_API tb_status tb_batch_export_many(const tb_batch* const* batches, int32_t n, int32_t* const* origins,
+                                      uint64_t* const* masks, int64_t* const* voxel_offset,
+                                      int64_t* const* leaf_offsets, tb_stream stream);
+
+
 /* Releases the batch's memory (stream-ordered on `stream`).  NULL is a no-op. */
 TB_API tb_status tb_batch_free(tb_batch* batch, tb_stream stream);
 
@@ -321,6 +333,14 @@ typedef struct tb_out_buffers {
 TB_API tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const int64_t* leaf_offsets,
                                   int32_t num_grids, int64_t num_leaves, const tb_out_buffers* out,
                                   int64_t* out_counts, tb_stream stream);
+
+/* Self-test of failure detection without a GPU fault: one thread waits, with
+ * the same bounded spin as the pass kernel's grid barrier, for a device flag
+ * that is preset (set_flag != 0) or that nothing ever sets; after spin_limit
+ * polls (>= 1; about 100 ns each past the first 256) the wait gives up.
+ * Returns TB_OK when the flag was seen, TB_ERR_DEVICE_TIMEOUT when the wait
+ * ran out; either way the context stays usable.  Blocks once. */
+TB_API tb_status tb_selftest_wait(int32_t set_flag, int32_t spin_limit, tb_stream stream);
 
 /* Kernel timing for profiling (library extension, no counterpart on the
  * pages).  With `on` >= 1 on the calling thread, every kernel the library

@@ -91,6 +91,8 @@ def lib():
                 "tb_multi": [vp, vp, vp, i32, vp, vp, pp],
                 "tb_refine_masked": [vp, vp, i32, vp, vp, pp],
                 "tb_kernel_map": [vp, vp, vp, vp, i32, i32, vp, i64, vp],
+                "tb_selftest_wait": [i32, i32, vp],
+                "tb_batch_export_many": [vp, i32, vp, vp, vp, vp, vp],
                 "tb_validate": [vp, vp],
                 "tb_batch_get_view": [vp, ctypes.POINTER(_View)],
                 "tb_batch_export": [vp, vp, vp, vp, vp, vp],
@@ -134,6 +136,12 @@ def _stream(stream=None) -> int:
         else:
             _RAW_STREAM = lambda: torch.cuda.current_stream().cuda_stream
     return int(_RAW_STREAM())
+
+
+def selftest_wait(set_flag: bool, spin_limit: int = 1 << 16, stream=None):
+    """Failure-detection self-test: a bounded device wait on a flag that is
+    preset or never set; raises TBError(TB_ERR_DEVICE_TIMEOUT) when it ran out."""
+    _check(lib().tb_selftest_wait(1 if set_flag else 0, int(spin_limit), ctypes.c_void_p(_stream(stream))))
 
 
 def kernel_launch_count() -> int:
@@ -499,3 +507,26 @@ def export_host(b: Batch, origins: np.ndarray, masks: np.ndarray, voxel_offset: 
         return None if x is None else ctypes.c_void_p(_ptr(x)[0])
     _check(lib().tb_batch_export(b.handle, p(origins), p(masks), p(voxel_offset), p(leaf_offsets),
                                  ctypes.c_void_p(_stream(stream))))
+
+
+def export_many(batches: Sequence[Batch], origins=None, masks=None, voxel_offset=None, leaf_offsets=None,
+                stream=None):
+    """Enqueues the copies of several batches' leaf records (one list entry per
+    batch; a list, or an entry, may be None to skip) -- one copy kernel for
+    all destinations the device can write (device or pinned host memory)."""
+    n = len(batches)
+    keep = []
+
+    def plist(xs):
+        if xs is None:
+            return None
+        arr = (ctypes.c_void_p * n)()
+        for i, x in enumerate(xs):
+            if x is not None:
+                p, k = _ptr(x)
+                keep.append(k)
+                arr[i] = p
+        return arr
+    hs = (ctypes.c_void_p * n)(*[b.handle.value for b in batches])
+    _check(lib().tb_batch_export_many(hs, n, plist(origins), plist(masks), plist(voxel_offset),
+                                      plist(leaf_offsets), ctypes.c_void_p(_stream(stream))))

@@ -68,12 +68,12 @@ thread_local long long t_launches = 0;
 // ---------------------------------------------------------------- kernel timing
 
 enum KernelKind {
-  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKLeafTable, kKNumKinds
+  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKLeafTable, kKExport, kKNumKinds
 };
 const char* const kKernelNames[kKNumKinds] = {"prepass_ijk",   "prepass_leaves", "chain",         "write_ijk",
                                               "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
                                               "write_refine_dilate", "validate", "write_multi",   "prune",
-                                              "kernel_map",    "leaf_table"};
+                                              "kernel_map",    "leaf_table",    "export"};
 
 struct ProfRec {
   int kind;
@@ -1136,6 +1136,24 @@ tb_status tb_multi(const tb_batch* in, const tb_op* ops, const int32_t* chain_le
   return run_ops(in, chains, alloc, (cudaStream_t)stream, outs);
 }
 
+tb_status tb_selftest_wait(int32_t set_flag, int32_t spin_limit, tb_stream stream) {
+  if (spin_limit < 1) return fail(TB_ERR_INVALID_ARG, "tb_selftest_wait: spin_limit must be positive");
+  cudaStream_t s = (cudaStream_t)stream;
+  const Mem mem{nullptr, s};
+  uint32_t* d = (uint32_t*)mem.get(8);  // [0] the flag, [1] the error word
+  if (!d) return fail(TB_ERR_OOM, "tb_selftest_wait: allocation failed");
+  Guard g{&mem, d};
+  TB_CUDA(cudaMemsetAsync(d, 0, 8, s));
+  if (set_flag) TB_CUDA(cudaMemsetAsync(d, 1, 1, s));
+  TB_CUDA(launch(kKValidate, s, [&] { return launch_wait_selftest(d, (uint32_t)spin_limit, d + 1, s); }));
+  unsigned int* h = (unsigned int*)t_pinned.get(64);
+  if (!h) return fail(TB_ERR_OOM, "pinned buffer");
+  TB_CUDA(cudaMemcpyAsync(h, d + 1, 4, cudaMemcpyDeviceToHost, s));
+  TB_CUDA(cudaStreamSynchronize(s));
+  if (*h & kErrTimeout) return fail(TB_ERR_DEVICE_TIMEOUT, "a device-side wait timed out (self-test)");
+  return TB_OK;
+}
+
 tb_status tb_validate(const tb_batch* b, tb_stream stream) {
   tb_status st = check_batch(b);
   if (st != TB_OK) return st;
@@ -1193,17 +1211,55 @@ tb_status tb_batch_get_view(const tb_batch* b, tb_batch_view* v) {
   return TB_OK;
 }
 
+tb_status tb_batch_export_many(const tb_batch* const* batches, int32_t n, int32_t* const* origins,
+                               uint64_t* const* masks, int64_t* const* voxel_offset, int64_t* const* leaf_offsets,
+                               tb_stream stream) {
+  if (n < 0 || (n > 0 && !batches)) return fail(TB_ERR_INVALID_ARG, "tb_batch_export_many: bad batch list");
+  for (int32_t i = 0; i < n; ++i)
+    if (!batches[i]) return fail(TB_ERR_INVALID_ARG, "tb_batch_export_many: batch %d is NULL", i);
+  cudaStream_t s = (cudaStream_t)stream;
+  CopyTasks tasks;
+  tasks.n = 0;
+  // one copy task per array whose destination the device can write (device
+  // memory, or pinned host memory through its mapped address); plain copies
+  // for the rest
+  auto add = [&](const void* src, void* dst, unsigned long long bytes) -> tb_status {
+    if (!dst || !bytes) return TB_OK;
+    void* dev = nullptr;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, dst) == cudaSuccess &&
+        (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged || at.type == cudaMemoryTypeHost))
+      dev = at.devicePointer;
+    cudaGetLastError();
+    if (!dev) {
+      TB_CUDA(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s));
+      return TB_OK;
+    }
+    if (tasks.n == kMaxCopyTasks) {
+      TB_CUDA(launch(kKExport, s, [&] { return launch_copies(tasks, s); }));
+      tasks.n = 0;
+    }
+    tasks.t[tasks.n++] = CopyTask{src, dev, bytes};
+    return TB_OK;
+  };
+  for (int32_t i = 0; i < n; ++i) {
+    const tb_batch* b = batches[i];
+    tb_status st = TB_OK;
+    if (origins && st == TB_OK) st = add(b->origins, origins[i], (unsigned long long)b->L * 12);
+    if (masks && st == TB_OK) st = add(b->masks, masks[i], (unsigned long long)b->L * 64);
+    if (voxel_offset && st == TB_OK) st = add(b->voxel_offset, voxel_offset[i], (unsigned long long)b->L * 8);
+    if (leaf_offsets && st == TB_OK) st = add(b->leaf_offsets, leaf_offsets[i], (unsigned long long)(b->B + 1) * 8);
+    if (st != TB_OK) return st;
+  }
+  if (tasks.n) TB_CUDA(launch(kKExport, s, [&] { return launch_copies(tasks, s); }));
+  return TB_OK;
+}
+
 tb_status tb_batch_export(const tb_batch* b, int32_t* origins, uint64_t* masks, int64_t* voxel_offset,
                           int64_t* leaf_offsets, tb_stream stream) {
   if (!b) return fail(TB_ERR_INVALID_ARG, "tb_batch_export: batch is NULL");
-  cudaStream_t s = (cudaStream_t)stream;
-  if (origins && b->L) TB_CUDA(cudaMemcpyAsync(origins, b->origins, (size_t)b->L * 12, cudaMemcpyDefault, s));
-  if (masks && b->L) TB_CUDA(cudaMemcpyAsync(masks, b->masks, (size_t)b->L * 64, cudaMemcpyDefault, s));
-  if (voxel_offset && b->L)
-    TB_CUDA(cudaMemcpyAsync(voxel_offset, b->voxel_offset, (size_t)b->L * 8, cudaMemcpyDefault, s));
-  if (leaf_offsets)
-    TB_CUDA(cudaMemcpyAsync(leaf_offsets, b->leaf_offsets, (size_t)(b->B + 1) * 8, cudaMemcpyDefault, s));
-  return TB_OK;
+  return tb_batch_export_many(&b, 1, origins ? &origins : nullptr, masks ? &masks : nullptr,
+                              voxel_offset ? &voxel_offset : nullptr, leaf_offsets ? &leaf_offsets : nullptr, stream);
 }
 
 tb_status tb_batch_free(tb_batch* b, tb_stream stream) {

@@ -721,20 +721,29 @@ __device__ __forceinline__ void leaves_bounds(const int32_t* origins, const uint
 // a monotone arrival counter; barrier n completes when the counter reaches
 // n * gridDim.x.  The wait gives up after kSpinLimit polls with kErrTimeout
 // set, so a broken barrier ends the kernel instead of hanging it.
+// Waits until *p reaches `target` (a wrap-safe difference) or `limit` polls
+// have passed; then sets kErrTimeout in *err and returns false.  Every
+// spin-wait on another block's progress in this library goes through a
+// bounded wait like this one.
+__device__ __forceinline__ bool wait_reach(const uint32_t* p, uint32_t target, uint32_t limit, unsigned int* err) {
+  uint32_t spins = 0;
+  while ((int)(ld_relaxed(p) - target) < 0) {
+    if (++spins > limit) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+    if (spins > 256) __nanosleep(32);
+  }
+  return true;
+}
+
 __device__ __forceinline__ void grid_sync(GridBarrier* bar, unsigned int* err) {
   __syncthreads();  // the block's writes before thread 0's release below
   if (threadIdx.x == 0) {
     unsigned int old;
     asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;" : "=r"(old) : "l"(&bar->count) : "memory");
     const unsigned int target = (old / gridDim.x + 1) * gridDim.x;
-    uint32_t spins = 0;
-    while ((int)(ld_relaxed(&bar->count) - target) < 0) {
-      if (++spins > kSpinLimit) {
-        atomicOr(err, kErrTimeout);
-        break;
-      }
-      if (spins > 256) __nanosleep(32);
-    }
+    wait_reach(&bar->count, target, kSpinLimit, err);
     asm volatile("fence.acq_rel.gpu;" ::: "memory");  // with the relaxed poll: an acquire
   }
   __syncthreads();

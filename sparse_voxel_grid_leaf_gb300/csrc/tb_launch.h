@@ -56,6 +56,23 @@ cudaError_t launch_kmap(const KmapArgs& k, int blocks, cudaStream_t s);
 cudaError_t launch_prune(const uint64_t* masks, const int32_t* leaf_grid, const int64_t* voxel_offset,
                          const int64_t* vbase, const uint8_t* flags, long long L, uint64_t* out, int blocks,
                          cudaStream_t s);
+// Copies of several arrays in one launch (tb_batch_export_many): task t
+// copies `bytes` from src to dst; both device-accessible (device memory, or
+// pinned host memory seen through unified addressing).
+constexpr int kMaxCopyTasks = 64;
+struct CopyTask {
+  const void* src;
+  void* dst;
+  unsigned long long bytes;
+};
+struct CopyTasks {
+  CopyTask t[kMaxCopyTasks];
+  int32_t n;
+};
+cudaError_t launch_copies(const CopyTasks& c, cudaStream_t s);
+
+// Self-test of the bounded device waits (tb_selftest_wait).
+cudaError_t launch_wait_selftest(const uint32_t* flag, uint32_t limit, unsigned int* err, cudaStream_t s);
 cudaError_t launch_validate(const int32_t* origins, const uint64_t* masks, const int32_t* leaf_grid,
                             const int64_t* leaf_offsets, long long L, int32_t B, unsigned int* err,
                             int blocks, cudaStream_t s);

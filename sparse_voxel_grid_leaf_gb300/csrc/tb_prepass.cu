@@ -66,6 +66,32 @@ __global__ void __launch_bounds__(256) k_prune(const uint64_t* masks, const int3
   }
 }
 
+// Several copies in one launch: blockIdx.y picks the task; 16-byte vectors
+// where both ends are 16-byte aligned, bytes otherwise.
+__global__ void __launch_bounds__(256) k_copies(const CopyTasks c) {
+  const CopyTask& t = c.t[blockIdx.y];
+  const unsigned long long tid = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+  const bool vec = (((uintptr_t)t.src | (uintptr_t)t.dst) & 15u) == 0;
+  unsigned long long done = 0;
+  if (vec) {
+    const unsigned long long nv = t.bytes / 16;
+    const int4* s4 = (const int4*)t.src;
+    int4* d4 = (int4*)t.dst;
+    for (unsigned long long i = tid; i < nv; i += stride) d4[i] = __ldg(s4 + i);
+    done = nv * 16;
+  }
+  const unsigned char* s1 = (const unsigned char*)t.src;
+  unsigned char* d1 = (unsigned char*)t.dst;
+  for (unsigned long long i = done + tid; i < t.bytes; i += stride) d1[i] = s1[i];
+}
+
+// Self-test of the bounded waits: one thread waits for *flag to reach 1 with
+// the same bounded spin as the grid barrier, `limit` polls at most.
+__global__ void k_wait_selftest(const uint32_t* flag, uint32_t limit, unsigned int* err) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) wait_reach(flag, 1u, limit, err);
+}
+
 // Canonical-order comparison of two leaf origins: signed tile, then x-major
 // upper child offset, then x-major lower child offset.
 __device__ __forceinline__ bool canon_less(const int32_t a[3], const int32_t b[3]) {
@@ -127,6 +153,21 @@ cudaError_t launch_prune(const uint64_t* masks, const int32_t* leaf_grid, const 
                          const int64_t* vbase, const uint8_t* flags, long long L, uint64_t* out, int blocks,
                          cudaStream_t s) {
   k_prune<<<blocks, 256, 0, s>>>(masks, leaf_grid, voxel_offset, vbase, flags, L, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_copies(const CopyTasks& c, cudaStream_t s) {
+  if (c.n <= 0) return cudaSuccess;
+  unsigned long long most = 0;
+  for (int i = 0; i < c.n; ++i) most = c.t[i].bytes > most ? c.t[i].bytes : most;
+  unsigned long long bx = (most / 16 + 255) / 256;
+  bx = bx < 1 ? 1 : (bx > 64 ? 64 : bx);
+  k_copies<<<dim3((unsigned)bx, (unsigned)c.n), 256, 0, s>>>(c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_selftest(const uint32_t* flag, uint32_t limit, unsigned int* err, cudaStream_t s) {
+  k_wait_selftest<<<1, 32, 0, s>>>(flag, limit, err);
   return cudaGetLastError();
 }
 

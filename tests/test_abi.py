@@ -58,6 +58,10 @@ def test_host_side_argument_errors(lib):
     st = lib.tb_refine_masked(None, None, ctypes.c_int32(2), None, None, ctypes.byref(out))
     assert st == 1 and out.value is None
     assert b"batch is NULL" in lib.tb_last_error()
+    st = lib.tb_batch_export_many(None, ctypes.c_int32(2), None, None, None, None, None)
+    assert st == 1 and b"bad batch list" in lib.tb_last_error()
+    st = lib.tb_selftest_wait(ctypes.c_int32(0), ctypes.c_int32(0), None)  # a bad limit, before any CUDA call
+    assert st == 1
     st = lib.tb_batch_get_view(None, None)
     assert st == 1
     assert lib.tb_batch_free(None, None) == 0

@@ -454,3 +454,39 @@ def test_kernel_map_shells_sampled_rows():
                     q = (int(p[0]) + dx, int(p[1]) + dy, int(p[2]) + dz)
                     assert got[j, k] == where.get(q, -1)
                     k += 1
+
+
+# ---------------------------------------------------------- failure detection
+
+def test_bounded_wait_gives_up_and_leaves_the_device_usable():
+    # a wait on a flag that nothing sets ends with TB_ERR_DEVICE_TIMEOUT after
+    # its poll limit (no hang, no fault); a preset flag passes
+    import time
+    t0 = time.time()
+    with pytest.raises(tb.TBError) as e:
+        tb.selftest_wait(False, spin_limit=1 << 14)
+    assert e.value.status == 6
+    assert time.time() - t0 < 30
+    tb.selftest_wait(True, spin_limit=1 << 14)
+    check(*synth.make("pr1_b2_res32"), [("refine", 2)], "after a timed-out wait")
+
+
+def test_export_many_matches_arrays():
+    import torch
+    ijk, off = synth.make("pr1_b2_res32")
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    bs = [b0, tb.refine(b0), tb.box_dilate(b0)]
+    ref = [b.to_numpy(["origins", "masks", "voxel_offset", "leaf_offsets"]) for b in bs]
+    # pinned host, device and pageable (numpy) destinations, one batch skipped per list
+    o = [torch.empty((b.num_leaves, 3), dtype=torch.int32).pin_memory() for b in bs]
+    m = [torch.empty((b.num_leaves, 8), dtype=torch.int64, device="cuda") for b in bs]
+    v = [np.zeros(b.num_leaves, np.int64) for b in bs]
+    lo = [torch.empty(b.num_grids + 1, dtype=torch.int64).pin_memory() for b in bs[:2]] + [None]
+    tb.export_many(bs, o, m, v, lo)
+    torch.cuda.synchronize()
+    for i, r in enumerate(ref):
+        assert np.array_equal(o[i].numpy(), r["origins"])
+        assert np.array_equal(m[i].cpu().numpy().view(np.uint64), r["masks"])
+        assert np.array_equal(v[i], r["voxel_offset"])
+        if lo[i] is not None:
+            assert np.array_equal(lo[i].numpy(), r["leaf_offsets"])
