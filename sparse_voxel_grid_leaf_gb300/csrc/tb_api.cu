@@ -652,7 +652,7 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   // ---- the cooperative pass kernel
   {
     ChainArgs ca;
-    ca.pass = (PassArgs*)(ws + o_args);
+    ca.pass = (const PassArgs*)(ws + o_args);
     ca.n_chain = n_chain;
     ca.n_stage = n_stage;
     ca.bar = (GridBarrier*)(ws + o_bar);

@@ -958,20 +958,34 @@ struct Loaded {
   int ch, k;
 };
 
+// A front end's key layout, planned by every block for itself.
+struct FrontPlan {
+  KeyLayout K;
+  int32_t P;
+  int32_t valid;
+};
+
 // Copies pass (ch, k) into the block's shared copy unless it is already
-// there; returns its op (< 0: none).
-__device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, PassArgs& dst, Loaded& held) {
+// there (with a front end's planned layout in place of its placeholder);
+// returns its op (< 0: none).  The pass array is read-only in the launch.
+__device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, PassArgs& dst, Loaded& held,
+                                         const FrontPlan& fp) {
   static_assert(sizeof(PassArgs) % 8 == 0 && sizeof(PassArgs) / 8 <= kThreads, "pass argument copy");
   __syncthreads();  // the previous phase is done with dst (and held is settled)
   if (ch != held.ch || k != held.k) {
     const unsigned long long* from = reinterpret_cast<const unsigned long long*>(c.pass + ch * c.n_stage + k);
-    if (threadIdx.x < sizeof(PassArgs) / 8)
-      reinterpret_cast<unsigned long long*>(&dst)[threadIdx.x] = __ldcg(from + threadIdx.x);  // L2: a front end's arguments are patched in the launch
+    if (threadIdx.x < sizeof(PassArgs) / 8) reinterpret_cast<unsigned long long*>(&dst)[threadIdx.x] = __ldg(from + threadIdx.x);
     __syncthreads();
     if (threadIdx.x == 0) {
+      if (fp.valid && ch == 0 && k == 0) {
+        dst.K = fp.K;
+        dst.P = fp.P;
+        dst.sorted = fp.P & 1;
+      }
       held.ch = ch;
       held.k = k;
     }
+    __syncthreads();
   }
   return dst.op;
 }
@@ -1006,24 +1020,24 @@ constexpr unsigned long long kSplitWCap = 1ull << 40;  // weights above this are
 // Work of chain ch in a phase of stage k, or -1 when it takes no part.
 __device__ __forceinline__ long long split_weight(const ChainArgs& c, int ch, int k, int kind, int d, Split& sp) {
   const PassArgs* p = c.pass + ch * c.n_stage + k;
-  const int op = __ldg(&p->op);
+  const int op = p->op;
   if (op < 0) return -1;
   unsigned long long w;
   if (kind == kSplitEmit) {
     const unsigned long long* cd = p->src_count_dev;
-    const unsigned long long n = cd ? __ldcg(cd) : (unsigned long long)__ldg(&p->src_count);
-    const int32_t lo[3] = {__ldg(&p->lo[0]), __ldg(&p->lo[1]), __ldg(&p->lo[2])};
-    const int32_t hi[3] = {__ldg(&p->hi[0]), __ldg(&p->hi[1]), __ldg(&p->hi[2])};
-    const unsigned long long T = (unsigned long long)pass_targets(op, __ldg(&p->factor), lo, hi);
+    const unsigned long long n = cd ? __ldcg(cd) : (unsigned long long)p->src_count;
+    const int32_t lo[3] = {p->lo[0], p->lo[1], p->lo[2]};
+    const int32_t hi[3] = {p->hi[0], p->hi[1], p->hi[2]};
+    const unsigned long long T = (unsigned long long)pass_targets(op, p->factor, lo, hi);
     w = n < kSplitWCap ? n * T : kSplitWCap;
-    atomicMax(&sp.maxP, __ldcg(&p->P));
-    if (!__ldg(&p->last)) sp.more = 1;
+    atomicMax(&sp.maxP, p->P);
+    if (!p->last) sp.more = 1;
   } else if (kind == kSplitLeaves) {
     const PassCtl* ctl = p->ctl;
     const ReadbackHeader* rb = p->rb;
     w = __ldcg(&ctl->head_totals[0]) + leaves_slot_cost(op) * __ldcg(&rb->num_slots);
   } else {
-    if (kind == kSplitSort && d >= __ldcg(&p->P)) return -1;
+    if (kind == kSplitSort && d >= p->P) return -1;
     const ReadbackHeader* rb = p->rb;
     w = __ldcg(&rb->num_slots);
   }
@@ -1042,22 +1056,22 @@ struct StageInfo {
   int op, P, last, T;
 };
 
-__device__ void load_stage(const ChainArgs& c, int k, StageInfo* si) {
+__device__ void load_stage(const ChainArgs& c, int k, StageInfo* si, const FrontPlan& fp) {
   __syncthreads();  // the previous stage's splits are done with si
   const int ch = threadIdx.x;
   if (ch < c.n_chain && ch < kWarpChains) {
     const PassArgs* p = c.pass + ch * c.n_stage + k;
     StageInfo& e = si[ch];
-    e.op = __ldg(&p->op);
-    e.P = __ldcg(&p->P);
-    e.last = __ldg(&p->last);
+    e.op = p->op;
+    e.P = (fp.valid && ch == 0 && k == 0) ? fp.P : p->P;  // a front end's planned digit passes
+    e.last = p->last;
     e.rb = p->rb;
     e.ctl = p->ctl;
     e.src_count_dev = p->src_count_dev;
-    e.src_count = __ldg(&p->src_count);
-    const int32_t lo[3] = {__ldg(&p->lo[0]), __ldg(&p->lo[1]), __ldg(&p->lo[2])};
-    const int32_t hi[3] = {__ldg(&p->hi[0]), __ldg(&p->hi[1]), __ldg(&p->hi[2])};
-    e.T = pass_targets(e.op, __ldg(&p->factor), lo, hi);
+    e.src_count = p->src_count;
+    const int32_t lo[3] = {p->lo[0], p->lo[1], p->lo[2]};
+    const int32_t hi[3] = {p->hi[0], p->hi[1], p->hi[2]};
+    e.T = pass_targets(e.op, p->factor, lo, hi);
   }
   __syncthreads();
 }
@@ -1179,12 +1193,12 @@ __device__ void split_grid(const ChainArgs& c, int k, int kind, int d, Split& sp
 // in serial mode every chain that takes part, as block blockIdx.x of the grid.
 template <class Body>
 __device__ __forceinline__ void for_share(const ChainArgs& c, int k, int kind, int d, const Split& sp, PassArgs& a,
-                                          Loaded& held, Body body) {
+                                          Loaded& held, const FrontPlan& fp, Body body) {
   const int serial = sp.serial;
   const int nit = serial ? c.n_chain : (sp.ch >= 0 ? 1 : 0);
   for (int it = 0; it < nit; ++it) {
     const int ch = serial ? it : sp.ch;
-    if (load_pass(c, ch, k, a, held) < 0) continue;
+    if (load_pass(c, ch, k, a, held, fp) < 0) continue;
     if (serial && kind == kSplitSort && d >= a.P) continue;
     body(a, ch, serial ? (int)blockIdx.x : sp.vb, serial ? (int)gridDim.x : sp.vg);
   }
@@ -1207,10 +1221,10 @@ __device__ void phase_front(const PassArgs& a) {
 }
 
 // After a grid barrier: every block reads the bbox and the checks, and plans
-// the pass's key layout; block 0 writes it into the pass's arguments in
-// device memory.  Returns false (in every block alike) when the call must
-// stop: bad offsets or origins, or a key wider than 64 bits.
-__device__ bool front_plan(const ChainArgs& c, const PassArgs& a) {
+// the pass's key layout for itself (into fp).  Returns false (in every block
+// alike) when the call must stop: bad offsets or origins, or a key wider than
+// 64 bits.
+__device__ bool front_plan(const ChainArgs& c, const PassArgs& a, FrontPlan& fp) {
   __shared__ int ok;
   if (threadIdx.x == 0) {
     const unsigned int err = __ldcg(c.err);
@@ -1225,11 +1239,10 @@ __device__ bool front_plan(const ChainArgs& c, const PassArgs& a) {
       good = make_layout(a.B, bb, bb[0] > bb[3], K);
       if (!good) {
         if (blockIdx.x == 0) atomicOr(c.err, kErrLayout);
-      } else if (blockIdx.x == 0) {
-        PassArgs& g = c.pass[0];
-        g.K = K;
-        g.P = (K.W + 7) / 8;
-        g.sorted = g.P & 1;
+      } else {
+        fp.K = K;
+        fp.P = (K.W + 7) / 8;
+        fp.valid = 1;
       }
     }
     ok = good ? 1 : 0;
@@ -1248,17 +1261,18 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
   __shared__ Split sp;
   __shared__ Loaded held;
   __shared__ StageInfo si[kWarpChains];
+  __shared__ FrontPlan fp;
   if (threadIdx.x == 0) {
     held.ch = -1;
     held.k = -1;
+    fp.valid = 0;
   }
   if (c.front) {  // one one-pass chain: plan its key from the input's bbox
-    load_pass(c, 0, 0, a, held);
+    load_pass(c, 0, 0, a, held, fp);
     phase_front(a);
     grid_sync(c.bar, c.err);
-    if (!front_plan(c, a)) return;
-    grid_sync(c.bar, c.err);
-    if (threadIdx.x == 0) held.ch = -1;  // reload the planned arguments
+    if (!front_plan(c, a, fp)) return;
+    if (threadIdx.x == 0) held.ch = -1;  // reload with the planned layout
   }
   const bool small = c.n_chain <= kWarpChains;
   auto split = [&](int k, int kind, int d) {
@@ -1269,11 +1283,11 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
     }
   };
   for (int k = 0; k < c.n_stage; ++k) {
-    if (small) load_stage(c, k, si);
+    if (small) load_stage(c, k, si, fp);
     split(k, kSplitEmit, 0);
     const int maxP = sp.maxP;
     const bool more = sp.more != 0;
-    for_share(c, k, kSplitEmit, 0, sp, a, held, [&](const PassArgs& pa, int, int vb, int vg) {
+    for_share(c, k, kSplitEmit, 0, sp, a, held, fp, [&](const PassArgs& pa, int, int vb, int vg) {
       stamp(pa, 0);
       dispatch_emit(pa, sm, vb, vg);
       stamp(pa, 1);
@@ -1281,12 +1295,12 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
     grid_sync(c.bar, c.err);
     for (int d = 0; d < maxP; ++d) {
       split(k, kSplitSort, d);
-      for_share(c, k, kSplitSort, d, sp, a, held,
+      for_share(c, k, kSplitSort, d, sp, a, held, fp,
                 [&](const PassArgs& pa, int, int vb, int vg) { phase_sort(pa, d, sm, vb, vg); });
       grid_sync(c.bar, c.err);
     }
     split(k, kSplitIndex, 0);
-    for_share(c, k, kSplitIndex, 0, sp, a, held, [&](const PassArgs& pa, int, int vb, int vg) {
+    for_share(c, k, kSplitIndex, 0, sp, a, held, fp, [&](const PassArgs& pa, int, int vb, int vg) {
       stamp(pa, 2);
       phase_index(pa, sm, vb, vg);
       stamp(pa, 3);
@@ -1295,7 +1309,7 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
     // the leaves and voxel offsets share one split: the block aggregates of
     // the leaves phase are indexed by virtual block
     split(k, kSplitLeaves, 0);
-    for_share(c, k, kSplitLeaves, 0, sp, a, held, [&](const PassArgs& pa, int ch, int vb, int vg) {
+    for_share(c, k, kSplitLeaves, 0, sp, a, held, fp, [&](const PassArgs& pa, int ch, int vb, int vg) {
       // the totals and per-grid offsets: a block near the end of the chain's
       // share, which holds few leaves
       if (sp.serial ? (int)blockIdx.x == (int)gridDim.x - 1 - (ch % (int)gridDim.x) : vb == vg - 1) {
@@ -1305,7 +1319,7 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
       dispatch_leaves(pa, sm, vb, vg);
     });
     grid_sync(c.bar, c.err);
-    for_share(c, k, -1, 0, sp, a, held, [&](const PassArgs& pa, int, int vb, int vg) {
+    for_share(c, k, -1, 0, sp, a, held, fp, [&](const PassArgs& pa, int, int vb, int vg) {
       if (pa.last) phase_voxel_offsets(pa, sm, vb, vg);
       stamp(pa, 4);
     });

@@ -163,16 +163,17 @@ struct PassArgs {
 // passes over the same input; pass[c * n_stage + k] is stage k of chain c
 // (op < 0 where chain c is shorter).  The array lives in device memory.
 // With `front` set, pass 0 of chain 0 (the only pass) is a front end whose
-// key layout the kernel plans itself from the input's bbox, writing K, P and
-// `sorted` into that pass's arguments before the emission.
+// key layout every block plans itself from the input's bbox (its K, P and
+// `sorted` in the pass's arguments are placeholders).
 struct ChainArgs {
-  PassArgs* pass;
+  const PassArgs* pass;  // [n_chain * n_stage], device memory
   int32_t n_chain;
   int32_t n_stage;
   GridBarrier* bar;
   unsigned int* err;
   int32_t front;
 };
+
 
 // Outputs of the final writer.
 struct WriteOut {

@@ -193,7 +193,7 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   // the pass arguments go to the scratch array from host stack memory
   TB_STATIC_CUDA(cudaMemcpyAsync(scratch + o_args, &a, sizeof a, cudaMemcpyHostToDevice, stream));
   ChainArgs ca;
-  ca.pass = (PassArgs*)(scratch + o_args);
+  ca.pass = (const PassArgs*)(scratch + o_args);
   ca.n_chain = 1;
   ca.n_stage = 1;
   ca.bar = (GridBarrier*)(scratch + o_bar);
