@@ -1275,7 +1275,11 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
     if (threadIdx.x == 0) held.ch = -1;  // reload with the planned layout
   }
   const bool small = c.n_chain <= kWarpChains;
+  // one chain takes the whole grid in every phase: its split is set once a
+  // stage (after the stage's emission split, which also reads maxP and more)
+  const bool one = c.n_chain == 1;
   auto split = [&](int k, int kind, int d) {
+    if (one && kind != kSplitEmit) return;
     if (small) {
       split_warp(c, si, kind, d, sp);
     } else {
