@@ -29,9 +29,9 @@
  *  - Streams.  All device work is enqueued on `stream` (NULL = legacy default
  *    stream) of the current CUDA device.  A producing call blocks the host
  *    once, on the readback of the per-grid counts (PR #757, Summary item 1,
- *    readback bullet); tb_from_ijk and tb_from_leaves block once more, on a
- *    coordinate-range readback that sizes the sort key.  Outputs are ready in
- *    stream order when the call returns.
+ *    readback bullet); for tb_from_ijk and tb_from_leaves the pass kernel
+ *    reads the input's coordinate range itself and sizes the sort key on the
+ *    device.  Outputs are ready in stream order when the call returns.
  *  - Memory.  `alloc` may be NULL: memory then comes from cudaMallocAsync on
  *    the device's default memory pool.  Otherwise every device allocation
  *    (outputs and per-call scratch) goes through alloc->alloc / alloc->free,

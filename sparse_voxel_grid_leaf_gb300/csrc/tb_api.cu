@@ -68,9 +68,9 @@ thread_local long long t_launches = 0;
 // ---------------------------------------------------------------- kernel timing
 
 enum KernelKind {
-  kKPrepassIjk, kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKLeafTable, kKExport, kKNumKinds
+  kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKLeafTable, kKExport, kKNumKinds
 };
-const char* const kKernelNames[kKNumKinds] = {"prepass_ijk",   "prepass_leaves", "chain",         "write_ijk",
+const char* const kKernelNames[kKNumKinds] = {"prepass_leaves", "chain",         "write_ijk",
                                               "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
                                               "write_refine_dilate", "validate", "write_multi",   "prune",
                                               "kernel_map",    "leaf_table",    "export"};
@@ -447,13 +447,13 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     }
   }
 
-  // ---- key layouts (front ends: after the range prepass)
+  // ---- key layouts (front ends: planned in the pass kernel from the input bbox)
   for (auto& pc : plans) {
     if (!front) {
       st = plan_layouts(pc, B, src.batch->bbox, src.batch->L == 0);
       if (st != TB_OK) return st;
     } else {
-      for (auto& pl : pc) pl.P = kMaxDigitPasses;  // sized for the widest key until the prepass
+      for (auto& pl : pc) pl.P = kMaxDigitPasses;  // buffers sized for the widest key
     }
   }
 

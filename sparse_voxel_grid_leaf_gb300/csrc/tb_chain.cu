@@ -1,25 +1,29 @@
 // The batched pass as one cooperative, persistent kernel per call, and the
-// final writer (fVDB PR #757 "Batched leaf-mask topology construction for
+// final writers (fVDB PR #757 "Batched leaf-mask topology construction for
 // generated conv grids", Summary item 1; item 2 for the box dilation).
 //
 // k_chain runs every pass of a call -- one or several chains of passes over
-// the same input -- with all blocks co-resident; phases are separated by a
-// bounded software grid barrier:
+// the same input, stage by stage, the chains of a stage side by side on
+// shares of the grid -- with all blocks co-resident; phases are separated by
+// a bounded software grid barrier:
+//   [front ends: input bbox -> key plan]
 //   emission -> digit pass 0 .. P-1 -> index -> leaves (merge, popcounts,
-//   bboxes; or the hand-off of an intermediate pass) -> voxel offsets.
+//   bboxes, staged records; or the hand-off of an intermediate pass) ->
+//   voxel offsets.
 // Everything the host needs to size the outputs then comes back in one
-// readback, and k_write_final writes the leaf records without any scan.
+// readback, and the writers copy the staged records into the exact outputs.
 //
-// Emission: one thread per source leaf (or input voxel) writes one slot per
-// non-empty target leaf -- 8 octant children for refine x2, the coarse leaf
-// for coarsen x2, up to 27 neighbours for a box dilation -- with
-// warp-aggregated slot claims, and builds the radix histograms of every digit
-// pass in shared memory.
+// Emission: one thread per (source leaf or input voxel, chunk of targets)
+// writes one slot per non-empty target leaf -- the f^3 children of a
+// refinement by f, the coarse leaf of a coarsening, up to 27 neighbours of a
+// box dilation, up to 64 fine leaves of a fused refinement then dilation --
+// with warp-aggregated slot claims, and counts the first digit's histogram.
 // Sort: the grid index is the key's most significant field, so one global LSD
 // sort over the varying key bits replaces the PR's segmented sorts.  A digit
 // pass is a onesweep tile loop: warp multisplit ranking (match.any), per-digit
-// decoupled look-back, shared-memory staging, coalesced scatter.
-// Dedup: head flags on the sorted keys (new leaf / lower node / upper node /
+// decoupled look-back, shared-memory staging, coalesced scatter, and the next
+// digit's histogram.
+// Index: head flags on the sorted keys (new leaf / lower node / upper node /
 // grid), a tile scan with warp-window look-back.
 #include "tb_common.cuh"
 #include "tb_launch.h"

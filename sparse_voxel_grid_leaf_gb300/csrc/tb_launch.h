@@ -20,11 +20,11 @@ inline size_t readback_bytes(int32_t B) {
          6 * sizeof(unsigned int) * (size_t)B;
 }
 
-cudaError_t launch_prepass_ijk(const int32_t* ijk, long long N, const int64_t* off, int32_t B,
-                               ReadbackHeader* rb, int blocks, cudaStream_t s);
+// Voxel bbox and checks of a raw leaf list (the allocation-free refinement).
 cudaError_t launch_prepass_leaves(const int32_t* origins, const uint64_t* masks, long long L,
                                   const int64_t* off, int32_t B, ReadbackHeader* rb, int blocks,
                                   cudaStream_t s);
+
 // Kernel map between two batches (tb_kmap.cu).  Box offsets d enumerate
 // [lo, hi] x-major; stride 1 or 2, forward or transposed.
 constexpr int kKmapMaxCand = 128;  // candidate input leaves of one output leaf

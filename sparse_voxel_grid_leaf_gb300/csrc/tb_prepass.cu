@@ -1,10 +1,9 @@
-// Front-end range prepasses and the canonical-batch validator.
-//
-// The ijk and leaf front ends (fVDB PR #757 "Batched leaf-mask topology
-// construction for generated conv grids", Follow-ups paragraph) first read
-// the input's voxel bounding box, which sizes the sort key, and check the
-// jagged offsets; tb_validate checks the invariants every produced batch
-// satisfies (canonical order per grid, non-zero masks, aligned origins).
+// Auxiliary kernels: the leaf-range prepass of the allocation-free refinement
+// (its input's voxel bounding box sizes the sort key; fVDB PR #757 "Batched
+// leaf-mask topology construction for generated conv grids"), masked
+// refinement's pruning, batched exports, the bounded-wait self-test, and the
+// canonical-batch validator (tb_validate: canonical order per grid, non-zero
+// masks, aligned origins).
 #include "tb_common.cuh"
 #include "tb_launch.h"
 
@@ -13,14 +12,6 @@ namespace tb {
 namespace {
 
 // ---------------------------------------------------------------- front-end prepasses
-
-__global__ void __launch_bounds__(256) k_prepass_ijk(const int32_t* ijk, long long N, const int64_t* off,
-                                                     int32_t B, ReadbackHeader* rb) {
-  int32_t mn[3], mx[3];
-  ijk_bounds(ijk, N, mn, mx);
-  reduce_bbox(mn, mx, rb->bbox_enc);
-  check_offsets(off, B, N, &rb->err);
-}
 
 // Exact voxel bbox of a leaf list (from the set bits), plus origin alignment.
 __global__ void __launch_bounds__(256) k_prepass_leaves(const int32_t* origins, const uint64_t* masks,
@@ -136,12 +127,6 @@ __global__ void __launch_bounds__(256) k_validate(const int32_t* origins, const 
 }
 
 }  // namespace
-
-cudaError_t launch_prepass_ijk(const int32_t* ijk, long long N, const int64_t* off, int32_t B,
-                               ReadbackHeader* rb, int blocks, cudaStream_t s) {
-  k_prepass_ijk<<<blocks, 256, 0, s>>>(ijk, N, off, B, rb);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_prepass_leaves(const int32_t* origins, const uint64_t* masks, long long L, const int64_t* off,
                                   int32_t B, ReadbackHeader* rb, int blocks, cudaStream_t s) {
