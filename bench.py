@@ -277,9 +277,10 @@ def kernel_bytes(ps):
       emission   source records (80 B: origin, mask, grid; 12 B per voxel) + 12 S
       sort       24 S P (key and reference read and written per digit pass)
       index      8 S (keys) + 12 L_out (run start, lower and upper index)
-      leaves     20 L_out + 4 S + the sources again (64 B masks, or 12 B per
-                 voxel slot), then 80 L_out hand-off (intermediate) or
-                 84 L_out staged record, popcount and grid (last)
+      leaves     20 L_out + 4 S + the source masks again (64 B per source
+                 leaf; an ijk slot carries its voxel's bit), then 80 L_out
+                 hand-off (intermediate) or 84 L_out staged record, popcount
+                 and grid (last)
       writer     96 L_out read (staged record, grid, voxel offset, node
                  indices) + 124 L_out written + 16 per lower + 12 per upper
     """
@@ -291,7 +292,7 @@ def kernel_bytes(ps):
         L_in, S, L_out = p["L_in"], p["S"], p["L_out"]
         ijk = p["kind"] == "ijk"
         src = 24 * L_in if ijk else 80 * L_in     # ijk: the bbox read, then the emission's
-        merge = 20 * L_out + 4 * S + (12 * S if ijk else 64 * L_in)
+        merge = 20 * L_out + 4 * S + (0 if ijk else 64 * L_in)
         chain = src + 12 * S + 24 * S * p["P"] + 8 * S + 12 * L_out + merge
         chain += 80 * L_out if p.get("inter") else 84 * L_out
         acc("chain", chain)

@@ -292,8 +292,9 @@ __device__ void phase_emit(const PassArgs& a, Smem& sm, int vb, int vg) {
         bits &= bits - 1;
         uint32_t val;
         if (OP == kIjk) {
+          // the voxel's bit in its leaf, n = 64 x + 8 y + z: all the merge needs
           key = encode_key(a.K, g, lc[0] >> 3, lc[1] >> 3, lc[2] >> 3);
-          val = (uint32_t)i;
+          val = (uint32_t)(((lc[0] & 7) << 6) | ((lc[1] & 7) << 3) | (lc[2] & 7));
         } else {
           uint32_t code;
           int32_t tl[3];
@@ -500,12 +501,10 @@ __device__ __forceinline__ uint64_t merge_run(const PassArgs& a, const uint32_t*
   (void)unit;
   for (uint32_t s = s0 + w; s < s1; s += 8) {
     const uint32_t val = __ldcg(vals + s);
-    if constexpr (OP == kIjk) {
-      const long long n = val;
-      const int32_t x = __ldg(a.ijk + 3 * n), y = __ldg(a.ijk + 3 * n + 1), z = __ldg(a.ijk + 3 * n + 2);
-      const uint64_t bit = 1ull << (8 * (y & 7) + (z & 7));
+    if constexpr (OP == kIjk) {  // the slot holds the voxel's bit n = 64 x + 8 y + z
+      const uint64_t bit = 1ull << (val & 63u);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) c[k] |= ((x & 7) == k) ? bit : 0ull;
+      for (int k = 0; k < 8; ++k) c[k] |= ((int)(val >> 6) == k) ? bit : 0ull;
     } else {
     uint64_t m[8];
     load_mask(a.src_masks, (long long)(val >> a.code_bits), m);

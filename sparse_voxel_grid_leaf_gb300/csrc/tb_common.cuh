@@ -28,8 +28,9 @@ constexpr int kNumOps = 6;
 constexpr int kBins = 256;            // 8-bit radix digits
 constexpr int kMaxDigitPasses = 8;    // 64-bit key
 // slot value = source index << code_bits | target code; code_bits per pass
-// kind (pass_code_bits): 0 for the front ends, 3 log2(f) for refine and
-// coarsen by f, 5 for a box dilation, 6 for refine-then-dilate
+// kind (pass_code_bits): 0 for the leaf front end, 3 log2(f) for refine and
+// coarsen by f, 5 for a box dilation, 6 for refine-then-dilate.  The ijk
+// front end's slot value is the voxel's bit in its leaf, 64 x + 8 y + z.
 
 // Error bits reported through the readback header.
 constexpr uint32_t kErrTimeout = 1u;       // a bounded wait (look-back or grid barrier) gave up
