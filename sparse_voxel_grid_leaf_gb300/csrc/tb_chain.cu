@@ -212,15 +212,23 @@ __device__ __forceinline__ bool target_nonempty(const PassArgs& a, const uint64_
   const int tlx = a.lo[0] < 0 ? -1 : 0, tly = a.lo[1] < 0 ? -1 : 0, tlz = a.lo[2] < 0 ? -1 : 0;
   const int ny = (a.hi[1] > 0 ? 1 : 0) - tly + 1, nz = (a.hi[2] > 0 ? 1 : 0) - tlz + 1;
   const int tz = tlz + (int)(t % nz), ty = tly + (int)((t / nz) % ny), tx = tlx + (int)(t / (nz * ny));
-  const uint32_t zx = dilate_zone(tx, a.lo[0], a.hi[0]), zy = dilate_zone(ty, a.lo[1], a.hi[1]),
-                 zz = dilate_zone(tz, a.lo[2], a.hi[2]);
-  uint64_t xs = 0, ym = 0;
+  uint64_t xs = 0, ym = 0, zm;
+  if (a.lo[0] >= -1 && a.lo[1] >= -1 && a.lo[2] >= -1 && a.hi[0] <= 1 && a.hi[1] <= 1 && a.hi[2] <= 1) {
+    // a box within [-1, 1]^3: the zones are the whole leaf (offset 0) or the
+    // facing plane (offset +-1)
+    xs = tx < 0 ? m[0] : (tx > 0 ? m[7] : all);
+    ym = ty < 0 ? 0x00000000000000FFull : (ty > 0 ? 0xFF00000000000000ull : ~0ull);
+    zm = tz < 0 ? 0x0101010101010101ull : (tz > 0 ? 0x8080808080808080ull : ~0ull);
+  } else {
+    const uint32_t zx = dilate_zone(tx, a.lo[0], a.hi[0]), zy = dilate_zone(ty, a.lo[1], a.hi[1]),
+                   zz = dilate_zone(tz, a.lo[2], a.hi[2]);
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    if ((zx >> k) & 1u) xs |= m[k];
-    if ((zy >> k) & 1u) ym |= 0xFFull << (8 * k);
+    for (int k = 0; k < 8; ++k) {
+      if ((zx >> k) & 1u) xs |= m[k];
+      if ((zy >> k) & 1u) ym |= 0xFFull << (8 * k);
+    }
+    zm = 0x0101010101010101ull * zz;
   }
-  const uint64_t zm = 0x0101010101010101ull * zz;
   code = (uint32_t)(9 * (tx + 1) + 3 * (ty + 1) + (tz + 1));
   out[0] = lc[0] + tx;
   out[1] = lc[1] + ty;
