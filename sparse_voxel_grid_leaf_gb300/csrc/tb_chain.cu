@@ -764,8 +764,13 @@ __device__ void phase_leaves(const PassArgs& a, Smem& sm, int vb, int vg) {
       gg[r] = 0;
       lcs[r][0] = lcs[r][1] = lcs[r][2] = 0;
       if (valid[r]) {
-        s0 = __ldcg(a.run_start + u);
-        s1 = u + 1 < U ? __ldcg(a.run_start + u + 1) : (uint32_t)S;
+        if (S == U) {  // every run is one slot (refinement): leaf u is slot u
+          s0 = (uint32_t)u;
+          s1 = (uint32_t)u + 1;
+        } else {
+          s0 = __ldcg(a.run_start + u);
+          s1 = u + 1 < U ? __ldcg(a.run_start + u + 1) : (uint32_t)S;
+        }
         decode_key(a.K, __ldcg(keys + s0), gg[r], lcs[r]);
       }
       word[r] = merge_run<OP>(a, vals, s0, s1, w);
