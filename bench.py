@@ -536,7 +536,57 @@ def per_op_tables(tb, torch, synth, stream, flush, main_workload):
         res[wl] = row
         fine.free()
         b0.free()
+    res["pyramid_b48_res64"] = pyramid_table(tb, torch, synth, stream, flush)
     return res
+
+
+PYRAMID = [("e1", [("coarsen", 2)]), ("e2", [("coarsen", 4)]), ("e3", [("coarsen", 8)]),
+           ("u2", [("coarsen", 8), ("refine", 2)]),
+           ("d2", [("coarsen", 8), ("refine", 2), DIL]),
+           ("u1", [("coarsen", 8), ("refine", 2), DIL, ("refine", 2)]),
+           ("d1", [("coarsen", 8), ("refine", 2), DIL, ("refine", 2), DIL]),
+           ("u0", [("coarsen", 8), ("refine", 2), DIL, ("refine", 2), DIL, ("refine", 2)])]
+
+
+def pyramid_table(tb, torch, synth, stream, flush):
+    """The 4-level pyramid rebuild on pyramid_b48_res64 (encoder coarsenings
+    by 2, 4, 8; decoder refinements with a k3s1 dilation per level; 11 passes
+    of the pages' schedule): as 8 calls level by level, and as one tb_multi
+    call of the 8 chains (one launch; fused passes).  Median ms of 20 after
+    5 warm-ups, L2 flushed; the front end is not included."""
+    ijk, off = synth.make("pyramid_b48_res64")
+    b0 = tb.from_ijk(torch.from_numpy(ijk).cuda(), torch.from_numpy(off).cuda())
+    plan = tb.MultiPlan([o for _, o in PYRAMID])
+
+    def levels():
+        e1, e2, e3 = tb.coarsen(b0, 2), tb.coarsen(b0, 4), tb.coarsen(b0, 8)
+        u2 = tb.refine(e3)
+        d2 = tb.box_dilate(u2)
+        u1 = tb.refine(d2)
+        d1 = tb.box_dilate(u1)
+        u0 = tb.refine(d1)
+        return [e1, e2, e3, u2, d2, u1, d1, u0]
+    row = {}
+    for lab, fn in (("pyramid_8_calls", levels), ("pyramid_one_multi", lambda: plan(b0))):
+        ts = []
+        vox = 0
+        for it in range(25):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            rs = fn()
+            e.record(stream)
+            e.synchronize()
+            if it == 0:
+                vox = sum(int(x.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for x in rs)
+            for x in rs:
+                x.free()
+            if it >= 5:
+                ts.append(s.elapsed_time(e))
+        med = statistics.median(ts)
+        row[lab] = {"ms": med, "out_voxels": vox, "Gvox_per_s": vox / med / 1e6}
+    b0.free()
+    return row
 
 
 def main():

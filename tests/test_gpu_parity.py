@@ -490,3 +490,14 @@ def test_export_many_matches_arrays():
         assert np.array_equal(v[i], r["voxel_offset"])
         if lo[i] is not None:
             assert np.array_equal(lo[i].numpy(), r["leaf_offsets"])
+
+
+def test_pyramid_b48_one_multi_call():
+    # the same eight pyramid levels as one tb_multi call (one launch, fused passes)
+    import bench
+    ijk, off = synth.make("pyramid_b48_res64")
+    L0 = tb.from_ijk(dev(ijk), dev(off))
+    outs = tb.multi(L0, [ops for _, ops in bench.PYRAMID])
+    for (name, ops), b in zip(bench.PYRAMID, outs):
+        assert_same(b.to_numpy(), oracle.run_voxels(ijk, off, ops), "multi " + name)
+        b.validate()
