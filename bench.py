@@ -252,7 +252,8 @@ def pass_stats(outs):
 
     def add(kind, L_in, b):
         ps.append({"kind": kind, "L_in": L_in, "S": b.build_slots, "L_out": b.num_leaves,
-                   "P": b.build_digit_passes, "NL": b.num_lowers, "NU": b.num_uppers, "B": b.num_grids})
+                   "P": b.build_digit_passes, "NL": b.num_lowers, "NU": b.num_uppers, "B": b.num_grids,
+                   "kernel": "member" if b.build_member_ctas else "chain"})
     add("ijk", b0.build_source_leaves, b0)
     add("refine", b0.num_leaves, outs["refine2"])
     add("coarsen", b0.num_leaves, outs["coarsen2"])
@@ -266,10 +267,12 @@ def pass_stats(outs):
 
 def kernel_bytes(ps):
     """Algorithmic DRAM bytes per kernel over one step (each record read or
-    written once; per-grid arrays ignored).  "chain" is the cooperative kernel
-    of a call: emission, digit passes, index, leaves and voxel offsets of each
-    of its passes; "write_<op>" is the final writer of a one-chain call,
-    "write_multi" the one writer of all chains of a tb_multi call.
+    written once; per-grid arrays ignored).  "chain" is the cooperative
+    whole-grid pass kernel of a call and "member" the member launch (one
+    cluster per grid), whichever built the pass: emission, digit passes,
+    index, leaves and voxel offsets of each of its passes; "write_<op>" is the
+    final writer of a one-chain call, "write_multi" the one writer of all
+    chains of a tb_multi call.
 
     Per pass, with L_in source leaves (voxels for the ijk front end), S slots,
     L_out unique leaves and P digit passes:
@@ -295,7 +298,7 @@ def kernel_bytes(ps):
         merge = 20 * L_out + 4 * S + (0 if ijk else 64 * L_in)
         chain = src + 12 * S + 24 * S * p["P"] + 8 * S + 12 * L_out + merge
         chain += 80 * L_out if p.get("inter") else 84 * L_out
-        acc("chain", chain)
+        acc(p.get("kernel", "chain"), chain)
         if not p.get("inter"):
             w = "write_" + p["kind"] if SEPARATE or ijk else "write_multi"
             acc(w, 96 * L_out + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])

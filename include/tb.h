@@ -127,6 +127,9 @@ typedef struct tb_batch_view {
   int32_t build_key_bits;            /* width of the compressed sort key          */
   int32_t build_digit_passes;        /* 8-bit radix passes run                    */
   int64_t num_voxels;                /* active voxels of the whole batch (host)   */
+  int32_t build_member_ctas;         /* CTAs per member of the pass's member launch,
+                                        0: the whole-grid kernel (tb_set_launch_mode) */
+  int32_t reserved;
 } tb_batch_view;
 
 /* Per-kernel timing record (see tb_profile_enable). */
@@ -353,6 +356,17 @@ TB_API tb_status tb_selftest_wait(int32_t set_flag, int32_t spin_limit, tb_strea
  * them; it returns the number of distinct records (which may exceed `max`). */
 TB_API tb_status tb_profile_enable(int32_t on);
 TB_API int32_t tb_profile_read(tb_kernel_stat* stats, int32_t max);
+
+/* Launch shape of the pass kernel (library extension: the pages prescribe
+ * none).  mode 0 (default): a member launch -- one cluster of 1 to 8 CTAs per
+ * grid of every chain, each running its grid's passes as a batch of one grid,
+ * the call's counts gathered by the last cluster to finish -- when every grid
+ * is small (at most 16384 candidate leaves or input voxels per CTA of its
+ * cluster, and at most 4096 grids), else the cooperative whole-grid kernel;
+ * 1: always the whole-grid kernel; 2: a member launch for every non-empty
+ * input.  Both give identical outputs.  Process-wide; returns the previous
+ * mode, or -1 (mode unchanged) for a mode outside 0..2. */
+TB_API int32_t tb_set_launch_mode(int32_t mode);
 
 /* Number of kernels this thread has launched through the library so far. */
 TB_API int64_t tb_kernel_launch_count(void);

@@ -59,7 +59,8 @@ class _View(ctypes.Structure):
                    "lower_offsets", "upper_offsets", "lower_origins", "lower_parent", "upper_origins")] + \
                [("build_slots", ctypes.c_int64), ("build_source_leaves", ctypes.c_int64),
                 ("build_key_bits", ctypes.c_int32), ("build_digit_passes", ctypes.c_int32),
-                ("num_voxels", ctypes.c_int64)]
+                ("num_voxels", ctypes.c_int64), ("build_member_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
 
 class _KStat(ctypes.Structure):
@@ -110,6 +111,8 @@ def lib():
             L.tb_profile_enable.restype = ctypes.c_int
             L.tb_profile_read.argtypes = [ctypes.POINTER(_KStat), ctypes.c_int32]
             L.tb_profile_read.restype = ctypes.c_int32
+            L.tb_set_launch_mode.argtypes = [ctypes.c_int32]
+            L.tb_set_launch_mode.restype = ctypes.c_int32
             _lib = L
         return _lib
 
@@ -147,6 +150,20 @@ def selftest_wait(set_flag: bool, spin_limit: int = 1 << 16, stream=None):
 def kernel_launch_count() -> int:
     """Kernels launched through the library by the calling thread so far."""
     return int(lib().tb_kernel_launch_count())
+
+
+LAUNCH_MODES = {"auto": 0, "grid": 1, "member": 2}
+
+
+def set_launch_mode(mode: str) -> str:
+    """Launch shape of the pass kernel for the whole process: "auto" (member
+    launches -- one cluster per grid of every chain -- where every grid is
+    small, else the whole-grid kernel), "grid" or "member".  Returns the
+    previous mode."""
+    prev = lib().tb_set_launch_mode(LAUNCH_MODES[mode])
+    if prev < 0:
+        raise ValueError("launch mode %r" % (mode,))
+    return {v: k for k, v in LAUNCH_MODES.items()}[prev]
 
 
 def profile_enable(on=True):
@@ -226,6 +243,8 @@ class Batch:
     build_source_leaves = property(lambda self: int(self._view().build_source_leaves))
     build_key_bits = property(lambda self: int(self._view().build_key_bits))
     build_digit_passes = property(lambda self: int(self._view().build_digit_passes))
+    # CTAs per member of the member launch that built the batch; 0: whole-grid kernel
+    build_member_ctas = property(lambda self: int(self._view().build_member_ctas))
     num_voxels = property(lambda self: int(self._view().num_voxels))
 
     @property

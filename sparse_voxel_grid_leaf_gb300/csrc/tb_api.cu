@@ -15,7 +15,9 @@
 // the front ends the pass kernel reads the input's bbox and plans the key
 // itself; the host repeats that plan after the readback.
 #include <algorithm>
+#include <atomic>
 #include <chrono>
+#include <cstddef>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -32,7 +34,7 @@ using namespace tb;
 
 struct tb_batch {
   int64_t build_slots = 0, build_sources = 0;
-  int32_t build_key_bits = 0, build_digit_passes = 0;
+  int32_t build_key_bits = 0, build_digit_passes = 0, build_member_ctas = 0;
   int32_t B = 0;
   int device = 0;
   int64_t L = 0, NL = 0, NU = 0;
@@ -68,23 +70,25 @@ thread_local long long t_launches = 0;
 // ---------------------------------------------------------------- kernel timing
 
 enum KernelKind {
-  kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKLeafTable, kKExport, kKNumKinds
+  kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKLeafTable,
+  kKExport, kKMember, kKNumKinds
 };
 const char* const kKernelNames[kKNumKinds] = {"prepass_leaves", "chain",         "write_ijk",
                                               "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
                                               "write_refine_dilate", "validate", "write_multi",   "prune",
-                                              "kernel_map",    "leaf_table",    "export"};
+                                              "kernel_map",    "leaf_table",    "export",        "member"};
 
 struct ProfRec {
   int kind;
   cudaEvent_t a, b;
 };
 thread_local int t_prof = 0;  // 1: kernel events, 2: also pass-phase stamps
-constexpr int kNumGpuPhases = 4;
-constexpr int kNumPhases = 7;
-const char* const kPhaseNames[kNumPhases] = {"phase_emit",       "phase_sort",     "phase_dedup_merge",
-                                             "phase_offsets",    "host_before_sync", "host_sync_wait",
-                                             "host_after_sync"};
+constexpr int kNumGpuPhases = 5;
+constexpr int kNumPhases = 11;
+const char* const kPhaseNames[kNumPhases] = {"phase_emit",      "phase_sort",       "phase_dedup_merge",
+                                             "phase_leaves",    "phase_offsets",    "phase_entry",
+                                             "host_before_sync", "host_sync_wait",  "host_after_sync",
+                                             "host_plan",       "host_alloc"};
 double host_ms_since(const std::chrono::steady_clock::time_point& t0) {
   return std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
 }
@@ -141,6 +145,7 @@ tb_status fail(tb_status st, const char* fmt, ...) {
 struct DeviceInfo {
   int sms = 0;
   int occ_chain = 1;
+  int occ_member = 1;
   int occ_write[kNumOps] = {};
   int occ_write_multi = 1;
   bool coop = false;
@@ -160,6 +165,7 @@ tb_status device_info(int dev, DeviceInfo** out) {
     if (!coop) return fail(TB_ERR_CUDA, "device %d does not support cooperative launches", dev);
     d.coop = true;
     d.occ_chain = chain_occupancy();
+    d.occ_member = member_occupancy();
     for (int op = 0; op < kNumOps; ++op) d.occ_write[op] = write_final_occupancy(op);
     d.occ_write_multi = write_multi_occupancy();
     // keep freed memory in the default pool between calls
@@ -237,6 +243,7 @@ struct Pinned {
   }
 };
 thread_local Pinned t_pinned;
+thread_local unsigned int t_seq = 0;  // readback flag values of this thread's calls
 
 bool device_accessible(const void* p) {
   if (!p) return false;
@@ -265,7 +272,41 @@ struct PassPlan {
   int P = 0;
   long long sort_tiles = 0, dedup_tiles = 0;
   size_t rb = 0, ctl = 0, sort_status = 0, dedup_status = 0, first = 0;
+  size_t unit_ctl = 0;       // member launches: the members' control blocks
+  long long ctl_stride = 0;  // and their size
 };
+
+// ---------------------------------------------------------------- launch shape
+
+// 0: member launches where they pay, 1: always the whole-grid kernel, 2:
+// member launches whenever possible (tb_set_launch_mode).
+std::atomic<int> g_launch_mode{0};
+// A member launch saves the whole-grid kernel's barriers and long look-backs
+// but runs each grid's leaves phase on the member's own CTAs, so it pays
+// where every grid's leaves are few for its CTAs (measured on GB300: single
+// refine / coarsen / dilate calls on 16 or 48 grids of resolution 64, every
+// front end tried) and loses where one chain's leaves dominate: several
+// chains in one call, the fused refine-then-dilate merge, large grids.
+constexpr long long kMemberSlotsPerCta = 2048;        // candidate leaves of one grid per member CTA
+constexpr long long kMemberVoxelsPerCta = 16384;      // front ends: input voxels of one grid per member CTA
+constexpr int32_t kMemberMaxGrids = 4096;             // the last member scans its chain's grid counts alone
+
+// CTAs per member of a member launch (1, 2, 4 or 8: the most whose clusters
+// all fit on the device at once), or 0 for the whole-grid kernel.  `nmax` is
+// the most stage-0 sources of one grid (-1: not known on the host), `mmax`
+// the largest slot capacity per stage-0 source of any pass, `heavy` whether a
+// pass is the fused refine-then-dilate.
+int member_ctas(int n_chain, int32_t B, long long count, long long nmax, long long mmax, long long resident,
+                bool front, bool heavy) {
+  const int mode = g_launch_mode.load();
+  if (mode == 1 || B < 1 || count <= 0) return 0;
+  int cl = 8;
+  while (cl > 1 && (long long)n_chain * B * cl > resident) cl >>= 1;
+  if (mode == 2) return cl;
+  if (B > kMemberMaxGrids || n_chain > 1 || heavy) return 0;
+  const long long n = nmax >= 0 ? nmax : 2 * ((count + B - 1) / B);  // unknown: twice the mean
+  return n * mmax <= (front ? kMemberVoxelsPerCta : kMemberSlotsPerCta) * cl ? cl : 0;
+}
 
 long long slots_per_source(const PassSpec& s) { return pass_targets(s.op, s.factor, s.lo, s.hi); }
 
@@ -447,10 +488,32 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     }
   }
 
+  // ---- launch shape: a member launch (one cluster per grid of every chain)
+  // where every grid is small, else the whole-grid kernel
+  const bool off_on_host = front && src.offsets && !device_accessible(src.offsets);
+  int cl = 0;
+  {
+    long long nmax = -1, mmax = 1;
+    const int64_t* hoff = src.kind == kSrcBatch ? src.batch->leaf_offsets_host.data()
+                                                : (off_on_host ? src.offsets : nullptr);
+    if (hoff && B > 0) {
+      nmax = 0;
+      for (int32_t g = 0; g < B; ++g) nmax = std::max<long long>(nmax, hoff[g + 1] - hoff[g]);
+    }
+    bool heavy = false;
+    for (const auto& pc : plans)
+      for (const auto& pl : pc) {
+        if (src.count > 0) mmax = std::max(mmax, pl.slot_cap / src.count);
+        heavy |= pl.spec.op == kRefineDilate;
+      }
+    cl = member_ctas(n_chain, B, src.count, nmax, mmax, (long long)di->sms * di->occ_member, front, heavy);
+  }
+  const int32_t B_key = cl ? 1 : B;  // a member's keys have no grid field
+
   // ---- key layouts (front ends: planned in the pass kernel from the input bbox)
   for (auto& pc : plans) {
     if (!front) {
-      st = plan_layouts(pc, B, src.batch->bbox, src.batch->L == 0);
+      st = plan_layouts(pc, B_key, src.batch->bbox, src.batch->L == 0);
       if (st != TB_OK) return st;
     } else {
       for (auto& pl : pc) pl.P = kMaxDigitPasses;  // buffers sized for the widest key
@@ -466,9 +529,16 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   for (int ch = 0; ch < n_chain; ++ch) o_rb_last[ch] = c.take(rb_stride);
   const size_t readback_span = c.off;
   const size_t o_bar = c.take(sizeof(GridBarrier));
+  const size_t o_done = c.take((size_t)n_chain * 4);  // finished members of each chain
+  const size_t o_exit = c.take(16);                   // CTAs (or chains) out of the pass kernel
+  const long long total = src.count;  // stage-0 sources of the call
   for (int ch = 0; ch < n_chain; ++ch)
     for (size_t p = 0; p < plans[ch].size(); ++p) {
       PassPlan& pl = plans[ch][p];
+      if (cl) {  // members: the chain's readback block; their own control is carved below
+        pl.rb = o_rb_last[ch];
+        continue;
+      }
       // status words for full tiles, or one short tile per block of a small pass
       pl.sort_tiles = std::max({1ll, (pl.slot_cap + kSortTile - 1) / kSortTile,
                                 std::min<long long>(G, (pl.slot_cap + 255) / 256)});
@@ -483,8 +553,23 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   for (auto& pc : plans) n_pass_total += pc.size();
   const size_t o_ts = c.take(t_prof >= 2 ? n_pass_total * 8 * sizeof(unsigned long long) : 0);
   const size_t zero_bytes = c.off;
+  // member launches: control blocks and status words per member and pass,
+  // carved from the grids' source offsets and zeroed by the members
+  const long long ctl_rb_bytes = (long long)((readback_bytes(1) + 15) & ~(size_t)15);
+  if (cl)
+    for (int ch = 0; ch < n_chain; ++ch)
+      for (size_t p = 0; p < plans[ch].size(); ++p) {
+        PassPlan& pl = plans[ch][p];
+        const long long M = pl.slot_cap / total;
+        pl.ctl_stride = (ctl_rb_bytes + (long long)offsetof(PassCtl, hist) + (long long)pl.P * kBins * 4 + 16 + 63) &
+                        ~63ll;
+        pl.unit_ctl = c.take((size_t)B * (size_t)pl.ctl_stride);
+        pl.sort_status = c.take((size_t)member_first(total, M, kSortTile, cl, B) * pl.P * kBins * 4);
+        pl.dedup_status = c.take((size_t)member_first(total, M, kDedupTile, 0, B) * 3 * 8);
+      }
   struct ChainBufs {
     size_t keys0, keys1, vals0, vals1, run, llow, lup, voff, pop, lg, blk, grp, inter[2][3];
+    long long m_slots, m_out[2];  // member launches: capacities per stage-0 source
   };
   std::vector<ChainBufs> cb(n_chain);
   for (int ch = 0; ch < n_chain; ++ch) {
@@ -501,14 +586,20 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     b.keys1 = c.take((size_t)max_slots * 8);
     b.vals0 = c.take((size_t)max_slots * 4);
     b.vals1 = c.take((size_t)max_slots * 4);
-    b.run = c.take((size_t)(max_slots + 1) * 4);
-    b.llow = c.take((size_t)last_slots * 4);
-    b.lup = c.take((size_t)last_slots * 4);
-    b.voff = c.take((size_t)last_slots * 8);
-    b.pop = c.take((size_t)last_slots * 4);
-    b.lg = c.take((size_t)last_slots * 4);
-    b.blk = c.take((size_t)G * 8);
-    b.grp = c.take((size_t)G * 32 * 8);
+    // members index the per-leaf arrays like their slots; each adds one run sentinel
+    const long long leaf_slots = cl ? max_slots : last_slots;
+    const long long aggs = cl ? (long long)B * cl : G;
+    b.run = c.take((size_t)(max_slots + 1 + (cl ? B : 0)) * 4);
+    b.llow = c.take((size_t)leaf_slots * 4);
+    b.lup = c.take((size_t)leaf_slots * 4);
+    b.voff = c.take((size_t)leaf_slots * 8);
+    b.pop = c.take((size_t)leaf_slots * 4);
+    b.lg = c.take((size_t)leaf_slots * 4);
+    b.blk = c.take((size_t)aggs * 8);
+    b.grp = c.take((size_t)aggs * 32 * 8);
+    b.m_slots = total > 0 ? max_slots / total : 0;
+    b.m_out[0] = total > 0 ? max_inter[0] / total : 0;
+    b.m_out[1] = total > 0 ? max_inter[1] / total : 0;
     for (int k = 0; k < 2; ++k) {
       b.inter[k][0] = c.take((size_t)max_inter[k] * 12);
       b.inter[k][1] = c.take((size_t)max_inter[k] * 64);
@@ -516,7 +607,6 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     }
   }
   const size_t o_args = c.take(sizeof(PassArgs) * (size_t)n_chain * n_stage);
-  const size_t o_tasks = c.take(n_chain > 1 ? sizeof(WriteTask) * (size_t)n_chain : 0);
   // staging of host-resident inputs
   const int32_t* in_ijk = src.ijk;
   const int32_t* in_orig = src.origins;
@@ -534,11 +624,13 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     if (st_b) o_st_b = c.take((size_t)src.count * 64);
   }
   if (front) {
-    st_off = !device_accessible(src.offsets);
+    st_off = off_on_host;
     if (st_off) o_st_off = c.take((size_t)(B + 1) * 8);
   }
   const size_t ws_bytes = c.off;
+  const auto t_alloc = std::chrono::steady_clock::now();
   char* ws = (char*)mem.get(ws_bytes);
+  const auto t_alloced = std::chrono::steady_clock::now();
   if (!ws && ws_bytes) return fail(TB_ERR_OOM, "workspace allocation of %zu bytes failed", ws_bytes);
   Guard ws_guard{&mem, ws};
   TB_CUDA(cudaMemsetAsync(ws, 0, zero_bytes, stream));
@@ -562,6 +654,8 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   const size_t ts_bytes = t_prof >= 2 ? n_pass_total * 64 : 0;
   char* pinned = (char*)t_pinned.get(readback_span + ts_bytes + args_bytes + 64);
   if (!pinned) return fail(TB_ERR_OOM, "pinned host buffer failed");
+  unsigned int* host_flag = (unsigned int*)(pinned + readback_span + ts_bytes + args_bytes);
+  const bool flagged = t_prof < 2;  // profiling reads its stamps through the stream
   unsigned long long* host_ts = (unsigned long long*)(pinned + readback_span);
   PassArgs* host_args = (PassArgs*)(pinned + readback_span + ts_bytes);
   const ReadbackHeader* host_rb0 = (const ReadbackHeader*)(pinned + o_rb_last[0]);
@@ -645,33 +739,95 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       a.out_origins = (int32_t*)(ws + bf.inter[k & 1][0]);
       a.out_masks = (uint64_t*)(ws + bf.inter[k & 1][1]);
       a.out_grid = (int32_t*)(ws + bf.inter[k & 1][2]);
+      if (cl) {  // a member template (see PassArgs)
+        a.member = 1;
+        a.cl = cl;
+        a.unit_off = src.kind == kSrcBatch ? src.batch->leaf_offsets : in_off;
+        a.m_stage = pl.slot_cap / total;
+        a.m_slots = bf.m_slots;
+        a.m_out = bf.m_out[k & 1];
+        a.unit_ctl = ws + pl.unit_ctl;
+        a.ctl_stride = pl.ctl_stride;
+        a.ctl_rb_bytes = ctl_rb_bytes;
+        a.ctl = nullptr;
+        a.first = nullptr;
+        const long long T = slots_per_source(pl.spec), mean = (total + B - 1) / B;
+        const long long want = (mean * a.m_stage + (long long)cl * 256 - 1) / ((long long)cl * 256);
+        a.tchunk = (int32_t)std::max(1ll, std::min({T, want, 32ll}));
+      }
     }
   }
   TB_CUDA(cudaMemcpyAsync(ws + o_args, host_args, args_bytes, cudaMemcpyHostToDevice, stream));
 
   // ---- the cooperative pass kernel
   {
-    ChainArgs ca;
+    ChainArgs ca{};
     ca.pass = (const PassArgs*)(ws + o_args);
     ca.n_chain = n_chain;
     ca.n_stage = n_stage;
     ca.bar = (GridBarrier*)(ws + o_bar);
     ca.err = (unsigned int*)(ws + o_err);
     ca.front = front ? 1 : 0;  // the kernel reads the input's bbox and plans the key itself
-    TB_CUDA(launch(kKChain, stream, [&] { return launch_chain(ca, G, stream); }));
+    if (flagged) {
+      __atomic_store_n(host_flag, 0u, __ATOMIC_RELAXED);
+      ca.host_span = pinned;
+      ca.dev_span = ws;
+      ca.span_bytes = (long long)readback_span;
+      ca.exit_ctr = (unsigned int*)(ws + o_exit);
+      ca.host_flag = host_flag;
+      ca.seq = ++t_seq;
+    }
+    if (cl) {
+      ca.B = B;
+      ca.cl = cl;
+      ca.done = (unsigned int*)(ws + o_done);
+      TB_CUDA(launch(kKMember, stream, [&] { return launch_member(ca, n_chain * B, cl, stream); }));
+    } else {
+      TB_CUDA(launch(kKChain, stream, [&] { return launch_chain(ca, G, stream); }));
+    }
   }
 
-  // ---- the one count readback of the call
-  if (t_prof >= 2) TB_CUDA(cudaMemcpyAsync(host_ts, ws + o_ts, ts_bytes, cudaMemcpyDeviceToHost, stream));
-  TB_CUDA(cudaMemcpyAsync(pinned, ws, readback_span, cudaMemcpyDeviceToHost, stream));
+  // ---- the one count readback of the call: the kernel's copy to pinned
+  // memory, seen through the host flag; else (profiling, or a kernel that
+  // stopped early) through the stream
   const auto t_sync = std::chrono::steady_clock::now();
-  TB_CUDA(cudaStreamSynchronize(stream));
+  if (flagged) {
+    const unsigned int seq = t_seq;
+    bool seen = false;
+    for (unsigned int it = 1;; ++it) {
+      if (__atomic_load_n(host_flag, __ATOMIC_ACQUIRE) == seq) {
+        seen = true;
+        break;
+      }
+      if ((it & 63u) == 0 && cudaStreamQuery(stream) != cudaErrorNotReady) {
+        seen = __atomic_load_n(host_flag, __ATOMIC_ACQUIRE) == seq;
+        break;
+      }
+    }
+    if (!seen) {
+      TB_CUDA(cudaStreamSynchronize(stream));
+      TB_CUDA(cudaMemcpy(pinned, ws, readback_span, cudaMemcpyDeviceToHost));
+    }
+  } else {
+    if (t_prof >= 2) TB_CUDA(cudaMemcpyAsync(host_ts, ws + o_ts, ts_bytes, cudaMemcpyDeviceToHost, stream));
+    TB_CUDA(cudaMemcpyAsync(pinned, ws, readback_span, cudaMemcpyDeviceToHost, stream));
+    TB_CUDA(cudaStreamSynchronize(stream));
+  }
   const auto t_synced = std::chrono::steady_clock::now();
   if (t_prof >= 2) {
-    t_phase_ms[4] += std::chrono::duration<double, std::milli>(t_sync - t_entry).count();
-    t_phase_ms[5] += std::chrono::duration<double, std::milli>(t_synced - t_sync).count();
-    t_phase_n[4] += 1;
-    t_phase_n[5] += 1;
+    t_phase_ms[6] += std::chrono::duration<double, std::milli>(t_sync - t_entry).count();
+    t_phase_ms[7] += std::chrono::duration<double, std::milli>(t_synced - t_sync).count();
+    t_phase_n[6] += 1;
+    t_phase_n[7] += 1;
+    t_phase_ms[9] += std::chrono::duration<double, std::milli>(t_alloc - t_entry).count();
+    t_phase_ms[10] += std::chrono::duration<double, std::milli>(t_alloced - t_alloc).count();
+    t_phase_n[9] += 1;
+    t_phase_n[10] += 1;
+    // kernel entry (the first pass's slot 6, earliest block) to the first emission
+    if (n_pass_total && host_ts[6] && ~host_ts[6] <= ~host_ts[0]) {
+      t_phase_ms[5] += (double)(~host_ts[0] - ~host_ts[6]) * 1e-6;
+      t_phase_n[5] += 1;
+    }
     // phase j of stage k spans, over the chains' passes of the stage, from the
     // latest end of phase j-1 (the earliest start for j = 0) to the latest end
     for (int k = 0; k < n_stage; ++k)
@@ -701,7 +857,7 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       bb[a] = dec_min(host_rb0->bbox_enc[a]);
       bb[3 + a] = dec_max(host_rb0->bbox_enc[3 + a]);
     }
-    st = plan_layouts(plans[0], B, bb, bb[0] > bb[3]);
+    st = plan_layouts(plans[0], B_key, bb, bb[0] > bb[3]);
     if (st != TB_OK) return st;
     if (err & kErrLayout) return fail(TB_ERR_CUDA, "internal: device and host key layouts disagree");
     PassArgs& a0 = host_args[0];
@@ -745,6 +901,7 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     b->build_sources = plans[ch].size() == 1 ? (int64_t)last.in_cap : -1;
     b->build_key_bits = last.K.W;
     b->build_digit_passes = last.P;
+    b->build_member_ctas = cl;
     st = alloc_outputs(b, mem);
     if (st != TB_OK) {
       undo();
@@ -765,16 +922,16 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
     }
   } else {
-    // one writer launch per kMaxWriteTasks chains; the tasks go through
-    // pageable memory, which the driver copies before the call returns
-    std::vector<WriteTask> tasks(n_chain);
+    // one writer launch per kMaxWriteTasks chains, the tasks in its parameter
+    WriteTasks wt;
     for (int c0 = 0; c0 < n_chain; c0 += kMaxWriteTasks) {
       const int nt = std::min(kMaxWriteTasks, n_chain - c0);
       long long quads = 0, leaves_max = B + 1;
+      std::memset(&wt, 0, sizeof wt);
+      wt.n = nt;
       for (int j = 0; j < nt; ++j) {
         const int ch = c0 + j;
-        WriteTask& t = tasks[ch];
-        std::memset(&t, 0, sizeof t);
+        WriteTask& t = wt.t[j];
         t.a = host_args[(size_t)ch * n_stage + plans[ch].size() - 1];
         fill_write_out(made[ch], t.o);
         t.leaves = made[ch]->L;
@@ -783,10 +940,8 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
         quads += t.quads;
         leaves_max = std::max<long long>(leaves_max, quads * 4);
       }
-      WriteTask* dtasks = (WriteTask*)(ws + o_tasks) + c0;
-      TB_CUDA(cudaMemcpyAsync(dtasks, &tasks[c0], sizeof(WriteTask) * nt, cudaMemcpyHostToDevice, stream));
       const int wb = blocks_for(leaves_max, kWriteLeavesPerBlock, (long long)di->sms * di->occ_write_multi);
-      const cudaError_t e = launch(kKWriteMulti, stream, [&] { return launch_write_multi(dtasks, nt, wb, stream); });
+      const cudaError_t e = launch(kKWriteMulti, stream, [&] { return launch_write_multi(wt, wb, stream); });
       if (e != cudaSuccess) {
         undo();
         return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
@@ -795,8 +950,8 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   }
   for (int ch = 0; ch < n_chain; ++ch) outs[ch] = made[ch];
   if (t_prof >= 2) {
-    t_phase_ms[6] += host_ms_since(t_synced);
-    t_phase_n[6] += 1;
+    t_phase_ms[8] += host_ms_since(t_synced);
+    t_phase_n[8] += 1;
   }
   return TB_OK;
 }
@@ -1207,6 +1362,7 @@ tb_status tb_batch_get_view(const tb_batch* b, tb_batch_view* v) {
   v->build_source_leaves = b->build_sources;
   v->build_key_bits = b->build_key_bits;
   v->build_digit_passes = b->build_digit_passes;
+  v->build_member_ctas = b->build_member_ctas;
   v->num_voxels = b->voxel_base_host.empty() ? 0 : b->voxel_base_host.back();
   return TB_OK;
 }
@@ -1289,6 +1445,11 @@ const char* tb_status_string(tb_status s) {
 int32_t tb_version(void) { return 100; }
 
 int64_t tb_kernel_launch_count(void) { return t_launches; }
+
+int32_t tb_set_launch_mode(int32_t mode) {
+  if (mode < 0 || mode > 2) return -1;
+  return g_launch_mode.exchange(mode);
+}
 
 tb_status tb_profile_enable(int32_t on) {
   t_prof = on < 0 ? 0 : on;

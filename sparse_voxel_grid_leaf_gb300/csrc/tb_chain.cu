@@ -74,8 +74,8 @@ union Smem {
 };
 
 // Profiling stamps of the GPU global timer over all blocks: slot 0 holds the
-// earliest block start (as the max of its complement), slot k > 0 the latest
-// block end of phase k.
+// earliest block start (as the max of its complement), slot k in 1..5 the
+// latest block end of phase k, slot 6 the earliest kernel entry (complemented).
 __device__ __forceinline__ void stamp(const PassArgs& a, int k) {
   if (a.phase_ts && threadIdx.x == 0) {
     unsigned long long t;
@@ -1228,9 +1228,9 @@ __device__ __forceinline__ void for_share(const ChainArgs& c, int k, int kind, i
 __device__ void phase_front(const PassArgs& a) {
   int32_t mn[3], mx[3];
   if (a.op == kIjk) {
-    ijk_bounds(a.ijk, a.src_count, mn, mx);
+    ijk_bounds(a.ijk, a.src_count, mn, mx, (int)blockIdx.x, (int)gridDim.x);
   } else {
-    leaves_bounds(a.src_origins, a.src_masks, a.src_count, mn, mx, a.err);
+    leaves_bounds(a.src_origins, a.src_masks, a.src_count, mn, mx, a.err, (int)blockIdx.x, (int)gridDim.x);
   }
   reduce_bbox(mn, mx, a.rb->bbox_enc);
   check_offsets(a.in_offsets, a.B, a.src_count, a.err);
@@ -1267,6 +1267,34 @@ __device__ bool front_plan(const ChainArgs& c, const PassArgs& a, FrontPlan& fp)
   return ok != 0;
 }
 
+// The last CTA out of a pass kernel (`expected` arrivals) copies the call's
+// readback span to pinned host memory, then sets the host flag to the call's
+// sequence number (system-scope fences order the copy before the flag), so
+// the host can take the counts without a stream synchronisation.  A kernel
+// that stops early never sets the flag; the host then falls back to the
+// stream.
+__device__ void publish_readback(const ChainArgs& c, unsigned int expected) {
+  if (!c.host_span) return;
+  __shared__ unsigned int out_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    out_last = atomicAdd(c.exit_ctr, 1u) + 1u == expected ? 1u : 0u;
+    if (out_last) __threadfence();
+  }
+  __syncthreads();
+  if (!out_last) return;
+  const uint4* src = reinterpret_cast<const uint4*>(c.dev_span);
+  uint4* dst = reinterpret_cast<uint4*>(c.host_span);
+  for (long long i = threadIdx.x; i < c.span_bytes / 16; i += blockDim.x) dst[i] = __ldcg(src + i);
+  __threadfence_system();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence_system();
+    *reinterpret_cast<volatile unsigned int*>(c.host_flag) = c.seq;
+  }
+}
+
 // One stage of the launch runs stage k of every chain, phase by phase, the
 // chains of a phase side by side on their shares of the grid.  Stamps:
 // 1 emission, 2 digit passes, 3 index, 4 leaves and voxel offsets.
@@ -1282,6 +1310,12 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
     held.ch = -1;
     held.k = -1;
     fp.valid = 0;
+    unsigned long long* ts = c.pass[0].phase_ts;
+    if (ts) {  // kernel entry, earliest block
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      atomicMax(ts + 6, ~t);
+    }
   }
   if (c.front) {  // one one-pass chain: plan its key from the input's bbox
     load_pass(c, 0, 0, a, held, fp);
@@ -1337,14 +1371,281 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
         __syncthreads();
       }
       dispatch_leaves(pa, sm, vb, vg);
+      stamp(pa, 4);
     });
     grid_sync(c.bar, c.err);
     for_share(c, k, -1, 0, sp, a, held, fp, [&](const PassArgs& pa, int, int vb, int vg) {
       if (pa.last) phase_voxel_offsets(pa, sm, vb, vg);
-      stamp(pa, 4);
+      stamp(pa, 5);
     });
     if (more) grid_sync(c.bar, c.err);
   }
+  publish_readback(c, gridDim.x);
+}
+
+// ---------------------------------------------------------------- member launches
+
+// k_member runs every grid of every chain of a call on its own: member
+// u = ch * B + g, one cluster of `cl` CTAs, takes grid g of chain ch through
+// all of the chain's passes as a batch of one grid (its keys have no grid
+// field) on its share of the chain's buffers.  Phases are separated by
+// cluster barriers and look-backs span the member's own CTAs, so no member
+// waits on another; the last member to finish turns the members' counts into
+// each chain's per-grid offsets and totals, and the writer reads every leaf
+// from its member's share.  This is the launch for batches of small grids,
+// where the whole-grid phases of k_chain are bound by the latency of their
+// barriers and look-backs rather than by their work.
+
+// A barrier over the member's CTAs that also orders their global-memory
+// accesses (release / acquire at cluster scope).
+__device__ __forceinline__ void member_sync(int cl) {
+  __syncthreads();
+  if (cl > 1)
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+struct MemberInfo {
+  long long o0, n;  // the grid's first stage-0 source and its count
+  int ok;
+};
+
+// Stage k of chain ch for grid g: the stage template made the member's own
+// (sources, slot arrays, control block, status words), and the member's
+// control block zeroed by its CTAs.  False in every thread when the grid's
+// source offsets are out of order (flagged in the error word).
+__device__ bool member_args(const ChainArgs& c, int ch, int k, int g, int vb, PassArgs& a, MemberInfo& mi) {
+  __syncthreads();  // the previous stage is done with a
+  const unsigned long long* from = reinterpret_cast<const unsigned long long*>(c.pass + ch * c.n_stage + k);
+  if (threadIdx.x < sizeof(PassArgs) / 8) reinterpret_cast<unsigned long long*>(&a)[threadIdx.x] = __ldg(from + threadIdx.x);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int32_t B = a.B;
+    const long long o0 = __ldg(a.unit_off + g), o1 = __ldg(a.unit_off + g + 1);
+    bool ok = true;
+    if (k == 0) {  // every member checks its own offsets (later stages reuse them)
+      const long long total = a.src_count;
+      ok = o0 >= 0 && o1 >= o0 && o1 <= total && (g > 0 || o0 == 0) && (g + 1 < B || o1 == total);
+      if (!ok && vb == 0) atomicOr(a.err, kErrBadOffsets);
+    }
+    mi.ok = ok ? 1 : 0;
+    const long long n = ok ? o1 - o0 : 0;
+    mi.o0 = o0;
+    mi.n = n;
+    const long long cap = n * a.m_stage;
+    char* blk = a.unit_ctl + (long long)g * a.ctl_stride;
+    a.rb = reinterpret_cast<ReadbackHeader*>(blk);
+    a.leaf_off = reinterpret_cast<int64_t*>(blk + sizeof(ReadbackHeader));
+    a.lower_off = a.leaf_off + 2;
+    a.upper_off = a.lower_off + 2;
+    a.grid_vox = a.upper_off + 2;
+    a.gbox = reinterpret_cast<unsigned int*>(a.grid_vox + 1);
+    a.ctl = reinterpret_cast<PassCtl*>(blk + a.ctl_rb_bytes);
+    a.first = reinterpret_cast<uint32_t*>(blk + a.ctl_stride - 16);
+    a.sort_status += member_first(o0, a.m_stage, kSortTile, a.cl, g) * a.P * kBins;
+    a.sort_tiles_cap = (cap + kSortTile - 1) / kSortTile + a.cl;
+    a.dedup_status += member_first(o0, a.m_stage, kDedupTile, 0, g) * 3;
+    const long long xs = o0 * a.m_slots, xo = o0 * a.m_out;
+    a.keys[0] += xs;
+    a.keys[1] += xs;
+    a.vals[0] += xs;
+    a.vals[1] += xs;
+    a.run_start += xs + g;
+    a.leaf_lower += xs;
+    a.leaf_upper += xs;
+    a.leaf_voff += xs;
+    a.leaf_pop += xs;
+    a.leaf_g += xs;
+    a.blk_agg += (long long)g * a.cl;  // the chain's [B][cl] block and [B][cl][32] group aggregates
+    a.grp_agg += (long long)g * a.cl * (kThreads / 8);
+    a.out_origins += 3 * xo;
+    a.out_masks += 8 * xo;
+    a.out_grid += xo;
+    if (k == 0) {
+      if (a.op == kIjk) {
+        a.ijk += 3 * o0;
+      } else {
+        a.src_origins += 3 * o0;
+        a.src_masks += 8 * o0;
+      }
+      a.src_count = n;
+    } else {  // the member's leaves of the previous stage
+      const PassArgs* p = c.pass + ch * c.n_stage + k - 1;
+      const long long po = o0 * p->m_out;
+      a.src_origins = p->out_origins + 3 * po;
+      a.src_masks = p->out_masks + 8 * po;
+      a.src_count_dev =
+          &reinterpret_cast<const ReadbackHeader*>(p->unit_ctl + (long long)g * p->ctl_stride)->num_leaves;
+    }
+    a.src_grid = nullptr;
+    a.slot_cap = cap;
+    a.B = 1;
+    a.sorted = a.P & 1;
+  }
+  __syncthreads();
+  if (!mi.ok) return false;
+  uint32_t* blk = reinterpret_cast<uint32_t*>(a.rb);
+  const long long words = a.ctl_stride / 4, stride = (long long)a.cl * kThreads;
+  for (long long i = (long long)vb * kThreads + threadIdx.x; i < words; i += stride) blk[i] = 0u;
+  return true;
+}
+
+// The member's status words of the stage's digit passes and index phase,
+// zeroed by its CTAs (after a front end has planned its digit passes).
+__device__ void member_zero_status(const PassArgs& a, int vb) {
+  const long long stride = (long long)a.cl * kThreads, first = (long long)vb * kThreads + threadIdx.x;
+  const long long sw = a.sort_tiles_cap * a.P * kBins;
+  for (long long i = first; i < sw; i += stride) a.sort_status[i] = 0u;
+  const long long dw = 3 * ((a.slot_cap + kDedupTile - 1) / kDedupTile);
+  for (long long i = first; i < dw; i += stride) a.dedup_status[i] = 0ull;
+}
+
+// A front end's member: its grid's voxel bbox, then every CTA plans the
+// member's key from it (a batch of one grid); the chain's bbox (for the
+// host) accumulates the members'.  False in every thread if the key needs
+// more than 64 bits.
+__device__ bool member_front(const ChainArgs& c, PassArgs& a, int vb) {
+  int32_t mn[3], mx[3];
+  if (a.op == kIjk) {
+    ijk_bounds(a.ijk, a.src_count, mn, mx, vb, a.cl);
+  } else {
+    leaves_bounds(a.src_origins, a.src_masks, a.src_count, mn, mx, a.err, vb, a.cl);
+  }
+  reduce_bbox(mn, mx, a.rb->bbox_enc);
+  member_sync(a.cl);
+  __shared__ int ok;
+  if (threadIdx.x == 0) {
+    int32_t bb[6];
+    for (int ax = 0; ax < 3; ++ax) {
+      bb[ax] = dec_min(__ldcg(&a.rb->bbox_enc[ax]));
+      bb[3 + ax] = dec_max(__ldcg(&a.rb->bbox_enc[3 + ax]));
+    }
+    KeyLayout K;
+    const bool good = make_layout(1, bb, bb[0] > bb[3], K);
+    if (good) {
+      a.K = K;
+      a.P = (K.W + 7) / 8;
+      a.sorted = a.P & 1;
+    } else if (vb == 0) {
+      atomicOr(a.err, kErrLayout);
+    }
+    ok = good ? 1 : 0;
+  }
+  if (vb == 0 && threadIdx.x < 6) {
+    const unsigned int e = __ldcg(&a.rb->bbox_enc[threadIdx.x]);
+    if (e) atomicMax(&c.pass[0].rb->bbox_enc[threadIdx.x], e);
+  }
+  __syncthreads();
+  return ok != 0;
+}
+
+// The last member of chain ch: the chain's per-grid leaf / lower / upper
+// offsets (exclusive scans of its members' counts), voxel counts, bboxes and
+// totals.  Counts stay below 2^30, so two of them share a 64-bit scan.
+__device__ void member_epilogue(const ChainArgs& c, int ch, Smem& sm) {
+  unsigned long long* scratch = sm.dedup.scan;
+  const int B = c.B, tid = threadIdx.x;
+  int kl = c.n_stage - 1;
+  while (kl > 0 && c.pass[ch * c.n_stage + kl].op < 0) --kl;
+  const PassArgs* t = c.pass + ch * c.n_stage + kl;
+  const char* ub = t->unit_ctl;
+  const long long st = t->ctl_stride;
+  constexpr unsigned long long lo32 = 0xFFFFFFFFull;
+  unsigned long long carry_a = 0, carry_b = 0;  // (leaves | lowers << 32), (uppers | slots << 32)
+  for (int base = 0; base < B; base += kThreads) {
+    const int g = base + tid;
+    const ReadbackHeader* r = g < B ? reinterpret_cast<const ReadbackHeader*>(ub + (long long)g * st) : nullptr;
+    unsigned long long va = 0, vc = 0;
+    if (r) {
+      va = __ldcg(&r->num_leaves) | (__ldcg(&r->num_lowers) << 32);
+      vc = __ldcg(&r->num_uppers) | (__ldcg(&r->num_slots) << 32);
+    }
+    unsigned long long ta, tc;
+    const unsigned long long ea = carry_a + block_excl_scan_256(va, scratch, &ta);
+    const unsigned long long eb = carry_b + block_excl_scan_256(vc, scratch, &tc);
+    if (r) {
+      t->leaf_off[g] = (int64_t)(ea & lo32);
+      t->lower_off[g] = (int64_t)(ea >> 32);
+      t->upper_off[g] = (int64_t)(eb & lo32);
+      const int64_t* uo = reinterpret_cast<const int64_t*>(r + 1);  // leaf | lower | upper offsets, voxels, bbox
+      t->grid_vox[g] = __ldcg(uo + 6);
+      const unsigned int* ugb = reinterpret_cast<const unsigned int*>(uo + 7);
+#pragma unroll
+      for (int e = 0; e < 6; ++e) t->gbox[6 * g + e] = __ldcg(ugb + e);
+    }
+    carry_a += ta;
+    carry_b += tc;
+  }
+  if (tid == 0) {
+    t->leaf_off[B] = (int64_t)(carry_a & lo32);
+    t->lower_off[B] = (int64_t)(carry_a >> 32);
+    t->upper_off[B] = (int64_t)(carry_b & lo32);
+    t->rb->num_leaves = carry_a & lo32;
+    t->rb->num_lowers = carry_a >> 32;
+    t->rb->num_uppers = carry_b & lo32;
+    t->rb->num_slots = carry_b >> 32;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) k_member(const ChainArgs c) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  __shared__ __align__(16) PassArgs a;
+  __shared__ MemberInfo mi;
+  const int cl = c.cl;
+  const int vb = (int)(blockIdx.x % (unsigned)cl), u = (int)(blockIdx.x / (unsigned)cl);
+  const int ch = u / c.B, g = u % c.B;
+  if (threadIdx.x == 0) {
+    unsigned long long* ts = c.pass[0].phase_ts;
+    if (ts) {  // kernel entry, earliest block
+      unsigned long long t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      atomicMax(ts + 6, ~t);
+    }
+  }
+  for (int k = 0; k < c.n_stage; ++k) {
+    if (c.pass[ch * c.n_stage + k].op < 0) break;
+    if (!member_args(c, ch, k, g, vb, a, mi)) return;
+    member_sync(cl);
+    if (c.front && k == 0 && !member_front(c, a, vb)) return;
+    member_zero_status(a, vb);
+    member_sync(cl);
+    stamp(a, 0);
+    dispatch_emit(a, sm, vb, cl);
+    stamp(a, 1);
+    member_sync(cl);
+    for (int d = 0; d < a.P; ++d) {
+      phase_sort(a, d, sm, vb, cl);
+      member_sync(cl);
+    }
+    stamp(a, 2);
+    phase_index(a, sm, vb, cl);
+    stamp(a, 3);
+    member_sync(cl);
+    if (vb == cl - 1) {
+      phase_finish(a, sm);
+      __syncthreads();
+    }
+    dispatch_leaves(a, sm, vb, cl);
+    stamp(a, 4);
+    member_sync(cl);
+    if (a.last) {
+      phase_voxel_offsets(a, sm, vb, cl);
+      stamp(a, 5);
+      member_sync(cl);
+    }
+  }
+  // the member is done: count it; the chain's last one writes its offsets
+  if (vb != 0) return;
+  __shared__ unsigned int last;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    last = atomicAdd(c.done + ch, 1u) + 1u == (unsigned int)c.B ? 1u : 0u;
+    if (last) __threadfence();
+  }
+  __syncthreads();
+  if (!last) return;
+  member_epilogue(c, ch, sm);
+  publish_readback(c, (unsigned int)c.n_chain);  // the chains' last members
 }
 
 // ---------------------------------------------------------------- final writer
@@ -1368,10 +1669,41 @@ __device__ __forceinline__ void write_grid_arrays(const PassArgs& a, const Write
   }
 }
 
+// A leaf's links to its grid and nodes, each in the lanes that write it.
+struct LeafLinks {
+  long long voff = 0;         // lane 0: voxels before the leaf in its grid
+  uint32_t parent = 0;        // lane 3: its lower node, index within the grid
+  long long lower = 0;        // lane 4: its lower node, index within the batch
+  bool new_lower = false;     // lane 4: the leaf is its lower node's first
+  uint32_t lower_parent = 0;  // lane 4: its upper node, index within the grid
+  long long upper = 0;        // lane 5: its upper node, index within the batch
+  bool new_upper = false;     // lane 5: the leaf is its upper node's first
+};
+
+// Links of leaf u of a whole-batch pass (node indices are the batch's).
+__device__ __forceinline__ LeafLinks links_batch(const PassArgs& a, long long u, uint32_t g, int w) {
+  LeafLinks lk;
+  if (w == 0) lk.voff = a.leaf_voff[u];
+  if (w == 3 || w == 4) {
+    const uint32_t lw = a.leaf_lower[u];
+    lk.parent = (uint32_t)((long long)lw - a.lower_off[g]);
+    lk.lower = lw;
+    lk.new_lower = u == 0 || a.leaf_lower[u - 1] != lw;
+  }
+  if (w == 4 || w == 5) {
+    const uint32_t up = a.leaf_upper[u] & ~kGridFirst;
+    lk.lower_parent = (uint32_t)((long long)up - a.upper_off[g]);
+    lk.upper = up;
+    lk.new_upper = u == 0 || (a.leaf_upper[u - 1] & ~kGridFirst) != up;
+  }
+  return lk;
+}
+
 // The record of leaf u of the calling lane's 8-lane group from its merged
-// mask (lane w holds word w), grid and origin; all 32 lanes of the warp call it.
-__device__ __forceinline__ void write_record(const PassArgs& a, const WriteOut& o, long long u, bool valid,
-                                             uint64_t word, uint32_t g, const int32_t org[3]) {
+// mask (lane w holds word w), grid, origin and links; all 32 lanes of the
+// warp call it.
+__device__ __forceinline__ void write_record(const WriteOut& o, long long u, bool valid, uint64_t word, uint32_t g,
+                                             const int32_t org[3], const LeafLinks& lk) {
   const int lane = threadIdx.x & 31, w = lane & 7;
   const uint32_t pop = __popcll(word);
   uint32_t incl = pop;
@@ -1397,39 +1729,79 @@ __device__ __forceinline__ void write_record(const PassArgs& a, const WriteOut& 
   if (w < 6) o.leaf_bbox[6 * u + w] = oa + ma;
   if (w == 6) o.word_prefix[u] = wp;
   if (w == 7) o.leaf_grid[u] = (int32_t)g;
-  if (w == 0) o.voxel_offset[u] = a.leaf_voff[u];
-  if (w == 3) o.leaf_parent[u] = (int32_t)((long long)a.leaf_lower[u] - a.lower_off[g]);
-  if (w == 4) {
-    const uint32_t lw = a.leaf_lower[u];
-    if (u == 0 || a.leaf_lower[u - 1] != lw) {
+  if (w == 0) o.voxel_offset[u] = lk.voff;
+  if (w == 3) o.leaf_parent[u] = (int32_t)lk.parent;
+  if (w == 4 && lk.new_lower) {
 #pragma unroll
-      for (int c = 0; c < 3; ++c) o.lower_origins[3 * (long long)lw + c] = (int32_t)((uint32_t)org[c] & ~127u);
-      o.lower_parent[lw] = (int32_t)((long long)(a.leaf_upper[u] & ~kGridFirst) - a.upper_off[g]);
-    }
+    for (int c = 0; c < 3; ++c) o.lower_origins[3 * lk.lower + c] = (int32_t)((uint32_t)org[c] & ~127u);
+    o.lower_parent[lk.lower] = (int32_t)lk.lower_parent;
   }
-  if (w == 5) {
-    const uint32_t up = a.leaf_upper[u] & ~kGridFirst;
-    if (u == 0 || (a.leaf_upper[u - 1] & ~kGridFirst) != up) {
+  if (w == 5 && lk.new_upper) {
 #pragma unroll
-      for (int c = 0; c < 3; ++c) o.upper_origins[3 * (long long)up + c] = (int32_t)((uint32_t)org[c] & ~4095u);
-    }
+    for (int c = 0; c < 3; ++c) o.upper_origins[3 * lk.upper + c] = (int32_t)((uint32_t)org[c] & ~4095u);
   }
 }
 
-// Leaf u (< U or not) from the records staged by the leaves phase.
-__device__ __forceinline__ void write_leaf_staged(const PassArgs& a, const WriteOut& o, long long u, long long U) {
+// Leaf u (< U or not) of a member launch's chain: its grid g is the last whose
+// first leaf is at most u, and its record sits in member g's share at the
+// leaf's index within the grid; node indices there are the grid's own.
+__device__ __forceinline__ void write_leaf_member(const PassArgs& a, const WriteOut& o, long long u, long long U) {
   const int w = threadIdx.x & 7;
   const bool valid = u < U;
   uint32_t g = 0;
   int32_t org[3] = {0, 0, 0};
   uint64_t word = 0;
+  LeafLinks lk;
+  if (valid) {
+    int lo = 0, hi = a.B;  // leaf_off comes from an earlier kernel: read-only cached loads see it
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(a.leaf_off + mid) <= u) lo = mid; else hi = mid;
+    }
+    g = (uint32_t)lo;
+    const long long ul = u - __ldg(a.leaf_off + g);
+    const long long o0 = __ldg(a.unit_off + g);
+    const long long xs = o0 * a.m_slots + ul, xo = o0 * a.m_out + ul;
+    word = __ldcg(a.out_masks + 8 * xo + w);
+#pragma unroll
+    for (int c = 0; c < 3; ++c) org[c] = __ldcg(a.out_origins + 3 * xo + c);
+    if (w == 0) lk.voff = __ldcg(a.leaf_voff + xs);
+    if (w == 3 || w == 4) {
+      const uint32_t lw = __ldcg(a.leaf_lower + xs);
+      lk.parent = lw;
+      lk.lower = __ldg(a.lower_off + g) + lw;
+      lk.new_lower = ul == 0 || __ldcg(a.leaf_lower + xs - 1) != lw;
+    }
+    if (w == 4 || w == 5) {
+      const uint32_t up = __ldcg(a.leaf_upper + xs) & ~kGridFirst;
+      lk.lower_parent = up;
+      lk.upper = __ldg(a.upper_off + g) + up;
+      lk.new_upper = ul == 0 || (__ldcg(a.leaf_upper + xs - 1) & ~kGridFirst) != up;
+    }
+  }
+  write_record(o, u, valid, word, g, org, lk);
+}
+
+// Leaf u (< U or not) from the records staged by the leaves phase.
+__device__ __forceinline__ void write_leaf_staged(const PassArgs& a, const WriteOut& o, long long u, long long U) {
+  if (a.member) {
+    write_leaf_member(a, o, u, U);
+    return;
+  }
+  const int w = threadIdx.x & 7;
+  const bool valid = u < U;
+  uint32_t g = 0;
+  int32_t org[3] = {0, 0, 0};
+  uint64_t word = 0;
+  LeafLinks lk;
   if (valid) {
     word = __ldcg(a.out_masks + 8 * u + w);
     g = __ldcg(a.leaf_g + u);
 #pragma unroll
     for (int c = 0; c < 3; ++c) org[c] = __ldcg(a.out_origins + 3 * u + c);
+    lk = links_batch(a, u, g, w);
   }
-  write_record(a, o, u, valid, word, g, org);
+  write_record(o, u, valid, word, g, org, lk);
 }
 
 // Leaf u of a pass: from the staged records when there are any, else by
@@ -1454,7 +1826,9 @@ __device__ __forceinline__ void write_leaf(const PassArgs& a, const WriteOut& o,
     for (int c = 0; c < 3; ++c) org[c] = (int32_t)((uint32_t)lc[c] << 3);
   }
   const uint64_t word = merge_run<OP>(a, vals, s0, s1, w);
-  write_record(a, o, u, valid, word, g, org);
+  LeafLinks lk;
+  if (valid) lk = links_batch(a, u, g, w);
+  write_record(o, u, valid, word, g, org, lk);
 }
 
 template <int OP>
@@ -1469,15 +1843,12 @@ __global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, cons
 }
 
 // The writers of several chains in one launch, from the records their leaves
-// phases staged.  Tasks (one per chain, up to kMaxWriteTasks) are held in
-// shared memory; the leaves of all chains form one index space in units of 4
-// leaves, so a warp's 4 groups always belong to one chain.
-__global__ void __launch_bounds__(kThreads) k_write_multi(const WriteTask* tasks, int n_task) {
-  __shared__ __align__(16) WriteTask t[kMaxWriteTasks];
-  static_assert(sizeof(WriteTask) % 8 == 0, "task copy");
-  for (int i = threadIdx.x; i < n_task * (int)(sizeof(WriteTask) / 8); i += kThreads)
-    reinterpret_cast<unsigned long long*>(t)[i] = __ldg(reinterpret_cast<const unsigned long long*>(tasks) + i);
-  __syncthreads();
+// phases staged.  Tasks (one per chain, up to kMaxWriteTasks) come as one
+// kernel parameter; the leaves of all chains form one index space in units of
+// 4 leaves, so a warp's 4 groups always belong to one chain.
+__global__ void __launch_bounds__(kThreads) k_write_multi(const __grid_constant__ WriteTasks wt) {
+  const WriteTask* t = wt.t;  // read in place: the lanes of a warp read the same task
+  const int n_task = wt.n;
   const int tid = threadIdx.x, lane = tid & 31;
   const int B = t[0].a.B;
   const long long gtid = (long long)blockIdx.x * kThreads + tid, nthreads = (long long)gridDim.x * kThreads;
@@ -1517,6 +1888,30 @@ cudaError_t launch_chain(const ChainArgs& c, int blocks, cudaStream_t s) {
   return cudaLaunchCooperativeKernel((const void*)k_chain, dim3(blocks), dim3(kThreads), args, sizeof(Smem), s);
 }
 
+int member_occupancy() {
+  int n = 0;
+  if (cudaFuncSetAttribute(k_member, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(Smem)) != cudaSuccess)
+    return 1;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k_member, kThreads, sizeof(Smem)) != cudaSuccess) n = 1;
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch_member(const ChainArgs& c, int members, int cl, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(members * cl));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sizeof(Smem);
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)cl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = cl > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, k_member, c);
+}
+
 int write_final_occupancy(int op) {
   switch (op) {
     case kIjk: return write_occupancy<kIjk>();
@@ -1534,8 +1929,8 @@ int write_multi_occupancy() {
   return n > 0 ? n : 1;
 }
 
-cudaError_t launch_write_multi(const WriteTask* tasks, int n_task, int blocks, cudaStream_t s) {
-  k_write_multi<<<blocks, kThreads, 0, s>>>(tasks, n_task);
+cudaError_t launch_write_multi(const WriteTasks& tasks, int blocks, cudaStream_t s) {
+  k_write_multi<<<blocks, kThreads, 0, s>>>(tasks);
   return cudaGetLastError();
 }
 

@@ -158,6 +158,19 @@ struct PassArgs {
   int32_t* out_origins;
   uint64_t* out_masks;
   int32_t* out_grid;
+  // member launches (k_member): every grid of a chain runs as its own batch of
+  // one grid on its share of the chain's buffers.  In a member template the
+  // buffer pointers above are the chain's bases, and B, rb and the per-grid
+  // arrays are the chain's; the kernel derives each member's arguments.
+  int32_t member;            // 1: a member template
+  int32_t cl;                // CTAs per member (one cluster)
+  const int64_t* unit_off;   // [B+1] first stage-0 source (leaf or voxel) of each grid
+  long long m_stage;         // slots of this stage per stage-0 source (capacity)
+  long long m_slots;         // slot-array capacity of the chain per stage-0 source
+  long long m_out;           // out-array capacity of this stage per stage-0 source
+  char* unit_ctl;            // this stage's member control blocks, ctl_stride bytes apart
+  long long ctl_stride;      // readback part | PassCtl (P histogram rows) | first[3]
+  long long ctl_rb_bytes;    // bytes of the readback part
 };
 
 // Arguments of one cooperative launch: n_chain chains of up to n_stage
@@ -173,6 +186,20 @@ struct ChainArgs {
   GridBarrier* bar;
   unsigned int* err;
   int32_t front;
+  // member launches: B grids per chain, cl CTAs per member, and the
+  // finished members of each chain (zeroed)
+  int32_t B;
+  int32_t cl;
+  unsigned int* done;  // [n_chain]
+  // the readback without a stream synchronisation: the last CTA out copies
+  // the readback span (span_bytes, a multiple of 16, from dev_span) to pinned
+  // host memory and then stores `seq` to the host flag; null host_span: off
+  char* host_span;
+  const char* dev_span;
+  long long span_bytes;
+  unsigned int* exit_ctr;  // zeroed
+  unsigned int* host_flag;
+  unsigned int seq;
 };
 
 
@@ -244,6 +271,11 @@ struct WriteTask {
   long long leaves;     // output leaves of the chain
   long long quad_base;  // first 4-leaf unit of the chain in the launch's index space
   long long quads;      // its 4-leaf units
+};
+// The tasks of one writer launch, passed by value as its kernel parameter.
+struct WriteTasks {
+  WriteTask t[kMaxWriteTasks];
+  int32_t n;
 };
 
 #ifdef __CUDACC__
@@ -664,14 +696,16 @@ __device__ __forceinline__ void check_offsets(const int64_t* off, int32_t B, lon
   }
 }
 
-// This thread's share (grid-stride) of the bounds of N voxel coordinates.
-__device__ __forceinline__ void ijk_bounds(const int32_t* ijk, long long N, int32_t mn[3], int32_t mx[3]) {
+// This thread's share (stride over the vg blocks of a virtual grid) of the
+// bounds of N voxel coordinates.
+__device__ __forceinline__ void ijk_bounds(const int32_t* ijk, long long N, int32_t mn[3], int32_t mx[3], int vb,
+                                           int vg) {
   for (int a = 0; a < 3; ++a) {
     mn[a] = INT32_MAX;
     mx[a] = INT32_MIN;
   }
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < N; i += stride)
+  const long long stride = (long long)vg * blockDim.x;
+  for (long long i = (long long)vb * blockDim.x + threadIdx.x; i < N; i += stride)
 #pragma unroll
     for (int a = 0; a < 3; ++a) {
       const int32_t v = __ldg(ijk + 3 * i + a);
@@ -680,16 +714,17 @@ __device__ __forceinline__ void ijk_bounds(const int32_t* ijk, long long N, int3
     }
 }
 
-// This thread's share of the exact voxel bounds of L leaves (from their set
-// bits); flags origins that are not multiples of 8.
+// This thread's share (over a virtual grid, as ijk_bounds) of the exact voxel
+// bounds of L leaves (from their set bits); flags origins that are not
+// multiples of 8.
 __device__ __forceinline__ void leaves_bounds(const int32_t* origins, const uint64_t* masks, long long L,
-                                              int32_t mn[3], int32_t mx[3], unsigned int* err) {
+                                              int32_t mn[3], int32_t mx[3], unsigned int* err, int vb, int vg) {
   for (int a = 0; a < 3; ++a) {
     mn[a] = INT32_MAX;
     mx[a] = INT32_MIN;
   }
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < L; i += stride) {
+  const long long stride = (long long)vg * blockDim.x;
+  for (long long i = (long long)vb * blockDim.x + threadIdx.x; i < L; i += stride) {
     uint64_t m[8];
     load_mask(masks, i, m);
     uint64_t all = 0;

@@ -81,10 +81,14 @@ cudaError_t launch_validate(const int32_t* origins, const uint64_t* masks, const
 size_t chain_smem_bytes();
 int chain_occupancy();
 cudaError_t launch_chain(const ChainArgs& c, int blocks, cudaStream_t s);
+// The member launch: one cluster of `cl` CTAs (1, 2, 4 or 8) per grid of
+// every chain (`members` = chains x grids), nothing co-resident required.
+int member_occupancy();
+cudaError_t launch_member(const ChainArgs& c, int members, int cl, cudaStream_t s);
 int write_final_occupancy(int op);
 cudaError_t launch_write_final(int op, const PassArgs& a, const WriteOut& o, int blocks, cudaStream_t s);
 int write_multi_occupancy();
-cudaError_t launch_write_multi(const WriteTask* tasks, int n_task, int blocks, cudaStream_t s);
+cudaError_t launch_write_multi(const WriteTasks& tasks, int blocks, cudaStream_t s);
 
 // Sets the calling thread's tb_last_error() message.
 void set_error_message(const char* msg);

@@ -133,4 +133,14 @@ TB_HD inline bool make_layout(int32_t B, const int32_t bb[6], bool empty, KeyLay
   return K.W <= 64;
 }
 
+// Member launches carve a chain's per-member arrays from the grids' stage-0
+// source offsets: member g owns units [member_first(off[g], ...),
+// member_first(off[g + 1], ...)) of an array where it needs
+// ceil((off[g + 1] - off[g]) m / d) + e units.  The range always holds them:
+// floor((x + y) / d) - floor(x / d) >= ceil(y / d) - 1, and each member adds
+// e + 1 units.  member_first(total, m, d, e, B) is the array's size.
+TB_HD inline long long member_first(long long off_g, long long m, long long d, long long e, long long g) {
+  return (off_g * m) / d + g * (e + 1);
+}
+
 }  // namespace tb

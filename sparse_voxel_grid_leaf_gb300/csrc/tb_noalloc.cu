@@ -192,7 +192,7 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   // ---- the same cooperative pass kernel as tb_refine
   // the pass arguments go to the scratch array from host stack memory
   TB_STATIC_CUDA(cudaMemcpyAsync(scratch + o_args, &a, sizeof a, cudaMemcpyHostToDevice, stream));
-  ChainArgs ca;
+  ChainArgs ca{};
   ca.pass = (const PassArgs*)(scratch + o_args);
   ca.n_chain = 1;
   ca.n_stage = 1;

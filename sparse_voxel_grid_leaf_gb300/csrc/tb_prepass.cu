@@ -18,7 +18,7 @@ __global__ void __launch_bounds__(256) k_prepass_leaves(const int32_t* origins, 
                                                         long long L, const int64_t* off, int32_t B,
                                                         ReadbackHeader* rb) {
   int32_t mn[3], mx[3];
-  leaves_bounds(origins, masks, L, mn, mx, &rb->err);
+  leaves_bounds(origins, masks, L, mn, mx, &rb->err, (int)blockIdx.x, (int)gridDim.x);
   reduce_bbox(mn, mx, rb->bbox_enc);
   check_offsets(off, B, L, &rb->err);
 }

@@ -58,6 +58,16 @@ def _built():
     __graft_entry__.build()
 
 
+@pytest.fixture(scope="module", autouse=True, params=["grid", "member"])
+def launch_mode(request, _built):
+    """Every test runs with both launch shapes of the pass kernel: the
+    whole-grid cooperative kernel and the member launch (one cluster per grid
+    of every chain), forced for every input."""
+    prev = tb.set_launch_mode(request.param)
+    yield request.param
+    tb.set_launch_mode(prev)
+
+
 # ------------------------------------------------------------- small exact cases
 
 def test_pr1_from_ijk_then_refine():
@@ -263,6 +273,25 @@ def test_deterministic_repeat():
     first = tb.box_dilate(b).to_numpy()
     for _ in range(3):
         assert_same(tb.box_dilate(b).to_numpy(), first, "repeat")
+
+
+def test_auto_launch_shape():
+    """The default picks a member launch for a batch of small grids; the
+    outputs equal the whole-grid kernel's."""
+    prev = tb.set_launch_mode("auto")
+    try:
+        ijk, off = synth.make("shells_b16_res64")
+        tb.profile_read()
+        tb.profile_enable(1)
+        b = tb.from_ijk(dev(ijk), dev(off))
+        small = tb.refine(b).to_numpy()
+        names = tb.profile_read()
+        assert "member" in names and "chain" not in names, names
+        tb.set_launch_mode("grid")
+        assert_same(small, tb.refine(b).to_numpy(), "auto vs grid")
+    finally:
+        tb.profile_enable(0)
+        tb.set_launch_mode(prev)
 
 
 def test_launches_are_counted():
