@@ -472,20 +472,41 @@ __device__ __forceinline__ uint64_t merge_run(const PassArgs& a, const uint32_t*
     // lane w builds target word w: along x, the fine positions 8 tx + w - d
     // (d in [lo, hi]) inside the refined 16^3 block, i.e. source words
     // (8 tx + w - d) / 2; along y and z, the child quadrants (cy, cz) whose
-    // dilation reaches the target, each refined and dilated as a plane
+    // dilation reaches the target, each refined and dilated as a plane.
+    // The run's slot values come 8 at a time (lane w holds slot 8 j + w) and
+    // the next slot's source words are loaded while this slot's are combined.
     const int cb = a.code_bits;
-    uint64_t word = 0;
-    for (uint32_t s = s0; s < s1; ++s) {
-      const uint32_t val = __ldcg(vals + s);
+    const uint32_t gmask = 0xFFu << (threadIdx.x & 24u);  // this lane's group of 8
+    auto xword = [&](uint32_t val) {  // lane w's x-dilated source word of a slot
       const long long src = (long long)(val >> cb);
-      const int code = (int)(val & 63u);
-      const int tx = (code >> 4) - 1, ty = ((code >> 2) & 3) - 1, tz = (code & 3) - 1;
+      const int tx = (int)((val & 63u) >> 4) - 1;
       uint64_t mx = 0;
       for (int d = a.lo[0]; d <= a.hi[0]; ++d) {
         const int fx = 8 * tx + w - d;
         if (fx >= 0 && fx < 16) mx |= __ldcg(a.src_masks + 8 * src + (fx >> 1));
       }
+      return mx;
+    };
+    uint64_t word = 0;
+    const uint32_t n = s1 - s0;
+    uint32_t vcache = 0, val_next = 0;
+    uint64_t mx_next = 0;
+    if (n) {
+      vcache = __ldcg(vals + s0 + min((uint32_t)w, n - 1u));
+      val_next = __shfl_sync(gmask, vcache, 0, 8);
+      mx_next = xword(val_next);
+    }
+    for (uint32_t i = 0; i < n; ++i) {
+      const uint32_t val = val_next;
+      const uint64_t mx = mx_next;
+      if (i + 1 < n) {
+        if (((i + 1) & 7u) == 0) vcache = __ldcg(vals + s0 + i + 1 + min((uint32_t)w, n - i - 2u));
+        val_next = __shfl_sync(gmask, vcache, (int)((i + 1) & 7u), 8);
+        mx_next = xword(val_next);
+      }
       if (!mx) continue;
+      const int code = (int)(val & 63u);
+      const int ty = ((code >> 2) & 3) - 1, tz = (code & 3) - 1;
 #pragma unroll
       for (int cy = 0; cy < 2; ++cy) {
         const int dy = ty - cy;
@@ -494,6 +515,7 @@ __device__ __forceinline__ uint64_t merge_run(const PassArgs& a, const uint32_t*
         for (int cz = 0; cz < 2; ++cz) {
           const int dz = tz - cz;
           if (dz < -1 || dz > 1 || (dz < 0 && a.lo[2] >= 0) || (dz > 0 && a.hi[2] <= 0)) continue;
+          if (!(mx & (0x0F0F0F0Full << (32 * cy + 4 * cz)))) continue;  // an empty quadrant adds nothing
           word |= dilate_y1(dilate_z1(refine_word(mx, cy, cz), dz, a.lo[2], a.hi[2]), dy, a.lo[1], a.hi[1]);
         }
       }
