@@ -146,6 +146,7 @@ struct DeviceInfo {
   int sms = 0;
   int occ_chain = 1;
   int occ_member = 1;
+  int member_fit[4] = {};  // clusters of 1, 2, 4, 8 CTAs of the member kernel the device runs at once
   int occ_write[kNumOps] = {};
   int occ_write_multi = 1;
   bool coop = false;
@@ -166,6 +167,7 @@ tb_status device_info(int dev, DeviceInfo** out) {
     d.coop = true;
     d.occ_chain = chain_occupancy();
     d.occ_member = member_occupancy();
+    for (int i = 0; i < 4; ++i) d.member_fit[i] = i ? member_clusters(1 << i) : d.sms * d.occ_member;
     for (int op = 0; op < kNumOps; ++op) d.occ_write[op] = write_final_occupancy(op);
     d.occ_write_multi = write_multi_occupancy();
     // keep freed memory in the default pool between calls
@@ -292,16 +294,20 @@ constexpr long long kMemberVoxelsPerCta = 16384;      // front ends: input voxel
 constexpr int32_t kMemberMaxGrids = 4096;             // the last member scans its chain's grid counts alone
 
 // CTAs per member of a member launch (1, 2, 4 or 8: the most whose clusters
-// all fit on the device at once), or 0 for the whole-grid kernel.  `nmax` is
+// the device runs all at once, `fit[log2 cl]`), or 0 for the whole-grid
+// kernel.  `nmax` is
 // the most stage-0 sources of one grid (-1: not known on the host), `mmax`
 // the largest slot capacity per stage-0 source of any pass, `heavy` whether a
 // pass is the fused refine-then-dilate.
-int member_ctas(int n_chain, int32_t B, long long count, long long nmax, long long mmax, long long resident,
+int member_ctas(int n_chain, int32_t B, long long count, long long nmax, long long mmax, const int fit[4],
                 bool front, bool heavy) {
   const int mode = g_launch_mode.load();
   if (mode == 1 || B < 1 || count <= 0) return 0;
-  int cl = 8;
-  while (cl > 1 && (long long)n_chain * B * cl > resident) cl >>= 1;
+  int cl = 8, lg = 3;
+  while (cl > 1 && (long long)n_chain * B > (long long)fit[lg]) {
+    cl >>= 1;
+    --lg;
+  }
   if (mode == 2) return cl;
   if (B > kMemberMaxGrids || n_chain > 1 || heavy) return 0;
   const long long n = nmax >= 0 ? nmax : 2 * ((count + B - 1) / B);  // unknown: twice the mean
@@ -506,7 +512,7 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
         if (src.count > 0) mmax = std::max(mmax, pl.slot_cap / src.count);
         heavy |= pl.spec.op == kRefineDilate;
       }
-    cl = member_ctas(n_chain, B, src.count, nmax, mmax, (long long)di->sms * di->occ_member, front, heavy);
+    cl = member_ctas(n_chain, B, src.count, nmax, mmax, di->member_fit, front, heavy);
   }
   const int32_t B_key = cl ? 1 : B;  // a member's keys have no grid field
 

@@ -84,6 +84,7 @@ cudaError_t launch_chain(const ChainArgs& c, int blocks, cudaStream_t s);
 // The member launch: one cluster of `cl` CTAs (1, 2, 4 or 8) per grid of
 // every chain (`members` = chains x grids), nothing co-resident required.
 int member_occupancy();
+int member_clusters(int cl);
 cudaError_t launch_member(const ChainArgs& c, int members, int cl, cudaStream_t s);
 int write_final_occupancy(int op);
 cudaError_t launch_write_final(int op, const PassArgs& a, const WriteOut& o, int blocks, cudaStream_t s);
