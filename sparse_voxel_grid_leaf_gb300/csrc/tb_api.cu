@@ -1228,7 +1228,37 @@ tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t l
   const size_t nb = (size_t)(in->B + 1) * 8;
   unsigned long long cap = 64;
   while (cap < 2ull * (unsigned long long)in->L) cap <<= 1;
-  char* ws = (char*)mem.get(2 * nb + cap * 4);
+  // input leaves one output leaf's reach spans along an axis: origins are
+  // multiples of 8, so eight residues of the origin cover every leaf
+  int span = 0;
+  for (int a = 0; a < 3; ++a)
+    for (long long o = 0; o < 64; o += 8) {
+      const int sh = stride == 2 ? 1 : 0;
+      long long qlo, qhi;
+      if (transposed) {
+        qlo = floor_div(o - hi[a] + (1 << sh) - 1, 1ll << sh);
+        qhi = floor_div(o + 7 - lo[a], 1ll << sh);
+      } else {
+        qlo = (o << sh) + lo[a];
+        qhi = ((o + 7) << sh) + hi[a];
+      }
+      span = std::max(span, (int)(floor_div(qhi, 8) - floor_div(qlo, 8) + 1));
+    }
+  const bool staged = span <= 3 && K <= kKmapStagedColumns;
+  // the tabulated reach (stride 1 or transposed): the same extents for every leaf
+  long long halo = 1;
+  for (int a = 0; a < 3; ++a)
+    halo *= transposed ? floor_div(7 - lo[a], stride) + floor_div(hi[a], stride) + 1 : 8 + hi[a] - lo[a];
+  // measured on GB300: the tabulated map wins where leaves are few and
+  // dense (B = 16, 48 shells); with hundreds of thousands of sparse leaves
+  // (the stress batch) each leaf's halo costs more than its entries, and the
+  // staged map with its candidate look-ups in a kernel of their own wins
+  const bool large = out->L >= kKmapLargeLeaves;
+  const bool tabulated = staged && !large && (stride == 1 || transposed) && halo <= kKmapHaloMax;
+  const long long cand_max = (long long)span * span * span;
+  const bool prepass = staged && large;
+  const size_t cand_bytes = prepass ? (size_t)(out->L * cand_max) * 4 : 0;
+  char* ws = (char*)mem.get(2 * nb + cap * 4 + cand_bytes);
   if (!ws) return fail(TB_ERR_OOM, "tb_kernel_map: workspace");
   Guard g{&mem, ws};
   int32_t* table = (int32_t*)(ws + 2 * nb);
@@ -1264,8 +1294,21 @@ tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t l
   k.stride = stride;
   k.transposed = transposed ? 1 : 0;
   k.map = map;
+  k.cands = prepass ? (int32_t*)(ws + 2 * nb + cap * 4) : nullptr;
+  k.cand_max = (int32_t)cand_max;
   const int blocks = blocks_for(out->L, 8, (long long)di->sms * 8);
-  TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap(k, blocks, s); }));
+  if (prepass) {
+    const int cb = blocks_for(out->L * cand_max, 256, (long long)di->sms * 8);
+    TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap_cands(k, cb, s); }));
+  }
+  if (tabulated) {
+    const int hb = blocks_for(out->L, 4, (long long)di->sms * 7);
+    TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap_halo(k, hb, s); }));
+  } else if (staged) {
+    TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap_staged(k, blocks, s); }));
+  } else {
+    TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap(k, blocks, s); }));
+  }
   return TB_OK;
 }
 

@@ -188,6 +188,309 @@ __global__ void __launch_bounds__(kKmapThreads, 4) k_kmap(const KmapArgs k) {
   }
 }
 
+// The same map for boxes whose reach from an output leaf spans at most 3
+// input leaves per axis (27 candidates; the host checks): the candidates'
+// mask words and the first voxel index of each word are staged in shared
+// memory, each active output voxel's position is packed once as three bytes
+// (its coordinate relative to the first candidate leaf, minus the column's
+// part), and each column's offset likewise, so an entry costs a byte-wise
+// add, one shared-memory word, a bit test and a popcount.  Coordinates
+// relative to the first candidate leaf's origin Q_b: stride 1 q = o + p + d,
+// so o - Q_b + p + d; forward stride 2, 2o - Q_b + 2p + d; transposed
+// stride 1, o - Q_b + p - d; transposed stride 2 (p - d even),
+// o/2 - Q_b + floor(p/2) - floor(d/2).
+constexpr int kStagedCand = 27;
+
+// The first and count of the input leaves along one axis that an output leaf
+// at voxel coordinate o reaches (leaf coordinates).
+__device__ __forceinline__ void reach(const KmapArgs& k, int ax, long long o, long long& a, int& n) {
+  const int sh = k.stride == 2 ? 1 : 0;
+  long long qlo, qhi;
+  if (k.transposed) {
+    qlo = (o - k.hi[ax] + (1 << sh) - 1) >> sh;  // ceil((o - hi) / s)
+    qhi = (o + 7 - k.lo[ax]) >> sh;
+  } else {
+    qlo = (o << sh) + k.lo[ax];
+    qhi = ((o + 7) << sh) + k.hi[ax];
+  }
+  a = qlo >> 3;
+  n = (int)((qhi >> 3) - a + 1);
+}
+
+// Candidate input leaves of every output leaf, one thread per (leaf,
+// candidate): the hash look-ups of all leaves run side by side here, so the
+// map kernel starts each leaf from one coalesced load.
+__global__ void __launch_bounds__(256) k_kmap_cands(const KmapArgs k) {
+  const long long total = k.L_out * k.cand_max;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+    const long long u = i / k.cand_max;
+    const int c = (int)(i - u * k.cand_max);
+    long long a[3];
+    int n[3];
+#pragma unroll
+    for (int ax = 0; ax < 3; ++ax) reach(k, ax, __ldg(k.out_origins + 3 * u + ax), a[ax], n[ax]);
+    int32_t ci = -1;
+    if (c < n[0] * n[1] * n[2]) {
+      const int n12 = n[1] * n[2];
+      ci = find_leaf(k, __ldg(k.out_grid + u), a[0] + c / n12, a[1] + (c / n[2]) % n[1], a[2] + c % n[2]);
+    }
+    k.cands[i] = ci;
+  }
+}
+constexpr int kStagedWarps = 8;
+struct KmapWarp {
+  uint64_t mask[kStagedCand * 8];  // word w of candidate c at 8 c + w (0: no candidate)
+  int32_t base[kStagedCand * 8];   // first voxel index of that word
+  int32_t cand[kStagedCand];
+  uint32_t vpk[512];               // per active voxel: 3 relative-coordinate bytes | parity << 24
+};
+
+__global__ void __launch_bounds__(kStagedWarps * 32, 4) k_kmap_staged(const KmapArgs k) {
+  __shared__ KmapWarp sw[kStagedWarps];
+  __shared__ uint32_t dpk[kKmapTab];  // per column: 3 offset bytes (biased by 8) | parity << 24
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  KmapWarp& W = sw[wib];
+  const long long nwarps = (long long)gridDim.x * kStagedWarps;
+  const int nb1 = k.hi[1] - k.lo[1] + 1, nb2 = k.hi[2] - k.lo[2] + 1;
+  const int K = (k.hi[0] - k.lo[0] + 1) * nb1 * nb2;
+  const int sh = k.stride == 2 ? 1 : 0, tr = k.transposed;
+  for (int i = threadIdx.x; i < K; i += kStagedWarps * 32) {
+    const int d[3] = {k.lo[0] + i / (nb1 * nb2), k.lo[1] + (i / nb2) % nb1, k.lo[2] + i % nb2};
+    uint32_t v = 0, par = 0;
+#pragma unroll
+    for (int ax = 0; ax < 3; ++ax) {
+      const int gv = tr ? -(d[ax] >> sh) : d[ax];
+      v |= (uint32_t)(gv + 8) << (8 * ax);
+      if (tr && sh) par |= (uint32_t)(d[ax] & 1) << (2 - ax);
+    }
+    dpk[i] = v | (par << 24);
+  }
+  __syncthreads();
+  for (long long u = (long long)blockIdx.x * kStagedWarps + wib; u < k.L_out; u += nwarps) {
+    const int32_t g = __ldg(k.out_grid + u);
+    long long a[3];
+    int n[3], A[3];
+#pragma unroll
+    for (int ax = 0; ax < 3; ++ax) {
+      const long long o = __ldg(k.out_origins + 3 * u + ax);
+      reach(k, ax, o, a[ax], n[ax]);
+      A[ax] = (int)((tr ? (o >> sh) : (o << sh)) - (a[ax] << 3));
+    }
+    const int n12 = n[1] * n[2], C = n[0] * n12;
+    if (k.cands) {
+      if (lane < C) W.cand[lane] = __ldcg(k.cands + u * k.cand_max + lane);
+    } else {
+      for (int c = lane; c < C; c += 32)
+        W.cand[c] = find_leaf(k, g, a[0] + c / n12, a[1] + (c / n[2]) % n[1], a[2] + c % n[2]);
+    }
+    __syncwarp();
+    const long long vin = __ldg(k.in_vbase + g);
+    for (int j = lane; j < 8 * C; j += 32) {
+      const int ci = W.cand[j >> 3], w = j & 7;
+      uint64_t m = 0;
+      int32_t b = -1;
+      if (ci >= 0) {
+        m = __ldg(k.in_masks + 8 * (long long)ci + w);
+        const uint64_t wp = __ldg(k.in_wp + ci);
+        const long long before = w ? (long long)((wp >> (9 * (w - 1))) & 511ull) : 0ll;
+        b = (int32_t)(vin + __ldg(k.in_voff + ci) + before);
+      }
+      W.mask[j] = m;
+      W.base[j] = b;
+    }
+    // the output leaf's active voxels in order (lane l lists bits 16 l .. 16 l + 15)
+    const uint32_t chunk = (uint32_t)(__ldg(k.out_masks + 8 * u + (lane >> 2)) >> (16 * (lane & 3))) & 0xFFFFu;
+    const uint32_t cnt = __popc(chunk);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    const uint32_t nvox = __shfl_sync(0xffffffffu, incl, 31);
+    uint32_t pos = incl - cnt, rest = chunk;
+    while (rest) {
+      const int bn = 16 * lane + __ffs(rest) - 1;
+      rest &= rest - 1;
+      const int p[3] = {bn >> 6, (bn >> 3) & 7, bn & 7};
+      uint32_t v = 0, par = 0;
+#pragma unroll
+      for (int ax = 0; ax < 3; ++ax) {
+        const int f = tr ? (p[ax] >> sh) : (p[ax] << sh);
+        v |= (uint32_t)(A[ax] + f) << (8 * ax);
+        if (tr && sh) par |= (uint32_t)(p[ax] & 1) << (2 - ax);
+      }
+      W.vpk[pos++] = v | (par << 24);
+    }
+    __syncwarp();
+    const long long j0 = __ldg(k.out_vbase + g) + __ldg(k.out_voff + u);
+    const long long E = (long long)nvox * K;
+    int32_t* row = k.map + j0 * K;
+    int r = lane / K, kk = lane % K;
+    const int step_r = 32 / K, step_k = 32 % K;
+    for (long long e = lane; e < E; e += 32) {
+      const uint32_t vp = W.vpk[r], dp = dpk[kk];
+      int32_t idx = -1;
+      if ((vp >> 24) == (dp >> 24)) {  // transposed stride 2: p - d even on every axis
+        const uint32_t rel = (vp & 0xFFFFFFu) + (dp & 0xFFFFFFu) - 0x080808u;
+        const uint32_t rx = rel & 0xFFu, ry = (rel >> 8) & 0xFFu, rz = (rel >> 16) & 0xFFu;
+        const int slot = (int)(((rx >> 3) * n12 + (ry >> 3) * n[2] + (rz >> 3)) * 8 + (rx & 7u));
+        const uint64_t word = W.mask[slot];
+        const uint32_t bit = ((ry & 7u) << 3) | (rz & 7u);
+        if ((word >> bit) & 1ull) idx = W.base[slot] + __popcll(word & ((1ull << bit) - 1ull));
+      }
+      row[e] = idx;
+      r += step_r;
+      kk += step_k;
+      if (kk >= K) {
+        kk -= K;
+        ++r;
+      }
+    }
+    __syncwarp();
+  }
+}
+
+// The map for reaches small enough to tabulate: the input voxel index of
+// every voxel of the output leaf's reach (the halo: E0 x E1 x E2 <= kHaloMax
+// voxels, the same extents for every leaf) is computed once per leaf, and an
+// entry is then one shared-memory word at halo offset base(p) + delta(d):
+//   stride 1          q = o + p + d          base p,        delta d - lo
+//   transposed 1      q = o + p - d          base p,        delta hi - d
+//   transposed 2      q = (o + p - d) / 2    base p / 2,    delta hi / 2 - d / 2 (floors;
+//                     p - d even on every axis, else no entry)
+// Each output leaf pays for its halo once; an entry costs two shared loads,
+// an add and the store, so the map is written at close to store rate.
+constexpr int kHaloMax = kKmapHaloMax;
+constexpr int kHaloWarps = 4;
+struct HaloWarp {
+  uint64_t mask[kStagedCand * 8];
+  int32_t base[kStagedCand * 8];
+  int32_t cand[kStagedCand];
+  int32_t H[kHaloMax];   // input voxel index of each halo voxel, or -1
+  uint16_t vh[512];      // per active output voxel: halo offset of base(p) | parity << 10
+};
+
+__global__ void __launch_bounds__(kHaloWarps * 32, 7) k_kmap_halo(const KmapArgs k) {
+  __shared__ HaloWarp sw[kHaloWarps];
+  __shared__ uint16_t dh[kKmapStagedColumns];  // per column: delta(d) | parity << 10
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  HaloWarp& W = sw[wib];
+  const long long nwarps = (long long)gridDim.x * kHaloWarps;
+  const int nb1 = k.hi[1] - k.lo[1] + 1, nb2 = k.hi[2] - k.lo[2] + 1;
+  const int K = (k.hi[0] - k.lo[0] + 1) * nb1 * nb2;
+  const int sh = k.stride == 2 ? 1 : 0, tr = k.transposed;
+  int E[3];
+#pragma unroll
+  for (int ax = 0; ax < 3; ++ax)
+    E[ax] = tr ? ((7 - k.lo[ax]) >> sh) + (k.hi[ax] >> sh) + 1 : 8 + k.hi[ax] - k.lo[ax];
+  const int E12 = E[1] * E[2];
+  for (int i = threadIdx.x; i < K; i += kHaloWarps * 32) {
+    const int d[3] = {k.lo[0] + i / (nb1 * nb2), k.lo[1] + (i / nb2) % nb1, k.lo[2] + i % nb2};
+    int delta[3];
+    uint32_t par = 0;
+#pragma unroll
+    for (int ax = 0; ax < 3; ++ax) {
+      delta[ax] = tr ? (k.hi[ax] >> sh) - (d[ax] >> sh) : d[ax] - k.lo[ax];
+      if (tr && sh) par |= (uint32_t)(d[ax] & 1) << (2 - ax);
+    }
+    dh[i] = (uint16_t)((delta[0] * E12 + delta[1] * E[2] + delta[2]) | (par << 10));
+  }
+  __syncthreads();
+  for (long long u = (long long)blockIdx.x * kHaloWarps + wib; u < k.L_out; u += nwarps) {
+    const int32_t g = __ldg(k.out_grid + u);
+    long long a[3];
+    int n[3], off[3];
+#pragma unroll
+    for (int ax = 0; ax < 3; ++ax) {
+      const long long o = __ldg(k.out_origins + 3 * u + ax);
+      reach(k, ax, o, a[ax], n[ax]);
+      const long long qlo = tr ? (o - k.hi[ax] + (1 << sh) - 1) >> sh : o + k.lo[ax];
+      off[ax] = (int)(qlo - (a[ax] << 3));  // the halo's first voxel within the first candidate leaf
+    }
+    const int n12 = n[1] * n[2], C = n[0] * n12;
+    if (k.cands) {
+      if (lane < C) W.cand[lane] = __ldcg(k.cands + u * k.cand_max + lane);
+    } else {
+      for (int c = lane; c < C; c += 32)
+        W.cand[c] = find_leaf(k, g, a[0] + c / n12, a[1] + (c / n[2]) % n[1], a[2] + c % n[2]);
+    }
+    __syncwarp();
+    const long long vin = __ldg(k.in_vbase + g);
+    for (int j = lane; j < 8 * C; j += 32) {
+      const int ci = W.cand[j >> 3], w = j & 7;
+      uint64_t m = 0;
+      int32_t b = 0;
+      if (ci >= 0) {
+        m = __ldg(k.in_masks + 8 * (long long)ci + w);
+        const uint64_t wp = __ldg(k.in_wp + ci);
+        const long long before = w ? (long long)((wp >> (9 * (w - 1))) & 511ull) : 0ll;
+        b = (int32_t)(vin + __ldg(k.in_voff + ci) + before);
+      }
+      W.mask[j] = m;
+      W.base[j] = b;
+    }
+    __syncwarp();
+    // the halo: lanes take (x, y) rows of E2 voxels
+    for (int t = lane; t < E[0] * E[1]; t += 32) {
+      const int hx = t / E[1], hy = t - hx * E[1];
+      const int rx = off[0] + hx, ry = off[1] + hy;
+      const int rowc = (rx >> 3) * n12 + (ry >> 3) * n[2];
+      const int bity = (ry & 7) << 3;
+      int32_t* hrow = W.H + t * E[2];
+      for (int hz = 0; hz < E[2]; ++hz) {
+        const int rz = off[2] + hz;
+        const int slot = (rowc + (rz >> 3)) * 8 + (rx & 7);
+        const uint64_t word = W.mask[slot];
+        const int bit = bity | (rz & 7);
+        hrow[hz] = ((word >> bit) & 1ull) ? W.base[slot] + __popcll(word & ((1ull << bit) - 1ull)) : -1;
+      }
+    }
+    // the output leaf's active voxels in order (lane l lists bits 16 l .. 16 l + 15)
+    const uint32_t chunk = (uint32_t)(__ldg(k.out_masks + 8 * u + (lane >> 2)) >> (16 * (lane & 3))) & 0xFFFFu;
+    const uint32_t cnt = __popc(chunk);
+    uint32_t incl = cnt;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+      if (lane >= o2) incl += y;
+    }
+    const int nvox = (int)__shfl_sync(0xffffffffu, incl, 31);
+    uint32_t pos = incl - cnt, rest = chunk;
+    while (rest) {
+      const int bn = 16 * lane + __ffs(rest) - 1;
+      rest &= rest - 1;
+      const int p[3] = {bn >> 6, (bn >> 3) & 7, bn & 7};
+      int hb = 0;
+      uint32_t par = 0;
+#pragma unroll
+      for (int ax = 0; ax < 3; ++ax) {
+        hb = hb * E[ax] + (tr ? (p[ax] >> sh) : p[ax]);
+        if (tr && sh) par |= (uint32_t)(p[ax] & 1) << (2 - ax);
+      }
+      W.vh[pos++] = (uint16_t)(hb | (par << 10));
+    }
+    __syncwarp();
+    const long long j0 = __ldg(k.out_vbase + g) + __ldg(k.out_voff + u);
+    const int Etot = nvox * K;
+    int32_t* row = k.map + j0 * K;
+    int r = lane / K, kk = lane % K;
+    const int step_r = 32 / K, step_k = 32 % K;
+    for (int e = lane; e < Etot; e += 32) {
+      const uint32_t vp = W.vh[r], dp = dh[kk];
+      row[e] = ((vp ^ dp) >> 10) ? -1 : W.H[(vp & 1023u) + (dp & 1023u)];
+      r += step_r;
+      kk += step_k;
+      if (kk >= K) {
+        kk -= K;
+        ++r;
+      }
+    }
+    __syncwarp();
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_leaf_table(const int32_t* origins, const int32_t* leaf_grid, long long L, int32_t* table,
@@ -198,6 +501,21 @@ cudaError_t launch_leaf_table(const int32_t* origins, const int32_t* leaf_grid, 
 
 cudaError_t launch_kmap(const KmapArgs& k, int blocks, cudaStream_t s) {
   k_kmap<<<blocks, kKmapThreads, 0, s>>>(k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kmap_cands(const KmapArgs& k, int blocks, cudaStream_t s) {
+  k_kmap_cands<<<blocks, 256, 0, s>>>(k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kmap_halo(const KmapArgs& k, int blocks, cudaStream_t s) {
+  k_kmap_halo<<<blocks, kHaloWarps * 32, 0, s>>>(k);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kmap_staged(const KmapArgs& k, int blocks, cudaStream_t s) {
+  k_kmap_staged<<<blocks, kStagedWarps * 32, 0, s>>>(k);
   return cudaGetLastError();
 }
 

@@ -46,10 +46,22 @@ struct KmapArgs {
   int32_t lo[3], hi[3];
   int32_t stride, transposed;
   int32_t* map;              // [V_out, K]
+  int32_t* cands;            // staged map: [L_out, cand_max] candidate input leaves (-1: none)
+  int32_t cand_max;          // span^3 of the staged map
 };
 cudaError_t launch_leaf_table(const int32_t* origins, const int32_t* leaf_grid, long long L, int32_t* table,
                               unsigned long long mask, int blocks, cudaStream_t s);
 cudaError_t launch_kmap(const KmapArgs& k, int blocks, cudaStream_t s);
+// The staged map: boxes whose reach from an output leaf spans at most 3 input
+// leaves per axis, with at most kKmapStagedColumns columns.
+constexpr int kKmapStagedColumns = 1024;
+cudaError_t launch_kmap_cands(const KmapArgs& k, int blocks, cudaStream_t s);
+// The tabulated map: stride 1 or transposed, the reach of an output leaf at
+// most kKmapHaloMax voxels (E0 x E1 x E2).
+constexpr int kKmapHaloMax = 1024;
+constexpr long long kKmapLargeLeaves = 65536;  // output leaves from which the staged map and look-up pass win
+cudaError_t launch_kmap_halo(const KmapArgs& k, int blocks, cudaStream_t s);
+cudaError_t launch_kmap_staged(const KmapArgs& k, int blocks, cudaStream_t s);
 
 // Masked refinement: keeps the voxels of each leaf whose flag (one byte per
 // voxel, in the batch's voxel order) is non-zero.

@@ -445,6 +445,8 @@ KMAP_CASES = [
     ([("refine", 2), PAD_N], (-1,) * 3, (1,) * 3, 2, True),     # k3s2 transpose
     ([("coarsen", 2)], (-2, -1, 0), (3, 1, 2), 2, False),       # uneven box, forward stride 2
     ([], (-7, 0, -2), (0, 7, 2), 1, False),                    # large box
+    ([PAD_P], (-1,) * 3, (1,) * 3, 1, True),                   # transposed stride 1
+    ([("refine", 2)], (-2,) * 3, (2,) * 3, 2, True),           # k5s2 transpose
 ]
 
 
@@ -483,6 +485,52 @@ def test_kernel_map_shells_sampled_rows():
                     q = (int(p[0]) + dx, int(p[1]) + dy, int(p[2]) + dz)
                     assert got[j, k] == where.get(q, -1)
                     k += 1
+
+
+def _popcount_below(mask_words, bn):
+    return sum(bin(int(mask_words[w])).count("1") for w in range(bn >> 6)) + \
+        bin(int(mask_words[bn >> 6]) & ((1 << (bn & 63)) - 1)).count("1")
+
+
+def test_kernel_map_stress_k2s2_transpose_sampled_leaves():
+    """Full stress size (the candidate look-up pass, then the tabulated map):
+    the k2s2 transpose map from the stress batch to its refinement.  The rows
+    of sampled output leaves are checked against the map's definition
+    (q = (p - d) / 2 where p - d is even), written out from the batches' own
+    leaf arrays."""
+    ijk, off = synth.make("stress_b64_res512")
+    b = tb.from_ijk(dev(ijk), dev(off))
+    fine = tb.refine(b)
+    got = tb.kernel_map(b, fine, (0,) * 3, (1,) * 3, 2, True)
+    ri, rf = b.to_numpy(), fine.to_numpy()
+    vin = np.concatenate([[0], np.cumsum(ri["voxel_counts"])])
+    vout = np.concatenate([[0], np.cumsum(rf["voxel_counts"])])
+    index = {(int(ri["leaf_grid"][i]),) + tuple(int(c) for c in ri["origins"][i]): i
+             for i in range(len(ri["origins"]))}
+    rng = np.random.default_rng(7)
+    for i in rng.choice(len(rf["origins"]), 150, replace=False):
+        g, o, m = int(rf["leaf_grid"][i]), [int(c) for c in rf["origins"][i]], rf["masks"][i]
+        rows = []
+        for n in range(512):
+            if not (int(m[n >> 6]) >> (n & 63)) & 1:
+                continue
+            p = (o[0] + (n >> 6), o[1] + ((n >> 3) & 7), o[2] + (n & 7))
+            row = []
+            for d in [(dx, dy, dz) for dx in (0, 1) for dy in (0, 1) for dz in (0, 1)]:
+                t = [p[a] - d[a] for a in range(3)]
+                if any(x % 2 for x in t):
+                    row.append(-1)
+                    continue
+                q = [x // 2 for x in t]
+                leaf = index.get((g, q[0] & ~7, q[1] & ~7, q[2] & ~7))
+                bn = ((q[0] & 7) << 6) | ((q[1] & 7) << 3) | (q[2] & 7)
+                if leaf is None or not (int(ri["masks"][leaf][bn >> 6]) >> (bn & 63)) & 1:
+                    row.append(-1)
+                    continue
+                row.append(int(vin[g] + ri["voxel_offset"][leaf] + _popcount_below(ri["masks"][leaf], bn)))
+            rows.append(row)
+        r0 = int(vout[g] + rf["voxel_offset"][i])
+        assert np.array_equal(got[r0:r0 + len(rows)].cpu().numpy(), np.array(rows, np.int32)), "leaf %d" % i
 
 
 # ---------------------------------------------------------- failure detection
