@@ -325,22 +325,23 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 4) k_kmap_staged(const Kmap
     }
     __syncwarp();
     const long long j0 = __ldg(k.out_vbase + g) + __ldg(k.out_voff + u);
-    const long long E = (long long)nvox * K;
+    const int Etot = (int)nvox * K;
     int32_t* row = k.map + j0 * K;
     int r = lane / K, kk = lane % K;
     const int step_r = 32 / K, step_k = 32 % K;
-    for (long long e = lane; e < E; e += 32) {
+    const uint32_t n2 = (uint32_t)n[2], nm = (uint32_t)(8 * C - 1);
+    for (int e = lane; e < Etot; e += 32) {
       const uint32_t vp = W.vpk[r], dp = dpk[kk];
-      int32_t idx = -1;
-      if ((vp >> 24) == (dp >> 24)) {  // transposed stride 2: p - d even on every axis
-        const uint32_t rel = (vp & 0xFFFFFFu) + (dp & 0xFFFFFFu) - 0x080808u;
-        const uint32_t rx = rel & 0xFFu, ry = (rel >> 8) & 0xFFu, rz = (rel >> 16) & 0xFFu;
-        const int slot = (int)(((rx >> 3) * n12 + (ry >> 3) * n[2] + (rz >> 3)) * 8 + (rx & 7u));
-        const uint64_t word = W.mask[slot];
-        const uint32_t bit = ((ry & 7u) << 3) | (rz & 7u);
-        if ((word >> bit) & 1ull) idx = W.base[slot] + __popcll(word & ((1ull << bit) - 1ull));
-      }
-      row[e] = idx;
+      // branch-free: a column of the wrong parity (transposed stride 2) reads
+      // a clamped slot and is then masked out
+      const uint32_t rel = (vp & 0xFFFFFFu) + (dp & 0xFFFFFFu) - 0x080808u;
+      const uint32_t rx = rel & 0xFFu, ry = (rel >> 8) & 0xFFu, rz = (rel >> 16) & 0xFFu;
+      const uint32_t slot = min((((rx >> 3) * (uint32_t)n12 + (ry >> 3) * n2 + (rz >> 3)) << 3) | (rx & 7u), nm);
+      const uint64_t word = W.mask[slot];
+      const uint32_t bit = ((ry & 7u) << 3) | (rz & 7u);
+      const uint64_t upto = word << (63u - bit);  // bit 63: the voxel; the rest: the voxels before it
+      const bool on = (vp >> 24) == (dp >> 24) && (upto >> 63);
+      row[e] = on ? W.base[slot] + __popcll(upto) - 1 : -1;
       r += step_r;
       kk += step_k;
       if (kk >= K) {
