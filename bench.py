@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-extra", action="store_true", help="skip the per-op and larger-workload tables")
     p.add_argument("--cpu-sample-steps", type=int, default=2)
     p.add_argument("--separate", action="store_true", help="one C-ABI call per chain instead of one tb_multi call")
+    p.add_argument("--kmap-only", action="store_true",
+                   help="only the kernel-map rows of the per-op table (shells_b16_res64 and stress_b64_res512)")
     return p.parse_args()
 
 
@@ -347,6 +349,11 @@ def run_ours(args):
         dist.init_process_group("nccl")
     tb.lib()
     stream = torch.cuda.current_stream()
+    if args.kmap_only:
+        flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
+        if rank == 0:
+            print(json.dumps({"per_op": kmap_table(tb, torch, synth, stream, flush)}), flush=True)
+        return
 
     ijk, off = rank_batch(synth, args.workload, rank)
     ijk_d = torch.from_numpy(ijk).cuda()
@@ -509,37 +516,65 @@ def per_op_tables(tb, torch, synth, stream, flush, main_workload):
                  ("refine_masked_half", lambda: tb.refine_masked(b0, flags)),
                  ("kmap_k3s1", lambda: tb.kernel_map(b0, b0)),
                  ("kmap_k2s2_transpose", lambda: tb.kernel_map(b0, fine, (0, 0, 0), (1, 1, 1), 2, True))]
-        for lab, fn in calls:
-            ts = []
-            vox = 0
-            nbytes = 0
-            for it in range(25):
-                flush.zero_()
-                s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                s.record(stream)
-                r = fn()
-                e.record(stream)
-                e.synchronize()
-                if isinstance(r, torch.Tensor):
-                    nbytes = r.numel() * 4
-                    del r
-                else:
-                    rs = r if isinstance(r, list) else [r]
-                    if it == 0:
-                        vox = sum(int(x.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for x in rs)
-                    for x in rs:
-                        x.free()
-                if it >= 5:
-                    ts.append(s.elapsed_time(e))
-            med = statistics.median(ts)
-            if nbytes:
-                row[lab] = {"ms": med, "map_bytes": nbytes, "map_GBps": nbytes / med / 1e6}
-            else:
-                row[lab] = {"ms": med, "out_voxels": vox, "Gvox_per_s": vox / med / 1e6}
+        row = time_calls(calls, torch, stream, flush)
         res[wl] = row
         fine.free()
         b0.free()
     res["pyramid_b48_res64"] = pyramid_table(tb, torch, synth, stream, flush)
+    return res
+
+
+def time_calls(calls, torch, stream, flush):
+    """{label: row} for (label, fn) calls: median ms of 20 CUDA-event
+    iterations after 5 warm-ups, L2 flushed before each; a call returning a
+    tensor (a kernel map) reports the GB/s of the map it writes, one returning
+    batches their output voxels per second."""
+    row = {}
+    for lab, fn in calls:
+        ts = []
+        vox = 0
+        nbytes = 0
+        for it in range(25):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record(stream)
+            r = fn()
+            e.record(stream)
+            e.synchronize()
+            if isinstance(r, torch.Tensor):
+                nbytes = r.numel() * 4
+                del r
+            else:
+                rs = r if isinstance(r, list) else [r]
+                if it == 0:
+                    vox = sum(int(x.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for x in rs)
+                for x in rs:
+                    x.free()
+            if it >= 5:
+                ts.append(s.elapsed_time(e))
+        med = statistics.median(ts)
+        if nbytes:
+            row[lab] = {"ms": med, "map_bytes": nbytes, "map_GBps": nbytes / med / 1e6}
+        else:
+            row[lab] = {"ms": med, "out_voxels": vox, "Gvox_per_s": vox / med / 1e6}
+    return row
+
+
+def kmap_table(tb, torch, synth, stream, flush):
+    """The kernel-map rows alone (as in per_op_tables) on shells_b16_res64 and
+    stress_b64_res512: the k3s1 same-topology map, then the k2s2 transpose map
+    to the refinement, 25 calls each."""
+    res = {}
+    for wl in ("shells_b16_res64", "stress_b64_res512"):
+        ijk, off = synth.make(wl)
+        b0 = tb.from_ijk(torch.from_numpy(ijk).cuda(), torch.from_numpy(off).cuda())
+        fine = tb.refine(b0)
+        res[wl] = time_calls([("kmap_k3s1", lambda: tb.kernel_map(b0, b0)),
+                              ("kmap_k2s2_transpose",
+                               lambda: tb.kernel_map(b0, fine, (0, 0, 0), (1, 1, 1), 2, True))],
+                             torch, stream, flush)
+        fine.free()
+        b0.free()
     return res
 
 
