@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--no-extra", action="store_true", help="skip the per-op and larger-workload tables")
     p.add_argument("--cpu-sample-steps", type=int, default=2)
     p.add_argument("--separate", action="store_true", help="one C-ABI call per chain instead of one tb_multi call")
+    p.add_argument("--phases", action="store_true",
+                   help="only the step's per-call phase breakdown (GPU timer stamps and host timers)")
     p.add_argument("--kmap-only", action="store_true",
                    help="only the kernel-map rows of the per-op table (shells_b16_res64 and stress_b64_res512)")
     return p.parse_args()
@@ -354,6 +356,10 @@ def run_ours(args):
         if rank == 0:
             print(json.dumps({"per_op": kmap_table(tb, torch, synth, stream, flush)}), flush=True)
         return
+    if args.phases:
+        if rank == 0:
+            print(json.dumps({"phases": phase_table(tb, torch, synth, args.workload, args.steps)}), flush=True)
+        return
 
     ijk, off = rank_batch(synth, args.workload, rank)
     ijk_d = torch.from_numpy(ijk).cuda()
@@ -558,6 +564,33 @@ def time_calls(calls, torch, stream, flush):
         else:
             row[lab] = {"ms": med, "out_voxels": vox, "Gvox_per_s": vox / med / 1e6}
     return row
+
+
+def phase_table(tb, torch, synth, workload, steps):
+    """Where a step's time goes, per call (the front end; the tb_multi call):
+    mean microseconds per call of each kernel and of each pass-kernel phase
+    (GPU global-timer stamps: entry to the first emission, emission, digit
+    passes, index, leaves, voxel offsets) and of the host's share of the
+    call, over `steps` steps after 5 warm-ups, without an L2 flush.  The
+    stamps add a little to the kernels they time."""
+    ijk, off = synth.make(workload)
+    ijk_d, off_d = torch.from_numpy(ijk).cuda(), torch.from_numpy(off).cuda()
+    plan = tb.MultiPlan([ops for _, ops in STEP[1:]])
+    res = {}
+    b0 = tb.from_ijk(ijk_d, off_d)
+    for label, fn in [("from_ijk", lambda: tb.from_ijk(ijk_d, off_d)), ("multi7", lambda: plan(b0))]:
+        for _ in range(5):
+            fn()
+        torch.cuda.synchronize()
+        tb.profile_read()
+        tb.profile_enable(2)
+        for _ in range(steps):
+            fn()
+        torch.cuda.synchronize()
+        prof = tb.profile_read()
+        tb.profile_enable(0)
+        res[label] = {k: 1e3 * ms / steps for k, (n, ms) in prof.items()}
+    return res
 
 
 def kmap_table(tb, torch, synth, stream, flush):
