@@ -67,6 +67,20 @@ def test_host_side_argument_errors(lib):
     assert lib.tb_batch_free(None, None) == 0
 
 
+def test_launch_mode_switch(lib):
+    # process-wide, host only: returns the previous mode, rejects others
+    lib.tb_set_launch_mode.restype = ctypes.c_int32
+    prev = lib.tb_set_launch_mode(ctypes.c_int32(2))
+    try:
+        assert prev in (0, 1, 2)
+        assert lib.tb_set_launch_mode(ctypes.c_int32(1)) == 2
+        assert lib.tb_set_launch_mode(ctypes.c_int32(3)) == -1
+        assert lib.tb_set_launch_mode(ctypes.c_int32(-1)) == -1
+        assert lib.tb_set_launch_mode(ctypes.c_int32(0)) == 1
+    finally:
+        lib.tb_set_launch_mode(ctypes.c_int32(prev))
+
+
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import sparse_voxel_grid_leaf_gb300 as tb
     monkeypatch.setattr(tb, "LIB_PATH", str(tmp_path / "missing.so"))
