@@ -15,7 +15,15 @@
 // its candidate input leaves (the few leaves any of its voxels can reach) are
 // looked up and kept in shared memory; the leaf's active voxels are listed in
 // shared memory; then the warp writes the leaf's voxels x K entries, which
-// are contiguous in the map.
+// are contiguous in the map.  Three forms of that warp's work, picked by the
+// host from the box and the output's size:
+//   k_kmap_halo    the input index of every voxel in the leaf's reach is
+//                  tabulated once; an entry is one shared-memory word
+//   k_kmap_staged  the candidates' mask words and word bases are staged; an
+//                  entry is a packed-coordinate add, a bit test and a
+//                  popcount (with k_kmap_cands doing the look-ups first for
+//                  large outputs)
+//   k_kmap         any box: an entry computes its input leaf and reads it
 #include "tb_common.cuh"
 #include "tb_launch.h"
 
