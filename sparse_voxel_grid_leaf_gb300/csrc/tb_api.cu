@@ -15,6 +15,7 @@
 // the front ends the pass kernel reads the input's bbox and plans the key
 // itself; the host repeats that plan after the readback.
 #include <algorithm>
+#include <array>
 #include <atomic>
 #include <chrono>
 #include <cstddef>
@@ -23,6 +24,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <unordered_map>
 #include <vector>
 
 #include "../../include/tb.h"
@@ -444,6 +446,20 @@ void fill_write_out(const tb_batch* b, WriteOut& wo) {
   wo.lower_origins = b->lower_origins;
   wo.lower_parent = b->lower_parent;
   wo.upper_origins = b->upper_origins;
+  wo.L_cap = b->L;  // the counts the arrays were carved for
+  wo.NL_cap = b->NL;
+  wo.NU_cap = b->NU;
+}
+
+// Output counts of the last call of each shape on this thread (source kind,
+// grids, source count, chains): the next call of that shape allocates its
+// outputs with some room above them and queues its writers right behind the
+// pass kernel, before the count readback.
+thread_local std::unordered_map<uint64_t, std::vector<std::array<long long, 3>>> t_hints;
+
+uint64_t mix(uint64_t h, long long v) {
+  h ^= (uint64_t)v;
+  return h * 0x100000001B3ull;
 }
 
 // Runs n chains of passes over one source in one cooperative launch and
@@ -793,6 +809,101 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     }
   }
 
+  // ---- outputs.  With the counts of the last call of the same shape, the
+  // outputs are allocated now with room to spare and the writers queued
+  // behind the pass kernel; a writer skips a chain that outgrew its room,
+  // and that chain is written again after the readback.
+  std::vector<tb_batch*> made(n_chain, nullptr);
+  auto undo = [&] {
+    for (tb_batch*& b : made)
+      if (b) {
+        mem.put(b->mem);
+        delete b;
+        b = nullptr;
+      }
+  };
+  // a batch with arrays for L, NL, NU (counts or room)
+  auto new_batch = [&](long long L, long long NL, long long NU) -> tb_batch* {
+    tb_batch* b = new tb_batch();
+    b->B = B;
+    b->device = dev;
+    b->L = L;
+    b->NL = NL;
+    b->NU = NU;
+    b->has_alloc = alloc != nullptr;
+    if (alloc) b->alloc = *alloc;
+    if (alloc_outputs(b, mem) != TB_OK) {
+      delete b;
+      return nullptr;
+    }
+    return b;
+  };
+  // the writers of some chains: one launch for a one-chain call, else one per
+  // kMaxWriteTasks chains with the tasks in its parameter
+  auto launch_writers = [&](const std::vector<int>& chs) -> cudaError_t {
+    if (n_chain == 1) {
+      WriteOut wo;
+      fill_write_out(made[0], wo);
+      const int op_last = plans[0].back().spec.op;
+      const int wb = blocks_for(std::max<long long>(wo.L_cap, B + 1), kWriteLeavesPerBlock,
+                                (long long)di->sms * di->occ_write[op_last]);
+      const PassArgs& a = host_args[plans[0].size() - 1];
+      return launch(kKWrite0 + op_last, stream, [&] { return launch_write_final(op_last, a, wo, wb, stream); });
+    }
+    WriteTasks wt;
+    for (size_t c0 = 0; c0 < chs.size(); c0 += kMaxWriteTasks) {
+      const int nt = (int)std::min<size_t>(kMaxWriteTasks, chs.size() - c0);
+      long long room = 0;
+      std::memset(&wt, 0, sizeof wt);
+      wt.n = nt;
+      for (int j = 0; j < nt; ++j) {
+        const int ch = chs[c0 + j];
+        wt.t[j].a = host_args[(size_t)ch * n_stage + plans[ch].size() - 1];
+        fill_write_out(made[ch], wt.t[j].o);
+        room += (wt.t[j].o.L_cap + 3) / 4 * 4;
+      }
+      const int wb = blocks_for(std::max<long long>(room, B + 1), kWriteLeavesPerBlock,
+                                (long long)di->sms * di->occ_write_multi);
+      const cudaError_t e = launch(kKWriteMulti, stream, [&] { return launch_write_multi(wt, wb, stream); });
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  };
+  uint64_t shape = mix(mix(mix(mix(0xCBF29CE484222325ull, src.kind), B), src.count), n_chain);
+  for (const auto& pc : plans)
+    for (const auto& pl : pc) {
+      shape = mix(mix(mix(shape, pl.spec.op), pl.spec.factor), pc.size());
+      for (int a = 0; a < 3; ++a) shape = mix(mix(shape, pl.spec.lo[a]), pl.spec.hi[a]);
+    }
+  std::vector<char> ahead(n_chain, 0);  // outputs allocated and written before the readback
+  {
+    const auto h = t_hints.find(shape);
+    if (h != t_hints.end() && h->second.size() == (size_t)n_chain) {
+      bool ok = true;
+      for (int ch = 0; ch < n_chain && ok; ++ch) {
+        const auto& c = h->second[ch];
+        made[ch] = new_batch(c[0] + c[0] / 8 + 16, c[1] + c[1] / 8 + 4, c[2] + c[2] / 8 + 2);
+        ok = made[ch] != nullptr;
+      }
+      std::vector<int> all(n_chain);
+      for (int ch = 0; ch < n_chain; ++ch) all[ch] = ch;
+      if (ok && launch_writers(all) == cudaSuccess) {
+        for (int ch = 0; ch < n_chain; ++ch) ahead[ch] = 1;
+      } else {
+        cudaGetLastError();
+        undo();
+      }
+    }
+  }
+  // every return from here on without outputs frees the batches made so far
+  struct Release {
+    decltype(undo)& f;
+    bool armed = true;
+    ~Release() {
+      if (armed) f();
+    }
+  } release{undo};
+
   // ---- the one count readback of the call: the kernel's copy to pinned
   // memory, seen through the host flag; else (profiling, or a kernel that
   // stopped early) through the stream
@@ -872,29 +983,49 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     a0.sorted = a0.P & 1;
   }
 
-  // ---- outputs, one writer launch per chain
-  std::vector<tb_batch*> made(n_chain, nullptr);
-  auto undo = [&] {
-    for (tb_batch* b : made)
-      if (b) {
-        mem.put(b->mem);
-        delete b;
-      }
-  };
+  // ---- each chain's batch: the one written ahead if its counts fit its
+  // room, else a batch of the exact size written now
+  std::vector<int> redo;
+  std::vector<std::array<long long, 3>> counts(n_chain);
   for (int ch = 0; ch < n_chain; ++ch) {
     const PassPlan& last = plans[ch].back();
     const ReadbackHeader* hr = (const ReadbackHeader*)(pinned + o_rb_last[ch]);
     const int64_t L = (int64_t)hr->num_leaves, NL = (int64_t)hr->num_lowers, NU = (int64_t)hr->num_uppers;
+    counts[ch] = {L, NL, NU};
     const int64_t* hoff = (const int64_t*)(hr + 1);
-    tb_batch* b = new tb_batch();
-    made[ch] = b;
-    b->B = B;
-    b->device = dev;
+    tb_batch* b = made[ch];
+    if (!(b && ahead[ch] && L <= b->L && NL <= b->NL && NU <= b->NU)) {
+      if (b) {
+        mem.put(b->mem);  // stream-ordered after the writer, which skipped it
+        delete b;
+        made[ch] = nullptr;
+      }
+      b = new_batch(L, NL, NU);
+      if (!b) {
+        undo();
+        return fail(TB_ERR_OOM, "output allocation failed");
+      }
+      made[ch] = b;
+      redo.push_back(ch);
+    }
     b->L = L;
     b->NL = NL;
     b->NU = NU;
-    b->has_alloc = alloc != nullptr;
-    if (alloc) b->alloc = *alloc;
+    // arrays of no elements read as NULL
+    if (L == 0) {
+      b->origins = nullptr;
+      b->masks = nullptr;
+      b->voxel_offset = nullptr;
+      b->word_prefix = nullptr;
+      b->leaf_bbox = nullptr;
+      b->leaf_grid = nullptr;
+      b->leaf_parent = nullptr;
+    }
+    if (NL == 0) {
+      b->lower_origins = nullptr;
+      b->lower_parent = nullptr;
+    }
+    if (NU == 0) b->upper_origins = nullptr;
     b->leaf_offsets_host.assign(hoff, hoff + B + 1);
     b->voxel_base_host.assign(B + 1, 0);
     for (int32_t g = 0; g < B; ++g) b->voxel_base_host[g + 1] = b->voxel_base_host[g] + hoff[3 * (B + 1) + g];
@@ -908,52 +1039,17 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     b->build_key_bits = last.K.W;
     b->build_digit_passes = last.P;
     b->build_member_ctas = cl;
-    st = alloc_outputs(b, mem);
-    if (st != TB_OK) {
-      undo();
-      return st;
-    }
   }
-  if (n_chain == 1) {
-    WriteOut wo;
-    fill_write_out(made[0], wo);
-    const int op_last = plans[0].back().spec.op;
-    const int wb = blocks_for(std::max<long long>(made[0]->L, B + 1), kWriteLeavesPerBlock,
-                              (long long)di->sms * di->occ_write[op_last]);
-    const PassArgs& a = host_args[plans[0].size() - 1];
-    const cudaError_t e =
-        launch(kKWrite0 + op_last, stream, [&] { return launch_write_final(op_last, a, wo, wb, stream); });
+  if (!redo.empty()) {
+    const cudaError_t e = launch_writers(redo);
     if (e != cudaSuccess) {
       undo();
       return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
     }
-  } else {
-    // one writer launch per kMaxWriteTasks chains, the tasks in its parameter
-    WriteTasks wt;
-    for (int c0 = 0; c0 < n_chain; c0 += kMaxWriteTasks) {
-      const int nt = std::min(kMaxWriteTasks, n_chain - c0);
-      long long quads = 0, leaves_max = B + 1;
-      std::memset(&wt, 0, sizeof wt);
-      wt.n = nt;
-      for (int j = 0; j < nt; ++j) {
-        const int ch = c0 + j;
-        WriteTask& t = wt.t[j];
-        t.a = host_args[(size_t)ch * n_stage + plans[ch].size() - 1];
-        fill_write_out(made[ch], t.o);
-        t.leaves = made[ch]->L;
-        t.quad_base = quads;
-        t.quads = (t.leaves + 3) / 4;
-        quads += t.quads;
-        leaves_max = std::max<long long>(leaves_max, quads * 4);
-      }
-      const int wb = blocks_for(leaves_max, kWriteLeavesPerBlock, (long long)di->sms * di->occ_write_multi);
-      const cudaError_t e = launch(kKWriteMulti, stream, [&] { return launch_write_multi(wt, wb, stream); });
-      if (e != cudaSuccess) {
-        undo();
-        return fail(TB_ERR_CUDA, "writer launch: %s", cudaGetErrorString(e));
-      }
-    }
   }
+  if (t_hints.size() > 256) t_hints.clear();
+  t_hints[shape] = counts;
+  release.armed = false;
   for (int ch = 0; ch < n_chain; ++ch) outs[ch] = made[ch];
   if (t_prof >= 2) {
     t_phase_ms[8] += host_ms_since(t_synced);

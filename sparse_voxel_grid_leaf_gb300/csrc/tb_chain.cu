@@ -1853,8 +1853,15 @@ __device__ __forceinline__ void write_leaf(const PassArgs& a, const WriteOut& o,
   write_record(o, u, valid, word, g, org, lk);
 }
 
+// Whether a chain's counts fit the room of its outputs.
+__device__ __forceinline__ bool write_fits(const PassArgs& a, const WriteOut& o) {
+  return (long long)__ldcg(&a.rb->num_leaves) <= o.L_cap && (long long)__ldcg(&a.rb->num_lowers) <= o.NL_cap &&
+         (long long)__ldcg(&a.rb->num_uppers) <= o.NU_cap;
+}
+
 template <int OP>
 __global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, const WriteOut o) {
+  if (!write_fits(a, o)) return;
   const long long U = (long long)a.rb->num_leaves;
   const int tid = threadIdx.x, lane = tid & 31;
   const long long gtid = (long long)blockIdx.x * kThreads + tid;
@@ -1866,23 +1873,35 @@ __global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, cons
 
 // The writers of several chains in one launch, from the records their leaves
 // phases staged.  Tasks (one per chain, up to kMaxWriteTasks) come as one
-// kernel parameter; the leaves of all chains form one index space in units of
-// 4 leaves, so a warp's 4 groups always belong to one chain.
+// kernel parameter; every block reads the chains' counts and lays the leaves
+// of the chains that fit their room out as one index space in units of 4
+// leaves, so a warp's 4 groups always belong to one chain.
 __global__ void __launch_bounds__(kThreads) k_write_multi(const __grid_constant__ WriteTasks wt) {
   const WriteTask* t = wt.t;  // read in place: the lanes of a warp read the same task
   const int n_task = wt.n;
+  __shared__ long long qbase[kMaxWriteTasks + 1], leaves[kMaxWriteTasks];
+  if (threadIdx.x == 0) {
+    long long q = 0;
+    for (int i = 0; i < n_task; ++i) {
+      const long long U = write_fits(t[i].a, t[i].o) ? (long long)__ldcg(&t[i].a.rb->num_leaves) : -1;
+      leaves[i] = U;
+      qbase[i] = q;
+      if (U > 0) q += (U + 3) / 4;
+    }
+    qbase[n_task] = q;
+  }
+  __syncthreads();
   const int tid = threadIdx.x, lane = tid & 31;
   const int B = t[0].a.B;
   const long long gtid = (long long)blockIdx.x * kThreads + tid, nthreads = (long long)gridDim.x * kThreads;
   for (long long i = gtid; i < (long long)n_task * (B + 1); i += nthreads)
-    write_grid_arrays(t[i / (B + 1)].a, t[i / (B + 1)].o, i % (B + 1));
-  const long long total = t[n_task - 1].quad_base + t[n_task - 1].quads;
+    if (leaves[i / (B + 1)] >= 0) write_grid_arrays(t[i / (B + 1)].a, t[i / (B + 1)].o, i % (B + 1));
+  const long long total = qbase[n_task];
   const long long nwarps = nthreads / 32;
   for (long long q = gtid / 32; q < total; q += nwarps) {
     int ch = 0;
-    while (ch + 1 < n_task && t[ch + 1].quad_base <= q) ++ch;
-    const WriteTask& tk = t[ch];
-    write_leaf_staged(tk.a, tk.o, (q - tk.quad_base) * 4 + (lane >> 3), tk.leaves);
+    while (ch + 1 < n_task && qbase[ch + 1] <= q) ++ch;
+    write_leaf_staged(t[ch].a, t[ch].o, (q - qbase[ch]) * 4 + (lane >> 3), leaves[ch]);
   }
 }
 

@@ -221,6 +221,9 @@ struct WriteOut {
   int32_t* lower_origins;
   int32_t* lower_parent;
   int32_t* upper_origins;
+  // the arrays' room: a writer whose counts exceed it writes nothing (the
+  // host sized it from an earlier call of the same shape and writes again)
+  long long L_cap, NL_cap, NU_cap;
 };
 
 // ---------------------------------------------------------------- keys
@@ -268,9 +271,6 @@ constexpr int kMaxWriteTasks = 16;
 struct WriteTask {
   PassArgs a;
   WriteOut o;
-  long long leaves;     // output leaves of the chain
-  long long quad_base;  // first 4-leaf unit of the chain in the launch's index space
-  long long quads;      // its 4-leaf units
 };
 // The tasks of one writer launch, passed by value as its kernel parameter.
 struct WriteTasks {
