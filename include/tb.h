@@ -36,7 +36,13 @@
  *    the device's default memory pool.  Otherwise every device allocation
  *    (outputs and per-call scratch) goes through alloc->alloc / alloc->free,
  *    which receive `stream`; the batch keeps a copy of the allocator and frees
- *    its memory through it.
+ *    its memory through it.  A call whose shape (source kind, grid count,
+ *    source count, ops) repeats an earlier call on the same thread allocates
+ *    its outputs before the count readback, with room for that call's counts
+ *    plus about an eighth, and queues its writers behind the pass kernel; the
+ *    batch's arrays may then be larger than its counts (the view reports the
+ *    counts).  Outputs that outgrow the room are written again at their exact
+ *    size within the same call.
  *  - Ownership.  Inputs are borrowed, read only, and may be freed once the
  *    call returns.  On TB_OK, *out is a new batch the caller releases with
  *    tb_batch_free.  On any error *out is set to NULL and nothing is leaked.
