@@ -242,6 +242,9 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   o.lower_origins = out->lower_origins;
   o.lower_parent = out->lower_parent;
   o.upper_origins = out->upper_origins;
+  o.L_cap = (long long)r.num_leaves;  // the counts just read back
+  o.NL_cap = (long long)r.num_lowers;
+  o.NU_cap = (long long)r.num_uppers;
   const int wb = blocks_of(std::max<long long>((long long)r.num_leaves, B + 1), kWriteLeavesPerBlock,
                            (long long)sms * write_final_occupancy(kRefine));
   TB_STATIC_CUDA(launch_write_final(kRefine, a, o, wb, stream));
