@@ -528,6 +528,40 @@ def export_host(b: Batch, origins: np.ndarray, masks: np.ndarray, voxel_offset: 
                                  ctypes.c_void_p(_stream(stream))))
 
 
+class ExportPlan:
+    """Destinations of tb_batch_export_many marshalled once, for repeated
+    exports of different batches into the same buffers:
+    ``plan = ExportPlan(origins, masks, voxel_offset, leaf_offsets)``, then
+    ``plan(batches)``.  Each argument is a list with one buffer (or None) per
+    batch, or None to skip that array; the buffers must stay alive."""
+
+    def __init__(self, origins=None, masks=None, voxel_offset=None, leaf_offsets=None):
+        lists = [x for x in (origins, masks, voxel_offset, leaf_offsets) if x is not None]
+        self.n = len(lists[0]) if lists else 0
+        self._keep = []
+
+        def plist(xs):
+            if xs is None:
+                return None
+            arr = (ctypes.c_void_p * self.n)()
+            for i, x in enumerate(xs):
+                if x is not None:
+                    p, k = _ptr(x)
+                    self._keep.append(k)
+                    arr[i] = p
+            return arr
+        self._lists = [plist(origins), plist(masks), plist(voxel_offset), plist(leaf_offsets)]
+        self._hs = (ctypes.c_void_p * self.n)()
+        self._fn = lib().tb_batch_export_many
+
+    def __call__(self, batches: Sequence[Batch], stream=None):
+        if len(batches) != self.n:
+            raise TBError(1, "export plan for %d batches called with %d" % (self.n, len(batches)))
+        for i, b in enumerate(batches):
+            self._hs[i] = b.handle.value
+        _check(self._fn(self._hs, self.n, *self._lists, ctypes.c_void_p(_stream(stream))))
+
+
 def export_many(batches: Sequence[Batch], origins=None, masks=None, voxel_offset=None, leaf_offsets=None,
                 stream=None):
     """Enqueues the copies of several batches' leaf records (one list entry per

@@ -567,6 +567,19 @@ def test_export_many_matches_arrays():
         assert np.array_equal(v[i], r["voxel_offset"])
         if lo[i] is not None:
             assert np.array_equal(lo[i].numpy(), r["leaf_offsets"])
+    # the same through a prepared plan, into cleared buffers, twice
+    plan = tb.ExportPlan(o, m, v, lo)
+    for _ in range(2):
+        for x in o + m:
+            x.zero_()
+        for x in v:
+            x[:] = 0
+        plan(bs)
+        torch.cuda.synchronize()
+        for i, r in enumerate(ref):
+            assert np.array_equal(o[i].numpy(), r["origins"])
+            assert np.array_equal(m[i].cpu().numpy().view(np.uint64), r["masks"])
+            assert np.array_equal(v[i], r["voxel_offset"])
 
 
 def test_pyramid_b48_one_multi_call():
