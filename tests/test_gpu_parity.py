@@ -294,6 +294,24 @@ def test_auto_launch_shape():
         tb.set_launch_mode(prev)
 
 
+def test_outputs_sized_ahead_grow_and_shrink():
+    """A call shape that repeats allocates its outputs before the count
+    readback from the previous call's counts: when the new counts are larger
+    the chain is written again at its exact size; when smaller the batch
+    keeps spare room.  Either way every array equals the oracle's."""
+    # same grid count and voxel count, very different leaf counts
+    dense, off = synth.random_voxels(3, 400, 12, seed=91, origin=(-6, 5, -4100))
+    sparse, off2 = synth.random_voxels(3, 400, 400, seed=92, origin=(-6, 5, -4100))
+    assert np.array_equal(off, off2)
+    for first, second in ((dense, sparse), (sparse, dense)):
+        for ijk in (first, second):  # the second call reuses the first one's counts
+            check(ijk, off, [("refine", 2)], "ahead %d" % len(ijk))
+            b = tb.from_ijk(dev(ijk), dev(off))
+            outs = tb.multi(b, [[("refine", 2)], [DIL]])
+            for o, ops in zip(outs, ([("refine", 2)], [DIL])):
+                assert_same(o.to_numpy(), oracle.run_voxels(ijk, off, ops), "ahead multi %s" % (ops,))
+
+
 def test_launches_are_counted():
     n0 = tb.kernel_launch_count()
     ijk, off = synth.make("pr1_b2_res32")
