@@ -312,6 +312,56 @@ def test_outputs_sized_ahead_grow_and_shrink():
                 assert_same(o.to_numpy(), oracle.run_voxels(ijk, off, ops), "ahead multi %s" % (ops,))
 
 
+def _random_op(rng):
+    k = int(rng.integers(0, 4))
+    if k == 0:
+        return ("refine", int(rng.choice([2, 4])))
+    if k == 1:
+        return ("coarsen", int(rng.choice([2, 4, 8])))
+    lo = tuple(int(x) for x in rng.integers(-3, 1, 3))
+    hi = tuple(int(x) for x in rng.integers(0, 4, 3))
+    return ("dilate", lo, hi)
+
+
+def _random_chain(rng, n_max, growth_max=128):
+    """Up to n_max random ops whose voxel-count growth (refinement f^3, box
+    volume) stays within growth_max, so the oracle's per-voxel sets stay small."""
+    ops, growth = [], 1
+    while len(ops) < n_max:
+        op = _random_op(rng)
+        g = op[1] ** 3 if op[0] == "refine" else (
+            int(np.prod([h - l + 1 for l, h in zip(op[1], op[2])])) if op[0] == "dilate" else 1)
+        if growth * g > growth_max:
+            if ops:
+                break
+            continue
+        ops.append(op)
+        growth *= g
+    return ops
+
+
+def test_random_chains_fuzz():
+    """Seeded random batches (grid counts, sizes, spans, origins across the
+    tile boundaries, empty members) through random chains of up to three ops
+    and a two-chain multi call, every array against the oracle."""
+    rng = np.random.default_rng(1234)
+    for trial in range(24):
+        B = int(rng.integers(1, 7))
+        n = int(rng.integers(1, 300))
+        span = int(rng.integers(4, 120))
+        origin = tuple(int(x) for x in rng.integers(-4200, 4200, 3))
+        empty = tuple(int(g) for g in range(B) if rng.random() < 0.2)
+        ijk, off = synth.random_voxels(B, n, span, seed=500 + trial, origin=origin, empty=empty)
+        chain_a = _random_chain(rng, int(rng.integers(1, 4)))
+        chain_b = _random_chain(rng, int(rng.integers(1, 3)))
+        where = "trial %d B=%d n=%d span=%d %s / %s" % (trial, B, n, span, chain_a, chain_b)
+        b = tb.from_ijk(dev(ijk), dev(off))
+        assert_same(tb.chain(b, chain_a).to_numpy(), oracle.run_voxels(ijk, off, chain_a), where)
+        outs = tb.multi(b, [chain_a, chain_b])
+        assert_same(outs[0].to_numpy(), oracle.run_voxels(ijk, off, chain_a), where + " multi a")
+        assert_same(outs[1].to_numpy(), oracle.run_voxels(ijk, off, chain_b), where + " multi b")
+
+
 def test_launches_are_counted():
     n0 = tb.kernel_launch_count()
     ijk, off = synth.make("pr1_b2_res32")
