@@ -217,8 +217,9 @@ TB_API tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask,
  * column k enumerates the offsets x-major: k = ((dx-lo0) ny + (dy-lo1)) nz +
  * (dz-lo2)), map[j * K + k] is the index, in the voxel order of `in`, of the
  * input voxel that p reads through d, or -1:
- *   stride 1:                  p + d
+ *   stride 1, transposed == 0: p + d
  *   stride 2, transposed == 0: 2 p + d      (e.g. conv_grid k2s2, box [0,1])
+ *   stride 1, transposed != 0: p - d
  *   stride 2, transposed != 0: (p - d) / 2 where p - d is even on every axis
  *                              (conv_transpose_grid k2s2: box [0,1]; k3s2:
  *                              box [-1,1])
@@ -244,8 +245,9 @@ TB_API tb_status tb_chain(const tb_batch* in, const tb_op* ops, int32_t n_ops, c
 /* Several chains over the same input in one call: chain c applies
  * chain_lengths[c] ops taken in order from `ops` (the chains' ops are
  * concatenated); outs[c] receives its result (a copy of the input when its
- * length is 0).  All chains run in one cooperative launch, phase by phase, so
- * they share the grid barriers, the readback and the call's host overhead --
+ * length is 0).  All chains run in one launch -- the cooperative whole-grid
+ * kernel, phase by phase, or a member launch (tb_set_launch_mode) -- so
+ * they share the launch, the readback and the call's host overhead --
  * the batching of PR #757 (Summary) extended from batch members to the
  * several topologies a convolution plan derives from one grid.  Results equal
  * those of separate tb_chain calls.  On error every outs[c] is NULL.
