@@ -82,6 +82,14 @@ def popcount(w: int) -> int:
     return bin(int(w)).count("1")
 
 
+def canon_tuple(o) -> Tuple[int, ...]:
+    """Canonical sort tuple of an origin: signed root tile floor(v/4096), then
+    the x-major upper child offset floor(v/128) mod 32, then the x-major lower
+    child offset floor(v/8) mod 16 (fVDB PR #757, Summary item 1, sort bullet)."""
+    o = [int(v) for v in o]
+    return tuple(v // 4096 for v in o) + tuple((v // 128) % 32 for v in o) + tuple((v // 8) % 16 for v in o)
+
+
 def check_derived(res: Dict[str, np.ndarray]):
     """Per-leaf/per-grid arrays against a direct recomputation from the masks."""
     B = len(res["leaf_offsets"]) - 1
@@ -124,6 +132,11 @@ def check_derived(res: Dict[str, np.ndarray]):
             p = int(res["leaf_parent"][i])
             assert 0 <= p < len(lowers)
             assert tuple(res["lower_origins"][nlo + p]) == tuple((origins[i - lo] // 128 * 128).tolist())
+        # every node list strictly increasing in canonical order
+        for name, first, n in (("origins", lo, hi - lo), ("lower_origins", nlo, len(lowers)),
+                               ("upper_origins", ulo, len(uppers))):
+            keys = [canon_tuple(o) for o in res[name][first:first + n]]
+            assert all(a < b for a, b in zip(keys, keys[1:])), name + " not in canonical order"
         for j in range(len(lowers)):
             p = int(res["lower_parent"][nlo + j])
             assert 0 <= p < len(uppers)

@@ -17,6 +17,7 @@ import pytest
 import oracle
 from sparse_voxel_grid_leaf_gb300 import synth
 from tests import _helpers as H
+from tests import test_oracle_pins as P
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.cpp")
 
@@ -43,6 +44,11 @@ MUTANTS = {
     "voxel_offset_global": ("int64_t vox_in_grid = 0;\n", "static int64_t vox_in_grid = 0;\n"),
     "node_counts_swapped": ("node_counts[3 * g + 0] = int32_t(G.uppers.size());",
                             "node_counts[3 * g + 0] = int32_t(G.lowers.size());"),
+    # lower-node list left in std::set's lexicographic order
+    "lowers_unsorted": ("std::sort(g.lowers.begin(), g.lowers.end(), by_canon);", ""),
+    # parent indices taken from the lexicographic order, the list itself sorted
+    "leaf_parent_lexicographic": ("for (size_t i = 0; i < g.lowers.size(); ++i) lower_index[g.lowers[i]] = int32_t(i);",
+                                  "{ int32_t i = 0; for (const Vox& v : lower_set) lower_index[v] = i++; }"),
 }
 
 
@@ -54,6 +60,9 @@ def _pins(lib):
     res = oracle.run_voxels(vox, np.array([0, len(vox)]), lib=lib)
     assert np.array_equal(res["origins"], exp)
     assert list(res["node_counts"][0]) == [int(v) for v in sec["expected_node_counts"][0]]
+
+    res, sec = P.node_order_case(lib)
+    P.check_node_order(res, sec)
 
     sec = H.read_sections("leaf_bits.txt")
     sets = [set(), set()]

@@ -51,6 +51,30 @@ def test_golden_canonical_order():
     H.check_derived(res)
 
 
+def node_order_case(lib=None):
+    """The hand-worked node-order fixture through the oracle: (result, sections)."""
+    sec = H.read_sections("node_order.txt")
+    vox = np.array([[int(v) for v in row] for row in sec["voxels"]], np.int32)
+    return oracle.run_voxels(vox, np.array([0, len(vox)], np.int64), lib=lib), sec
+
+
+def check_node_order(res, sec):
+    rows = lambda name: np.array([[int(v) for v in r] for r in sec[name]], np.int32)
+    assert np.array_equal(res["origins"], rows("expected_origins"))
+    assert np.array_equal(res["lower_origins"], rows("expected_lower_origins"))
+    assert np.array_equal(res["upper_origins"], rows("expected_upper_origins"))
+    assert res["leaf_parent"].tolist() == [int(v) for v in sec["expected_leaf_parent"][0]]
+    assert res["lower_parent"].tolist() == [int(v) for v in sec["expected_lower_parent"][0]]
+    assert list(res["node_counts"][0]) == [int(v) for v in sec["expected_node_counts"][0]]
+
+
+def test_golden_node_order():
+    # lower nodes in different root tiles: canonical order != lexicographic
+    res, sec = node_order_case()
+    check_node_order(res, sec)
+    H.check_derived(res)
+
+
 def test_golden_leaf_bits():
     sec = H.read_sections("leaf_bits.txt")
     B = int(sec["num_grids"][0][0])
