@@ -1,25 +1,32 @@
 #!/usr/bin/env python3
 """Benchmark of the batched generated-topology pass (one JSON line on stdout).
 
-Workload (default): B=16 one-voxel-thick ellipsoid shells at resolution 64
-(semi-axes U[0.30,0.48]*64, seed 0) -- the synthetic shell batches fVDB PR
-#757 times its conv-grid builders on ("Measurements": ~7.8k voxels per
-member, resolution 64, median of 20 CUDA-event iterations).
+Workload (default): stress_b64_res512 -- B=64 members at resolution 512,
+even members one-voxel-thick ellipsoid shells (semi-axes U[0.05,0.12]*512),
+odd members Bernoulli(0.02) blobs in boxes of side U{64..128}, every member
+moved to straddle a +-4096 root-tile boundary in one of the eight sign
+octants (1.31 M input voxels).  It is the largest of the workloads, all of
+which fit one GPU; the B=16 and B=48 shell batches of fVDB PR #757's
+"Measurements" (~7.8k voxels per member, resolution 64, median of 20
+CUDA-event iterations) are timed per call in the ``per_op`` table and the
+``target`` block.
 
 One step runs every pass of the hot path once over the batch, each through
 the library's C ABI:
   from_ijk (ijk front end), refine x2 (conv_transpose_grid k2s2),
   coarsen x2 (conv_grid k2s2), dilate [-1,1]^3 (conv_grid k3s1), the two pad
   octants {-1,0}^3 and {0,1}^3, the k3s2 transpose chain (refine x2 then the
-  {-1,0}^3 pad) and coarsen x4 -- 8 calls; the library fuses each chain into
-  one pass, so 8 passes.
+  {-1,0}^3 pad) and coarsen x4 -- the front end, then one tb_multi call of the
+  seven chains.
 value = output voxels of the step's calls / device time of the step.
 
 Legs: device-resident inputs (value); end to end from pinned host memory with
 the results read back (e2e); a repetition with per-kernel CUDA events for the
-roofline of the dominant kernel; the CPU oracle on a bounded sample
-(cpu_baseline).  ``--impl reference`` times the oracle alone (the reference
-arm of this benchmark).
+roofline of the dominant kernel (algorithmic bytes per pass: 76 per source
+leaf, 116 per output leaf, 24 per slot per digit pass); the CPU oracle on a
+bounded sample (cpu_baseline: one thread, primary; all host threads,
+secondary).  ``--impl reference`` times the oracle alone (the reference arm
+of this benchmark).
 """
 import argparse
 import hashlib
@@ -52,9 +59,10 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default="shells_b16_res64")
+    p.add_argument("--workload", default="stress_b64_res512")
     p.add_argument("--no-extra", action="store_true", help="skip the per-op and larger-workload tables")
-    p.add_argument("--cpu-sample-steps", type=int, default=2)
+    p.add_argument("--cpu-sample-members", type=int, default=16,
+                   help="members of the batch in the single-thread oracle sample (0: no CPU baseline)")
     p.add_argument("--separate", action="store_true", help="one C-ABI call per chain instead of one tb_multi call")
     p.add_argument("--phases", action="store_true",
                    help="only the step's per-call phase breakdown (GPU timer stamps and host timers)")
@@ -151,28 +159,56 @@ def source_hash():
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_step(ijk, off, threads):
-    """One step of the oracle, members spread over `threads` threads.
-    Returns output voxels of the step's calls (the metric's count)."""
+def oracle_step(ijk, off, threads, members=None):
+    """One step of the oracle over the given members (default: all), the
+    members spread over `threads` threads (members are independent; the
+    oracle itself is unchanged).  Returns the output voxels of the step's
+    calls on those members (the metric's count)."""
     import concurrent.futures as cf
     import numpy as np
     import oracle
     B = len(off) - 1
-    members = [(ijk[off[g]:off[g + 1]], np.array([0, off[g + 1] - off[g]], np.int64)) for g in range(B)]
-    total = 0
+    members = range(B) if members is None else members
+    subs = [(ijk[off[g]:off[g + 1]], np.array([0, off[g + 1] - off[g]], np.int64)) for g in members]
 
     def one(args):
         sub, o, ops = args
         return int(oracle.run_voxels(sub, o, ops)["voxel_counts"].sum())
 
-    jobs = []
-    for _, ops in STEP:
-        for sub, o in members:
-            jobs.append((sub, o, ops))
+    jobs = [(sub, o, ops) for _, ops in STEP for sub, o in subs]
+    if threads == 1:
+        return sum(map(one, jobs))
     with cf.ThreadPoolExecutor(max_workers=threads) as ex:
-        for v in ex.map(one, jobs):
-            total += v
-    return total
+        return sum(ex.map(one, jobs))
+
+
+def host_cores():
+    """(nproc: threads this process may run on, hardware threads of the host
+    -- std::thread::hardware_concurrency)."""
+    return cpu_threads(), os.cpu_count() or 1
+
+
+def cpu_baseline(ijk, off, n_members):
+    """The oracle, as it stands, on a bounded sample of the workload: the
+    step's eight calls on members 0..n_members-1 with one thread (primary:
+    the oracle is single-threaded), and on all members spread over every
+    host thread (secondary).  voxels/s is the metric's unit."""
+    B = len(off) - 1
+    sample = list(range(min(n_members, B)))
+    nproc, hw = host_cores()
+    t0 = time.perf_counter()
+    v1 = oracle_step(ijk, off, 1, sample)
+    dt1 = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    vn = oracle_step(ijk, off, nproc)
+    dtn = time.perf_counter() - t0
+    return {"value": v1 / dt1, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "one step (all eight calls) on members 0-%d of %d, one thread: %d output voxels in %.1f s"
+                      % (len(sample) - 1, B, v1, dt1),
+            "nproc": nproc, "hardware_concurrency": hw,
+            "threaded": {"value": vn / dtn, "unit": UNIT, "cores": nproc,
+                         "sample": "one full step (all %d members), members over %d threads: %.1f s"
+                                   % (B, nproc, dtn)}}
 
 
 def cpu_threads():
@@ -184,27 +220,41 @@ def cpu_threads():
 
 # ------------------------------------------------------------------ reference arm
 
+REF_MEMBERS_PER_STEP = 16
+
+
 def run_reference(args):
+    """The oracle timed alone on this arm's workload and metric: each step is
+    the eight calls on a block of REF_MEMBERS_PER_STEP members (rotating
+    through the batch from step to step), members over every host thread."""
     from sparse_voxel_grid_leaf_gb300 import synth
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     ijk, off = synth.make(args.workload)
-    threads = cpu_threads()
-    for _ in range(args.warmup):
-        oracle_step(ijk, off, threads)
+    B = len(off) - 1
+    threads, hw = host_cores()
+    per = min(REF_MEMBERS_PER_STEP, B) if B else 0
+
+    def block(i):
+        return [(i * per + j) % B for j in range(per)] if B else []
+    for i in range(args.warmup):
+        oracle_step(ijk, off, threads, block(i))
     t0 = time.perf_counter()
     vox = 0
-    for _ in range(args.steps):
-        vox += oracle_step(ijk, off, threads)
+    for i in range(args.steps):
+        vox += oracle_step(ijk, off, threads, block(args.warmup + i))
     dt = time.perf_counter() - t0
     value = vox / dt
+    sample = ("each step: the eight calls on %d of the %d members (a rotating block), members over %d threads"
+              % (per, B, threads))
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
-            "data": "synthetic", "config": {"workload": args.workload, "step": [s for s, _ in STEP]},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "sample": "%d full steps, members over %d threads" % (args.steps, threads)},
+            "data": "synthetic", "config": {"workload": args.workload, "step": [s for s, _ in STEP],
+                                            "members_per_step": per},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+                             "nproc": threads, "hardware_concurrency": hw},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -309,10 +359,20 @@ def kernel_bytes(ps):
     return by
 
 
+def pass_bytes(p):
+    """Algorithmic bytes of one pass: each source record read once (76 B per
+    source leaf: origin and 64-byte mask; 12 B per voxel for the ijk front
+    end), each output leaf record written once (116 B: origin, mask, voxel
+    offset, word prefix, leaf bbox), each slot's 8-byte key and 4-byte source
+    reference read and written once per digit pass (24 B per slot per pass),
+    and about 100 B of per-grid arrays per grid."""
+    src = 12 * p["L_in"] if p["kind"] == "ijk" else 76 * p["L_in"]
+    return src + 116 * p["L_out"] + 24 * p["S"] * p["P"] + 100 * p["B"]
+
+
 def pass_model_bytes(ps):
-    """Whole-pass byte model: 76 B per source leaf, 116 B per output leaf,
-    24 B per slot per digit pass."""
-    return sum(76 * p["L_in"] + 116 * p["L_out"] + 24 * p["S"] * p["P"] for p in ps)
+    """Whole-step byte model: the sum of pass_bytes over the step's passes."""
+    return sum(pass_bytes(p) for p in ps)
 
 
 def rank_batch(synth, workload, rank):
@@ -444,31 +504,28 @@ def run_ours(args):
     tot_kernel_ms = sum(ms for _, ms in prof.values())
     dom = max(prof, key=lambda k: prof[k][1])
     n_launch, dom_ms = prof[dom]
-    bytes_step = kb.get(dom, 0)
+    # algorithmic bytes of the passes the dominant (pass) kernel runs per step
+    dom_passes = [p for p in ps if p.get("kernel") == dom]
+    bytes_step = sum(pass_bytes(p) for p in dom_passes)
     achieved = bytes_step * reps / (dom_ms / 1e3) / 1e9
     traffic = kernel_traffic(dom)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": dom,
                 "bytes_per_launch": bytes_step * reps / n_launch, "us_per_launch": 1e3 * dom_ms / n_launch,
+                "launches_per_step": n_launch / reps,
+                "bytes_model": "per pass 76 L_in + 116 L_out + 24 S P + 100 B (12 per voxel for an ijk source)",
+                "passes": [{k: p[k] for k in ("kind", "L_in", "S", "P", "L_out", "B")} for p in dom_passes],
                 "share_of_kernel_time": dom_ms / tot_kernel_ms, "peak_source": peak_kind + " hbm_gbs (copy)"}
     kernels = {k: {"launches_per_step": n / reps, "us_per_launch": 1e3 * ms / n,
                    "share": ms / tot_kernel_ms,
-                   "GBps": (kb.get(k, 0) * reps / (ms / 1e3) / 1e9) if kb.get(k) else None}
+                   "phase_model_GBps": (kb.get(k, 0) * reps / (ms / 1e3) / 1e9) if kb.get(k) else None}
                for k, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1])}
     model = pass_model_bytes(ps)
 
     # ---- CPU oracle on a bounded sample (rank 0, one GPU only)
     cpu = None
-    if rank == 0 and world == 1 and args.cpu_sample_steps > 0:
-        threads = cpu_threads()
-        t0 = time.perf_counter()
-        cv = 0
-        for _ in range(args.cpu_sample_steps):
-            cv += oracle_step(ijk, off, threads)
-        dt = time.perf_counter() - t0
-        cpu = {"value": cv / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
-               "sample": "%d full steps of the same workload (all passes, all members), members over %d threads"
-                         % (args.cpu_sample_steps, threads)}
+    if rank == 0 and world == 1 and args.cpu_sample_members > 0:
+        cpu = cpu_baseline(ijk, off, args.cpu_sample_members)
 
     # ---- per-op and larger-workload tables (median of 20 after 5 warm-ups)
     extra = {}
@@ -491,7 +548,7 @@ def run_ours(args):
             "pass_model": {"bytes_per_step": model, "GBps": model / (ms_per_step / 1e3) / 1e9,
                            "frac": model / (ms_per_step / 1e3) / 1e9 / peak},
             "kernels": kernels, "gpu_launches": launches, "cpu_baseline": cpu,
-            "clocks": clk.summary(), "per_op": extra}
+            "clocks": clk.summary(), "target": target_block(extra, peak), "per_op": extra}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -508,7 +565,7 @@ def per_op_tables(tb, torch, synth, stream, flush, main_workload):
     ops = [("refine2", [("refine", 2)]), ("coarsen2", [("coarsen", 2)]), ("dilate_k3s1", [DIL]),
            ("pad_neg", [PAD_N]), ("k3s2", [("refine", 2), PAD_N]), ("coarsen4", [("coarsen", 4)]),
            ("conv_k5s1", [("dilate", (-2, -2, -2), (2, 2, 2))])]
-    for wl in (main_workload, "shells_b48_res64", "stress_b64_res512"):
+    for wl in dict.fromkeys(("shells_b16_res64", "shells_b48_res64", "stress_b64_res512", main_workload)):
         ijk, off = synth.make(wl)
         ijk_d, off_d = torch.from_numpy(ijk).cuda(), torch.from_numpy(off).cuda()
         b0 = tb.from_ijk(ijk_d, off_d)
@@ -541,6 +598,7 @@ def time_calls(calls, torch, stream, flush):
         ts = []
         vox = 0
         nbytes = 0
+        stats = None
         for it in range(25):
             flush.zero_()
             s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -555,6 +613,10 @@ def time_calls(calls, torch, stream, flush):
                 rs = r if isinstance(r, list) else [r]
                 if it == 0:
                     vox = sum(int(x.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for x in rs)
+                    one = rs[0] if len(rs) == 1 else None
+                    stats = None if one is None else {
+                        "L_in": one.build_source_leaves, "S": one.build_slots, "P": one.build_digit_passes,
+                        "L_out": one.num_leaves, "B": one.num_grids}
                 for x in rs:
                     x.free()
             if it >= 5:
@@ -564,11 +626,34 @@ def time_calls(calls, torch, stream, flush):
             row[lab] = {"ms": med, "map_bytes": nbytes, "map_GBps": nbytes / med / 1e6}
         else:
             row[lab] = {"ms": med, "out_voxels": vox, "Gvox_per_s": vox / med / 1e6}
+            if stats is not None:
+                row[lab]["last_pass"] = stats
     return row
 
 
+def target_block(per_op, peak):
+    """The single conv-grid calls at B=48 and at stress size against the HBM
+    roofline: ms per call (median of 20, L2 flushed) and the call's
+    algorithmic bytes (pass_bytes) over that time, as a fraction of the
+    measured copy bandwidth.  Each of these calls is one pass."""
+    out = {}
+    kinds = {"refine2": "refine", "coarsen2": "coarsen", "dilate_k3s1": "dilate"}
+    for wl in ("shells_b48_res64", "stress_b64_res512"):
+        for lab, kind in kinds.items():
+            r = (per_op.get(wl) or {}).get(lab)
+            if not r or "last_pass" not in r:
+                continue
+            p = dict(r["last_pass"], kind=kind)
+            nbytes = pass_bytes(p)
+            gbps = nbytes / (r["ms"] / 1e3) / 1e9
+            out["%s/%s" % (wl, lab)] = {"ms": r["ms"], "bytes": nbytes, "GBps": gbps, "frac": gbps / peak,
+                                        "S": p["S"], "P": p["P"], "L_in": p["L_in"], "L_out": p["L_out"]}
+    return out
+
+
 def phase_table(tb, torch, synth, workload, steps):
-    """Where a step's time goes, per call (the front end; the tb_multi call):
+    """Where a step's time goes, per call (the front end; the tb_multi call;
+    refine x2, coarsen x2 and dilate [-1,1]^3 alone):
     mean microseconds per call of each kernel and of each pass-kernel phase
     (GPU global-timer stamps: entry to the first emission, emission, digit
     passes, index, leaves, voxel offsets) and of the host's share of the
@@ -579,7 +664,9 @@ def phase_table(tb, torch, synth, workload, steps):
     plan = tb.MultiPlan([ops for _, ops in STEP[1:]])
     res = {}
     b0 = tb.from_ijk(ijk_d, off_d)
-    for label, fn in [("from_ijk", lambda: tb.from_ijk(ijk_d, off_d)), ("multi7", lambda: plan(b0))]:
+    calls = [("from_ijk", lambda: tb.from_ijk(ijk_d, off_d)), ("multi7", lambda: plan(b0))] + \
+            [(lab, (lambda o=o: tb.chain(b0, o))) for lab, o in STEP[1:4]]
+    for label, fn in calls:
         for _ in range(5):
             fn()
         torch.cuda.synchronize()

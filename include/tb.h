@@ -75,7 +75,8 @@ typedef enum {
   TB_ERR_COORD_OVERFLOW = 4,  /* an output coordinate would leave int32              */
   TB_ERR_NOT_CANONICAL = 5,   /* tb_validate found an order/mask/offset violation    */
   TB_ERR_DEVICE_TIMEOUT = 6,  /* a bounded device-side wait gave up (result invalid) */
-  TB_ERR_TOO_LARGE = 7        /* sizes beyond the library's documented limits        */
+  TB_ERR_TOO_LARGE = 7,       /* sizes beyond the library's documented limits        */
+  TB_ERR_INTERNAL = 8         /* an internal bound of the library was exceeded (bug) */
 } tb_status;
 
 typedef struct tb_allocator {
@@ -331,16 +332,20 @@ typedef struct tb_out_buffers {
  *   (duplicates merge); out: caller-owned output buffers (see tb_out_buffers);
  *   out_counts: optional host int64[3] receiving the output's leaf, lower-node
  *   and upper-node totals (also written when the capacity check fails).
+ * Every input and output pointer must be device memory (or managed memory):
+ * a host pointer returns TB_ERR_INVALID_ARG before any launch.
  * Scratch is one static device array of 32 MiB that every GPU loading the
  * library holds until the process exits; about 52 bytes per candidate leaf
  * (8 per input leaf) plus per-grid control, so inputs of up to roughly 75k
- * leaves fit.  Larger inputs, or outputs beyond the given capacities, return
- * TB_ERR_TOO_LARGE before anything is written.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress); make it before
- * any stream capture.  Calls share the array and its contents persist: each
- * call clears its control region first, and calls that overlap on the GPU
- * race.  Blocks twice (range readback, count readback) into host stack
- * memory. */
+ * leaves fit.  An input that cannot fit (more than 80,659 leaves) returns
+ * TB_ERR_TOO_LARGE before any launch; one whose key layout needs more room,
+ * or outputs beyond the given capacities, return TB_ERR_TOO_LARGE before
+ * anything is written.  Each call looks up the array's device address on the
+ * current device (cudaGetSymbolAddress); the first lookup on a device can
+ * load the library's device code, so make the first call before any stream
+ * capture.  Calls share the array and its contents persist: each call clears
+ * its control region first, and calls that overlap on the GPU race.  Blocks
+ * twice (range readback, count readback) into host stack memory. */
 TB_API tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const int64_t* leaf_offsets,
                                   int32_t num_grids, int64_t num_leaves, const tb_out_buffers* out,
                                   int64_t* out_counts, tb_stream stream);
@@ -375,6 +380,19 @@ TB_API int32_t tb_profile_read(tb_kernel_stat* stats, int32_t max);
  * input.  Both give identical outputs.  Process-wide; returns the previous
  * mode, or -1 (mode unchanged) for a mode outside 0..2. */
 TB_API int32_t tb_set_launch_mode(int32_t mode);
+
+/* How the whole-grid kernel puts a pass's output leaves in canonical order
+ * (library extension; PR #757, Summary item 1, names the canonical NanoVDB
+ * node order, which both ways produce).  mode 0 (default): where the pass's
+ * output can hold at most 16384 lower nodes (a bound from the source's lower
+ * nodes, or its voxel / leaf count for a front end), the node path: every
+ * target leaf sets its bit in its lower node's 4096-bit child mask, the few
+ * lower nodes are ranked by canonical key and every leaf's index is its
+ * node's leaf base plus the set bits before it -- no radix sort; elsewhere
+ * the radix sort and head-flag scan.  mode 1: always the radix sort.  Both
+ * give identical outputs.  Process-wide; returns the previous mode, or -1
+ * (mode unchanged) for a mode outside 0..1. */
+TB_API int32_t tb_set_node_mode(int32_t mode);
 
 /* Number of kernels this thread has launched through the library so far. */
 TB_API int64_t tb_kernel_launch_count(void);

@@ -178,15 +178,18 @@ def batch_voxels(result: Dict[str, np.ndarray]) -> Tuple[np.ndarray, np.ndarray]
     index n = 64 x + 8 y + z (fVDB PR #757: every build path enumerates voxels
     identically) -- as ``(ijk [V,3], offsets [B+1])``."""
     origins, masks, lo = result["origins"], result["masks"], result["leaf_offsets"]
-    out, offs = [], [0]
-    for g in range(len(lo) - 1):
-        for i in range(int(lo[g]), int(lo[g + 1])):
-            o = origins[i]
-            for n in range(512):
-                if (int(masks[i][n >> 6]) >> (n & 63)) & 1:
-                    out.append((int(o[0]) + (n >> 6), int(o[1]) + ((n >> 3) & 7), int(o[2]) + (n & 7)))
-        offs.append(len(out))
-    return np.array(out, np.int32).reshape(-1, 3), np.array(offs, np.int64)
+    L = origins.shape[0]
+    # bit n of a leaf is bit n & 63 of word n >> 6; the little-endian bytes of
+    # the eight words, unpacked low bit first, list the bits in ascending n
+    bits = np.unpackbits(np.ascontiguousarray(masks, np.uint64).view(np.uint8).reshape(L, 64), axis=1,
+                         bitorder="little")
+    leaf, n = np.nonzero(bits)            # row-major: leaf by leaf, ascending n
+    local = np.stack([n >> 6, (n >> 3) & 7, n & 7], axis=1)
+    ijk = (origins[leaf].astype(np.int64) + local).astype(np.int32).reshape(-1, 3)
+    per_leaf = bits.sum(axis=1, dtype=np.int64)
+    first = np.concatenate([[0], np.cumsum(per_leaf)])
+    offs = first[np.asarray(lo, np.int64)]
+    return ijk, offs.astype(np.int64)
 
 
 def run_masked_refine(result: Dict[str, np.ndarray], voxel_mask: np.ndarray, factor: int,

@@ -33,7 +33,7 @@ LIB_PATH = os.path.join(_HERE, "libtb.so")
 TB_OK = 0
 STATUS_NAMES = {0: "TB_OK", 1: "TB_ERR_INVALID_ARG", 2: "TB_ERR_OOM", 3: "TB_ERR_CUDA",
                 4: "TB_ERR_COORD_OVERFLOW", 5: "TB_ERR_NOT_CANONICAL", 6: "TB_ERR_DEVICE_TIMEOUT",
-                7: "TB_ERR_TOO_LARGE"}
+                7: "TB_ERR_TOO_LARGE", 8: "TB_ERR_INTERNAL"}
 OP_REFINE, OP_COARSEN, OP_BOX_DILATE = 0, 1, 2
 
 
@@ -113,6 +113,8 @@ def lib():
             L.tb_profile_read.restype = ctypes.c_int32
             L.tb_set_launch_mode.argtypes = [ctypes.c_int32]
             L.tb_set_launch_mode.restype = ctypes.c_int32
+            L.tb_set_node_mode.argtypes = [ctypes.c_int32]
+            L.tb_set_node_mode.restype = ctypes.c_int32
             _lib = L
         return _lib
 
@@ -164,6 +166,16 @@ def set_launch_mode(mode: str) -> str:
     if prev < 0:
         raise ValueError("launch mode %r" % (mode,))
     return {v: k for k, v in LAUNCH_MODES.items()}[prev]
+
+
+def set_node_mode(mode: str) -> str:
+    """How the whole-grid kernel orders a pass's output leaves, for the whole
+    process: "auto" (lower-node child masks where the output's lower nodes are
+    few, else the radix sort) or "sort".  Returns the previous mode."""
+    prev = lib().tb_set_node_mode({"auto": 0, "sort": 1}[mode])
+    if prev < 0:
+        raise ValueError("node mode %r" % (mode,))
+    return {0: "auto", 1: "sort"}[prev]
 
 
 def profile_enable(on=True):

@@ -249,7 +249,9 @@ struct Pinned {
 thread_local Pinned t_pinned;
 thread_local unsigned int t_seq = 0;  // readback flag values of this thread's calls
 
-bool device_accessible(const void* p) {
+}  // namespace
+
+bool tb::device_accessible(const void* p) {
   if (!p) return false;
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
@@ -258,6 +260,8 @@ bool device_accessible(const void* p) {
   }
   return at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged;
 }
+
+namespace {
 
 // ---------------------------------------------------------------- pass plan
 
@@ -274,6 +278,14 @@ struct PassPlan {
   int32_t bbox[6];           // output voxel bbox (exact)
   KeyLayout K;
   int P = 0;
+  // node path (see PassArgs): the bound on the output's lower nodes, and the
+  // workspace of the node tables
+  bool node = false;
+  int node_zero = 0, mid = 0, node_cap = 0;
+  long long node_bound = 0;
+  uint32_t node_hslots = 0;
+  size_t nh_key = 0, th_key = 0, node_mask = 0, gmin = 0, node_key = 0, node_lc = 0, node_tile = 0, node_rank = 0,
+         node_wpre = 0, rank_cnt = 0, tile_rank = 0, node_list = 0, tile_list = 0, nref = 0;
   long long sort_tiles = 0, dedup_tiles = 0;
   size_t rb = 0, ctl = 0, sort_status = 0, dedup_status = 0, first = 0;
   size_t unit_ctl = 0;       // member launches: the members' control blocks
@@ -317,6 +329,32 @@ int member_ctas(int n_chain, int32_t B, long long count, long long nmax, long lo
 }
 
 long long slots_per_source(const PassSpec& s) { return pass_targets(s.op, s.factor, s.lo, s.hi); }
+
+// 0: the node path wherever its bound allows (whole-grid launches), 1: never
+// (tb_set_node_mode).
+std::atomic<int> g_node_mode{0};
+// Staged masks of a node-path pass are cleared in its nodes phase (no phase
+// of their own) when its slots' masks take at most this many bytes.
+constexpr long long kNodeClearInline = 16ll << 20;
+
+// How many output lower nodes one source lower node can reach in a pass: a
+// lower node spans 128 voxels per axis; refinement by f spreads it over f
+// nodes per axis, coarsening keeps it inside one, a box dilation by at most
+// 7 voxels reaches one more node on each side it extends to, and the fused
+// refine-then-dilate reaches one more beyond the refined 2.
+long long node_factor(const PassSpec& s) {
+  auto side = [&](int base) {
+    long long f = 1;
+    for (int a = 0; a < 3; ++a) f *= base + (s.lo[a] < 0 ? 1 : 0) + (s.hi[a] > 0 ? 1 : 0);
+    return f;
+  };
+  switch (s.op) {
+    case kRefine: return (long long)s.factor * s.factor * s.factor;
+    case kDilate: return side(1);
+    case kRefineDilate: return side(2);
+    default: return 1;  // coarsening; the front ends (bound: one node per source)
+  }
+}
 
 // Output bbox of one pass from its input bbox; false on int32 overflow.
 bool propagate_bbox(const PassSpec& s, const int32_t in[6], int32_t out[6]) {
@@ -542,6 +580,30 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     }
   }
 
+  // ---- node path: passes of the whole-grid kernel whose output lower nodes
+  // are bounded by kNodeCap (the bound follows the source's lower nodes
+  // through the chain; a front end's is its source count)
+  for (auto& pc : plans) {
+    long long bound = src.kind == kSrcBatch ? std::max<long long>(src.batch->NL, 1) : std::max(src.count, 1ll);
+    for (auto& pl : pc) {
+      const long long f = node_factor(pl.spec);
+      bound = bound > pl.slot_cap / f ? pl.slot_cap : std::min(pl.slot_cap, bound * f);
+      bound = std::max(bound, 1ll);
+      pl.node_bound = bound;
+      pl.node = !cl && g_node_mode.load() == 0 && bound <= kNodeCap;
+      if (pl.node) {
+        pl.node_zero = pl.spec.op == kRefine ? 0 : (pl.slot_cap * 64 <= kNodeClearInline ? 1 : 2);
+        pl.mid = pl.node_zero == 2 ? 3 : 2;
+        pl.node_cap = (int)bound;
+        uint32_t h = 64;  // ids are table slots: room for the bound with probes to spare
+        while (h < (uint32_t)bound + (uint32_t)bound / 4u + 16u) h <<= 1;
+        pl.node_hslots = h;
+      } else {
+        pl.mid = pl.P;
+      }
+    }
+  }
+
   // ---- workspace: a zeroed control region (the call's error word and the
   // last passes' readback blocks first, so one copy reads them all), then the
   // slot buffers of every chain
@@ -567,9 +629,15 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       pl.dedup_tiles = std::max(1ll, (pl.slot_cap + kDedupTile - 1) / kDedupTile);
       pl.rb = p + 1 == plans[ch].size() ? o_rb_last[ch] : c.take(rb_bytes);
       pl.ctl = c.take(sizeof(PassCtl));
-      pl.sort_status = c.take((size_t)pl.P * pl.sort_tiles * kBins * 4);
-      pl.dedup_status = c.take((size_t)pl.dedup_tiles * 3 * 8);
+      pl.sort_status = c.take(pl.node ? 0 : (size_t)pl.P * pl.sort_tiles * kBins * 4);
+      pl.dedup_status = c.take(pl.node ? 0 : (size_t)pl.dedup_tiles * 3 * 8);
       pl.first = c.take((size_t)3 * B * 4);
+      if (pl.node) {  // the node tables that start empty
+        pl.nh_key = c.take((size_t)pl.node_hslots * 8);
+        pl.th_key = c.take((size_t)pl.node_hslots * 8);
+        pl.node_mask = c.take((size_t)pl.node_hslots * 512);
+        pl.gmin = c.take((size_t)2 * B * 4);
+      }
     }
   size_t n_pass_total = 0;
   for (auto& pc : plans) n_pass_total += pc.size();
@@ -628,6 +696,21 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       b.inter[k][2] = c.take((size_t)max_inter[k] * 4);
     }
   }
+  for (auto& pc : plans)
+    for (auto& pl : pc)
+      if (pl.node) {
+        const size_t hs = (size_t)pl.node_hslots;
+        pl.node_key = c.take(hs * 8);
+        pl.node_lc = c.take(hs * 16);
+        pl.node_tile = c.take(hs * 4);
+        pl.node_rank = c.take(hs * 4);
+        pl.node_wpre = c.take(hs * 256);
+        pl.rank_cnt = c.take((size_t)pl.node_cap * 4);
+        pl.tile_rank = c.take(hs * 4);
+        pl.node_list = c.take((size_t)pl.node_cap * 4);
+        pl.tile_list = c.take((size_t)pl.node_cap * 4);
+        pl.nref = c.take((size_t)pl.slot_cap * 4);
+      }
   const size_t o_args = c.take(sizeof(PassArgs) * (size_t)n_chain * n_stage);
   // staging of host-resident inputs
   const int32_t* in_ijk = src.ijk;
@@ -696,12 +779,38 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       a.K = pl.K;
       a.op = pl.spec.op;
       a.B = B;
-      a.P = pl.P;
+      a.P = pl.node ? 0 : pl.P;
+      a.mid = pl.mid;
+      if (pl.node) {
+        a.node = 1;
+        a.node_zero = pl.node_zero;
+        a.node_cap = pl.node_cap;
+        a.node_hmask = pl.node_hslots - 1u;
+        a.nh_key = (unsigned long long*)(ws + pl.nh_key);
+        a.th_key = (unsigned long long*)(ws + pl.th_key);
+        a.node_mask = (uint64_t*)(ws + pl.node_mask);
+        a.gmin = (uint32_t*)(ws + pl.gmin);
+        a.node_key = (uint64_t*)(ws + pl.node_key);
+        a.node_lc = (int32_t*)(ws + pl.node_lc);
+        a.node_tile = (uint32_t*)(ws + pl.node_tile);
+        a.node_rank = (uint32_t*)(ws + pl.node_rank);
+        a.node_wpre = (uint32_t*)(ws + pl.node_wpre);
+        a.rank_cnt = (uint32_t*)(ws + pl.rank_cnt);
+        a.tile_rank = (uint32_t*)(ws + pl.tile_rank);
+        a.node_list = (uint32_t*)(ws + pl.node_list);
+        a.tile_list = (uint32_t*)(ws + pl.tile_list);
+        a.nref = (uint32_t*)(ws + pl.nref);
+      }
       a.last = k + 1 == (int)plans[ch].size();
       {  // targets per emission thread: about one round of the grid's threads
+        // (the node path: about four rounds, so the grid's blocks finish together)
         const long long T = slots_per_source(pl.spec);
         const long long want = (pl.in_cap * T + (long long)G * 256 - 1) / ((long long)G * 256);
         a.tchunk = (int32_t)std::max(1ll, std::min({T, want, 32ll}));
+        if (pl.node) {
+          const long long chunks = std::max(1ll, std::min(T, (4ll * G * 256 + pl.in_cap - 1) / std::max(1ll, pl.in_cap)));
+          a.tchunk = (int32_t)std::max(1ll, std::min(32ll, (T + chunks - 1) / chunks));
+        }
       }
       for (int ax = 0; ax < 3; ++ax) {
         a.lo[ax] = pl.spec.lo[ax];
@@ -964,7 +1073,7 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   }
   const unsigned int err = *(const unsigned int*)(pinned + o_err);
   if (err & kErrTimeout) return fail(TB_ERR_DEVICE_TIMEOUT, "a device-side wait timed out");
-  if (err & kErrSlotOverflow) return fail(TB_ERR_CUDA, "internal: emitted slots exceeded the bound");
+  if (err & kErrSlotOverflow) return fail(TB_ERR_INTERNAL, "internal: emitted slots exceeded the bound");
   if (front) {  // the layout the kernel planned, again on the host, for the batch and the writer
     if (err & kErrBadOffsets)
       return fail(TB_ERR_INVALID_ARG, "offsets must start at 0, be non-decreasing and end at %lld", src.count);
@@ -1037,7 +1146,7 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
     b->build_slots = (int64_t)hr->num_slots;
     b->build_sources = plans[ch].size() == 1 ? (int64_t)last.in_cap : -1;
     b->build_key_bits = last.K.W;
-    b->build_digit_passes = last.P;
+    b->build_digit_passes = last.node ? 0 : last.P;  // the node path sorts nothing
     b->build_member_ctas = cl;
   }
   if (!redo.empty()) {
@@ -1583,6 +1692,7 @@ const char* tb_status_string(tb_status s) {
     case TB_ERR_NOT_CANONICAL: return "TB_ERR_NOT_CANONICAL";
     case TB_ERR_DEVICE_TIMEOUT: return "TB_ERR_DEVICE_TIMEOUT";
     case TB_ERR_TOO_LARGE: return "TB_ERR_TOO_LARGE";
+    case TB_ERR_INTERNAL: return "TB_ERR_INTERNAL";
   }
   return "TB_ERR_UNKNOWN";
 }
@@ -1594,6 +1704,11 @@ int64_t tb_kernel_launch_count(void) { return t_launches; }
 int32_t tb_set_launch_mode(int32_t mode) {
   if (mode < 0 || mode > 2) return -1;
   return g_launch_mode.exchange(mode);
+}
+
+int32_t tb_set_node_mode(int32_t mode) {
+  if (mode < 0 || mode > 1) return -1;
+  return g_node_mode.exchange(mode);
 }
 
 tb_status tb_profile_enable(int32_t on) {

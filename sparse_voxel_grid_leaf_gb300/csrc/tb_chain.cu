@@ -49,6 +49,13 @@ struct SmemSort {
 struct SmemEmit {
   unsigned int hist[kMaxDigitPasses][kBins];
 };
+// Node path emission: the child-mask bits of a few lower nodes gathered per
+// block and flushed to the node tables once at the end of the phase.
+constexpr int kNodeSlots = 8;
+struct SmemNodes {
+  uint32_t id[kNodeSlots];              // node id + 1, 0: free
+  uint32_t mask[kNodeSlots][128];       // child mask as 32-bit words
+};
 struct SmemDedup {
   unsigned long long scan[8];
   unsigned long long base[3];
@@ -65,7 +72,13 @@ struct SmemLeaves {
 struct SmemFinish {
   uint32_t s[kThreads];
 };
+struct SmemPlace {
+  uint32_t base[kNodeCap];  // leaves before the node of each rank
+  uint32_t scan[8];
+};
 union Smem {
+  SmemPlace place;
+  SmemNodes nodes;
   SmemSort sort;
   SmemEmit emit;
   SmemDedup dedup;
@@ -81,6 +94,120 @@ __device__ __forceinline__ void stamp(const PassArgs& a, int k) {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     atomicMax(&a.phase_ts[k], k == 0 ? ~t : t);
+  }
+}
+
+// ---------------------------------------------------------------- node path: lower-node child masks
+
+// Hash of a node or tile key (the splitmix64 finaliser).
+__device__ __forceinline__ uint32_t mix_key(uint64_t z) {
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  return (uint32_t)(z ^ (z >> 31));
+}
+
+// Id of `key` in an open-addressing table of key + 1 per slot (0: free;
+// zeroed): the key's slot, claimed by compare-and-swap when the key is new,
+// in which case `made(id)` runs in the claiming thread.  The id is the slot
+// itself, so a thread that finds the key needs nothing more (no counter, no
+// wait); what made() writes is read after a grid barrier.  Relaxed loads at
+// GPU scope.
+template <class Made>
+__device__ __forceinline__ uint32_t table_id(const PassArgs& a, unsigned long long* keys, uint64_t key, Made made) {
+  const unsigned long long want = key + 1ull;
+  uint32_t h = mix_key(key) & a.node_hmask;
+  for (uint32_t probe = 0; probe <= a.node_hmask; ++probe, h = (h + 1u) & a.node_hmask) {
+    unsigned long long cur = ld_relaxed(keys + h);
+    if (cur == 0ull) {
+      cur = atomicCAS(keys + h, 0ull, want);
+      if (cur == 0ull) {
+        made(h);
+        return h;
+      }
+    }
+    if (cur == want) return h;
+  }
+  atomicOr(a.err, kErrSlotOverflow);  // table full: the host's bound was wrong
+  return 0;
+}
+
+// Lower node `nk` (key >> lower_bits of target leaf tl in grid g): its id,
+// made if new, and its slot in the block's cache of child masks (-1: none;
+// a slot is claimed by its id).
+__device__ __forceinline__ uint32_t node_lookup(const PassArgs& a, SmemNodes* sn, uint64_t nk, uint64_t key,
+                                                const int32_t tl[3], uint32_t g, int& slot) {
+  const KeyLayout& K = a.K;
+  const uint32_t id = table_id(a, a.nh_key, nk, [&](uint32_t nid) {
+    a.node_key[nid] = nk;
+    int32_t* nl = a.node_lc + 4ull * nid;
+    nl[0] = tl[0] >> 4;
+    nl[1] = tl[1] >> 4;
+    nl[2] = tl[2] >> 4;
+    nl[3] = (int32_t)g;
+    const uint64_t tk = shr64(key, K.node_bits);
+    a.node_tile[nid] = table_id(a, a.th_key, tk, [&](uint32_t tid) {
+      const uint32_t li = atomicAdd(&a.ctl->n_tiles, 1u);  // the compact list of tiles
+      if (li < (uint32_t)a.node_cap) a.tile_list[li] = tid;
+    });
+    const uint32_t li = atomicAdd(&a.ctl->n_nodes, 1u);  // the compact list of nodes
+    if (li < (uint32_t)a.node_cap) a.node_list[li] = nid;
+    else atomicOr(a.err, kErrSlotOverflow);
+  });
+  slot = -1;
+  if (!sn) return id;
+  for (int j = 0; j < kNodeSlots; ++j) {
+    const uint32_t v = *reinterpret_cast<volatile uint32_t*>(&sn->id[j]);
+    if (v == id + 1u) {
+      slot = j;
+      break;
+    }
+    if (v == 0u) {
+      const uint32_t old = atomicCAS(&sn->id[j], 0u, id + 1u);
+      if (old == 0u || old == id + 1u) {
+        slot = j;
+        break;
+      }
+    }
+  }
+  return id;
+}
+
+// A run of child-mask bits of one 32-bit word of one node, merged in
+// registers before its one atomic OR (into the block cache, or the node
+// table for a node without a cache slot).
+struct NodeRun {
+  uint32_t id, w32, bits;
+  int slot;
+};
+__device__ __forceinline__ void run_flush(const PassArgs& a, SmemNodes& sn, NodeRun& run) {
+  if (!run.bits) return;
+  if (run.slot >= 0) {
+    atomicOr(&sn.mask[run.slot][run.w32], run.bits);
+  } else {
+    atomicOr(reinterpret_cast<unsigned int*>(a.node_mask + 64ull * run.id) + run.w32, run.bits);
+  }
+  run.bits = 0;
+}
+
+// The end of a node-path emission: the block's gathered child-mask bits go
+// to the node tables, one atomic OR per non-zero 64-bit word.
+__device__ __forceinline__ void emit_flush(const PassArgs& a, SmemNodes& sn) {
+  __syncthreads();
+  for (int i = threadIdx.x; i < kNodeSlots * 64; i += kThreads) {
+    const int j = i >> 6, w = i & 63;
+    const uint32_t id1 = sn.id[j];
+    if (!id1) continue;  // a slot is used only once its id is set
+    const unsigned long long v = (unsigned long long)sn.mask[j][2 * w] | ((unsigned long long)sn.mask[j][2 * w + 1] << 32);
+    if (v) atomicOr(reinterpret_cast<unsigned long long*>(a.node_mask) + 64ull * (id1 - 1u) + w, v);
+  }
+}
+
+__device__ __forceinline__ void put_node_slot(const PassArgs& a, unsigned long long pos, uint32_t nref, uint32_t val) {
+  if (pos < (unsigned long long)a.slot_cap) {
+    a.nref[pos] = nref;
+    a.vals[0][pos] = val;
+  } else {
+    atomicOr(a.err, kErrSlotOverflow);
   }
 }
 
@@ -234,6 +361,43 @@ __device__ __forceinline__ bool target_nonempty(const PassArgs& a, const uint64_
   out[1] = lc[1] + ty;
   out[2] = lc[2] + tz;
   return (xs & ym & zm) != 0;
+}
+
+// The slot code and leaf coordinate of target `t` of a source leaf at leaf
+// coordinate lc (the geometry of target_nonempty, without its test).
+template <int OP>
+__device__ __forceinline__ void target_geometry(const PassArgs& a, const int32_t lc[3], uint32_t t, uint32_t& code,
+                                                int32_t out[3]) {
+  if constexpr (OP == kRefine) {
+    const int f = a.factor;
+    const int cx = (int)t / (f * f), cy = ((int)t / f) % f, cz = (int)t % f;
+    code = t;
+    out[0] = f * lc[0] + cx;
+    out[1] = f * lc[1] + cy;
+    out[2] = f * lc[2] + cz;
+  } else if constexpr (OP == kLeaves || OP == kCoarsen) {
+    const int sh = OP == kCoarsen ? log2_factor(a.factor) : 0, fm = (1 << sh) - 1;
+    code = OP == kCoarsen ? (uint32_t)((((lc[0] & fm) << sh) | (lc[1] & fm)) << sh | (lc[2] & fm)) : 0u;
+    out[0] = lc[0] >> sh;
+    out[1] = lc[1] >> sh;
+    out[2] = lc[2] >> sh;
+  } else if constexpr (OP == kRefineDilate) {
+    const int tlx = refine_dilate_lo(a.lo[0]), tly = refine_dilate_lo(a.lo[1]), tlz = refine_dilate_lo(a.lo[2]);
+    const int ny = refine_dilate_hi(a.hi[1]) - tly + 1, nz = refine_dilate_hi(a.hi[2]) - tlz + 1;
+    const int tz = tlz + (int)(t % nz), ty = tly + (int)((t / nz) % ny), tx = tlx + (int)(t / (nz * ny));
+    code = (uint32_t)(((tx + 1) * 4 + (ty + 1)) * 4 + (tz + 1));
+    out[0] = 2 * lc[0] + tx;
+    out[1] = 2 * lc[1] + ty;
+    out[2] = 2 * lc[2] + tz;
+  } else {  // kDilate
+    const int tlx = a.lo[0] < 0 ? -1 : 0, tly = a.lo[1] < 0 ? -1 : 0, tlz = a.lo[2] < 0 ? -1 : 0;
+    const int ny = (a.hi[1] > 0 ? 1 : 0) - tly + 1, nz = (a.hi[2] > 0 ? 1 : 0) - tlz + 1;
+    const int tz = tlz + (int)(t % nz), ty = tly + (int)((t / nz) % ny), tx = tlx + (int)(t / (nz * ny));
+    code = (uint32_t)(9 * (tx + 1) + 3 * (ty + 1) + (tz + 1));
+    out[0] = lc[0] + tx;
+    out[1] = lc[1] + ty;
+    out[2] = lc[2] + tz;
+  }
 }
 
 // Targets per source leaf of an op.
@@ -963,7 +1127,482 @@ __device__ void phase_voxel_offsets(const PassArgs& a, Smem& sm, int vb, int vg)
   }
 }
 
+// ---------------------------------------------------------------- node path phases
+
+// After the emission: a warp per lower node (in the list the emission kept)
+// takes its child mask's popcount prefix per word and its leaf count,
+// and ranks the node among all nodes by canonical key (node keys are
+// unique); a warp per tile ranks the tile.  The per-grid first node and tile
+// ranks and the totals follow.  With node_zero == 1 the staged masks of the
+// pass's slots are cleared here too.
+__device__ __noinline__ void phase_nodes(const PassArgs& a, int vb, int vg) {
+  const uint32_t n = min(__ldcg(&a.ctl->n_nodes), (uint32_t)a.node_cap);
+  const uint32_t nt = min(__ldcg(&a.ctl->n_tiles), (uint32_t)a.node_cap);
+  const int lane = threadIdx.x & 31;
+  const KeyLayout& K = a.K;
+  const long long nw = (long long)vg * (kThreads / 32);
+  for (long long it = (long long)vb * (kThreads / 32) + (threadIdx.x >> 5); it < (long long)n + nt; it += nw) {
+    if (it < (long long)n) {  // a lower node
+      const uint32_t id = __ldcg(a.node_list + it);
+      const unsigned long long k1 = __ldcg(a.nh_key + id);
+      const uint64_t* m = a.node_mask + 64ull * id;
+      const uint64_t x0 = __ldcg(m + 2 * lane), x1 = __ldcg(m + 2 * lane + 1);
+      const uint32_t c0 = __popcll(x0), c = c0 + __popcll(x1);
+      uint32_t incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      a.node_wpre[64ull * id + 2 * lane] = incl - c;
+      a.node_wpre[64ull * id + 2 * lane + 1] = incl - c + c0;
+      const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+      uint32_t r = 0;  // the nodes that sort before this one
+      for (uint32_t j = lane; j < n; j += 32) r += __ldcg(a.nh_key + __ldcg(a.node_list + j)) < k1 ? 1u : 0u;
+      r = __reduce_add_sync(0xffffffffu, r);
+      if (lane == 0) {
+        a.node_rank[id] = r;
+        a.rank_cnt[r] = total;
+        atomicAdd(&a.ctl->head_totals[0], (unsigned long long)total);
+        atomicMax(a.gmin + __ldcg(a.node_lc + 4ull * id + 3), ~r);
+      }
+    } else {  // a tile
+      const uint32_t t = __ldcg(a.tile_list + (it - n));
+      const unsigned long long k1 = __ldcg(a.th_key + t);
+      uint32_t r = 0;
+      for (uint32_t j = lane; j < nt; j += 32) r += __ldcg(a.th_key + __ldcg(a.tile_list + j)) < k1 ? 1u : 0u;
+      r = __reduce_add_sync(0xffffffffu, r);
+      if (lane == 0) {
+        a.tile_rank[t] = r;
+        const uint32_t g = K.gw ? (uint32_t)shr64(k1 - 1ull, K.gshift - K.node_bits) : 0u;
+        atomicMax(a.gmin + a.B + g, ~r);
+      }
+    }
+  }
+  if (a.node_zero == 1) {  // clear the staged masks of up to one leaf per slot
+    long long S = (long long)__ldcg(&a.rb->num_slots);
+    if (S > a.slot_cap) S = a.slot_cap;
+    uint4* z = reinterpret_cast<uint4*>(a.out_masks);
+    for (long long i = (long long)vb * kThreads + threadIdx.x; i < 4 * S; i += (long long)vg * kThreads)
+      z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// The clear phase of node_zero == 2: the staged masks of the pass's leaves.
+__device__ void phase_clear(const PassArgs& a, int vb, int vg) {
+  const long long U = (long long)__ldcg(&a.ctl->head_totals[0]);
+  uint4* z = reinterpret_cast<uint4*>(a.out_masks);
+  for (long long i = (long long)vb * kThreads + threadIdx.x; i < 4 * U; i += (long long)vg * kThreads)
+    z[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// The eight words of one target's contribution to its target leaf, from the
+// source leaf's mask m (target code `code`; for the ijk front end `code` is
+// the voxel's bit n = 64 x + 8 y + z in its leaf).
+template <int OP>
+__device__ __forceinline__ void contrib_words(const PassArgs& a, const uint64_t m[8], uint32_t code, uint64_t c[8]) {
+#pragma unroll
+  for (int k = 0; k < 8; ++k) c[k] = 0;
+  if constexpr (OP == kIjk) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c[k] = ((int)(code >> 6) == k) ? 1ull << (code & 63u) : 0ull;
+  } else if constexpr (OP == kLeaves) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c[k] = m[k];
+  } else if constexpr (OP == kRefine) {
+    const int f = a.factor;
+    if (f == 2) {  // child (cx, cy, cz): word k from parent word 4 cx + k / 2
+      const int cx = (code >> 2) & 1, cy = (code >> 1) & 1, cz = code & 1;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) c[k] = refine_word(cx ? m[4 + (k >> 1)] : m[k >> 1], cy, cz);
+      return;
+    }
+    const int cx = (int)code / (f * f), cy = ((int)code / f) % f, cz = (int)code % f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int j = (8 * cx + k) / f;
+      uint64_t pw = 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) pw = q == j ? m[q] : pw;
+      c[k] = refine_word_f(pw, cy, cz, f);
+    }
+  } else if constexpr (OP == kCoarsen) {
+    const int f = a.factor;
+    if (f == 2) {
+      const int qx = (code >> 2) & 1, qy = (code >> 1) & 1, qz = code & 1;
+#pragma unroll
+      for (int X = 0; X < 4; ++X) {
+        const uint64_t cw = coarsen_word(m[2 * X] | m[2 * X + 1], qy, qz);
+        c[X] = qx == 0 ? cw : 0ull;
+        c[4 + X] = qx == 1 ? cw : 0ull;
+      }
+    } else {
+      const int sh = log2_factor(f), fm = f - 1, cs = 8 / f;
+      const int qx = (int)(code >> (2 * sh)), qy = (int)(code >> sh) & fm, qz = (int)code & fm;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int X = k - qx * cs;
+        if (X < 0 || X >= cs) continue;
+        uint64_t t = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j / f == X) t |= m[j];
+        c[k] = coarsen_word_f(t, qy, qz, f);
+      }
+    }
+  } else if constexpr (OP == kRefineDilate) {
+    // word w: along x the fine positions 8 tx + w - d inside the refined
+    // 16^3 block (source words (8 tx + w - d) / 2), along y and z the child
+    // quadrants whose dilation reaches the target
+    const int tx = (int)(code >> 4) - 1, ty = ((int)(code >> 2) & 3) - 1, tz = ((int)code & 3) - 1;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      uint64_t mx = 0;
+      for (int d = a.lo[0]; d <= a.hi[0]; ++d) {
+        const int fx = 8 * tx + w - d;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          if (fx >= 0 && fx < 16 && (fx >> 1) == q) mx |= m[q];
+      }
+      if (!mx) continue;
+      uint64_t word = 0;
+#pragma unroll
+      for (int cy = 0; cy < 2; ++cy) {
+        const int dy = ty - cy;
+        if (dy < -1 || dy > 1 || (dy < 0 && a.lo[1] >= 0) || (dy > 0 && a.hi[1] <= 0)) continue;
+#pragma unroll
+        for (int cz = 0; cz < 2; ++cz) {
+          const int dz = tz - cz;
+          if (dz < -1 || dz > 1 || (dz < 0 && a.lo[2] >= 0) || (dz > 0 && a.hi[2] <= 0)) continue;
+          if (!(mx & (0x0F0F0F0Full << (32 * cy + 4 * cz)))) continue;
+          word |= dilate_y1(dilate_z1(refine_word(mx, cy, cz), dz, a.lo[2], a.hi[2]), dy, a.lo[1], a.hi[1]);
+        }
+      }
+      c[w] = word;
+    }
+  } else {  // kDilate
+    const int tx = (int)(code / 9) - 1, ty = (int)((code / 3) % 3) - 1, tz = (int)(code % 3) - 1;
+    if (a.lo[0] >= -1 && a.lo[1] >= -1 && a.lo[2] >= -1 && a.hi[0] <= 1 && a.hi[1] <= 1 && a.hi[2] <= 1) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        c[k] = dilate_y1(dilate_z1(dilate_x1(m, k, tx, a.lo[0], a.hi[0]), tz, a.lo[2], a.hi[2]), ty, a.lo[1],
+                         a.hi[1]);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        c[k] = dilate_y(dilate_z(dilate_x(m, k, tx, a.lo[0], a.hi[0]), tz, a.lo[2], a.hi[2]), ty, a.lo[1], a.hi[1]);
+    }
+  }
+}
+
+// One item of a node-path sweep: source idx / nchunks (a leaf, or a voxel
+// for the ijk front end) and its chunk of targets.  Loads the source (mask
+// m, leaf coordinate lc -- voxel coordinate for the ijk front end -- and
+// grid g) and tests the chunk's targets: bit t - t0 of `bits` is set for
+// each non-empty target t.
+template <int OP>
+__device__ __forceinline__ void node_item(const PassArgs& a, long long idx, uint32_t k, uint32_t T, uint32_t nchunks,
+                                          uint64_t m[8], int32_t lc[3], uint32_t& g, long long& i, uint32_t& t0,
+                                          uint32_t& bits) {
+  i = idx / nchunks;
+  t0 = (uint32_t)(idx - i * nchunks) * k;
+  const uint32_t t1 = t0 + k < T ? t0 + k : T;
+  bits = 0;
+  if (OP == kIjk) {
+    lc[0] = __ldg(a.ijk + 3 * i);
+    lc[1] = __ldg(a.ijk + 3 * i + 1);
+    lc[2] = __ldg(a.ijk + 3 * i + 2);
+    g = (uint32_t)grid_of(a.in_offsets, a.B, i);
+    bits = 1u;
+    return;
+  }
+  load_mask(a.src_masks, i, m);
+  lc[0] = __ldcg(a.src_origins + 3 * i) >> 3;
+  lc[1] = __ldcg(a.src_origins + 3 * i + 1) >> 3;
+  lc[2] = __ldcg(a.src_origins + 3 * i + 2) >> 3;
+  for (uint32_t t = t0; t < t1; ++t) {
+    uint32_t code;
+    int32_t tl[3];
+    if (target_nonempty<OP>(a, m, lc, t, code, tl)) bits |= 1u << (t - t0);
+  }
+  g = bits ? (a.src_grid ? (uint32_t)__ldcg(a.src_grid + i) : (uint32_t)grid_of(a.in_offsets, a.B, i)) : 0u;
+}
+
+// Target t of an item: its code (the ijk front end: the voxel's bit in its
+// leaf), leaf coordinate tl and canonical key.
+template <int OP>
+__device__ __forceinline__ uint64_t node_target(const PassArgs& a, const int32_t lc[3], uint32_t g, uint32_t t,
+                                                uint32_t& code, int32_t tl[3]) {
+  if (OP == kIjk) {
+    tl[0] = lc[0] >> 3;
+    tl[1] = lc[1] >> 3;
+    tl[2] = lc[2] >> 3;
+    code = (uint32_t)(((lc[0] & 7) << 6) | ((lc[1] & 7) << 3) | (lc[2] & 7));
+  } else {
+    target_geometry<OP>(a, lc, t, code, tl);
+  }
+  return encode_key(a.K, g, tl[0], tl[1], tl[2]);
+}
+
+// The warp's first look-ups of an item step: each lane's first non-empty
+// target's lower node, one table look-up per distinct node of the warp (the
+// lanes of a warp work on neighbouring sources), into the lanes' caches.
+template <int OP>
+__device__ __forceinline__ void node_prime(const PassArgs& a, SmemNodes* sn, const int32_t lc[3], uint32_t g,
+                                           uint32_t bits, uint32_t t0, uint64_t& cache_nk, uint32_t& cache_id,
+                                           int& cache_slot) {
+  const int lane = threadIdx.x & 31;
+  uint64_t nk = 0, key = 0;
+  int32_t tl[3] = {0, 0, 0};
+  if (bits) {
+    uint32_t code;
+    key = node_target<OP>(a, lc, g, t0 + (uint32_t)(__ffs(bits) - 1), code, tl);
+    nk = shr64(key, a.K.lower_bits);
+  }
+  const bool need = bits && nk + 1ull != cache_nk;
+  const uint32_t nmask = __ballot_sync(0xffffffffu, need);
+  if (!nmask) return;
+  const uint32_t peers = __match_any_sync(0xffffffffu, nk) & nmask;
+  const int leader = need ? __ffs(peers) - 1 : lane;
+  uint32_t id = 0;
+  int slot = -1;
+  if (need && lane == leader) id = node_lookup(a, sn, nk, key, tl, g, slot);
+  id = __shfl_sync(0xffffffffu, id, leader);
+  slot = __shfl_sync(0xffffffffu, slot, leader);
+  if (need) {
+    cache_nk = nk + 1ull;
+    cache_id = id;
+    cache_slot = slot;
+  }
+}
+
+// Leaves before the node of each rank (exclusive scan of the nodes' leaf
+// counts in rank order) into shared memory, by every block for itself.
+__device__ __forceinline__ uint32_t scan_node_bases(const PassArgs& a, SmemPlace& s) {
+  const uint32_t n = min(__ldcg(&a.ctl->n_nodes), (uint32_t)a.node_cap);
+  uint32_t carry = 0;
+  for (uint32_t c0 = 0; c0 < n; c0 += kThreads) {
+    const uint32_t i = c0 + threadIdx.x;
+    const uint32_t v = i < n ? __ldcg(a.rank_cnt + i) : 0u;
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan_256(v, s.scan, &tot);
+    if (i < n) s.base[i] = carry + ex;
+    carry += tot;
+  }
+  __syncthreads();
+  return n;
+}
+
+// The place phase.  Every block scans the node leaf counts in rank order
+// into shared memory (the leaves before each node).  Then, a thread per slot
+// over the whole grid: the slot's target leaf is one set bit of its lower
+// node's child mask, and its index is the node's base plus the set bits
+// before it; the leaf's record (origin, grid, links) is written -- by every
+// slot of the leaf alike -- and the slot's contribution, computed from its
+// source mask, is merged into the leaf's staged mask (stored where each leaf
+// has one slot, else OR-ed into the cleared masks).
+template <int OP>
+__device__ __noinline__ void phase_place(const PassArgs& a, Smem& sm, int vb, int vg) {
+  SmemPlace& s = sm.place;
+  const int tid = threadIdx.x;
+  scan_node_bases(a, s);
+  const int32_t B = a.B;
+  if (vb == 0 && tid == 0) {  // the pass's lower and upper node totals
+    a.ctl->head_totals[1] = __ldcg(&a.ctl->n_nodes);
+    a.ctl->head_totals[2] = __ldcg(&a.ctl->n_tiles);
+  }
+  if (vb == 0 && a.last) {  // 1 + first leaf / lower / upper index of every grid (0: empty grid)
+    for (int g = tid; g < B; g += kThreads) {
+      const uint32_t el = __ldcg(a.gmin + g), eu = __ldcg(a.gmin + B + g);
+      a.first[g] = el ? s.base[~el] + 1u : 0u;
+      a.first[B + g] = el ? ~el + 1u : 0u;
+      a.first[2 * B + g] = eu ? ~eu + 1u : 0u;
+    }
+  }
+  // Node tables are read-only from here on and no SM has loaded them into its
+  // L1 before (they were written by stores and atomics and read at L2), so
+  // they are read through L1.
+  const long long nthreads = (long long)vg * kThreads, gt = (long long)vb * kThreads + tid;
+  long long S = (long long)__ldcg(&a.rb->num_slots);
+  if (S > a.slot_cap) S = a.slot_cap;
+  for (long long sl = gt; sl < S; sl += nthreads) {
+    const uint32_t nref = __ldcg(a.nref + sl), val = __ldcg(a.vals[0] + sl);
+    const uint32_t id = nref >> 12, bit = nref & 4095u;
+    const uint64_t mw = __ldca(a.node_mask + 64ull * id + (bit >> 6));
+    const uint32_t rank = __ldca(a.node_rank + id), wpre = __ldca(a.node_wpre + 64ull * id + (bit >> 6));
+    const int32_t* lc = a.node_lc + 4ull * id;
+    const int32_t g = __ldca(lc + 3);
+    const long long u = (long long)s.base[rank] + wpre + __popcll(mw & ((1ull << (bit & 63u)) - 1ull));
+    // the leaf's record (every slot of a leaf writes the same one)
+    int32_t* o = a.out_origins + 3 * u;
+    o[0] = (int32_t)(((uint32_t)__ldca(lc) << 7) | ((bit >> 8) << 3));
+    o[1] = (int32_t)(((uint32_t)__ldca(lc + 1) << 7) | (((bit >> 4) & 15u) << 3));
+    o[2] = (int32_t)(((uint32_t)__ldca(lc + 2) << 7) | ((bit & 15u) << 3));
+    if (a.last) {
+      const bool f = ~__ldca(a.gmin + g) == rank && u == (long long)s.base[rank];
+      a.leaf_g[u] = (uint32_t)g;
+      a.leaf_lower[u] = rank;
+      a.leaf_upper[u] = __ldca(a.tile_rank + __ldca(a.node_tile + id)) | (f ? kGridFirst : 0u);
+    } else {
+      a.out_grid[u] = g;
+    }
+    uint64_t m[8];
+    uint32_t code = val;
+    if (OP != kIjk) {
+      load_mask(a.src_masks, (long long)(val >> a.code_bits), m);
+      code = val & ((1u << a.code_bits) - 1u);
+    }
+    uint64_t c[8];
+    contrib_words<OP>(a, m, code, c);
+    if (a.node_zero == 0) {  // the leaf's only contribution
+      uint4* d = reinterpret_cast<uint4*>(a.out_masks + 8 * u);
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        d[w] = make_uint4((uint32_t)c[2 * w], (uint32_t)(c[2 * w] >> 32), (uint32_t)c[2 * w + 1],
+                          (uint32_t)(c[2 * w + 1] >> 32));
+    } else {
+#pragma unroll
+      for (int w = 0; w < 8; ++w)
+        if (c[w]) atomicOr(reinterpret_cast<unsigned long long*>(a.out_masks + 8 * u + w), (unsigned long long)c[w]);
+    }
+  }
+}
+
+__device__ void dispatch_place(const PassArgs& a, Smem& sm, int vb, int vg) {
+  switch (a.op) {
+    case kIjk: phase_place<kIjk>(a, sm, vb, vg); break;
+    case kLeaves: phase_place<kLeaves>(a, sm, vb, vg); break;
+    case kRefine: phase_place<kRefine>(a, sm, vb, vg); break;
+    case kCoarsen: phase_place<kCoarsen>(a, sm, vb, vg); break;
+    case kRefineDilate: phase_place<kRefineDilate>(a, sm, vb, vg); break;
+    default: phase_place<kDilate>(a, sm, vb, vg); break;
+  }
+}
+
+// Middle phase d of a node-path pass: nodes, [clear,] place.
+__device__ void node_middle(const PassArgs& a, int d, Smem& sm, int vb, int vg) {
+  if (d == 0) {
+    phase_nodes(a, vb, vg);
+  } else if (d + 1 < a.mid) {
+    phase_clear(a, vb, vg);
+  } else {
+    stamp(a, 2);
+    dispatch_place(a, sm, vb, vg);
+    stamp(a, 3);
+  }
+}
+
+// The node path's emission: calls of their own, so that their node tables'
+// state does not weigh on the rest of the kernel's registers.
+// Items of one thread tested before one slot claim in a node-path emission.
+constexpr int kNodeItems = 8;
+
+template <int OP>
+__device__ __noinline__ void emit_node(const PassArgs& a, Smem& sm, int vb, int vg) {
+  SmemNodes& sn = sm.nodes;
+  for (int i = threadIdx.x; i < kNodeSlots * 129; i += kThreads) {
+    if (i < kNodeSlots) sn.id[i] = 0u;
+    else (&sn.mask[0][0])[i - kNodeSlots] = 0u;
+  }
+  __syncthreads();
+  const long long ns = a.src_count_dev ? (long long)__ldcg(a.src_count_dev) : a.src_count;
+  const uint32_t T = targets_per_source<OP>(a);
+  uint32_t k = (a.tchunk > 0 && (uint32_t)a.tchunk < T) ? (uint32_t)a.tchunk : T;
+  if (k > 32) k = 32;  // a thread's targets are one 32-bit set
+  const uint32_t nchunks = (T + k - 1) / k;
+  const long long items = ns * (long long)nchunks;
+  const long long stride = (long long)vg * kThreads;
+  // each thread a run of consecutive items (neighbouring sources share nodes)
+  const long long gt = (long long)vb * kThreads + threadIdx.x;
+  const long long per = (items + stride - 1) / stride;
+  uint64_t cache_nk = 0;  // the thread's last lower node (key + 1; 0: none), its id and block slot
+  uint32_t cache_id = 0;
+  int cache_slot = -1;
+  NodeRun run{0u, 0u, 0u, -1};
+  for (long long qb = 0; qb < per; qb += kNodeItems) {  // uniform
+  // first the tests of up to kNodeItems items, so the warp claims their slots at once
+  uint32_t bits[kNodeItems];
+  uint32_t cnt = 0;
+#pragma unroll
+  for (int q = 0; q < kNodeItems; ++q) {
+    bits[q] = 0;
+    const long long idx = gt * per + qb + q;
+    if (qb + q < per && idx < items) {
+      uint64_t m[8];
+      int32_t lc[3];
+      uint32_t g, t0;
+      long long i;
+      node_item<OP>(a, idx, k, T, nchunks, m, lc, g, i, t0, bits[q]);
+      cnt += __popc(bits[q]);
+    }
+  }
+  unsigned long long wbase;
+  uint32_t wtotal;
+  unsigned long long pos = claim_slots(a, cnt, wbase, wtotal);
+#pragma unroll 1
+  for (int q = 0; q < kNodeItems; ++q) {  // uniform
+    if (qb + q >= per) break;
+    const long long idx = gt * per + qb + q;
+    uint32_t b = bits[0];
+#pragma unroll
+    for (int j = 1; j < kNodeItems; ++j) b = j == q ? bits[j] : b;
+    int32_t lc[3] = {0, 0, 0};
+    uint32_t g = 0, t0 = 0;
+    long long i = 0;
+    if (b) {  // the item's source again (its mask is not needed)
+      i = idx / nchunks;
+      t0 = (uint32_t)(idx - i * nchunks) * k;
+      if (OP == kIjk) {
+        lc[0] = __ldg(a.ijk + 3 * i);
+        lc[1] = __ldg(a.ijk + 3 * i + 1);
+        lc[2] = __ldg(a.ijk + 3 * i + 2);
+        g = (uint32_t)grid_of(a.in_offsets, a.B, i);
+      } else {
+        lc[0] = __ldcg(a.src_origins + 3 * i) >> 3;
+        lc[1] = __ldcg(a.src_origins + 3 * i + 1) >> 3;
+        lc[2] = __ldcg(a.src_origins + 3 * i + 2) >> 3;
+        g = a.src_grid ? (uint32_t)__ldcg(a.src_grid + i) : (uint32_t)grid_of(a.in_offsets, a.B, i);
+      }
+    }
+    node_prime<OP>(a, &sn, lc, g, b, t0, cache_nk, cache_id, cache_slot);
+    while (b) {
+      const uint32_t t = t0 + (uint32_t)(__ffs(b) - 1);
+      b &= b - 1;
+      uint32_t code;
+      int32_t tl[3];
+      const uint64_t key = node_target<OP>(a, lc, g, t, code, tl);
+      const uint64_t nk = shr64(key, a.K.lower_bits);
+      if (nk + 1ull != cache_nk) {
+        cache_id = node_lookup(a, &sn, nk, key, tl, g, cache_slot);
+        cache_nk = nk + 1ull;
+      }
+      const uint32_t bit = ((uint32_t)(tl[0] & 15) << 8) | ((uint32_t)(tl[1] & 15) << 4) | (uint32_t)(tl[2] & 15);
+      if (run.bits && (run.id != cache_id || run.w32 != (bit >> 5))) run_flush(a, sn, run);
+      run.id = cache_id;
+      run.slot = cache_slot;
+      run.w32 = bit >> 5;
+      run.bits |= 1u << (bit & 31u);
+      put_node_slot(a, pos++, (cache_id << 12) | bit,
+                    OP == kIjk ? code : (((uint32_t)i << a.code_bits) | code));
+    }
+  }
+  }
+  run_flush(a, sn, run);
+  emit_flush(a, sn);
+}
+
 __device__ void dispatch_emit(const PassArgs& a, Smem& sm, int vb, int vg) {
+  if (a.node) {
+    switch (a.op) {
+      case kIjk: emit_node<kIjk>(a, sm, vb, vg); break;
+      case kLeaves: emit_node<kLeaves>(a, sm, vb, vg); break;
+      case kRefine: emit_node<kRefine>(a, sm, vb, vg); break;
+      case kCoarsen: emit_node<kCoarsen>(a, sm, vb, vg); break;
+      case kRefineDilate: emit_node<kRefineDilate>(a, sm, vb, vg); break;
+      default: emit_node<kDilate>(a, sm, vb, vg); break;
+    }
+    return;
+  }
   switch (a.op) {
     case kIjk: phase_emit<kIjk>(a, sm, vb, vg); break;
     case kLeaves: phase_emit<kLeaves>(a, sm, vb, vg); break;
@@ -980,7 +1619,135 @@ __device__ __noinline__ void leaves_refine_dilate(const PassArgs& a, Smem& sm, i
   phase_leaves<kRefineDilate>(a, sm, vb, vg);
 }
 
+// The node path's leaves phase (last pass), a call of its own: the records
+// are placed already, so a thread takes a leaf -- each 8-lane group eight
+// consecutive leaves of its range at a time -- for its popcount and bbox, and
+// the group carries the segmented voxel aggregate and the grid bbox as the
+// leaves phase above does.
+__device__ __noinline__ void leaves_staged(const PassArgs& a, Smem& sm, int vb, int vg) {
+  SmemLeaves& s = sm.lv;
+  const long long U = (long long)__ldcg(&a.ctl->head_totals[0]);
+  const int tid = threadIdx.x, lane = tid & 31, w = tid & 7, grp = tid >> 3;
+  const long long C = (U + vg - 1) / vg;
+  const long long c = (C + kThreads / 8 - 1) / (kThreads / 8);
+  const long long bbeg = (long long)vb * C, bend = bbeg + C < U ? bbeg + C : U;
+  const long long gbeg = bbeg + grp * c, gend = gbeg + c < bend ? gbeg + c : bend;
+  const uint32_t gmask = 0xFFu << (lane & ~7);
+  uint32_t acc_g = 0xFFFFFFFFu, F = 0;
+  unsigned int acc_e[6] = {0, 0, 0, 0, 0, 0};
+  unsigned long long V = 0;
+  for (long long base = gbeg; base < gend; base += 8) {  // uniform within the group
+    const long long u = base + w;
+    const bool valid = u < gend;
+    uint32_t pop = 0, f = 0;
+    if (valid) {
+      uint64_t m[8];
+      load_mask(a.out_masks, u, m);
+      const uint32_t g = __ldcg(a.leaf_g + u);
+      int32_t o[3];
+#pragma unroll
+      for (int k = 0; k < 3; ++k) o[k] = __ldcg(a.out_origins + 3 * u + k);
+      f = (__ldcg(a.leaf_upper + u) & kGridFirst) ? 1u : 0u;
+      uint64_t orw = 0;
+      uint32_t xb = 0;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        pop += __popcll(m[k]);
+        orw |= m[k];
+        xb |= m[k] ? 1u << k : 0u;
+      }
+      const uint32_t yb = bits_of_bytes(orw);
+      uint64_t z = orw | (orw >> 32);
+      z |= z >> 16;
+      z |= z >> 8;
+      const uint32_t zb = (uint32_t)(z & 0xFFull);
+      const unsigned int e[6] = {enc_min(o[0] + __ffs(xb) - 1), enc_min(o[1] + __ffs(yb) - 1),
+                                 enc_min(o[2] + __ffs(zb) - 1), enc_max(o[0] + 31 - __clz(xb)),
+                                 enc_max(o[1] + 31 - __clz(yb)), enc_max(o[2] + 31 - __clz(zb))};
+      if (g != acc_g) {
+        if (acc_g != 0xFFFFFFFFu)
+#pragma unroll
+          for (int k = 0; k < 6; ++k) atomicMax(&a.gbox[6 * acc_g + k], acc_e[k]);
+        acc_g = g;
+#pragma unroll
+        for (int k = 0; k < 6; ++k) acc_e[k] = e[k];
+      } else {
+#pragma unroll
+        for (int k = 0; k < 6; ++k) acc_e[k] = max(acc_e[k], e[k]);
+      }
+      a.leaf_pop[u] = pop;
+    }
+    // segmented scan of (grid-first flag, voxels) over the group's 8 leaves
+    uint32_t Fi = f;
+    unsigned long long Vi = pop;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) {
+      const uint32_t F2 = __shfl_up_sync(gmask, Fi, off, 8);
+      const unsigned long long V2 = __shfl_up_sync(gmask, Vi, off, 8);
+      if (w >= off) {
+        if (!Fi) Vi += V2;
+        Fi |= F2;
+      }
+    }
+    const uint32_t Ft = __shfl_sync(gmask, Fi, 7, 8);
+    const unsigned long long Vt = __shfl_sync(gmask, Vi, 7, 8);
+    V = Ft ? Vt : V + Vt;
+    F |= Ft;
+  }
+  // the group's pending grid bbox: its last leaf's grid, merged over the
+  // lanes that hold it; a lane left on an earlier grid reaches memory itself
+  const int wl = gend > gbeg ? (int)((gend - 1 - gbeg) & 7) : 0;
+  const uint32_t lg = __shfl_sync(gmask, acc_g, wl, 8);
+  if (acc_g != lg && acc_g != 0xFFFFFFFFu)
+#pragma unroll
+    for (int k = 0; k < 6; ++k) atomicMax(&a.gbox[6 * acc_g + k], acc_e[k]);
+#pragma unroll
+  for (int k = 0; k < 6; ++k) {
+    unsigned int v = acc_g == lg ? acc_e[k] : 0u;
+#pragma unroll
+    for (int off = 1; off < 8; off <<= 1) v = max(v, __shfl_xor_sync(gmask, v, off, 8));
+    if (w == 0) s.grp_box[grp][k] = v;
+  }
+  if (w == 0) {
+    s.grp_f[grp] = F;
+    s.grp_v[grp] = V;
+    s.grp_g[grp] = lg;
+    a.grp_agg[(long long)vb * (kThreads / 8) + grp] = ((unsigned long long)F << 63) | V;
+  }
+  __syncthreads();
+  if (tid < 6) {  // grid bboxes: one atomic per grid run of the groups
+    uint32_t cg = 0xFFFFFFFFu;
+    unsigned int ce = 0;
+    for (int j = 0; j < kThreads / 8; ++j) {
+      const uint32_t gj = s.grp_g[j];
+      if (gj == 0xFFFFFFFFu) continue;
+      const unsigned int ej = s.grp_box[j][tid];
+      if (gj == cg) {
+        ce = max(ce, ej);
+      } else {
+        if (cg != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * cg + tid], ce);
+        cg = gj;
+        ce = ej;
+      }
+    }
+    if (cg != 0xFFFFFFFFu) atomicMax(&a.gbox[6 * cg + tid], ce);
+  }
+  if (tid == 32) {  // the block's segmented voxel aggregate
+    uint32_t bf = 0;
+    unsigned long long bv = 0;
+    for (int j = 0; j < kThreads / 8; ++j) {
+      bv = s.grp_f[j] ? s.grp_v[j] : bv + s.grp_v[j];
+      bf |= s.grp_f[j];
+    }
+    a.blk_agg[vb] = ((unsigned long long)bf << 63) | bv;
+  }
+}
+
 __device__ void dispatch_leaves(const PassArgs& a, Smem& sm, int vb, int vg) {
+  if (a.node) {  // the place phase merged the leaves; a last pass counts them
+    if (a.last) leaves_staged(a, sm, vb, vg);
+    return;
+  }
   switch (a.op) {
     case kIjk: phase_leaves<kIjk>(a, sm, vb, vg); break;
     case kLeaves: phase_leaves<kLeaves>(a, sm, vb, vg); break;
@@ -1017,8 +1784,11 @@ __device__ __forceinline__ int load_pass(const ChainArgs& c, int ch, int k, Pass
     if (threadIdx.x == 0) {
       if (fp.valid && ch == 0 && k == 0) {
         dst.K = fp.K;
-        dst.P = fp.P;
-        dst.sorted = fp.P & 1;
+        if (!dst.node) {
+          dst.P = fp.P;
+          dst.mid = fp.P;
+          dst.sorted = fp.P & 1;
+        }
       }
       held.ch = ch;
       held.k = k;
@@ -1043,7 +1813,8 @@ enum SplitKind { kSplitEmit, kSplitSort, kSplitIndex, kSplitLeaves };
 struct Split {
   int ch, vb, vg;  // this block's chain (< 0: none), its virtual block index and grid size
   int serial;      // 1: more chains take part than there are blocks
-  int maxP, more;  // emission split: most digit passes of the stage; some pass is intermediate
+  int maxP, more;  // emission split: most middle phases of the stage; some pass is intermediate
+  int any_index;   // emission split: some pass of the stage sorts (and so runs the index phase)
 };
 
 // Relative cost of merging one slot in the leaves phase: a leaf costs its
@@ -1068,14 +1839,16 @@ __device__ __forceinline__ long long split_weight(const ChainArgs& c, int ch, in
     const int32_t hi[3] = {p->hi[0], p->hi[1], p->hi[2]};
     const unsigned long long T = (unsigned long long)pass_targets(op, p->factor, lo, hi);
     w = n < kSplitWCap ? n * T : kSplitWCap;
-    atomicMax(&sp.maxP, p->P);
+    atomicMax(&sp.maxP, p->mid);
     if (!p->last) sp.more = 1;
+    if (!p->node) sp.any_index = 1;
   } else if (kind == kSplitLeaves) {
     const PassCtl* ctl = p->ctl;
     const ReadbackHeader* rb = p->rb;
     w = __ldcg(&ctl->head_totals[0]) + leaves_slot_cost(op) * __ldcg(&rb->num_slots);
   } else {
-    if (kind == kSplitSort && d >= p->P) return -1;
+    if (kind == kSplitSort && d >= p->mid) return -1;
+    if (kind == kSplitIndex && p->node) return -1;
     const ReadbackHeader* rb = p->rb;
     w = __ldcg(&rb->num_slots);
   }
@@ -1091,7 +1864,7 @@ struct StageInfo {
   const PassCtl* ctl;
   const unsigned long long* src_count_dev;
   long long src_count;
-  int op, P, last, T;
+  int op, mid, node, last, T;
 };
 
 __device__ void load_stage(const ChainArgs& c, int k, StageInfo* si, const FrontPlan& fp) {
@@ -1101,7 +1874,9 @@ __device__ void load_stage(const ChainArgs& c, int k, StageInfo* si, const Front
     const PassArgs* p = c.pass + ch * c.n_stage + k;
     StageInfo& e = si[ch];
     e.op = p->op;
-    e.P = (fp.valid && ch == 0 && k == 0) ? fp.P : p->P;  // a front end's planned digit passes
+    e.node = p->node;
+    // a sorting front end's planned digit passes
+    e.mid = (fp.valid && ch == 0 && k == 0 && !p->node) ? fp.P : p->mid;
     e.last = p->last;
     e.rb = p->rb;
     e.ctl = p->ctl;
@@ -1122,7 +1897,7 @@ __device__ void split_warp(const ChainArgs& c, const StageInfo* si, int kind, in
   if (threadIdx.x < 32) {
     const int ch = threadIdx.x;
     long long w = -1;
-    int P = 0, more = 0;
+    int P = 0, more = 0, sorts = 0;
     if (ch < n && si[ch].op >= 0) {
       const StageInfo& e = si[ch];
       unsigned long long v = 0;
@@ -1135,12 +1910,13 @@ __device__ void split_warp(const ChainArgs& c, const StageInfo* si, int kind, in
       } else if (kind == kSplitLeaves) {
         v = __ldcg(&e.ctl->head_totals[0]) + leaves_slot_cost(e.op) * __ldcg(&e.rb->num_slots);
       } else {
-        on = !(kind == kSplitSort && d >= e.P);
+        on = !(kind == kSplitSort && d >= e.mid) && !(kind == kSplitIndex && e.node);
         if (on) v = __ldcg(&e.rb->num_slots);
       }
       if (on) w = (long long)(v < kSplitWCap ? v : kSplitWCap);
-      P = e.P;
+      P = e.mid;
       more = !e.last;
+      sorts = !e.node;
     }
     const unsigned long long own = w >= 0 ? kSplitOne + (unsigned long long)w : 0ull;
     unsigned long long incl = own;
@@ -1152,6 +1928,7 @@ __device__ void split_warp(const ChainArgs& c, const StageInfo* si, int kind, in
     const unsigned long long total = __shfl_sync(0xffffffffu, incl, 31), ex = incl - own;
     const int maxP = __reduce_max_sync(0xffffffffu, (unsigned)P);
     const bool any_more = __any_sync(0xffffffffu, more);
+    const bool any_sort = __any_sync(0xffffffffu, sorts);
     const unsigned long long nact = total / kSplitOne, wt = total % kSplitOne;
     if (ch == 0) {
       sp.ch = -1;
@@ -1160,6 +1937,7 @@ __device__ void split_warp(const ChainArgs& c, const StageInfo* si, int kind, in
       sp.serial = nact > G ? 1 : 0;
       sp.maxP = maxP;
       sp.more = any_more ? 1 : 0;
+      sp.any_index = any_sort ? 1 : 0;
     }
     __syncwarp();
     if (w >= 0 && nact <= G) {
@@ -1186,6 +1964,7 @@ __device__ void split_grid(const ChainArgs& c, int k, int kind, int d, Split& sp
     sp.vg = 0;
     sp.maxP = 0;
     sp.more = 0;
+    sp.any_index = 0;
   }
   __syncthreads();
   const int n = c.n_chain;
@@ -1201,6 +1980,7 @@ __device__ void split_grid(const ChainArgs& c, int k, int kind, int d, Split& sp
     if (tid == 0) {
       sp.maxP = 0;
       sp.more = 0;
+      sp.any_index = 0;
     }
     __syncthreads();
   }
@@ -1237,7 +2017,8 @@ __device__ __forceinline__ void for_share(const ChainArgs& c, int k, int kind, i
   for (int it = 0; it < nit; ++it) {
     const int ch = serial ? it : sp.ch;
     if (load_pass(c, ch, k, a, held, fp) < 0) continue;
-    if (serial && kind == kSplitSort && d >= a.P) continue;
+    if (kind == kSplitSort && d >= a.mid) continue;
+    if (kind == kSplitIndex && a.node) continue;
     body(a, ch, serial ? (int)blockIdx.x : sp.vb, serial ? (int)gridDim.x : sp.vg);
   }
 }
@@ -1369,19 +2150,27 @@ __global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
       stamp(pa, 1);
     });
     grid_sync(c.bar, c.err);
+    const bool any_index = sp.any_index != 0;
     for (int d = 0; d < maxP; ++d) {
       split(k, kSplitSort, d);
-      for_share(c, k, kSplitSort, d, sp, a, held, fp,
-                [&](const PassArgs& pa, int, int vb, int vg) { phase_sort(pa, d, sm, vb, vg); });
+      for_share(c, k, kSplitSort, d, sp, a, held, fp, [&](const PassArgs& pa, int, int vb, int vg) {
+        if (pa.node) {
+          node_middle(pa, d, sm, vb, vg);
+        } else {
+          phase_sort(pa, d, sm, vb, vg);
+        }
+      });
       grid_sync(c.bar, c.err);
     }
-    split(k, kSplitIndex, 0);
-    for_share(c, k, kSplitIndex, 0, sp, a, held, fp, [&](const PassArgs& pa, int, int vb, int vg) {
-      stamp(pa, 2);
-      phase_index(pa, sm, vb, vg);
-      stamp(pa, 3);
-    });
-    grid_sync(c.bar, c.err);
+    if (any_index) {
+      split(k, kSplitIndex, 0);
+      for_share(c, k, kSplitIndex, 0, sp, a, held, fp, [&](const PassArgs& pa, int, int vb, int vg) {
+        stamp(pa, 2);
+        phase_index(pa, sm, vb, vg);
+        stamp(pa, 3);
+      });
+      grid_sync(c.bar, c.err);
+    }
     // the leaves and voxel offsets share one split: the block aggregates of
     // the leaves phase are indexed by virtual block
     split(k, kSplitLeaves, 0);

@@ -25,6 +25,7 @@ namespace tb {
 enum PassOp : int32_t { kIjk = 0, kLeaves = 1, kRefine = 2, kCoarsen = 3, kDilate = 4, kRefineDilate = 5 };
 constexpr int kNumOps = 6;
 
+constexpr int kNodeCap = 16384;       // most lower nodes (and tiles) of a node-path pass
 constexpr int kBins = 256;            // 8-bit radix digits
 constexpr int kMaxDigitPasses = 8;    // 64-bit key
 // slot value = source index << code_bits | target code; code_bits per pass
@@ -86,7 +87,9 @@ static_assert(sizeof(ReadbackHeader) == 64, "readback header layout");
 struct PassCtl {
   unsigned int dedup_tile_ctr;
   unsigned int dedup_ticket;
-  unsigned int pad[6];
+  unsigned int n_nodes;  // node path: lower nodes made by the emission
+  unsigned int n_tiles;  // node path: root tiles (upper nodes) made by the emission
+  unsigned int pad[4];
   unsigned int sort_tile_ctr[kMaxDigitPasses];
   unsigned long long head_totals[4];
   unsigned int hist[kMaxDigitPasses][kBins];
@@ -158,6 +161,34 @@ struct PassArgs {
   int32_t* out_origins;
   uint64_t* out_masks;
   int32_t* out_grid;
+  // Node path (whole-grid launches whose output lower nodes are few): the
+  // emission records every target leaf as a bit of its lower node's 4096-bit
+  // child mask (NanoVDB's lower-node child mask, x-major bit order = the
+  // canonical order of the leaves inside the node) in a hash table of lower
+  // nodes; the nodes phase ranks the nodes by their canonical keys and takes
+  // the masks' popcount prefixes; the place phase gives every leaf its index
+  // (leaves before its node + set bits before it in its node's mask), writes
+  // its record and merges every slot's contribution into it.  No sort.
+  int32_t node;           // 1: this pass takes the node path
+  int32_t node_zero;      // staged masks cleared: 0 never (one slot per leaf), 1 in the nodes phase, 2 in a phase of their own
+  int32_t mid;            // phases between emission and leaves: P digit passes (and the index), or nodes [, clear], place
+  int32_t node_cap;       // most lower nodes (the host's bound)
+  uint32_t node_hmask;    // hash slots - 1 (a power of two): node and tile ids are slots
+  int32_t node_pad;
+  unsigned long long* nh_key;  // [hslots] lower-node key + 1, 0 = free (zeroed)
+  unsigned long long* th_key;  // [hslots] tile key + 1, 0 = free (zeroed)
+  uint64_t* node_mask;         // [hslots][64] child masks (zeroed)
+  uint32_t* gmin;              // [2][B] ~(rank of the first lower node), ~(rank of the first tile) per grid (zeroed)
+  uint64_t* node_key;          // [hslots] key >> lower_bits
+  int32_t* node_lc;            // [hslots][4] lower-node coordinate (leaf coordinate >> 4) per axis, grid
+  uint32_t* node_tile;         // [hslots] tile id
+  uint32_t* node_rank;         // [hslots] canonical rank within the batch
+  uint32_t* node_wpre;         // [hslots][64] set bits of the child mask before each word
+  uint32_t* rank_cnt;          // [node_cap] leaves of the node of each rank
+  uint32_t* tile_rank;         // [hslots]
+  uint32_t* node_list;         // [node_cap] the nodes' ids in order of making
+  uint32_t* tile_list;         // [node_cap] the tiles' ids in order of making
+  uint32_t* nref;              // [slot_cap] node id << 12 | child bit of each slot
   // member launches (k_member): every grid of a chain runs as its own batch of
   // one grid on its share of the chain's buffers.  In a member template the
   // buffer pointers above are the chain's bases, and B, rb and the per-grid

@@ -106,4 +106,8 @@ cudaError_t launch_write_multi(const WriteTasks& tasks, int blocks, cudaStream_t
 // Sets the calling thread's tb_last_error() message.
 void set_error_message(const char* msg);
 
+// True for device or managed memory (cudaPointerGetAttributes); false for
+// NULL, pageable or pinned host memory.
+bool device_accessible(const void* p);
+
 }  // namespace tb

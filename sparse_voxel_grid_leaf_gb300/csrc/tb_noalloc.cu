@@ -12,15 +12,16 @@
 // until the process exits.
 //
 // The same emission, sort, dedup and writer kernels as tb_refine run on
-// pointers into that array.  The first call on a device looks up the array's
-// device address with cudaGetSymbolAddress (the array's name in host code is
-// only a host-side stand-in); make that first call before any stream capture.
-// Every call reuses the array, whose contents persist between calls: the
-// control region is cleared at the start of each call, and calls that
-// overlap on the GPU (other streams, other threads) race on it.
+// pointers into that array.  Each call looks up the array's device address on
+// the current device with cudaGetSymbolAddress (the array's name in host code
+// is only a host-side stand-in, and a device reset between calls can move the
+// array); the first lookup on a device can load the library's device code, so
+// make the first call before any stream capture.  Every call reuses the
+// array, whose contents persist between calls: the control region is cleared
+// at the start of each call, and calls that overlap on the GPU (other
+// streams, other threads) race on it.
 #include <algorithm>
 #include <cstring>
-#include <mutex>
 
 #include "../../include/tb.h"
 #include "tb_common.cuh"
@@ -35,27 +36,29 @@ constexpr size_t kStaticScratchBytes = 32ull << 20;  // 32 MiB per device
 
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-std::mutex g_static_mu;
-void* g_static_ptr[64] = {};
-
 tb_status static_fail(tb_status st, const char* msg) {
   set_error_message(msg);
   return st;
 }
 
-// Device address of the scratch array on the current device (set up once).
-tb_status scratch_address(int dev, char** out) {
-  if (dev < 0 || dev >= 64) return static_fail(TB_ERR_INVALID_ARG, "device ordinal out of range");
-  std::lock_guard<std::mutex> lk(g_static_mu);
-  if (!g_static_ptr[dev]) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-    if (e != cudaSuccess || !p) return static_fail(TB_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed");
-    g_static_ptr[dev] = p;
+// Device address of the scratch array on the current device, looked up on
+// every call (never cached: after a device reset the module is loaded again
+// and the array can sit elsewhere).
+tb_status scratch_address(char** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+  if (e != cudaSuccess || !p) {
+    cudaGetLastError();
+    return static_fail(TB_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed");
   }
-  *out = (char*)g_static_ptr[dev];
+  *out = (char*)p;
   return TB_OK;
 }
+
+// Bytes of the scratch carve that grow with the candidate slots alone: two
+// key and two value buffers of the digit passes, the run starts and the
+// per-leaf arrays of the last pass (see the carve in tb_refine_static).
+constexpr size_t kSlotBytes = 8 + 8 + 4 + 4 + 4 + 4 + 4 + 8 + 4 + 4;
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -86,10 +89,25 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   if (B == 0 && L != 0) return static_fail(TB_ERR_INVALID_ARG, "tb_refine_static: leaves without grids");
   if (((uintptr_t)masks & 15) != 0) return static_fail(TB_ERR_INVALID_ARG, "tb_refine_static: masks must be 16-byte aligned");
   if (L >= (1ll << (32 - pass_code_bits(kRefine, 2)))) return static_fail(TB_ERR_TOO_LARGE, "tb_refine_static: too many input leaves");
+  // up to 8 candidate slots per input leaf, each needing kSlotBytes of scratch
+  if ((unsigned long long)L * 8ull * kSlotBytes > kStaticScratchBytes)
+    return static_fail(TB_ERR_TOO_LARGE, "tb_refine_static: input needs more than the 32 MiB static scratch");
+  // every pointer the kernels touch must be device memory
+  if (!device_accessible(leaf_offsets) || (L > 0 && (!device_accessible(origins) || !device_accessible(masks))))
+    return static_fail(TB_ERR_INVALID_ARG, "tb_refine_static: inputs must be device memory");
+  {
+    const void* outs[] = {out->leaf_offsets, out->lower_offsets, out->upper_offsets, out->voxel_counts,
+                          out->grid_bbox,    out->node_counts,   out->origins,       out->masks,
+                          out->voxel_offset, out->word_prefix,   out->leaf_bbox,     out->leaf_grid,
+                          out->leaf_parent,  out->lower_origins, out->lower_parent,  out->upper_origins};
+    for (const void* p : outs)
+      if (p && !device_accessible(p))
+        return static_fail(TB_ERR_INVALID_ARG, "tb_refine_static: output buffers must be device memory");
+  }
   int dev = 0;
   TB_STATIC_CUDA(cudaGetDevice(&dev));
   char* scratch = nullptr;
-  tb_status st = scratch_address(dev, &scratch);
+  tb_status st = scratch_address(&scratch);
   if (st != TB_OK) return st;
   int sms = 0;
   TB_STATIC_CUDA(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
@@ -124,6 +142,7 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   std::memset(&a, 0, sizeof a);
   if (!make_layout(B, ob, empty, a.K)) return static_fail(TB_ERR_TOO_LARGE, "tb_refine_static: sort key wider than 64 bits");
   a.P = (a.K.W + 7) / 8;
+  a.mid = a.P;  // the radix sort orders the leaves (no node tables here)
 
   // ---- carve the scratch array
   const long long S = 8 * L;
@@ -207,7 +226,7 @@ tb_status tb_refine_static(const int32_t* origins, const uint64_t* masks, const 
   TB_STATIC_CUDA(cudaStreamSynchronize(stream));
   r.err |= derr;
   if (r.err & kErrTimeout) return static_fail(TB_ERR_DEVICE_TIMEOUT, "tb_refine_static: a device wait timed out");
-  if (r.err & kErrSlotOverflow) return static_fail(TB_ERR_CUDA, "tb_refine_static: internal slot bound exceeded");
+  if (r.err & kErrSlotOverflow) return static_fail(TB_ERR_INTERNAL, "tb_refine_static: internal slot bound exceeded");
   if (out_counts) {
     out_counts[0] = (int64_t)r.num_leaves;
     out_counts[1] = (int64_t)r.num_lowers;

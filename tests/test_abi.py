@@ -67,6 +67,21 @@ def test_host_side_argument_errors(lib):
     assert lib.tb_batch_free(None, None) == 0
 
 
+def test_static_refine_host_checks(lib):
+    """tb_refine_static answers before any launch: an input too large for its
+    static scratch array, and a host-resident leaf_offsets array."""
+    import numpy as np
+    lib.tb_last_error.restype = ctypes.c_char_p
+    out = (ctypes.c_byte * 256)()   # a zeroed tb_out_buffers (152 bytes)
+    offs = np.array([0, 0], np.int64)
+    st = lib.tb_refine_static(None, None, ctypes.c_void_p(offs.ctypes.data), ctypes.c_int32(1), ctypes.c_int64(0),
+                              ctypes.byref(out), None, None)
+    assert st == 1 and b"device memory" in lib.tb_last_error()
+    st = lib.tb_refine_static(ctypes.c_void_p(64), ctypes.c_void_p(64), ctypes.c_void_p(offs.ctypes.data),
+                              ctypes.c_int32(1), ctypes.c_int64(80660), ctypes.byref(out), None, None)
+    assert st == 7 and b"32 MiB" in lib.tb_last_error()
+
+
 def test_launch_mode_switch(lib):
     # process-wide, host only: returns the previous mode, rejects others
     lib.tb_set_launch_mode.restype = ctypes.c_int32

@@ -58,14 +58,19 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.fixture(scope="module", autouse=True, params=["grid", "member"])
+@pytest.fixture(scope="module", autouse=True, params=["grid", "grid-sort", "member"])
 def launch_mode(request, _built):
-    """Every test runs with both launch shapes of the pass kernel: the
-    whole-grid cooperative kernel and the member launch (one cluster per grid
-    of every chain), forced for every input."""
-    prev = tb.set_launch_mode(request.param)
+    """Every test runs with both launch shapes of the pass kernel, forced for
+    every input: the whole-grid cooperative kernel -- with the lower-node
+    child masks ordering every pass whose lower nodes are few ("grid"), and
+    with the radix sort for every pass ("grid-sort") -- and the member launch
+    (one cluster per grid of every chain)."""
+    shape = request.param.split("-")[0]
+    prev = tb.set_launch_mode(shape)
+    prev_node = tb.set_node_mode("sort" if request.param.endswith("-sort") else "auto")
     yield request.param
     tb.set_launch_mode(prev)
+    tb.set_node_mode(prev_node)
 
 
 # ------------------------------------------------------------- small exact cases
@@ -380,7 +385,8 @@ def test_shells_b16(ops):
     check(ijk, off, ops, "b16 %s" % (ops,))
 
 
-@pytest.mark.parametrize("ops", [[("refine", 2)], [("coarsen", 2)], [DIL], [PAD_N]])
+@pytest.mark.parametrize("ops", [[("refine", 2)], [("coarsen", 2)], [DIL], [PAD_N], [PAD_P],
+                                 [("refine", 2), PAD_N]])
 def test_shells_b48(ops):
     ijk, off = synth.make("shells_b48_res64")
     check(ijk, off, ops, "b48 %s" % (ops,))
@@ -407,7 +413,35 @@ def test_pyramid_b48_schedule():
         assert_same(b.to_numpy(), oracle.run_voxels(ijk, off, ops), name)
 
 
-STRESS_SAMPLE = [0, 1, 6, 9, 14, 31, 46, 63]   # shells and blobs, all eight octants
+K5S1 = ("dilate", (-2, -2, -2), (2, 2, 2))   # conv_grid k5s1
+STRESS_OPS = {"from_ijk": [], "refine2": [("refine", 2)], "coarsen4": [("coarsen", 4)], "dilate_k3s1": [DIL],
+              "pad_neg": [PAD_N], "k3s2": [("refine", 2), PAD_N], "conv_k5s1": [K5S1],
+              "round_trip": [("refine", 2), ("coarsen", 2)]}
+MULTI5 = [[("refine", 2)], [("coarsen", 2)], [DIL], [PAD_N], [("refine", 2), PAD_N]]
+_STRESS_ORACLE = {}
+
+
+def member_oracle(ijk, off, ops):
+    """The oracle's result for every member run alone (members are
+    independent), on a thread pool: {g: arrays}.  Cached per chain, so both
+    launch shapes compare against one oracle run."""
+    import concurrent.futures as cf
+    import os
+    key = repr(ops)
+    if key not in _STRESS_ORACLE:
+        def one(g):
+            sub = ijk[off[g]:off[g + 1]]
+            return oracle.run_voxels(sub, np.array([0, len(sub)]), ops)
+        with cf.ThreadPoolExecutor(max_workers=os.cpu_count() or 4) as ex:
+            _STRESS_ORACLE[key] = dict(enumerate(ex.map(one, range(len(off) - 1))))
+    return _STRESS_ORACLE[key]
+
+
+def assert_members(got, ijk, off, ops, where):
+    exp = member_oracle(ijk, off, ops)
+    assert len(got["leaf_offsets"]) == len(off)
+    for g in range(len(off) - 1):
+        assert_same(oracle.member(got, g), exp[g], "%s member %d" % (where, g))
 
 
 @pytest.fixture(scope="module")
@@ -416,27 +450,46 @@ def stress():
     return ijk, off, tb.from_ijk(dev(ijk), dev(off))
 
 
-@pytest.mark.parametrize("ops", [[], [("refine", 2)], [("coarsen", 4)], [DIL]])
-def test_stress_full_size_sampled_members(stress, ops):
-    """Full B=64 res-512 batch on the GPU; the oracle runs sampled members alone
-    (members are independent), compared array by array."""
+@pytest.mark.parametrize("name", sorted(STRESS_OPS))
+def test_stress_full_size_all_members(stress, name):
+    """Full B=64 res-512 batch (shells and blobs straddling the +-4096 tiles in
+    all eight octants) in the launch configuration the benchmark times; every
+    member's arrays equal the oracle's run of that member alone."""
     ijk, off, b0 = stress
+    ops = STRESS_OPS[name]
     b = tb.chain(b0, ops) if ops else b0
     got = b.to_numpy()
     b.validate()
-    for g in STRESS_SAMPLE:
-        sub_ijk = ijk[off[g]:off[g + 1]]
-        exp = oracle.run_voxels(sub_ijk, np.array([0, len(sub_ijk)]), ops)
-        assert_same(oracle.member(got, g), exp, "member %d" % g)
-    # whole-batch properties that hold at any size
-    if ops == [("refine", 2)]:
+    assert_members(got, ijk, off, ops, name)
+    if name == "k3s2":
+        # above the fused refine-then-pad bound this chain runs as two passes
+        assert b.build_source_leaves != b0.num_leaves
+    if name == "refine2":
         assert np.array_equal(got["voxel_counts"], 8 * b0.to_numpy(["voxel_counts"])["voxel_counts"])
+    if name == "round_trip":
+        assert_same(got, b0.to_numpy(), "refine->coarsen")
 
 
-def test_stress_round_trip_full_size(stress):
+def test_stress_multi5_all_members(stress):
+    """The five conv-grid chains in one tb_multi call at stress size."""
     ijk, off, b0 = stress
-    back = tb.chain(b0, [("refine", 2), ("coarsen", 2)]).to_numpy()
-    assert_same(back, b0.to_numpy(), "refine->coarsen")
+    for ops, b in zip(MULTI5, tb.multi(b0, MULTI5)):
+        assert_members(b.to_numpy(), ijk, off, ops, "multi %s" % (ops,))
+        b.validate()
+
+
+def test_stress_masked_refine_half(stress):
+    """Masked refinement with half of the stress batch's voxels flagged."""
+    ijk, off, b0 = stress
+    base = b0.to_numpy()
+    V = int(base["voxel_counts"].sum())
+    flags = (np.random.default_rng(0).random(V) < 0.5).astype(np.uint8)
+    key = "masked-half"
+    if key not in _STRESS_ORACLE:
+        _STRESS_ORACLE[key] = oracle.run_masked_refine(base, flags, 2)
+    got = tb.refine_masked(b0, torch.from_numpy(flags).cuda(), 2)
+    assert_same(got.to_numpy(), _STRESS_ORACLE[key], "masked half")
+    got.validate()
 
 
 # ---------------------------------------------------------- masked refinement
@@ -491,6 +544,20 @@ def test_fused_chains(ops):
     check(ijk, off, ops, "fused random %s" % (ops,))
     ijk, off = synth.make("shells_b16_res64")
     check(ijk, off, ops, "fused shells %s" % (ops,))
+
+
+def test_node_path_is_taken(launch_mode):
+    """The whole-grid kernel orders by lower-node child masks where the
+    output's lower nodes are few (no digit passes), by radix sort where told
+    to; the member launch always sorts."""
+    ijk, off = synth.make("shells_b16_res64")
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    for ops in ([("refine", 2)], [DIL], [("coarsen", 2)], [("refine", 2), PAD_N]):
+        b = tb.chain(b0, ops)
+        if launch_mode == "grid":
+            assert b.build_digit_passes == 0, ops
+        else:
+            assert b.build_digit_passes > 0, ops
 
 
 def test_fused_chains_are_one_pass():

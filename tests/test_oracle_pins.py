@@ -355,8 +355,9 @@ def test_batch_voxel_order_matches_voxel_offsets():
         for i in range(lo, int(res["leaf_offsets"][g + 1])):
             first = int(voffs[g] + res["voxel_offset"][i])
             o = res["origins"][i]
-            n = min(n for n in range(512) if (int(res["masks"][i][n >> 6]) >> (n & 63)) & 1)
-            assert part[first - voffs[g]] == (o[0] + (n >> 6), o[1] + ((n >> 3) & 7), o[2] + (n & 7))
+            ns = [n for n in range(512) if (int(res["masks"][i][n >> 6]) >> (n & 63)) & 1]
+            want = [(o[0] + (n >> 6), o[1] + ((n >> 3) & 7), o[2] + (n & 7)) for n in ns]
+            assert part[first - voffs[g]:first - voffs[g] + len(ns)] == want
 
 
 def test_masked_refine_all_none_and_brute():
