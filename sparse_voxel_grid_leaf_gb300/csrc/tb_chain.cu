@@ -2615,6 +2615,64 @@ __device__ __forceinline__ void write_leaf_staged(const PassArgs& a, const Write
   write_record(o, u, valid, word, g, org, lk);
 }
 
+// Leaf u from the records staged by a whole-batch pass, one thread per leaf:
+// a warp's 32 consecutive leaves make every load and store coalesced (masks
+// as 16-byte vectors).
+__device__ __forceinline__ void write_leaf_thread(const PassArgs& a, const WriteOut& o, long long u) {
+  uint64_t m[8];
+  load_mask(a.out_masks, u, m);
+  const uint32_t g = __ldcg(a.leaf_g + u);
+  int32_t org[3];
+#pragma unroll
+  for (int c = 0; c < 3; ++c) org[c] = __ldcg(a.out_origins + 3 * u + c);
+  const long long voff = __ldcg(a.leaf_voff + u);
+  const uint32_t lw = __ldcg(a.leaf_lower + u), up = __ldcg(a.leaf_upper + u) & ~kGridFirst;
+  const bool new_lower = u == 0 || __ldcg(a.leaf_lower + u - 1) != lw;
+  const bool new_upper = u == 0 || (__ldcg(a.leaf_upper + u - 1) & ~kGridFirst) != up;
+  // word prefix: field k = voxels in words 0..k (k = 0..6); bbox of the set bits
+  uint64_t wp = 0, orw = 0;
+  uint32_t run = 0, xb = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    run += __popcll(m[k]);
+    if (k < 7) wp |= (uint64_t)run << (9 * k);
+    orw |= m[k];
+    xb |= m[k] ? 1u << k : 0u;
+  }
+  const uint32_t yb = bits_of_bytes(orw);
+  uint64_t z = orw | (orw >> 32);
+  z |= z >> 16;
+  z |= z >> 8;
+  const uint32_t zb = (uint32_t)(z & 0xFFull);
+  uint4* dm = reinterpret_cast<uint4*>(o.masks + 8 * u);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    dm[q] = make_uint4((uint32_t)m[2 * q], (uint32_t)(m[2 * q] >> 32), (uint32_t)m[2 * q + 1],
+                       (uint32_t)(m[2 * q + 1] >> 32));
+#pragma unroll
+  for (int c = 0; c < 3; ++c) o.origins[3 * u + c] = org[c];
+  int32_t* bb = o.leaf_bbox + 6 * u;
+  bb[0] = org[0] + __ffs(xb) - 1;
+  bb[1] = org[1] + __ffs(yb) - 1;
+  bb[2] = org[2] + __ffs(zb) - 1;
+  bb[3] = org[0] + 31 - __clz(xb);
+  bb[4] = org[1] + 31 - __clz(yb);
+  bb[5] = org[2] + 31 - __clz(zb);
+  o.word_prefix[u] = wp;
+  o.leaf_grid[u] = (int32_t)g;
+  o.voxel_offset[u] = voff;
+  o.leaf_parent[u] = (int32_t)((long long)lw - a.lower_off[g]);
+  if (new_lower) {
+#pragma unroll
+    for (int c = 0; c < 3; ++c) o.lower_origins[3 * (long long)lw + c] = (int32_t)((uint32_t)org[c] & ~127u);
+    o.lower_parent[lw] = (int32_t)((long long)up - a.upper_off[g]);
+  }
+  if (new_upper) {
+#pragma unroll
+    for (int c = 0; c < 3; ++c) o.upper_origins[3 * (long long)up + c] = (int32_t)((uint32_t)org[c] & ~4095u);
+  }
+}
+
 // Leaf u of a pass: from the staged records when there are any, else by
 // merging its run of slots here.
 template <int OP>
@@ -2653,8 +2711,12 @@ __global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, cons
   if (!write_fits(a, o)) return;
   const long long U = (long long)a.rb->num_leaves;
   const int tid = threadIdx.x, lane = tid & 31;
-  const long long gtid = (long long)blockIdx.x * kThreads + tid;
-  for (long long g = gtid; g <= a.B; g += (long long)gridDim.x * kThreads) write_grid_arrays(a, o, g);
+  const long long gtid = (long long)blockIdx.x * kThreads + tid, nthreads = (long long)gridDim.x * kThreads;
+  for (long long g = gtid; g <= a.B; g += nthreads) write_grid_arrays(a, o, g);
+  if (a.out_masks && !a.member) {  // staged records of a whole-batch pass
+    for (long long u = gtid; u < U; u += nthreads) write_leaf_thread(a, o, u);
+    return;
+  }
   const long long groups = (long long)gridDim.x * (kThreads / 8);
   for (long long ub = (long long)blockIdx.x * (kThreads / 8) + (tid >> 5) * 4; ub < U; ub += groups)
     write_leaf<OP>(a, o, ub + (lane >> 3), U);
@@ -2663,8 +2725,9 @@ __global__ void __launch_bounds__(kThreads) k_write_final(const PassArgs a, cons
 // The writers of several chains in one launch, from the records their leaves
 // phases staged.  Tasks (one per chain, up to kMaxWriteTasks) come as one
 // kernel parameter; every block reads the chains' counts and lays the leaves
-// of the chains that fit their room out as one index space in units of 4
-// leaves, so a warp's 4 groups always belong to one chain.
+// of the chains that fit their room out as one index space in units of 32
+// leaves, a warp's unit within one chain: one thread per leaf for a
+// whole-batch pass, 8 lanes per leaf for a member launch's shares.
 __global__ void __launch_bounds__(kThreads) k_write_multi(const __grid_constant__ WriteTasks wt) {
   const WriteTask* t = wt.t;  // read in place: the lanes of a warp read the same task
   const int n_task = wt.n;
@@ -2675,7 +2738,7 @@ __global__ void __launch_bounds__(kThreads) k_write_multi(const __grid_constant_
       const long long U = write_fits(t[i].a, t[i].o) ? (long long)__ldcg(&t[i].a.rb->num_leaves) : -1;
       leaves[i] = U;
       qbase[i] = q;
-      if (U > 0) q += (U + 3) / 4;
+      if (U > 0) q += (U + 31) / 32;
     }
     qbase[n_task] = q;
   }
@@ -2690,7 +2753,12 @@ __global__ void __launch_bounds__(kThreads) k_write_multi(const __grid_constant_
   for (long long q = gtid / 32; q < total; q += nwarps) {
     int ch = 0;
     while (ch + 1 < n_task && qbase[ch + 1] <= q) ++ch;
-    write_leaf_staged(t[ch].a, t[ch].o, (q - qbase[ch]) * 4 + (lane >> 3), leaves[ch]);
+    const long long u0 = (q - qbase[ch]) * 32;
+    if (t[ch].a.member) {  // a member launch's shares: 8 lanes per leaf, 4 leaves at a time
+      for (int j = 0; j < 8; ++j) write_leaf_member(t[ch].a, t[ch].o, u0 + 4 * j + (lane >> 3), leaves[ch]);
+    } else if (u0 + lane < leaves[ch]) {
+      write_leaf_thread(t[ch].a, t[ch].o, u0 + lane);
+    }
   }
 }
 
