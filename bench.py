@@ -306,8 +306,8 @@ def pass_stats(outs):
 
     def add(kind, L_in, b):
         ps.append({"kind": kind, "L_in": L_in, "S": b.build_slots, "L_out": b.num_leaves,
-                   "P": b.build_digit_passes, "NL": b.num_lowers, "NU": b.num_uppers, "B": b.num_grids,
-                   "kernel": "member" if b.build_member_ctas else "chain"})
+                   "P": model_digit_passes(b), "P_run": b.build_digit_passes, "NL": b.num_lowers,
+                   "NU": b.num_uppers, "B": b.num_grids, "kernel": "member" if b.build_member_ctas else "chain"})
     add("ijk", b0.build_source_leaves, b0)
     add("refine", b0.num_leaves, outs["refine2"])
     add("coarsen", b0.num_leaves, outs["coarsen2"])
@@ -357,6 +357,14 @@ def kernel_bytes(ps):
             w = "write_" + p["kind"] if SEPARATE or ijk else "write_multi"
             acc(w, 96 * L_out + 124 * L_out + 16 * p["NL"] + 12 * p["NU"])
     return by
+
+
+def model_digit_passes(b):
+    """P of the byte model: the 8-bit digit passes a radix sort over the key
+    bits that vary across the batch takes, ceil(W / 8) for the pass's
+    compressed key of W bits -- a property of the workload, whichever way the
+    library orders the leaves (the lower-node child-mask path runs none)."""
+    return (b.build_key_bits + 7) // 8
 
 
 def pass_bytes(p):
@@ -514,7 +522,7 @@ def run_ours(args):
                 "bytes_per_launch": bytes_step * reps / n_launch, "us_per_launch": 1e3 * dom_ms / n_launch,
                 "launches_per_step": n_launch / reps,
                 "bytes_model": "per pass 76 L_in + 116 L_out + 24 S P + 100 B (12 per voxel for an ijk source)",
-                "passes": [{k: p[k] for k in ("kind", "L_in", "S", "P", "L_out", "B")} for p in dom_passes],
+                "passes": [{k: p[k] for k in ("kind", "L_in", "S", "P", "P_run", "L_out", "B")} for p in dom_passes],
                 "share_of_kernel_time": dom_ms / tot_kernel_ms, "peak_source": peak_kind + " hbm_gbs (copy)"}
     kernels = {k: {"launches_per_step": n / reps, "us_per_launch": 1e3 * ms / n,
                    "share": ms / tot_kernel_ms,
@@ -615,8 +623,8 @@ def time_calls(calls, torch, stream, flush):
                     vox = sum(int(x.to_numpy(["voxel_counts"])["voxel_counts"].sum()) for x in rs)
                     one = rs[0] if len(rs) == 1 else None
                     stats = None if one is None else {
-                        "L_in": one.build_source_leaves, "S": one.build_slots, "P": one.build_digit_passes,
-                        "L_out": one.num_leaves, "B": one.num_grids}
+                        "L_in": one.build_source_leaves, "S": one.build_slots, "P": model_digit_passes(one),
+                        "P_run": one.build_digit_passes, "L_out": one.num_leaves, "B": one.num_grids}
                 for x in rs:
                     x.free()
             if it >= 5:
@@ -647,7 +655,8 @@ def target_block(per_op, peak):
             nbytes = pass_bytes(p)
             gbps = nbytes / (r["ms"] / 1e3) / 1e9
             out["%s/%s" % (wl, lab)] = {"ms": r["ms"], "bytes": nbytes, "GBps": gbps, "frac": gbps / peak,
-                                        "S": p["S"], "P": p["P"], "L_in": p["L_in"], "L_out": p["L_out"]}
+                                        "S": p["S"], "P": p["P"], "P_run": p.get("P_run"), "L_in": p["L_in"],
+                                        "L_out": p["L_out"]}
     return out
 
 

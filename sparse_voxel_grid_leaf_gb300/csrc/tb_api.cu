@@ -337,22 +337,20 @@ std::atomic<int> g_node_mode{0};
 // of their own) when its slots' masks take at most this many bytes.
 constexpr long long kNodeClearInline = 16ll << 20;
 
-// How many output lower nodes one source lower node can reach in a pass: a
-// lower node spans 128 voxels per axis; refinement by f spreads it over f
-// nodes per axis, coarsening keeps it inside one, a box dilation by at most
-// 7 voxels reaches one more node on each side it extends to, and the fused
-// refine-then-dilate reaches one more beyond the refined 2.
-long long node_factor(const PassSpec& s) {
-  auto side = [&](int base) {
-    long long f = 1;
-    for (int a = 0; a < 3; ++a) f *= base + (s.lo[a] < 0 ? 1 : 0) + (s.hi[a] > 0 ? 1 : 0);
-    return f;
-  };
+// Per axis, how many lower nodes the image of one source lower node spans
+// after a pass, given `span` before it (a lower node spans 128 voxels per
+// axis).  Refinement by f multiplies the span by f; coarsening by f maps a
+// run of s nodes into at most (s - 1) / f + 2 nodes (one for s = 1); a box
+// dilation by at most 7 voxels reaches one more node on each side it
+// extends to; refinement by 2 then such a box does both.
+long long node_span(const PassSpec& s, int axis, long long span) {
+  const long long ext = (s.lo[axis] < 0 ? 1 : 0) + (s.hi[axis] > 0 ? 1 : 0);
   switch (s.op) {
-    case kRefine: return (long long)s.factor * s.factor * s.factor;
-    case kDilate: return side(1);
-    case kRefineDilate: return side(2);
-    default: return 1;  // coarsening; the front ends (bound: one node per source)
+    case kRefine: return span * s.factor;
+    case kCoarsen: return span == 1 ? 1 : (span - 1) / s.factor + 2;
+    case kDilate: return span + ext;
+    case kRefineDilate: return 2 * span + ext;
+    default: return span;  // the front ends: one node per source at most
   }
 }
 
@@ -584,10 +582,15 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
   // are bounded by kNodeCap (the bound follows the source's lower nodes
   // through the chain; a front end's is its source count)
   for (auto& pc : plans) {
-    long long bound = src.kind == kSrcBatch ? std::max<long long>(src.batch->NL, 1) : std::max(src.count, 1ll);
+    const long long base = src.kind == kSrcBatch ? std::max<long long>(src.batch->NL, 1) : std::max(src.count, 1ll);
+    long long span[3] = {1, 1, 1};  // per axis, the nodes one source node reaches through the chain so far
     for (auto& pl : pc) {
-      const long long f = node_factor(pl.spec);
-      bound = bound > pl.slot_cap / f ? pl.slot_cap : std::min(pl.slot_cap, bound * f);
+      long long f = 1;
+      for (int ax = 0; ax < 3; ++ax) {
+        span[ax] = std::min(node_span(pl.spec, ax, span[ax]), 1ll << 20);
+        f *= span[ax];
+      }
+      long long bound = base > pl.slot_cap / f ? pl.slot_cap : std::min(pl.slot_cap, base * f);
       bound = std::max(bound, 1ll);
       pl.node_bound = bound;
       pl.node = !cl && g_node_mode.load() == 0 && bound <= kNodeCap;
