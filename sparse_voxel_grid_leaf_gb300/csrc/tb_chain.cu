@@ -2101,7 +2101,9 @@ __device__ void publish_readback(const ChainArgs& c, unsigned int expected) {
 // One stage of the launch runs stage k of every chain, phase by phase, the
 // chains of a phase side by side on their shares of the grid.  Stamps:
 // 1 emission, 2 digit passes, 3 index, 4 leaves and voxel offsets.
-__global__ void __launch_bounds__(kThreads) k_chain(const ChainArgs c) {
+// Two blocks per SM at least: the register cap this sets keeps every phase
+// inlined into the kernel within 128 registers a thread.
+__global__ void __launch_bounds__(kThreads, 2) k_chain(const ChainArgs c) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   __shared__ __align__(16) PassArgs a;
@@ -2397,7 +2399,7 @@ __device__ void member_epilogue(const ChainArgs& c, int ch, Smem& sm) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads) k_member(const ChainArgs c) {
+__global__ void __launch_bounds__(kThreads, 2) k_member(const ChainArgs c) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
   __shared__ __align__(16) PassArgs a;
