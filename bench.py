@@ -691,18 +691,25 @@ def phase_table(tb, torch, synth, workload, steps):
 
 
 def kmap_table(tb, torch, synth, stream, flush):
-    """The kernel-map rows alone (as in per_op_tables) on shells_b16_res64 and
-    stress_b64_res512: the k3s1 same-topology map, then the k2s2 transpose map
-    to the refinement, 25 calls each."""
+    """The kernel-map rows alone (as in per_op_tables) on the B=16 and B=48
+    shells and the stress batch: the k3s1 same-topology map, then the k2s2
+    transpose map to the refinement, 25 calls each, in every kernel form
+    (tb.set_kmap_mode; "auto" is the form the library picks)."""
     res = {}
-    for wl in ("shells_b16_res64", "stress_b64_res512"):
+    for wl in ("shells_b16_res64", "shells_b48_res64", "stress_b64_res512"):
         ijk, off = synth.make(wl)
         b0 = tb.from_ijk(torch.from_numpy(ijk).cuda(), torch.from_numpy(off).cuda())
         fine = tb.refine(b0)
-        res[wl] = time_calls([("kmap_k3s1", lambda: tb.kernel_map(b0, b0)),
-                              ("kmap_k2s2_transpose",
-                               lambda: tb.kernel_map(b0, fine, (0, 0, 0), (1, 1, 1), 2, True))],
-                             torch, stream, flush)
+        res[wl] = {}
+        for form in tb.KMAP_MODES:
+            prev = tb.set_kmap_mode(form)
+            try:
+                res[wl][form] = time_calls([("kmap_k3s1", lambda: tb.kernel_map(b0, b0)),
+                                            ("kmap_k2s2_transpose",
+                                             lambda: tb.kernel_map(b0, fine, (0, 0, 0), (1, 1, 1), 2, True))],
+                                           torch, stream, flush)
+            finally:
+                tb.set_kmap_mode(prev)
         fine.free()
         b0.free()
     return res

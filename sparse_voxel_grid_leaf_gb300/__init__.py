@@ -115,6 +115,8 @@ def lib():
             L.tb_set_launch_mode.restype = ctypes.c_int32
             L.tb_set_node_mode.argtypes = [ctypes.c_int32]
             L.tb_set_node_mode.restype = ctypes.c_int32
+            L.tb_set_kmap_mode.argtypes = [ctypes.c_int32]
+            L.tb_set_kmap_mode.restype = ctypes.c_int32
             _lib = L
         return _lib
 
@@ -176,6 +178,19 @@ def set_node_mode(mode: str) -> str:
     if prev < 0:
         raise ValueError("node mode %r" % (mode,))
     return {0: "auto", 1: "sort"}[prev]
+
+
+KMAP_MODES = {"auto": 0, "staged": 1, "staged_prepass": 2, "tabulated": 3, "per_entry": 4}
+
+
+def set_kmap_mode(mode: str) -> str:
+    """Which kernel writes ``kernel_map``, for the whole process: "auto",
+    "staged", "staged_prepass", "tabulated" or "per_entry" (each where the box
+    allows it, else per entry).  Returns the previous mode."""
+    prev = lib().tb_set_kmap_mode(KMAP_MODES[mode])
+    if prev < 0:
+        raise ValueError("kmap mode %r" % (mode,))
+    return {v: k for k, v in KMAP_MODES.items()}[prev]
 
 
 def profile_enable(on=True):

@@ -72,13 +72,13 @@ thread_local long long t_launches = 0;
 // ---------------------------------------------------------------- kernel timing
 
 enum KernelKind {
-  kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKLeafTable,
+  kKPrepassLeaves, kKChain, kKWrite0, kKValidate = kKWrite0 + kNumOps, kKWriteMulti, kKPrune, kKKmap, kKKmapPrep,
   kKExport, kKMember, kKNumKinds
 };
 const char* const kKernelNames[kKNumKinds] = {"prepass_leaves", "chain",         "write_ijk",
                                               "write_leaves",  "write_refine",   "write_coarsen", "write_dilate",
                                               "write_refine_dilate", "validate", "write_multi",   "prune",
-                                              "kernel_map",    "leaf_table",    "export",        "member"};
+                                              "kernel_map",    "kmap_prep",    "export",        "member"};
 
 struct ProfRec {
   int kind;
@@ -333,6 +333,9 @@ long long slots_per_source(const PassSpec& s) { return pass_targets(s.op, s.fact
 // 0: the node path wherever its bound allows (whole-grid launches), 1: never
 // (tb_set_node_mode).
 std::atomic<int> g_node_mode{0};
+// Form of the kernel map (tb_set_kmap_mode): 0 picked by the host, 1 staged,
+// 2 staged after the candidate look-up pass, 3 tabulated, 4 per entry.
+std::atomic<int> g_kmap_mode{0};
 // Staged masks of a node-path pass are cleared in its nodes phase (no phase
 // of their own) when its slots' masks take at most this many bytes.
 constexpr long long kNodeClearInline = 16ll << 20;
@@ -1457,29 +1460,54 @@ tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t l
   long long halo = 1;
   for (int a = 0; a < 3; ++a)
     halo *= transposed ? floor_div(7 - lo[a], stride) + floor_div(hi[a], stride) + 1 : 8 + hi[a] - lo[a];
-  // measured on GB300: the tabulated map wins where leaves are few and
-  // dense (B = 16, 48 shells); with hundreds of thousands of sparse leaves
-  // (the stress batch) each leaf's halo costs more than its entries, and the
-  // staged map with its candidate look-ups in a kernel of their own wins
-  const bool large = out->L >= kKmapLargeLeaves;
-  const bool tabulated = staged && !large && (stride == 1 || transposed) && halo <= kKmapHaloMax;
+  const bool tabulable = span <= 3 && K <= kKmapTabColumns && (stride == 1 || transposed) && halo <= kKmapHaloMax;
+  // measured on GB300 (L2 flushed, whole calls): the staged map wins once
+  // the output has enough leaves to fill the GPU -- one leaf per warp where
+  // the reach spans 3 leaves per axis (B = 48 shells k3s1, 8,164 leaves:
+  // 61 us against 74 us tabulated; stress batch, 83,722 leaves: 190 us
+  // against 379 us), chunks of 16 leaves per warp where it spans 1 (B = 48
+  // k2s2 transpose, 31,128 leaves: 68 us against 102 us; stress, 392,508
+  // leaves: 150 us against 760 us); below that the tabulated map wins
+  // (B = 16 shells: k3s1 32 us against 36 us, k2s2 transpose 45 us against
+  // 57 us).  The look-up pass of its own measured slower than the staged
+  // map's own look-ups everywhere; it stays as a form of its own.
+  enum { kPerEntry, kStaged, kStagedPrepass, kTabulated } form = kPerEntry;
+  switch (g_kmap_mode.load()) {
+    case 0: {
+      const bool many = out->L >= (span == 3 ? 32ll : 128ll) * di->sms;
+      form = tabulable && (!many || !staged) ? kTabulated : staged ? kStaged : kPerEntry;
+      break;
+    }
+    case 1: form = staged ? kStaged : kPerEntry; break;
+    case 2: form = staged ? kStagedPrepass : kPerEntry; break;
+    case 3: form = tabulable ? kTabulated : kPerEntry; break;
+    default: form = kPerEntry; break;
+  }
   const long long cand_max = (long long)span * span * span;
-  const bool prepass = staged && large;
+  const bool prepass = form == kStagedPrepass;
   const size_t cand_bytes = prepass ? (size_t)(out->L * cand_max) * 4 : 0;
-  char* ws = (char*)mem.get(2 * nb + cap * 4 + cand_bytes);
+  // workspace: the two voxel-base arrays, the leaf table, the staged map's
+  // chunk counter (16 bytes), the candidates of the look-up pass
+  char* ws = (char*)mem.get(2 * nb + cap * 4 + 16 + cand_bytes);
   if (!ws) return fail(TB_ERR_OOM, "tb_kernel_map: workspace");
   Guard g{&mem, ws};
   int32_t* table = (int32_t*)(ws + 2 * nb);
-  // pageable sources: staged before the calls return
-  TB_CUDA(cudaMemcpyAsync(ws, in->voxel_base_host.data(), nb, cudaMemcpyHostToDevice, s));
-  TB_CUDA(cudaMemcpyAsync(ws + nb, out->voxel_base_host.data(), nb, cudaMemcpyHostToDevice, s));
+  unsigned int* next_chunk = (unsigned int*)(ws + 2 * nb + cap * 4);
   TB_CUDA(cudaMemsetAsync(table, 0xFF, cap * 4, s));
-  if (in->L) {
-    const int tb_blocks = blocks_for(in->L, 256, (long long)di->sms * 8);
-    TB_CUDA(launch(kKLeafTable, s, [&] {
-      return launch_leaf_table(in->origins, in->leaf_grid, in->L, table, cap - 1, tb_blocks, s);
-    }));
-  }
+  KmapPrep kp;
+  kp.in_counts = in->voxel_counts;
+  kp.out_counts = out->voxel_counts;
+  kp.B = in->B;
+  kp.in_vbase = (int64_t*)ws;
+  kp.out_vbase = (int64_t*)(ws + nb);
+  kp.origins = in->origins;
+  kp.leaf_grid = in->leaf_grid;
+  kp.L = in->L;
+  kp.table = table;
+  kp.mask = cap - 1;
+  kp.next_chunk = next_chunk;
+  const int prep_blocks = in->L ? blocks_for(in->L, 256, (long long)di->sms * 8) : 1;
+  TB_CUDA(launch(kKKmapPrep, s, [&] { return launch_kmap_prep(kp, prep_blocks, s); }));
   KmapArgs k;
   k.in_origins = in->origins;
   k.in_masks = in->masks;
@@ -1492,6 +1520,7 @@ tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t l
   k.out_origins = out->origins;
   k.out_masks = out->masks;
   k.out_voff = out->voxel_offset;
+  k.out_wp = out->word_prefix;
   k.out_grid = out->leaf_grid;
   k.out_vbase = (const int64_t*)(ws + nb);
   k.L_out = out->L;
@@ -1502,19 +1531,21 @@ tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t l
   k.stride = stride;
   k.transposed = transposed ? 1 : 0;
   k.map = map;
-  k.cands = prepass ? (int32_t*)(ws + 2 * nb + cap * 4) : nullptr;
+  k.cands = prepass ? (int32_t*)(ws + 2 * nb + cap * 4 + 16) : nullptr;
+  k.next_chunk = next_chunk;
   k.cand_max = (int32_t)cand_max;
-  const int blocks = blocks_for(out->L, 8, (long long)di->sms * 8);
+  k.span = span;
   if (prepass) {
     const int cb = blocks_for(out->L * cand_max, 256, (long long)di->sms * 8);
     TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap_cands(k, cb, s); }));
   }
-  if (tabulated) {
+  if (form == kTabulated) {
     const int hb = blocks_for(out->L, 4, (long long)di->sms * 7);
     TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap_halo(k, hb, s); }));
-  } else if (staged) {
-    TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap_staged(k, blocks, s); }));
+  } else if (form == kStaged || form == kStagedPrepass) {
+    TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap_staged(k, di->sms, s); }));
   } else {
+    const int blocks = blocks_for(out->L, 8, (long long)di->sms * 8);
     TB_CUDA(launch(kKKmap, s, [&] { return launch_kmap(k, blocks, s); }));
   }
   return TB_OK;
@@ -1712,6 +1743,11 @@ int32_t tb_set_launch_mode(int32_t mode) {
 int32_t tb_set_node_mode(int32_t mode) {
   if (mode < 0 || mode > 1) return -1;
   return g_node_mode.exchange(mode);
+}
+
+int32_t tb_set_kmap_mode(int32_t mode) {
+  if (mode < 0 || mode > 4) return -1;
+  return g_kmap_mode.exchange(mode);
 }
 
 tb_status tb_profile_enable(int32_t on) {

@@ -40,28 +40,49 @@ struct KmapArgs {
   const int32_t* out_origins;
   const uint64_t* out_masks;
   const int64_t* out_voff;
+  const uint64_t* out_wp;    // [L_out] output word prefixes
   const int32_t* out_grid;
   const int64_t* out_vbase;  // [B+1] first voxel index of each output grid
   long long L_out;
   int32_t lo[3], hi[3];
   int32_t stride, transposed;
   int32_t* map;              // [V_out, K]
-  int32_t* cands;            // staged map: [L_out, cand_max] candidate input leaves (-1: none)
+  int32_t* cands;            // staged map: [L_out, cand_max] candidate input leaves (-1: none), or NULL
   int32_t cand_max;          // span^3 of the staged map
+  int32_t span;              // input leaves a leaf's reach spans per axis, at most (1..3 in the staged map)
+  unsigned int* next_chunk;  // staged map: the next chunk of output leaves (zeroed by the set-up)
 };
-cudaError_t launch_leaf_table(const int32_t* origins, const int32_t* leaf_grid, long long L, int32_t* table,
-                              unsigned long long mask, int blocks, cudaStream_t s);
+// Set-up of a kernel map: both batches' per-grid voxel bases from their
+// device voxel counts, the staged map's chunk counter, the input leaf table.
+struct KmapPrep {
+  const int64_t* in_counts;
+  const int64_t* out_counts;  // [B] voxels per grid
+  int32_t B;
+  int64_t* in_vbase;
+  int64_t* out_vbase;         // [B+1] written
+  const int32_t* origins;
+  const int32_t* leaf_grid;   // the input's leaves
+  long long L;
+  int32_t* table;             // all -1 on entry
+  unsigned long long mask;
+  unsigned int* next_chunk;   // zeroed (or NULL)
+};
+cudaError_t launch_kmap_prep(const KmapPrep& p, int blocks, cudaStream_t s);
 cudaError_t launch_kmap(const KmapArgs& k, int blocks, cudaStream_t s);
 // The staged map: boxes whose reach from an output leaf spans at most 3 input
-// leaves per axis, with at most kKmapStagedColumns columns.
+// leaves per axis, with at most kKmapStagedColumns columns (a batch of output
+// leaves per warp for spans of up to 2 and at most kKmapBatchColumns
+// columns, else one leaf per warp).
 constexpr int kKmapStagedColumns = 1024;
+constexpr int kKmapBatchColumns = 32;
 cudaError_t launch_kmap_cands(const KmapArgs& k, int blocks, cudaStream_t s);
 // The tabulated map: stride 1 or transposed, the reach of an output leaf at
-// most kKmapHaloMax voxels (E0 x E1 x E2).
+// most kKmapHaloMax voxels (E0 x E1 x E2) and at most 3 input leaves per
+// axis, at most kKmapTabColumns columns.
+constexpr int kKmapTabColumns = 1024;
 constexpr int kKmapHaloMax = 1024;
-constexpr long long kKmapLargeLeaves = 65536;  // output leaves from which the staged map and look-up pass win
 cudaError_t launch_kmap_halo(const KmapArgs& k, int blocks, cudaStream_t s);
-cudaError_t launch_kmap_staged(const KmapArgs& k, int blocks, cudaStream_t s);
+cudaError_t launch_kmap_staged(const KmapArgs& k, int sms, cudaStream_t s);
 
 // Masked refinement: keeps the voxels of each leaf whose flag (one byte per
 // voxel, in the batch's voxel order) is non-zero.

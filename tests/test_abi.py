@@ -96,6 +96,19 @@ def test_launch_mode_switch(lib):
         lib.tb_set_launch_mode(ctypes.c_int32(prev))
 
 
+def test_kmap_mode_switch(lib):
+    lib.tb_set_kmap_mode.restype = ctypes.c_int32
+    prev = lib.tb_set_kmap_mode(ctypes.c_int32(4))
+    try:
+        assert prev in range(5)
+        assert lib.tb_set_kmap_mode(ctypes.c_int32(1)) == 4
+        assert lib.tb_set_kmap_mode(ctypes.c_int32(5)) == -1
+        assert lib.tb_set_kmap_mode(ctypes.c_int32(-1)) == -1
+        assert lib.tb_set_kmap_mode(ctypes.c_int32(0)) == 1
+    finally:
+        lib.tb_set_kmap_mode(ctypes.c_int32(prev))
+
+
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     import sparse_voxel_grid_leaf_gb300 as tb
     monkeypatch.setattr(tb, "LIB_PATH", str(tmp_path / "missing.so"))

@@ -2,6 +2,8 @@
 bit, on the same seeded inputs (fVDB PR #757's test plan compares topologies
 element-wise; the result is a unique set in a total order, so any difference
 is a bug).  Calls go through the C ABI via the Python binding."""
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -582,11 +584,23 @@ KMAP_CASES = [
     ([], (-7, 0, -2), (0, 7, 2), 1, False),                    # large box
     ([PAD_P], (-1,) * 3, (1,) * 3, 1, True),                   # transposed stride 1
     ([("refine", 2)], (-2,) * 3, (2,) * 3, 2, True),           # k5s2 transpose
+    ([("refine", 2)], (0, 0, 0), (3, 0, 0), 2, True),          # 4 columns, two per parity class
+    ([("refine", 2)], (-7, -7, 0), (-7, -6, 1), 2, True),      # a reach past the output leaf's own
 ]
 
 
+KMAP_FORMS = ["auto", "staged", "staged_prepass", "tabulated", "per_entry"]
+
+
+@pytest.fixture(params=KMAP_FORMS)
+def kmap_form(request):
+    prev = tb.set_kmap_mode(request.param)
+    yield request.param
+    tb.set_kmap_mode(prev)
+
+
 @pytest.mark.parametrize("case", range(len(KMAP_CASES)))
-def test_kernel_map(case):
+def test_kernel_map(case, kmap_form):
     ops, lo, hi, stride, transposed = KMAP_CASES[case]
     ijk, off = synth.random_voxels(4, 150, 26, seed=81, origin=(-4100, 4085, -13), empty=(2,))
     b_in = tb.from_ijk(dev(ijk), dev(off))
@@ -594,8 +608,37 @@ def test_kernel_map(case):
     got = tb.kernel_map(b_in, b_out, lo, hi, stride, transposed).cpu().numpy()
     exp = oracle.run_kernel_map(b_in.to_numpy(), b_out.to_numpy(), lo, hi, stride, transposed)
     assert got.shape == exp.shape
-    assert np.array_equal(got, exp), "kernel map case %d: %d of %d entries differ" % (
-        case, int((got != exp).sum()), got.size)
+    assert np.array_equal(got, exp), "kernel map case %d (%s): %d of %d entries differ" % (
+        case, kmap_form, int((got != exp).sum()), got.size)
+
+
+@pytest.mark.parametrize("case", range(3))
+def test_kernel_map_dense_leaves(case, kmap_form):
+    """Full leaves (512 voxels each): the staged form cuts a warp's 32 leaves
+    into batches by its listed-voxel capacity; odd map offsets (a map that
+    does not start on 16 bytes) take the scalar head and tail."""
+    ops, lo, hi, stride, transposed = [([], (-1,) * 3, (1,) * 3, 1, False),
+                                       ([("refine", 2)], (0,) * 3, (1,) * 3, 2, True),
+                                       ([("coarsen", 2)], (0,) * 3, (1,) * 3, 2, False)][case]
+    ijk, off = synth.random_voxels(2, 6, 6, seed=3, origin=(-20, 5, 9))
+    b_in = tb.chain(tb.from_ijk(dev(ijk), dev(off)), [("refine", 8)])
+    b_out = tb.chain(b_in, ops) if ops else b_in
+    exp = oracle.run_kernel_map(b_in.to_numpy(), b_out.to_numpy(), lo, hi, stride, transposed)
+    got = tb.kernel_map(b_in, b_out, lo, hi, stride, transposed).cpu().numpy()
+    assert np.array_equal(got, exp), (kmap_form, int((got != exp).sum()))
+    # the same map written one int32 past a 16-byte boundary
+    v = b_out._view()
+    K = exp.shape[1]
+    buf = torch.full((int(v.num_voxels) * K + 8,), 7, dtype=torch.int32, device="cuda")
+    lo_a = (ctypes.c_int32 * 3)(*lo)
+    hi_a = (ctypes.c_int32 * 3)(*hi)
+    st = tb.lib().tb_kernel_map(b_in.handle, b_out.handle, lo_a, hi_a, stride, 1 if transposed else 0,
+                                ctypes.c_void_p(buf.data_ptr() + 4), int(v.num_voxels) * K, None)
+    assert st == 0
+    torch.cuda.synchronize()
+    out = buf.cpu().numpy()
+    assert out[0] == 7 and (out[1 + exp.size:] == 7).all()
+    assert np.array_equal(out[1:1 + exp.size].reshape(exp.shape), exp)
 
 
 def test_kernel_map_shells_sampled_rows():
@@ -628,8 +671,9 @@ def _popcount_below(mask_words, bn):
 
 
 def test_kernel_map_stress_k2s2_transpose_sampled_leaves():
-    """Full stress size (the candidate look-up pass, then the tabulated map):
-    the k2s2 transpose map from the stress batch to its refinement.  The rows
+    """Full stress size, the form the library picks there (the staged map,
+    chunks of 16 output leaves per warp): the k2s2 transpose map from the
+    stress batch to its refinement.  The rows
     of sampled output leaves are checked against the map's definition
     (q = (p - d) / 2 where p - d is even), written out from the batches' own
     leaf arrays."""
