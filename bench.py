@@ -67,7 +67,12 @@ def parse():
     p.add_argument("--phases", action="store_true",
                    help="only the step's per-call phase breakdown (GPU timer stamps and host timers)")
     p.add_argument("--kmap-only", action="store_true",
-                   help="only the kernel-map rows of the per-op table (shells_b16_res64 and stress_b64_res512)")
+                   help="only the kernel-map rows, in every kernel form, on the B=16 and B=48 shells and the "
+                        "stress batch")
+    p.add_argument("--kmap-workloads", default="shells_b16_res64,shells_b48_res64,stress_b64_res512",
+                   help="--kmap-only: comma-separated workloads")
+    p.add_argument("--kmap-forms", default="auto,staged,staged_prepass,tabulated,per_entry",
+                   help="--kmap-only: comma-separated kernel forms (tb.set_kmap_mode)")
     return p.parse_args()
 
 
@@ -149,10 +154,13 @@ def kernel_traffic(name):
 
 
 def source_hash():
+    """Hash of the sources of the pass kernels and the calls that plan them
+    (every CUDA source but the kernel maps'): traffic figures taken before a
+    change there no longer describe the kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_voxel_grid_leaf_gb300", "csrc")
     for n in sorted(os.listdir(csrc)):
-        if n.endswith((".cu", ".cuh", ".h")):
+        if n.endswith((".cu", ".cuh", ".h")) and n != "tb_kmap.cu":
             h.update(open(os.path.join(csrc, n), "rb").read())
     return h.hexdigest()[:16]
 
@@ -422,7 +430,9 @@ def run_ours(args):
     if args.kmap_only:
         flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda")
         if rank == 0:
-            print(json.dumps({"per_op": kmap_table(tb, torch, synth, stream, flush)}), flush=True)
+            print(json.dumps({"per_op": kmap_table(tb, torch, synth, stream, flush,
+                                                   args.kmap_workloads.split(","), args.kmap_forms.split(","))}),
+                  flush=True)
         return
     if args.phases:
         if rank == 0:
@@ -690,18 +700,18 @@ def phase_table(tb, torch, synth, workload, steps):
     return res
 
 
-def kmap_table(tb, torch, synth, stream, flush):
-    """The kernel-map rows alone (as in per_op_tables) on the B=16 and B=48
-    shells and the stress batch: the k3s1 same-topology map, then the k2s2
-    transpose map to the refinement, 25 calls each, in every kernel form
+def kmap_table(tb, torch, synth, stream, flush, workloads, forms):
+    """The kernel-map rows alone (as in per_op_tables) on the given
+    workloads: the k3s1 same-topology map, then the k2s2 transpose map to
+    the refinement, 25 calls each, in each given kernel form
     (tb.set_kmap_mode; "auto" is the form the library picks)."""
     res = {}
-    for wl in ("shells_b16_res64", "shells_b48_res64", "stress_b64_res512"):
+    for wl in workloads:
         ijk, off = synth.make(wl)
         b0 = tb.from_ijk(torch.from_numpy(ijk).cuda(), torch.from_numpy(off).cuda())
         fine = tb.refine(b0)
         res[wl] = {}
-        for form in tb.KMAP_MODES:
+        for form in forms:
             prev = tb.set_kmap_mode(form)
             try:
                 res[wl][form] = time_calls([("kmap_k3s1", lambda: tb.kernel_map(b0, b0)),
