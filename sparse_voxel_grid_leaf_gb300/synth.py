@@ -61,14 +61,17 @@ def shell_voxels(rng: SplitMix64, res: int, r_lo: float, r_hi: float,
                  scale: float = 1.0) -> np.ndarray:
     """One-voxel-thick ellipsoid shell.
 
-    Centre ``c ~ U[0.45, 0.55] * res`` and semi-axes ``r ~ U[r_lo, r_hi] * res``
-    (times ``scale``) per axis.  With ``p = ijk + 0.5`` and
+    Semi-axes ``r ~ U[r_lo, r_hi] * res`` (times ``scale``), drawn first, then
+    centre ``c ~ U[0.45, 0.55] * res``, per axis.  (In this order the B=16
+    shells at res 64 average 7,861 voxels per member and the B=48 batch has
+    378,382, matching the "~7.8k voxels/member" and "~375k" the workloads are
+    sized by.)  With ``p = ijk + 0.5`` and
     ``q = |(p - c) / r|``, the radial implicit value is
     ``f = |p - c| * (q - 1) / q`` (signed distance to the surface along the
     ray from the centre); a voxel is active iff ``|f| <= 0.5``.
     """
-    c = (0.45 + 0.10 * rng.uniform(3)) * res
     r = (r_lo + (r_hi - r_lo) * rng.uniform(3)) * res * scale
+    c = (0.45 + 0.10 * rng.uniform(3)) * res
     half = float(np.max(r)) + 2.0
     lo = np.floor(c - half).astype(np.int64)
     hi = np.ceil(c + half).astype(np.int64)
