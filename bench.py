@@ -307,13 +307,18 @@ def free_all(outs):
 
 def pass_stats(outs):
     """Per pass (L_in, S, L_out, P, NL, NU, kind) for the byte model.  Every
-    call of the step is one pass: k3s2 (refine x2 then the {-1,0}^3 pad) and
-    coarsen x4 are each fused into one pass by the library."""
+    call of the step is one pass but k3s2 (refine x2 then the {-1,0}^3 pad):
+    the library fuses it into one pass for inputs of at most 32,768 leaves,
+    and runs its two passes otherwise (a batch built by more than one pass
+    reports -1 source leaves).  Its first pass then equals the refine x2
+    call of the same step (same input, same op), so that call's counts stand
+    for it; coarsen x4 is always one pass."""
     b0 = outs["from_ijk"]
     ps = []
 
-    def add(kind, L_in, b):
-        ps.append({"kind": kind, "L_in": L_in, "S": b.build_slots, "L_out": b.num_leaves,
+    def add(kind, L_in, b, S=None, L_out=None):
+        ps.append({"kind": kind, "L_in": L_in, "S": b.build_slots if S is None else S,
+                   "L_out": b.num_leaves if L_out is None else L_out,
                    "P": model_digit_passes(b), "P_run": b.build_digit_passes, "NL": b.num_lowers,
                    "NU": b.num_uppers, "B": b.num_grids, "kernel": "member" if b.build_member_ctas else "chain"})
     add("ijk", b0.build_source_leaves, b0)
@@ -322,7 +327,14 @@ def pass_stats(outs):
     add("dilate", b0.num_leaves, outs["dilate_k3s1"])
     add("dilate", b0.num_leaves, outs["pad_neg"])
     add("dilate", b0.num_leaves, outs["pad_pos"])
-    add("refine_dilate", b0.num_leaves, outs["k3s2"])
+    k3 = outs["k3s2"]
+    if k3.build_source_leaves < 0:
+        r2 = outs["refine2"]
+        # its refine pass, handing its leaves to the pad pass (no writer)
+        ps.append(dict(ps[1], kernel="member" if k3.build_member_ctas else "chain", inter=True))
+        add("dilate", r2.num_leaves, k3)
+    else:
+        add("refine_dilate", b0.num_leaves, k3)
     add("coarsen", b0.num_leaves, outs["coarsen4"])
     return ps
 
