@@ -274,10 +274,12 @@ TB_API tb_status tb_batch_export(const tb_batch* batch, int32_t* origins, uint64
 
 /* The same for n batches at once: origins[i], masks[i], voxel_offset[i],
  * leaf_offsets[i] receive batch i's arrays (each of the four lists, and each
- * entry, may be NULL to skip).  Destinations the device can write -- device
- * memory, or pinned host memory through its mapped address -- are filled by
- * one copy kernel for all arrays (up to 64 per launch); others by plain
- * copies.  Enqueued on `stream`; the caller synchronizes before reading host
+ * entry, may be NULL to skip).  Arrays of 1 MiB or more are copied by the
+ * copy engines (no SM time, so an export overlaps kernels on other
+ * streams); smaller ones whose destination the device can write -- device
+ * memory, or pinned host memory through its mapped address -- by one copy
+ * kernel for all of them (up to 64 per launch); the rest by plain copies.
+ * Enqueued on `stream`; the caller synchronizes before reading host
  * buffers. */
 TB_API tb_status tb_batch_export_many(const tb_batch* const* batches, int32_t n, int32_t* const* origins,
                                       uint64_t* const* masks, int64_t* const* voxel_offset,

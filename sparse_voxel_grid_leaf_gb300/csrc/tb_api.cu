@@ -1655,6 +1655,9 @@ tb_status tb_batch_get_view(const tb_batch* b, tb_batch_view* v) {
   return TB_OK;
 }
 
+// Arrays at least this large are exported by the copy engines.
+constexpr unsigned long long kExportEngineBytes = 1ull << 20;
+
 tb_status tb_batch_export_many(const tb_batch* const* batches, int32_t n, int32_t* const* origins,
                                uint64_t* const* masks, int64_t* const* voxel_offset, int64_t* const* leaf_offsets,
                                tb_stream stream) {
@@ -1664,11 +1667,17 @@ tb_status tb_batch_export_many(const tb_batch* const* batches, int32_t n, int32_
   cudaStream_t s = (cudaStream_t)stream;
   CopyTasks tasks;
   tasks.n = 0;
-  // one copy task per array whose destination the device can write (device
-  // memory, or pinned host memory through its mapped address); plain copies
-  // for the rest
+  // arrays of kExportEngineBytes or more go to the copy engines (measured on
+  // GB300: the same device-to-host rate as the copy kernel, and no SM time,
+  // so they overlap kernels on other streams); the smaller ones whose
+  // destination the device can write (device memory, or pinned host memory
+  // through its mapped address) to one copy kernel; plain copies for the rest
   auto add = [&](const void* src, void* dst, unsigned long long bytes) -> tb_status {
     if (!dst || !bytes) return TB_OK;
+    if (bytes >= kExportEngineBytes) {
+      TB_CUDA(cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, s));
+      return TB_OK;
+    }
     void* dev = nullptr;
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, dst) == cudaSuccess &&

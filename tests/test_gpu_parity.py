@@ -761,6 +761,31 @@ def test_export_many_matches_arrays():
             assert np.array_equal(v[i], r["voxel_offset"])
 
 
+def test_export_many_large_arrays():
+    """Arrays of 1 MiB and more (here the masks, 5.6 MB, and the origins) go
+    through the copy engines, the small ones through the copy kernel, in the
+    same call."""
+    import torch
+    ijk, off = synth.make("shells_b16_res64")
+    b0 = tb.from_ijk(dev(ijk), dev(off))
+    bs = [tb.chain(b0, [("refine", 2), ("refine", 2)]), b0]
+    ref = [b.to_numpy(["origins", "masks", "voxel_offset", "leaf_offsets"]) for b in bs]
+    assert bs[0].num_leaves * 64 >= 1 << 20 and bs[1].num_leaves * 64 < 1 << 20
+    o = [torch.zeros((b.num_leaves, 3), dtype=torch.int32).pin_memory() for b in bs]
+    m = [torch.zeros((b.num_leaves, 8), dtype=torch.int64).pin_memory() for b in bs]
+    v = [torch.zeros(b.num_leaves, dtype=torch.int64).pin_memory() for b in bs]
+    lo = [torch.zeros(b.num_grids + 1, dtype=torch.int64).pin_memory() for b in bs]
+    stream = torch.cuda.Stream()
+    stream.wait_stream(torch.cuda.current_stream())
+    tb.export_many(bs, o, m, v, lo, stream=stream)
+    stream.synchronize()
+    for i, r in enumerate(ref):
+        assert np.array_equal(o[i].numpy(), r["origins"])
+        assert np.array_equal(m[i].numpy().view(np.uint64), r["masks"])
+        assert np.array_equal(v[i].numpy(), r["voxel_offset"])
+        assert np.array_equal(lo[i].numpy(), r["leaf_offsets"])
+
+
 def test_pyramid_b48_one_multi_call():
     # the same eight pyramid levels as one tb_multi call (one launch, fused passes)
     import bench
