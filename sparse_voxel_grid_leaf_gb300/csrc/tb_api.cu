@@ -324,8 +324,16 @@ int member_ctas(int n_chain, int32_t B, long long count, long long nmax, long lo
   }
   if (mode == 2) return cl;
   if (B > kMemberMaxGrids || n_chain > 1 || heavy) return 0;
-  const long long n = nmax >= 0 ? nmax : 2 * ((count + B - 1) / B);  // unknown: twice the mean
-  return n * mmax <= (front ? kMemberVoxelsPerCta : kMemberSlotsPerCta) * cl ? cl : 0;
+  const long long mean = (count + B - 1) / B, per_cta = front ? kMemberVoxelsPerCta : kMemberSlotsPerCta;
+  // a member launch lasts as long as its largest grid: with grids of very
+  // unequal sizes (the largest above twice the mean) and a largest grid of
+  // more than a quarter of the budget per CTA, the whole-grid kernel wins
+  // (measured on GB300, 48 shells of 0.25x-4x the area: refinement 79 us
+  // against 117 us, the {-1,0}^3 pad 78 against 96 us; coarsening, one
+  // candidate per source, still 65 against 76 us as a member launch)
+  if (nmax > 2 * mean && nmax * mmax > per_cta / 4 * cl) return 0;
+  const long long n = nmax >= 0 ? nmax : 2 * mean;  // unknown: twice the mean
+  return n * mmax <= per_cta * cl ? cl : 0;
 }
 
 long long slots_per_source(const PassSpec& s) { return pass_targets(s.op, s.factor, s.lo, s.hi); }

@@ -296,6 +296,16 @@ def test_auto_launch_shape():
         assert "member" in names and "chain" not in names, names
         tb.set_launch_mode("grid")
         assert_same(small, tb.refine(b).to_numpy(), "auto vs grid")
+        # grids of very unequal sizes (0.25x-4x): the whole-grid kernel
+        tb.set_launch_mode("auto")
+        ijk, off = synth.make("pyramid_b48_res64")
+        b = tb.from_ijk(dev(ijk), dev(off))
+        tb.profile_read()
+        uneven = tb.refine(b).to_numpy()
+        names = tb.profile_read()
+        assert "chain" in names and "member" not in names, names
+        tb.set_launch_mode("member")
+        assert_same(uneven, tb.refine(b).to_numpy(), "auto vs member")
     finally:
         tb.profile_enable(0)
         tb.set_launch_mode(prev)
