@@ -304,6 +304,11 @@ std::atomic<int> g_launch_mode{0};
 // front end tried) and loses where one chain's leaves dominate: several
 // chains in one call, the fused refine-then-dilate merge, large grids.
 constexpr long long kMemberSlotsPerCta = 2048;        // candidate leaves of one grid per member CTA
+// Refinement alone: the whole-grid kernel's node path stores each target
+// leaf's one slot directly (no clearing, no merge), so it wins from fewer
+// candidates per member CTA (measured on GB300: 48 shells, about 400 per
+// CTA, 76 us against 84 us; 16 shells, about 200, 72 us against 63 us).
+constexpr long long kMemberRefineSlotsPerCta = 256;
 constexpr long long kMemberVoxelsPerCta = 16384;      // front ends: input voxels of one grid per member CTA
 constexpr int32_t kMemberMaxGrids = 4096;             // the last member scans its chain's grid counts alone
 
@@ -312,9 +317,10 @@ constexpr int32_t kMemberMaxGrids = 4096;             // the last member scans i
 // kernel.  `nmax` is
 // the most stage-0 sources of one grid (-1: not known on the host), `mmax`
 // the largest slot capacity per stage-0 source of any pass, `heavy` whether a
-// pass is the fused refine-then-dilate.
+// pass is the fused refine-then-dilate, `refine_only` whether every pass is
+// a refinement.
 int member_ctas(int n_chain, int32_t B, long long count, long long nmax, long long mmax, const int fit[4],
-                bool front, bool heavy) {
+                bool front, bool heavy, bool refine_only) {
   const int mode = g_launch_mode.load();
   if (mode == 1 || B < 1 || count <= 0) return 0;
   int cl = 8, lg = 3;
@@ -324,7 +330,8 @@ int member_ctas(int n_chain, int32_t B, long long count, long long nmax, long lo
   }
   if (mode == 2) return cl;
   if (B > kMemberMaxGrids || n_chain > 1 || heavy) return 0;
-  const long long mean = (count + B - 1) / B, per_cta = front ? kMemberVoxelsPerCta : kMemberSlotsPerCta;
+  const long long mean = (count + B - 1) / B;
+  const long long per_cta = front ? kMemberVoxelsPerCta : refine_only ? kMemberRefineSlotsPerCta : kMemberSlotsPerCta;
   // a member launch lasts as long as its largest grid: with grids of very
   // unequal sizes (the largest above twice the mean) and a largest grid of
   // more than a quarter of the budget per CTA, the whole-grid kernel wins
@@ -569,13 +576,14 @@ tb_status run(const Source& src, const std::vector<std::vector<PassSpec>>& chain
       nmax = 0;
       for (int32_t g = 0; g < B; ++g) nmax = std::max<long long>(nmax, hoff[g + 1] - hoff[g]);
     }
-    bool heavy = false;
+    bool heavy = false, refine_only = !front;
     for (const auto& pc : plans)
       for (const auto& pl : pc) {
         if (src.count > 0) mmax = std::max(mmax, pl.slot_cap / src.count);
         heavy |= pl.spec.op == kRefineDilate;
+        refine_only &= pl.spec.op == kRefine;
       }
-    cl = member_ctas(n_chain, B, src.count, nmax, mmax, di->member_fit, front, heavy);
+    cl = member_ctas(n_chain, B, src.count, nmax, mmax, di->member_fit, front, heavy, refine_only);
   }
   const int32_t B_key = cl ? 1 : B;  // a member's keys have no grid field
 
