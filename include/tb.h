@@ -194,6 +194,13 @@ TB_API tb_status tb_coarsen(const tb_batch* in, int32_t factor, const tb_allocat
 TB_API tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const int32_t hi[3],
                         const tb_allocator* alloc, tb_stream stream, tb_batch** out);
 
+/* The box of the stride-1 topology of a uniform kernel of size K (the rule
+ * above, written once): lo[a] = -floor((K-1)/2), hi[a] = ceil((K-1)/2) on
+ * every axis for conv_grid; with transpose != 0 the mirror image [-hi, -lo]
+ * for conv_transpose_grid.  Host only, no device work.  TB_ERR_INVALID_ARG
+ * for K outside 1..15 or NULL lo/hi (left unwritten). */
+TB_API tb_status tb_stride1_box(int32_t kernel_size, int32_t transpose, int32_t lo[3], int32_t hi[3]);
+
 /* Masked refinement (fVDB PR #757 test plan: masked refine; Summary item 1:
  * masked subdivision prunes upstream, then refines): the refinement by
  * `factor` (2, 4 or 8) of the voxels of `in` whose flag is non-zero.

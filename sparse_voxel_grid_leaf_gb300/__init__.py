@@ -92,6 +92,7 @@ def lib():
                 "tb_multi": [vp, vp, vp, i32, vp, vp, pp],
                 "tb_refine_masked": [vp, vp, i32, vp, vp, pp],
                 "tb_kernel_map": [vp, vp, vp, vp, i32, i32, vp, i64, vp],
+                "tb_stride1_box": [i32, i32, vp, vp],
                 "tb_selftest_wait": [i32, i32, vp],
                 "tb_batch_export_many": [vp, i32, vp, vp, vp, vp, vp],
                 "tb_validate": [vp, vp],
@@ -513,17 +514,15 @@ def kernel_map(b_in: Batch, b_out: Batch, lo=(-1, -1, -1), hi=(1, 1, 1), stride:
 
 
 def stride1_box(kernel_size: int, transpose: bool = False) -> Tuple[Tuple[int, int, int], Tuple[int, int, int]]:
-    """Box of the stride-1 topology of a uniform kernel of size K (2..15):
-    [-floor((K-1)/2), ceil((K-1)/2)] per axis for conv_grid (for even K the
-    extra offset is on the positive side, a reading the pages leave open), and
-    its mirror image for conv_transpose_grid."""
-    K = int(kernel_size)
-    if K < 1 or K > 15:
-        raise TBError(1, "kernel size %d is outside 1..15" % K)
-    lo, hi = -((K - 1) // 2), K // 2
-    if transpose:
-        lo, hi = -hi, -lo
-    return (lo, lo, lo), (hi, hi, hi)
+    """Box of the stride-1 topology of a uniform kernel of size K (1..15), from
+    the library (tb_stride1_box): [-floor((K-1)/2), ceil((K-1)/2)] per axis
+    for conv_grid (for even K the extra offset is on the positive side, a
+    reading the pages leave open), and its mirror image for
+    conv_transpose_grid."""
+    lo = (ctypes.c_int32 * 3)()
+    hi = (ctypes.c_int32 * 3)()
+    _check(lib().tb_stride1_box(int(kernel_size), 1 if transpose else 0, lo, hi))
+    return tuple(lo), tuple(hi)
 
 
 def conv_grid_stride1(b: Batch, kernel_size: int, stream=None) -> Batch:

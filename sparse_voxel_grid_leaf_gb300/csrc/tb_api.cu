@@ -1367,6 +1367,24 @@ tb_status tb_box_dilate(const tb_batch* in, const int32_t lo[3], const int32_t h
   return tb_chain(in, &op, 1, alloc, stream, out);
 }
 
+tb_status tb_stride1_box(int32_t kernel_size, int32_t transpose, int32_t lo[3], int32_t hi[3]) {
+  if (!lo || !hi) return fail(TB_ERR_INVALID_ARG, "tb_stride1_box: lo/hi NULL");
+  if (kernel_size < 1 || kernel_size > 15)
+    return fail(TB_ERR_INVALID_ARG, "tb_stride1_box: kernel size %d is outside 1..15", kernel_size);
+  // [-floor((K-1)/2), ceil((K-1)/2)]: for even K the extra offset on the positive side
+  int32_t l = -((kernel_size - 1) / 2), h = kernel_size / 2;
+  if (transpose) {
+    const int32_t t = l;
+    l = -h;
+    h = -t;
+  }
+  for (int a = 0; a < 3; ++a) {
+    lo[a] = l;
+    hi[a] = h;
+  }
+  return TB_OK;
+}
+
 tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask, int32_t factor, const tb_allocator* alloc,
                            tb_stream stream, tb_batch** out) {
   if (out) *out = nullptr;

@@ -96,6 +96,18 @@ def test_launch_mode_switch(lib):
         lib.tb_set_launch_mode(ctypes.c_int32(prev))
 
 
+def test_stride1_box_rule():
+    """The K -> box rule, written once in the library: odd K symmetric, even K
+    with the extra offset on the positive side, transpose mirrored."""
+    import sparse_voxel_grid_leaf_gb300 as tb
+    for K, lo, hi in ((1, 0, 0), (2, 0, 1), (3, -1, 1), (4, -1, 2), (5, -2, 2), (15, -7, 7)):
+        assert tb.stride1_box(K) == ((lo,) * 3, (hi,) * 3)
+        assert tb.stride1_box(K, True) == ((-hi,) * 3, (-lo,) * 3)
+    for K in (0, 16, -3):
+        with pytest.raises(tb.TBError):
+            tb.stride1_box(K)
+
+
 def test_kmap_mode_switch(lib):
     lib.tb_set_kmap_mode.restype = ctypes.c_int32
     prev = lib.tb_set_kmap_mode(ctypes.c_int32(4))
