@@ -1419,9 +1419,9 @@ tb_status tb_refine_masked(const tb_batch* in, const uint8_t* voxel_mask, int32_
     TB_CUDA(cudaMemcpyAsync(ws + o_flags, voxel_mask, (size_t)V, cudaMemcpyHostToDevice, s));
     flags = (const uint8_t*)(ws + o_flags);
   }
-  // pageable source: the copy is staged before the call returns
-  TB_CUDA(cudaMemcpyAsync(ws + o_base, in->voxel_base_host.data(), (size_t)(in->B + 1) * 8, cudaMemcpyHostToDevice,
-                          s));
+  // the voxel bases from the batch's device counts (no host copy, so the
+  // host runs ahead of the stream)
+  TB_CUDA(launch(kKPrune, s, [&] { return launch_voxel_bases(in->voxel_counts, in->B, (int64_t*)(ws + o_base), s); }));
   tb_batch pruned = *in;
   pruned.masks = in->L ? (uint64_t*)(ws + o_masks) : nullptr;
   if (in->L) {

@@ -104,6 +104,10 @@ struct CopyTasks {
 };
 cudaError_t launch_copies(const CopyTasks& c, cudaStream_t s);
 
+// Per-grid voxel bases [B+1] (exclusive prefix, then the total) of a
+// batch's device voxel counts [B], one block.
+cudaError_t launch_voxel_bases(const int64_t* counts, int32_t B, int64_t* vbase, cudaStream_t s);
+
 // Self-test of the bounded device waits (tb_selftest_wait).
 cudaError_t launch_wait_selftest(const uint32_t* flag, uint32_t limit, unsigned int* err, cudaStream_t s);
 cudaError_t launch_validate(const int32_t* origins, const uint64_t* masks, const int32_t* leaf_grid,

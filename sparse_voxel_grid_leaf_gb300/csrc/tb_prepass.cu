@@ -77,6 +77,35 @@ __global__ void __launch_bounds__(256) k_copies(const CopyTasks c) {
   for (unsigned long long i = done + tid; i < t.bytes; i += stride) d1[i] = s1[i];
 }
 
+// Per-grid voxel bases: vbase[0] = 0, vbase[g + 1] = vbase[g] + counts[g],
+// one block scanning 256 grids at a time.
+__global__ void __launch_bounds__(256) k_voxel_bases(const int64_t* counts, int32_t B, int64_t* vbase) {
+  __shared__ long long part[8];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  if (threadIdx.x == 0) vbase[0] = 0;
+  long long carry = 0;
+  for (int base = 0; base < B; base += 256) {
+    const int i = base + threadIdx.x;
+    long long v = i < B ? counts[i] : 0;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += y;
+    }
+    if (lane == 31) part[wib] = v;
+    __syncthreads();
+    long long before = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      before += w < wib ? part[w] : 0;
+      total += part[w];
+    }
+    if (i < B) vbase[i + 1] = carry + before + v;
+    carry += total;
+    __syncthreads();
+  }
+}
+
 // Self-test of the bounded waits: one thread waits for *flag to reach 1 with
 // the same bounded spin as the grid barrier, `limit` polls at most.
 __global__ void k_wait_selftest(const uint32_t* flag, uint32_t limit, unsigned int* err) {
@@ -148,6 +177,11 @@ cudaError_t launch_copies(const CopyTasks& c, cudaStream_t s) {
   unsigned long long bx = (most / 16 + 255) / 256;
   bx = bx < 1 ? 1 : (bx > 64 ? 64 : bx);
   k_copies<<<dim3((unsigned)bx, (unsigned)c.n), 256, 0, s>>>(c);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_voxel_bases(const int64_t* counts, int32_t B, int64_t* vbase, cudaStream_t s) {
+  k_voxel_bases<<<1, 256, 0, s>>>(counts, B, vbase);
   return cudaGetLastError();
 }
 
