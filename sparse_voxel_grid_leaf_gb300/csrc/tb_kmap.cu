@@ -265,8 +265,9 @@ __device__ __forceinline__ void reach(const KmapArgs& k, int ax, long long o, lo
 
 // Candidate input leaves of every output leaf, one thread per (leaf,
 // candidate) in the span^3 layout: the hash look-ups of all leaves run side
-// by side here, so the map kernel starts each batch of leaves from coalesced
-// loads.  Used where the candidates are many (span 3).
+// by side here, and the map kernel then reads each leaf's candidates with
+// coalesced loads.  An optional pass (the "staged after a look-up pass"
+// form): on GB300 the staged kernels' own look-ups measured faster.
 __global__ void __launch_bounds__(256) k_kmap_cands(const KmapArgs k) {
   const long long total = k.L_out * k.cand_max;
   const long long stride = (long long)gridDim.x * blockDim.x;
