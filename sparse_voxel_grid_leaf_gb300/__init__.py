@@ -591,8 +591,9 @@ class ExportPlan:
 def export_many(batches: Sequence[Batch], origins=None, masks=None, voxel_offset=None, leaf_offsets=None,
                 stream=None):
     """Enqueues the copies of several batches' leaf records (one list entry per
-    batch; a list, or an entry, may be None to skip) -- one copy kernel for
-    all destinations the device can write (device or pinned host memory)."""
+    batch; a list, or an entry, may be None to skip): arrays of 1 MiB or more
+    through the copy engines, the smaller ones whose destination the device
+    can write (device or pinned host memory) through one copy kernel."""
     n = len(batches)
     keep = []
 

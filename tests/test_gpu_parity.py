@@ -796,6 +796,51 @@ def test_export_many_large_arrays():
         assert np.array_equal(lo[i].numpy(), r["leaf_offsets"])
 
 
+def test_pipelined_steps_export_what_they_built():
+    """The bench's end-to-end pattern: each step's outputs exported to pinned
+    host memory on a copy stream while the next step runs, and freed on the
+    compute stream once their export is done.  Every step's host arrays
+    equal the oracle's for that step."""
+    import torch
+    ijk, off = synth.make("shells_b16_res64")
+    chains = [[("refine", 2)], [("coarsen", 2)], [DIL]]
+    want = [oracle.run_voxels(ijk, off, ops) for ops in chains]
+    plan = tb.MultiPlan(chains)
+    ijk_h, off_h = torch.from_numpy(ijk).pin_memory(), torch.from_numpy(off).pin_memory()
+    copy = torch.cuda.Stream()
+    stream = torch.cuda.current_stream()
+    steps, pending = 4, None
+    host = [[(torch.zeros((len(w["origins"]), 3), dtype=torch.int32).pin_memory(),
+              torch.zeros((len(w["origins"]), 8), dtype=torch.int64).pin_memory(),
+              torch.zeros((len(w["origins"]),), dtype=torch.int64).pin_memory(),
+              torch.zeros((len(off),), dtype=torch.int64).pin_memory()) for w in want] for _ in range(steps)]
+    for i in range(steps):
+        b0 = tb.from_ijk(ijk_h, off_h)
+        outs = plan(b0)
+        ready = torch.cuda.Event()
+        ready.record(stream)
+        copy.wait_event(ready)
+        tb.export_many(outs, *[[h[j] for h in host[i]] for j in range(4)], stream=copy)
+        done = torch.cuda.Event()
+        done.record(copy)
+        if pending is not None:
+            stream.wait_event(pending[1])
+            for b in pending[0]:
+                b.free()
+        pending = (outs + [b0], done)
+    stream.wait_event(pending[1])
+    for b in pending[0]:
+        b.free()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        for j, w in enumerate(want):
+            o, m, v, lo = host[i][j]
+            assert np.array_equal(o.numpy(), w["origins"]), (i, j)
+            assert np.array_equal(m.numpy().view(np.uint64), w["masks"]), (i, j)
+            assert np.array_equal(v.numpy(), w["voxel_offset"]), (i, j)
+            assert np.array_equal(lo.numpy(), w["leaf_offsets"]), (i, j)
+
+
 def test_pyramid_b48_one_multi_call():
     # the same eight pyramid levels as one tb_multi call (one launch, fused passes)
     import bench
