@@ -406,11 +406,11 @@ TB_API int32_t tb_set_node_mode(int32_t mode);
 /* Which kernel writes tb_kernel_map (library extension: the pages prescribe
  * none).  mode 0 (default): picked from the box and the output's size -- the
  * staged form (the candidate input leaves' mask words staged in shared
- * memory: batches of up to 16 output leaves per warp where an output leaf's
+ * memory: batches of 4 to 16 output leaves per warp where an output leaf's
  * reach spans at most 2 input leaves per axis and the box has at most 32
  * columns, else one leaf per warp) where the reach spans at most 3 input
- * leaves per axis and the output has many leaves (at least 32 per SM for a
- * span of 3, 128 per SM otherwise); the tabulated form (a table of the
+ * leaves per axis and the output has at least 32 leaves per SM; the
+ * tabulated form (a table of the
  * input voxel index of every voxel in an output leaf's reach, one leaf per
  * warp) for fewer leaves where the reach is small; else the per-entry form.
  * mode 1: staged; 2: staged after a candidate look-up pass of its own; 3:

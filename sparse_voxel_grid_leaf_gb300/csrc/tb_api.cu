@@ -1496,19 +1496,19 @@ tb_status tb_kernel_map(const tb_batch* in, const tb_batch* out, const int32_t l
     halo *= transposed ? floor_div(7 - lo[a], stride) + floor_div(hi[a], stride) + 1 : 8 + hi[a] - lo[a];
   const bool tabulable = span <= 3 && K <= kKmapTabColumns && (stride == 1 || transposed) && halo <= kKmapHaloMax;
   // measured on GB300 (L2 flushed, whole calls): the staged map wins once
-  // the output has enough leaves to fill the GPU -- one leaf per warp where
-  // the reach spans 3 leaves per axis (B = 48 shells k3s1, 8,164 leaves:
-  // 61 us against 74 us tabulated; stress batch, 83,722 leaves: 190 us
-  // against 379 us), chunks of 16 leaves per warp where it spans 1 (B = 48
-  // k2s2 transpose, 31,128 leaves: 68 us against 102 us; stress, 392,508
-  // leaves: 150 us against 760 us); below that the tabulated map wins
-  // (B = 16 shells: k3s1 32 us against 36 us, k2s2 transpose 45 us against
-  // 57 us).  The look-up pass of its own measured slower than the staged
-  // map's own look-ups everywhere; it stays as a form of its own.
+  // the output has at least about 32 leaves per SM -- one leaf per warp
+  // where the reach spans 3 leaves per axis (B = 48 shells k3s1, 8,164
+  // leaves: 61 us against 67 us tabulated; stress batch, 83,722 leaves: 202
+  // us against 381 us), chunks of 4 to 16 leaves per warp where it spans 1
+  // (B = 16 k2s2 transpose, 10,547 leaves: 39 us against 45 us; B = 48: 55
+  // against 100 us; stress: 145 against 747 us); below that the tabulated
+  // map wins (B = 16 k3s1, 2,905 leaves: 35 us against 37 us).  The look-up
+  // pass of its own measured slower than the staged map's own look-ups
+  // everywhere; it stays as a form of its own.
   enum { kPerEntry, kStaged, kStagedPrepass, kTabulated } form = kPerEntry;
   switch (g_kmap_mode.load()) {
     case 0: {
-      const bool many = out->L >= (span == 3 ? 32ll : 128ll) * di->sms;
+      const bool many = out->L >= 32ll * di->sms;
       form = tabulable && (!many || !staged) ? kTabulated : staged ? kStaged : kPerEntry;
       break;
     }

@@ -410,10 +410,11 @@ __global__ void __launch_bounds__(kLeafWarps * 32, 4) k_kmap_leafwarp(const Kmap
 
 // The staged map for reaches of up to 2 input leaves per axis (8 candidates)
 // and boxes of up to kKmapBatchColumns columns.  A warp takes a chunk of
-// consecutive output leaves (16 with one candidate each, else 8; small
-// enough that the chunks, handed out one at a time, end together) and cuts
-// it into batches of as many leaves as fit kStagedSlots candidate mask words
-// (8 per candidate).  For a batch it
+// consecutive output leaves (16 with one candidate each, else 8, halved
+// down to 4 where the output has too few leaves for two chunks per warp;
+// small enough that the chunks, handed out one at a time, end together)
+// and cuts it into batches of as many leaves as fit kStagedSlots candidate
+// mask words (8 per candidate).  For a batch it
 //   1. looks up the candidates, a lane per leaf and candidate,
 //   2. stages the candidates' mask words and the first input voxel index of
 //      each word in shared memory, a lane per word,
@@ -528,7 +529,10 @@ __global__ void __launch_bounds__(kStagedWarps * 32, 4) k_kmap_staged(const Kmap
   for (int pc = 0; pc < 8; ++pc) single &= C.pcnt[pc] <= 1;
   const int S = k.span, S2 = S * S, Cn = S2 * S, words = 8 * Cn;
   const int gmax = kStagedSlots / words;  // leaves per batch (>= 4: Cn <= 8)
-  const int cs = gmax >= 16 ? 16 : 8;     // leaves per chunk
+  // leaves per chunk: 16 (8 for a span of 2), halved down to 4 while there
+  // are fewer than two chunks per warp of the grid
+  int cs = gmax >= 16 ? 16 : 8;
+  while (cs > 4 && (k.L_out + cs - 1) / cs < 2ll * gridDim.x * kStagedWarps) cs >>= 1;
   const long long nchunks = (k.L_out + cs - 1) / cs;
   // this lane's place in step 1 (batch leaf, candidate and its offsets) and
   // in the flat entry rounds, divided out once
@@ -856,11 +860,11 @@ cudaError_t launch_kmap_staged(const KmapArgs& k, int sms, cudaStream_t s) {
     k_kmap_leafwarp<<<blocks, kLeafWarps * 32, 0, s>>>(k);
     return cudaGetLastError();
   }
-  // chunks of 16 output leaves per warp (8 with span 2), handed out by the
-  // counter; shared memory: the column tables, then per warp the staged
-  // words and a round's 32 voxel packs
-  const int cs = kStagedSlots / (8 * S * S * S) >= 16 ? 16 : 8;
-  const long long chunks = (k.L_out + cs - 1) / cs;
+  // chunks of 4 to 16 output leaves per warp (the kernel picks the size
+  // from the grid), handed out by the counter; the grid is sized for chunks
+  // of 4.  Shared memory: the column tables, then per warp the staged words
+  // and a round's 32 voxel packs
+  const long long chunks = (k.L_out + 3) / 4;
   const size_t smem = sizeof(StagedSmem) + (size_t)kStagedWarps * (sizeof(StagedWarp) + 128);
   const int blocks = (int)std::max(1ll, std::min((chunks + kStagedWarps - 1) / kStagedWarps, 4ll * sms));
   k_kmap_staged<<<blocks, kStagedWarps * 32, smem, s>>>(k);
